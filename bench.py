@@ -1,0 +1,369 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA chunk scan: forward + backward tokens/s on the KDA layer
+training shape of a 1.7B KDA:GQA hybrid (B=4, T=8192, H=HV=16, K=V=128, bf16,
+chunk 64), one GPU per rank, inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--path auto|simt|tcgen05]
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on a bounded sample of the same workload instead.  Under torchrun each
+rank runs its own replica of the workload (the scan is independent per head,
+so ranks share no data; only the timing is reduced with a max).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "chunk_kda fwd+bwd tokens/s (B=4,T=8192,H=16,K=V=128 bf16); % roofline"
+# Algorithmic bytes per head-token of the fused forward and backward (bf16 I/O,
+# K = V = 128, chunk 64): forward reads q, k, v, g (4 x 256 B) and beta (2 B)
+# and writes o (256 B); backward reads q, k, v, g, beta, do (1282 B), writes
+# dq, dk, dv, dg, dbeta (1026 B) and writes + reads the fp32 chunk-boundary
+# states (2 x 128*128*4 / 64 = 2048 B).
+FWD_BYTES_PER_HEAD_TOKEN = 1282
+BWD_BYTES_PER_HEAD_TOKEN = 4356
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _src_hash(name):
+    path = os.path.join(ROOT, "gated_delta_rule_41_gb300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:12] if os.path.exists(path) else ""
+
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
+# keyed by kernel name: (bytes per launch at the benchmark workload, the
+# source file, that file's hash when captured).  A kernel whose source has
+# changed since reports traffic null.
+NCU_TRAFFIC = {}
+
+
+def kernel_algo_bytes(name, w):
+    """Algorithmic bytes one launch of kernel `name` must move at workload w.
+
+    Inputs are counted once at their dtype, outputs once, fp32 workspace
+    intermediates once each way (per-kernel rooflines)."""
+    B, T, H, HV, K, V, C = w.B, w.T, w.H, w.HV, w.K, w.V, w.chunk
+    e = 2 if str(w.dtype).endswith("bfloat16") else 4
+    BH, NT = B * HV, T // C
+    tok_in = B * T * (2 * H * K * e + HV * (V * e + K * e + e))   # q, k, v, g, beta
+    o = BH * T * V * e
+    f32 = 4
+    WQK = 3 * BH * T * K * f32      # W, Qh, Kb
+    U = BH * T * V * f32
+    CC = BH * NT * C * C * f32      # one C x C matrix per chunk
+    gam = BH * NT * K * f32
+    hs = BH * NT * K * V * f32
+    if name == "simt_intra":
+        return tok_in + WQK + U + 2 * CC + gam
+    if name == "simt_state_fwd":
+        return WQK + U + CC + gam + max(o, hs + U)
+    if name == "simt_state_bwd":
+        return WQK + CC + gam + o + hs + U
+    if name == "simt_vgrad":
+        return 2 * hs + 2 * U + 2 * o + CC + WQK + 2 * CC + o
+    if name == "simt_kgrad":
+        return tok_in + WQK + 3 * CC + 2 * B * T * HV * K * f32 + BH * T * K * e
+    if name == "simt_group_sum":
+        return 2 * B * T * HV * K * f32 + 2 * B * T * H * K * e
+    if name == "tc_fwd":
+        return BH * T * FWD_BYTES_PER_HEAD_TOKEN * (K / 128)
+    return None
+
+
+def start_clock_sampler():
+    f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    try:
+        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                              "-lms", "200"], stdout=f, stderr=subprocess.DEVNULL)
+    except OSError:
+        p = None
+    return p, f.name
+
+
+def stop_clock_sampler(p, path, gpu_index):
+    if p is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    p.terminate()
+    try:
+        p.wait(timeout=5)
+    except subprocess.TimeoutExpired:
+        p.kill()
+    sms, smax, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in open(path):
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9 or not parts[0].isdigit() or int(parts[0]) != gpu_index:
+            continue
+        try:
+            sms.append(float(parts[1]))
+            smax = float(parts[2])
+        except ValueError:
+            continue
+        for n, val in zip(names, parts[5:9]):
+            if val.lower().startswith("active"):
+                reasons.add(n)
+    os.unlink(path)
+    return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": smax,
+            "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle on a bounded sample (reference arm and cpu_baseline)
+# --------------------------------------------------------------------------
+
+def oracle_sample(w, inp_cpu, nheads, tsample):
+    """Time the float64 oracle (forward + backward) on the first `tsample`
+    tokens of `nheads` heads of the workload; return the throughput scaled to
+    the metric's unit (whole-workload tokens/s: the oracle's cost is linear in
+    heads and in tokens), the seconds taken and the threads used."""
+    import oracle
+    from gated_delta_rule_41_gb300.inputs import to_f64
+    heads = [(i // w.HV, i % w.HV) for i in range(nheads)]
+    # gather the sampled heads into one [1, T, n, X] problem (H == HV here)
+    take = lambda x: to_f64(torch.stack([x[b, :tsample, hv] for b, hv in heads], dim=1)[None])
+    q, k, v, g, do = (take(inp_cpu[n]) for n in ("q", "k", "v", "g", "do"))
+    beta = to_f64(torch.stack([inp_cpu["beta"][b, :tsample, hv] for b, hv in heads],
+                              dim=1)[None])
+    t0 = time.perf_counter()
+    oracle.fwd_recurrent(q, k, v, g, beta)
+    oracle.bwd_recurrent(q, k, v, g, beta, do)
+    dt = time.perf_counter() - t0
+    frac = (nheads / (w.B * w.HV)) * (tsample / w.T)
+    return w.tokens * frac / dt, dt, oracle.num_threads()
+
+
+def reference_arm(args, w):
+    import torch as _t  # noqa: F401
+    from gated_delta_rule_41_gb300 import inputs as I
+    import oracle
+    oracle.build()
+    inp = I.make_chunk_inputs(w, device="cpu")
+    nheads = min(w.B * w.HV, max(1, oracle.num_threads()))
+    tsample = 1024
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, nheads, tsample)
+    vals = []
+    for _ in range(args.steps):
+        v, dt, cores = oracle_sample(w, inp, nheads, tsample)
+        vals.append(v)
+    value = statistics.median(vals)
+    sample = (f"per step: first {tsample} of T={w.T} tokens of {nheads} of {w.B * w.HV} "
+              f"heads, forward+backward, scaled to the whole workload")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": w.tokens / value * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, "oracle"),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, path):
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K, "V": w.V,
+            "chunk": w.chunk, "pass": "fwd+bwd", "path": path,
+            "l2": "inputs larger than L2 (q, k, v, g = 512 MiB bf16; no flush needed)",
+            "parallelism": "one independent replica per rank"}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    global torch
+    import torch
+    from gated_delta_rule_41_gb300 import inputs as I
+
+    w = I.TRAIN_BF16
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            reference_arm(args, w)
+        return
+
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from gated_delta_rule_41_gb300 import build as kbuild
+    kbuild.build()
+    import gated_delta_rule_41_gb300 as kda
+
+    inp = I.make_chunk_inputs(w, device=dev, seed=w.seed + rank)
+    q, k, v, g, beta, do = (inp[n] for n in ("q", "k", "v", "g", "beta", "do"))
+    dims_f = kda.kda.make_dims(q, v, w.chunk, None, args.path)
+    ws_f = torch.empty(max(1, kda.workspace_bytes(dims_f, False)), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(1, kda.workspace_bytes(dims_f, True)), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(v)
+    grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                 dg=torch.empty_like(g), dbeta=torch.empty_like(beta), dh0=None)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.chunk_kda_fwd(q, k, v, g, beta, chunk_size=w.chunk, impl=args.path, workspace=ws_f,
+                          out=o)
+        kda.chunk_kda_bwd(q, k, v, g, beta, do, chunk_size=w.chunk, impl=args.path,
+                          workspace=ws_b, grads=grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    kda.check()
+
+    # ---- timed region: device-resident inputs ----
+    sampler, spath = start_clock_sampler() if rank == 0 else (None, None)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    kda.timing_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    kernels = kda.timing_read()
+    kda.timing_enable(False)
+    clocks = stop_clock_sampler(sampler, spath, local) if rank == 0 else None
+    kda.check()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * w.tokens / (ms / 1e3)
+
+    # ---- end to end: pinned host buffers, copies inside the timed region ----
+    h_in = {n: inp[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "do")}
+    h_out = {n: torch.empty_like(x, device="cpu").pin_memory()
+             for n, x in (("o", o), ("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta))}
+    d_in = {n: torch.empty_like(inp[n]) for n in h_in}
+    h2d = sum(x.numel() * x.element_size() for x in h_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in h_out.values())
+
+    def e2e_step():
+        for n in h_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        kda.chunk_kda_fwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"],
+                          chunk_size=w.chunk, impl=args.path, workspace=ws_f, out=o)
+        kda.chunk_kda_bwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"], d_in["do"],
+                          chunk_size=w.chunk, impl=args.path, workspace=ws_b, grads=grads)
+        h_out["o"].copy_(o, non_blocking=True)
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            h_out[n].copy_(grads[n], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * w.tokens / (e2e_ms / 1e3)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel ----
+    hbm, tf, tf_sus, peak_src = _peaks()
+    total_k = sum(t for t, _ in kernels.values()) or 1.0
+    dom = max(kernels, key=lambda n: kernels[n][0])
+    dom_ms, dom_n = kernels[dom]
+    per_launch_ms = dom_ms / dom_n
+    algo = kernel_algo_bytes(dom, w)
+    achieved = algo / (per_launch_ms / 1e3) / 1e9 if algo else None
+    traffic = None
+    if dom in NCU_TRAFFIC:
+        tb, src, h = NCU_TRAFFIC[dom]
+        traffic = tb if _src_hash(src) == h else None
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": (achieved / hbm) if achieved else None,
+                "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs, copy bandwidth)",
+                "algo_bytes_per_launch": algo, "ms_per_launch": per_launch_ms}
+    step_bytes = w.B * w.T * w.HV * (FWD_BYTES_PER_HEAD_TOKEN + BWD_BYTES_PER_HEAD_TOKEN)
+    step_roof_ms = step_bytes / (hbm * 1e9) * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w, args.path),
+        "roofline": roofline,
+        "step_roofline": {"bytes": step_bytes, "roofline_ms": step_roof_ms,
+                          "frac": step_roof_ms / ms, "note": "whole fwd+bwd step at HBM peak"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": int(sum(n for _, n in kernels.values())),
+        "kernels": {n: {"launches": c, "ms_per_launch": t / c, "share": t / total_k}
+                    for n, (t, c) in sorted(kernels.items(), key=lambda x: -x[1][0])},
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        inp_cpu = {n: inp[n].cpu() for n in ("q", "k", "v", "g", "beta", "do")}
+        nheads = min(w.B * w.HV, max(1, oracle.num_threads()))
+        cv, cdt, cores = oracle_sample(w, inp_cpu, nheads, w.T)
+        line["cpu_baseline"] = {"value": cv, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{nheads} of {w.B * w.HV} heads, full T={w.T}, "
+                                          f"forward+backward, {cdt:.1f} s, scaled to the "
+                                          f"whole workload"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

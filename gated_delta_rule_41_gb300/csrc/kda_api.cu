@@ -1,0 +1,169 @@
+// C ABI of libkda: argument validation and kernel selection.  Every entry
+// point validates fully before the first launch, so a rejected call enqueues
+// nothing and writes nothing.
+#include <stdint.h>
+
+#include "kda_common.cuh"
+
+namespace {
+
+using namespace kda;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status check_common(const kda_dims* d, bool need_chunk) {
+    if (!d) return KDA_ERR_INVALID_ARG;
+    if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+    if (d->impl != KDA_IMPL_AUTO && d->impl != KDA_IMPL_SIMT && d->impl != KDA_IMPL_TCGEN05)
+        return KDA_ERR_INVALID_ARG;
+    if (d->B < 0 || d->H <= 0 || d->HV <= 0 || d->K <= 0 || d->V <= 0) return KDA_ERR_SHAPE;
+    if (need_chunk && d->T < 0) return KDA_ERR_SHAPE;
+    if (d->HV % d->H != 0) return KDA_ERR_SHAPE;
+    if (d->K > 128 || d->V > 128) return KDA_ERR_UNSUPPORTED;
+    if ((long long)d->B * d->HV > 65535) return KDA_ERR_UNSUPPORTED;
+    if (need_chunk) {
+        const int c = d->chunk_size;
+        if (c != 16 && c != 32 && c != 64) return KDA_ERR_UNSUPPORTED;
+        if (d->T % c != 0) return KDA_ERR_SHAPE;
+    }
+    return KDA_OK;
+}
+
+// The SIMT kernels tile K across 256 threads: K must divide 256.
+bool simt_supported(const kda_dims& d) { return 256 % d.K == 0; }
+
+// Resolves AUTO; returns KDA_IMPL_SIMT or KDA_IMPL_TCGEN05, or -1 if neither fits.
+int pick_impl(const kda_dims& d) {
+    if (d.impl == KDA_IMPL_TCGEN05) return tc_supported(d) ? KDA_IMPL_TCGEN05 : -1;
+    if (d.impl == KDA_IMPL_SIMT) return simt_supported(d) ? KDA_IMPL_SIMT : -1;
+    if (tc_supported(d)) return KDA_IMPL_TCGEN05;
+    return simt_supported(d) ? KDA_IMPL_SIMT : -1;
+}
+
+// `required` pointers may be null only when the tensors are empty (`empty`).
+kda_status check_ptrs(bool empty, std::initializer_list<const void*> required,
+                      std::initializer_list<const void*> optional) {
+    for (const void* p : required) {
+        if (!p && !empty) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    }
+    for (const void* p : optional)
+        if (p && !aligned16(p)) return KDA_ERR_ALIGNMENT;
+    return KDA_OK;
+}
+
+size_t ws_bytes(const kda_dims& d, int impl, int for_bwd) {
+    return impl == KDA_IMPL_TCGEN05 ? tc_workspace_bytes(d, for_bwd)
+                                    : simt_workspace_bytes(d, for_bwd);
+}
+
+kda_status check_ws(const kda_dims& d, int impl, int for_bwd, const void* ws, size_t bytes) {
+    const size_t need = ws_bytes(d, impl, for_bwd);
+    if (need == 0) return KDA_OK;
+    if (!ws || bytes < need) return KDA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return KDA_ERR_ALIGNMENT;
+    return KDA_OK;
+}
+
+// Empty sequence (T == 0): the final state is the initial one, and the
+// gradient of h0 is the upstream gradient of the final state.
+kda_status copy_or_zero(const kda_dims& d, float* dst, const float* src, cudaStream_t s) {
+    if (!dst) return KDA_OK;
+    const size_t bytes = (size_t)d.B * d.HV * d.K * d.V * sizeof(float);
+    const cudaError_t e = src ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s)
+                              : cudaMemsetAsync(dst, 0, bytes, s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_chunk_workspace_bytes(const kda_dims* d, int for_bwd) {
+    if (check_common(d, true) != KDA_OK) return 0;
+    const int impl = pick_impl(*d);
+    if (impl < 0) return 0;
+    return ws_bytes(*d, impl, for_bwd ? 1 : 0);
+}
+
+kda_status kda_chunk_fwd(const kda_dims* d, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* h0, void* o,
+                         int output_final_state, float* ht, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    kda_status st = check_common(d, true);
+    if (st != KDA_OK) return st;
+    const int impl = pick_impl(*d);
+    if (impl < 0) return KDA_ERR_UNSUPPORTED;
+    if (output_final_state && !ht && d->B > 0) return KDA_ERR_INVALID_ARG;
+    const bool empty = d->B == 0 || d->T == 0;
+    if ((st = check_ptrs(empty, {q, k, v, g, beta, o},
+                         {h0, output_final_state ? ht : nullptr})) != KDA_OK)
+        return st;
+    if ((st = check_ws(*d, impl, 0, workspace, workspace_bytes)) != KDA_OK) return st;
+    float* ht_out = output_final_state ? ht : nullptr;
+    auto s = static_cast<cudaStream_t>(stream);
+    if (d->B == 0) return KDA_OK;
+    if (d->T == 0) return copy_or_zero(*d, ht_out, h0, s);
+    if (impl == KDA_IMPL_TCGEN05) return tc_fwd(*d, q, k, v, g, beta, h0, o, ht_out, workspace, s);
+    return simt_fwd(*d, q, k, v, g, beta, h0, o, ht_out, workspace, s);
+}
+
+kda_status kda_chunk_bwd(const kda_dims* d, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* h0, const void* dout,
+                         const float* dht, void* dq, void* dk, void* dv, void* dg,
+                         void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    kda_status st = check_common(d, true);
+    if (st != KDA_OK) return st;
+    const int impl = pick_impl(*d);
+    if (impl < 0) return KDA_ERR_UNSUPPORTED;
+    const bool empty = d->B == 0 || d->T == 0;
+    if ((st = check_ptrs(empty, {q, k, v, g, beta, dout, dq, dk, dv, dg, dbeta},
+                         {h0, dht, dh0})) != KDA_OK)
+        return st;
+    if ((st = check_ws(*d, impl, 1, workspace, workspace_bytes)) != KDA_OK) return st;
+    auto s = static_cast<cudaStream_t>(stream);
+    if (d->B == 0) return KDA_OK;
+    if (d->T == 0) return copy_or_zero(*d, dh0, dht, s);
+    if (impl == KDA_IMPL_TCGEN05)
+        return tc_bwd(*d, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
+                      s);
+    return simt_bwd(*d, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
+                    s);
+}
+
+kda_status kda_recurrent_step(const kda_dims* d, const void* q, const void* k, const void* v,
+                              const void* g, const void* beta, float* state, void* o,
+                              void* stream) {
+    kda_status st = check_common(d, false);
+    if (st != KDA_OK) return st;
+    if ((st = check_ptrs(d->B == 0, {q, k, v, g, beta, state, o}, {})) != KDA_OK) return st;
+    if (d->B == 0) return KDA_OK;
+    return decode_launch(*d, q, k, v, g, beta, state, o, static_cast<cudaStream_t>(stream));
+}
+
+kda_status kda_check(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    kda_status st = tc_take_error(static_cast<cudaStream_t>(stream));
+    if (st != KDA_OK) return st;
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+const char* kda_status_str(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_SHAPE: return "invalid shape";
+        case KDA_ERR_UNSUPPORTED: return "unsupported sizes, dtype or implementation";
+        case KDA_ERR_ALIGNMENT: return "pointer not aligned";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDA_ERR_CUDA: return "CUDA error";
+        case KDA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int kda_version(void) { return 10000; }
+
+}  // extern "C"

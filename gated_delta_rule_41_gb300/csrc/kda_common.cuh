@@ -1,0 +1,65 @@
+// Shared device helpers and internal launcher declarations of libkda.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr float kGateFloor = -5.0f;  // g is clamped at -5 before exp
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Round a byte count up to a 256-byte multiple (workspace sub-allocation).
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline kda_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// ---- internal launchers (validated arguments only) ----
+kda_status decode_launch(const kda_dims& d, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, float* state, void* o,
+                         cudaStream_t s);
+
+size_t simt_workspace_bytes(const kda_dims& d, int for_bwd);
+kda_status simt_fwd(const kda_dims& d, const void* q, const void* k, const void* v,
+                    const void* g, const void* beta, const float* h0, void* o, float* ht,
+                    void* ws, cudaStream_t s);
+kda_status simt_bwd(const kda_dims& d, const void* q, const void* k, const void* v,
+                    const void* g, const void* beta, const float* h0, const void* dout,
+                    const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
+                    float* dh0, void* ws, cudaStream_t s);
+
+bool tc_supported(const kda_dims& d);
+size_t tc_workspace_bytes(const kda_dims& d, int for_bwd);
+kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v,
+                  const void* g, const void* beta, const float* h0, void* o, float* ht,
+                  void* ws, cudaStream_t s);
+kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v,
+                  const void* g, const void* beta, const float* h0, const void* dout,
+                  const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
+                  float* dh0, void* ws, cudaStream_t s);
+// Reads and clears the device error word of the tensor-core kernels.
+kda_status tc_take_error(cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,861 @@
+// Generic fp32 CUDA-core (SIMT) chunk scan: any K, V <= 128, chunk 16/32/64,
+// f32 or bf16 inputs, all arithmetic in fp32.
+//
+// Chunk form (K3 README, table 实现路线表, row L2: (1) cumsum of the clamped
+// gate inside each chunk, (2) the lower-triangular system, (3) the solve,
+// (4) the state passed between chunks).  Per head and chunk of C rows, with
+// qs = scale*q, G_r = sum_{s<=r} max(g_s,-5) and gl = G_{C-1}:
+//     A[i][j]   = beta_i sum_c k_ic k_jc exp(G_ic - G_jc)      j < i
+//     T         = (I + A)^{-1}
+//     W         = T diag(beta) (k o exp(G)),  U = T diag(beta) v
+//     Aqk[r][j] = sum_c qs_rc k_jc exp(G_rc - G_jc)            j <= r
+//     Qh = qs o exp(G),  Kb = k o exp(gl - G),  gam = exp(gl)
+//     delta = U - W S;  O = Qh S + Aqk delta;  S <- diag(gam) S + Kb^T delta
+// Backward of those steps, chunk by chunk in reverse, with dS the gradient of
+// the state at the END of the chunk and S0 the state at its start:
+//     ddelta = Aqk^T dO + Kb dS
+//     dS0    = diag(gam) dS + Qh^T dO - W^T ddelta
+//     dQh = dO S0^T, dW = -ddelta S0^T, dKb = delta dS^T, dgam = rowsum(dS o S0)
+//     dAqk = mask(dO delta^T), dU = ddelta
+//     dT = mask_strict(dU (beta v)^T + dW (beta k o exp(G))^T)
+//     dA = -mask_strict(T^T dT T^T);   d(beta v) = T^T dU;  d(beta khat) = T^T dW
+// then through the pairwise decays into dq, dk, dbeta, dG, and
+// dg_s = [g_s >= -5] * sum_{r>=s} dG_r.
+//
+// Kernels (one launch each, all stream ordered):
+//   intra   (chunk, head)    : G, A, T, Aqk, W, U, Qh, Kb, gam     -> workspace
+//   state_f (V tile, head)   : sequential over chunks; delta, o, h, ht
+//   state_b (V tile, head)   : reverse over chunks; dh (= dS), ddelta, dh0
+//   vgrad   (chunk, head)    : contractions over V (dQh, dW, dKb, dgam, dAqk,
+//                              dTv, dv, dbeta from v)
+//   kgrad   (chunk, head)    : chunk-local algebra over C and K -> dq, dk, dg, dbeta
+//   group   (token)          : GVA sum of dq, dk over value heads, cast
+#include <algorithm>
+
+#include "kda_common.cuh"
+#include "kda_timing.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVT = 32;  // value columns per CTA in the state passes
+
+struct Ws {
+    float *W, *U, *Qh, *Kb, *Aqk, *Tm, *gam, *dlt;   // forward quantities
+    float *hs, *dhs, *ddl;                           // bwd: states, state grads, ddelta
+    float *dQh, *dWm, *dKb, *dgam, *dAqk, *dTv, *dbv;  // bwd: V contractions
+    float *dqh, *dkh;                                // bwd: dq, dk per value head (fp32)
+};
+
+struct Dims {
+    int B, T, H, HV, K, V, C, NT, G;
+    float scale;
+};
+
+Dims make_dims(const kda_dims& d) {
+    Dims r;
+    r.B = d.B; r.T = d.T; r.H = d.H; r.HV = d.HV; r.K = d.K; r.V = d.V;
+    r.C = d.chunk_size; r.NT = d.T / d.chunk_size; r.G = d.HV / d.H; r.scale = d.scale;
+    return r;
+}
+
+// Workspace carve-up; returns the total size.  With base == nullptr only sizes.
+size_t carve(const Dims& d, int for_bwd, char* base, Ws* w) {
+    const size_t BH = (size_t)d.B * d.HV, T = d.T, K = d.K, V = d.V, C = d.C, NT = d.NT;
+    size_t off = 0;
+    auto take = [&](size_t nfloats) {
+        float* p = base ? reinterpret_cast<float*>(base + off) : nullptr;
+        off += align256(nfloats * sizeof(float));
+        return p;
+    };
+    Ws x{};
+    x.W = take(BH * T * K);
+    x.U = take(BH * T * V);
+    x.Qh = take(BH * T * K);
+    x.Kb = take(BH * T * K);
+    x.Aqk = take(BH * NT * C * C);
+    x.Tm = take(BH * NT * C * C);
+    x.gam = take(BH * NT * K);
+    x.dlt = take(BH * T * V);
+    if (for_bwd) {
+        x.hs = take(BH * NT * K * V);
+        x.dhs = take(BH * NT * K * V);
+        x.ddl = take(BH * T * V);
+        x.dQh = take(BH * T * K);
+        x.dWm = take(BH * T * K);
+        x.dKb = take(BH * T * K);
+        x.dgam = take(BH * NT * K);
+        x.dAqk = take(BH * NT * C * C);
+        x.dTv = take(BH * NT * C * C);
+        x.dbv = take(BH * T);
+        x.dqh = take((size_t)d.B * T * d.HV * K);
+        x.dkh = take((size_t)d.B * T * d.HV * K);
+    }
+    if (w) *w = x;
+    return off;
+}
+
+__device__ __forceinline__ size_t tok_idx(const Dims& d, int b, int t, int head, int nheads,
+                                          int width) {
+    return (((size_t)b * d.T + t) * nheads + head) * width;
+}
+
+// ---------------------------------------------------------------------------
+// intra: per (chunk, head)
+// smem: k[C][K+1], qs[C][K+1], G[C][K+1], A[C][C+1], Tm[C][C+1], beta[C]
+// ---------------------------------------------------------------------------
+size_t intra_smem(const Dims& d) {
+    return sizeof(float) * (3 * (size_t)d.C * (d.K + 1) + 2 * (size_t)d.C * (d.C + 1) + d.C);
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
+             const Tin* __restrict__ v, const Tin* __restrict__ g, const Tin* __restrict__ beta) {
+    const int n = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / d.HV, hv = bh % d.HV, h = hv / d.G;
+    const int C = d.C, K = d.K, V = d.V, KP = K + 1, CP = C + 1;
+    const int tid = threadIdx.x;
+    extern __shared__ float sm[];
+    float* kS = sm;
+    float* qS = kS + C * KP;
+    float* GS = qS + C * KP;
+    float* A = GS + C * KP;
+    float* Tm = A + C * CP;
+    float* bS = Tm + C * CP;
+    const int t0 = n * C;
+
+    for (int i = tid; i < C * K; i += kThreads) {
+        const int r = i / K, c = i % K;
+        const size_t iq = tok_idx(d, b, t0 + r, h, d.H, K) + c;
+        const size_t ig = tok_idx(d, b, t0 + r, hv, d.HV, K) + c;
+        kS[r * KP + c] = to_f(k[iq]);
+        qS[r * KP + c] = d.scale * to_f(q[iq]);
+        GS[r * KP + c] = fmaxf(to_f(g[ig]), kGateFloor);
+    }
+    for (int r = tid; r < C; r += kThreads) bS[r] = to_f(beta[((size_t)b * d.T + t0 + r) * d.HV + hv]);
+    __syncthreads();
+    for (int c = tid; c < K; c += kThreads) {  // (1) in-chunk cumsum
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) {
+            acc += GS[r * KP + c];
+            GS[r * KP + c] = acc;
+        }
+    }
+    __syncthreads();
+
+    // (2) A (strictly lower, beta-scaled) and Aqk (lower incl. diagonal)
+    float* Aqk_g = w.Aqk + ((size_t)bh * d.NT + n) * C * C;
+    for (int p = tid; p < C * C; p += kThreads) {
+        const int i = p % C, j = p / C;
+        float a = 0.f, aq = 0.f;
+        if (j <= i) {
+            for (int c = 0; c < K; ++c) {
+                const float e = expf(GS[i * KP + c] - GS[j * KP + c]);
+                const float kj = kS[j * KP + c] * e;
+                a += kS[i * KP + c] * kj;
+                aq += qS[i * KP + c] * kj;
+            }
+        }
+        A[i * CP + j] = j < i ? bS[i] * a : 0.f;
+        Aqk_g[i * C + j] = j <= i ? aq : 0.f;
+    }
+    __syncthreads();
+
+    // (3) T = (I + A)^{-1}; column j solved top to bottom
+    for (int j = tid; j < C; j += kThreads) {
+        for (int i = 0; i < j; ++i) Tm[i * CP + j] = 0.f;
+        Tm[j * CP + j] = 1.f;
+        for (int i = j + 1; i < C; ++i) {
+            float acc = 0.f;
+            for (int m = j; m < i; ++m) acc += A[i * CP + m] * Tm[m * CP + j];
+            Tm[i * CP + j] = -acc;
+        }
+    }
+    __syncthreads();
+
+    float* Tm_g = w.Tm + ((size_t)bh * d.NT + n) * C * C;
+    for (int p = tid; p < C * C; p += kThreads) Tm_g[p] = Tm[(p / C) * CP + p % C];
+    const size_t row0 = (size_t)bh * d.T + t0;
+    for (int i = tid; i < C * K; i += kThreads) {
+        const int r = i / K, c = i % K;
+        const float G = GS[r * KP + c], gl = GS[(C - 1) * KP + c];
+        w.Qh[(row0 + r) * K + c] = qS[r * KP + c] * expf(G);
+        w.Kb[(row0 + r) * K + c] = kS[r * KP + c] * expf(gl - G);
+        kS[r * KP + c] = bS[r] * kS[r * KP + c] * expf(G);  // beta k o exp(G), in place
+    }
+    for (int c = tid; c < K; c += kThreads)
+        w.gam[((size_t)bh * d.NT + n) * K + c] = expf(GS[(C - 1) * KP + c]);
+    __syncthreads();
+
+    // W = T (beta k o exp(G)),  U = T (beta v)
+    for (int i = tid; i < C * K; i += kThreads) {
+        const int r = i / K, c = i % K;
+        float acc = 0.f;
+        for (int m = 0; m <= r; ++m) acc += Tm[r * CP + m] * kS[m * KP + c];
+        w.W[(row0 + r) * K + c] = acc;
+    }
+    for (int i = tid; i < C * V; i += kThreads) {
+        const int r = i / V, j = i % V;
+        float acc = 0.f;
+        for (int m = 0; m <= r; ++m)
+            acc += Tm[r * CP + m] * bS[m] * to_f(v[tok_idx(d, b, t0 + m, hv, d.HV, V) + j]);
+        w.U[(row0 + r) * V + j] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// state_f: per (V tile of kVT columns, head); sequential over chunks.
+// mode bits: 1 = write o, 2 = store h (state at chunk start) and delta.
+// smem: W[C][K], Qh[C][K], Kb[C][K], Aqk[C][C], gam[K], S[K][VT], U/delta[C][VT]
+// ---------------------------------------------------------------------------
+size_t statef_smem(const Dims& d) {
+    return sizeof(float) * (3 * (size_t)d.C * d.K + (size_t)d.C * d.C + d.K +
+                            (size_t)d.K * kVT + 2 * (size_t)d.C * kVT);
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(kThreads)
+state_fwd_kernel(Dims d, Ws w, const float* __restrict__ h0, Tout* __restrict__ o,
+                 float* __restrict__ ht, int mode) {
+    const int vt = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / d.HV, hv = bh % d.HV;
+    const int C = d.C, K = d.K, V = d.V;
+    const int j0 = vt * kVT;
+    const int VT = min(kVT, V - j0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    extern __shared__ float sm[];
+    float* Ws_ = sm;
+    float* Qs = Ws_ + C * K;
+    float* Kbs = Qs + C * K;
+    float* As = Kbs + C * K;
+    float* gs = As + C * C;
+    float* S = gs + K;
+    float* Us = S + K * kVT;
+    float* Ds = Us + C * kVT;
+
+    for (int i = tid; i < K * kVT; i += kThreads) {
+        const int c = i / kVT, j = i % kVT;
+        S[i] = (h0 && j < VT) ? h0[((size_t)bh * K + c) * V + j0 + j] : 0.f;
+    }
+    for (int n = 0; n < d.NT; ++n) {
+        __syncthreads();
+        const size_t row0 = (size_t)bh * d.T + (size_t)n * C;
+        for (int i = tid; i < C * K; i += kThreads) {
+            Ws_[i] = w.W[row0 * K + i];
+            Qs[i] = w.Qh[row0 * K + i];
+            Kbs[i] = w.Kb[row0 * K + i];
+        }
+        for (int i = tid; i < C * C; i += kThreads) As[i] = w.Aqk[((size_t)bh * d.NT + n) * C * C + i];
+        for (int c = tid; c < K; c += kThreads) gs[c] = w.gam[((size_t)bh * d.NT + n) * K + c];
+        for (int i = tid; i < C * kVT; i += kThreads) {
+            const int r = i / kVT, j = i % kVT;
+            Us[i] = j < VT ? w.U[(row0 + r) * V + j0 + j] : 0.f;
+        }
+        if (mode & 2) {
+            float* hs = w.hs + ((size_t)bh * d.NT + n) * K * V;
+            for (int i = tid; i < K * kVT; i += kThreads) {
+                const int c = i / kVT, j = i % kVT;
+                if (j < VT) hs[(size_t)c * V + j0 + j] = S[i];
+            }
+        }
+        __syncthreads();
+        // delta = U - W S   (thread: column lane, rows warp + 8i)
+        for (int r = warp; r < C; r += kThreads / 32) {
+            float acc = 0.f;
+            for (int c = 0; c < K; ++c) acc += Ws_[r * K + c] * S[c * kVT + lane];
+            const float dl = Us[r * kVT + lane] - acc;
+            Ds[r * kVT + lane] = dl;
+            if ((mode & 2) && lane < VT) w.dlt[(row0 + r) * V + j0 + lane] = dl;
+        }
+        __syncthreads();
+        if (mode & 1) {  // O = Qh S + Aqk delta
+            for (int r = warp; r < C; r += kThreads / 32) {
+                float acc = 0.f;
+                for (int c = 0; c < K; ++c) acc += Qs[r * K + c] * S[c * kVT + lane];
+                for (int m = 0; m <= r; ++m) acc += As[r * C + m] * Ds[m * kVT + lane];
+                if (lane < VT) o[tok_idx(d, b, n * C + r, hv, d.HV, V) + j0 + lane] = from_f<Tout>(acc);
+            }
+        }
+        __syncthreads();
+        // S <- diag(gam) S + Kb^T delta
+        for (int c = warp; c < K; c += kThreads / 32) {
+            float acc = gs[c] * S[c * kVT + lane];
+            for (int m = 0; m < C; ++m) acc += Kbs[m * K + c] * Ds[m * kVT + lane];
+            S[c * kVT + lane] = acc;
+        }
+    }
+    __syncthreads();
+    if (ht) {
+        for (int i = tid; i < K * kVT; i += kThreads) {
+            const int c = i / kVT, j = i % kVT;
+            if (j < VT) ht[((size_t)bh * K + c) * V + j0 + j] = S[i];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// state_b: per (V tile, head); reverse over chunks.
+// smem: W[C][K], Qh[C][K], Kb[C][K], Aqk[C][C], gam[K], dS[K][VT], dO[C][VT], dd[C][VT]
+// ---------------------------------------------------------------------------
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+state_bwd_kernel(Dims d, Ws w, const Tin* __restrict__ dout, const float* __restrict__ dht,
+                 float* __restrict__ dh0) {
+    const int vt = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / d.HV, hv = bh % d.HV;
+    const int C = d.C, K = d.K, V = d.V;
+    const int j0 = vt * kVT;
+    const int VT = min(kVT, V - j0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    extern __shared__ float sm[];
+    float* Ws_ = sm;
+    float* Qs = Ws_ + C * K;
+    float* Kbs = Qs + C * K;
+    float* As = Kbs + C * K;
+    float* gs = As + C * C;
+    float* dS = gs + K;
+    float* dOs = dS + K * kVT;
+    float* dds = dOs + C * kVT;
+
+    for (int i = tid; i < K * kVT; i += kThreads) {
+        const int c = i / kVT, j = i % kVT;
+        dS[i] = (dht && j < VT) ? dht[((size_t)bh * K + c) * V + j0 + j] : 0.f;
+    }
+    for (int n = d.NT - 1; n >= 0; --n) {
+        __syncthreads();
+        const size_t row0 = (size_t)bh * d.T + (size_t)n * C;
+        for (int i = tid; i < C * K; i += kThreads) {
+            Ws_[i] = w.W[row0 * K + i];
+            Qs[i] = w.Qh[row0 * K + i];
+            Kbs[i] = w.Kb[row0 * K + i];
+        }
+        for (int i = tid; i < C * C; i += kThreads) As[i] = w.Aqk[((size_t)bh * d.NT + n) * C * C + i];
+        for (int c = tid; c < K; c += kThreads) gs[c] = w.gam[((size_t)bh * d.NT + n) * K + c];
+        for (int i = tid; i < C * kVT; i += kThreads) {
+            const int r = i / kVT, j = i % kVT;
+            dOs[i] = j < VT ? to_f(dout[tok_idx(d, b, n * C + r, hv, d.HV, V) + j0 + j]) : 0.f;
+        }
+        {
+            float* dh = w.dhs + ((size_t)bh * d.NT + n) * K * V;
+            for (int i = tid; i < K * kVT; i += kThreads) {
+                const int c = i / kVT, j = i % kVT;
+                if (j < VT) dh[(size_t)c * V + j0 + j] = dS[i];
+            }
+        }
+        __syncthreads();
+        // ddelta = Aqk^T dO + Kb dS
+        for (int r = warp; r < C; r += kThreads / 32) {
+            float acc = 0.f;
+            for (int t = r; t < C; ++t) acc += As[t * C + r] * dOs[t * kVT + lane];
+            for (int c = 0; c < K; ++c) acc += Kbs[r * K + c] * dS[c * kVT + lane];
+            dds[r * kVT + lane] = acc;
+            if (lane < VT) w.ddl[(row0 + r) * V + j0 + lane] = acc;
+        }
+        __syncthreads();
+        // dS0 = diag(gam) dS + Qh^T dO - W^T ddelta
+        for (int c = warp; c < K; c += kThreads / 32) {
+            float acc = gs[c] * dS[c * kVT + lane];
+            for (int r = 0; r < C; ++r)
+                acc += Qs[r * K + c] * dOs[r * kVT + lane] - Ws_[r * K + c] * dds[r * kVT + lane];
+            dS[c * kVT + lane] = acc;
+        }
+    }
+    __syncthreads();
+    if (dh0) {
+        for (int i = tid; i < K * kVT; i += kThreads) {
+            const int c = i / kVT, j = i % kVT;
+            if (j < VT) dh0[((size_t)bh * K + c) * V + j0 + j] = dS[i];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// vgrad: per (chunk, head); contractions over V, in slices of 32 columns.
+// smem: S0[K][33], dS[K][33], dl[C][33], dd[C][33], dO[C][33], v[C][33],
+//       Tm[C][C+1], beta[C], dbv[C]
+// ---------------------------------------------------------------------------
+constexpr int kVS = 32, kVSP = 33;
+constexpr int kMaxPer = 32;  // C*K/256 and C*C/256 upper bounds (C<=64, K<=128)
+
+size_t vgrad_smem(const Dims& d) {
+    return sizeof(float) * (2 * (size_t)d.K * kVSP + 4 * (size_t)d.C * kVSP +
+                            (size_t)d.C * (d.C + 1) + 2 * (size_t)d.C);
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ beta,
+             const Tin* __restrict__ dout, Tin* __restrict__ dv) {
+    const int n = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / d.HV, hv = bh % d.HV;
+    const int C = d.C, K = d.K, V = d.V, CP = C + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    extern __shared__ float sm[];
+    float* S0 = sm;
+    float* dSs = S0 + K * kVSP;
+    float* dls = dSs + K * kVSP;
+    float* dds = dls + C * kVSP;
+    float* dOs = dds + C * kVSP;
+    float* vs = dOs + C * kVSP;
+    float* Tm = vs + C * kVSP;
+    float* bS = Tm + C * CP;
+    float* dbv = bS + C;
+
+    const size_t row0 = (size_t)bh * d.T + (size_t)n * C;
+    const float* hs = w.hs + ((size_t)bh * d.NT + n) * K * V;
+    const float* dh = w.dhs + ((size_t)bh * d.NT + n) * K * V;
+    for (int p = tid; p < C * C; p += kThreads) Tm[(p / C) * CP + p % C] = w.Tm[((size_t)bh * d.NT + n) * C * C + p];
+    for (int r = tid; r < C; r += kThreads) {
+        bS[r] = to_f(beta[((size_t)b * d.T + n * C + r) * d.HV + hv]);
+        dbv[r] = 0.f;
+    }
+
+    // ownership: (r, c) outputs with c = tid % K, r = tid / K + i * (256 / K)
+    const int ck = tid % K, rstep = kThreads / K;
+    const int nrk = (C * K + kThreads - 1) / kThreads;
+    // (r, m) outputs with m = tid % C, r = tid / C + i * (256 / C)
+    const int mc = tid % C, rcstep = kThreads / C;
+    const int nrc = (C * C + kThreads - 1) / kThreads;
+    float aQ[kMaxPer], aW[kMaxPer], aKb[kMaxPer], aAq[kMaxPer], aTv[kMaxPer];
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) aQ[i] = aW[i] = aKb[i] = aAq[i] = aTv[i] = 0.f;
+    float agam = 0.f;
+
+    for (int j0 = 0; j0 < V; j0 += kVS) {
+        const int VS = min(kVS, V - j0);
+        __syncthreads();
+        for (int i = tid; i < K * kVS; i += kThreads) {
+            const int c = i / kVS, j = i % kVS;
+            const bool ok = j < VS;
+            S0[c * kVSP + j] = ok ? hs[(size_t)c * V + j0 + j] : 0.f;
+            dSs[c * kVSP + j] = ok ? dh[(size_t)c * V + j0 + j] : 0.f;
+        }
+        for (int i = tid; i < C * kVS; i += kThreads) {
+            const int r = i / kVS, j = i % kVS;
+            const bool ok = j < VS;
+            dls[r * kVSP + j] = ok ? w.dlt[(row0 + r) * V + j0 + j] : 0.f;
+            dds[r * kVSP + j] = ok ? w.ddl[(row0 + r) * V + j0 + j] : 0.f;
+            const size_t it = tok_idx(d, b, n * C + r, hv, d.HV, V) + j0 + j;
+            dOs[r * kVSP + j] = ok ? to_f(dout[it]) : 0.f;
+            vs[r * kVSP + j] = ok ? to_f(v[it]) : 0.f;
+        }
+        __syncthreads();
+        // C x K contractions
+        for (int j = 0; j < kVS; ++j) {
+            const float s0 = S0[ck * kVSP + j], ds = dSs[ck * kVSP + j];
+            if (tid < K) agam += ds * s0;
+#pragma unroll
+            for (int i = 0; i < kMaxPer; ++i) {
+                if (i < nrk) {
+                    const int r = tid / K + i * rstep;
+                    if (r < C) {
+                        aQ[i] += dOs[r * kVSP + j] * s0;
+                        aW[i] -= dds[r * kVSP + j] * s0;
+                        aKb[i] += dls[r * kVSP + j] * ds;
+                    }
+                }
+            }
+        }
+        // C x C contractions
+        for (int j = 0; j < kVS; ++j) {
+            const float dlm = dls[mc * kVSP + j], vm = vs[mc * kVSP + j];
+#pragma unroll
+            for (int i = 0; i < kMaxPer; ++i) {
+                if (i < nrc) {
+                    const int r = tid / C + i * rcstep;
+                    if (r < C) {
+                        aAq[i] += dOs[r * kVSP + j] * dlm;
+                        aTv[i] += dds[r * kVSP + j] * vm;
+                    }
+                }
+            }
+        }
+        // d(beta v) = T^T ddelta -> dv = beta * that; dbeta += sum_j that * v
+        for (int m = warp; m < C; m += kThreads / 32) {
+            float acc = 0.f;
+            for (int i = m; i < C; ++i) acc += Tm[i * CP + m] * dds[i * kVSP + lane];
+            if (lane < VS)
+                dv[tok_idx(d, b, n * C + m, hv, d.HV, V) + j0 + lane] = from_f<Tin>(bS[m] * acc);
+            float pb = lane < VS ? acc * vs[m * kVSP + lane] : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, off);
+            if (lane == 0) dbv[m] += pb;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+        if (i < nrk) {
+            const int r = tid / K + i * rstep;
+            if (r < C) {
+                w.dQh[(row0 + r) * K + ck] = aQ[i];
+                w.dWm[(row0 + r) * K + ck] = aW[i];
+                w.dKb[(row0 + r) * K + ck] = aKb[i];
+            }
+        }
+        if (i < nrc) {
+            const int r = tid / C + i * rcstep;
+            if (r < C) {
+                const size_t base = ((size_t)bh * d.NT + n) * C * C;
+                w.dAqk[base + r * C + mc] = mc <= r ? aAq[i] : 0.f;
+                w.dTv[base + r * C + mc] = mc < r ? aTv[i] : 0.f;
+            }
+        }
+    }
+    if (tid < K) w.dgam[((size_t)bh * d.NT + n) * K + tid] = agam;
+    for (int r = tid; r < C; r += kThreads) w.dbv[row0 + r] = dbv[r];
+}
+
+// ---------------------------------------------------------------------------
+// kgrad: per (chunk, head); chunk-local algebra over C and K.
+// smem: k[C][K+1], qs[C][K+1], G[C][K+1], X[C][K+1], Y[C][K+1],
+//       Tm[C][C+1], dAqk[C][C+1], D[C][C+1], beta[C], dbeta[C]
+// ---------------------------------------------------------------------------
+size_t kgrad_smem(const Dims& d) {
+    return sizeof(float) * (5 * (size_t)d.C * (d.K + 1) + 3 * (size_t)d.C * (d.C + 1) + 2 * d.C);
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
+             const Tin* __restrict__ g, const Tin* __restrict__ beta, Tin* __restrict__ dg,
+             Tin* __restrict__ dbeta) {
+    const int n = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / d.HV, hv = bh % d.HV, h = hv / d.G;
+    const int C = d.C, K = d.K, KP = K + 1, CP = C + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    extern __shared__ float sm[];
+    float* kS = sm;
+    float* qS = kS + C * KP;
+    float* GS = qS + C * KP;
+    float* X = GS + C * KP;   // dW, then d(beta khat)
+    float* Y = X + C * KP;    // beta khat, then dG
+    float* Tm = Y + C * KP;
+    float* dAq = Tm + C * CP;
+    float* D = dAq + C * CP;  // dT -> dT T^T -> dA
+    float* bS = D + C * CP;
+    float* dbS = bS + C;
+    const int t0 = n * C;
+    const size_t row0 = (size_t)bh * d.T + t0;
+    const size_t cc0 = ((size_t)bh * d.NT + n) * C * C;
+
+    for (int i = tid; i < C * K; i += kThreads) {
+        const int r = i / K, c = i % K;
+        const size_t iq = tok_idx(d, b, t0 + r, h, d.H, K) + c;
+        kS[r * KP + c] = to_f(k[iq]);
+        qS[r * KP + c] = d.scale * to_f(q[iq]);
+        GS[r * KP + c] = fmaxf(to_f(g[tok_idx(d, b, t0 + r, hv, d.HV, K) + c]), kGateFloor);
+        X[r * KP + c] = w.dWm[(row0 + r) * K + c];
+    }
+    for (int p = tid; p < C * C; p += kThreads) {
+        Tm[(p / C) * CP + p % C] = w.Tm[cc0 + p];
+        dAq[(p / C) * CP + p % C] = w.dAqk[cc0 + p];
+    }
+    for (int r = tid; r < C; r += kThreads) {
+        bS[r] = to_f(beta[((size_t)b * d.T + t0 + r) * d.HV + hv]);
+        dbS[r] = w.dbv[row0 + r];
+    }
+    __syncthreads();
+    for (int c = tid; c < K; c += kThreads) {
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) {
+            acc += GS[r * KP + c];
+            GS[r * KP + c] = acc;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < C * K; i += kThreads) {
+        const int r = i / K, c = i % K;
+        Y[r * KP + c] = bS[r] * kS[r * KP + c] * expf(GS[r * KP + c]);
+    }
+    __syncthreads();
+    // dT[i][m] = beta_m dTv[i][m] + sum_c dW[i][c] (beta khat)[m][c], m < i
+    for (int p = tid; p < C * C; p += kThreads) {
+        const int m = p % C, i = p / C;
+        float acc = 0.f;
+        if (m < i) {
+            acc = bS[m] * w.dTv[cc0 + i * C + m];
+            for (int c = 0; c < K; ++c) acc += X[i * KP + c] * Y[m * KP + c];
+        }
+        D[i * CP + m] = acc;
+    }
+    __syncthreads();
+    // dbeta += sum_c d(beta khat)[m][c] khat[m][c], with d(beta khat) = T^T dW
+    // and in the same pass: X <- T^T dW
+    {
+        float reg[kMaxPer];
+        const int nr = (C * K + kThreads - 1) / kThreads;
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u) {
+            reg[u] = 0.f;
+            if (u < nr) {
+                const int i = tid + u * kThreads;
+                if (i < C * K) {
+                    const int m = i / K, c = i % K;
+                    float acc = 0.f;
+                    for (int r = m; r < C; ++r) acc += Tm[r * CP + m] * X[r * KP + c];
+                    reg[u] = acc;
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u) {
+            if (u < nr) {
+                const int i = tid + u * kThreads;
+                if (i < C * K) X[(i / K) * KP + i % K] = reg[u];
+            }
+        }
+        // Y2 = dT T^T  (into registers, then back into D)
+        const int nrc = (C * C + kThreads - 1) / kThreads;
+        float rc[kMaxPer];
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u) {
+            rc[u] = 0.f;
+            if (u < nrc) {
+                const int p = tid + u * kThreads;
+                if (p < C * C) {
+                    const int i = p / C, j = p % C;
+                    float acc = 0.f;
+                    for (int m = 0; m < C; ++m) acc += D[i * CP + m] * Tm[j * CP + m];
+                    rc[u] = acc;
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u) {
+            if (u < nrc) {
+                const int p = tid + u * kThreads;
+                if (p < C * C) D[(p / C) * CP + p % C] = rc[u];
+            }
+        }
+        __syncthreads();
+        // dA = -mask_strict(T^T Y2)
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u) {
+            rc[u] = 0.f;
+            if (u < nrc) {
+                const int p = tid + u * kThreads;
+                if (p < C * C) {
+                    const int i = p / C, j = p % C;
+                    float acc = 0.f;
+                    if (j < i)
+                        for (int m = 0; m < C; ++m) acc += Tm[m * CP + i] * D[m * CP + j];
+                    rc[u] = -acc;
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u) {
+            if (u < nrc) {
+                const int p = tid + u * kThreads;
+                if (p < C * C) D[(p / C) * CP + p % C] = rc[u];
+            }
+        }
+    }
+    __syncthreads();
+
+    // Per element (r, c): direct terms and the pairwise-decay terms.
+    // Y is reused for dG.
+    for (int i = tid; i < C * K; i += kThreads) {
+        const int r = i / K, c = i % K;
+        const float G = GS[r * KP + c], gl = GS[(C - 1) * KP + c];
+        const float kr = kS[r * KP + c], qr = qS[r * KP + c];
+        const float eG = expf(G), eL = expf(gl - G);
+        const float dKbeta = X[r * KP + c];  // d(beta khat)
+        const float dQh = w.dQh[(row0 + r) * K + c];
+        const float dKb = w.dKb[(row0 + r) * K + c];
+        float dk = bS[r] * dKbeta * eG + dKb * eL;
+        float dqs = dQh * eG;
+        float dG = dKbeta * bS[r] * kr * eG + dQh * qr * eG - dKb * kr * eL;
+        // row side: j <= r
+        float sA = 0.f, sQ = 0.f;
+        for (int j = 0; j <= r; ++j) {
+            const float e = expf(G - GS[j * KP + c]);
+            const float kj = kS[j * KP + c] * e;
+            if (j < r) sA += D[r * CP + j] * kj;
+            sQ += dAq[r * CP + j] * kj;
+        }
+        dk += bS[r] * sA;
+        dqs += sQ;
+        dG += bS[r] * kr * sA + qr * sQ;
+        // column side: t >= r
+        float cA = 0.f, cQ = 0.f;
+        for (int t = r; t < C; ++t) {
+            const float e = expf(GS[t * KP + c] - G);
+            if (t > r) cA += D[t * CP + r] * bS[t] * kS[t * KP + c] * e;
+            cQ += dAq[t * CP + r] * qS[t * KP + c] * e;
+        }
+        dk += cA + cQ;
+        dG -= kr * (cA + cQ);
+        Y[r * KP + c] = dG;
+        w.dqh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = d.scale * dqs;
+        w.dkh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = dk;
+        // dbeta: khat . d(beta khat) and k . (sum_j dA k e) -- reduced below
+        X[r * KP + c] = dKbeta * kr * eG + kr * sA;
+    }
+    __syncthreads();
+    // last-row terms of dG: sum_r dKb_r Kb_r + dgam * gam
+    for (int c = tid; c < K; c += kThreads) {
+        const float gl = GS[(C - 1) * KP + c];
+        float acc = w.dgam[((size_t)bh * d.NT + n) * K + c] * expf(gl);
+        for (int r = 0; r < C; ++r)
+            acc += w.dKb[(row0 + r) * K + c] * kS[r * KP + c] * expf(gl - GS[r * KP + c]);
+        Y[(C - 1) * KP + c] += acc;
+    }
+    // dbeta per row
+    for (int r = warp; r < C; r += kThreads / 32) {
+        float acc = 0.f;
+        for (int c = lane; c < K; c += 32) acc += X[r * KP + c];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) dbeta[((size_t)b * d.T + t0 + r) * d.HV + hv] = from_f<Tin>(acc + dbS[r]);
+    }
+    __syncthreads();
+    // dg_s = [g_s >= -5] sum_{r >= s} dG_r
+    for (int c = tid; c < K; c += kThreads) {
+        float acc = 0.f;
+        for (int r = C - 1; r >= 0; --r) {
+            acc += Y[r * KP + c];
+            const size_t ig = tok_idx(d, b, t0 + r, hv, d.HV, K) + c;
+            dg[ig] = from_f<Tin>(to_f(g[ig]) >= kGateFloor ? acc : 0.f);
+        }
+    }
+}
+
+// dq[b,t,h,:] = sum over the G value heads of the group; cast to the dtype.
+template <typename Tin>
+__global__ void group_sum_kernel(Dims d, const float* __restrict__ dqh,
+                                 const float* __restrict__ dkh, Tin* __restrict__ dq,
+                                 Tin* __restrict__ dk) {
+    const size_t total = (size_t)d.B * d.T * d.H * d.K;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int c = i % d.K;
+        const size_t bth = i / d.K;  // (b*T + t)*H + h
+        const int h = bth % d.H;
+        const size_t bt = bth / d.H;
+        float sq = 0.f, sk = 0.f;
+        for (int u = 0; u < d.G; ++u) {
+            const size_t j = (bt * d.HV + (size_t)h * d.G + u) * d.K + c;
+            sq += dqh[j];
+            sk += dkh[j];
+        }
+        dq[i] = from_f<Tin>(sq);
+        dk[i] = from_f<Tin>(sk);
+    }
+}
+
+template <typename F>
+kda_status set_smem(F* kernel, size_t bytes) {
+    if (bytes > 227 * 1024) return KDA_ERR_UNSUPPORTED;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)bytes) == cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
+}
+
+template <typename Tin>
+kda_status run_forward_parts(const Dims& d, const Ws& w, const void* q, const void* k,
+                             const void* v, const void* g, const void* beta, const float* h0,
+                             void* o, float* ht, int mode, cudaStream_t s) {
+    kda_status st;
+    const size_t si = intra_smem(d), sf = statef_smem(d);
+    if ((st = set_smem(intra_kernel<Tin>, si)) != KDA_OK) return st;
+    if ((st = set_smem(state_fwd_kernel<Tin>, sf)) != KDA_OK) return st;
+    {
+        TimedLaunch tl("simt_intra", s);
+        intra_kernel<Tin><<<dim3(d.NT, d.B * d.HV), kThreads, si, s>>>(
+            d, w, static_cast<const Tin*>(q), static_cast<const Tin*>(k),
+            static_cast<const Tin*>(v), static_cast<const Tin*>(g), static_cast<const Tin*>(beta));
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    {
+        TimedLaunch tl("simt_state_fwd", s);
+        state_fwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, d.B * d.HV), kThreads, sf, s>>>(
+            d, w, h0, static_cast<Tin*>(o), ht, mode);
+    }
+    return launch_status();
+}
+
+}  // namespace
+
+size_t simt_workspace_bytes(const kda_dims& kd, int for_bwd) {
+    return carve(make_dims(kd), for_bwd, nullptr, nullptr);
+}
+
+kda_status simt_fwd(const kda_dims& kd, const void* q, const void* k, const void* v,
+                    const void* g, const void* beta, const float* h0, void* o, float* ht,
+                    void* ws, cudaStream_t s) {
+    const Dims d = make_dims(kd);
+    Ws w;
+    carve(d, 0, static_cast<char*>(ws), &w);
+    if (kd.dtype == KDA_BF16)
+        return run_forward_parts<__nv_bfloat16>(d, w, q, k, v, g, beta, h0, o, ht, 1, s);
+    return run_forward_parts<float>(d, w, q, k, v, g, beta, h0, o, ht, 1, s);
+}
+
+namespace {
+template <typename Tin>
+kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, const float* h0, const void* dout,
+                      const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
+                      float* dh0, cudaStream_t s) {
+    kda_status st = run_forward_parts<Tin>(d, w, q, k, v, g, beta, h0, nullptr, nullptr, 2, s);
+    if (st != KDA_OK) return st;
+    const size_t sb = statef_smem(d), sv = vgrad_smem(d), sk = kgrad_smem(d);
+    if ((st = set_smem(state_bwd_kernel<Tin>, sb)) != KDA_OK) return st;
+    if ((st = set_smem(vgrad_kernel<Tin>, sv)) != KDA_OK) return st;
+    if ((st = set_smem(kgrad_kernel<Tin>, sk)) != KDA_OK) return st;
+    const int BH = d.B * d.HV;
+    {
+        TimedLaunch tl("simt_state_bwd", s);
+        state_bwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, BH), kThreads, sb, s>>>(
+            d, w, static_cast<const Tin*>(dout), dht, dh0);
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    {
+        TimedLaunch tl("simt_vgrad", s);
+        vgrad_kernel<Tin><<<dim3(d.NT, BH), kThreads, sv, s>>>(
+            d, w, static_cast<const Tin*>(v), static_cast<const Tin*>(beta),
+            static_cast<const Tin*>(dout), static_cast<Tin*>(dv));
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    {
+        TimedLaunch tl("simt_kgrad", s);
+        kgrad_kernel<Tin><<<dim3(d.NT, BH), kThreads, sk, s>>>(
+            d, w, static_cast<const Tin*>(q), static_cast<const Tin*>(k),
+            static_cast<const Tin*>(g), static_cast<const Tin*>(beta), static_cast<Tin*>(dg),
+            static_cast<Tin*>(dbeta));
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    const size_t total = (size_t)d.B * d.T * d.H * d.K;
+    const int nblk = (int)std::min<size_t>((total + 255) / 256, 152 * 16);
+    {
+        TimedLaunch tl("simt_group_sum", s);
+        group_sum_kernel<Tin><<<nblk, 256, 0, s>>>(d, w.dqh, w.dkh, static_cast<Tin*>(dq),
+                                                   static_cast<Tin*>(dk));
+    }
+    return launch_status();
+}
+}  // namespace
+
+kda_status simt_bwd(const kda_dims& kd, const void* q, const void* k, const void* v,
+                    const void* g, const void* beta, const float* h0, const void* dout,
+                    const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
+                    float* dh0, void* ws, cudaStream_t s) {
+    const Dims d = make_dims(kd);
+    Ws w;
+    carve(d, 1, static_cast<char*>(ws), &w);
+    if (kd.dtype == KDA_BF16)
+        return simt_bwd_t<__nv_bfloat16>(d, w, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg,
+                                         dbeta, dh0, s);
+    return simt_bwd_t<float>(d, w, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0,
+                             s);
+}
+
+}  // namespace kda

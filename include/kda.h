@@ -1,0 +1,146 @@
+/*
+ * kda.h -- C ABI of libkda.so: Kimi Delta Attention (KDA) chunk scan and
+ * single-token decode step, hand-written CUDA for sm_103a (GB300).
+ *
+ * The operation (per batch b and value head hv, state S of K x V floats):
+ *
+ *     a_t = exp(max(g_t, -5))                 per key channel
+ *     e_t = v_t - (diag(a_t) S_{t-1})^T k_t   the key reads the decayed state
+ *     S_t = diag(a_t) S_{t-1} + beta_t k_t e_t^T
+ *     o_t = S_t^T (scale * q_t)               the query reads the updated state
+ *
+ * Defined by "KDA 训练 → 推理 手写实现" (K3 README), table 实现路线表, row L1
+ * (recurrence), row L2 (chunk form: in-chunk cumsum of g, lower-triangular
+ * system, triangular solve, state passing between chunks), row L6 (decode
+ * state [B,HV,K,V]); its table 关键约束 / 风险点 fixes GVA (value head hv
+ * reads key head hv / (HV/H), dq/dk summed back over the group), scale
+ * 1/sqrt(K) applied to q at entry, the clamp of g at -5 before exp, and
+ * chunk_size 64 with T % chunk_size == 0.  The "KDA CUDA Trainer" README
+ * (section on the mixing module) fixes the order: decay, delta write, read.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * Layout   All tensors are dense, row-major, contiguous:
+ *            q, k  [B,T,H,K]    v, o, do  [B,T,HV,V]    g  [B,T,HV,K]
+ *            beta  [B,T,HV]     states (h0, ht, dht, dh0, decode state) [B,HV,K,V]
+ *          Gradients have the shape of the input they belong to (dq, dk at
+ *          H heads; dv, dg, dbeta at HV heads).
+ * Dtypes   q, k, v, g, beta, o and all gradients of those are `dtype`
+ *          (KDA_F32 or KDA_BF16).  States are always float32.
+ * Memory   Every pointer is a DEVICE pointer.  The caller owns every buffer,
+ *          including the workspace.  The library never allocates, frees or
+ *          synchronises inside these calls; all work is enqueued on `stream`
+ *          (a cudaStream_t; NULL = legacy default stream).
+ * Gates    g is a log-decay: values <= 0 are the supported domain (values
+ *          below -5 are clamped to -5; positive values may overflow the
+ *          in-chunk decay factors and are not supported).
+ * Errors   Arguments are validated before any launch; on a validation error
+ *          nothing is enqueued and no output is written.  KDA_ERR_CUDA means
+ *          a launch failed (cudaGetLastError); KDA_ERR_TIMEOUT means a device
+ *          wait gave up (reported by kda_check).
+ * Threads  Calls are thread-safe; calls on different streams may overlap if
+ *          they use distinct outputs and workspaces.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null pointer where one is required, bad flag */
+    KDA_ERR_SHAPE = 2,        /* non-positive size, HV % H != 0, T % chunk != 0 */
+    KDA_ERR_UNSUPPORTED = 3,  /* K or V > 128, chunk not in {16,32,64}, impl not
+                                 available for these sizes or this dtype */
+    KDA_ERR_ALIGNMENT = 4,    /* a pointer is not 16-byte aligned */
+    KDA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
+    KDA_ERR_CUDA = 6,         /* a CUDA launch or runtime call failed */
+    KDA_ERR_TIMEOUT = 7       /* a bounded device wait expired */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Which kernel family runs the chunk scan.
+ *   KDA_IMPL_AUTO     tensor-core path when it supports the sizes, else SIMT.
+ *   KDA_IMPL_SIMT     fp32 CUDA-core kernels; any K, V <= 128, chunk 16/32/64,
+ *                     f32 or bf16 inputs.
+ *   KDA_IMPL_TCGEN05  tcgen05/TMEM tensor-core kernels; bf16, K = V in
+ *                     {64, 128}, chunk 64.  KDA_ERR_UNSUPPORTED otherwise. */
+typedef enum { KDA_IMPL_AUTO = 0, KDA_IMPL_SIMT = 1, KDA_IMPL_TCGEN05 = 2 } kda_impl;
+
+typedef struct {
+    int B, T, H, HV, K, V;
+    int chunk_size;   /* 16, 32 or 64; T % chunk_size == 0 (ignored by the decode step) */
+    float scale;      /* multiplies q; pass 1/sqrt(K) for the standard scale */
+    kda_dtype dtype;
+    kda_impl impl;
+} kda_dims;
+
+/* Bytes of device workspace that kda_chunk_fwd (for_bwd = 0) or
+ * kda_chunk_bwd (for_bwd = 1) needs for these dims; 0 on invalid dims.
+ * The workspace must be 256-byte aligned and need not be zeroed. */
+size_t kda_chunk_workspace_bytes(const kda_dims* dims, int for_bwd);
+
+/* Chunked forward scan (K3 row L2; row L1 semantics).
+ *   h0                 initial state [B,HV,K,V] f32, or NULL for zeros.
+ *   o                  output [B,T,HV,V] (dtype).
+ *   output_final_state nonzero: write the state after token T-1 to ht.
+ *   ht                 [B,HV,K,V] f32; required iff output_final_state. */
+kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* h0, void* o,
+                         int output_final_state, float* ht, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Backward of kda_chunk_fwd (K3 row L4 role: dq, dk, dv, dg, dbeta).
+ * Stateless: it recomputes the forward from the inputs.
+ *   dout   upstream gradient of o [B,T,HV,V] (dtype).
+ *   dht    upstream gradient of the final state [B,HV,K,V] f32, or NULL.
+ *   dq, dk [B,T,H,K]; dv [B,T,HV,V]; dg [B,T,HV,K]; dbeta [B,T,HV] (dtype).
+ *   dh0    gradient of h0 [B,HV,K,V] f32, or NULL to skip.
+ * dg is zero where g < -5 (the clamp); g == -5 passes the gradient. */
+kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* h0, const void* dout,
+                         const float* dht, void* dq, void* dk, void* dv, void* dg,
+                         void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* One decode token per head, state updated in place (K3 row L6).
+ * dims->T is ignored; q, k [B,H,K]; v, o [B,HV,V]; g [B,HV,K]; beta [B,HV]
+ * (dtype); state [B,HV,K,V] f32, read and overwritten. */
+kda_status kda_recurrent_step(const kda_dims* dims, const void* q, const void* k,
+                              const void* v, const void* g, const void* beta, float* state,
+                              void* o, void* stream);
+
+/* Synchronise `stream`, then report (and clear) any error a kernel recorded on
+ * the device since the last check: KDA_ERR_TIMEOUT for an expired bounded
+ * wait, KDA_ERR_CUDA for a runtime error. */
+kda_status kda_check(void* stream);
+
+/* Diagnostics: per-kernel device timing.  kda_timing_enable(1) clears the
+ * totals and, until kda_timing_enable(0), brackets every kernel the library
+ * launches with two CUDA events recorded on that launch's stream (the events
+ * are created on first use and reused).  kda_timing_count() returns the
+ * number of distinct kernel names seen; kda_timing_entry(i, ...) copies the
+ * i-th name (NUL-terminated, truncated to name_len), its summed device time
+ * in milliseconds and its launch count, and returns 0 (-1 if i is out of
+ * range).  Both readers wait for the recorded events.  Not for use inside
+ * CUDA graph capture. */
+void kda_timing_enable(int on);
+int kda_timing_count(void);
+int kda_timing_entry(int i, char* name, int name_len, double* total_ms, long* launches);
+
+/* Static description of a status code. */
+const char* kda_status_str(kda_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,64 @@
+"""Shared helpers for the parity tests: tolerances, comparison, and running
+the float64 oracle on the same (dtype-rounded) inputs, whole or per head."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from gated_delta_rule_41_gb300.inputs import to_f64
+
+# Tolerances: fp32 inputs 1e-4 absolute; bf16 inputs 1e-2 absolute plus 2e-2
+# relative, per element, against the float64 oracle fed the same values.
+TOL = {torch.float32: (1e-4, 0.0), torch.bfloat16: (1e-2, 2e-2)}
+
+
+def assert_close(name, got, ref, dtype):
+    """|got - ref| <= atol + rtol*|ref| elementwise; reports the worst case."""
+    atol, rtol = TOL[dtype]
+    g = got.detach().to("cpu", torch.float64).numpy() if isinstance(got, torch.Tensor) else got
+    ref = np.asarray(ref, dtype=np.float64)
+    assert g.shape == ref.shape, (name, g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    err = np.abs(g - ref)
+    bound = atol + rtol * np.abs(ref)
+    bad = err > bound
+    fro = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30)
+    if bad.any():
+        idx = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(
+            f"{name}: {bad.sum()} / {bad.size} elements out of tolerance "
+            f"(atol {atol}, rtol {rtol}); worst at {idx}: got {g[idx]:.6g} ref {ref[idx]:.6g}; "
+            f"max abs err {err.max():.3g}, rel fro err {fro:.3g}")
+    return float(err.max()), float(fro)
+
+
+def oracle_chunk(inp, want_bwd, heads=None):
+    """Run the oracle on the inputs dict (torch, any device).
+
+    heads=None: all heads.  Otherwise a list of (b, hv); results are returned
+    per head as dicts of arrays shaped like the one-head slices [1,T,1,X].
+    Only valid per head when H == HV (no GVA group sums needed).
+    """
+    q, k, v, g, beta = (to_f64(inp[n]) for n in ("q", "k", "v", "g", "beta"))
+    h0 = to_f64(inp.get("h0"))
+    do = to_f64(inp.get("do"))
+    dht = to_f64(inp.get("dht"))
+    if heads is None:
+        o, ht = oracle.fwd_recurrent(q, k, v, g, beta, h0=h0)
+        res = dict(o=o, ht=ht)
+        if want_bwd:
+            res.update(oracle.bwd_recurrent(q, k, v, g, beta, do, h0=h0, dht=dht))
+        return res
+    assert q.shape[2] == v.shape[2], "per-head oracle runs need H == HV"
+    out = []
+    for b, hv in heads:
+        sl = lambda x: None if x is None else x[b:b + 1, :, hv:hv + 1]
+        st = lambda x: None if x is None else x[b:b + 1, hv:hv + 1]
+        qs, ks, vs, gs, bs = sl(q), sl(k), sl(v), sl(g), beta[b:b + 1, :, hv:hv + 1]
+        o, ht = oracle.fwd_recurrent(qs, ks, vs, gs, bs, h0=st(h0))
+        r = dict(o=o, ht=ht)
+        if want_bwd:
+            r.update(oracle.bwd_recurrent(qs, ks, vs, gs, bs, sl(do), h0=st(h0), dht=st(dht)))
+        out.append(r)
+    return out

@@ -1,0 +1,185 @@
+"""Parity of the CUDA chunk scan (forward and backward) with the float64
+oracle, on the seeded workloads and on edge cases.  All calls go through the
+C ABI via the ctypes binding."""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_41_gb300 as kda
+from gated_delta_rule_41_gb300 import inputs as I
+from gated_delta_rule_41_gb300.inputs import to_f64
+import oracle
+from parity_util import assert_close, oracle_chunk
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = ["simt", "tcgen05"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gated_delta_rule_41_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def run_gpu(inp, w, impl, backward=True):
+    dev = "cuda"
+    t = {n: (x.to(dev) if x is not None else None) for n, x in inp.items()}
+    try:
+        o, ht = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                  initial_state=t["h0"], output_final_state=True,
+                                  chunk_size=w.chunk, impl=impl)
+    except kda.KdaError as e:
+        if e.status == 3 and impl != "simt":
+            pytest.skip(f"{impl} does not support this shape")
+        raise
+    res = dict(o=o, ht=ht)
+    if backward:
+        res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                     dht=t["dht"], initial_state=t["h0"], chunk_size=w.chunk,
+                                     impl=impl))
+    torch.cuda.synchronize()
+    kda.check()
+    return res
+
+
+GRADS = ["dq", "dk", "dv", "dg", "dbeta"]
+
+
+def compare_all(res, ref, w, backward=True, with_h0=False):
+    assert_close("o", res["o"], ref["o"], w.dtype)
+    assert_close("ht", res["ht"], ref["ht"], w.dtype)
+    if backward:
+        for n in GRADS:
+            assert_close(n, res[n], ref[n], w.dtype)
+        if with_h0:
+            assert_close("dh0", res["dh0"], ref["dh0"], w.dtype)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_tiny_gva_fp32(impl):
+    w = I.TINY_GVA_F32
+    inp = I.make_chunk_inputs(w)
+    res = run_gpu(inp, w, impl)
+    ref = oracle_chunk(inp, True)
+    compare_all(res, ref, w)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_fp32_gva_chunks_with_h0(impl, chunk):
+    w = I.Workload("fp32_gva", 2, 128, 2, 4, 32, 32, chunk, torch.float32, g_sigma=2.0,
+                   h0_std=0.3, dht=True, seed=21)
+    inp = I.make_chunk_inputs(w)
+    res = run_gpu(inp, w, impl)
+    compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_small_bf16_full(impl):
+    w = I.SMALL_BF16
+    inp = I.make_chunk_inputs(w)
+    res = run_gpu(inp, w, impl)
+    compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_fp32_k128_full_tile(impl):
+    w = I.Workload("fp32_k128", 1, 192, 2, 2, 128, 128, 64, torch.float32, g_sigma=2.0,
+                   h0_std=0.1, dht=True, seed=22)
+    inp = I.make_chunk_inputs(w)
+    res = run_gpu(inp, w, impl)
+    compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_bf16_gva_k128(impl):
+    w = I.Workload("bf16_gva_k128", 2, 256, 2, 4, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
+                   dht=True, seed=23)
+    inp = I.make_chunk_inputs(w)
+    res = run_gpu(inp, w, impl)
+    compare_all(res, oracle_chunk(inp, True), w)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_clamp_active_below_minus_five(impl):
+    """Gates far below -5 reach the kernel: it must clamp them and pass no
+    gradient through them (g == -5 exactly still passes)."""
+    w = I.Workload("clamp", 2, 128, 2, 2, 64, 64, 64, torch.bfloat16, g_mu=3.0, g_sigma=3.0,
+                   h0_std=0.2, dht=True, seed=24)
+    inp = I.make_chunk_inputs(w, g_floor=None)
+    g = inp["g"].float()
+    g[:, :8] = -5.0  # exact boundary values
+    inp["g"] = g.to(w.dtype)
+    assert (inp["g"].float() < -5).float().mean() > 0.2
+    res = run_gpu(inp, w, impl)
+    ref = oracle_chunk(inp, True)
+    compare_all(res, ref, w, with_h0=True)
+    assert torch.all(res["dg"].float().cpu()[inp["g"].float() < -5] == 0)
+
+
+def test_ragged_value_width_simt():
+    """V not a multiple of the 32-column tile, small K."""
+    w = I.Workload("ragged_v", 1, 64, 1, 2, 16, 40, 32, torch.float32, h0_std=0.5, dht=True,
+                   seed=25)
+    inp = I.make_chunk_inputs(w)
+    res = run_gpu(inp, w, "simt")
+    compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
+
+
+def test_empty_sequence_and_batch():
+    w = I.Workload("empty", 2, 0, 1, 1, 64, 64, 64, torch.bfloat16, h0_std=1.0, dht=True)
+    inp = I.make_chunk_inputs(w, device="cuda")
+    o, ht = kda.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                              initial_state=inp["h0"], output_final_state=True)
+    gr = kda.chunk_kda_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["do"],
+                           dht=inp["dht"], initial_state=inp["h0"])
+    torch.cuda.synchronize()
+    assert o.numel() == 0
+    assert torch.equal(ht, inp["h0"])
+    assert torch.equal(gr["dh0"], inp["dht"])
+    w0 = I.Workload("empty_b", 0, 64, 1, 1, 64, 64, 64, torch.bfloat16)
+    inp0 = I.make_chunk_inputs(w0, device="cuda")
+    o0, _ = kda.chunk_kda_fwd(inp0["q"], inp0["k"], inp0["v"], inp0["g"], inp0["beta"])
+    assert o0.numel() == 0
+
+
+# ---- full-size workloads: sampled heads against the oracle ----
+
+def _sampled(w, heads, impl, backward):
+    inp = I.make_chunk_inputs(w, device="cuda")
+    res = run_gpu(inp, w, impl, backward=backward)
+    refs = oracle_chunk(inp, backward, heads=heads)
+    for (b, hv), ref in zip(heads, refs):
+        sl = lambda x: x[b:b + 1, :, hv:hv + 1]
+        assert_close(f"o[{b},{hv}]", sl(res["o"]), ref["o"], w.dtype)
+        assert_close(f"ht[{b},{hv}]", res["ht"][b:b + 1, hv:hv + 1], ref["ht"], w.dtype)
+        if backward:
+            for n in GRADS:
+                assert_close(f"{n}[{b},{hv}]", sl(res[n]), ref[n], w.dtype)
+    return res
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_train_shape_full_size_sampled_heads(impl):
+    w = I.TRAIN_BF16
+    res = _sampled(w, [(0, 0), (1, 7), (3, 15)], impl, backward=True)
+    for n in ["o"] + GRADS:
+        assert torch.isfinite(res[n].float()).all(), n
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_long_context_full_size_sampled_heads(impl):
+    _sampled(I.LONG_BF16, [(0, 0), (0, 31)], impl, backward=False)
+
+
+def test_impls_agree_train_shape_subset():
+    """The SIMT and tensor-core paths agree with each other on a slice of the
+    training workload (T = 1024)."""
+    w = I.TRAIN_BF16
+    inp = I.make_chunk_inputs(w, device="cuda", T=1024)
+    a = run_gpu(inp, w, "simt")
+    b = run_gpu(inp, w, "tcgen05")
+    for n in ["o", "ht"] + GRADS:
+        assert_close(n, b[n], a[n].double().cpu().numpy(), w.dtype)
