@@ -9,7 +9,9 @@ namespace {
 
 using namespace kda;
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+unsigned elem_bytes(const kda_dims& d) { return d.dtype == KDA_BF16 ? 2u : 4u; }
 
 kda_status check_common(const kda_dims* d, bool need_chunk) {
     if (!d) return KDA_ERR_INVALID_ARG;
@@ -40,16 +42,23 @@ int pick_impl(const kda_dims& d) {
     return simt_supported(d) ? KDA_IMPL_SIMT : -1;
 }
 
-// `required` pointers may be null only when the tensors are empty (`empty`).
-kda_status check_ptrs(bool empty, std::initializer_list<const void*> required,
+// `required` pointers may be null only when the tensors are empty (`empty`);
+// every non-null pointer must be aligned to `align` bytes.
+kda_status check_ptrs(bool empty, unsigned align, std::initializer_list<const void*> required,
                       std::initializer_list<const void*> optional) {
     for (const void* p : required) {
         if (!p && !empty) return KDA_ERR_INVALID_ARG;
-        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+        if (!aligned(p, align)) return KDA_ERR_ALIGNMENT;
     }
     for (const void* p : optional)
-        if (p && !aligned16(p)) return KDA_ERR_ALIGNMENT;
+        if (p && !aligned(p, align)) return KDA_ERR_ALIGNMENT;
     return KDA_OK;
+}
+
+// Alignment the chunk kernels need: the tensor-core path moves tiles with TMA
+// and 128-bit accesses (16 bytes); the SIMT path reads elements.
+unsigned chunk_align(const kda_dims& d, int impl) {
+    return impl == KDA_IMPL_TCGEN05 ? 16u : elem_bytes(d);
 }
 
 size_t ws_bytes(const kda_dims& d, int impl, int for_bwd) {
@@ -96,8 +105,10 @@ kda_status kda_chunk_fwd(const kda_dims* d, const void* q, const void* k, const 
     if (impl < 0) return KDA_ERR_UNSUPPORTED;
     if (output_final_state && !ht && d->B > 0) return KDA_ERR_INVALID_ARG;
     const bool empty = d->B == 0 || d->T == 0;
-    if ((st = check_ptrs(empty, {q, k, v, g, beta, o},
+    if ((st = check_ptrs(empty, chunk_align(*d, impl), {q, k, v, g, o},
                          {h0, output_final_state ? ht : nullptr})) != KDA_OK)
+        return st;
+    if ((st = check_ptrs(empty, elem_bytes(*d), {beta}, {})) != KDA_OK)
         return st;
     if ((st = check_ws(*d, impl, 0, workspace, workspace_bytes)) != KDA_OK) return st;
     float* ht_out = output_final_state ? ht : nullptr;
@@ -118,8 +129,10 @@ kda_status kda_chunk_bwd(const kda_dims* d, const void* q, const void* k, const 
     const int impl = pick_impl(*d);
     if (impl < 0) return KDA_ERR_UNSUPPORTED;
     const bool empty = d->B == 0 || d->T == 0;
-    if ((st = check_ptrs(empty, {q, k, v, g, beta, dout, dq, dk, dv, dg, dbeta},
+    if ((st = check_ptrs(empty, chunk_align(*d, impl), {q, k, v, g, dout, dq, dk, dv, dg},
                          {h0, dht, dh0})) != KDA_OK)
+        return st;
+    if ((st = check_ptrs(empty, elem_bytes(*d), {beta, dbeta}, {})) != KDA_OK)
         return st;
     if ((st = check_ws(*d, impl, 1, workspace, workspace_bytes)) != KDA_OK) return st;
     auto s = static_cast<cudaStream_t>(stream);
@@ -137,7 +150,10 @@ kda_status kda_recurrent_step(const kda_dims* d, const void* q, const void* k, c
                               void* stream) {
     kda_status st = check_common(d, false);
     if (st != KDA_OK) return st;
-    if ((st = check_ptrs(d->B == 0, {q, k, v, g, beta, state, o}, {})) != KDA_OK) return st;
+    // the state is streamed with 128-bit accesses; the token vectors by element
+    if ((st = check_ptrs(d->B == 0, 16u, {state}, {})) != KDA_OK) return st;
+    if ((st = check_ptrs(d->B == 0, elem_bytes(*d), {q, k, v, g, beta, o}, {})) != KDA_OK)
+        return st;
     if (d->B == 0) return KDA_OK;
     return decode_launch(*d, q, k, v, g, beta, state, o, static_cast<cudaStream_t>(stream));
 }

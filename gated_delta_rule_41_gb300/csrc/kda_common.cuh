@@ -42,6 +42,13 @@ kda_status decode_launch(const kda_dims& d, const void* q, const void* k, const 
                          cudaStream_t s);
 
 size_t simt_workspace_bytes(const kda_dims& d, int for_bwd);
+// fp32 per-chunk quantities of the SIMT intra-chunk kernel (inside its workspace).
+struct SimtIntraOut {
+    float *W, *U, *Qh, *Kb, *Aqk, *gam;
+};
+kda_status simt_intra_only(const kda_dims& d, const void* q, const void* k, const void* v,
+                           const void* g, const void* beta, void* ws, SimtIntraOut* out,
+                           cudaStream_t s);
 kda_status simt_fwd(const kda_dims& d, const void* q, const void* k, const void* v,
                     const void* g, const void* beta, const float* h0, void* o, float* ht,
                     void* ws, cudaStream_t s);

@@ -760,20 +760,28 @@ kda_status set_smem(F* kernel, size_t bytes) {
 }
 
 template <typename Tin>
-kda_status run_forward_parts(const Dims& d, const Ws& w, const void* q, const void* k,
-                             const void* v, const void* g, const void* beta, const float* h0,
-                             void* o, float* ht, int mode, cudaStream_t s) {
+kda_status run_intra(const Dims& d, const Ws& w, const void* q, const void* k, const void* v,
+                     const void* g, const void* beta, cudaStream_t s) {
     kda_status st;
-    const size_t si = intra_smem(d), sf = statef_smem(d);
+    const size_t si = intra_smem(d);
     if ((st = set_smem(intra_kernel<Tin>, si)) != KDA_OK) return st;
-    if ((st = set_smem(state_fwd_kernel<Tin>, sf)) != KDA_OK) return st;
     {
         TimedLaunch tl("simt_intra", s);
         intra_kernel<Tin><<<dim3(d.NT, d.B * d.HV), kThreads, si, s>>>(
             d, w, static_cast<const Tin*>(q), static_cast<const Tin*>(k),
             static_cast<const Tin*>(v), static_cast<const Tin*>(g), static_cast<const Tin*>(beta));
     }
-    if ((st = launch_status()) != KDA_OK) return st;
+    return launch_status();
+}
+
+template <typename Tin>
+kda_status run_forward_parts(const Dims& d, const Ws& w, const void* q, const void* k,
+                             const void* v, const void* g, const void* beta, const float* h0,
+                             void* o, float* ht, int mode, cudaStream_t s) {
+    kda_status st = run_intra<Tin>(d, w, q, k, v, g, beta, s);
+    if (st != KDA_OK) return st;
+    const size_t sf = statef_smem(d);
+    if ((st = set_smem(state_fwd_kernel<Tin>, sf)) != KDA_OK) return st;
     {
         TimedLaunch tl("simt_state_fwd", s);
         state_fwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, d.B * d.HV), kThreads, sf, s>>>(
@@ -786,6 +794,22 @@ kda_status run_forward_parts(const Dims& d, const Ws& w, const void* q, const vo
 
 size_t simt_workspace_bytes(const kda_dims& kd, int for_bwd) {
     return carve(make_dims(kd), for_bwd, nullptr, nullptr);
+}
+
+kda_status simt_intra_only(const kda_dims& kd, const void* q, const void* k, const void* v,
+                           const void* g, const void* beta, void* ws, SimtIntraOut* out,
+                           cudaStream_t s) {
+    const Dims d = make_dims(kd);
+    Ws w;
+    carve(d, 0, static_cast<char*>(ws), &w);
+    out->W = w.W;
+    out->U = w.U;
+    out->Qh = w.Qh;
+    out->Kb = w.Kb;
+    out->Aqk = w.Aqk;
+    out->gam = w.gam;
+    if (kd.dtype == KDA_BF16) return run_intra<__nv_bfloat16>(d, w, q, k, v, g, beta, s);
+    return run_intra<float>(d, w, q, k, v, g, beta, s);
 }
 
 kda_status simt_fwd(const kda_dims& kd, const void* q, const void* k, const void* v,

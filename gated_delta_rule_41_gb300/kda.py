@@ -73,6 +73,8 @@ def load_library():
         lib.kda_timing_entry.argtypes = [I, ctypes.c_char_p, I, ctypes.POINTER(ctypes.c_double),
                                          ctypes.POINTER(ctypes.c_long)]
         lib.kda_timing_entry.restype = I
+        lib.kda_selftest_mma.argtypes = [P, P, P, I, I, P, P]
+        lib.kda_selftest_mma.restype = I
         _lib = lib
         return lib
 
@@ -205,3 +207,19 @@ def timing_read() -> dict:
         if lib.kda_timing_entry(i, name, 64, ctypes.byref(ms), ctypes.byref(n)) == 0:
             out[name.value.decode()] = (ms.value, n.value)
     return out
+
+
+def selftest_mma(A, B, use_tma=True, stream=None):
+    """D = A @ B^T through one tcgen05 MMA chain (A [128,64], B [N,64] bf16)."""
+    lib = load_library()
+    _check_dev(A, B)
+    N = B.shape[0]
+    D = torch.zeros(128, N, dtype=torch.float32, device=A.device)
+    status = torch.zeros(1, dtype=torch.int32, device=A.device)
+    st = lib.kda_selftest_mma(_ptr(A), _ptr(B), _ptr(D), N, int(use_tma), _ptr(status),
+                              _stream(stream))
+    _raise(st, "kda_selftest_mma")
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise KdaError(7, "kda_selftest_mma")
+    return D

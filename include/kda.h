@@ -31,6 +31,10 @@
  *          including the workspace.  The library never allocates, frees or
  *          synchronises inside these calls; all work is enqueued on `stream`
  *          (a cudaStream_t; NULL = legacy default stream).
+ * Alignment  Every pointer must be aligned to its element size.  In addition:
+ *          the decode state must be 16-byte aligned; with the tensor-core
+ *          implementation q, k, v, g, o, dout, dq, dk, dv, dg, h0, ht, dht
+ *          and dh0 must be 16-byte aligned; the workspace 256-byte aligned.
  * Gates    g is a log-decay: values <= 0 are the supported domain (values
  *          below -5 are clamped to -5; positive values may overflow the
  *          in-chunk decay factors and are not supported).
@@ -56,7 +60,7 @@ typedef enum {
     KDA_ERR_SHAPE = 2,        /* non-positive size, HV % H != 0, T % chunk != 0 */
     KDA_ERR_UNSUPPORTED = 3,  /* K or V > 128, chunk not in {16,32,64}, impl not
                                  available for these sizes or this dtype */
-    KDA_ERR_ALIGNMENT = 4,    /* a pointer is not 16-byte aligned */
+    KDA_ERR_ALIGNMENT = 4,    /* a pointer is misaligned (see Alignment above) */
     KDA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
     KDA_ERR_CUDA = 6,         /* a CUDA launch or runtime call failed */
     KDA_ERR_TIMEOUT = 7       /* a bounded device wait expired */
@@ -132,6 +136,15 @@ kda_status kda_check(void* stream);
 void kda_timing_enable(int on);
 int kda_timing_count(void);
 int kda_timing_entry(int i, char* name, int name_len, double* total_ms, long* launches);
+
+/* Diagnostics: self-test of the tensor-core building blocks.  Computes
+ * D[128 x N] = A[128 x 64] * B[N x 64]^T (A, B bf16 row-major, D fp32
+ * row-major; N = 64 or 128; all device pointers) with one tcgen05 MMA chain
+ * from 128B-swizzled shared-memory tiles staged by TMA (use_tma != 0) or by
+ * thread stores (use_tma == 0).  *status (device int, caller-zeroed) is set
+ * to 1 if a bounded device wait expired.  Enqueued on `stream`. */
+kda_status kda_selftest_mma(const void* A, const void* B, float* D, int N, int use_tma,
+                            int* status, void* stream);
 
 /* Static description of a status code. */
 const char* kda_status_str(kda_status status);

@@ -58,7 +58,7 @@ def test_workspace_sizes(lib):
 
 
 FAKE = ctypes.c_void_p(1 << 20)       # never dereferenced: validation fails first
-MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
+MISALIGNED = ctypes.c_void_p((1 << 20) + 1)
 
 
 def fwd(lib, d, ptrs=None, ws=None, nws=0, final=0, ht=None):

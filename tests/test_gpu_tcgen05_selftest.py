@@ -1,0 +1,26 @@
+"""The tensor-core building blocks (TMA into 128B-swizzled tiles, tcgen05.mma
+with shared-memory descriptors, TMEM accumulator read back by tcgen05.ld)
+against a plain fp32 product of the same bf16 operands."""
+import pytest
+import torch
+
+import gated_delta_rule_41_gb300 as kda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gated_delta_rule_41_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("use_tma", [True, False])
+def test_mma_chain_matches_fp32_product(N, use_tma):
+    g = torch.Generator(device="cpu").manual_seed(N + use_tma)
+    A = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, 64, generator=g).to(torch.bfloat16)
+    ref = A.double() @ B.double().T
+    D = kda.kda.selftest_mma(A.cuda(), B.cuda(), use_tma=use_tma)
+    torch.testing.assert_close(D.double().cpu(), ref, atol=1e-3, rtol=1e-4)
