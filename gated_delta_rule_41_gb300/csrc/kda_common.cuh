@@ -49,6 +49,18 @@ struct SimtIntraOut {
 kda_status simt_intra_only(const kda_dims& d, const void* q, const void* k, const void* v,
                            const void* g, const void* beta, void* ws, SimtIntraOut* out,
                            cudaStream_t s);
+// All fp32 arrays of the SIMT workspace (bwd carve; the forward arrays come
+// first, so their addresses are the same in the forward carve).
+struct SimtWsPtrs {
+    float *W, *U, *Qh, *Kb, *Aqk, *Tm, *gam, *dlt;
+    float *hs, *dhs, *ddl, *dQh, *dWm, *dKb, *dgam, *dAqk, *dTv, *dbv, *dqh, *dkh;
+};
+void simt_ws_ptrs(const kda_dims& d, int for_bwd, void* ws, SimtWsPtrs* out);
+// Chunk-local backward (kgrad) and the GVA group sum, from the V-contraction
+// results already in the workspace (dQh, dWm, dKb, dgam, dAqk, dTv, dbv, Tm).
+kda_status simt_bwd_tail(const kda_dims& d, void* ws, const void* q, const void* k,
+                         const void* g, const void* beta, void* dq, void* dk, void* dg,
+                         void* dbeta, cudaStream_t s);
 kda_status simt_fwd(const kda_dims& d, const void* q, const void* k, const void* v,
                     const void* g, const void* beta, const float* h0, void* o, float* ht,
                     void* ws, cudaStream_t s);

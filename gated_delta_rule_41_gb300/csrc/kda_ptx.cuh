@@ -52,6 +52,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
     asm volatile(
@@ -147,6 +155,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     d |= (uint64_t)2 << 61;                     // 128-byte swizzle
     return d;
 }
+
+// Shared-memory matrix descriptor, MN-major operand (M or N contiguous) with
+// the 128-byte swizzle: for each K index a 128-byte row of 64 consecutive
+// M/N elements, 8 K-rows per 1024-byte atom; `mn_block_stride` = bytes
+// between consecutive 64-element M/N blocks.  One MMA (K = 16) spans two
+// 8-row K groups, so K advances by 2048 bytes per instruction.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_block_stride) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((mn_block_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset
+    d |= (uint64_t)(1024 >> 4) << 32;                          // stride byte offset
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+constexpr uint32_t kAMajorMN = 1u << 15, kBMajorMN = 1u << 16;
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {

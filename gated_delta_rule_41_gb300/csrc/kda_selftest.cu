@@ -34,17 +34,36 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 128 threads.  smem: A tile 16 KB, B tile up to 16 KB, barriers.
+// MN-major operand descriptor with the 128-byte swizzle: for each K index a
+// 128-byte row of 64 consecutive M/N elements, 8 K-rows per 1024-byte atom.
+// `mn_stride` = bytes between consecutive 64-element M/N blocks, `k_stride`
+// = bytes between consecutive 8-row K groups.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// 128 threads.  smem (160 KB, so that any stride reading stays in bounds):
+// A tile at 0 (16 KB), B tile at 64 KB (up to 16 KB), barriers at 144 KB.
+// flags: bit0 TMA staging, bit1 A MN-major, bit2 B MN-major, bit3 swap the
+// two stride fields of the MN-major descriptors.
 __global__ void __launch_bounds__(128, 1)
 selftest_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
                 const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
-                float* __restrict__ D, int N, int use_tma, int* status) {
+                float* __restrict__ D, int N, int flags, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int use_tma = flags & 1, a_mn = (flags >> 1) & 1, b_mn = (flags >> 2) & 1,
+              swap = (flags >> 3) & 1;
     uint8_t* sA = smem;
-    uint8_t* sB = smem + 16384;
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + 32768);
+    uint8_t* sB = smem + 65536;
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + 147456);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* holder = reinterpret_cast<uint32_t*>(bar_tma + 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -66,8 +85,20 @@ selftest_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ 
     if (use_tma) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(bar_tma, (128 + N) * 128);
-            tma_load_2d(sA, &ma, bar_tma, 0, 0);
-            tma_load_2d(sB, &mb, bar_tma, 0, 0);
+            // K-major: one box of 64 (k) x rows.  MN-major: boxes of 64 (m/n) x 64 (k),
+            // consecutive 64-element M/N blocks 8 KB apart.
+            if (a_mn) {
+                tma_load_2d(sA, &ma, bar_tma, 0, 0);
+                tma_load_2d(sA + 8192, &ma, bar_tma, 64, 0);
+            } else {
+                tma_load_2d(sA, &ma, bar_tma, 0, 0);
+            }
+            if (b_mn) {
+                for (int nb = 0; nb < N / 64; ++nb)
+                    tma_load_2d(sB + nb * 8192, &mb, bar_tma, nb * 64, 0);
+            } else {
+                tma_load_2d(sB, &mb, bar_tma, 0, 0);
+            }
         }
     } else {
         for (int i = threadIdx.x; i < 128 * 8; i += 128) {
@@ -91,10 +122,16 @@ selftest_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ 
     }
     if (threadIdx.x == 0 && ok) {
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(128, N);
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem, sdesc_sw128(smem_u32(sA) + kk * 32), sdesc_sw128(smem_u32(sB) + kk * 32),
-                     idesc, kk > 0);
+        const uint32_t idesc =
+            idesc_bf16_f32(128, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
+        const uint32_t lbo = swap ? 1024u : 8192u, sbo = swap ? 8192u : 1024u;
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = a_mn ? sdesc_mn_sw128(smem_u32(sA) + kk * 2048, lbo, sbo)
+                                     : sdesc_sw128(smem_u32(sA) + kk * 32);
+            const uint64_t bd = b_mn ? sdesc_mn_sw128(smem_u32(sB) + kk * 2048, lbo, sbo)
+                                     : sdesc_sw128(smem_u32(sB) + kk * 32);
+            mma_bf16(tmem, ad, bd, idesc, kk > 0);
+        }
         mma_commit(bar_mma);
     }
     if (ok) {
@@ -123,19 +160,26 @@ selftest_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ 
 }  // namespace
 }  // namespace kda
 
-extern "C" kda_status kda_selftest_mma(const void* A, const void* B, float* D, int N, int use_tma,
+extern "C" kda_status kda_selftest_mma(const void* A, const void* B, float* D, int N, int flags,
                                        int* status, void* stream) {
     using namespace kda;
-    if (!A || !B || !D || !status || (N != 64 && N != 128)) return KDA_ERR_INVALID_ARG;
+    if (!A || !B || !D || !status || (N != 64 && N != 128) || flags < 0 || flags > 15)
+        return KDA_ERR_INVALID_ARG;
+    const bool a_mn = (flags >> 1) & 1, b_mn = (flags >> 2) & 1;
+    if ((a_mn || b_mn) && !(flags & 1)) return KDA_ERR_INVALID_ARG;  // MN-major needs TMA
     CUtensorMap ma, mb;
-    if (!make_map_bf16(&ma, A, 128, 64, 64, 128) || !make_map_bf16(&mb, B, N, 64, 64, N))
-        return KDA_ERR_CUDA;
-    const int smem = 32768 + 64 + 1024;
+    // A: [128 m][64 k] (K-major) or [64 k][128 m] (MN-major); B likewise with N.
+    const bool okA = a_mn ? make_map_bf16(&ma, A, 64, 128, 64, 64)
+                          : make_map_bf16(&ma, A, 128, 64, 64, 128);
+    const bool okB = b_mn ? make_map_bf16(&mb, B, 64, N, 64, 64)
+                          : make_map_bf16(&mb, B, N, 64, 64, N);
+    if (!okA || !okB) return KDA_ERR_CUDA;
+    const int smem = 147456 + 64 + 1024;
     if (cudaFuncSetAttribute(selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return KDA_ERR_CUDA;
     selftest_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
         ma, mb, static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), D, N,
-        use_tma, status);
+        flags, status);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -659,44 +659,117 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     }
     __syncthreads();
 
-    // Per element (r, c): direct terms and the pairwise-decay terms.
-    // Y is reused for dG.
+    // Per element (r, c): direct terms and the pairwise-decay terms
+    //   sA = sum_{j<r} dA[r][j] k_j e(r,j),   sQ = sum_{j<=r} dAqk[r][j] k_j e(r,j)
+    //   cA = sum_{t>r} dA[t][r] beta_t k_t e(t,r),  cQ = sum_{t>=r} dAqk[t][r] qs_t e(t,r)
+    // with e(t,j) = exp(G_t - G_j).  The decay is factored per 16-row block
+    // (reference b = first row of the block): e(t,j) = E_t F[R(t)][R(j)] / E_j
+    // with E_r = exp(G_r - G_b(r)) in [e^-75, 1] and F[R][J] = exp(G_bR - G_bJ),
+    // so the inner loops are plain FMAs over tables and no factor overflows.
+    // Tm's storage (no longer needed) holds F, exp(G_b) and exp(G_last - G_b).
+    const int NB = C / 16;
+    float* Fb = Tm;                   // Fb[(R*4 + J)*K + c]
+    float* eGbS = Tm + 16 * K;        // eGbS[R*K + c] = exp(G_bR)
+    float* eLbS = Tm + 20 * K;        // eLbS[R*K + c] = exp(G_last - G_bR)
+    for (int i = tid; i < 16 * K; i += kThreads) {
+        const int R = i / (4 * K), J = (i / K) % 4, c = i % K;
+        Fb[i] = (R < NB && J <= R) ? expf(GS[16 * R * KP + c] - GS[16 * J * KP + c]) : 0.f;
+    }
+    for (int i = tid; i < NB * K; i += kThreads) {
+        const int R = i / K, c = i % K;
+        eGbS[i] = expf(GS[16 * R * KP + c]);
+        eLbS[i] = expf(GS[(C - 1) * KP + c] - GS[16 * R * KP + c]);
+    }
+    // Y <- KE[j][c] = k_j / E_j   (row-side table)
     for (int i = tid; i < C * K; i += kThreads) {
         const int r = i / K, c = i % K;
-        const float G = GS[r * KP + c], gl = GS[(C - 1) * KP + c];
-        const float kr = kS[r * KP + c], qr = qS[r * KP + c];
-        const float eG = expf(G), eL = expf(gl - G);
-        const float dKbeta = X[r * KP + c];  // d(beta khat)
-        const float dQh = w.dQh[(row0 + r) * K + c];
-        const float dKb = w.dKb[(row0 + r) * K + c];
-        float dk = bS[r] * dKbeta * eG + dKb * eL;
-        float dqs = dQh * eG;
-        float dG = dKbeta * bS[r] * kr * eG + dQh * qr * eG - dKb * kr * eL;
-        // row side: j <= r
-        float sA = 0.f, sQ = 0.f;
-        for (int j = 0; j <= r; ++j) {
-            const float e = expf(G - GS[j * KP + c]);
-            const float kj = kS[j * KP + c] * e;
-            if (j < r) sA += D[r * CP + j] * kj;
-            sQ += dAq[r * CP + j] * kj;
+        Y[r * KP + c] = kS[r * KP + c] * expf(GS[(r & ~15) * KP + c] - GS[r * KP + c]);
+    }
+    __syncthreads();
+    const int nper = (C * K + kThreads - 1) / kThreads;
+    float sAr[kMaxPer], sQr[kMaxPer], dKr[kMaxPer];
+#pragma unroll
+    for (int u = 0; u < kMaxPer; ++u) {
+        sAr[u] = sQr[u] = dKr[u] = 0.f;
+        const int i = tid + u * kThreads;
+        if (u < nper && i < C * K) {
+            const int r = i / K, c = i % K, R = r >> 4;
+            float sA = 0.f, sQ = 0.f;
+            for (int J = 0; J <= R; ++J) {
+                float pa = 0.f, pq = 0.f;
+                const int jend = min(16 * J + 15, r);
+                for (int j = 16 * J; j <= jend; ++j) {
+                    const float ke = Y[j * KP + c];
+                    pa += D[r * CP + j] * ke;  // D[r][r] = 0 (strictly lower)
+                    pq += dAq[r * CP + j] * ke;
+                }
+                const float f = Fb[(R * 4 + J) * K + c];
+                sA += f * pa;
+                sQ += f * pq;
+            }
+            const float E = expf(GS[r * KP + c] - GS[(r & ~15) * KP + c]);
+            sAr[u] = sA * E;
+            sQr[u] = sQ * E;
+            dKr[u] = X[r * KP + c];  // d(beta khat)
         }
-        dk += bS[r] * sA;
-        dqs += sQ;
-        dG += bS[r] * kr * sA + qr * sQ;
-        // column side: t >= r
-        float cA = 0.f, cQ = 0.f;
-        for (int t = r; t < C; ++t) {
-            const float e = expf(GS[t * KP + c] - G);
-            if (t > r) cA += D[t * CP + r] * bS[t] * kS[t * KP + c] * e;
-            cQ += dAq[t * CP + r] * qS[t * KP + c] * e;
+    }
+    __syncthreads();
+    // X <- KLb[t][c] = beta_t k_t E_t,  Y <- QL[t][c] = qs_t E_t   (column-side tables)
+    for (int i = tid; i < C * K; i += kThreads) {
+        const int r = i / K, c = i % K;
+        const float E = expf(GS[r * KP + c] - GS[(r & ~15) * KP + c]);
+        X[r * KP + c] = bS[r] * kS[r * KP + c] * E;
+        Y[r * KP + c] = qS[r * KP + c] * E;
+    }
+    __syncthreads();
+    float dGr[kMaxPer], dbr[kMaxPer];
+#pragma unroll
+    for (int u = 0; u < kMaxPer; ++u) {
+        dGr[u] = dbr[u] = 0.f;
+        const int i = tid + u * kThreads;
+        if (u < nper && i < C * K) {
+            const int r = i / K, c = i % K, J = r >> 4;
+            float cA = 0.f, cQ = 0.f;
+            for (int R = J; R < NB; ++R) {
+                float pa = 0.f, pq = 0.f;
+                for (int t = max(16 * R, r); t < 16 * R + 16; ++t) {
+                    pa += D[t * CP + r] * X[t * KP + c];  // D[r][r] = 0
+                    pq += dAq[t * CP + r] * Y[t * KP + c];
+                }
+                const float f = Fb[(R * 4 + J) * K + c];
+                cA += f * pa;
+                cQ += f * pq;
+            }
+            const float G = GS[r * KP + c];
+            const float E = expf(G - GS[(r & ~15) * KP + c]);
+            const float Einv = 1.f / E;
+            cA *= Einv;
+            cQ *= Einv;
+            const float eG = eGbS[J * K + c] * E;      // exp(G_r)
+            const float eL = eLbS[J * K + c] * Einv;   // exp(G_last - G_r)
+            const float kr = kS[r * KP + c], qr = qS[r * KP + c];
+            const float dKbeta = dKr[u], sA = sAr[u], sQ = sQr[u];
+            const float dQh = w.dQh[(row0 + r) * K + c];
+            const float dKb = w.dKb[(row0 + r) * K + c];
+            const float br = bS[r];
+            const float dk = br * dKbeta * eG + dKb * eL + br * sA + cA + cQ;
+            const float dqs = dQh * eG + sQ;
+            dGr[u] = dKbeta * br * kr * eG + dQh * qr * eG - dKb * kr * eL + br * kr * sA +
+                     qr * sQ - kr * (cA + cQ);
+            dbr[u] = dKbeta * kr * eG + kr * sA;
+            w.dqh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = d.scale * dqs;
+            w.dkh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = dk;
         }
-        dk += cA + cQ;
-        dG -= kr * (cA + cQ);
-        Y[r * KP + c] = dG;
-        w.dqh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = d.scale * dqs;
-        w.dkh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = dk;
-        // dbeta: khat . d(beta khat) and k . (sum_j dA k e) -- reduced below
-        X[r * KP + c] = dKbeta * kr * eG + kr * sA;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kMaxPer; ++u) {
+        const int i = tid + u * kThreads;
+        if (u < nper && i < C * K) {
+            const int r = i / K, c = i % K;
+            Y[r * KP + c] = dGr[u];
+            X[r * KP + c] = dbr[u];
+        }
     }
     __syncthreads();
     // last-row terms of dG: sum_r dKb_r Kb_r + dgam * gam
@@ -825,30 +898,13 @@ kda_status simt_fwd(const kda_dims& kd, const void* q, const void* k, const void
 
 namespace {
 template <typename Tin>
-kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, const void* v,
-                      const void* g, const void* beta, const float* h0, const void* dout,
-                      const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
-                      float* dh0, cudaStream_t s) {
-    kda_status st = run_forward_parts<Tin>(d, w, q, k, v, g, beta, h0, nullptr, nullptr, 2, s);
-    if (st != KDA_OK) return st;
-    const size_t sb = statef_smem(d), sv = vgrad_smem(d), sk = kgrad_smem(d);
-    if ((st = set_smem(state_bwd_kernel<Tin>, sb)) != KDA_OK) return st;
-    if ((st = set_smem(vgrad_kernel<Tin>, sv)) != KDA_OK) return st;
+kda_status simt_tail_t(const Dims& d, const Ws& w, const void* q, const void* k, const void* g,
+                       const void* beta, void* dq, void* dk, void* dg, void* dbeta,
+                       cudaStream_t s) {
+    kda_status st;
+    const size_t sk = kgrad_smem(d);
     if ((st = set_smem(kgrad_kernel<Tin>, sk)) != KDA_OK) return st;
     const int BH = d.B * d.HV;
-    {
-        TimedLaunch tl("simt_state_bwd", s);
-        state_bwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, BH), kThreads, sb, s>>>(
-            d, w, static_cast<const Tin*>(dout), dht, dh0);
-    }
-    if ((st = launch_status()) != KDA_OK) return st;
-    {
-        TimedLaunch tl("simt_vgrad", s);
-        vgrad_kernel<Tin><<<dim3(d.NT, BH), kThreads, sv, s>>>(
-            d, w, static_cast<const Tin*>(v), static_cast<const Tin*>(beta),
-            static_cast<const Tin*>(dout), static_cast<Tin*>(dv));
-    }
-    if ((st = launch_status()) != KDA_OK) return st;
     {
         TimedLaunch tl("simt_kgrad", s);
         kgrad_kernel<Tin><<<dim3(d.NT, BH), kThreads, sk, s>>>(
@@ -866,7 +922,55 @@ kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, 
     }
     return launch_status();
 }
+
+template <typename Tin>
+kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, const float* h0, const void* dout,
+                      const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
+                      float* dh0, cudaStream_t s) {
+    kda_status st = run_forward_parts<Tin>(d, w, q, k, v, g, beta, h0, nullptr, nullptr, 2, s);
+    if (st != KDA_OK) return st;
+    const size_t sb = statef_smem(d), sv = vgrad_smem(d);
+    if ((st = set_smem(state_bwd_kernel<Tin>, sb)) != KDA_OK) return st;
+    if ((st = set_smem(vgrad_kernel<Tin>, sv)) != KDA_OK) return st;
+    const int BH = d.B * d.HV;
+    {
+        TimedLaunch tl("simt_state_bwd", s);
+        state_bwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, BH), kThreads, sb, s>>>(
+            d, w, static_cast<const Tin*>(dout), dht, dh0);
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    {
+        TimedLaunch tl("simt_vgrad", s);
+        vgrad_kernel<Tin><<<dim3(d.NT, BH), kThreads, sv, s>>>(
+            d, w, static_cast<const Tin*>(v), static_cast<const Tin*>(beta),
+            static_cast<const Tin*>(dout), static_cast<Tin*>(dv));
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    return simt_tail_t<Tin>(d, w, q, k, g, beta, dq, dk, dg, dbeta, s);
+}
 }  // namespace
+
+void simt_ws_ptrs(const kda_dims& kd, int for_bwd, void* ws, SimtWsPtrs* o) {
+    const Dims d = make_dims(kd);
+    Ws w;
+    carve(d, for_bwd, static_cast<char*>(ws), &w);
+    o->W = w.W; o->U = w.U; o->Qh = w.Qh; o->Kb = w.Kb; o->Aqk = w.Aqk; o->Tm = w.Tm;
+    o->gam = w.gam; o->dlt = w.dlt; o->hs = w.hs; o->dhs = w.dhs; o->ddl = w.ddl;
+    o->dQh = w.dQh; o->dWm = w.dWm; o->dKb = w.dKb; o->dgam = w.dgam; o->dAqk = w.dAqk;
+    o->dTv = w.dTv; o->dbv = w.dbv; o->dqh = w.dqh; o->dkh = w.dkh;
+}
+
+kda_status simt_bwd_tail(const kda_dims& kd, void* ws, const void* q, const void* k,
+                         const void* g, const void* beta, void* dq, void* dk, void* dg,
+                         void* dbeta, cudaStream_t s) {
+    const Dims d = make_dims(kd);
+    Ws w;
+    carve(d, 1, static_cast<char*>(ws), &w);
+    if (kd.dtype == KDA_BF16)
+        return simt_tail_t<__nv_bfloat16>(d, w, q, k, g, beta, dq, dk, dg, dbeta, s);
+    return simt_tail_t<float>(d, w, q, k, g, beta, dq, dk, dg, dbeta, s);
+}
 
 kda_status simt_bwd(const kda_dims& kd, const void* q, const void* k, const void* v,
                     const void* g, const void* beta, const float* h0, const void* dout,

@@ -77,7 +77,7 @@ struct ChainArgs {
     const float* h0;    // [BH][K][V] or null
     __nv_bfloat16* o;   // [B,T,HV,V]
     float* ht;          // [BH][K][V] or null
-    float* h_out;       // [BH][NT][K][V] or null (states at chunk starts)
+    __nv_bfloat16* h_out;  // [BH][NT][K][V] or null (states at chunk starts, bf16)
     __nv_bfloat16* delta_out;  // [BH*T][V] or null
 };
 
@@ -224,9 +224,9 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     tmem_ld32(tmem + lane_off + TM_S + cb * 32, r);
                 }
                 if (a.h_out) {
-                    float* hp = a.h_out + (((size_t)bh * NT + n) * kD + cb * 32) * kD + v;
+                    __nv_bfloat16* hp = a.h_out + (((size_t)bh * NT + n) * kD + cb * 32) * kD + v;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) hp[(size_t)i * kD] = r[i];
+                    for (int i = 0; i < 32; ++i) hp[(size_t)i * kD] = __float2bfloat16_rn(r[i]);
                 }
                 uint8_t* base = sS + (cb >> 1) * 16384;
 #pragma unroll
@@ -299,7 +299,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             // E3: output rows of chunk n
             const uint32_t tO = (n & 1) ? TM_O1 : TM_O0;
 #pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
+            for (int cb = 0; a.o && cb < 2; ++cb) {
                 tmem_ld32(tmem + lane_off + tO + cb * 32, r);
                 __nv_bfloat16* op =
                     a.o + (((size_t)b * a.T + (size_t)n * kC + cb * 32) * a.HV + hv) * kD + v;
@@ -317,15 +317,765 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     if (warp == 1) tmem_dealloc(tmem, TM_COLS);
 }
 
+// ===========================================================================
+// Reverse state pass (backward chain).  One CTA per (b, hv) walks the chunks
+// from last to first with dS (gradient of the state at the END of the
+// current chunk) on chip, fp32 in TMEM, transposed (lane = value column):
+//     ddelta^T = dS^T Kb^T + dO^T Aqk                 (M=128 v, N=64 rows)
+//     dS0^T    = diag(gam) dS^T + dO^T Qh - ddelta^T W   (M=128 v, N=128 k)
+// dO, Aqk, Qh and W are used straight from their TMA tiles as MN-major
+// operands; dS^T and -ddelta^T are written by the epilogue as K-major tiles.
+// Writes dS of every chunk (bf16 [K][V]) and ddelta (bf16 [C][V]) for the
+// gradient kernel, and dh0.
+// ===========================================================================
+constexpr uint32_t RB_DO = 0;        // dO [64 t][128 v]: two 64-column boxes, 8 KB apart
+constexpr uint32_t RB_Q = 16384;     // Qh [64 t][128 k]
+constexpr uint32_t RB_W = 32768;     // W  [64 r][128 k]
+constexpr uint32_t RB_KBT = 49152;   // Kb^T [128 k][64 r]
+constexpr uint32_t RB_AQK = 65536;   // Aqk [64 t][64 r]
+constexpr uint32_t RB_GAM = 73728;
+constexpr uint32_t TM2_S = 0, TM2_DD = 128, TM2_COLS = 256;
+
+struct ChainBwdArgs {
+    int B, T, HV, NT;
+    const float* gam;
+    const float* dht;            // [BH][K][V] or null
+    float* dh0;                  // [BH][K][V] or null
+    __nv_bfloat16* dh_out;       // [BH][NT][K][V]
+    __nv_bfloat16* dd_out;       // [BH*T][V]
+};
+
+__global__ void __launch_bounds__(192, 1)
+chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kbt,
+                 const __grid_constant__ CUtensorMap tm_aqk, ChainBwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* empty = full + 2;
+    uint64_t* bar_S = full + 4;
+    uint64_t* bar_delta = full + 5;
+    uint64_t* bar_dd = full + 6;
+    uint64_t* bar_D4 = full + 7;
+    uint64_t* bar_fin = full + 8;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 9);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int b = bh / a.HV, hv = bh % a.HV;
+    const int NT = a.NT;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(&empty[0], 129);
+        mbar_init(&empty[1], 129);
+        mbar_init(bar_S, 128);
+        mbar_init(bar_delta, 128);
+        mbar_init(bar_dd, 1);
+        mbar_init(bar_D4, 1);
+        mbar_init(bar_fin, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, TM2_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_do);
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_w);
+            prefetch_tmap(&tm_kbt);
+            prefetch_tmap(&tm_aqk);
+            int issued = 0;
+            for (int i = 0; i < NT; ++i) {
+                const int n = NT - 1 - i, s = i & 1;
+                if (!wait_bar(&empty[s], ((i >> 1) & 1) ^ 1, 11)) break;
+                uint8_t* st = smem + s * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], STAGE_TX);
+                const int row = bh * a.T + n * kC;
+                const int crow = bh * NT + n;
+                const int trow = b * a.T + n * kC;
+                tma_load_3d(st + RB_DO, &tm_do, &full[s], 0, hv, trow);
+                tma_load_3d(st + RB_DO + 8192, &tm_do, &full[s], 64, hv, trow);
+                tma_load_2d(st + RB_Q, &tm_q, &full[s], 0, row);
+                tma_load_2d(st + RB_Q + 8192, &tm_q, &full[s], 64, row);
+                tma_load_2d(st + RB_W, &tm_w, &full[s], 0, row);
+                tma_load_2d(st + RB_W + 8192, &tm_w, &full[s], 64, row);
+                tma_load_2d(st + RB_KBT, &tm_kbt, &full[s], 0, crow * kD);
+                tma_load_2d(st + RB_AQK, &tm_aqk, &full[s], 0, crow * kC);
+                bulk_load(st + RB_GAM, a.gam + (size_t)crow * kD, 512, &full[s]);
+                issued = i + 1;
+            }
+            for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
+                wait_bar(&full[i & 1], (i >> 1) & 1, 12);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
+            const uint32_t sS = smem_u32(smem + OFF_S), sD = smem_u32(smem + OFF_DELTA);
+            for (int i = 0; i < NT; ++i) {
+                const int s = i & 1;
+                const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+                if (!wait_bar(&full[s], (i >> 1) & 1, 13)) break;
+                if (!wait_bar(bar_S, i & 1, 14)) break;
+                tc_fence_after();
+                // ddelta^T = dS^T Kb^T  (B = Kb^T tile read MN-major: N = rows r)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + TM2_DD,
+                             sdesc_sw128(sS + (kk >> 2) * 16384 + (kk & 3) * 32),
+                             sdesc_mn_sw128(st + RB_KBT + kk * 2048, 8192), id64 | kBMajorMN,
+                             kk > 0);
+                // ddelta^T += dO^T Aqk
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM2_DD, sdesc_mn_sw128(st + RB_DO + kk * 2048, 8192),
+                             sdesc_mn_sw128(st + RB_AQK + kk * 2048, 8192),
+                             id64 | kAMajorMN | kBMajorMN, 1);
+                mma_commit(bar_dd);
+                // dS^T += dO^T Qh
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM2_S, sdesc_mn_sw128(st + RB_DO + kk * 2048, 8192),
+                             sdesc_mn_sw128(st + RB_Q + kk * 2048, 8192),
+                             id128 | kAMajorMN | kBMajorMN, 1);
+                if (!wait_bar(bar_delta, i & 1, 15)) break;
+                tc_fence_after();
+                // dS^T += (-ddelta^T) W
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + TM2_S, sdesc_sw128(sD + kk * 32),
+                             sdesc_mn_sw128(st + RB_W + kk * 2048, 8192), id128 | kBMajorMN, 1);
+                mma_commit(bar_D4);
+                mma_commit(&empty[s]);
+            }
+            mma_commit(bar_fin);
+            wait_bar(bar_fin, 0, 16);
+        }
+    } else {
+        const int q = warp & 3;
+        const int v = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        uint8_t* sS = smem + OFF_S;
+        uint8_t* sDelta = smem + OFF_DELTA;
+        float r[32];
+        bool ok = true;
+
+        // E1: dS (end of chunk n) -> bf16 operand tile and dh_out; TMEM copy scaled by gam_n.
+        auto e1 = [&](int i) -> bool {
+            const int n = NT - 1 - i, s = i & 1;
+            if (!wait_bar_warp(&full[s], (i >> 1) & 1, 17)) return false;
+            const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + RB_GAM);
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                if (i == 0) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = a.dht ? a.dht[((size_t)bh * kD + cb * 32 + j) * kD + v] : 0.f;
+                } else {
+                    tmem_ld32(tmem + lane_off + TM2_S + cb * 32, r);
+                }
+                __nv_bfloat16* hp = a.dh_out + (((size_t)bh * NT + n) * kD + cb * 32) * kD + v;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hp[(size_t)j * kD] = __float2bfloat16_rn(r[j]);
+                uint8_t* base = sS + (cb >> 1) * 16384;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 pk;
+                    pk.x = pack_bf16(r[8 * j + 0], r[8 * j + 1]);
+                    pk.y = pack_bf16(r[8 * j + 2], r[8 * j + 3]);
+                    pk.z = pack_bf16(r[8 * j + 4], r[8 * j + 5]);
+                    pk.w = pack_bf16(r[8 * j + 6], r[8 * j + 7]);
+                    *reinterpret_cast<uint4*>(base + sw128_offset(v, (cb & 1) * 32 + 8 * j)) = pk;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] *= gam[cb * 32 + j];
+                tmem_st32(tmem + lane_off + TM2_S + cb * 32, r);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_S);
+            return true;
+        };
+
+        ok = e1(0);
+        for (int i = 0; ok && i < NT; ++i) {
+            const int n = NT - 1 - i, s = i & 1;
+            if (!wait_bar_warp(bar_dd, i & 1, 18)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+                tmem_ld32(tmem + lane_off + TM2_DD + cb * 32, r);
+                __nv_bfloat16* dp =
+                    a.dd_out + ((size_t)bh * a.T + (size_t)n * kC + cb * 32) * kD + v;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dp[(size_t)j * kD] = __float2bfloat16_rn(r[j]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 pk;
+                    pk.x = pack_bf16(-r[8 * j + 0], -r[8 * j + 1]);
+                    pk.y = pack_bf16(-r[8 * j + 2], -r[8 * j + 3]);
+                    pk.z = pack_bf16(-r[8 * j + 4], -r[8 * j + 5]);
+                    pk.w = pack_bf16(-r[8 * j + 6], -r[8 * j + 7]);
+                    *reinterpret_cast<uint4*>(sDelta + sw128_offset(v, cb * 32 + 8 * j)) = pk;
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_delta);
+            mbar_arrive(&empty[s]);
+            if (!wait_bar_warp(bar_D4, i & 1, 19)) { ok = false; break; }
+            tc_fence_after();
+            if (i + 1 < NT) {
+                if (!e1(i + 1)) { ok = false; break; }
+            } else if (a.dh0) {
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    tmem_ld32(tmem + lane_off + TM2_S + cb * 32, r);
+                    float* hp = a.dh0 + ((size_t)bh * kD + cb * 32) * kD + v;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) hp[(size_t)j * kD] = r[j];
+                }
+            }
+        }
+        (void)ok;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TM2_COLS);
+}
+
+// ===========================================================================
+// Backward contractions over V, one CTA per (chunk, head), with S0 (state at
+// the chunk start) and dS (gradient at its end) from the two chains:
+//     D1 = S0 dO^T       = dQh^T      (M=128 k, N=64)
+//     D2 = S0 ddelta^T   = -dW^T
+//     D3 = dS delta^T    = dKb^T
+//     D4 = [dO; ddelta] [delta; v]^T : top-left = dO delta^T (-> dAqk),
+//                                      bottom-right = ddelta v^T (-> dTv)
+//     D5 = ddelta^T T    = d(beta v)^T (M=128 v, N=64): dv = beta * D5^T,
+//                                       dbeta += sum_v D5^T o v
+// plus dgam = rowsum(dS o S0).  Results go to the fp32 workspace arrays
+// read by the chunk-local backward kernel; dv is written directly.
+// ===========================================================================
+constexpr uint32_t G_S0 = 0, G_DS = 32768, G_ODD = 65536, G_DV = 98304, G_T = 131072;
+constexpr uint32_t G_BAR = 139264, G_DBV = G_BAR + 64;
+constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
+constexpr uint32_t GRAD_SMEM = G_DBV + 256 + 1024;
+
+struct GradArgs {
+    int T, HV, NT;
+    const __nv_bfloat16* beta;  // [B,T,HV]
+    __nv_bfloat16* dv;          // [B,T,HV,V]
+    float *dQh, *dWm, *dKb, *dgam, *dAqk, *dTv, *dbv;
+};
+
+__global__ void __launch_bounds__(192, 1)
+grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dh,
+              const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dd,
+              const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ CUtensorMap tm_t, GradArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + G_BAR);
+    uint64_t* bar_mma = bar_tma + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 2);
+    float* dbv_s = reinterpret_cast<float*>(smem + G_DBV);  // [64]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / a.HV, hv = bh % a.HV;
+    const int NT = a.NT;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 64) dbv_s[threadIdx.x] = 0.f;
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int row = bh * a.T + n * kC;
+    const int crow = bh * NT + n;
+    const int trow = b * a.T + n * kC;
+
+    if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(bar_tma, GRAD_TX);
+        tma_load_2d(smem + G_S0, &tm_h, bar_tma, 0, crow * kD);
+        tma_load_2d(smem + G_S0 + 16384, &tm_h, bar_tma, 64, crow * kD);
+        tma_load_2d(smem + G_DS, &tm_dh, bar_tma, 0, crow * kD);
+        tma_load_2d(smem + G_DS + 16384, &tm_dh, bar_tma, 64, crow * kD);
+        tma_load_3d(smem + G_ODD, &tm_do, bar_tma, 0, hv, trow);
+        tma_load_3d(smem + G_ODD + 16384, &tm_do, bar_tma, 64, hv, trow);
+        tma_load_2d(smem + G_ODD + 8192, &tm_dd, bar_tma, 0, row);
+        tma_load_2d(smem + G_ODD + 24576, &tm_dd, bar_tma, 64, row);
+        tma_load_2d(smem + G_DV, &tm_d, bar_tma, 0, row);
+        tma_load_2d(smem + G_DV + 16384, &tm_d, bar_tma, 64, row);
+        tma_load_3d(smem + G_DV + 8192, &tm_v, bar_tma, 0, hv, trow);
+        tma_load_3d(smem + G_DV + 24576, &tm_v, bar_tma, 64, hv, trow);
+        tma_load_2d(smem + G_T, &tm_t, bar_tma, 0, crow * kC);
+    } else if (warp == 1 && lane == 0) {
+        if (wait_bar(bar_tma, 0, 21)) {
+            tc_fence_after();
+            const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
+            const uint32_t s0 = smem_u32(smem + G_S0), ds = smem_u32(smem + G_DS);
+            const uint32_t odd = smem_u32(smem + G_ODD), dvt = smem_u32(smem + G_DV);
+            const uint32_t tt = smem_u32(smem + G_T);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                mma_bf16(tmem + 0, sdesc_sw128(s0 + ko), sdesc_sw128(odd + ko), id64, kk > 0);
+                mma_bf16(tmem + 64, sdesc_sw128(s0 + ko), sdesc_sw128(odd + 8192 + ko), id64,
+                         kk > 0);
+                mma_bf16(tmem + 128, sdesc_sw128(ds + ko), sdesc_sw128(dvt + ko), id64, kk > 0);
+                mma_bf16(tmem + 256, sdesc_sw128(odd + ko), sdesc_sw128(dvt + ko), id128, kk > 0);
+            }
+            // D5 = ddelta^T T: ddelta tile read MN-major (v blocks 16 KB apart), T MN-major
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + 192, sdesc_mn_sw128(odd + 8192 + kk * 2048, 16384),
+                         sdesc_mn_sw128(tt + kk * 2048, 8192), id64 | kAMajorMN | kBMajorMN,
+                         kk > 0);
+            mma_commit(bar_mma);
+            wait_bar(bar_mma, 0, 22);
+        }
+    } else if (warp >= 2) {
+        const int q = warp & 3;
+        const int l = q * 32 + lane;  // TMEM lane: k for D1-D3, row for D4, v for D5
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        float r[32];
+        bool ok = wait_bar_warp(bar_tma, 0, 23);
+        // dgam[k] = sum_v dS[k][v] S0[k][v] from the bf16 tiles (independent of the MMAs)
+        if (ok) {
+            float acc = 0.f;
+#pragma unroll 1
+            for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint32_t off = kb * 16384 + sw128_offset(l, c8 * 8);
+                    const uint4 x = *reinterpret_cast<const uint4*>(smem + G_S0 + off);
+                    const uint4 y = *reinterpret_cast<const uint4*>(smem + G_DS + off);
+                    const __nv_bfloat162* xa = reinterpret_cast<const __nv_bfloat162*>(&x);
+                    const __nv_bfloat162* ya = reinterpret_cast<const __nv_bfloat162*>(&y);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 xf = __bfloat1622float2(xa[u]), yf = __bfloat1622float2(ya[u]);
+                        acc += xf.x * yf.x + xf.y * yf.y;
+                    }
+                }
+            a.dgam[(size_t)crow * kD + l] = acc;
+        }
+        ok = ok && wait_bar_warp(bar_mma, 0, 24);
+        if (ok) {
+            tc_fence_after();
+            const size_t rb = (size_t)row * kD;
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+                tmem_ld32(tmem + lane_off + 0 + cb * 32, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a.dQh[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
+                tmem_ld32(tmem + lane_off + 64 + cb * 32, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a.dWm[rb + (size_t)(cb * 32 + j) * kD + l] = -r[j];
+                tmem_ld32(tmem + lane_off + 128 + cb * 32, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a.dKb[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
+            }
+            const size_t cc = (size_t)crow * kC * kC;
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                tmem_ld32(tmem + lane_off + 256 + cb * 32, r);
+                if (l < 64 && cb < 2) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = cb * 32 + j;
+                        a.dAqk[cc + (size_t)l * kC + m] = m <= l ? r[j] : 0.f;
+                    }
+                } else if (l >= 64 && cb >= 2) {
+                    const int i = l - 64;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = cb * 32 + j - 64;
+                        a.dTv[cc + (size_t)i * kC + m] = m < i ? r[j] : 0.f;
+                    }
+                }
+            }
+            // D5: lane = v
+#pragma unroll 1
+            for (int cb = 0; cb < 2; ++cb) {
+                tmem_ld32(tmem + lane_off + 192 + cb * 32, r);
+#pragma unroll 4
+                for (int j = 0; j < 32; ++j) {
+                    const int m = cb * 32 + j;
+                    const float bt =
+                        __bfloat162float(a.beta[((size_t)trow + m) * a.HV + hv]);
+                    a.dv[(((size_t)trow + m) * a.HV + hv) * kD + l] = __float2bfloat16_rn(bt * r[j]);
+                    const uint32_t voff = G_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
+                    float p = r[j] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                    if (lane == 0) atomicAdd(&dbv_s[m], p);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x < 64) a.dbv[(size_t)row + threadIdx.x] = dbv_s[threadIdx.x];
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ===========================================================================
+// Intra-chunk quantities on tensor cores, one CTA (128 threads) per (chunk,
+// head): K3 row L2 steps (1)-(3) plus the operands of the state passes.
+//   (1) G = cumsum(max(g,-5)) per key channel (thread c owns channel c).
+//   (2) A, Aqk: the pairwise decay exp(G_i - G_j) is factored per 16-row
+//       block R with reference row b = 16R:  exp(G_i - G_b) <= 1 on the left,
+//       exp(G_b - G_j) on the right (<= 1 for earlier blocks, <= e^75 inside
+//       the block since g >= -5), so no factor overflows fp32/bf16.
+//       D_R = Left Right_R^T (M=128, N=16(R+1), K=128), where Left row
+//       32R + 16s + u holds token 16R+u (s=0: k, s=1: scale*q) times
+//       exp(G - G_b), so TMEM warp quadrant R holds exactly block R's rows.
+//   (3) T = (I + A)^{-1} (fp32, blocked forward substitution),
+//       W^T = Khat^T (T diag beta)^T, U^T = V^T (T diag beta)^T with Khat and
+//       V read MN-major from their tiles.
+// Writes W, Qh, U, Kb^T, Aqk, T (bf16 operand arrays), T (fp32) and gam.
+// ===========================================================================
+constexpr uint32_t I_K = 0, I_Q = 16384, I_G = 32768, I_V = 49152;   // TMA tiles, 16 KB each
+constexpr uint32_t I_LEFT = 65536;                                   // 128 rows x 128, 32 KB
+constexpr uint32_t I_R0 = 98304;   // Right_R: 16(R+1) rows x 128: 4, 8, 12, 16 KB
+constexpr uint32_t I_KHAT = I_R0 + 40960;                            // 16 KB
+constexpr uint32_t I_TB = I_KHAT + 16384;                            // T*beta, 64x64 bf16, 8 KB
+constexpr uint32_t I_A = I_TB + 8192;                                // fp32 [64][65]
+constexpr uint32_t I_T = I_A + 64 * 65 * 4;                          // fp32 [64][65]
+constexpr uint32_t I_BETA = I_T + 64 * 65 * 4;                       // fp32 [64]
+constexpr uint32_t I_BAR = I_BETA + 256;
+constexpr uint32_t INTRA_SMEM = I_BAR + 64 + 1024;
+constexpr uint32_t INTRA_TX = 4 * 16384;
+
+__host__ __device__ constexpr uint32_t right_off(int R) {  // byte offset of Right_R
+    return I_R0 + 2048u * (uint32_t)(R * (R + 1));         // sum_{J<R} 4096 (J+1)
+}
+__host__ __device__ constexpr uint32_t right_col(int R) {  // TMEM column of D_R
+    return 8u * (uint32_t)(R * (R + 1));                   // sum_{J<R} 16 (J+1)
+}
+
+struct IntraArgs {
+    int T, H, HV, NT;
+    float scale;
+    const __nv_bfloat16* beta;
+    __nv_bfloat16 *W2, *Q2, *U2, *KbT2, *Aqk2, *T2;
+    float *Tm, *gam;
+};
+
+template <int R>
+__device__ __forceinline__ void intra_read_block(uint32_t taddr, float* out /* 64 */) {
+    // lanes of warp quadrant R: columns of D_R (16(R+1) of them)
+    float r[32];
+    constexpr int N = 16 * (R + 1);
+#pragma unroll
+    for (int cb = 0; cb < (N + 31) / 32; ++cb) {
+        tmem_ld32(taddr + cb * 32, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (cb * 32 + j < N) out[cb * 32 + j] = r[j];
+    }
+#pragma unroll
+    for (int j = N; j < 64; ++j) out[j] = 0.f;
+}
+
+__global__ void __launch_bounds__(128, 1)
+intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
+                IntraArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + I_BAR);
+    uint64_t* bar_a = bar_tma + 1;
+    uint64_t* bar_w = bar_tma + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    float* sA = reinterpret_cast<float*>(smem + I_A);
+    float* sT = reinterpret_cast<float*>(smem + I_T);
+    float* sBeta = reinterpret_cast<float*>(smem + I_BETA);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / a.HV, hv = bh % a.HV, h = hv / (a.HV / a.H);
+    const int trow = b * a.T + n * kC;        // token row in [B*T]
+    const int row0 = bh * a.T + n * kC;       // row in the [BH*T] workspace arrays
+    const int crow = bh * a.NT + n;           // chunk index
+
+    if (tid == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_a, 1);
+        mbar_init(bar_w, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_holder, 256);
+        tmem_relinquish();
+    }
+    if (tid < kC) sBeta[tid] = __bfloat162float(a.beta[((size_t)trow + tid) * a.HV + hv]);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_tma, INTRA_TX);
+        tma_load_3d(smem + I_K, &tm_k, bar_tma, 0, h, trow);
+        tma_load_3d(smem + I_K + 8192, &tm_k, bar_tma, 64, h, trow);
+        tma_load_3d(smem + I_Q, &tm_q, bar_tma, 0, h, trow);
+        tma_load_3d(smem + I_Q + 8192, &tm_q, bar_tma, 64, h, trow);
+        tma_load_3d(smem + I_G, &tm_g, bar_tma, 0, hv, trow);
+        tma_load_3d(smem + I_G + 8192, &tm_g, bar_tma, 64, hv, trow);
+        tma_load_3d(smem + I_V, &tm_v, bar_tma, 0, hv, trow);
+        tma_load_3d(smem + I_V + 8192, &tm_v, bar_tma, 64, hv, trow);
+    }
+    bool ok = wait_bar_warp(bar_tma, 0, 31);
+
+    // ---- (1) cumsum and decay factors: thread c owns key channel c ----
+    const int c = tid;
+    const uint32_t kbo = (c >> 6) * 8192, cc = c & 63;
+    auto ld = [&](uint32_t tile, int r) {
+        return __bfloat162float(
+            *reinterpret_cast<const __nv_bfloat16*>(smem + tile + kbo + sw128_offset(r, cc)));
+    };
+    auto st = [&](uint32_t off, float x) {
+        *reinterpret_cast<__nv_bfloat16*>(smem + off) = __float2bfloat16_rn(x);
+    };
+    float G[kC];
+    {
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < kC; ++r) {
+            acc += fmaxf(ld(I_G, r), kGateFloor);
+            G[r] = acc;
+        }
+    }
+    float eGb[4], eLb[4];  // exp(G_b), exp(G_last - G_b) per block
+#pragma unroll
+    for (int R = 0; R < 4; ++R) {
+        eGb[R] = __expf(G[16 * R]);
+        eLb[R] = __expf(G[kC - 1] - G[16 * R]);
+    }
+    a.gam[(size_t)crow * kD + c] = __expf(G[kC - 1]);
+
+    // ---- operands: Left, Right_R, Khat (smem); Qh, Kb^T (global) ----
+#pragma unroll 4
+    for (int r = 0; r < kC; ++r) {
+        const int R = r >> 4, u = r & 15;
+        const float Gb = G[16 * R];
+        const float E = __expf(G[r] - Gb);        // <= 1
+        const float Einv = __expf(Gb - G[r]);     // in [1, e^75]
+        const float kv = ld(I_K, r), qv = a.scale * ld(I_Q, r);
+        const uint32_t lrow_k = 32 * R + u, lrow_q = 32 * R + 16 + u;
+        st(I_LEFT + (c >> 6) * 16384 + sw128_offset(lrow_k, cc), kv * E);
+        st(I_LEFT + (c >> 6) * 16384 + sw128_offset(lrow_q, cc), qv * E);
+        // Right_Rr (Rr >= R): k_r exp(G_{b(Rr)} - G_r) = k_r Einv exp(G_{b(Rr)} - G_b)
+#pragma unroll
+        for (int Rr = 0; Rr < 4; ++Rr) {
+            if (Rr < R) continue;
+            const float f = Rr == R ? 1.f : __expf(G[16 * Rr] - Gb);
+            const uint32_t rows = 16u * (Rr + 1);
+            st(right_off(Rr) + (c >> 6) * (rows * 128u) + sw128_offset(r, cc), kv * Einv * f);
+        }
+        const float eG = eGb[R] * E;              // exp(G_r)
+        st(I_KHAT + kbo + sw128_offset(r, cc), kv * eG);
+        a.Q2[((size_t)row0 + r) * kD + c] = __float2bfloat16_rn(qv * eG);
+        a.KbT2[((size_t)crow * kD + c) * kC + r] = __float2bfloat16_rn(kv * eLb[R] * Einv);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- (2) D_R = Left Right_R^T ----
+    if (tid == 0 && ok) {
+        const uint32_t left = smem_u32(smem + I_LEFT);
+#pragma unroll
+        for (int R = 0; R < 4; ++R) {
+            const uint32_t rows = 16u * (R + 1);
+            const uint32_t right = smem_u32(smem + right_off(R));
+            const uint32_t id = idesc_bf16_f32(128, 16 * (R + 1));
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16(tmem + right_col(R),
+                         sdesc_sw128(left + (kk >> 2) * 16384 + (kk & 3) * 32),
+                         sdesc_sw128(right + (kk >> 2) * (rows * 128u) + (kk & 3) * 32), id,
+                         kk > 0);
+        }
+        mma_commit(bar_a);
+    }
+    ok = ok && wait_bar_warp(bar_a, 0, 32);
+    tc_fence_after();
+    if (ok) {
+        // warp R reads block R: lanes 0-15 -> A rows, 16-31 -> Aqk rows
+        float d[64];
+        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + right_col(warp);
+        if (warp == 0) intra_read_block<0>(taddr, d);
+        else if (warp == 1) intra_read_block<1>(taddr, d);
+        else if (warp == 2) intra_read_block<2>(taddr, d);
+        else intra_read_block<3>(taddr, d);
+        const int u = lane & 15, i = 16 * warp + u;
+        if (lane < 16) {
+            const float bi = sBeta[i];
+#pragma unroll
+            for (int j = 0; j < kC; ++j) sA[i * 65 + j] = j < i ? bi * d[j] : 0.f;
+        } else {
+            __nv_bfloat16* ap = a.Aqk2 + ((size_t)crow * kC + i) * kC;
+#pragma unroll
+            for (int j = 0; j < kC; j += 8) {
+                uint4 pk;
+                pk.x = pack_bf16(j + 0 <= i ? d[j + 0] : 0.f, j + 1 <= i ? d[j + 1] : 0.f);
+                pk.y = pack_bf16(j + 2 <= i ? d[j + 2] : 0.f, j + 3 <= i ? d[j + 3] : 0.f);
+                pk.z = pack_bf16(j + 4 <= i ? d[j + 4] : 0.f, j + 5 <= i ? d[j + 5] : 0.f);
+                pk.w = pack_bf16(j + 6 <= i ? d[j + 6] : 0.f, j + 7 <= i ? d[j + 7] : 0.f);
+                *reinterpret_cast<uint4*>(ap + j) = pk;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- (3) T = (I + A)^{-1}: diagonal 16x16 blocks, then block rows ----
+    if (tid < 64) {
+        const int R = tid >> 4, jj = tid & 15, j = 16 * R + jj;
+        for (int i = 0; i < kC; ++i) sT[i * 65 + j] = 0.f;
+        sT[j * 65 + j] = 1.f;
+        for (int ii = jj + 1; ii < 16; ++ii) {
+            const int i = 16 * R + ii;
+            float acc = 0.f;
+            for (int m = j; m < i; ++m) acc += sA[i * 65 + m] * sT[m * 65 + j];
+            sT[i * 65 + j] = -acc;
+        }
+    }
+    __syncthreads();
+    for (int dist = 1; dist < 4; ++dist) {
+        // X_RJ = sum_{M=J}^{R-1} A_RM T_MJ for J = R - dist, stored in the (R,J) block of sA
+        // (A's own (R,J) block is no longer needed once consumed below).
+        const int nblk = 4 - dist;
+        float xv[8];
+        for (int e = 0; e < 8; ++e) {
+            const int idx = tid + e * 128;
+            xv[e] = 0.f;
+            if (idx < nblk * 256) {
+                const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
+                const int J = blk, R = blk + dist, i = 16 * R + ii, j = 16 * J + jj;
+                float acc = 0.f;
+                for (int m = 16 * J; m < 16 * R; ++m) acc += sA[i * 65 + m] * sT[m * 65 + j];
+                xv[e] = acc;
+            }
+        }
+        __syncthreads();
+        for (int e = 0; e < 8; ++e) {
+            const int idx = tid + e * 128;
+            if (idx < nblk * 256) {
+                const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
+                const int R = blk + dist;
+                sT[(16 * R + ii) * 65 + 16 * blk + jj] = xv[e];  // staging: X in T's slot
+            }
+        }
+        __syncthreads();
+        // T_RJ = -T_RR X_RJ
+        for (int e = 0; e < 8; ++e) {
+            const int idx = tid + e * 128;
+            xv[e] = 0.f;
+            if (idx < nblk * 256) {
+                const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
+                const int R = blk + dist, i = 16 * R + ii, j = 16 * blk + jj;
+                float acc = 0.f;
+                for (int m = 16 * R; m <= i; ++m) acc += sT[i * 65 + m] * sT[m * 65 + j];
+                xv[e] = -acc;
+            }
+        }
+        __syncthreads();
+        for (int e = 0; e < 8; ++e) {
+            const int idx = tid + e * 128;
+            if (idx < nblk * 256) {
+                const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
+                const int R = blk + dist;
+                sT[(16 * R + ii) * 65 + 16 * blk + jj] = xv[e];
+            }
+        }
+        __syncthreads();
+    }
+    // T (fp32, bf16) to global; T*beta to the B-operand tile
+    for (int idx = tid; idx < kC * kC; idx += 128) {
+        const int i = idx >> 6, j = idx & 63;
+        const float t = sT[i * 65 + j];
+        a.Tm[(size_t)crow * kC * kC + idx] = t;
+        a.T2[(size_t)crow * kC * kC + idx] = __float2bfloat16_rn(t);
+        st(I_TB + sw128_offset(i, j), t * sBeta[j]);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && ok) {
+        const uint32_t id = idesc_bf16_f32(128, 64) | kAMajorMN;
+        const uint32_t kh = smem_u32(smem + I_KHAT), vt = smem_u32(smem + I_V);
+        const uint32_t tb = smem_u32(smem + I_TB);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            mma_bf16(tmem + 0, sdesc_mn_sw128(kh + kk * 2048, 8192), sdesc_sw128(tb + kk * 32), id,
+                     kk > 0);
+            mma_bf16(tmem + 64, sdesc_mn_sw128(vt + kk * 2048, 8192), sdesc_sw128(tb + kk * 32), id,
+                     kk > 0);
+        }
+        mma_commit(bar_w);
+    }
+    ok = ok && wait_bar_warp(bar_w, 0, 33);
+    tc_fence_after();
+    if (ok) {
+        float r[32];
+        const uint32_t lo = (uint32_t)(warp * 32) << 16;
+        const int l = warp * 32 + lane;  // k for W^T, v for U^T
+#pragma unroll 1
+        for (int cb = 0; cb < 2; ++cb) {
+            tmem_ld32(tmem + lo + cb * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                a.W2[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
+            tmem_ld32(tmem + lo + 64 + cb * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                a.U2[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // Converts the fp32 per-chunk quantities of the SIMT intra kernel into the
-// bf16 operand layouts of the chain kernel.
+// bf16 operand layouts of the tensor-core kernels (T2 only when non-null).
 __global__ void pack_operands_kernel(int BH, int T, int NT, const float* __restrict__ W,
                                      const float* __restrict__ Qh, const float* __restrict__ U,
                                      const float* __restrict__ Kb, const float* __restrict__ Aqk,
-                                     __nv_bfloat16* __restrict__ W2, __nv_bfloat16* __restrict__ Q2,
-                                     __nv_bfloat16* __restrict__ U2,
+                                     const float* __restrict__ Tm, __nv_bfloat16* __restrict__ W2,
+                                     __nv_bfloat16* __restrict__ Q2, __nv_bfloat16* __restrict__ U2,
                                      __nv_bfloat16* __restrict__ KbT2,
-                                     __nv_bfloat16* __restrict__ Aqk2) {
+                                     __nv_bfloat16* __restrict__ Aqk2,
+                                     __nv_bfloat16* __restrict__ T2) {
     const size_t nrow = (size_t)BH * T * kD;
     const size_t ncc = (size_t)BH * NT * kC * kC;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nrow;
@@ -337,7 +1087,10 @@ __global__ void pack_operands_kernel(int BH, int T, int NT, const float* __restr
         const size_t chunk = i / (kC * kD), rem = i % (kC * kD);
         const size_t k = rem / kC, c = rem % kC;
         KbT2[i] = __float2bfloat16_rn(Kb[(chunk * kC + c) * kD + k]);
-        if (i < ncc) Aqk2[i] = __float2bfloat16_rn(Aqk[i]);
+        if (i < ncc) {
+            Aqk2[i] = __float2bfloat16_rn(Aqk[i]);
+            if (T2) T2[i] = __float2bfloat16_rn(Tm[i]);
+        }
     }
 }
 
@@ -378,12 +1131,28 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
            CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over a token tensor [B*T][heads][128] (a per-head tile of 64
+// tokens is a box {64 columns, 1 head, 64 tokens}), 128B swizzle.
+bool make_map_tok(CUtensorMap* m, const void* ptr, uint64_t BT, uint64_t heads) {
+    EncodeFn enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {kD, heads, BT};
+    cuuint64_t strides[2] = {kD * 2, heads * kD * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 struct TcWs {
-    char* simt;                      // SIMT intra workspace (fp32 quantities)
-    __nv_bfloat16 *W2, *Q2, *U2, *KbT2, *Aqk2;
+    char* simt;  // SIMT workspace (fp32 quantities)
+    __nv_bfloat16 *W2, *Q2, *U2, *KbT2, *Aqk2;       // forward chain operands
+    __nv_bfloat16 *T2, *h2, *d2, *dh2, *dd2;         // backward only
 };
 
-size_t tc_carve(const kda_dims& d, char* base, TcWs* w) {
+size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     const size_t BH = (size_t)d.B * d.HV, T = d.T, NT = d.T / kC;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -391,44 +1160,86 @@ size_t tc_carve(const kda_dims& d, char* base, TcWs* w) {
         off += align256(bytes);
         return p;
     };
+    auto bf = [&](size_t elems) { return reinterpret_cast<__nv_bfloat16*>(take(elems * 2)); };
     TcWs x{};
-    x.simt = take(simt_workspace_bytes(d, 0));
-    x.W2 = reinterpret_cast<__nv_bfloat16*>(take(BH * T * kD * 2));
-    x.Q2 = reinterpret_cast<__nv_bfloat16*>(take(BH * T * kD * 2));
-    x.U2 = reinterpret_cast<__nv_bfloat16*>(take(BH * T * kD * 2));
-    x.KbT2 = reinterpret_cast<__nv_bfloat16*>(take(BH * NT * kD * kC * 2));
-    x.Aqk2 = reinterpret_cast<__nv_bfloat16*>(take(BH * NT * kC * kC * 2));
+    x.simt = take(simt_workspace_bytes(d, for_bwd));
+    x.W2 = bf(BH * T * kD);
+    x.Q2 = bf(BH * T * kD);
+    x.U2 = bf(BH * T * kD);
+    x.KbT2 = bf(BH * NT * kD * kC);
+    x.Aqk2 = bf(BH * NT * kC * kC);
+    if (for_bwd) {
+        x.T2 = bf(BH * NT * kC * kC);
+        x.h2 = bf(BH * NT * kD * kD);
+        x.d2 = bf(BH * T * kD);
+        x.dh2 = bf(BH * NT * kD * kD);
+        x.dd2 = bf(BH * T * kD);
+    }
     if (w) *w = x;
     return off;
 }
 
-}  // namespace
-
-bool tc_supported(const kda_dims& d) {
-    return d.dtype == KDA_BF16 && d.K == kD && d.V == kD && d.chunk_size == kC &&
-           get_encoder() != nullptr;
-}
-
-size_t tc_workspace_bytes(const kda_dims& d, int for_bwd) {
-    if (for_bwd) return simt_workspace_bytes(d, 1);
-    return tc_carve(d, nullptr, nullptr);
-}
-
-kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
-                  const void* beta, const float* h0, void* o, float* ht, void* ws,
-                  cudaStream_t s) {
-    TcWs w;
-    tc_carve(d, static_cast<char*>(ws), &w);
-    SimtIntraOut io;
-    kda_status st = simt_intra_only(d, q, k, v, g, beta, w.simt, &io, s);
+// Intra-chunk quantities (SIMT, fp32) and their bf16 operand copies.
+kda_status run_intra_pack(const kda_dims& d, const TcWs& w, const void* q, const void* k,
+                          const void* v, const void* g, const void* beta, cudaStream_t s,
+                          SimtIntraOut* io) {
+    kda_status st = simt_intra_only(d, q, k, v, g, beta, w.simt, io, s);
     if (st != KDA_OK) return st;
+    SimtWsPtrs p;
+    simt_ws_ptrs(d, 0, w.simt, &p);
     const int BH = d.B * d.HV, NT = d.T / kC;
     {
         TimedLaunch tl("tc_pack", s);
-        pack_operands_kernel<<<152 * 8, 256, 0, s>>>(BH, d.T, NT, io.W, io.Qh, io.U, io.Kb, io.Aqk,
-                                                     w.W2, w.Q2, w.U2, w.KbT2, w.Aqk2);
+        pack_operands_kernel<<<152 * 8, 256, 0, s>>>(BH, d.T, NT, io->W, io->Qh, io->U, io->Kb,
+                                                     io->Aqk, p.Tm, w.W2, w.Q2, w.U2, w.KbT2,
+                                                     w.Aqk2, w.T2);
     }
-    if ((st = launch_status()) != KDA_OK) return st;
+    return launch_status();
+}
+
+// Intra-chunk quantities on tensor cores, written straight into the operand
+// arrays (and T, gam into the fp32 workspace arrays the backward tail reads).
+kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const void* k,
+                        const void* v, const void* g, const void* beta, cudaStream_t s,
+                        float** gam_out) {
+    SimtWsPtrs p;
+    simt_ws_ptrs(d, 0, w.simt, &p);
+    const int BH = d.B * d.HV, NT = d.T / kC;
+    const uint64_t BT = (uint64_t)d.B * d.T;
+    CUtensorMap mk, mq, mg, mv;
+    if (!make_map_tok(&mk, k, BT, d.H) || !make_map_tok(&mq, q, BT, d.H) ||
+        !make_map_tok(&mg, g, BT, d.HV) || !make_map_tok(&mv, v, BT, d.HV))
+        return KDA_ERR_CUDA;
+    IntraArgs a;
+    a.T = d.T;
+    a.H = d.H;
+    a.HV = d.HV;
+    a.NT = NT;
+    a.scale = d.scale;
+    a.beta = static_cast<const __nv_bfloat16*>(beta);
+    a.W2 = w.W2;
+    a.Q2 = w.Q2;
+    a.U2 = w.U2;
+    a.KbT2 = w.KbT2;
+    a.Aqk2 = w.Aqk2;
+    a.T2 = w.T2;
+    a.Tm = p.Tm;
+    a.gam = p.gam;
+    if (cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)INTRA_SMEM) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    {
+        TimedLaunch tl("tc_intra", s);
+        intra_tc_kernel<<<dim3(NT, BH), 128, INTRA_SMEM, s>>>(mk, mq, mg, mv, a);
+    }
+    *gam_out = p.gam;
+    return launch_status();
+}
+
+kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, const float* h0,
+                         void* o, float* ht, __nv_bfloat16* h_out, __nv_bfloat16* delta_out,
+                         cudaStream_t s) {
+    const int BH = d.B * d.HV, NT = d.T / kC;
     CUtensorMap mw, mq, mk, ma, mu;
     const uint64_t rows = (uint64_t)BH * d.T;
     if (!make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
@@ -442,12 +1253,12 @@ kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v
     args.T = d.T;
     args.HV = d.HV;
     args.NT = NT;
-    args.gam = io.gam;
+    args.gam = gam;
     args.h0 = h0;
     args.o = static_cast<__nv_bfloat16*>(o);
     args.ht = ht;
-    args.h_out = nullptr;
-    args.delta_out = nullptr;
+    args.h_out = h_out;
+    args.delta_out = delta_out;
     if (cudaFuncSetAttribute(chain_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)CHAIN_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -458,12 +1269,103 @@ kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v
     return launch_status();
 }
 
+}  // namespace
+
+bool tc_supported(const kda_dims& d) {
+    return d.dtype == KDA_BF16 && d.K == kD && d.V == kD && d.chunk_size == kC &&
+           get_encoder() != nullptr;
+}
+
+size_t tc_workspace_bytes(const kda_dims& d, int for_bwd) {
+    return tc_carve(d, for_bwd ? 1 : 0, nullptr, nullptr);
+}
+
+kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
+                  const void* beta, const float* h0, void* o, float* ht, void* ws,
+                  cudaStream_t s) {
+    TcWs w;
+    tc_carve(d, 0, static_cast<char*>(ws), &w);
+    SimtIntraOut io;
+    kda_status st = run_intra_pack(d, w, q, k, v, g, beta, s, &io);
+    if (st != KDA_OK) return st;
+    return run_chain_fwd(d, w, io.gam, h0, o, ht, nullptr, nullptr, s);
+}
+
 kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
                   const void* beta, const float* h0, const void* dout, const float* dht,
                   void* dq, void* dk, void* dv, void* dg, void* dbeta, float* dh0, void* ws,
                   cudaStream_t s) {
-    // The backward runs the SIMT kernels until its tensor-core kernels land.
-    return simt_bwd(d, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, ws, s);
+    TcWs w;
+    tc_carve(d, 1, static_cast<char*>(ws), &w);
+    SimtIntraOut io;
+    kda_status st = run_intra_pack(d, w, q, k, v, g, beta, s, &io);
+    if (st != KDA_OK) return st;
+    // forward recompute: chunk-start states and delta
+    if ((st = run_chain_fwd(d, w, io.gam, h0, nullptr, nullptr, w.h2, w.d2, s)) != KDA_OK)
+        return st;
+    const int BH = d.B * d.HV, NT = d.T / kC;
+    const uint64_t rows = (uint64_t)BH * d.T;
+    // reverse chain
+    {
+        CUtensorMap mdo, mq, mw, mk, ma;
+        if (!make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
+            !make_map(&mq, w.Q2, rows, kD, 64, 64, true) ||
+            !make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
+            !make_map(&mk, w.KbT2, (uint64_t)BH * NT * kD, kC, 64, 128, true) ||
+            !make_map(&ma, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
+            return KDA_ERR_CUDA;
+        ChainBwdArgs a;
+        a.B = d.B;
+        a.T = d.T;
+        a.HV = d.HV;
+        a.NT = NT;
+        a.gam = io.gam;
+        a.dht = dht;
+        a.dh0 = dh0;
+        a.dh_out = w.dh2;
+        a.dd_out = w.dd2;
+        if (cudaFuncSetAttribute(chain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)CHAIN_SMEM) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        TimedLaunch tl("tc_chain_bwd", s);
+        chain_bwd_kernel<<<BH, 192, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, a);
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    // contractions over V
+    {
+        SimtWsPtrs p;
+        simt_ws_ptrs(d, 1, w.simt, &p);
+        CUtensorMap mh, mdh, mdo, mdd, md, mv, mt;
+        const uint64_t srows = (uint64_t)BH * NT * kD;
+        if (!make_map(&mh, w.h2, srows, kD, 64, 128, true) ||
+            !make_map(&mdh, w.dh2, srows, kD, 64, 128, true) ||
+            !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
+            !make_map(&mdd, w.dd2, rows, kD, 64, 64, true) ||
+            !make_map(&md, w.d2, rows, kD, 64, 64, true) ||
+            !make_map_tok(&mv, v, (uint64_t)d.B * d.T, d.HV) ||
+            !make_map(&mt, w.T2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
+            return KDA_ERR_CUDA;
+        GradArgs a;
+        a.T = d.T;
+        a.HV = d.HV;
+        a.NT = NT;
+        a.beta = static_cast<const __nv_bfloat16*>(beta);
+        a.dv = static_cast<__nv_bfloat16*>(dv);
+        a.dQh = p.dQh;
+        a.dWm = p.dWm;
+        a.dKb = p.dKb;
+        a.dgam = p.dgam;
+        a.dAqk = p.dAqk;
+        a.dTv = p.dTv;
+        a.dbv = p.dbv;
+        if (cudaFuncSetAttribute(grad_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)GRAD_SMEM) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        TimedLaunch tl("tc_grad_v", s);
+        grad_v_kernel<<<dim3(NT, BH), 192, GRAD_SMEM, s>>>(mh, mdh, mdo, mdd, md, mv, mt, a);
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    return simt_bwd_tail(d, w.simt, q, k, g, beta, dq, dk, dg, dbeta, s);
 }
 
 kda_status tc_take_error(cudaStream_t s) {

@@ -138,12 +138,14 @@ int kda_timing_count(void);
 int kda_timing_entry(int i, char* name, int name_len, double* total_ms, long* launches);
 
 /* Diagnostics: self-test of the tensor-core building blocks.  Computes
- * D[128 x N] = A[128 x 64] * B[N x 64]^T (A, B bf16 row-major, D fp32
- * row-major; N = 64 or 128; all device pointers) with one tcgen05 MMA chain
- * from 128B-swizzled shared-memory tiles staged by TMA (use_tma != 0) or by
- * thread stores (use_tma == 0).  *status (device int, caller-zeroed) is set
- * to 1 if a bounded device wait expired.  Enqueued on `stream`. */
-kda_status kda_selftest_mma(const void* A, const void* B, float* D, int N, int use_tma,
+ * D[128 x N] = A[128 x 64] * B[N x 64]^T (D fp32 row-major; N = 64 or 128;
+ * all device pointers) with one tcgen05 MMA chain from 128B-swizzled
+ * shared-memory tiles.  flags: bit 0 stage by TMA (else by thread stores);
+ * bit 1 A is given K-minor, i.e. as A^T [64][128] row-major (MN-major
+ * operand, TMA only); bit 2 B likewise as B^T [64][N]; bit 3 swap the two
+ * stride fields of the MN-major descriptor.  *status (device int,
+ * caller-zeroed) is set to 1 if a bounded device wait expired. */
+kda_status kda_selftest_mma(const void* A, const void* B, float* D, int N, int flags,
                             int* status, void* stream);
 
 /* Static description of a status code. */
