@@ -190,6 +190,34 @@ def workload_config(w, path):
             "parallelism": "one independent replica per rank"}
 
 
+def measure_decode(kda, dev, hbm):
+    """Decode step at B=256, HV=16, K=V=128 (state 256 MiB fp32), 64 steps,
+    timed with CUDA events; HBM roofline of the step."""
+    from gated_delta_rule_41_gb300 import inputs as I
+    w = I.DECODE_BF16
+    d = I.make_decode_inputs(w, device=dev)
+    state = d["state"]
+    o = torch.empty(w.B, w.HV, w.V, dtype=w.dtype, device=dev)
+    args = [(d["q"][s], d["k"][s], d["v"][s], d["g"][s], d["beta"][s]) for s in range(w.steps)]
+    for s in range(4):
+        kda.recurrent_step(*args[s], state, out=o)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(w.steps):
+        kda.recurrent_step(*args[s], state, out=o)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / w.steps
+    el = 2 if w.dtype == torch.bfloat16 else 4
+    io = w.B * (2 * w.H * w.K + w.HV * (w.V + w.K + 1) + w.HV * w.V) * el
+    bytes_ = 2 * state.numel() * 4 + io
+    gbs = bytes_ / (ms / 1e3) / 1e9
+    return {"workload": w.name, "ms_per_step": ms, "bytes_per_step": bytes_,
+            "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm, "bound": "hbm",
+            "note": "state read once and written once per step; state (256 MiB) > L2"}
+
+
 # --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
@@ -350,6 +378,8 @@ def main():
                     for n, (t, c) in sorted(kernels.items(), key=lambda x: -x[1][0])},
         "clocks": clocks,
     }
+    if world == 1:
+        line["decode"] = measure_decode(kda, dev, hbm)
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

@@ -42,13 +42,6 @@ kda_status decode_launch(const kda_dims& d, const void* q, const void* k, const 
                          cudaStream_t s);
 
 size_t simt_workspace_bytes(const kda_dims& d, int for_bwd);
-// fp32 per-chunk quantities of the SIMT intra-chunk kernel (inside its workspace).
-struct SimtIntraOut {
-    float *W, *U, *Qh, *Kb, *Aqk, *gam;
-};
-kda_status simt_intra_only(const kda_dims& d, const void* q, const void* k, const void* v,
-                           const void* g, const void* beta, void* ws, SimtIntraOut* out,
-                           cudaStream_t s);
 // All fp32 arrays of the SIMT workspace (bwd carve; the forward arrays come
 // first, so their addresses are the same in the forward carve).
 struct SimtWsPtrs {
@@ -61,6 +54,13 @@ void simt_ws_ptrs(const kda_dims& d, int for_bwd, void* ws, SimtWsPtrs* out);
 kda_status simt_bwd_tail(const kda_dims& d, void* ws, const void* q, const void* k,
                          const void* g, const void* beta, void* dq, void* dk, void* dg,
                          void* dbeta, cudaStream_t s);
+// GVA reduction: dq[b,t,h] = sum over the value heads of group h of dqh (fp32).
+kda_status group_sum_launch(const kda_dims& d, const float* dqh, const float* dkh, void* dq,
+                            void* dk, cudaStream_t s);
+// Chunk-local backward for bf16, K = V = 128, chunk 64 (register-tiled fp32).
+kda_status local_bwd_launch(const kda_dims& d, const SimtWsPtrs& p, const void* q,
+                            const void* k, const void* g, const void* beta, void* dq, void* dk,
+                            void* dg, void* dbeta, cudaStream_t s);
 kda_status simt_fwd(const kda_dims& d, const void* q, const void* k, const void* v,
                     const void* g, const void* beta, const float* h0, void* o, float* ht,
                     void* ws, cudaStream_t s);

@@ -514,7 +514,8 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
 //       Tm[C][C+1], dAqk[C][C+1], D[C][C+1], beta[C], dbeta[C]
 // ---------------------------------------------------------------------------
 size_t kgrad_smem(const Dims& d) {
-    return sizeof(float) * (5 * (size_t)d.C * (d.K + 1) + 3 * (size_t)d.C * (d.C + 1) + 2 * d.C);
+    return sizeof(float) * (5 * (size_t)d.C * (d.K + 1) + 3 * (size_t)d.C * (d.C + 1) + 2 * d.C +
+                            18 * (size_t)d.K);
 }
 
 template <typename Tin>
@@ -537,6 +538,9 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     float* D = dAq + C * CP;  // dT -> dT T^T -> dA
     float* bS = D + C * CP;
     float* dbS = bS + C;
+    float* Fb = dbS + C;              // Fb[fidx(R,J)*K + c] = exp(G_bR - G_bJ), J <= R
+    float* eGbS = Fb + 10 * K;        // eGbS[R*K + c] = exp(G_bR)
+    float* eLbS = eGbS + 4 * K;       // eLbS[R*K + c] = exp(G_last - G_bR)
     const int t0 = n * C;
     const size_t row0 = (size_t)bh * d.T + t0;
     const size_t cc0 = ((size_t)bh * d.NT + n) * C * C;
@@ -666,14 +670,12 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     // (reference b = first row of the block): e(t,j) = E_t F[R(t)][R(j)] / E_j
     // with E_r = exp(G_r - G_b(r)) in [e^-75, 1] and F[R][J] = exp(G_bR - G_bJ),
     // so the inner loops are plain FMAs over tables and no factor overflows.
-    // Tm's storage (no longer needed) holds F, exp(G_b) and exp(G_last - G_b).
     const int NB = C / 16;
-    float* Fb = Tm;                   // Fb[(R*4 + J)*K + c]
-    float* eGbS = Tm + 16 * K;        // eGbS[R*K + c] = exp(G_bR)
-    float* eLbS = Tm + 20 * K;        // eLbS[R*K + c] = exp(G_last - G_bR)
+    auto fidx = [](int R, int J) { return R * (R + 1) / 2 + J; };
     for (int i = tid; i < 16 * K; i += kThreads) {
         const int R = i / (4 * K), J = (i / K) % 4, c = i % K;
-        Fb[i] = (R < NB && J <= R) ? expf(GS[16 * R * KP + c] - GS[16 * J * KP + c]) : 0.f;
+        if (R < NB && J <= R)
+            Fb[fidx(R, J) * K + c] = expf(GS[16 * R * KP + c] - GS[16 * J * KP + c]);
     }
     for (int i = tid; i < NB * K; i += kThreads) {
         const int R = i / K, c = i % K;
@@ -703,7 +705,7 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
                     pa += D[r * CP + j] * ke;  // D[r][r] = 0 (strictly lower)
                     pq += dAq[r * CP + j] * ke;
                 }
-                const float f = Fb[(R * 4 + J) * K + c];
+                const float f = Fb[fidx(R, J) * K + c];
                 sA += f * pa;
                 sQ += f * pq;
             }
@@ -736,7 +738,7 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
                     pa += D[t * CP + r] * X[t * KP + c];  // D[r][r] = 0
                     pq += dAq[t * CP + r] * Y[t * KP + c];
                 }
-                const float f = Fb[(R * 4 + J) * K + c];
+                const float f = Fb[fidx(R, J) * K + c];
                 cA += f * pa;
                 cQ += f * pq;
             }
@@ -869,22 +871,6 @@ size_t simt_workspace_bytes(const kda_dims& kd, int for_bwd) {
     return carve(make_dims(kd), for_bwd, nullptr, nullptr);
 }
 
-kda_status simt_intra_only(const kda_dims& kd, const void* q, const void* k, const void* v,
-                           const void* g, const void* beta, void* ws, SimtIntraOut* out,
-                           cudaStream_t s) {
-    const Dims d = make_dims(kd);
-    Ws w;
-    carve(d, 0, static_cast<char*>(ws), &w);
-    out->W = w.W;
-    out->U = w.U;
-    out->Qh = w.Qh;
-    out->Kb = w.Kb;
-    out->Aqk = w.Aqk;
-    out->gam = w.gam;
-    if (kd.dtype == KDA_BF16) return run_intra<__nv_bfloat16>(d, w, q, k, v, g, beta, s);
-    return run_intra<float>(d, w, q, k, v, g, beta, s);
-}
-
 kda_status simt_fwd(const kda_dims& kd, const void* q, const void* k, const void* v,
                     const void* g, const void* beta, const float* h0, void* o, float* ht,
                     void* ws, cudaStream_t s) {
@@ -950,6 +936,21 @@ kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, 
     return simt_tail_t<Tin>(d, w, q, k, g, beta, dq, dk, dg, dbeta, s);
 }
 }  // namespace
+
+kda_status group_sum_launch(const kda_dims& kd, const float* dqh, const float* dkh, void* dq,
+                            void* dk, cudaStream_t s) {
+    const Dims d = make_dims(kd);
+    const size_t total = (size_t)d.B * d.T * d.H * d.K;
+    const int nblk = (int)std::min<size_t>((total + 255) / 256, 152 * 16);
+    TimedLaunch tl("group_sum", s);
+    if (kd.dtype == KDA_BF16)
+        group_sum_kernel<__nv_bfloat16><<<nblk, 256, 0, s>>>(
+            d, dqh, dkh, static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk));
+    else
+        group_sum_kernel<float><<<nblk, 256, 0, s>>>(d, dqh, dkh, static_cast<float*>(dq),
+                                                     static_cast<float*>(dk));
+    return launch_status();
+}
 
 void simt_ws_ptrs(const kda_dims& kd, int for_bwd, void* ws, SimtWsPtrs* o) {
     const Dims d = make_dims(kd);

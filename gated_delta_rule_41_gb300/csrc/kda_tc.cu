@@ -1066,34 +1066,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// Converts the fp32 per-chunk quantities of the SIMT intra kernel into the
-// bf16 operand layouts of the tensor-core kernels (T2 only when non-null).
-__global__ void pack_operands_kernel(int BH, int T, int NT, const float* __restrict__ W,
-                                     const float* __restrict__ Qh, const float* __restrict__ U,
-                                     const float* __restrict__ Kb, const float* __restrict__ Aqk,
-                                     const float* __restrict__ Tm, __nv_bfloat16* __restrict__ W2,
-                                     __nv_bfloat16* __restrict__ Q2, __nv_bfloat16* __restrict__ U2,
-                                     __nv_bfloat16* __restrict__ KbT2,
-                                     __nv_bfloat16* __restrict__ Aqk2,
-                                     __nv_bfloat16* __restrict__ T2) {
-    const size_t nrow = (size_t)BH * T * kD;
-    const size_t ncc = (size_t)BH * NT * kC * kC;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nrow;
-         i += (size_t)gridDim.x * blockDim.x) {
-        W2[i] = __float2bfloat16_rn(W[i]);
-        Q2[i] = __float2bfloat16_rn(Qh[i]);
-        U2[i] = __float2bfloat16_rn(U[i]);
-        // KbT2[(chunk*128 + k)*64 + c] = Kb[(chunk*64 + c)*128 + k]
-        const size_t chunk = i / (kC * kD), rem = i % (kC * kD);
-        const size_t k = rem / kC, c = rem % kC;
-        KbT2[i] = __float2bfloat16_rn(Kb[(chunk * kC + c) * kD + k]);
-        if (i < ncc) {
-            Aqk2[i] = __float2bfloat16_rn(Aqk[i]);
-            if (T2) T2[i] = __float2bfloat16_rn(Tm[i]);
-        }
-    }
-}
-
 // ---- host: tensor maps ----
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1148,8 +1120,8 @@ bool make_map_tok(CUtensorMap* m, const void* ptr, uint64_t BT, uint64_t heads) 
 
 struct TcWs {
     char* simt;  // SIMT workspace (fp32 quantities)
-    __nv_bfloat16 *W2, *Q2, *U2, *KbT2, *Aqk2;       // forward chain operands
-    __nv_bfloat16 *T2, *h2, *d2, *dh2, *dd2;         // backward only
+    __nv_bfloat16 *W2, *Q2, *U2, *KbT2, *Aqk2, *T2;  // chain operands, T
+    __nv_bfloat16 *h2, *d2, *dh2, *dd2;              // backward only
 };
 
 size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
@@ -1168,8 +1140,8 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     x.U2 = bf(BH * T * kD);
     x.KbT2 = bf(BH * NT * kD * kC);
     x.Aqk2 = bf(BH * NT * kC * kC);
+    x.T2 = bf(BH * NT * kC * kC);
     if (for_bwd) {
-        x.T2 = bf(BH * NT * kC * kC);
         x.h2 = bf(BH * NT * kD * kD);
         x.d2 = bf(BH * T * kD);
         x.dh2 = bf(BH * NT * kD * kD);
@@ -1177,24 +1149,6 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     }
     if (w) *w = x;
     return off;
-}
-
-// Intra-chunk quantities (SIMT, fp32) and their bf16 operand copies.
-kda_status run_intra_pack(const kda_dims& d, const TcWs& w, const void* q, const void* k,
-                          const void* v, const void* g, const void* beta, cudaStream_t s,
-                          SimtIntraOut* io) {
-    kda_status st = simt_intra_only(d, q, k, v, g, beta, w.simt, io, s);
-    if (st != KDA_OK) return st;
-    SimtWsPtrs p;
-    simt_ws_ptrs(d, 0, w.simt, &p);
-    const int BH = d.B * d.HV, NT = d.T / kC;
-    {
-        TimedLaunch tl("tc_pack", s);
-        pack_operands_kernel<<<152 * 8, 256, 0, s>>>(BH, d.T, NT, io->W, io->Qh, io->U, io->Kb,
-                                                     io->Aqk, p.Tm, w.W2, w.Q2, w.U2, w.KbT2,
-                                                     w.Aqk2, w.T2);
-    }
-    return launch_status();
 }
 
 // Intra-chunk quantities on tensor cores, written straight into the operand
@@ -1285,10 +1239,10 @@ kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v
                   cudaStream_t s) {
     TcWs w;
     tc_carve(d, 0, static_cast<char*>(ws), &w);
-    SimtIntraOut io;
-    kda_status st = run_intra_pack(d, w, q, k, v, g, beta, s, &io);
+    float* gam = nullptr;
+    kda_status st = run_intra_tc(d, w, q, k, v, g, beta, s, &gam);
     if (st != KDA_OK) return st;
-    return run_chain_fwd(d, w, io.gam, h0, o, ht, nullptr, nullptr, s);
+    return run_chain_fwd(d, w, gam, h0, o, ht, nullptr, nullptr, s);
 }
 
 kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
@@ -1297,11 +1251,11 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                   cudaStream_t s) {
     TcWs w;
     tc_carve(d, 1, static_cast<char*>(ws), &w);
-    SimtIntraOut io;
-    kda_status st = run_intra_pack(d, w, q, k, v, g, beta, s, &io);
+    float* gam = nullptr;
+    kda_status st = run_intra_tc(d, w, q, k, v, g, beta, s, &gam);
     if (st != KDA_OK) return st;
     // forward recompute: chunk-start states and delta
-    if ((st = run_chain_fwd(d, w, io.gam, h0, nullptr, nullptr, w.h2, w.d2, s)) != KDA_OK)
+    if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s)) != KDA_OK)
         return st;
     const int BH = d.B * d.HV, NT = d.T / kC;
     const uint64_t rows = (uint64_t)BH * d.T;
@@ -1319,7 +1273,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.T = d.T;
         a.HV = d.HV;
         a.NT = NT;
-        a.gam = io.gam;
+        a.gam = gam;
         a.dht = dht;
         a.dh0 = dh0;
         a.dh_out = w.dh2;

@@ -72,8 +72,13 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
  *   KDA_IMPL_AUTO     tensor-core path when it supports the sizes, else SIMT.
  *   KDA_IMPL_SIMT     fp32 CUDA-core kernels; any K, V <= 128, chunk 16/32/64,
  *                     f32 or bf16 inputs.
- *   KDA_IMPL_TCGEN05  tcgen05/TMEM tensor-core kernels; bf16, K = V in
- *                     {64, 128}, chunk 64.  KDA_ERR_UNSUPPORTED otherwise. */
+ *   KDA_IMPL_TCGEN05  tcgen05/TMEM tensor-core kernels; bf16, K = V = 128,
+ *                     chunk 64.  KDA_ERR_UNSUPPORTED otherwise.  The
+ *                     tensor-core backward does not take dht (it keeps the
+ *                     chunk states as bf16, which an O(1) final-state gradient
+ *                     does not fit to the accuracy bar): with dht != NULL,
+ *                     AUTO runs the SIMT backward and TCGEN05 returns
+ *                     KDA_ERR_UNSUPPORTED. */
 typedef enum { KDA_IMPL_AUTO = 0, KDA_IMPL_SIMT = 1, KDA_IMPL_TCGEN05 = 2 } kda_impl;
 
 typedef struct {

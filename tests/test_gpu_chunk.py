@@ -93,13 +93,25 @@ def test_fp32_k128_full_tile(impl):
     compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
 
 
-@pytest.mark.parametrize("impl", IMPLS)
-def test_bf16_gva_k128(impl):
+@pytest.mark.parametrize("impl,with_dht", [("simt", True), ("auto", True), ("simt", False),
+                                           ("tcgen05", False)])
+def test_bf16_gva_k128(impl, with_dht):
+    """K = V = 128 with GVA; with an O(1) upstream final-state gradient the
+    backward runs the fp32 kernels (AUTO), without it the tensor cores."""
     w = I.Workload("bf16_gva_k128", 2, 256, 2, 4, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
-                   dht=True, seed=23)
+                   dht=with_dht, seed=23)
     inp = I.make_chunk_inputs(w)
     res = run_gpu(inp, w, impl)
     compare_all(res, oracle_chunk(inp, True), w)
+
+
+def test_tcgen05_backward_refuses_final_state_gradient():
+    w = I.Workload("bf16_dht", 1, 128, 1, 1, 128, 128, 64, torch.bfloat16, dht=True, seed=26)
+    t = {n: (x.cuda() if x is not None else None) for n, x in I.make_chunk_inputs(w).items()}
+    with pytest.raises(kda.KdaError) as ei:
+        kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], dht=t["dht"],
+                          impl="tcgen05")
+    assert ei.value.status == 3
 
 
 @pytest.mark.parametrize("impl", IMPLS)
