@@ -124,6 +124,27 @@ kda_status kda_recurrent_step(const kda_dims* dims, const void* q, const void* k
                               const void* v, const void* g, const void* beta, float* state,
                               void* o, void* stream);
 
+/* Allocation-free variant of kda_chunk_fwd, for callers that cannot
+ * allocate device memory where they run the scan: code running while a CUDA
+ * graph is captured, runtimes that only hand out memory from a pool fixed at
+ * start-up, or step loops that forbid allocation.  (The pages describe no
+ * such entry point; it is an addition of this library.)
+ *   Arguments and results are those of kda_chunk_fwd without the workspace;
+ *   dims->impl is ignored and the SIMT kernels run.  Their scratch lives in a
+ *   file-scope device array of 32 MiB that every GPU loading the library
+ *   keeps until the process exits.  Sizes whose scratch would exceed 32 MiB
+ *   are rejected with KDA_ERR_WORKSPACE before anything is enqueued (about
+ *   B*HV*T*(4K+2V)*4 bytes plus two 64x64 fp32 matrices per chunk and head).
+ *   The function calls no cudaMalloc, cudaFree or allocating library routine.
+ *   Its first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress with that device current); make that first call
+ *   before any stream capture.  Every call shares the one array and nothing in
+ *   it needs to start at zero; calls whose work overlaps on the GPU (several
+ *   streams, several host threads) race on it, so serialise them. */
+kda_status kda_chunk_fwd_noalloc(const kda_dims* dims, const void* q, const void* k,
+                                 const void* v, const void* g, const void* beta, const float* h0,
+                                 void* o, int output_final_state, float* ht, void* stream);
+
 /* Synchronise `stream`, then report (and clear) any error a kernel recorded on
  * the device since the last check: KDA_ERR_TIMEOUT for an expired bounded
  * wait, KDA_ERR_CUDA for a runtime error. */
