@@ -230,6 +230,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--B", type=int, default=None,
+                    help="override the batch (profiling / sweeps; default: the workload's)")
+    ap.add_argument("--T", type=int, default=None,
+                    help="override the sequence length (profiling / sweeps)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -238,6 +242,11 @@ def main():
     from gated_delta_rule_41_gb300 import inputs as I
 
     w = I.TRAIN_BF16
+    if args.B is not None or args.T is not None:
+        import dataclasses
+        B = w.B if args.B is None else args.B
+        T = w.T if args.T is None else args.T
+        w = dataclasses.replace(w, B=B, T=T, name=f"kda_layer_B{B}_T{T}_H16_K128")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

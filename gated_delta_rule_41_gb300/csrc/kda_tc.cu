@@ -1319,7 +1319,11 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         grad_v_kernel<<<dim3(NT, BH), 192, GRAD_SMEM, s>>>(mh, mdh, mdo, mdd, md, mv, mt, a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
-    return simt_bwd_tail(d, w.simt, q, k, g, beta, dq, dk, dg, dbeta, s);
+    SimtWsPtrs p;
+    simt_ws_ptrs(d, 1, w.simt, &p);
+    if ((st = local_bwd_launch(d, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
+    if (d.HV == d.H) return KDA_OK;
+    return group_sum_launch(d, p.dqh, p.dkh, dq, dk, s);
 }
 
 kda_status tc_take_error(cudaStream_t s) {
