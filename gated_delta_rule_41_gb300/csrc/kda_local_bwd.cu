@@ -1,5 +1,5 @@
 // Chunk-local part of the backward for K = V = 128, chunk 64: register-tiled
-// fp32 CUDA-core kernel, one CTA (256 threads) per (chunk, head).
+// fp32 CUDA-core kernel, one CTA (512 threads) per (chunk, head).
 //
 // Inputs per chunk (fp32 workspace, written by the V-contraction kernel and
 // the intra-chunk kernel): T, dW, dQh, dKb, dAqk, dTv, dgam, dbv; and q, k,
@@ -18,17 +18,18 @@
 //           (+ sum_r dKb_r Kb_r + dgam gam on the last row)
 //     dbeta = dbv + sum_c (dKb' k e^G + k sA)
 //     dg_s  = [g_s >= -5] sum_{r>=s} dG_r,   dq = scale dqs
-// Thread (tr, tc) = (tid / 32, tid % 32) owns rows 8tr..8tr+7 and columns
+// Thread (tr, tc) = (tid / 32, tid % 32) owns rows 4tr..4tr+3 and columns
 // tc + 32j of every 64 x 128 result (and columns tc, tc+32 of 64 x 64 ones),
-// so each reduction step loads 8 broadcast row values and a few
-// conflict-free column values for 16-32 independent FMAs.
+// so each reduction step loads 4 broadcast row values and a few
+// conflict-free column values for 8-16 independent FMAs.  The fp32 inputs
+// arrive with asynchronous 4-byte copies (many in flight per thread).
 #include "kda_common.cuh"
 #include "kda_timing.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int C = 64, K = 128, KP = K + 1, CP = C + 1, NTH = 256;
+constexpr int C = 64, K = 128, KP = K + 1, CP = C + 1, NTH = 512, RPT = 4;
 
 struct LocalArgs {
     int T, H, HV, NT, G;
@@ -36,6 +37,16 @@ struct LocalArgs {
     const float *Tm, *dW, *dQh, *dKb, *dAqk, *dTv, *dgam, *dbv;
     float *dqh, *dkh;  // fp32 per-value-head outputs (used when G > 1)
 };
+
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 template <typename Tin>
 __global__ void __launch_bounds__(NTH, 1)
@@ -67,19 +78,24 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
     };
     auto fidx = [](int R, int J) { return R * (R + 1) / 2 + J; };
 
-    // ---- load ----
+    // ---- load: fp32 arrays asynchronously, bf16 inputs converted ----
+    for (int i = tid; i < C * K; i += NTH) {
+        const int r = i / K, c = i % K;
+        cp_async4(&X[r * KP + c], &a.dW[(row0 + r) * K + c]);
+    }
+    for (int i = tid; i < C * C; i += NTH) {
+        const int r = i / C, c = i % C;
+        cp_async4(&Ts[r * CP + c], &a.Tm[cc0 + i]);
+        cp_async4(&Aq[r * CP + c], &a.dAqk[cc0 + i]);
+    }
+#pragma unroll 4
     for (int i = tid; i < C * K; i += NTH) {
         const int r = i / K, c = i % K;
         kS[r * KP + c] = to_f(k[tok(r, h, a.H) + c]);
         qS[r * KP + c] = a.scale * to_f(q[tok(r, h, a.H) + c]);
         GS[r * KP + c] = fmaxf(to_f(g[tok(r, hv, a.HV) + c]), kGateFloor);
-        X[r * KP + c] = a.dW[(row0 + r) * K + c];
     }
-    for (int i = tid; i < C * C; i += NTH) {
-        const int r = i / C, c = i % C;
-        Ts[r * CP + c] = a.Tm[cc0 + i];
-        Aq[r * CP + c] = a.dAqk[cc0 + i];
-    }
+    cp_async_wait_all();
     if (tid < C) bS[tid] = to_f(beta[((size_t)b * a.T + t0 + tid) * a.HV + hv]);
     __syncthreads();
     if (tid < K) {
@@ -105,24 +121,24 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
     }
     __syncthreads();
 
-    const int r0 = 8 * tr;
+    const int r0 = RPT * tr;
     // ---- dT = mask_strict(beta_m dTv + dW Y^T)  (64 x 64; cols tc, tc+32) ----
     {
-        float acc[8][2];
+        float acc[RPT][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = 0.f;
+        for (int i = 0; i < RPT; ++i) acc[i][0] = acc[i][1] = 0.f;
 #pragma unroll 4
         for (int c = 0; c < K; ++c) {
             const float y0 = Y[tc * KP + c], y1 = Y[(tc + 32) * KP + c];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < RPT; ++i) {
                 const float x = X[(r0 + i) * KP + c];
                 acc[i][0] += x * y0;
                 acc[i][1] += x * y1;
             }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < RPT; ++i)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int ii = r0 + i, m = tc + 32 * u;
@@ -132,9 +148,9 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
     __syncthreads();
     // ---- dKb' = T^T dW  (64 x 128) -> Y ----
     {
-        float acc[8][4];
+        float acc[RPT][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < RPT; ++i)
 #pragma unroll
             for (int u = 0; u < 4; ++u) acc[i][u] = 0.f;
 #pragma unroll 2
@@ -143,7 +159,7 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
 #pragma unroll
             for (int u = 0; u < 4; ++u) xv[u] = X[rr * KP + tc + 32 * u];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < RPT; ++i) {
                 const float tv = Ts[rr * CP + r0 + i];  // T[rr][m], zero for rr < m
 #pragma unroll
                 for (int u = 0; u < 4; ++u) acc[i][u] += tv * xv[u];
@@ -151,20 +167,20 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
         }
         __syncthreads();  // Y (beta khat) fully consumed by dT above
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < RPT; ++i)
 #pragma unroll
             for (int u = 0; u < 4; ++u) Y[(r0 + i) * KP + tc + 32 * u] = acc[i][u];
     }
     // ---- Y2 = dT T^T, then dA = -mask_strict(T^T Y2)  (in D) ----
     {
-        float acc[8][2];
+        float acc[RPT][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = 0.f;
+        for (int i = 0; i < RPT; ++i) acc[i][0] = acc[i][1] = 0.f;
 #pragma unroll 4
         for (int m = 0; m < C; ++m) {
             const float t0v = Ts[tc * CP + m], t1v = Ts[(tc + 32) * CP + m];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < RPT; ++i) {
                 const float dv = D[(r0 + i) * CP + m];
                 acc[i][0] += dv * t0v;
                 acc[i][1] += dv * t1v;
@@ -172,18 +188,18 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < RPT; ++i) {
             D[(r0 + i) * CP + tc] = acc[i][0];
             D[(r0 + i) * CP + tc + 32] = acc[i][1];
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = 0.f;
+        for (int i = 0; i < RPT; ++i) acc[i][0] = acc[i][1] = 0.f;
 #pragma unroll 4
         for (int m = 0; m < C; ++m) {
             const float y0 = D[m * CP + tc], y1 = D[m * CP + tc + 32];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < RPT; ++i) {
                 const float tv = Ts[m * CP + r0 + i];  // T[m][i]
                 acc[i][0] += tv * y0;
                 acc[i][1] += tv * y1;
@@ -191,7 +207,7 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < RPT; ++i)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int ii = r0 + i, j = tc + 32 * u;
@@ -205,18 +221,18 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
     }
     __syncthreads();
 
-    // ---- row side: sA, sQ for rows r0..r0+7 (one 16-row block R) ----
+    // ---- row side: sA, sQ for rows r0..r0+RPT-1 (one 16-row block R) ----
     const int R = r0 >> 4;
-    float sA[8][4], sQ[8][4];
+    float sA[RPT][4], sQ[RPT][4];
     {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < RPT; ++i)
 #pragma unroll
             for (int u = 0; u < 4; ++u) sA[i][u] = sQ[i][u] = 0.f;
         for (int J = 0; J <= R; ++J) {
-            float pa[8][4], pq[8][4];
+            float pa[RPT][4], pq[RPT][4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < RPT; ++i)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) pa[i][u] = pq[i][u] = 0.f;
 #pragma unroll 2
@@ -225,7 +241,7 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
 #pragma unroll
                 for (int u = 0; u < 4; ++u) ke[u] = X[j * KP + tc + 32 * u];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < RPT; ++i) {
                     const float da = D[(r0 + i) * CP + j], dq_ = Aq[(r0 + i) * CP + j];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -238,7 +254,7 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
             for (int u = 0; u < 4; ++u) {
                 const float f = Fb[fidx(R, J) * K + tc + 32 * u];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < RPT; ++i) {
                     sA[i][u] += f * pa[i][u];
                     sQ[i][u] += f * pq[i][u];
                 }
@@ -254,17 +270,17 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
     }
     __syncthreads();
     // QL[t][c] = qs_t E_t: kept in registers per column block below (E recomputed).
-    float cAQ[8][4];
+    float cAQ[RPT][4];
     {
         const int J = R;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < RPT; ++i)
 #pragma unroll
             for (int u = 0; u < 4; ++u) cAQ[i][u] = 0.f;
         for (int RR = J; RR < 4; ++RR) {
-            float pa[8][4];
+            float pa[RPT][4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < RPT; ++i)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) pa[i][u] = 0.f;
 #pragma unroll 2
@@ -277,7 +293,7 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
                     ql[u] = qS[t * KP + c] * __expf(GS[t * KP + c] - GS[16 * RR * KP + c]);
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < RPT; ++i) {
                     const float da = D[t * CP + r0 + i], dq_ = Aq[t * CP + r0 + i];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) pa[i][u] += da * kl[u] + dq_ * ql[u];
@@ -287,7 +303,7 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
             for (int u = 0; u < 4; ++u) {
                 const float f = Fb[fidx(RR, J) * K + tc + 32 * u];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) cAQ[i][u] += f * pa[i][u];
+                for (int i = 0; i < RPT; ++i) cAQ[i][u] += f * pa[i][u];
             }
         }
     }
@@ -295,11 +311,11 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
 
     // ---- assemble per element; dG into X, dbeta partials into GS? (GS still needed) ----
     // dG -> X (KLb no longer needed), dbeta partial -> D rows? use Aq-free space: reuse Ts.
-    float dGv[8][4], dbp[8];
+    float dGv[RPT][4], dbp[RPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dbp[i] = 0.f;
+    for (int i = 0; i < RPT; ++i) dbp[i] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RPT; ++i) {
         const int r = r0 + i;
         const float br = bS[r];
 #pragma unroll
@@ -332,12 +348,12 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < RPT; ++i)
 #pragma unroll
         for (int u = 0; u < 4; ++u) X[(r0 + i) * KP + tc + 32 * u] = dGv[i][u];
     // dbeta: reduce the 32 column groups of each row with warp shuffles
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RPT; ++i) {
         float v = dbp[i];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
