@@ -10,7 +10,7 @@
 //     delta^T = U^T - D12W       (epilogue, fp32 -> bf16 operand in smem)
 //     O^T   = S^T Qh^T + delta^T Aqk^T
 //     S^T   = diag(gam) S^T + delta^T Kb       (gam applied by the epilogue)
-// Per-chunk operands (W, Qh, Kb^T, Aqk, U as bf16; gam fp32) arrive by TMA
+// Per-chunk operands (W, Qh, Kb, Aqk, U as bf16; gam fp32) arrive by TMA
 // into a two-stage ring.  Warp roles: warp 0 issues TMA, warp 1 owns TMEM and
 // issues MMAs (one thread), warps 2-5 are the epilogue (one TMEM lane per
 // value column).  Every mbarrier wait is bounded: on expiry the kernel records
@@ -57,7 +57,7 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, in
 // ---- shared-memory plan of the chain kernel (offsets from a 1024-aligned base) ----
 constexpr uint32_t OFF_W = 0;          // 64 rows x 128 bf16, 2 k-blocks of 8 KB
 constexpr uint32_t OFF_Q = 16384;      // same for Qh
-constexpr uint32_t OFF_KBT = 32768;    // Kb^T: 128 rows (k) x 64 bf16 (c)
+constexpr uint32_t OFF_KBT = 32768;    // Kb: 64 rows (c) x 128 bf16 (k), 2 k-blocks
 constexpr uint32_t OFF_AQK = 49152;    // Aqk: 64 rows x 64 bf16
 constexpr uint32_t OFF_U = 57344;      // U: 64 x 128 bf16, row-major, unswizzled
 constexpr uint32_t OFF_GAM = 73728;    // gam: 128 fp32
@@ -144,7 +144,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 tma_load_2d(st + OFF_W + 8192, &tm_w, &full[s], 64, row);
                 tma_load_2d(st + OFF_Q, &tm_q, &full[s], 0, row);
                 tma_load_2d(st + OFF_Q + 8192, &tm_q, &full[s], 64, row);
-                tma_load_2d(st + OFF_KBT, &tm_kbt, &full[s], 0, crow * kD);
+                tma_load_2d(st + OFF_KBT, &tm_kbt, &full[s], 0, row);
+                tma_load_2d(st + OFF_KBT + 8192, &tm_kbt, &full[s], 64, row);
                 tma_load_2d(st + OFF_AQK, &tm_aqk, &full[s], 0, crow * kC);
                 tma_load_2d(st + OFF_U, &tm_u, &full[s], 0, row);
                 bulk_load(st + OFF_GAM, a.gam + (size_t)crow * kD, 512, &full[s]);
@@ -185,9 +186,10 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 if (!wait_bar(bar_delta, n & 1, 5)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int kk = 0; kk < 4; ++kk)  // Kb tile [64 c][128 k] read MN-major (N = k)
                     mma_bf16(tmem + TM_S, sdesc_sw128(sD + kk * 32),
-                             sdesc_sw128(st + OFF_KBT + kk * 32), idesc128, 1);
+                             sdesc_mn_sw128(st + OFF_KBT + kk * 2048, 8192),
+                             idesc128 | kBMajorMN, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tO, sdesc_sw128(sD + kk * 32), sdesc_sw128(st + OFF_AQK + kk * 32),
@@ -331,7 +333,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 constexpr uint32_t RB_DO = 0;        // dO [64 t][128 v]: two 64-column boxes, 8 KB apart
 constexpr uint32_t RB_Q = 16384;     // Qh [64 t][128 k]
 constexpr uint32_t RB_W = 32768;     // W  [64 r][128 k]
-constexpr uint32_t RB_KBT = 49152;   // Kb^T [128 k][64 r]
+constexpr uint32_t RB_KBT = 49152;   // Kb [64 r][128 k]
 constexpr uint32_t RB_AQK = 65536;   // Aqk [64 t][64 r]
 constexpr uint32_t RB_GAM = 73728;
 constexpr uint32_t TM2_S = 0, TM2_DD = 128, TM2_COLS = 256;
@@ -409,7 +411,8 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 tma_load_2d(st + RB_Q + 8192, &tm_q, &full[s], 64, row);
                 tma_load_2d(st + RB_W, &tm_w, &full[s], 0, row);
                 tma_load_2d(st + RB_W + 8192, &tm_w, &full[s], 64, row);
-                tma_load_2d(st + RB_KBT, &tm_kbt, &full[s], 0, crow * kD);
+                tma_load_2d(st + RB_KBT, &tm_kbt, &full[s], 0, row);
+                tma_load_2d(st + RB_KBT + 8192, &tm_kbt, &full[s], 64, row);
                 tma_load_2d(st + RB_AQK, &tm_aqk, &full[s], 0, crow * kC);
                 bulk_load(st + RB_GAM, a.gam + (size_t)crow * kD, 512, &full[s]);
                 issued = i + 1;
@@ -427,12 +430,12 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 if (!wait_bar(&full[s], (i >> 1) & 1, 13)) break;
                 if (!wait_bar(bar_S, i & 1, 14)) break;
                 tc_fence_after();
-                // ddelta^T = dS^T Kb^T  (B = Kb^T tile read MN-major: N = rows r)
+                // ddelta^T = dS^T Kb^T  (B = Kb tile [64 r][128 k], K-major)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16(tmem + TM2_DD,
                              sdesc_sw128(sS + (kk >> 2) * 16384 + (kk & 3) * 32),
-                             sdesc_mn_sw128(st + RB_KBT + kk * 2048, 8192), id64 | kBMajorMN,
+                             sdesc_sw128(st + RB_KBT + (kk >> 2) * 8192 + (kk & 3) * 32), id64,
                              kk > 0);
                 // ddelta^T += dO^T Aqk
 #pragma unroll
@@ -744,9 +747,10 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
 }
 
 // ===========================================================================
-// Intra-chunk quantities on tensor cores, one CTA (128 threads) per (chunk,
+// Intra-chunk quantities on tensor cores, one CTA (512 threads) per (chunk,
 // head): K3 row L2 steps (1)-(3) plus the operands of the state passes.
-//   (1) G = cumsum(max(g,-5)) per key channel (thread c owns channel c).
+//   (1) G = cumsum(max(g,-5)) per key channel (thread (c, R) owns channel c
+//       of the 16-row block R; block sums are exchanged through smem).
 //   (2) A, Aqk: the pairwise decay exp(G_i - G_j) is factored per 16-row
 //       block R with reference row b = 16R:  exp(G_i - G_b) <= 1 on the left,
 //       exp(G_b - G_j) on the right (<= 1 for earlier blocks, <= e^75 inside
@@ -762,13 +766,15 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
 constexpr uint32_t I_K = 0, I_Q = 16384, I_G = 32768, I_V = 49152;   // TMA tiles, 16 KB each
 constexpr uint32_t I_LEFT = 65536;                                   // 128 rows x 128, 32 KB
 constexpr uint32_t I_R0 = 98304;   // Right_R: 16(R+1) rows x 128: 4, 8, 12, 16 KB
-constexpr uint32_t I_KHAT = I_R0 + 40960;                            // 16 KB
-constexpr uint32_t I_TB = I_KHAT + 16384;                            // T*beta, 64x64 bf16, 8 KB
+constexpr uint32_t I_KHAT = I_G;     // Khat overwrites the consumed g tile
+constexpr uint32_t I_TB = I_R0 + 40960;                              // T*beta, 64x64 bf16, 8 KB
 constexpr uint32_t I_A = I_TB + 8192;                                // fp32 [64][65]
 constexpr uint32_t I_T = I_A + 64 * 65 * 4;                          // fp32 [64][65]
 constexpr uint32_t I_BETA = I_T + 64 * 65 * 4;                       // fp32 [64]
-constexpr uint32_t I_BAR = I_BETA + 256;
+constexpr uint32_t I_GX = I_BETA + 256;                              // fp32 [2][4][128]
+constexpr uint32_t I_BAR = I_GX + 4096;
 constexpr uint32_t INTRA_SMEM = I_BAR + 64 + 1024;
+constexpr int kIntraThreads = 512;
 constexpr uint32_t INTRA_TX = 4 * 16384;
 
 __host__ __device__ constexpr uint32_t right_off(int R) {  // byte offset of Right_R
@@ -782,7 +788,7 @@ struct IntraArgs {
     int T, H, HV, NT;
     float scale;
     const __nv_bfloat16* beta;
-    __nv_bfloat16 *W2, *Q2, *U2, *KbT2, *Aqk2, *T2;
+    __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2;
     float *Tm, *gam;
 };
 
@@ -802,7 +808,7 @@ __device__ __forceinline__ void intra_read_block(uint32_t taddr, float* out /* 6
     for (int j = N; j < 64; ++j) out[j] = 0.f;
 }
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kIntraThreads, 1)
 intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
                 IntraArgs a) {
@@ -816,6 +822,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     float* sA = reinterpret_cast<float*>(smem + I_A);
     float* sT = reinterpret_cast<float*>(smem + I_T);
     float* sBeta = reinterpret_cast<float*>(smem + I_BETA);
+    float* sGtot = reinterpret_cast<float*>(smem + I_GX);   // [4][128] block sums
+    float* sGb = sGtot + 4 * kD;                             // [4][128] G at block starts
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x, bh = blockIdx.y;
@@ -852,8 +860,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     bool ok = wait_bar_warp(bar_tma, 0, 31);
 
-    // ---- (1) cumsum and decay factors: thread c owns key channel c ----
-    const int c = tid;
+    // ---- (1) cumsum: thread (c, R) owns key channel c of row block R ----
+    const int c = tid & (kD - 1), R = tid >> 7;
     const uint32_t kbo = (c >> 6) * 8192, cc = c & 63;
     auto ld = [&](uint32_t tile, int r) {
         return __bfloat162float(
@@ -862,46 +870,61 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     auto st = [&](uint32_t off, float x) {
         *reinterpret_cast<__nv_bfloat16*>(smem + off) = __float2bfloat16_rn(x);
     };
-    float G[kC];
+    float G[16];
     {
         float acc = 0.f;
 #pragma unroll
-        for (int r = 0; r < kC; ++r) {
-            acc += fmaxf(ld(I_G, r), kGateFloor);
-            G[r] = acc;
+        for (int u = 0; u < 16; ++u) {
+            acc += fmaxf(ld(I_G, 16 * R + u), kGateFloor);
+            G[u] = acc;
         }
+        sGtot[R * kD + c] = acc;
     }
-    float eGb[4], eLb[4];  // exp(G_b), exp(G_last - G_b) per block
+    __syncthreads();
+    float off = 0.f, Glast = 0.f;
 #pragma unroll
-    for (int R = 0; R < 4; ++R) {
-        eGb[R] = __expf(G[16 * R]);
-        eLb[R] = __expf(G[kC - 1] - G[16 * R]);
+    for (int p = 0; p < 4; ++p) {
+        const float t = sGtot[p * kD + c];
+        if (p < R) off += t;
+        Glast += t;
     }
-    a.gam[(size_t)crow * kD + c] = __expf(G[kC - 1]);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) G[u] += off;
+    sGb[R * kD + c] = G[0];
+    __syncthreads();
+    float Gb[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
+    if (R == 3) a.gam[(size_t)crow * kD + c] = __expf(Glast);
 
-    // ---- operands: Left, Right_R, Khat (smem); Qh, Kb^T (global) ----
-#pragma unroll 4
-    for (int r = 0; r < kC; ++r) {
-        const int R = r >> 4, u = r & 15;
-        const float Gb = G[16 * R];
-        const float E = __expf(G[r] - Gb);        // <= 1
-        const float Einv = __expf(Gb - G[r]);     // in [1, e^75]
-        const float kv = ld(I_K, r), qv = a.scale * ld(I_Q, r);
-        const uint32_t lrow_k = 32 * R + u, lrow_q = 32 * R + 16 + u;
-        st(I_LEFT + (c >> 6) * 16384 + sw128_offset(lrow_k, cc), kv * E);
-        st(I_LEFT + (c >> 6) * 16384 + sw128_offset(lrow_q, cc), qv * E);
-        // Right_Rr (Rr >= R): k_r exp(G_{b(Rr)} - G_r) = k_r Einv exp(G_{b(Rr)} - G_b)
+    // ---- operands for rows 16R..16R+15: Left, Right_Rr (Rr >= R), Khat; Qh, Kb ----
+    {
+        const float eGb = __expf(Gb[R]);            // exp(G_b)
+        const float eLb = __expf(Glast - Gb[R]);    // exp(G_last - G_b)
+        float F[4];                                 // exp(G_b(Rr) - G_b(R)), Rr >= R
 #pragma unroll
-        for (int Rr = 0; Rr < 4; ++Rr) {
-            if (Rr < R) continue;
-            const float f = Rr == R ? 1.f : __expf(G[16 * Rr] - Gb);
-            const uint32_t rows = 16u * (Rr + 1);
-            st(right_off(Rr) + (c >> 6) * (rows * 128u) + sw128_offset(r, cc), kv * Einv * f);
+        for (int Rr = 0; Rr < 4; ++Rr) F[Rr] = Rr > R ? __expf(Gb[Rr] - Gb[R]) : 1.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int r = 16 * R + u;
+            const float E = __expf(G[u] - Gb[R]);        // <= 1
+            const float Einv = __expf(Gb[R] - G[u]);     // in [1, e^75]
+            const float kv = ld(I_K, r), qv = a.scale * ld(I_Q, r);
+            st(I_LEFT + (c >> 6) * 16384 + sw128_offset(32 * R + u, cc), kv * E);
+            st(I_LEFT + (c >> 6) * 16384 + sw128_offset(32 * R + 16 + u, cc), qv * E);
+            const float ke = kv * Einv;
+#pragma unroll
+            for (int Rr = 0; Rr < 4; ++Rr) {
+                if (Rr < R) continue;
+                const uint32_t rows = 16u * (Rr + 1);
+                st(right_off(Rr) + (c >> 6) * (rows * 128u) + sw128_offset(r, cc), ke * F[Rr]);
+            }
+            const float eG = eGb * E;                    // exp(G_r)
+            a.Q2[((size_t)row0 + r) * kD + c] = __float2bfloat16_rn(qv * eG);
+            a.Kb2[((size_t)row0 + r) * kD + c] = __float2bfloat16_rn(kv * eLb * Einv);
+            // Khat overwrites g's slot of this thread's own element (g already consumed)
+            st(I_KHAT + kbo + sw128_offset(r, cc), kv * eG);
         }
-        const float eG = eGb[R] * E;              // exp(G_r)
-        st(I_KHAT + kbo + sw128_offset(r, cc), kv * eG);
-        a.Q2[((size_t)row0 + r) * kD + c] = __float2bfloat16_rn(qv * eG);
-        a.KbT2[((size_t)crow * kD + c) * kC + r] = __float2bfloat16_rn(kv * eLb[R] * Einv);
     }
     fence_async_smem();
     tc_fence_before();
@@ -912,13 +935,13 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (tid == 0 && ok) {
         const uint32_t left = smem_u32(smem + I_LEFT);
 #pragma unroll
-        for (int R = 0; R < 4; ++R) {
-            const uint32_t rows = 16u * (R + 1);
-            const uint32_t right = smem_u32(smem + right_off(R));
-            const uint32_t id = idesc_bf16_f32(128, 16 * (R + 1));
+        for (int RR = 0; RR < 4; ++RR) {
+            const uint32_t rows = 16u * (RR + 1);
+            const uint32_t right = smem_u32(smem + right_off(RR));
+            const uint32_t id = idesc_bf16_f32(128, 16 * (RR + 1));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + right_col(R),
+                mma_bf16(tmem + right_col(RR),
                          sdesc_sw128(left + (kk >> 2) * 16384 + (kk & 3) * 32),
                          sdesc_sw128(right + (kk >> 2) * (rows * 128u) + (kk & 3) * 32), id,
                          kk > 0);
@@ -927,7 +950,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     ok = ok && wait_bar_warp(bar_a, 0, 32);
     tc_fence_after();
-    if (ok) {
+    if (ok && warp < 4) {
         // warp R reads block R: lanes 0-15 -> A rows, 16-31 -> Aqk rows
         float d[64];
         const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + right_col(warp);
@@ -957,11 +980,11 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
     // ---- (3) T = (I + A)^{-1}: diagonal 16x16 blocks, then block rows ----
     if (tid < 64) {
-        const int R = tid >> 4, jj = tid & 15, j = 16 * R + jj;
+        const int RB = tid >> 4, jj = tid & 15, j = 16 * RB + jj;
         for (int i = 0; i < kC; ++i) sT[i * 65 + j] = 0.f;
         sT[j * 65 + j] = 1.f;
         for (int ii = jj + 1; ii < 16; ++ii) {
-            const int i = 16 * R + ii;
+            const int i = 16 * RB + ii;
             float acc = 0.f;
             for (int m = j; m < i; ++m) acc += sA[i * 65 + m] * sT[m * 65 + j];
             sT[i * 65 + j] = -acc;
@@ -969,56 +992,57 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     __syncthreads();
     for (int dist = 1; dist < 4; ++dist) {
-        // X_RJ = sum_{M=J}^{R-1} A_RM T_MJ for J = R - dist, stored in the (R,J) block of sA
-        // (A's own (R,J) block is no longer needed once consumed below).
+        // X_RJ = sum_{M=J}^{R-1} A_RM T_MJ for J = R - dist, staged in T's (R,J) slot
         const int nblk = 4 - dist;
-        float xv[8];
-        for (int e = 0; e < 8; ++e) {
-            const int idx = tid + e * 128;
+        float xv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int idx = tid + e * kIntraThreads;
             xv[e] = 0.f;
             if (idx < nblk * 256) {
                 const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-                const int J = blk, R = blk + dist, i = 16 * R + ii, j = 16 * J + jj;
+                const int J = blk, RB = blk + dist, i = 16 * RB + ii, j = 16 * J + jj;
                 float acc = 0.f;
-                for (int m = 16 * J; m < 16 * R; ++m) acc += sA[i * 65 + m] * sT[m * 65 + j];
+                for (int m = 16 * J; m < 16 * RB; ++m) acc += sA[i * 65 + m] * sT[m * 65 + j];
                 xv[e] = acc;
             }
         }
         __syncthreads();
-        for (int e = 0; e < 8; ++e) {
-            const int idx = tid + e * 128;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int idx = tid + e * kIntraThreads;
             if (idx < nblk * 256) {
                 const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-                const int R = blk + dist;
-                sT[(16 * R + ii) * 65 + 16 * blk + jj] = xv[e];  // staging: X in T's slot
+                sT[(16 * (blk + dist) + ii) * 65 + 16 * blk + jj] = xv[e];
             }
         }
         __syncthreads();
         // T_RJ = -T_RR X_RJ
-        for (int e = 0; e < 8; ++e) {
-            const int idx = tid + e * 128;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int idx = tid + e * kIntraThreads;
             xv[e] = 0.f;
             if (idx < nblk * 256) {
                 const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-                const int R = blk + dist, i = 16 * R + ii, j = 16 * blk + jj;
+                const int RB = blk + dist, i = 16 * RB + ii, j = 16 * blk + jj;
                 float acc = 0.f;
-                for (int m = 16 * R; m <= i; ++m) acc += sT[i * 65 + m] * sT[m * 65 + j];
+                for (int m = 16 * RB; m <= i; ++m) acc += sT[i * 65 + m] * sT[m * 65 + j];
                 xv[e] = -acc;
             }
         }
         __syncthreads();
-        for (int e = 0; e < 8; ++e) {
-            const int idx = tid + e * 128;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int idx = tid + e * kIntraThreads;
             if (idx < nblk * 256) {
                 const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-                const int R = blk + dist;
-                sT[(16 * R + ii) * 65 + 16 * blk + jj] = xv[e];
+                sT[(16 * (blk + dist) + ii) * 65 + 16 * blk + jj] = xv[e];
             }
         }
         __syncthreads();
     }
     // T (fp32, bf16) to global; T*beta to the B-operand tile
-    for (int idx = tid; idx < kC * kC; idx += 128) {
+    for (int idx = tid; idx < kC * kC; idx += kIntraThreads) {
         const int i = idx >> 6, j = idx & 63;
         const float t = sT[i * 65 + j];
         a.Tm[(size_t)crow * kC * kC + idx] = t;
@@ -1044,20 +1068,20 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     ok = ok && wait_bar_warp(bar_w, 0, 33);
     tc_fence_after();
-    if (ok) {
+    if (ok && warp < 8) {
+        // warps 0-3: W^T (lane = k); warps 4-7: U^T (lane = v)
         float r[32];
-        const uint32_t lo = (uint32_t)(warp * 32) << 16;
-        const int l = warp * 32 + lane;  // k for W^T, v for U^T
+        const int q4 = warp & 3;
+        const uint32_t lo = (uint32_t)(q4 * 32) << 16;
+        const int l = q4 * 32 + lane;
+        const uint32_t col = warp < 4 ? 0u : 64u;
+        __nv_bfloat16* dst = warp < 4 ? a.W2 : a.U2;
 #pragma unroll 1
         for (int cb = 0; cb < 2; ++cb) {
-            tmem_ld32(tmem + lo + cb * 32, r);
+            tmem_ld32(tmem + lo + col + cb * 32, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                a.W2[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
-            tmem_ld32(tmem + lo + 64 + cb * 32, r);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                a.U2[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
+                dst[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
         }
     }
     tc_fence_before();
@@ -1120,7 +1144,7 @@ bool make_map_tok(CUtensorMap* m, const void* ptr, uint64_t BT, uint64_t heads) 
 
 struct TcWs {
     char* simt;  // SIMT workspace (fp32 quantities)
-    __nv_bfloat16 *W2, *Q2, *U2, *KbT2, *Aqk2, *T2;  // chain operands, T
+    __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2;  // chain operands, T
     __nv_bfloat16 *h2, *d2, *dh2, *dd2;              // backward only
 };
 
@@ -1138,7 +1162,7 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     x.W2 = bf(BH * T * kD);
     x.Q2 = bf(BH * T * kD);
     x.U2 = bf(BH * T * kD);
-    x.KbT2 = bf(BH * NT * kD * kC);
+    x.Kb2 = bf(BH * T * kD);
     x.Aqk2 = bf(BH * NT * kC * kC);
     x.T2 = bf(BH * NT * kC * kC);
     if (for_bwd) {
@@ -1174,7 +1198,7 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     a.W2 = w.W2;
     a.Q2 = w.Q2;
     a.U2 = w.U2;
-    a.KbT2 = w.KbT2;
+    a.Kb2 = w.Kb2;
     a.Aqk2 = w.Aqk2;
     a.T2 = w.T2;
     a.Tm = p.Tm;
@@ -1184,7 +1208,7 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
         return KDA_ERR_CUDA;
     {
         TimedLaunch tl("tc_intra", s);
-        intra_tc_kernel<<<dim3(NT, BH), 128, INTRA_SMEM, s>>>(mk, mq, mg, mv, a);
+        intra_tc_kernel<<<dim3(NT, BH), kIntraThreads, INTRA_SMEM, s>>>(mk, mq, mg, mv, a);
     }
     *gam_out = p.gam;
     return launch_status();
@@ -1198,7 +1222,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     const uint64_t rows = (uint64_t)BH * d.T;
     if (!make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
         !make_map(&mq, w.Q2, rows, kD, 64, 64, true) ||
-        !make_map(&mk, w.KbT2, (uint64_t)BH * NT * kD, kC, 64, 128, true) ||
+        !make_map(&mk, w.Kb2, rows, kD, 64, 64, true) ||
         !make_map(&ma, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true) ||
         !make_map(&mu, w.U2, rows, kD, 128, 64, false))
         return KDA_ERR_CUDA;
@@ -1265,7 +1289,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         if (!make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
             !make_map(&mq, w.Q2, rows, kD, 64, 64, true) ||
             !make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
-            !make_map(&mk, w.KbT2, (uint64_t)BH * NT * kD, kC, 64, 128, true) ||
+            !make_map(&mk, w.Kb2, rows, kD, 64, 64, true) ||
             !make_map(&ma, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
             return KDA_ERR_CUDA;
         ChainBwdArgs a;
