@@ -574,7 +574,8 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 constexpr uint32_t G_S0 = 0, G_DS = 32768, G_ODD = 65536, G_DV = 98304, G_T = 131072;
 constexpr uint32_t G_BAR = 139264, G_DBV = G_BAR + 64;
 constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
-constexpr uint32_t GRAD_SMEM = G_DBV + 256 + 1024;
+constexpr uint32_t GRAD_SMEM = G_DBV + 512 + 1024;
+constexpr int kGradThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
 
 struct GradArgs {
     int T, HV, NT;
@@ -583,7 +584,7 @@ struct GradArgs {
     float *dQh, *dWm, *dKb, *dgam, *dAqk, *dTv, *dbv;
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGradThreads, 1)
 grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dh,
               const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dd,
               const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_v,
@@ -595,6 +596,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 2);
     float* dbv_s = reinterpret_cast<float*>(smem + G_DBV);  // [64]
+    float* beta_s = dbv_s + 64;                              // [64]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x, bh = blockIdx.y;
@@ -606,7 +608,11 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         mbar_init(bar_mma, 1);
         fence_mbar_init();
     }
-    if (threadIdx.x < 64) dbv_s[threadIdx.x] = 0.f;
+    if (threadIdx.x < 64) {
+        dbv_s[threadIdx.x] = 0.f;
+        beta_s[threadIdx.x] = __bfloat162float(
+            a.beta[((size_t)b * a.T + (size_t)n * kC + threadIdx.x) * a.HV + hv]);
+    }
     if (warp == 1) {
         tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
@@ -660,13 +666,14 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             wait_bar(bar_mma, 0, 22);
         }
     } else if (warp >= 2) {
-        const int q = warp & 3;
+        // 8 epilogue warps: two per TMEM lane quadrant, splitting the columns.
+        const int q = warp & 3, half = (warp - 2) >> 2;
         const int l = q * 32 + lane;  // TMEM lane: k for D1-D3, row for D4, v for D5
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         float r[32];
         bool ok = wait_bar_warp(bar_tma, 0, 23);
         // dgam[k] = sum_v dS[k][v] S0[k][v] from the bf16 tiles (independent of the MMAs)
-        if (ok) {
+        if (ok && half == 0) {
             float acc = 0.f;
 #pragma unroll 1
             for (int kb = 0; kb < 2; ++kb)
@@ -689,53 +696,50 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         if (ok) {
             tc_fence_after();
             const size_t rb = (size_t)row * kD;
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                tmem_ld32(tmem + lane_off + 0 + cb * 32, r);
+            const int cb = half;  // columns 32*cb .. 32*cb+31 of D1-D3 and D5
+            tmem_ld32(tmem + lane_off + 0 + cb * 32, r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) a.dQh[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
-                tmem_ld32(tmem + lane_off + 64 + cb * 32, r);
+            for (int j = 0; j < 32; ++j) a.dQh[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
+            tmem_ld32(tmem + lane_off + 64 + cb * 32, r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) a.dWm[rb + (size_t)(cb * 32 + j) * kD + l] = -r[j];
-                tmem_ld32(tmem + lane_off + 128 + cb * 32, r);
+            for (int j = 0; j < 32; ++j) a.dWm[rb + (size_t)(cb * 32 + j) * kD + l] = -r[j];
+            tmem_ld32(tmem + lane_off + 128 + cb * 32, r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) a.dKb[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
-            }
-            const size_t cc = (size_t)crow * kC * kC;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                tmem_ld32(tmem + lane_off + 256 + cb * 32, r);
-                if (l < 64 && cb < 2) {
+            for (int j = 0; j < 32; ++j) a.dKb[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
+            // D4: lanes 0-63 need columns 0-63 (dAqk), lanes 64-127 columns 64-127 (dTv)
+            {
+                const size_t cc = (size_t)crow * kC * kC;
+                const int c4 = (q < 2 ? 0 : 2) + half;
+                tmem_ld32(tmem + lane_off + 256 + c4 * 32, r);
+                float* dst;
+                int i;
+                if (q < 2) {
+                    i = l;
+                    dst = a.dAqk + cc + (size_t)i * kC + c4 * 32;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int m = cb * 32 + j;
-                        a.dAqk[cc + (size_t)l * kC + m] = m <= l ? r[j] : 0.f;
-                    }
-                } else if (l >= 64 && cb >= 2) {
-                    const int i = l - 64;
+                    for (int j = 0; j < 32; ++j) r[j] = (c4 * 32 + j) <= i ? r[j] : 0.f;
+                } else {
+                    i = l - 64;
+                    dst = a.dTv + cc + (size_t)i * kC + (c4 - 2) * 32;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int m = cb * 32 + j - 64;
-                        a.dTv[cc + (size_t)i * kC + m] = m < i ? r[j] : 0.f;
-                    }
+                    for (int j = 0; j < 32; ++j) r[j] = ((c4 - 2) * 32 + j) < i ? r[j] : 0.f;
                 }
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(dst + j) = make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
             }
-            // D5: lane = v
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                tmem_ld32(tmem + lane_off + 192 + cb * 32, r);
+            // D5: lane = v, columns m = 32*cb .. 32*cb+31
+            tmem_ld32(tmem + lane_off + 192 + cb * 32, r);
 #pragma unroll 4
-                for (int j = 0; j < 32; ++j) {
-                    const int m = cb * 32 + j;
-                    const float bt =
-                        __bfloat162float(a.beta[((size_t)trow + m) * a.HV + hv]);
-                    a.dv[(((size_t)trow + m) * a.HV + hv) * kD + l] = __float2bfloat16_rn(bt * r[j]);
-                    const uint32_t voff = G_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
-                    float p = r[j] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
+            for (int j = 0; j < 32; ++j) {
+                const int m = cb * 32 + j;
+                const float bt = beta_s[m];
+                a.dv[(((size_t)trow + m) * a.HV + hv) * kD + l] = __float2bfloat16_rn(bt * r[j]);
+                const uint32_t voff = G_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
+                float p = r[j] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                    if (lane == 0) atomicAdd(&dbv_s[m], p);
-                }
+                for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                if (lane == 0) atomicAdd(&dbv_s[m], p);
             }
         }
     }
@@ -1340,7 +1344,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                                  (int)GRAD_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
         TimedLaunch tl("tc_grad_v", s);
-        grad_v_kernel<<<dim3(NT, BH), 192, GRAD_SMEM, s>>>(mh, mdh, mdo, mdd, md, mv, mt, a);
+        grad_v_kernel<<<dim3(NT, BH), kGradThreads, GRAD_SMEM, s>>>(mh, mdh, mdo, mdd, md, mv, mt, a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     SimtWsPtrs p;
