@@ -262,14 +262,15 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
         }
     }
     __syncthreads();
-    // ---- column-side tables X <- KLb = beta k E, kS kept; QL = qs E into GS? no:
-    //      QL is built on the fly from qS and E (one multiply per use).
+    // ---- column-side tables: X <- KLb = beta k E, qS <- QL = qs E ----
+    // (the assembly below recovers qs = QL / E)
     for (int i = tid; i < C * K; i += NTH) {
         const int r = i / K, c = i % K;
-        X[r * KP + c] = bS[r] * kS[r * KP + c] * __expf(GS[r * KP + c] - GS[(r & ~15) * KP + c]);
+        const float E = __expf(GS[r * KP + c] - GS[(r & ~15) * KP + c]);
+        X[r * KP + c] = bS[r] * kS[r * KP + c] * E;
+        qS[r * KP + c] *= E;
     }
     __syncthreads();
-    // QL[t][c] = qs_t E_t: kept in registers per column block below (E recomputed).
     float cAQ[RPT][4];
     {
         const int J = R;
@@ -290,7 +291,7 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
                 for (int u = 0; u < 4; ++u) {
                     const int c = tc + 32 * u;
                     kl[u] = X[t * KP + c];
-                    ql[u] = qS[t * KP + c] * __expf(GS[t * KP + c] - GS[16 * RR * KP + c]);
+                    ql[u] = qS[t * KP + c];
                 }
 #pragma unroll
                 for (int i = 0; i < RPT; ++i) {
@@ -326,7 +327,7 @@ local_bwd_kernel(LocalArgs a, const Tin* __restrict__ q, const Tin* __restrict__
             const float Einv = 1.f / E;
             const float eG = eGb[R * K + c] * E;
             const float eL = eLb[R * K + c] * Einv;
-            const float kr = kS[r * KP + c], qr = qS[r * KP + c];
+            const float kr = kS[r * KP + c], qr = qS[r * KP + c] * Einv;  // QL / E
             const float dKbeta = Y[r * KP + c];
             const float dQh = a.dQh[(row0 + r) * K + c];
             const float dKb = a.dKb[(row0 + r) * K + c];

@@ -71,6 +71,116 @@ constexpr uint32_t CHAIN_SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_W = 128, TM_O0 = 192, TM_O1 = 256, TM_COLS = 512;
 
+// ---- epilogue steps shared by the two chains (thread <-> value column v) ----
+
+__device__ __forceinline__ void store_row_bf16(uint8_t* base, int v, int col0, const float (&r)[32],
+                                               float sign) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 pk;
+        pk.x = pack_bf16(sign * r[8 * j + 0], sign * r[8 * j + 1]);
+        pk.y = pack_bf16(sign * r[8 * j + 2], sign * r[8 * j + 3]);
+        pk.z = pack_bf16(sign * r[8 * j + 4], sign * r[8 * j + 5]);
+        pk.w = pack_bf16(sign * r[8 * j + 6], sign * r[8 * j + 7]);
+        *reinterpret_cast<uint4*>(base + sw128_offset(v, col0 + 8 * j)) = pk;
+    }
+}
+
+// Copies row v of a K-major bf16 tile (ncols = 64 or 128 columns, k-blocks of
+// `kb_stride` bytes) to out[c * ld + v] for every column c, times `sign`.
+__device__ __forceinline__ void tile_row_to_global(const uint8_t* tile, uint32_t kb_stride, int v,
+                                                   int ncols, float sign, __nv_bfloat16* out,
+                                                   size_t ld) {
+    for (int c8 = 0; c8 < ncols / 8; ++c8) {
+        const uint4 x = *reinterpret_cast<const uint4*>(
+            tile + (c8 >> 3) * kb_stride + sw128_offset(v, (c8 & 7) * 8));
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 f = __bfloat1622float2(h2[u]);
+            out[(size_t)(c8 * 8 + 2 * u) * ld] = __float2bfloat16_rn(sign * f.x);
+            out[(size_t)(c8 * 8 + 2 * u + 1) * ld] = __float2bfloat16_rn(sign * f.y);
+        }
+    }
+}
+
+// State step: S^T (lane v, columns k) from TMEM -- or, for the first chunk,
+// from `init` ([K][V] fp32, may be null = zeros) -- to the bf16 K-major
+// operand tile; the TMEM copy is scaled by gam (per column k); arrive on
+// `bar`; then, off the critical path, the bf16 state to out[k][v].
+__device__ __forceinline__ void chain_state_step(uint32_t tS, uint8_t* tile, const float* gam,
+                                                 bool first, const float* init, int v,
+                                                 uint64_t* bar, __nv_bfloat16* out) {
+    float r0[32], r1[32], r2[32], r3[32];
+    if (first) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            r0[i] = init ? init[(size_t)(i)*kD + v] : 0.f;
+            r1[i] = init ? init[(size_t)(32 + i) * kD + v] : 0.f;
+            r2[i] = init ? init[(size_t)(64 + i) * kD + v] : 0.f;
+            r3[i] = init ? init[(size_t)(96 + i) * kD + v] : 0.f;
+        }
+    } else {
+        tmem_ld32_nw(tS + 0, r0);
+        tmem_ld32_nw(tS + 32, r1);
+        tmem_ld32_nw(tS + 64, r2);
+        tmem_ld32_nw(tS + 96, r3);
+        tmem_wait_ld_dep(r0);
+        tmem_wait_ld_dep(r1);
+        tmem_wait_ld_dep(r2);
+        tmem_wait_ld_dep(r3);
+    }
+    store_row_bf16(tile, v, 0, r0, 1.f);
+    store_row_bf16(tile, v, 32, r1, 1.f);
+    store_row_bf16(tile + 16384, v, 0, r2, 1.f);
+    store_row_bf16(tile + 16384, v, 32, r3, 1.f);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        r0[i] *= gam[i];
+        r1[i] *= gam[32 + i];
+        r2[i] *= gam[64 + i];
+        r3[i] *= gam[96 + i];
+    }
+    tmem_st32_nw(tS + 0, r0);
+    tmem_st32_nw(tS + 32, r1);
+    tmem_st32_nw(tS + 64, r2);
+    tmem_st32_nw(tS + 96, r3);
+    tmem_wait_st();
+    fence_async_smem();
+    tc_fence_before();
+    mbar_arrive(bar);
+    if (out) tile_row_to_global(tile, 16384, v, kD, 1.f, out + v, kD);
+}
+
+// Delta step: 64 columns from TMEM (U - D if U is given) to the bf16
+// K-major operand tile (negated if `neg_tile`), arrive on bar1 and bar2,
+// then the true-sign bf16 values to out[c][v] (row stride kD) if given.
+__device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile,
+                                                 const __nv_bfloat16* U, bool neg_tile, int v,
+                                                 uint64_t* bar1, uint64_t* bar2,
+                                                 __nv_bfloat16* out) {
+    float d0[32], d1[32];
+    tmem_ld32_nw(tD, d0);
+    tmem_ld32_nw(tD + 32, d1);
+    tmem_wait_ld_dep(d0);
+    tmem_wait_ld_dep(d1);
+    if (U) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            d0[i] = __bfloat162float(U[i * kD + v]) - d0[i];
+            d1[i] = __bfloat162float(U[(32 + i) * kD + v]) - d1[i];
+        }
+    }
+    const float sg = neg_tile ? -1.f : 1.f;
+    store_row_bf16(tile, v, 0, d0, sg);
+    store_row_bf16(tile, v, 32, d1, sg);
+    fence_async_smem();
+    tc_fence_before();
+    mbar_arrive(bar1);
+    mbar_arrive(bar2);
+    if (out) tile_row_to_global(tile, 0, v, kC, sg, out + v, kD);
+}
+
 struct ChainArgs {
     int B, T, HV, NT;
     const float* gam;   // [BH*NT][128]
@@ -211,42 +321,14 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         float r[32];
         bool ok = true;
 
-        // E1: bring S_n to the bf16 operand tile, scale the TMEM copy by gam_n.
+        // E1: S_n -> bf16 operand tile; TMEM copy scaled by gam_n.
         auto e1 = [&](int n) -> bool {
             const int s = n & 1;
             if (!wait_bar_warp(&full[s], (n >> 1) & 1, 7)) return false;
             const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + OFF_GAM);
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                if (n == 0) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = a.h0 ? a.h0[((size_t)bh * kD + cb * 32 + i) * kD + v] : 0.f;
-                } else {
-                    tmem_ld32(tmem + lane_off + TM_S + cb * 32, r);
-                }
-                if (a.h_out) {
-                    __nv_bfloat16* hp = a.h_out + (((size_t)bh * NT + n) * kD + cb * 32) * kD + v;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) hp[(size_t)i * kD] = __float2bfloat16_rn(r[i]);
-                }
-                uint8_t* base = sS + (cb >> 1) * 16384;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 pk;
-                    pk.x = pack_bf16(r[8 * j + 0], r[8 * j + 1]);
-                    pk.y = pack_bf16(r[8 * j + 2], r[8 * j + 3]);
-                    pk.z = pack_bf16(r[8 * j + 4], r[8 * j + 5]);
-                    pk.w = pack_bf16(r[8 * j + 6], r[8 * j + 7]);
-                    *reinterpret_cast<uint4*>(base + sw128_offset(v, (cb & 1) * 32 + 8 * j)) = pk;
-                }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] *= gam[cb * 32 + i];
-                tmem_st32(tmem + lane_off + TM_S + cb * 32, r);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_S);
+            chain_state_step(tmem + lane_off + TM_S, sS, gam, n == 0,
+                             a.h0 ? a.h0 + (size_t)bh * kD * kD : nullptr, v, bar_S,
+                             a.h_out ? a.h_out + ((size_t)bh * NT + n) * kD * kD : nullptr);
             return true;
         };
 
@@ -258,33 +340,9 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             tc_fence_after();
             const __nv_bfloat16* U =
                 reinterpret_cast<const __nv_bfloat16*>(smem + s * STAGE_BYTES + OFF_U);
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                tmem_ld32(tmem + lane_off + TM_W + cb * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    r[i] = __bfloat162float(U[(cb * 32 + i) * kD + v]) - r[i];
-                if (a.delta_out) {
-                    __nv_bfloat16* dp =
-                        a.delta_out + ((size_t)bh * a.T + (size_t)n * kC + cb * 32) * kD + v;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) dp[(size_t)i * kD] = __float2bfloat16_rn(r[i]);
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 pk;
-                    pk.x = pack_bf16(r[8 * j + 0], r[8 * j + 1]);
-                    pk.y = pack_bf16(r[8 * j + 2], r[8 * j + 3]);
-                    pk.z = pack_bf16(r[8 * j + 4], r[8 * j + 5]);
-                    pk.w = pack_bf16(r[8 * j + 6], r[8 * j + 7]);
-                    *reinterpret_cast<uint4*>(sDelta + sw128_offset(v, cb * 32 + 8 * j)) = pk;
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_delta);
-            mbar_arrive(&empty[s]);
-
+            chain_delta_step(tmem + lane_off + TM_W, sDelta, U, false, v, bar_delta, &empty[s],
+                             a.delta_out ? a.delta_out + ((size_t)bh * a.T + (size_t)n * kC) * kD
+                                         : nullptr);
             if (!wait_bar_warp(bar_D3, n & 1, 9)) { ok = false; break; }
             tc_fence_after();
             if (n + 1 < NT) {
@@ -477,35 +535,9 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             const int n = NT - 1 - i, s = i & 1;
             if (!wait_bar_warp(&full[s], (i >> 1) & 1, 17)) return false;
             const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + RB_GAM);
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                if (i == 0) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        r[j] = a.dht ? a.dht[((size_t)bh * kD + cb * 32 + j) * kD + v] : 0.f;
-                } else {
-                    tmem_ld32(tmem + lane_off + TM2_S + cb * 32, r);
-                }
-                __nv_bfloat16* hp = a.dh_out + (((size_t)bh * NT + n) * kD + cb * 32) * kD + v;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) hp[(size_t)j * kD] = __float2bfloat16_rn(r[j]);
-                uint8_t* base = sS + (cb >> 1) * 16384;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 pk;
-                    pk.x = pack_bf16(r[8 * j + 0], r[8 * j + 1]);
-                    pk.y = pack_bf16(r[8 * j + 2], r[8 * j + 3]);
-                    pk.z = pack_bf16(r[8 * j + 4], r[8 * j + 5]);
-                    pk.w = pack_bf16(r[8 * j + 6], r[8 * j + 7]);
-                    *reinterpret_cast<uint4*>(base + sw128_offset(v, (cb & 1) * 32 + 8 * j)) = pk;
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] *= gam[cb * 32 + j];
-                tmem_st32(tmem + lane_off + TM2_S + cb * 32, r);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_S);
+            chain_state_step(tmem + lane_off + TM2_S, sS, gam, i == 0,
+                             a.dht ? a.dht + (size_t)bh * kD * kD : nullptr, v, bar_S,
+                             a.dh_out + ((size_t)bh * NT + n) * kD * kD);
             return true;
         };
 
@@ -514,27 +546,9 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             const int n = NT - 1 - i, s = i & 1;
             if (!wait_bar_warp(bar_dd, i & 1, 18)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll 1
-            for (int cb = 0; cb < 2; ++cb) {
-                tmem_ld32(tmem + lane_off + TM2_DD + cb * 32, r);
-                __nv_bfloat16* dp =
-                    a.dd_out + ((size_t)bh * a.T + (size_t)n * kC + cb * 32) * kD + v;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) dp[(size_t)j * kD] = __float2bfloat16_rn(r[j]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 pk;
-                    pk.x = pack_bf16(-r[8 * j + 0], -r[8 * j + 1]);
-                    pk.y = pack_bf16(-r[8 * j + 2], -r[8 * j + 3]);
-                    pk.z = pack_bf16(-r[8 * j + 4], -r[8 * j + 5]);
-                    pk.w = pack_bf16(-r[8 * j + 6], -r[8 * j + 7]);
-                    *reinterpret_cast<uint4*>(sDelta + sw128_offset(v, cb * 32 + 8 * j)) = pk;
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_delta);
-            mbar_arrive(&empty[s]);
+            // -ddelta^T to the operand tile; ddelta (true sign) to dd_out
+            chain_delta_step(tmem + lane_off + TM2_DD, sDelta, nullptr, true, v, bar_delta,
+                             &empty[s], a.dd_out + ((size_t)bh * a.T + (size_t)n * kC) * kD);
             if (!wait_bar_warp(bar_D4, i & 1, 19)) { ok = false; break; }
             tc_fence_after();
             if (i + 1 < NT) {
