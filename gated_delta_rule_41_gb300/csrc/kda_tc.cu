@@ -1108,6 +1108,380 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// ===========================================================================
+// Chunk-local backward on tensor cores (K = V = 128, chunk 64), one CTA of 512
+// threads per (chunk, head); thread (c, R) = (tid % 128, tid / 128) owns key
+// channel c of the 16-row block R, which is also TMEM lane c of its warp's
+// quadrant.  With Y = diag(beta) (k o e^G):
+//   P1  dT_raw = dW Y^T                 tcgen05, A = [dW; Y] (K-major, M=128)
+//   P2  dKb'^T = dW^T T                 tcgen05, both operands MN-major
+//   P3  Y2 = dT T^T, P4 dA = -mask(T^T Y2)   fp32 CUDA cores
+//   P5  row side, per block R: sum_j Right_R[j][c] [dA; dAqk][t][j]
+//       (Right_R[j] = k_j e^{G_bR - G_j}, the intra kernel's operand)
+//   P6  column side, per block pair (R, J<=R):
+//       sum_{t in R} (beta k E)_t[c] dA[t][j] + (qs E)_t[c] dAqk[t][j]
+//       combined with exp(G_bR - G_bJ) / E_j in the epilogue.
+// The assembly then forms dk, dq, dG, dbeta and dg (reverse cumsum per
+// channel in registers) exactly as the fp32 kernel does.
+// ===========================================================================
+constexpr uint32_t LB_K = 0, LB_Q = 16384, LB_G = 32768;     // TMA tiles, later fp32 scratch
+constexpr uint32_t LB_DWY = 49152;    // [dW; Y] 128 rows x 128, 2 k-blocks of 16 KB
+constexpr uint32_t LB_T = 81920;      // T bf16 [64 r][64 m]
+constexpr uint32_t LB_DAQ = 90112;    // [dA_R; dAqk_R] rows 32R + 16s + u, 64 columns j
+constexpr uint32_t LB_DAQT = 106496;  // transposed: rows j, columns t'' = 32R + 16s + u
+constexpr uint32_t LB_RIGHT = 122880; // Right_R tiles, 16(R+1) rows each
+constexpr uint32_t LB_LCOL = 163840;  // [beta k E; qs E] rows 32R + 16s + u, 128 c
+constexpr uint32_t LB_SMALL = 196608; // fp32 small arrays
+constexpr uint32_t LB_BAR = LB_SMALL + 8192;
+constexpr uint32_t LOCAL_TC_SMEM = LB_BAR + 64 + 1024;
+constexpr int kLocalTcThreads = 512;
+
+__host__ __device__ constexpr uint32_t right_rel(int R) { return 2048u * (uint32_t)(R * (R + 1)); }
+__host__ __device__ constexpr int pair_idx(int R, int J) { return R * (R + 1) / 2 + J; }
+
+struct LocalTcArgs {
+    int T, H, HV, NT, G;
+    float scale;
+    const float *Tm, *dW, *dQh, *dKb, *dAqk, *dTv, *dgam, *dbv;
+    const __nv_bfloat16 *q, *k, *g, *beta;
+    __nv_bfloat16 *dq, *dk, *dg, *dbeta;
+    float *dqh, *dkh;
+};
+
+__global__ void __launch_bounds__(kLocalTcThreads, 1)
+local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_g, LocalTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + LB_BAR);
+    uint64_t* bar_m1 = bar_tma + 1;
+    uint64_t* bar_m2 = bar_tma + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    float* sBeta = reinterpret_cast<float*>(smem + LB_SMALL);   // [64]
+    float* sDbeta = sBeta + 64;                                 // [64]
+    float* sGtot = sDbeta + 64;                                 // [4][128]
+    float* sGb = sGtot + 4 * kD;                                // [4][128]
+    float* sLast = sGb + 4 * kD;                                // [4][128]
+    float* Tf = reinterpret_cast<float*>(smem + LB_K);          // fp32 [64][65] (after build)
+    float* Df = Tf + 64 * 65;                                   // fp32 [64][65]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = tid & (kD - 1), R = tid >> 7;
+    const int n = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / a.HV, hv = bh % a.HV, h = hv / a.G;
+    const int trow = b * a.T + n * kC;
+    const size_t row0 = (size_t)bh * a.T + (size_t)n * kC;
+    const size_t cc0 = ((size_t)bh * a.NT + n) * kC * kC;
+    const uint32_t lane_off = (uint32_t)((c >> 5) * 32) << 16;
+
+    if (tid == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_m1, 1);
+        mbar_init(bar_m2, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    if (tid < kC) {
+        sBeta[tid] = __bfloat162float(a.beta[((size_t)trow + tid) * a.HV + hv]);
+        sDbeta[tid] = 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_tma, 3 * 16384);
+        tma_load_3d(smem + LB_K, &tm_k, bar_tma, 0, h, trow);
+        tma_load_3d(smem + LB_K + 8192, &tm_k, bar_tma, 64, h, trow);
+        tma_load_3d(smem + LB_Q, &tm_q, bar_tma, 0, h, trow);
+        tma_load_3d(smem + LB_Q + 8192, &tm_q, bar_tma, 64, h, trow);
+        tma_load_3d(smem + LB_G, &tm_g, bar_tma, 0, hv, trow);
+        tma_load_3d(smem + LB_G + 8192, &tm_g, bar_tma, 64, hv, trow);
+    }
+    bool ok = wait_bar_warp(bar_tma, 0, 41);
+
+    const uint32_t kbo = (c >> 6) * 8192, cc = c & 63;
+    auto ldt = [&](uint32_t tile, int r) {
+        return __bfloat162float(
+            *reinterpret_cast<const __nv_bfloat16*>(smem + tile + kbo + sw128_offset(r, cc)));
+    };
+    auto st = [&](uint32_t off, float x) {
+        *reinterpret_cast<__nv_bfloat16*>(smem + off) = __float2bfloat16_rn(x);
+    };
+    // ---- cumsum (thread (c, R): rows 16R..16R+15 of channel c) ----
+    float G[16];
+    {
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            acc += fmaxf(ldt(LB_G, 16 * R + u), kGateFloor);
+            G[u] = acc;
+        }
+        sGtot[R * kD + c] = acc;
+    }
+    __syncthreads();
+    float off = 0.f, Glast = 0.f;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float t = sGtot[p * kD + c];
+        if (p < R) off += t;
+        Glast += t;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) G[u] += off;
+    sGb[R * kD + c] = G[0];
+    __syncthreads();
+    float Gb[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
+    const float eGbR = __expf(Gb[R]), eLbR = __expf(Glast - Gb[R]);
+
+    // ---- build bf16 operands ----
+    {
+        float F[4];
+#pragma unroll
+        for (int Rr = 0; Rr < 4; ++Rr) F[Rr] = Rr > R ? __expf(Gb[Rr] - Gb[R]) : 1.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int r = 16 * R + u;
+            const float E = __expf(G[u] - Gb[R]);
+            const float Einv = __expf(Gb[R] - G[u]);
+            const float kv = ldt(LB_K, r), qv = a.scale * ldt(LB_Q, r), br = sBeta[r];
+            const uint32_t cb16 = (c >> 6) * 16384;
+            // [dW; Y]
+            st(LB_DWY + cb16 + sw128_offset(r, cc), a.dW[(row0 + r) * kD + c]);
+            st(LB_DWY + cb16 + sw128_offset(64 + r, cc), br * kv * eGbR * E);
+            // Right_Rr (Rr >= R)
+            const float ke = kv * Einv;
+#pragma unroll
+            for (int Rr = 0; Rr < 4; ++Rr) {
+                if (Rr < R) continue;
+                const uint32_t rows = 16u * (Rr + 1);
+                st(LB_RIGHT + right_rel(Rr) + (c >> 6) * (rows * 128u) + sw128_offset(r, cc),
+                   ke * F[Rr]);
+            }
+            // Lcol rows 32R + u (beta k E) and 32R + 16 + u (qs E)
+            st(LB_LCOL + cb16 + sw128_offset(32 * R + u, cc), br * kv * E);
+            st(LB_LCOL + cb16 + sw128_offset(32 * R + 16 + u, cc), qv * E);
+            if (c < kC) {  // T and dAqk (64 x 64), column c
+                st(LB_T + sw128_offset(r, c), a.Tm[cc0 + r * kC + c]);
+                const float dq_ = a.dAqk[cc0 + r * kC + c];
+                st(LB_DAQ + sw128_offset(32 * R + 16 + u, c), dq_);
+                const int t2 = 32 * R + 16 + u;
+                st(LB_DAQT + (t2 >> 6) * 8192 + sw128_offset(c, t2 & 63), dq_);
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- P1, P2 ----
+    if (tid == 0 && ok) {
+        const uint32_t dwy = smem_u32(smem + LB_DWY), tt = smem_u32(smem + LB_T);
+        const uint32_t id64 = idesc_bf16_f32(128, 64);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16(tmem + 0, sdesc_sw128(dwy + ko), sdesc_sw128(dwy + 8192 + ko), id64, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + 64, sdesc_mn_sw128(dwy + kk * 2048, 16384),
+                     sdesc_mn_sw128(tt + kk * 2048, 8192), id64 | kAMajorMN | kBMajorMN, kk > 0);
+        mma_commit(bar_m1);
+    }
+    ok = ok && wait_bar_warp(bar_m1, 0, 42);
+    tc_fence_after();
+    // ---- dT (fp32) from D1 rows i < 64; T in fp32 ----
+    if (ok && c < kC) {
+        float r16[16];
+        tmem_ld16(tmem + lane_off + 16 * R, r16);
+        const int i = c;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int m = 16 * R + e;
+            Df[i * 65 + m] = m < i ? sBeta[m] * a.dTv[cc0 + i * kC + m] + r16[e] : 0.f;
+        }
+    }
+    for (int idx = tid; idx < kC * kC; idx += kLocalTcThreads)
+        Tf[(idx >> 6) * 65 + (idx & 63)] = a.Tm[cc0 + idx];
+    __syncthreads();
+    // ---- P3: Y2 = dT T^T ; P4: dA = -mask_strict(T^T Y2)   (fp32, in Df) ----
+    {
+        const int tr = warp, tc = lane, r0 = 4 * tr;
+        float acc[4][2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.f;
+#pragma unroll 4
+        for (int m = 0; m < kC; ++m) {
+            const float t0v = Tf[tc * 65 + m], t1v = Tf[(tc + 32) * 65 + m];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float dv = Df[(r0 + i) * 65 + m];
+                acc[i][0] += dv * t0v;
+                acc[i][1] += dv * t1v;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            Df[(r0 + i) * 65 + tc] = acc[i][0];
+            Df[(r0 + i) * 65 + tc + 32] = acc[i][1];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.f;
+#pragma unroll 4
+        for (int m = 0; m < kC; ++m) {
+            const float y0 = Df[m * 65 + tc], y1 = Df[m * 65 + tc + 32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float tv = Tf[m * 65 + r0 + i];
+                acc[i][0] += tv * y0;
+                acc[i][1] += tv * y1;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int ii = r0 + i, j = tc + 32 * u;
+                Df[ii * 65 + j] = j < ii ? -acc[i][u] : 0.f;
+            }
+    }
+    __syncthreads();
+    // dA (bf16) into the row-side and column-side B tiles
+    for (int idx = tid; idx < kC * kC; idx += kLocalTcThreads) {
+        const int i = idx >> 6, j = idx & 63;
+        const float v = Df[i * 65 + j];
+        const int t2 = 32 * (i >> 4) + (i & 15);
+        st(LB_DAQ + sw128_offset(t2, j), v);
+        st(LB_DAQT + (t2 >> 6) * 8192 + sw128_offset(j, t2 & 63), v);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- P5 (row side), P6 (column side) ----
+    if (tid == 0 && ok) {
+        const uint32_t daq = smem_u32(smem + LB_DAQ), daqt = smem_u32(smem + LB_DAQT);
+        const uint32_t right = smem_u32(smem + LB_RIGHT), lcol = smem_u32(smem + LB_LCOL);
+#pragma unroll
+        for (int RR = 0; RR < 4; ++RR) {
+            const uint32_t id = idesc_bf16_f32(128, 32) | kAMajorMN;
+            for (int kk = 0; kk <= RR; ++kk)
+                mma_bf16(tmem + 128 + 32 * RR,
+                         sdesc_mn_sw128(right + right_rel(RR) + kk * 2048, 2048u * (RR + 1)),
+                         sdesc_sw128(daq + 4096u * RR + kk * 32), id, kk > 0);
+        }
+#pragma unroll
+        for (int RR = 0; RR < 4; ++RR)
+            for (int J = 0; J <= RR; ++J) {
+                const uint32_t id = idesc_bf16_f32(128, 16) | kAMajorMN;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+                    mma_bf16(tmem + 256 + 16 * pair_idx(RR, J),
+                             sdesc_mn_sw128(lcol + 4096u * RR + kk * 2048, 16384),
+                             sdesc_sw128(daqt + (RR >> 1) * 8192 + 2048u * J + (RR & 1) * 64 +
+                                         kk * 32),
+                             id, kk > 0);
+            }
+        mma_commit(bar_m2);
+    }
+    ok = ok && wait_bar_warp(bar_m2, 0, 43);
+    tc_fence_after();
+
+    // ---- assembly: thread (c, R) for rows t = 16R + u ----
+    float dG[16];
+    float lastp = 0.f;
+    if (ok) {
+        float dkb[16], cAQ[16], sAQ[32];
+        tmem_ld16(tmem + lane_off + 64 + 16 * R, dkb);          // d(beta khat) for t in R
+        tmem_ld32(tmem + lane_off + 128 + 32 * R, sAQ);         // sA raw | sQ raw
+#pragma unroll
+        for (int u = 0; u < 16; ++u) cAQ[u] = 0.f;
+        for (int Rp = R; Rp < 4; ++Rp) {
+            float d6[16];
+            tmem_ld16(tmem + lane_off + 256 + 16 * pair_idx(Rp, R), d6);
+            const float f = Rp > R ? __expf(Gb[Rp] - Gb[R]) : 1.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) cAQ[u] += f * d6[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int t = 16 * R + u;
+            const float E = __expf(G[u] - Gb[R]);
+            const float Einv = __expf(Gb[R] - G[u]);
+            const float eG = eGbR * E, eL = eLbR * Einv;
+            const size_t iqk = (((size_t)trow + t) * a.H + h) * kD + c;
+            const float kr = __bfloat162float(a.k[iqk]);
+            const float qr = a.scale * __bfloat162float(a.q[iqk]);
+            const float br = sBeta[t];
+            const float dKbeta = dkb[u];
+            const float dQh = a.dQh[(row0 + t) * kD + c];
+            const float dKb = a.dKb[(row0 + t) * kD + c];
+            const float sa = sAQ[u] * E, sq = sAQ[16 + u] * E, caq = cAQ[u] * Einv;
+            const float dkv = br * dKbeta * eG + dKb * eL + br * sa + caq;
+            const float dqs = dQh * eG + sq;
+            dG[u] = dKbeta * br * kr * eG + dQh * qr * eG - dKb * kr * eL + br * kr * sa +
+                    qr * sq - kr * caq;
+            lastp += dKb * kr * eL;
+            float dbp = dKbeta * kr * eG + kr * sa;
+            const size_t io = (((size_t)trow + t) * a.HV + hv) * kD + c;
+            if (a.G == 1) {
+                a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
+                a.dk[io] = __float2bfloat16_rn(dkv);
+            } else {
+                a.dqh[io] = a.scale * dqs;
+                a.dkh[io] = dkv;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dbp += __shfl_xor_sync(0xffffffffu, dbp, o);
+            if (lane == 0) atomicAdd(&sDbeta[t], dbp);
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) dG[u] = 0.f;
+    }
+    // block sums of dG and the last-row partials, for the reverse cumsum
+    float bsum = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) bsum += dG[u];
+    sGtot[R * kD + c] = bsum;
+    sLast[R * kD + c] = lastp;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    {
+        // dG_last += sum_r dKb_r Kb_r + dgam gam; it enters every row's suffix sum
+        float extra = a.dgam[((size_t)bh * a.NT + n) * kD + c] * __expf(Glast);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) extra += sLast[p * kD + c];
+        float run = extra;
+        for (int p = R + 1; p < 4; ++p) run += sGtot[p * kD + c];
+#pragma unroll
+        for (int u = 15; u >= 0; --u) {
+            run += dG[u];
+            const int t = 16 * R + u;
+            const size_t ig = (((size_t)trow + t) * a.HV + hv) * kD + c;
+            a.dg[ig] = __float2bfloat16_rn(__bfloat162float(a.g[ig]) >= kGateFloor ? run : 0.f);
+        }
+    }
+    if (tid < kC)
+        a.dbeta[((size_t)trow + tid) * a.HV + hv] =
+            __float2bfloat16_rn(sDbeta[tid] + a.dbv[row0 + tid]);
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
 // ---- host: tensor maps ----
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1229,6 +1603,50 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
         intra_tc_kernel<<<dim3(NT, BH), kIntraThreads, INTRA_SMEM, s>>>(mk, mq, mg, mv, a);
     }
     *gam_out = p.gam;
+    return launch_status();
+}
+
+kda_status run_local_bwd_tc(const kda_dims& d, const SimtWsPtrs& p, const void* q,
+                            const void* k, const void* g, const void* beta, void* dq, void* dk,
+                            void* dg, void* dbeta, cudaStream_t s) {
+    const uint64_t BT = (uint64_t)d.B * d.T;
+    CUtensorMap mk, mq, mg;
+    if (!make_map_tok(&mk, k, BT, d.H) || !make_map_tok(&mq, q, BT, d.H) ||
+        !make_map_tok(&mg, g, BT, d.HV))
+        return KDA_ERR_CUDA;
+    LocalTcArgs a;
+    a.T = d.T;
+    a.H = d.H;
+    a.HV = d.HV;
+    a.NT = d.T / kC;
+    a.G = d.HV / d.H;
+    a.scale = d.scale;
+    a.Tm = p.Tm;
+    a.dW = p.dWm;
+    a.dQh = p.dQh;
+    a.dKb = p.dKb;
+    a.dAqk = p.dAqk;
+    a.dTv = p.dTv;
+    a.dgam = p.dgam;
+    a.dbv = p.dbv;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k = static_cast<const __nv_bfloat16*>(k);
+    a.g = static_cast<const __nv_bfloat16*>(g);
+    a.beta = static_cast<const __nv_bfloat16*>(beta);
+    a.dq = static_cast<__nv_bfloat16*>(dq);
+    a.dk = static_cast<__nv_bfloat16*>(dk);
+    a.dg = static_cast<__nv_bfloat16*>(dg);
+    a.dbeta = static_cast<__nv_bfloat16*>(dbeta);
+    a.dqh = p.dqh;
+    a.dkh = p.dkh;
+    if (cudaFuncSetAttribute(local_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)LOCAL_TC_SMEM) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    {
+        TimedLaunch tl("tc_local_bwd", s);
+        local_bwd_tc_kernel<<<dim3(d.T / kC, d.B * d.HV), kLocalTcThreads, LOCAL_TC_SMEM, s>>>(
+            mk, mq, mg, a);
+    }
     return launch_status();
 }
 
@@ -1363,7 +1781,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     if ((st = launch_status()) != KDA_OK) return st;
     SimtWsPtrs p;
     simt_ws_ptrs(d, 1, w.simt, &p);
-    if ((st = local_bwd_launch(d, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
+    if ((st = run_local_bwd_tc(d, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
     if (d.HV == d.H) return KDA_OK;
     return group_sum_launch(d, p.dqh, p.dkh, dq, dk, s);
 }
