@@ -270,40 +270,43 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         if (lane == 0) {
             const uint32_t idesc64 = idesc_bf16_f32(128, 64);
             const uint32_t idesc128 = idesc_bf16_f32(128, 128);
-            const uint32_t sS = smem_u32(smem + OFF_S), sD = smem_u32(smem + OFF_DELTA);
+            // descriptors are built once; K offsets are added to the start field
+            const uint64_t dS = sdesc_sw128(smem_u32(smem + OFF_S));
+            const uint64_t dD = sdesc_sw128(smem_u32(smem + OFF_DELTA));
+            const uint32_t st0 = smem_u32(smem);
+            const uint64_t dW0 = sdesc_sw128(st0 + OFF_W), dQ0 = sdesc_sw128(st0 + OFF_Q);
+            const uint64_t dKb0 = sdesc_mn_sw128(st0 + OFF_KBT, 8192);
+            const uint64_t dAq0 = sdesc_sw128(st0 + OFF_AQK);
             for (int n = 0; n < NT; ++n) {
                 const int s = n & 1;
-                const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+                const uint64_t so = s ? (STAGE_BYTES >> 4) : 0;  // stage offset in 16-byte units
+
                 if (!wait_bar(&full[s], (n >> 1) & 1, 3)) break;
                 if (!wait_bar(bar_S, n & 1, 4)) break;
                 tc_fence_after();
                 const uint32_t tO = tmem + ((n & 1) ? TM_O1 : TM_O0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint32_t kb = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    mma_bf16(tmem + TM_W, sdesc_sw128(sS + ka), sdesc_sw128(st + OFF_W + kb),
-                             idesc64, kk > 0);
+                    const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    mma_bf16(tmem + TM_W, dS + ka, dW0 + so + kb, idesc64, kk > 0);
                 }
                 mma_commit(bar_D12);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t ka = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint32_t kb = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    mma_bf16(tO, sdesc_sw128(sS + ka), sdesc_sw128(st + OFF_Q + kb), idesc64,
-                             kk > 0);
+                    const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    mma_bf16(tO, dS + ka, dQ0 + so + kb, idesc64, kk > 0);
                 }
                 if (!wait_bar(bar_delta, n & 1, 5)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // Kb tile [64 c][128 k] read MN-major (N = k)
-                    mma_bf16(tmem + TM_S, sdesc_sw128(sD + kk * 32),
-                             sdesc_mn_sw128(st + OFF_KBT + kk * 2048, 8192),
+                    mma_bf16(tmem + TM_S, dD + ((kk * 32) >> 4), dKb0 + so + ((kk * 2048) >> 4),
                              idesc128 | kBMajorMN, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tO, sdesc_sw128(sD + kk * 32), sdesc_sw128(st + OFF_AQK + kk * 32),
-                             idesc64, 1);
+                    mma_bf16(tO, dD + ((kk * 32) >> 4), dAq0 + so + ((kk * 32) >> 4), idesc64, 1);
                 mma_commit(bar_D3);
                 mma_commit(&empty[s]);
             }
@@ -481,40 +484,43 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
-            const uint32_t sS = smem_u32(smem + OFF_S), sD = smem_u32(smem + OFF_DELTA);
+            const uint64_t dS = sdesc_sw128(smem_u32(smem + OFF_S));
+            const uint64_t dD = sdesc_sw128(smem_u32(smem + OFF_DELTA));
+            const uint32_t st0 = smem_u32(smem);
+            const uint64_t dKb0 = sdesc_sw128(st0 + RB_KBT);
+            const uint64_t dDO0 = sdesc_mn_sw128(st0 + RB_DO, 8192);
+            const uint64_t dAq0 = sdesc_mn_sw128(st0 + RB_AQK, 8192);
+            const uint64_t dQ0 = sdesc_mn_sw128(st0 + RB_Q, 8192);
+            const uint64_t dW0 = sdesc_mn_sw128(st0 + RB_W, 8192);
             for (int i = 0; i < NT; ++i) {
                 const int s = i & 1;
-                const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+                const uint64_t so = s ? (STAGE_BYTES >> 4) : 0;  // stage offset in 16-byte units
                 if (!wait_bar(&full[s], (i >> 1) & 1, 13)) break;
                 if (!wait_bar(bar_S, i & 1, 14)) break;
                 tc_fence_after();
                 // ddelta^T = dS^T Kb^T  (B = Kb tile [64 r][128 k], K-major)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + TM2_DD,
-                             sdesc_sw128(sS + (kk >> 2) * 16384 + (kk & 3) * 32),
-                             sdesc_sw128(st + RB_KBT + (kk >> 2) * 8192 + (kk & 3) * 32), id64,
-                             kk > 0);
+                    mma_bf16(tmem + TM2_DD, dS + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                             dKb0 + so + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), id64, kk > 0);
                 // ddelta^T += dO^T Aqk
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM2_DD, sdesc_mn_sw128(st + RB_DO + kk * 2048, 8192),
-                             sdesc_mn_sw128(st + RB_AQK + kk * 2048, 8192),
-                             id64 | kAMajorMN | kBMajorMN, 1);
+                    mma_bf16(tmem + TM2_DD, dDO0 + so + ((kk * 2048) >> 4),
+                             dAq0 + so + ((kk * 2048) >> 4), id64 | kAMajorMN | kBMajorMN, 1);
                 mma_commit(bar_dd);
                 // dS^T += dO^T Qh
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM2_S, sdesc_mn_sw128(st + RB_DO + kk * 2048, 8192),
-                             sdesc_mn_sw128(st + RB_Q + kk * 2048, 8192),
-                             id128 | kAMajorMN | kBMajorMN, 1);
+                    mma_bf16(tmem + TM2_S, dDO0 + so + ((kk * 2048) >> 4),
+                             dQ0 + so + ((kk * 2048) >> 4), id128 | kAMajorMN | kBMajorMN, 1);
                 if (!wait_bar(bar_delta, i & 1, 15)) break;
                 tc_fence_after();
                 // dS^T += (-ddelta^T) W
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + TM2_S, sdesc_sw128(sD + kk * 32),
-                             sdesc_mn_sw128(st + RB_W + kk * 2048, 8192), id128 | kBMajorMN, 1);
+                    mma_bf16(tmem + TM2_S, dD + ((kk * 32) >> 4), dW0 + so + ((kk * 2048) >> 4),
+                             id128 | kBMajorMN, 1);
                 mma_commit(bar_D4);
                 mma_commit(&empty[s]);
             }
@@ -1176,6 +1182,25 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const size_t cc0 = ((size_t)bh * a.NT + n) * kC * kC;
     const uint32_t lane_off = (uint32_t)((c >> 5) * 32) << 16;
 
+    // fp32 inputs of the build, staged asynchronously (16-byte copies) in
+    // regions the build only writes in its second pass: dW in the Lcol area,
+    // T and dAqk in the Right area.
+    float* stW = reinterpret_cast<float*>(smem + LB_LCOL);          // [64][128]
+    float* stT = reinterpret_cast<float*>(smem + LB_RIGHT);         // [64][64]
+    float* stA = stT + kC * kC;                                     // [64][64]
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int ch = tid + e * kLocalTcThreads;  // 16-byte chunk of dW
+        cp_async16(stW + ch * 4, a.dW + row0 * kD + ch * 4);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int ch = tid + e * kLocalTcThreads;
+        cp_async16(stT + ch * 4, a.Tm + cc0 + ch * 4);
+        cp_async16(stA + ch * 4, a.dAqk + cc0 + ch * 4);
+    }
+    cp_async_commit();
+
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_m1, 1);
@@ -1241,7 +1266,23 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
     const float eGbR = __expf(Gb[R]), eLbR = __expf(Glast - Gb[R]);
 
-    // ---- build bf16 operands ----
+    // ---- build bf16 operands: pass 1 from the staged fp32 inputs ----
+    cp_async_wait_all16();
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int r = 16 * R + u;
+        st(LB_DWY + (c >> 6) * 16384 + sw128_offset(r, cc), stW[r * kD + c]);
+        if (c < kC) {
+            st(LB_T + sw128_offset(r, c), stT[r * kC + c]);
+            const float dq_ = stA[r * kC + c];
+            st(LB_DAQ + sw128_offset(32 * R + 16 + u, c), dq_);
+            const int t2 = 32 * R + 16 + u;
+            st(LB_DAQT + (t2 >> 6) * 8192 + sw128_offset(c, t2 & 63), dq_);
+        }
+    }
+    __syncthreads();
+    // ---- pass 2: Y, Right_R, Lcol (overwrites the staging areas) ----
     {
         float F[4];
 #pragma unroll
@@ -1253,8 +1294,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             const float Einv = __expf(Gb[R] - G[u]);
             const float kv = ldt(LB_K, r), qv = a.scale * ldt(LB_Q, r), br = sBeta[r];
             const uint32_t cb16 = (c >> 6) * 16384;
-            // [dW; Y]
-            st(LB_DWY + cb16 + sw128_offset(r, cc), a.dW[(row0 + r) * kD + c]);
+            // Y rows of [dW; Y]
             st(LB_DWY + cb16 + sw128_offset(64 + r, cc), br * kv * eGbR * E);
             // Right_Rr (Rr >= R)
             const float ke = kv * Einv;
@@ -1268,13 +1308,6 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             // Lcol rows 32R + u (beta k E) and 32R + 16 + u (qs E)
             st(LB_LCOL + cb16 + sw128_offset(32 * R + u, cc), br * kv * E);
             st(LB_LCOL + cb16 + sw128_offset(32 * R + 16 + u, cc), qv * E);
-            if (c < kC) {  // T and dAqk (64 x 64), column c
-                st(LB_T + sw128_offset(r, c), a.Tm[cc0 + r * kC + c]);
-                const float dq_ = a.dAqk[cc0 + r * kC + c];
-                st(LB_DAQ + sw128_offset(32 * R + 16 + u, c), dq_);
-                const int t2 = 32 * R + 16 + u;
-                st(LB_DAQT + (t2 >> 6) * 8192 + sw128_offset(c, t2 & 63), dq_);
-            }
         }
     }
     fence_async_smem();
@@ -1301,17 +1334,28 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     tc_fence_after();
     // ---- dT (fp32) from D1 rows i < 64; T in fp32 ----
     if (ok && c < kC) {
-        float r16[16];
-        tmem_ld16(tmem + lane_off + 16 * R, r16);
+        float r16[16], tv[16];
         const int i = c;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) tv[e] = a.dTv[cc0 + i * kC + 16 * R + e];
+        tmem_ld16(tmem + lane_off + 16 * R, r16);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int m = 16 * R + e;
-            Df[i * 65 + m] = m < i ? sBeta[m] * a.dTv[cc0 + i * kC + m] + r16[e] : 0.f;
+            Df[i * 65 + m] = m < i ? sBeta[m] * tv[e] + r16[e] : 0.f;
         }
     }
-    for (int idx = tid; idx < kC * kC; idx += kLocalTcThreads)
-        Tf[(idx >> 6) * 65 + (idx & 63)] = a.Tm[cc0 + idx];
+    {
+        float tv[kC * kC / kLocalTcThreads];
+#pragma unroll
+        for (int e = 0; e < kC * kC / kLocalTcThreads; ++e)
+            tv[e] = a.Tm[cc0 + tid + e * kLocalTcThreads];
+#pragma unroll
+        for (int e = 0; e < kC * kC / kLocalTcThreads; ++e) {
+            const int idx = tid + e * kLocalTcThreads;
+            Tf[(idx >> 6) * 65 + (idx & 63)] = tv[e];
+        }
+    }
     __syncthreads();
     // ---- P3: Y2 = dT T^T ; P4: dA = -mask_strict(T^T Y2)   (fp32, in Df) ----
     {
@@ -1397,6 +1441,14 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
         mma_commit(bar_m2);
     }
+    // prefetch the assembly's per-element inputs while the MMAs run
+    float pQh[16], pKb[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int t = 16 * R + u;
+        pQh[u] = a.dQh[(row0 + t) * kD + c];
+        pKb[u] = a.dKb[(row0 + t) * kD + c];
+    }
     ok = ok && wait_bar_warp(bar_m2, 0, 43);
     tc_fence_after();
 
@@ -1427,8 +1479,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             const float qr = a.scale * __bfloat162float(a.q[iqk]);
             const float br = sBeta[t];
             const float dKbeta = dkb[u];
-            const float dQh = a.dQh[(row0 + t) * kD + c];
-            const float dKb = a.dKb[(row0 + t) * kD + c];
+            const float dQh = pQh[u];
+            const float dKb = pKb[u];
             const float sa = sAQ[u] * E, sq = sAQ[16 + u] * E, caq = cAQ[u] * Einv;
             const float dkv = br * dKbeta * eG + dKb * eL + br * sa + caq;
             const float dqs = dQh * eG + sq;
