@@ -792,9 +792,10 @@ constexpr uint32_t I_LEFT = 65536;                                   // 128 rows
 constexpr uint32_t I_R0 = 98304;   // Right_R: 16(R+1) rows x 128: 4, 8, 12, 16 KB
 constexpr uint32_t I_KHAT = I_G;     // Khat overwrites the consumed g tile
 constexpr uint32_t I_TB = I_R0 + 40960;                              // T*beta, 64x64 bf16, 8 KB
-constexpr uint32_t I_A = I_TB + 8192;                                // fp32 [64][65]
-constexpr uint32_t I_T = I_A + 64 * 65 * 4;                          // fp32 [64][65]
-constexpr uint32_t I_BETA = I_T + 64 * 65 * 4;                       // fp32 [64]
+constexpr int kAS = 68;              // row stride (floats) of A and T: rows stay 16-byte aligned
+constexpr uint32_t I_A = I_TB + 8192;                                // fp32 [64][kAS]
+constexpr uint32_t I_T = I_A + 64 * kAS * 4;                         // fp32 [64][kAS]
+constexpr uint32_t I_BETA = I_T + 64 * kAS * 4;                      // fp32 [64]
 constexpr uint32_t I_GX = I_BETA + 256;                              // fp32 [2][4][128]
 constexpr uint32_t I_BAR = I_GX + 4096;
 constexpr uint32_t INTRA_SMEM = I_BAR + 64 + 1024;
@@ -986,7 +987,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         if (lane < 16) {
             const float bi = sBeta[i];
 #pragma unroll
-            for (int j = 0; j < kC; ++j) sA[i * 65 + j] = j < i ? bi * d[j] : 0.f;
+            for (int j = 0; j < kC; ++j) sA[i * kAS + j] = j < i ? bi * d[j] : 0.f;
         } else {
             __nv_bfloat16* ap = a.Aqk2 + ((size_t)crow * kC + i) * kC;
 #pragma unroll
@@ -1002,73 +1003,79 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     __syncthreads();
 
-    // ---- (3) T = (I + A)^{-1}: diagonal 16x16 blocks, then block rows ----
+    // ---- (3) T = (I + A)^{-1}, A strictly lower: two 32 x 32 diagonal blocks by
+    // forward substitution (thread (RB, jj) keeps column jj of block RB in
+    // registers), then T_10 = -T_11 (A_10 T_00).  A's entries on and above the
+    // diagonal are stored zeros, so the dot products run over whole float4s. ----
     if (tid < 64) {
-        const int RB = tid >> 4, jj = tid & 15, j = 16 * RB + jj;
-        for (int i = 0; i < kC; ++i) sT[i * 65 + j] = 0.f;
-        sT[j * 65 + j] = 1.f;
-        for (int ii = jj + 1; ii < 16; ++ii) {
-            const int i = 16 * RB + ii;
-            float acc = 0.f;
-            for (int m = j; m < i; ++m) acc += sA[i * 65 + m] * sT[m * 65 + j];
-            sT[i * 65 + j] = -acc;
+        const int RB = tid >> 5, jj = tid & 31, o = 32 * RB;
+        float t[32];
+#pragma unroll
+        for (int m = 0; m < 32; ++m) t[m] = m == jj ? 1.f : 0.f;
+#pragma unroll
+        for (int ii = 1; ii < 32; ++ii) {
+            const float* arow = sA + (o + ii) * kAS + o;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < ii; m += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(arow + m);
+                acc[0] += a4.x * t[m];
+                acc[1] += a4.y * t[m + 1];
+                acc[2] += a4.z * t[m + 2];
+                acc[3] += a4.w * t[m + 3];
+            }
+            if (ii > jj) t[ii] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
+        }
+#pragma unroll
+        for (int m = 0; m < 32; ++m) sT[(o + m) * kAS + o + jj] = t[m];
+        if (RB == 1) {
+#pragma unroll
+            for (int m = 0; m < 32; ++m) sT[m * kAS + 32 + jj] = 0.f;   // T_01 = 0
         }
     }
     __syncthreads();
-    for (int dist = 1; dist < 4; ++dist) {
-        // X_RJ = sum_{M=J}^{R-1} A_RM T_MJ for J = R - dist, staged in T's (R,J) slot
-        const int nblk = 4 - dist;
-        float xv[2];
+    // X = A_10 T_00 into A's unused upper block (rows 0..31, columns 32..63)
+    {
+        const int jj = lane, i0 = 2 * warp;
+        float x0 = 0.f, x1 = 0.f;
+        const float* a0 = sA + (32 + i0) * kAS;
+        const float* a1 = a0 + kAS;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int idx = tid + e * kIntraThreads;
-            xv[e] = 0.f;
-            if (idx < nblk * 256) {
-                const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-                const int J = blk, RB = blk + dist, i = 16 * RB + ii, j = 16 * J + jj;
-                float acc = 0.f;
-                for (int m = 16 * J; m < 16 * RB; ++m) acc += sA[i * 65 + m] * sT[m * 65 + j];
-                xv[e] = acc;
-            }
+        for (int m = 0; m < 32; m += 4) {
+            const float4 p = *reinterpret_cast<const float4*>(a0 + m);
+            const float4 q = *reinterpret_cast<const float4*>(a1 + m);
+            const float t0 = sT[m * kAS + jj], t1 = sT[(m + 1) * kAS + jj];
+            const float t2 = sT[(m + 2) * kAS + jj], t3 = sT[(m + 3) * kAS + jj];
+            x0 += p.x * t0 + p.y * t1 + p.z * t2 + p.w * t3;
+            x1 += q.x * t0 + q.y * t1 + q.z * t2 + q.w * t3;
         }
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int idx = tid + e * kIntraThreads;
-            if (idx < nblk * 256) {
-                const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-                sT[(16 * (blk + dist) + ii) * 65 + 16 * blk + jj] = xv[e];
-            }
-        }
-        __syncthreads();
-        // T_RJ = -T_RR X_RJ
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int idx = tid + e * kIntraThreads;
-            xv[e] = 0.f;
-            if (idx < nblk * 256) {
-                const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-                const int RB = blk + dist, i = 16 * RB + ii, j = 16 * blk + jj;
-                float acc = 0.f;
-                for (int m = 16 * RB; m <= i; ++m) acc += sT[i * 65 + m] * sT[m * 65 + j];
-                xv[e] = -acc;
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int idx = tid + e * kIntraThreads;
-            if (idx < nblk * 256) {
-                const int blk = idx >> 8, ii = (idx >> 4) & 15, jj = idx & 15;
-                sT[(16 * (blk + dist) + ii) * 65 + 16 * blk + jj] = xv[e];
-            }
-        }
-        __syncthreads();
+        sA[i0 * kAS + 32 + jj] = x0;
+        sA[(i0 + 1) * kAS + 32 + jj] = x1;
     }
+    __syncthreads();
+    // T_10 = -T_11 X
+    {
+        const int jj = lane, i0 = 2 * warp;
+        float y0 = 0.f, y1 = 0.f;
+        const float* r0 = sT + (32 + i0) * kAS + 32;
+        const float* r1 = r0 + kAS;
+#pragma unroll
+        for (int m = 0; m < 32; m += 4) {
+            const float4 p = *reinterpret_cast<const float4*>(r0 + m);
+            const float4 q = *reinterpret_cast<const float4*>(r1 + m);
+            const float x0 = sA[m * kAS + 32 + jj], x1 = sA[(m + 1) * kAS + 32 + jj];
+            const float x2 = sA[(m + 2) * kAS + 32 + jj], x3 = sA[(m + 3) * kAS + 32 + jj];
+            y0 += p.x * x0 + p.y * x1 + p.z * x2 + p.w * x3;
+            y1 += q.x * x0 + q.y * x1 + q.z * x2 + q.w * x3;
+        }
+        sT[(32 + i0) * kAS + jj] = -y0;
+        sT[(32 + i0 + 1) * kAS + jj] = -y1;
+    }
+    __syncthreads();
     // T (fp32, bf16) to global; T*beta to the B-operand tile
     for (int idx = tid; idx < kC * kC; idx += kIntraThreads) {
         const int i = idx >> 6, j = idx & 63;
-        const float t = sT[i * 65 + j];
+        const float t = sT[i * kAS + j];
         a.Tm[(size_t)crow * kC * kC + idx] = t;
         a.T2[(size_t)crow * kC * kC + idx] = __float2bfloat16_rn(t);
         st(I_TB + sw128_offset(i, j), t * sBeta[j]);
@@ -1121,7 +1128,9 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // quadrant.  With Y = diag(beta) (k o e^G):
 //   P1  dT_raw = dW Y^T                 tcgen05, A = [dW; Y] (K-major, M=128)
 //   P2  dKb'^T = dW^T T                 tcgen05, both operands MN-major
-//   P3  Y2 = dT T^T, P4 dA = -mask(T^T Y2)   fp32 CUDA cores
+//   P3  Y2 = dT T^T, P4 dA = -mask(T^T Y2)   tcgen05 with every operand split
+//       into bf16 hi + lo parts and three products (hi hi + hi lo + lo hi),
+//       which keeps about 16 mantissa bits: T products need more than bf16
 //   P5  row side, per block R: sum_j Right_R[j][c] [dA; dAqk][t][j]
 //       (Right_R[j] = k_j e^{G_bR - G_j}, the intra kernel's operand)
 //   P6  column side, per block pair (R, J<=R):
@@ -1130,7 +1139,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // The assembly then forms dk, dq, dG, dbeta and dg (reverse cumsum per
 // channel in registers) exactly as the fp32 kernel does.
 // ===========================================================================
-constexpr uint32_t LB_K = 0, LB_Q = 16384, LB_G = 32768;     // TMA tiles, later fp32 scratch
+constexpr uint32_t LB_K = 0, LB_Q = 16384, LB_G = 32768;     // TMA tiles, read up to the end
 constexpr uint32_t LB_DWY = 49152;    // [dW; Y] 128 rows x 128, 2 k-blocks of 16 KB
 constexpr uint32_t LB_T = 81920;      // T bf16 [64 r][64 m]
 constexpr uint32_t LB_DAQ = 90112;    // [dA_R; dAqk_R] rows 32R + 16s + u, 64 columns j
@@ -1138,8 +1147,16 @@ constexpr uint32_t LB_DAQT = 106496;  // transposed: rows j, columns t'' = 32R +
 constexpr uint32_t LB_RIGHT = 122880; // Right_R tiles, 16(R+1) rows each
 constexpr uint32_t LB_LCOL = 163840;  // [beta k E; qs E] rows 32R + 16s + u, 128 c
 constexpr uint32_t LB_SMALL = 196608; // fp32 small arrays
-constexpr uint32_t LB_BAR = LB_SMALL + 8192;
+constexpr uint32_t LB_TLO = LB_SMALL + 8192;  // T low part, bf16 [64 r][64 m]
+constexpr uint32_t LB_DTV = LB_TLO + 8192;    // dTv fp32 [64][64], 16-byte chunks XOR-swizzled
+constexpr uint32_t LB_BAR = LB_DTV + 16384;
+// After P1/P2 the [dW; Y] area holds the split P3/P4 operands.  P3's A has
+// M = 128 rows of which only the first 64 matter: the hi tile's rows 64..127
+// are the lo tile, the lo tile's rows 64..127 the Y2 hi tile.
+constexpr uint32_t LB_DTH = LB_DWY, LB_DTL = LB_DWY + 8192;
+constexpr uint32_t LB_Y2H = LB_DWY + 16384, LB_Y2L = LB_DWY + 24576;
 constexpr uint32_t LOCAL_TC_SMEM = LB_BAR + 64 + 1024;
+static_assert(LOCAL_TC_SMEM <= 232448, "local backward exceeds the per-CTA shared memory limit");
 constexpr int kLocalTcThreads = 512;
 
 __host__ __device__ constexpr uint32_t right_rel(int R) { return 2048u * (uint32_t)(R * (R + 1)); }
@@ -1164,14 +1181,15 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + LB_BAR);
     uint64_t* bar_m1 = bar_tma + 1;
     uint64_t* bar_m2 = bar_tma + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    uint64_t* bar_m3 = bar_tma + 3;
+    uint64_t* bar_m4 = bar_tma + 4;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 5);
     float* sBeta = reinterpret_cast<float*>(smem + LB_SMALL);   // [64]
     float* sDbeta = sBeta + 64;                                 // [64]
     float* sGtot = sDbeta + 64;                                 // [4][128]
     float* sGb = sGtot + 4 * kD;                                // [4][128]
     float* sLast = sGb + 4 * kD;                                // [4][128]
-    float* Tf = reinterpret_cast<float*>(smem + LB_K);          // fp32 [64][65] (after build)
-    float* Df = Tf + 64 * 65;                                   // fp32 [64][65]
+    float* sDtv = reinterpret_cast<float*>(smem + LB_DTV);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = tid & (kD - 1), R = tid >> 7;
@@ -1198,6 +1216,10 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int ch = tid + e * kLocalTcThreads;
         cp_async16(stT + ch * 4, a.Tm + cc0 + ch * 4);
         cp_async16(stA + ch * 4, a.dAqk + cc0 + ch * 4);
+        // dTv row i, chunk qd lands in chunk qd ^ (i & 7): a thread reading
+        // its own row's chunks then meets no bank conflict within 8 lanes
+        const int i = ch >> 4, qd = ch & 15;
+        cp_async16(sDtv + i * kC + ((qd ^ (i & 7)) << 2), a.dTv + cc0 + ch * 4);
     }
     cp_async_commit();
 
@@ -1205,6 +1227,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         mbar_init(bar_tma, 1);
         mbar_init(bar_m1, 1);
         mbar_init(bar_m2, 1);
+        mbar_init(bar_m3, 1);
+        mbar_init(bar_m4, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -1274,7 +1298,9 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int r = 16 * R + u;
         st(LB_DWY + (c >> 6) * 16384 + sw128_offset(r, cc), stW[r * kD + c]);
         if (c < kC) {
-            st(LB_T + sw128_offset(r, c), stT[r * kC + c]);
+            const float t = stT[r * kC + c];
+            st(LB_T + sw128_offset(r, c), t);
+            st(LB_TLO + sw128_offset(r, c), t - __bfloat162float(__float2bfloat16_rn(t)));
             const float dq_ = stA[r * kC + c];
             st(LB_DAQ + sw128_offset(32 * R + 16 + u, c), dq_);
             const int t2 = 32 * R + 16 + u;
@@ -1332,83 +1358,98 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     ok = ok && wait_bar_warp(bar_m1, 0, 42);
     tc_fence_after();
-    // ---- dT (fp32) from D1 rows i < 64; T in fp32 ----
+    // Epilogues below run in the warps of TMEM quadrants 0 and 1 (c < 64):
+    // thread (c, R) owns row c of a 64 x 64 result, columns 16R..16R+15.
+    auto split_st = [&](uint32_t hi, uint32_t lo, uint32_t off, float x) {
+        const __nv_bfloat16 h16 = __float2bfloat16_rn(x);
+        *reinterpret_cast<__nv_bfloat16*>(smem + hi + off) = h16;
+        *reinterpret_cast<__nv_bfloat16*>(smem + lo + off) =
+            __float2bfloat16_rn(x - __bfloat162float(h16));
+    };
+    // ---- dT = mask_strict(beta_m dTv + dW Y^T), split hi + lo ----
     if (ok && c < kC) {
-        float r16[16], tv[16];
+        float r16[16];
+        tmem_ld16(tmem + lane_off + 16 * R, r16);
         const int i = c;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) tv[e] = a.dTv[cc0 + i * kC + 16 * R + e];
+        for (int x = 0; x < 4; ++x) {
+            const float4 t4 =
+                *reinterpret_cast<const float4*>(sDtv + i * kC + (((4 * R + x) ^ (i & 7)) << 2));
+            const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = 16 * R + 4 * x + e;
+                split_st(LB_DTH, LB_DTL, sw128_offset(i, m),
+                         m < i ? sBeta[m] * tv[e] + r16[4 * x + e] : 0.f);
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- P3: Y2 = dT T^T (TMEM columns 128..191) ----
+    if (tid == 0 && ok) {
+        const uint32_t dth = smem_u32(smem + LB_DTH), dtl = smem_u32(smem + LB_DTL);
+        const uint32_t th = smem_u32(smem + LB_T), tl = smem_u32(smem + LB_TLO);
+        const uint32_t id = idesc_bf16_f32(128, 64);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + 128, sdesc_sw128(dth + kk * 32), sdesc_sw128(th + kk * 32), id, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + 128, sdesc_sw128(dth + kk * 32), sdesc_sw128(tl + kk * 32), id, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + 128, sdesc_sw128(dtl + kk * 32), sdesc_sw128(th + kk * 32), id, 1);
+        mma_commit(bar_m3);
+    }
+    ok = ok && wait_bar_warp(bar_m3, 0, 44);
+    tc_fence_after();
+    if (ok && c < kC) {
+        float r16[16];
+        tmem_ld16(tmem + lane_off + 128 + 16 * R, r16);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) split_st(LB_Y2H, LB_Y2L, sw128_offset(c, 16 * R + e), r16[e]);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- P4: T^T Y2 (TMEM columns 0..63); T and Y2 both read MN-major. A
+    // spans M = 128: its second MN block (+8192 B) is don't-care data ----
+    if (tid == 0 && ok) {
+        const uint32_t th = smem_u32(smem + LB_T), tl = smem_u32(smem + LB_TLO);
+        const uint32_t yh = smem_u32(smem + LB_Y2H), yl = smem_u32(smem + LB_Y2L);
+        const uint32_t id = idesc_bf16_f32(128, 64) | kAMajorMN | kBMajorMN;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + 0, sdesc_mn_sw128(th + kk * 2048, 8192),
+                     sdesc_mn_sw128(yh + kk * 2048, 8192), id, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + 0, sdesc_mn_sw128(th + kk * 2048, 8192),
+                     sdesc_mn_sw128(yl + kk * 2048, 8192), id, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + 0, sdesc_mn_sw128(tl + kk * 2048, 8192),
+                     sdesc_mn_sw128(yh + kk * 2048, 8192), id, 1);
+        mma_commit(bar_m4);
+    }
+    ok = ok && wait_bar_warp(bar_m4, 0, 45);
+    tc_fence_after();
+    // dA = -mask_strict(T^T Y2) (bf16) into the row-side and column-side B tiles
+    if (ok && c < kC) {
+        float r16[16];
         tmem_ld16(tmem + lane_off + 16 * R, r16);
+        const int i = c, t2 = 32 * (i >> 4) + (i & 15);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-            const int m = 16 * R + e;
-            Df[i * 65 + m] = m < i ? sBeta[m] * tv[e] + r16[e] : 0.f;
+            const int j = 16 * R + e;
+            const float v = j < i ? -r16[e] : 0.f;
+            st(LB_DAQ + sw128_offset(t2, j), v);
+            st(LB_DAQT + (t2 >> 6) * 8192 + sw128_offset(j, t2 & 63), v);
         }
-    }
-    {
-        float tv[kC * kC / kLocalTcThreads];
-#pragma unroll
-        for (int e = 0; e < kC * kC / kLocalTcThreads; ++e)
-            tv[e] = a.Tm[cc0 + tid + e * kLocalTcThreads];
-#pragma unroll
-        for (int e = 0; e < kC * kC / kLocalTcThreads; ++e) {
-            const int idx = tid + e * kLocalTcThreads;
-            Tf[(idx >> 6) * 65 + (idx & 63)] = tv[e];
-        }
-    }
-    __syncthreads();
-    // ---- P3: Y2 = dT T^T ; P4: dA = -mask_strict(T^T Y2)   (fp32, in Df) ----
-    {
-        const int tr = warp, tc = lane, r0 = 4 * tr;
-        float acc[4][2];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.f;
-#pragma unroll 4
-        for (int m = 0; m < kC; ++m) {
-            const float t0v = Tf[tc * 65 + m], t1v = Tf[(tc + 32) * 65 + m];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float dv = Df[(r0 + i) * 65 + m];
-                acc[i][0] += dv * t0v;
-                acc[i][1] += dv * t1v;
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            Df[(r0 + i) * 65 + tc] = acc[i][0];
-            Df[(r0 + i) * 65 + tc + 32] = acc[i][1];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.f;
-#pragma unroll 4
-        for (int m = 0; m < kC; ++m) {
-            const float y0 = Df[m * 65 + tc], y1 = Df[m * 65 + tc + 32];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float tv = Tf[m * 65 + r0 + i];
-                acc[i][0] += tv * y0;
-                acc[i][1] += tv * y1;
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int ii = r0 + i, j = tc + 32 * u;
-                Df[ii * 65 + j] = j < ii ? -acc[i][u] : 0.f;
-            }
-    }
-    __syncthreads();
-    // dA (bf16) into the row-side and column-side B tiles
-    for (int idx = tid; idx < kC * kC; idx += kLocalTcThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        const float v = Df[i * 65 + j];
-        const int t2 = 32 * (i >> 4) + (i & 15);
-        st(LB_DAQ + sw128_offset(t2, j), v);
-        st(LB_DAQT + (t2 >> 6) * 8192 + sw128_offset(j, t2 & 63), v);
     }
     fence_async_smem();
     tc_fence_before();
@@ -1474,9 +1515,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             const float E = __expf(G[u] - Gb[R]);
             const float Einv = __expf(Gb[R] - G[u]);
             const float eG = eGbR * E, eL = eLbR * Einv;
-            const size_t iqk = (((size_t)trow + t) * a.H + h) * kD + c;
-            const float kr = __bfloat162float(a.k[iqk]);
-            const float qr = a.scale * __bfloat162float(a.q[iqk]);
+            const float kr = ldt(LB_K, t);
+            const float qr = a.scale * ldt(LB_Q, t);
             const float br = sBeta[t];
             const float dKbeta = dkb[u];
             const float dQh = pQh[u];
@@ -1525,7 +1565,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             run += dG[u];
             const int t = 16 * R + u;
             const size_t ig = (((size_t)trow + t) * a.HV + hv) * kD + c;
-            a.dg[ig] = __float2bfloat16_rn(__bfloat162float(a.g[ig]) >= kGateFloor ? run : 0.f);
+            a.dg[ig] = __float2bfloat16_rn(ldt(LB_G, t) >= kGateFloor ? run : 0.f);
         }
     }
     if (tid < kC)
