@@ -84,8 +84,27 @@ def kernel_algo_bytes(name, w):
         return tok_in + WQK + 3 * CC + 2 * B * T * HV * K * f32 + BH * T * K * e
     if name == "simt_group_sum":
         return 2 * B * T * HV * K * f32 + 2 * B * T * H * K * e
-    if name == "tc_fwd":
-        return BH * T * FWD_BYTES_PER_HEAD_TOKEN * (K / 128)
+    # tensor-core path (K = V = 128, chunk 64): per head-token bytes of the
+    # kernel's own inputs and outputs, bf16 operand arrays at 2 B/element,
+    # fp32 workspace arrays at 4 B; q and k are read once per query head.
+    if K == 128 and V == 128 and C == 64 and e == 2:
+        G = HV // H
+        qk = 2 * K * e // G                      # q, k per value head
+        ops = 4 * K * 2                          # W, Qh, U, Kb (bf16)
+        cc = C * 2                               # one bf16 C x C row per token
+        per = {
+            "tc_intra": qk + 2 * K * e + e + ops + 2 * cc + C * 4 + K * 4 // C,
+            "tc_chain_fwd": ops + cc + K * 4 // C + V * e,
+            "tc_chain_fwd_save": ops + cc + K * 4 // C + V * e + K * V * 2 // C + V * 2,
+            "tc_chain_states": ops + cc + K * 4 // C + K * V * 2 // C + V * 2,
+            "tc_chain_bwd": V * e + 3 * K * 2 + cc + K * 4 // C + K * V * 2 // C + V * 2,
+            "tc_grad_v": (2 * K * V * 2 // C + V * e + 2 * V * 2 + V * e + cc + e)
+                         + (V * e + 3 * K * 4 + K * 4 // C + 2 * C * 4 + 4),
+            "tc_local_bwd": (C * 4 + 3 * K * 4 + 2 * C * 4 + K * 4 // C + 4 + qk + K * e + e)
+                            + (2 * K * (e if G == 1 else 4) + K * e + e),
+        }
+        if name in per:
+            return BH * T * per[name]
     return None
 
 
@@ -183,9 +202,9 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w, path):
+def workload_config(w, path, bwd="saved"):
     return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K, "V": w.V,
-            "chunk": w.chunk, "pass": "fwd+bwd", "path": path,
+            "chunk": w.chunk, "pass": "fwd+bwd", "path": path, "backward": bwd,
             "l2": "inputs larger than L2 (q, k, v, g = 512 MiB bf16; no flush needed)",
             "parallelism": "one independent replica per rank"}
 
@@ -229,6 +248,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--bwd", default="saved", choices=["saved", "recompute"],
+                    help="saved: the backward starts from the forward's saved intermediates; "
+                         "recompute: stateless backward")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--B", type=int, default=None,
                     help="override the batch (profiling / sweeps; default: the workload's)")
@@ -272,16 +294,28 @@ def main():
     dims_f = kda.kda.make_dims(q, v, w.chunk, None, args.path)
     ws_f = torch.empty(max(1, kda.workspace_bytes(dims_f, False)), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(max(1, kda.workspace_bytes(dims_f, True)), dtype=torch.uint8, device=dev)
+    saving = args.bwd == "saved"
     o = torch.empty_like(v)
     grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                  dg=torch.empty_like(g), dbeta=torch.empty_like(beta), dh0=None)
     stream = torch.cuda.current_stream()
 
+    def fwd_bwd(q, k, v, g, beta, do):
+        # saved: the forward keeps its intermediates for the backward (as an
+        # autograd function saves tensors); recompute: a stateless backward
+        if saving:
+            _, _, sv = kda.chunk_kda_fwd(q, k, v, g, beta, chunk_size=w.chunk, impl=args.path,
+                                         workspace=ws_b, out=o, save_for_backward=True)
+            kda.chunk_kda_bwd(q, k, v, g, beta, do, chunk_size=w.chunk, impl=args.path,
+                              grads=grads, saved=sv)
+        else:
+            kda.chunk_kda_fwd(q, k, v, g, beta, chunk_size=w.chunk, impl=args.path,
+                              workspace=ws_f, out=o)
+            kda.chunk_kda_bwd(q, k, v, g, beta, do, chunk_size=w.chunk, impl=args.path,
+                              workspace=ws_b, grads=grads)
+
     def step():
-        kda.chunk_kda_fwd(q, k, v, g, beta, chunk_size=w.chunk, impl=args.path, workspace=ws_f,
-                          out=o)
-        kda.chunk_kda_bwd(q, k, v, g, beta, do, chunk_size=w.chunk, impl=args.path,
-                          workspace=ws_b, grads=grads)
+        fwd_bwd(q, k, v, g, beta, do)
 
     for _ in range(args.warmup):
         step()
@@ -324,10 +358,7 @@ def main():
     def e2e_step():
         for n in h_in:
             d_in[n].copy_(h_in[n], non_blocking=True)
-        kda.chunk_kda_fwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"],
-                          chunk_size=w.chunk, impl=args.path, workspace=ws_f, out=o)
-        kda.chunk_kda_bwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"], d_in["do"],
-                          chunk_size=w.chunk, impl=args.path, workspace=ws_b, grads=grads)
+        fwd_bwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"], d_in["do"])
         h_out["o"].copy_(o, non_blocking=True)
         for n in ("dq", "dk", "dv", "dg", "dbeta"):
             h_out[n].copy_(grads[n], non_blocking=True)
@@ -376,7 +407,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(w, args.path),
+        "data": "synthetic", "config": workload_config(w, args.path, args.bwd),
         "roofline": roofline,
         "step_roofline": {"bytes": step_bytes, "roofline_ms": step_roof_ms,
                           "frac": step_roof_ms / ms, "note": "whole fwd+bwd step at HBM peak"},

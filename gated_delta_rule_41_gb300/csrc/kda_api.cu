@@ -95,10 +95,10 @@ size_t kda_chunk_workspace_bytes(const kda_dims* d, int for_bwd) {
     return ws_bytes(*d, impl, for_bwd ? 1 : 0);
 }
 
-kda_status kda_chunk_fwd(const kda_dims* d, const void* q, const void* k, const void* v,
-                         const void* g, const void* beta, const float* h0, void* o,
-                         int output_final_state, float* ht, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+static kda_status chunk_fwd(const kda_dims* d, const void* q, const void* k, const void* v,
+                            const void* g, const void* beta, const float* h0, void* o,
+                            int output_final_state, float* ht, void* workspace,
+                            size_t workspace_bytes, void* stream, bool save) {
     kda_status st = check_common(d, true);
     if (st != KDA_OK) return st;
     const int impl = pick_impl(*d);
@@ -110,20 +110,22 @@ kda_status kda_chunk_fwd(const kda_dims* d, const void* q, const void* k, const 
         return st;
     if ((st = check_ptrs(empty, elem_bytes(*d), {beta}, {})) != KDA_OK)
         return st;
-    if ((st = check_ws(*d, impl, 0, workspace, workspace_bytes)) != KDA_OK) return st;
+    if ((st = check_ws(*d, impl, save ? 1 : 0, workspace, workspace_bytes)) != KDA_OK) return st;
     float* ht_out = output_final_state ? ht : nullptr;
     auto s = static_cast<cudaStream_t>(stream);
     if (d->B == 0) return KDA_OK;
     if (d->T == 0) return copy_or_zero(*d, ht_out, h0, s);
-    if (impl == KDA_IMPL_TCGEN05) return tc_fwd(*d, q, k, v, g, beta, h0, o, ht_out, workspace, s);
+    if (impl == KDA_IMPL_TCGEN05)
+        return tc_fwd(*d, q, k, v, g, beta, h0, o, ht_out, workspace, save, s);
+    // the SIMT backward recomputes everything: nothing extra to save
     return simt_fwd(*d, q, k, v, g, beta, h0, o, ht_out, workspace, s);
 }
 
-kda_status kda_chunk_bwd(const kda_dims* d, const void* q, const void* k, const void* v,
-                         const void* g, const void* beta, const float* h0, const void* dout,
-                         const float* dht, void* dq, void* dk, void* dv, void* dg,
-                         void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+static kda_status chunk_bwd(const kda_dims* d, const void* q, const void* k, const void* v,
+                            const void* g, const void* beta, const float* h0, const void* dout,
+                            const float* dht, void* dq, void* dk, void* dv, void* dg,
+                            void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                            void* stream, bool from_saved) {
     kda_status st = check_common(d, true);
     if (st != KDA_OK) return st;
     int impl = pick_impl(*d);
@@ -150,9 +152,43 @@ kda_status kda_chunk_bwd(const kda_dims* d, const void* q, const void* k, const 
     if (d->T == 0) return copy_or_zero(*d, dh0, dht, s);
     if (impl == KDA_IMPL_TCGEN05)
         return tc_bwd(*d, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
-                      s);
+                      from_saved, s);
     return simt_bwd(*d, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
                     s);
+}
+
+kda_status kda_chunk_fwd(const kda_dims* d, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* h0, void* o,
+                         int output_final_state, float* ht, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    return chunk_fwd(d, q, k, v, g, beta, h0, o, output_final_state, ht, workspace,
+                     workspace_bytes, stream, false);
+}
+
+kda_status kda_chunk_fwd_save(const kda_dims* d, const void* q, const void* k, const void* v,
+                              const void* g, const void* beta, const float* h0, void* o,
+                              int output_final_state, float* ht, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    return chunk_fwd(d, q, k, v, g, beta, h0, o, output_final_state, ht, workspace,
+                     workspace_bytes, stream, true);
+}
+
+kda_status kda_chunk_bwd(const kda_dims* d, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* h0, const void* dout,
+                         const float* dht, void* dq, void* dk, void* dv, void* dg,
+                         void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    return chunk_bwd(d, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
+                     workspace_bytes, stream, false);
+}
+
+kda_status kda_chunk_bwd_saved(const kda_dims* d, const void* q, const void* k, const void* v,
+                               const void* g, const void* beta, const float* h0,
+                               const void* dout, const float* dht, void* dq, void* dk, void* dv,
+                               void* dg, void* dbeta, float* dh0, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    return chunk_bwd(d, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
+                     workspace_bytes, stream, true);
 }
 
 kda_status kda_recurrent_step(const kda_dims* d, const void* q, const void* k, const void* v,

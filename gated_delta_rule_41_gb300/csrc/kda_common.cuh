@@ -71,13 +71,17 @@ kda_status simt_bwd(const kda_dims& d, const void* q, const void* k, const void*
 
 bool tc_supported(const kda_dims& d);
 size_t tc_workspace_bytes(const kda_dims& d, int for_bwd);
+// save: also keep the chunk-start states and delta in a backward-sized
+// workspace.  from_saved: the workspace holds a saving forward's results for
+// these inputs, so the intra-chunk recompute and the forward state pass are
+// skipped.
 kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v,
                   const void* g, const void* beta, const float* h0, void* o, float* ht,
-                  void* ws, cudaStream_t s);
+                  void* ws, bool save, cudaStream_t s);
 kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v,
                   const void* g, const void* beta, const float* h0, const void* dout,
                   const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
-                  float* dh0, void* ws, cudaStream_t s);
+                  float* dh0, void* ws, bool from_saved, cudaStream_t s);
 // Reads and clears the device error word of the tensor-core kernels.
 kda_status tc_take_error(cudaStream_t s);
 

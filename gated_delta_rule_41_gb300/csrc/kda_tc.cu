@@ -1769,7 +1769,9 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
                              (int)CHAIN_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
     {
-        TimedLaunch tl("tc_chain_fwd", s);
+        // three roles, timed apart: forward (o), saving forward (o and the
+        // chunk-start states), and the backward's recompute (states only)
+        TimedLaunch tl(!h_out ? "tc_chain_fwd" : o ? "tc_chain_fwd_save" : "tc_chain_states", s);
         chain_fwd_kernel<<<BH, 192, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, args);
     }
     return launch_status();
@@ -1787,28 +1789,34 @@ size_t tc_workspace_bytes(const kda_dims& d, int for_bwd) {
 }
 
 kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
-                  const void* beta, const float* h0, void* o, float* ht, void* ws,
+                  const void* beta, const float* h0, void* o, float* ht, void* ws, bool save,
                   cudaStream_t s) {
     TcWs w;
-    tc_carve(d, 0, static_cast<char*>(ws), &w);
+    tc_carve(d, save ? 1 : 0, static_cast<char*>(ws), &w);
     float* gam = nullptr;
     kda_status st = run_intra_tc(d, w, q, k, v, g, beta, s, &gam);
     if (st != KDA_OK) return st;
-    return run_chain_fwd(d, w, gam, h0, o, ht, nullptr, nullptr, s);
+    return run_chain_fwd(d, w, gam, h0, o, ht, save ? w.h2 : nullptr, save ? w.d2 : nullptr, s);
 }
 
 kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
                   const void* beta, const float* h0, const void* dout, const float* dht,
                   void* dq, void* dk, void* dv, void* dg, void* dbeta, float* dh0, void* ws,
-                  cudaStream_t s) {
+                  bool from_saved, cudaStream_t s) {
     TcWs w;
     tc_carve(d, 1, static_cast<char*>(ws), &w);
     float* gam = nullptr;
-    kda_status st = run_intra_tc(d, w, q, k, v, g, beta, s, &gam);
-    if (st != KDA_OK) return st;
-    // forward recompute: chunk-start states and delta
-    if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s)) != KDA_OK)
-        return st;
+    kda_status st = KDA_OK;
+    if (from_saved) {
+        SimtWsPtrs p0;
+        simt_ws_ptrs(d, 0, w.simt, &p0);  // where the intra kernel left gam
+        gam = p0.gam;
+    } else {
+        if ((st = run_intra_tc(d, w, q, k, v, g, beta, s, &gam)) != KDA_OK) return st;
+        // forward recompute: chunk-start states and delta
+        if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s)) != KDA_OK)
+            return st;
+    }
     const int BH = d.B * d.HV, NT = d.T / kC;
     const uint64_t rows = (uint64_t)BH * d.T;
     // reverse chain

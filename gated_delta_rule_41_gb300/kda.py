@@ -56,10 +56,12 @@ def load_library():
         P, D, I, S = ctypes.c_void_p, ctypes.POINTER(KdaDims), ctypes.c_int, ctypes.c_size_t
         lib.kda_chunk_workspace_bytes.argtypes = [D, I]
         lib.kda_chunk_workspace_bytes.restype = S
-        lib.kda_chunk_fwd.argtypes = [D, P, P, P, P, P, P, P, I, P, P, S, P]
-        lib.kda_chunk_fwd.restype = I
-        lib.kda_chunk_bwd.argtypes = [D] + [P] * 15 + [S, P]
-        lib.kda_chunk_bwd.restype = I
+        for name in ("kda_chunk_fwd", "kda_chunk_fwd_save"):
+            getattr(lib, name).argtypes = [D, P, P, P, P, P, P, P, I, P, P, S, P]
+            getattr(lib, name).restype = I
+        for name in ("kda_chunk_bwd", "kda_chunk_bwd_saved"):
+            getattr(lib, name).argtypes = [D] + [P] * 15 + [S, P]
+            getattr(lib, name).restype = I
         lib.kda_recurrent_step.argtypes = [D] + [P] * 8
         lib.kda_recurrent_step.restype = I
         lib.kda_check.argtypes = [P]
@@ -130,10 +132,21 @@ def _raise(st, what):
         raise KdaError(st, what)
 
 
+class SavedForward:
+    """Workspace filled by ``chunk_kda_fwd(..., save_for_backward=True)``.
+
+    Pass it as ``saved=`` to ``chunk_kda_bwd`` with the same inputs, before
+    any other call writes the workspace."""
+
+    def __init__(self, workspace, nbytes, dims):
+        self.workspace, self.nbytes, self.dims = workspace, nbytes, dims
+
+
 def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
                   chunk_size=64, impl="auto", workspace=None, out=None, final_state=None,
-                  stream=None):
-    """Chunked KDA forward.  Returns (o, final_state or None)."""
+                  stream=None, save_for_backward=False):
+    """Chunked KDA forward.  Returns (o, final_state or None), plus a
+    ``SavedForward`` when ``save_for_backward`` is set."""
     lib = load_library()
     _check_dev(q, k, v, g, beta, initial_state)
     dims = make_dims(q, v, chunk_size, scale, impl)
@@ -142,17 +155,23 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final
     if output_final_state:
         ht = (torch.empty(dims.B, dims.HV, dims.K, dims.V, dtype=torch.float32, device=q.device)
               if final_state is None else final_state)
-    ws, nws = _workspace(dims, False, q.device, workspace)
-    st = lib.kda_chunk_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                           _ptr(initial_state), _ptr(o), int(output_final_state), _ptr(ht),
-                           _ptr(ws), nws, _stream(stream))
-    _raise(st, "kda_chunk_fwd")
+    ws, nws = _workspace(dims, save_for_backward, q.device, workspace)
+    fn = lib.kda_chunk_fwd_save if save_for_backward else lib.kda_chunk_fwd
+    st = fn(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+            _ptr(initial_state), _ptr(o), int(output_final_state), _ptr(ht), _ptr(ws), nws,
+            _stream(stream))
+    _raise(st, "kda_chunk_fwd_save" if save_for_backward else "kda_chunk_fwd")
+    if save_for_backward:
+        return o, ht, SavedForward(ws, nws, dims)
     return o, ht
 
 
 def chunk_kda_bwd(q, k, v, g, beta, do, dht=None, scale=None, initial_state=None,
-                  chunk_size=64, impl="auto", workspace=None, grads=None, stream=None):
-    """Backward of chunk_kda_fwd.  Returns dict dq, dk, dv, dg, dbeta, dh0."""
+                  chunk_size=64, impl="auto", workspace=None, grads=None, stream=None,
+                  saved=None):
+    """Backward of chunk_kda_fwd.  Returns dict dq, dk, dv, dg, dbeta, dh0.
+    With ``saved`` (from a saving forward on the same inputs) the tensor-core
+    kernels start from the saved intermediates instead of recomputing them."""
     lib = load_library()
     _check_dev(q, k, v, g, beta, do, dht, initial_state)
     dims = make_dims(q, v, chunk_size, scale, impl)
@@ -161,13 +180,22 @@ def chunk_kda_bwd(q, k, v, g, beta, do, dht=None, scale=None, initial_state=None
                      dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
                      dh0=(torch.empty(dims.B, dims.HV, dims.K, dims.V, dtype=torch.float32,
                                       device=q.device) if initial_state is not None else None))
-    ws, nws = _workspace(dims, True, q.device, workspace)
-    st = lib.kda_chunk_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                           _ptr(initial_state), _ptr(do), _ptr(dht), _ptr(grads["dq"]),
-                           _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dg"]),
-                           _ptr(grads["dbeta"]), _ptr(grads.get("dh0")), _ptr(ws), nws,
-                           _stream(stream))
-    _raise(st, "kda_chunk_bwd")
+    if saved is not None:
+        if (saved.dims.B, saved.dims.T, saved.dims.H, saved.dims.HV, saved.dims.K, saved.dims.V,
+                saved.dims.chunk_size, saved.dims.impl) != (dims.B, dims.T, dims.H, dims.HV,
+                                                          dims.K, dims.V, dims.chunk_size,
+                                                          dims.impl):
+            raise KdaError(1, "chunk_kda_bwd: saved forward has other dims")
+        ws, nws, fn, what = saved.workspace, saved.nbytes, lib.kda_chunk_bwd_saved, \
+            "kda_chunk_bwd_saved"
+    else:
+        ws, nws = _workspace(dims, True, q.device, workspace)
+        fn, what = lib.kda_chunk_bwd, "kda_chunk_bwd"
+    st = fn(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+            _ptr(initial_state), _ptr(do), _ptr(dht), _ptr(grads["dq"]), _ptr(grads["dk"]),
+            _ptr(grads["dv"]), _ptr(grads["dg"]), _ptr(grads["dbeta"]), _ptr(grads.get("dh0")),
+            _ptr(ws), nws, _stream(stream))
+    _raise(st, what)
     return grads
 
 

@@ -117,6 +117,32 @@ kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, con
                          void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* Forward that also keeps in the workspace what the backward needs, the way
+ * an autograd function saves tensors for its backward pass: the intra-chunk
+ * operands (W, U, decayed q and k, Aqk, T), the chunk decays, and the state at
+ * every chunk start with each chunk's delta.  Arguments and results are
+ * those of kda_chunk_fwd, but the workspace must hold
+ * kda_chunk_workspace_bytes(dims, 1) bytes.  Hand that workspace, untouched,
+ * to kda_chunk_bwd_saved.  With the SIMT kernels it runs the plain forward
+ * (their backward recomputes). */
+kda_status kda_chunk_fwd_save(const kda_dims* dims, const void* q, const void* k,
+                              const void* v, const void* g, const void* beta, const float* h0,
+                              void* o, int output_final_state, float* ht, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Backward from a workspace filled by kda_chunk_fwd_save with the same dims
+ * (impl included), inputs and h0, and not written since.  Arguments, results
+ * and errors are those of kda_chunk_bwd.  The tensor-core kernels skip the
+ * intra-chunk recompute and the forward state pass; a call that runs the
+ * SIMT kernels (dims->impl SIMT, or AUTO with dht given) recomputes from the
+ * inputs, so its results do not depend on what the workspace holds.  A
+ * workspace not filled as stated gives undefined results, not an error. */
+kda_status kda_chunk_bwd_saved(const kda_dims* dims, const void* q, const void* k,
+                               const void* v, const void* g, const void* beta, const float* h0,
+                               const void* dout, const float* dht, void* dq, void* dk, void* dv,
+                               void* dg, void* dbeta, float* dh0, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* One decode token per head, state updated in place (K3 row L6).
  * dims->T is ignored; q, k [B,H,K]; v, o [B,HV,V]; g [B,HV,K]; beta [B,HV]
  * (dtype); state [B,HV,K,V] f32, read and overwritten. */

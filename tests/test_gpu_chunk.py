@@ -105,6 +105,43 @@ def test_bf16_gva_k128(impl, with_dht):
     compare_all(res, oracle_chunk(inp, True), w)
 
 
+@pytest.mark.parametrize("impl,wl", [
+    ("tcgen05", I.Workload("saved_k128", 2, 256, 2, 4, 128, 128, 64, torch.bfloat16,
+                           g_sigma=2.0, h0_std=0.1, seed=27)),
+    ("auto", I.Workload("saved_k128_dht", 1, 192, 2, 2, 128, 128, 64, torch.bfloat16,
+                        g_sigma=2.0, h0_std=0.1, dht=True, seed=28)),
+    ("simt", I.Workload("saved_simt", 2, 128, 2, 4, 32, 32, 32, torch.float32, g_sigma=2.0,
+                        h0_std=0.3, dht=True, seed=29)),
+])
+def test_saved_forward_backward(impl, wl):
+    """A saving forward followed by the backward from its workspace gives the
+    oracle's outputs and gradients (the tensor cores skip the recompute; the
+    SIMT kernels and AUTO with dht recompute)."""
+    t = {n: (x.cuda() if x is not None else None) for n, x in I.make_chunk_inputs(wl).items()}
+    o, ht, saved = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                     initial_state=t["h0"], output_final_state=True,
+                                     chunk_size=wl.chunk, impl=impl, save_for_backward=True)
+    # another call in between must not matter: it uses its own workspace
+    kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], chunk_size=wl.chunk, impl=impl)
+    res = dict(o=o, ht=ht)
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], dht=t["dht"],
+                                 initial_state=t["h0"], chunk_size=wl.chunk, impl=impl,
+                                 saved=saved))
+    torch.cuda.synchronize()
+    kda.check()
+    compare_all(res, oracle_chunk(I.make_chunk_inputs(wl), True), wl, with_h0=True)
+
+
+def test_saved_backward_rejects_other_dims():
+    w = I.Workload("saved_dims", 1, 128, 1, 1, 128, 128, 64, torch.bfloat16, seed=30)
+    t = {n: (x.cuda() if x is not None else None) for n, x in I.make_chunk_inputs(w).items()}
+    _, _, saved = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                    save_for_backward=True)
+    with pytest.raises(kda.KdaError):
+        kda.chunk_kda_bwd(t["q"][:, :64], t["k"][:, :64], t["v"][:, :64], t["g"][:, :64],
+                          t["beta"][:, :64], t["do"][:, :64], saved=saved)
+
+
 def test_tcgen05_backward_refuses_final_state_gradient():
     w = I.Workload("bf16_dht", 1, 128, 1, 1, 128, 128, 64, torch.bfloat16, dht=True, seed=26)
     t = {n: (x.cuda() if x is not None else None) for n, x in I.make_chunk_inputs(w).items()}
