@@ -71,6 +71,31 @@ constexpr uint32_t CHAIN_SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_W = 128, TM_O0 = 192, TM_O1 = 256, TM_COLS = 512;
 
+// Sums each of N (16 or 32) per-lane values over the 32 lanes of a warp with
+// N - 1 + (32 / N - 1) shuffles (a reduce-scatter butterfly: at offset o a
+// lane keeps the half of its remaining values selected by lane bit o and adds
+// the partner's copy of that half).  On return lane l holds the warp total of
+// value l * N / 32.  v is overwritten.
+template <int N>
+__device__ __forceinline__ float warp_sum_scatter(float (&v)[N]) {
+    static_assert(N == 16 || N == 32, "N must be 16 or 32");
+    const int lane = threadIdx.x & 31;
+    int o = 16;
+#pragma unroll
+    for (int n = N; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+#pragma unroll
+    for (; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    return v[0];
+}
+
 // ---- epilogue steps shared by the two chains (thread <-> value column v) ----
 
 __device__ __forceinline__ void store_row_bf16(uint8_t* base, int v, int col0, const float (&r)[32],
@@ -594,7 +619,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 constexpr uint32_t G_S0 = 0, G_DS = 32768, G_ODD = 65536, G_DV = 98304, G_T = 131072;
 constexpr uint32_t G_BAR = 139264, G_DBV = G_BAR + 64;
 constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
-constexpr uint32_t GRAD_SMEM = G_DBV + 512 + 1024;
+constexpr uint32_t GRAD_SMEM = G_DBV + 1280 + 1024;
 constexpr int kGradThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
 
 struct GradArgs {
@@ -615,8 +640,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + G_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 2);
-    float* dbv_s = reinterpret_cast<float*>(smem + G_DBV);  // [64]
-    float* beta_s = dbv_s + 64;                              // [64]
+    float* dbv_part = reinterpret_cast<float*>(smem + G_DBV);  // [4 lane quadrants][64]
+    float* beta_s = dbv_part + 4 * 64;                          // [64]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x, bh = blockIdx.y;
@@ -629,7 +654,6 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         fence_mbar_init();
     }
     if (threadIdx.x < 64) {
-        dbv_s[threadIdx.x] = 0.f;
         beta_s[threadIdx.x] = __bfloat162float(
             a.beta[((size_t)b * a.T + (size_t)n * kC + threadIdx.x) * a.HV + hv]);
     }
@@ -750,23 +774,26 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             }
             // D5: lane = v, columns m = 32*cb .. 32*cb+31
             tmem_ld32(tmem + lane_off + 192 + cb * 32, r);
-#pragma unroll 4
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int m = cb * 32 + j;
                 const float bt = beta_s[m];
                 a.dv[(((size_t)trow + m) * a.HV + hv) * kD + l] = __float2bfloat16_rn(bt * r[j]);
                 const uint32_t voff = G_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
-                float p = r[j] * __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                if (lane == 0) atomicAdd(&dbv_s[m], p);
+                r[j] *= __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
             }
+            // dbv[m] = sum over v of r: lane j ends with row cb*32 + j of this quadrant
+            dbv_part[q * 64 + cb * 32 + lane] = warp_sum_scatter<32>(r);
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (threadIdx.x < 64) a.dbv[(size_t)row + threadIdx.x] = dbv_s[threadIdx.x];
+    if (threadIdx.x < 64) {
+        const int m = threadIdx.x;
+        a.dbv[(size_t)row + m] =
+            (dbv_part[m] + dbv_part[64 + m]) + (dbv_part[128 + m] + dbv_part[192 + m]);
+    }
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -1185,8 +1212,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint64_t* bar_m4 = bar_tma + 4;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 5);
     float* sBeta = reinterpret_cast<float*>(smem + LB_SMALL);   // [64]
-    float* sDbeta = sBeta + 64;                                 // [64]
-    float* sGtot = sDbeta + 64;                                 // [4][128]
+    float* sDbp = sBeta + 64;                                   // [4 lane quadrants][64]
+    float* sGtot = sDbp + 4 * 64;                               // [4][128]
     float* sGb = sGtot + 4 * kD;                                // [4][128]
     float* sLast = sGb + 4 * kD;                                // [4][128]
     float* sDtv = reinterpret_cast<float*>(smem + LB_DTV);
@@ -1237,7 +1264,6 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     if (tid < kC) {
         sBeta[tid] = __bfloat162float(a.beta[((size_t)trow + tid) * a.HV + hv]);
-        sDbeta[tid] = 0.f;
     }
     tc_fence_before();
     __syncthreads();
@@ -1494,8 +1520,10 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     tc_fence_after();
 
     // ---- assembly: thread (c, R) for rows t = 16R + u ----
-    float dG[16];
+    float dG[16], dbps[16];
     float lastp = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) dbps[u] = 0.f;
     if (ok) {
         float dkb[16], cAQ[16], sAQ[32];
         tmem_ld16(tmem + lane_off + 64 + 16 * R, dkb);          // d(beta khat) for t in R
@@ -1527,7 +1555,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             dG[u] = dKbeta * br * kr * eG + dQh * qr * eG - dKb * kr * eL + br * kr * sa +
                     qr * sq - kr * caq;
             lastp += dKb * kr * eL;
-            float dbp = dKbeta * kr * eG + kr * sa;
+            dbps[u] = dKbeta * kr * eG + kr * sa;
             const size_t io = (((size_t)trow + t) * a.HV + hv) * kD + c;
             if (a.G == 1) {
                 a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
@@ -1536,13 +1564,16 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 a.dqh[io] = a.scale * dqs;
                 a.dkh[io] = dkv;
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dbp += __shfl_xor_sync(0xffffffffu, dbp, o);
-            if (lane == 0) atomicAdd(&sDbeta[t], dbp);
         }
     } else {
 #pragma unroll
         for (int u = 0; u < 16; ++u) dG[u] = 0.f;
+    }
+    // dbeta partials of rows 16R..16R+15 over this warp's 32 channels: lane
+    // pair (2u, 2u+1) ends with row 16R + u
+    {
+        const float tot = warp_sum_scatter<16>(dbps);
+        if (!(lane & 1)) sDbp[(warp & 3) * 64 + 16 * R + (lane >> 1)] = tot;
     }
     // block sums of dG and the last-row partials, for the reverse cumsum
     float bsum = 0.f;
@@ -1570,7 +1601,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     if (tid < kC)
         a.dbeta[((size_t)trow + tid) * a.HV + hv] =
-            __float2bfloat16_rn(sDbeta[tid] + a.dbv[row0 + tid]);
+            __float2bfloat16_rn((sDbp[tid] + sDbp[64 + tid]) + (sDbp[128 + tid] + sDbp[192 + tid]) +
+                                a.dbv[row0 + tid]);
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
