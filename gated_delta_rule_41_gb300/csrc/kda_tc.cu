@@ -68,6 +68,9 @@ constexpr uint32_t OFF_DELTA = OFF_S + 32768;  // delta^T operand: 128 rows x 64
 constexpr uint32_t OFF_BAR = OFF_DELTA + 16384;
 constexpr uint32_t CHAIN_SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
 
+// TMA warp, MMA warp, 8 epilogue warps (two per TMEM lane quadrant)
+constexpr int kChainThreads = 320, kChainEpi = 256;
+
 // TMEM columns
 constexpr uint32_t TM_S = 0, TM_W = 128, TM_O0 = 192, TM_O1 = 256, TM_COLS = 512;
 
@@ -111,12 +114,13 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* base, int v, int col0, c
     }
 }
 
-// Copies row v of a K-major bf16 tile (ncols = 64 or 128 columns, k-blocks of
-// `kb_stride` bytes) to out[c * ld + v] for every column c, times `sign`.
+// Copies columns [col0, col0 + ncols) of row v of a K-major bf16 tile
+// (64-column k-blocks `kb_stride` bytes apart) to out[c * ld] for each
+// column c, times `sign`.  col0 and ncols are multiples of 8.
 __device__ __forceinline__ void tile_row_to_global(const uint8_t* tile, uint32_t kb_stride, int v,
-                                                   int ncols, float sign, __nv_bfloat16* out,
-                                                   size_t ld) {
-    for (int c8 = 0; c8 < ncols / 8; ++c8) {
+                                                   int col0, int ncols, float sign,
+                                                   __nv_bfloat16* out, size_t ld) {
+    for (int c8 = col0 / 8; c8 < (col0 + ncols) / 8; ++c8) {
         const uint4 x = *reinterpret_cast<const uint4*>(
             tile + (c8 >> 3) * kb_stride + sw128_offset(v, (c8 & 7) * 8));
         const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
@@ -129,81 +133,71 @@ __device__ __forceinline__ void tile_row_to_global(const uint8_t* tile, uint32_t
     }
 }
 
-// State step: S^T (lane v, columns k) from TMEM -- or, for the first chunk,
-// from `init` ([K][V] fp32, may be null = zeros) -- to the bf16 K-major
-// operand tile; the TMEM copy is scaled by gam (per column k); arrive on
-// `bar`; then, off the critical path, the bf16 state to out[k][v].
+// The chains' epilogue has two threads per value column v (TMEM lane); each
+// takes one half of the columns of a step.
+
+// State step, columns k in [64 half, 64 half + 64): S^T (lane v) from TMEM --
+// or, for the first chunk, from `init` ([K][V] fp32, may be null = zeros) --
+// to k-block `half` of the bf16 K-major operand tile; the TMEM copy is scaled
+// by gam (per column k); arrive on `bar`; then, off the critical path, the
+// bf16 state to out[k][v].
 __device__ __forceinline__ void chain_state_step(uint32_t tS, uint8_t* tile, const float* gam,
-                                                 bool first, const float* init, int v,
+                                                 bool first, const float* init, int v, int half,
                                                  uint64_t* bar, __nv_bfloat16* out) {
-    float r0[32], r1[32], r2[32], r3[32];
+    const int k0 = 64 * half;
+    float r0[32], r1[32];
     if (first) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            r0[i] = init ? init[(size_t)(i)*kD + v] : 0.f;
-            r1[i] = init ? init[(size_t)(32 + i) * kD + v] : 0.f;
-            r2[i] = init ? init[(size_t)(64 + i) * kD + v] : 0.f;
-            r3[i] = init ? init[(size_t)(96 + i) * kD + v] : 0.f;
+            r0[i] = init ? init[(size_t)(k0 + i) * kD + v] : 0.f;
+            r1[i] = init ? init[(size_t)(k0 + 32 + i) * kD + v] : 0.f;
         }
     } else {
-        tmem_ld32_nw(tS + 0, r0);
-        tmem_ld32_nw(tS + 32, r1);
-        tmem_ld32_nw(tS + 64, r2);
-        tmem_ld32_nw(tS + 96, r3);
+        tmem_ld32_nw(tS + k0, r0);
+        tmem_ld32_nw(tS + k0 + 32, r1);
         tmem_wait_ld_dep(r0);
         tmem_wait_ld_dep(r1);
-        tmem_wait_ld_dep(r2);
-        tmem_wait_ld_dep(r3);
     }
-    store_row_bf16(tile, v, 0, r0, 1.f);
-    store_row_bf16(tile, v, 32, r1, 1.f);
-    store_row_bf16(tile + 16384, v, 0, r2, 1.f);
-    store_row_bf16(tile + 16384, v, 32, r3, 1.f);
+    uint8_t* kt = tile + 16384 * half;
+    store_row_bf16(kt, v, 0, r0, 1.f);
+    store_row_bf16(kt, v, 32, r1, 1.f);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        r0[i] *= gam[i];
-        r1[i] *= gam[32 + i];
-        r2[i] *= gam[64 + i];
-        r3[i] *= gam[96 + i];
+        r0[i] *= gam[k0 + i];
+        r1[i] *= gam[k0 + 32 + i];
     }
-    tmem_st32_nw(tS + 0, r0);
-    tmem_st32_nw(tS + 32, r1);
-    tmem_st32_nw(tS + 64, r2);
-    tmem_st32_nw(tS + 96, r3);
+    tmem_st32_nw(tS + k0, r0);
+    tmem_st32_nw(tS + k0 + 32, r1);
     tmem_wait_st();
     fence_async_smem();
     tc_fence_before();
     mbar_arrive(bar);
-    if (out) tile_row_to_global(tile, 16384, v, kD, 1.f, out + v, kD);
+    if (out) tile_row_to_global(kt, 16384, v, 0, 64, 1.f, out + (size_t)k0 * kD + v, kD);
 }
 
-// Delta step: 64 columns from TMEM (U - D if U is given) to the bf16
-// K-major operand tile (negated if `neg_tile`), arrive on bar1 and bar2,
-// then the true-sign bf16 values to out[c][v] (row stride kD) if given.
+// Delta step, columns c in [32 half, 32 half + 32) of 64: from TMEM (U - D if
+// U is given) to the bf16 K-major operand tile (negated if `neg_tile`),
+// arrive on bar1 and bar2, then the true-sign bf16 values to out[c][v] (row
+// stride kD) if given.
 __device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile,
                                                  const __nv_bfloat16* U, bool neg_tile, int v,
-                                                 uint64_t* bar1, uint64_t* bar2,
+                                                 int half, uint64_t* bar1, uint64_t* bar2,
                                                  __nv_bfloat16* out) {
-    float d0[32], d1[32];
-    tmem_ld32_nw(tD, d0);
-    tmem_ld32_nw(tD + 32, d1);
+    const int c0 = 32 * half;
+    float d0[32];
+    tmem_ld32_nw(tD + c0, d0);
     tmem_wait_ld_dep(d0);
-    tmem_wait_ld_dep(d1);
     if (U) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            d0[i] = __bfloat162float(U[i * kD + v]) - d0[i];
-            d1[i] = __bfloat162float(U[(32 + i) * kD + v]) - d1[i];
-        }
+        for (int i = 0; i < 32; ++i) d0[i] = __bfloat162float(U[(c0 + i) * kD + v]) - d0[i];
     }
     const float sg = neg_tile ? -1.f : 1.f;
-    store_row_bf16(tile, v, 0, d0, sg);
-    store_row_bf16(tile, v, 32, d1, sg);
+    store_row_bf16(tile, v, c0, d0, sg);
     fence_async_smem();
     tc_fence_before();
     mbar_arrive(bar1);
     mbar_arrive(bar2);
-    if (out) tile_row_to_global(tile, 0, v, kC, sg, out + v, kD);
+    if (out) tile_row_to_global(tile, 0, v, c0, 32, sg, out + v, kD);
 }
 
 struct ChainArgs {
@@ -216,7 +210,7 @@ struct ChainArgs {
     __nv_bfloat16* delta_out;  // [BH*T][V] or null
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kChainThreads, 1)
 chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_kbt,
                  const __grid_constant__ CUtensorMap tm_aqk,
@@ -241,10 +235,10 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 129);
-        mbar_init(&empty[1], 129);
-        mbar_init(bar_S, 128);
-        mbar_init(bar_delta, 128);
+        mbar_init(&empty[0], kChainEpi + 1);
+        mbar_init(&empty[1], kChainEpi + 1);
+        mbar_init(bar_S, kChainEpi);
+        mbar_init(bar_delta, kChainEpi);
         mbar_init(bar_D12, 1);
         mbar_init(bar_D3, 1);
         mbar_init(bar_fin, 1);
@@ -341,7 +335,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         }
     } else {
         // ---------------- epilogue: thread <-> value column v ----------------
-        const int q = warp & 3;
+        const int q = warp & 3, half = (warp - 2) >> 2;
         const int v = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         uint8_t* sS = smem + OFF_S;
@@ -355,7 +349,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             if (!wait_bar_warp(&full[s], (n >> 1) & 1, 7)) return false;
             const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + OFF_GAM);
             chain_state_step(tmem + lane_off + TM_S, sS, gam, n == 0,
-                             a.h0 ? a.h0 + (size_t)bh * kD * kD : nullptr, v, bar_S,
+                             a.h0 ? a.h0 + (size_t)bh * kD * kD : nullptr, v, half, bar_S,
                              a.h_out ? a.h_out + ((size_t)bh * NT + n) * kD * kD : nullptr);
             return true;
         };
@@ -368,7 +362,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             tc_fence_after();
             const __nv_bfloat16* U =
                 reinterpret_cast<const __nv_bfloat16*>(smem + s * STAGE_BYTES + OFF_U);
-            chain_delta_step(tmem + lane_off + TM_W, sDelta, U, false, v, bar_delta, &empty[s],
+            chain_delta_step(tmem + lane_off + TM_W, sDelta, U, false, v, half, bar_delta, &empty[s],
                              a.delta_out ? a.delta_out + ((size_t)bh * a.T + (size_t)n * kC) * kD
                                          : nullptr);
             if (!wait_bar_warp(bar_D3, n & 1, 9)) { ok = false; break; }
@@ -377,7 +371,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 if (!e1(n + 1)) { ok = false; break; }
             } else if (a.ht) {
 #pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
+                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     tmem_ld32(tmem + lane_off + TM_S + cb * 32, r);
                     float* hp = a.ht + ((size_t)bh * kD + cb * 32) * kD + v;
 #pragma unroll
@@ -387,7 +381,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             // E3: output rows of chunk n
             const uint32_t tO = (n & 1) ? TM_O1 : TM_O0;
 #pragma unroll 1
-            for (int cb = 0; a.o && cb < 2; ++cb) {
+            for (int cb = half; a.o && cb < half + 1; ++cb) {
                 tmem_ld32(tmem + lane_off + tO + cb * 32, r);
                 __nv_bfloat16* op =
                     a.o + (((size_t)b * a.T + (size_t)n * kC + cb * 32) * a.HV + hv) * kD + v;
@@ -433,7 +427,7 @@ struct ChainBwdArgs {
     __nv_bfloat16* dd_out;       // [BH*T][V]
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kChainThreads, 1)
 chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kbt,
                  const __grid_constant__ CUtensorMap tm_aqk, ChainBwdArgs a) {
@@ -457,10 +451,10 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 129);
-        mbar_init(&empty[1], 129);
-        mbar_init(bar_S, 128);
-        mbar_init(bar_delta, 128);
+        mbar_init(&empty[0], kChainEpi + 1);
+        mbar_init(&empty[1], kChainEpi + 1);
+        mbar_init(bar_S, kChainEpi);
+        mbar_init(bar_delta, kChainEpi);
         mbar_init(bar_dd, 1);
         mbar_init(bar_D4, 1);
         mbar_init(bar_fin, 1);
@@ -553,7 +547,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             wait_bar(bar_fin, 0, 16);
         }
     } else {
-        const int q = warp & 3;
+        const int q = warp & 3, half = (warp - 2) >> 2;
         const int v = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         uint8_t* sS = smem + OFF_S;
@@ -567,7 +561,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             if (!wait_bar_warp(&full[s], (i >> 1) & 1, 17)) return false;
             const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + RB_GAM);
             chain_state_step(tmem + lane_off + TM2_S, sS, gam, i == 0,
-                             a.dht ? a.dht + (size_t)bh * kD * kD : nullptr, v, bar_S,
+                             a.dht ? a.dht + (size_t)bh * kD * kD : nullptr, v, half, bar_S,
                              a.dh_out + ((size_t)bh * NT + n) * kD * kD);
             return true;
         };
@@ -578,7 +572,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             if (!wait_bar_warp(bar_dd, i & 1, 18)) { ok = false; break; }
             tc_fence_after();
             // -ddelta^T to the operand tile; ddelta (true sign) to dd_out
-            chain_delta_step(tmem + lane_off + TM2_DD, sDelta, nullptr, true, v, bar_delta,
+            chain_delta_step(tmem + lane_off + TM2_DD, sDelta, nullptr, true, v, half, bar_delta,
                              &empty[s], a.dd_out + ((size_t)bh * a.T + (size_t)n * kC) * kD);
             if (!wait_bar_warp(bar_D4, i & 1, 19)) { ok = false; break; }
             tc_fence_after();
@@ -586,7 +580,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 if (!e1(i + 1)) { ok = false; break; }
             } else if (a.dh0) {
 #pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
+                for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     tmem_ld32(tmem + lane_off + TM2_S + cb * 32, r);
                     float* hp = a.dh0 + ((size_t)bh * kD + cb * 32) * kD + v;
 #pragma unroll
@@ -1188,6 +1182,10 @@ constexpr int kLocalTcThreads = 512;
 
 __host__ __device__ constexpr uint32_t right_rel(int R) { return 2048u * (uint32_t)(R * (R + 1)); }
 __host__ __device__ constexpr int pair_idx(int R, int J) { return R * (R + 1) / 2 + J; }
+// fp32 dKb row r (512 bytes) in the assembly, staged in three freed areas
+__host__ __device__ constexpr uint32_t lb_dkb_row(int r) {
+    return r < 32 ? LB_DTV + 512u * r : r < 48 ? LB_T + 512u * (r - 32) : LB_TLO + 512u * (r - 48);
+}
 
 struct LocalTcArgs {
     int T, H, HV, NT, G;
@@ -1494,30 +1492,35 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                          sdesc_mn_sw128(right + right_rel(RR) + kk * 2048, 2048u * (RR + 1)),
                          sdesc_sw128(daq + 4096u * RR + kk * 32), id, kk > 0);
         }
+        // one MMA per block R covers the pairs (R, J <= R): their column
+        // blocks J are consecutive rows of the transposed tile and consecutive
+        // TMEM columns
 #pragma unroll
-        for (int RR = 0; RR < 4; ++RR)
-            for (int J = 0; J <= RR; ++J) {
-                const uint32_t id = idesc_bf16_f32(128, 16) | kAMajorMN;
+        for (int RR = 0; RR < 4; ++RR) {
+            const uint32_t id = idesc_bf16_f32(128, 16 * (RR + 1)) | kAMajorMN;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    mma_bf16(tmem + 256 + 16 * pair_idx(RR, J),
-                             sdesc_mn_sw128(lcol + 4096u * RR + kk * 2048, 16384),
-                             sdesc_sw128(daqt + (RR >> 1) * 8192 + 2048u * J + (RR & 1) * 64 +
-                                         kk * 32),
-                             id, kk > 0);
-            }
+            for (int kk = 0; kk < 2; ++kk)
+                mma_bf16(tmem + 256 + 16 * pair_idx(RR, 0),
+                         sdesc_mn_sw128(lcol + 4096u * RR + kk * 2048, 16384),
+                         sdesc_sw128(daqt + (RR >> 1) * 8192 + (RR & 1) * 64 + kk * 32), id,
+                         kk > 0);
+        }
         mma_commit(bar_m2);
     }
-    // prefetch the assembly's per-element inputs while the MMAs run
-    float pQh[16], pKb[16];
+    // stage the assembly's fp32 inputs dQh (into the [dW; Y] area) and dKb
+    // (rows 0..31 into the dTv area, 32..47 into T, 48..63 into T's low part):
+    // all of them were last read by P4
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-        const int t = 16 * R + u;
-        pQh[u] = a.dQh[(row0 + t) * kD + c];
-        pKb[u] = a.dKb[(row0 + t) * kD + c];
+    for (int e = 0; e < 4; ++e) {
+        const int ch = tid + e * kLocalTcThreads, r = ch >> 5, c4 = (ch & 31) * 4;
+        cp_async16(smem + LB_DWY + r * 512 + c4 * 4, a.dQh + (row0 + r) * kD + c4);
+        cp_async16(smem + lb_dkb_row(r) + c4 * 4, a.dKb + (row0 + r) * kD + c4);
     }
+    cp_async_commit();
     ok = ok && wait_bar_warp(bar_m2, 0, 43);
     tc_fence_after();
+    cp_async_wait_all16();
+    __syncthreads();
 
     // ---- assembly: thread (c, R) for rows t = 16R + u ----
     float dG[16], dbps[16];
@@ -1547,8 +1550,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             const float qr = a.scale * ldt(LB_Q, t);
             const float br = sBeta[t];
             const float dKbeta = dkb[u];
-            const float dQh = pQh[u];
-            const float dKb = pKb[u];
+            const float dQh = *reinterpret_cast<const float*>(smem + LB_DWY + t * 512 + c * 4);
+            const float dKb = *reinterpret_cast<const float*>(smem + lb_dkb_row(t) + c * 4);
             const float sa = sAQ[u] * E, sq = sAQ[16 + u] * E, caq = cAQ[u] * Einv;
             const float dkv = br * dKbeta * eG + dKb * eL + br * sa + caq;
             const float dqs = dQh * eG + sq;
@@ -1804,7 +1807,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         // three roles, timed apart: forward (o), saving forward (o and the
         // chunk-start states), and the backward's recompute (states only)
         TimedLaunch tl(!h_out ? "tc_chain_fwd" : o ? "tc_chain_fwd_save" : "tc_chain_states", s);
-        chain_fwd_kernel<<<BH, 192, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, args);
+        chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, args);
     }
     return launch_status();
 }
@@ -1874,7 +1877,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                                  (int)CHAIN_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
         TimedLaunch tl("tc_chain_bwd", s);
-        chain_bwd_kernel<<<BH, 192, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, a);
+        chain_bwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     // contractions over V
