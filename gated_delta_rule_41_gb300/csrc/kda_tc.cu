@@ -206,7 +206,7 @@ struct ChainArgs {
     const float* h0;    // [BH][K][V] or null
     __nv_bfloat16* o;   // [B,T,HV,V]
     float* ht;          // [BH][K][V] or null
-    __nv_bfloat16* h_out;  // [BH][NT][K][V] or null (states at chunk starts, bf16)
+    __nv_bfloat16* h_out;  // [BH][NT][V][K] or null (states at chunk starts, transposed, bf16)
     __nv_bfloat16* delta_out;  // [BH*T][V] or null
 };
 
@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_kbt,
                  const __grid_constant__ CUtensorMap tm_aqk,
-                 const __grid_constant__ CUtensorMap tm_u, ChainArgs a) {
+                 const __grid_constant__ CUtensorMap tm_u,
+                 const __grid_constant__ CUtensorMap tm_hout, ChainArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -303,6 +304,12 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 if (!wait_bar(&full[s], (n >> 1) & 1, 3)) break;
                 if (!wait_bar(bar_S, n & 1, 4)) break;
                 tc_fence_after();
+                if (a.h_out) {  // S_n^T tile (rows v) as it stands to h_out, by TMA
+                    const int y = (bh * NT + n) * kD;
+                    tma_store_2d(&tm_hout, smem + OFF_S, 0, y);
+                    tma_store_2d(&tm_hout, smem + OFF_S + 16384, 64, y);
+                    bulk_commit_group();
+                }
                 const uint32_t tO = tmem + ((n & 1) ? TM_O1 : TM_O0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -326,9 +333,12 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tO, dD + ((kk * 32) >> 4), dAq0 + so + ((kk * 32) >> 4), idesc64, 1);
+                // the next state step rewrites the tile once D3 completes
+                if (a.h_out) bulk_wait_read_all();
                 mma_commit(bar_D3);
                 mma_commit(&empty[s]);
             }
+            if (a.h_out) bulk_wait_all();
             // all issued MMAs complete before TMEM is released
             mma_commit(bar_fin);
             wait_bar(bar_fin, 0, 6);
@@ -350,7 +360,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + OFF_GAM);
             chain_state_step(tmem + lane_off + TM_S, sS, gam, n == 0,
                              a.h0 ? a.h0 + (size_t)bh * kD * kD : nullptr, v, half, bar_S,
-                             a.h_out ? a.h_out + ((size_t)bh * NT + n) * kD * kD : nullptr);
+                             nullptr);
             return true;
         };
 
@@ -423,14 +433,15 @@ struct ChainBwdArgs {
     const float* gam;
     const float* dht;            // [BH][K][V] or null
     float* dh0;                  // [BH][K][V] or null
-    __nv_bfloat16* dh_out;       // [BH][NT][K][V]
+    __nv_bfloat16* dh_out;       // [BH][NT][V][K] (transposed)
     __nv_bfloat16* dd_out;       // [BH*T][V]
 };
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kbt,
-                 const __grid_constant__ CUtensorMap tm_aqk, ChainBwdArgs a) {
+                 const __grid_constant__ CUtensorMap tm_aqk,
+                 const __grid_constant__ CUtensorMap tm_dhout, ChainBwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -517,6 +528,12 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 if (!wait_bar(&full[s], (i >> 1) & 1, 13)) break;
                 if (!wait_bar(bar_S, i & 1, 14)) break;
                 tc_fence_after();
+                {  // dS^T tile (rows v) of chunk n = NT-1-i to dh_out, by TMA
+                    const int y = (bh * NT + (NT - 1 - i)) * kD;
+                    tma_store_2d(&tm_dhout, smem + OFF_S, 0, y);
+                    tma_store_2d(&tm_dhout, smem + OFF_S + 16384, 64, y);
+                    bulk_commit_group();
+                }
                 // ddelta^T = dS^T Kb^T  (B = Kb tile [64 r][128 k], K-major)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
@@ -540,9 +557,11 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + TM2_S, dD + ((kk * 32) >> 4), dW0 + so + ((kk * 2048) >> 4),
                              id128 | kBMajorMN, 1);
+                bulk_wait_read_all();  // the next state step rewrites the tile
                 mma_commit(bar_D4);
                 mma_commit(&empty[s]);
             }
+            bulk_wait_all();
             mma_commit(bar_fin);
             wait_bar(bar_fin, 0, 16);
         }
@@ -562,7 +581,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + RB_GAM);
             chain_state_step(tmem + lane_off + TM2_S, sS, gam, i == 0,
                              a.dht ? a.dht + (size_t)bh * kD * kD : nullptr, v, half, bar_S,
-                             a.dh_out + ((size_t)bh * NT + n) * kD * kD);
+                             nullptr);
             return true;
         };
 
@@ -613,7 +632,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 constexpr uint32_t G_S0 = 0, G_DS = 32768, G_ODD = 65536, G_DV = 98304, G_T = 131072;
 constexpr uint32_t G_BAR = 139264, G_DBV = G_BAR + 64;
 constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
-constexpr uint32_t GRAD_SMEM = G_DBV + 1280 + 1024;
+constexpr uint32_t GRAD_SMEM = G_DBV + 2304 + 1024;
 constexpr int kGradThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
 
 struct GradArgs {
@@ -636,6 +655,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 2);
     float* dbv_part = reinterpret_cast<float*>(smem + G_DBV);  // [4 lane quadrants][64]
     float* beta_s = dbv_part + 4 * 64;                          // [64]
+    float* dg_part = beta_s + 64;                               // [2 halves][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x, bh = blockIdx.y;
@@ -688,10 +708,13 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16(tmem + 0, sdesc_sw128(s0 + ko), sdesc_sw128(odd + ko), id64, kk > 0);
-                mma_bf16(tmem + 64, sdesc_sw128(s0 + ko), sdesc_sw128(odd + 8192 + ko), id64,
-                         kk > 0);
-                mma_bf16(tmem + 128, sdesc_sw128(ds + ko), sdesc_sw128(dvt + ko), id64, kk > 0);
+                // S0 and dS are stored transposed (rows v): A operands read
+                // MN-major, K = v advancing 16 rows per step
+                const uint64_t as0 = sdesc_mn_sw128(s0 + kk * 2048, 16384);
+                const uint64_t ads = sdesc_mn_sw128(ds + kk * 2048, 16384);
+                mma_bf16(tmem + 0, as0, sdesc_sw128(odd + ko), id64 | kAMajorMN, kk > 0);
+                mma_bf16(tmem + 64, as0, sdesc_sw128(odd + 8192 + ko), id64 | kAMajorMN, kk > 0);
+                mma_bf16(tmem + 128, ads, sdesc_sw128(dvt + ko), id64 | kAMajorMN, kk > 0);
                 mma_bf16(tmem + 256, sdesc_sw128(odd + ko), sdesc_sw128(dvt + ko), id128, kk > 0);
             }
             // D5 = ddelta^T T: ddelta tile read MN-major (v blocks 16 KB apart), T MN-major
@@ -710,25 +733,20 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         float r[32];
         bool ok = wait_bar_warp(bar_tma, 0, 23);
-        // dgam[k] = sum_v dS[k][v] S0[k][v] from the bf16 tiles (independent of the MMAs)
-        if (ok && half == 0) {
+        // dgam[k] = sum_v dS[v][k] S0[v][k] from the bf16 tiles (independent of
+        // the MMAs); thread (k = l, half) sums rows v in [64 half, 64 half + 64)
+        {
             float acc = 0.f;
-#pragma unroll 1
-            for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint32_t off = kb * 16384 + sw128_offset(l, c8 * 8);
-                    const uint4 x = *reinterpret_cast<const uint4*>(smem + G_S0 + off);
-                    const uint4 y = *reinterpret_cast<const uint4*>(smem + G_DS + off);
-                    const __nv_bfloat162* xa = reinterpret_cast<const __nv_bfloat162*>(&x);
-                    const __nv_bfloat162* ya = reinterpret_cast<const __nv_bfloat162*>(&y);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 xf = __bfloat1622float2(xa[u]), yf = __bfloat1622float2(ya[u]);
-                        acc += xf.x * yf.x + xf.y * yf.y;
-                    }
+            if (ok) {
+                const uint32_t kb = (l >> 6) * 16384;
+#pragma unroll 8
+                for (int vv = 0; vv < 64; ++vv) {
+                    const uint32_t off = kb + sw128_offset(64 * half + vv, l & 63);
+                    acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + G_S0 + off)) *
+                           __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + G_DS + off));
                 }
-            a.dgam[(size_t)crow * kD + l] = acc;
+            }
+            dg_part[half * kD + l] = acc;
         }
         ok = ok && wait_bar_warp(bar_mma, 0, 24);
         if (ok) {
@@ -783,6 +801,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (threadIdx.x < kD)
+        a.dgam[(size_t)crow * kD + threadIdx.x] = dg_part[threadIdx.x] + dg_part[kD + threadIdx.x];
     if (threadIdx.x < 64) {
         const int m = threadIdx.x;
         a.dbv[(size_t)row + m] =
@@ -1789,6 +1809,12 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         !make_map(&ma, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true) ||
         !make_map(&mu, w.U2, rows, kD, 128, 64, false))
         return KDA_ERR_CUDA;
+    // chunk-start states, [BH*NT*V][K]: 64-column boxes of 128 rows (a dummy
+    // map over W when no states are kept)
+    CUtensorMap mh;
+    if (!(h_out ? make_map(&mh, h_out, (uint64_t)BH * NT * kD, kD, 64, 128, true)
+                : make_map(&mh, w.W2, rows, kD, 64, 64, true)))
+        return KDA_ERR_CUDA;
     ChainArgs args;
     args.B = d.B;
     args.T = d.T;
@@ -1807,7 +1833,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         // three roles, timed apart: forward (o), saving forward (o and the
         // chunk-start states), and the backward's recompute (states only)
         TimedLaunch tl(!h_out ? "tc_chain_fwd" : o ? "tc_chain_fwd_save" : "tc_chain_states", s);
-        chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, args);
+        chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, args);
     }
     return launch_status();
 }
@@ -1856,8 +1882,9 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     const uint64_t rows = (uint64_t)BH * d.T;
     // reverse chain
     {
-        CUtensorMap mdo, mq, mw, mk, ma;
-        if (!make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
+        CUtensorMap mdo, mq, mw, mk, ma, mdh;
+        if (!make_map(&mdh, w.dh2, (uint64_t)BH * NT * kD, kD, 64, 128, true) ||
+            !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
             !make_map(&mq, w.Q2, rows, kD, 64, 64, true) ||
             !make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
             !make_map(&mk, w.Kb2, rows, kD, 64, 64, true) ||
@@ -1877,7 +1904,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                                  (int)CHAIN_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
         TimedLaunch tl("tc_chain_bwd", s);
-        chain_bwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, a);
+        chain_bwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, mdh, a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     // contractions over V
