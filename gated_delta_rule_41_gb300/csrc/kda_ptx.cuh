@@ -66,6 +66,10 @@ __device__ __forceinline__ void bulk_commit_group() {
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// the sources of all but the most recent committed bulk store group have been read
+__device__ __forceinline__ void bulk_wait_read_but1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // all committed bulk stores are complete
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

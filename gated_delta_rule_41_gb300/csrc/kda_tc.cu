@@ -207,7 +207,7 @@ struct ChainArgs {
     __nv_bfloat16* o;   // [B,T,HV,V]
     float* ht;          // [BH][K][V] or null
     __nv_bfloat16* h_out;  // [BH][NT][V][K] or null (states at chunk starts, transposed, bf16)
-    __nv_bfloat16* delta_out;  // [BH*T][V] or null
+    __nv_bfloat16* delta_out;  // [BH][NT][V][C] or null (transposed); set iff h_out is
 };
 
 __global__ void __launch_bounds__(kChainThreads, 1)
@@ -215,7 +215,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_kbt,
                  const __grid_constant__ CUtensorMap tm_aqk,
                  const __grid_constant__ CUtensorMap tm_u,
-                 const __grid_constant__ CUtensorMap tm_hout, ChainArgs a) {
+                 const __grid_constant__ CUtensorMap tm_hout,
+                 const __grid_constant__ CUtensorMap tm_dout, ChainArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -317,6 +318,10 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
                     mma_bf16(tmem + TM_W, dS + ka, dW0 + so + kb, idesc64, kk > 0);
                 }
+                // the delta step rewrites the delta tile once D12 completes: the
+                // store of the previous delta must have read it (only this
+                // chunk's state store may still be reading)
+                if (a.h_out) bulk_wait_read_but1();
                 mma_commit(bar_D12);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -326,6 +331,10 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 }
                 if (!wait_bar(bar_delta, n & 1, 5)) break;
                 tc_fence_after();
+                if (a.delta_out) {  // delta_n^T tile (rows v) to delta_out, by TMA
+                    tma_store_2d(&tm_dout, smem + OFF_DELTA, 0, (bh * NT + n) * kD);
+                    bulk_commit_group();
+                }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // Kb tile [64 c][128 k] read MN-major (N = k)
                     mma_bf16(tmem + TM_S, dD + ((kk * 32) >> 4), dKb0 + so + ((kk * 2048) >> 4),
@@ -333,12 +342,13 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tO, dD + ((kk * 32) >> 4), dAq0 + so + ((kk * 32) >> 4), idesc64, 1);
-                // the next state step rewrites the tile once D3 completes
-                if (a.h_out) bulk_wait_read_all();
+                // the next state step rewrites the state tile once D3 completes
+                // (this chunk's delta store may still be reading its tile)
+                if (a.h_out) bulk_wait_read_but1();
                 mma_commit(bar_D3);
                 mma_commit(&empty[s]);
             }
-            if (a.h_out) bulk_wait_all();
+            bulk_wait_all();
             // all issued MMAs complete before TMEM is released
             mma_commit(bar_fin);
             wait_bar(bar_fin, 0, 6);
@@ -373,8 +383,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             const __nv_bfloat16* U =
                 reinterpret_cast<const __nv_bfloat16*>(smem + s * STAGE_BYTES + OFF_U);
             chain_delta_step(tmem + lane_off + TM_W, sDelta, U, false, v, half, bar_delta, &empty[s],
-                             a.delta_out ? a.delta_out + ((size_t)bh * a.T + (size_t)n * kC) * kD
-                                         : nullptr);
+                             nullptr);
             if (!wait_bar_warp(bar_D3, n & 1, 9)) { ok = false; break; }
             tc_fence_after();
             if (n + 1 < NT) {
@@ -630,7 +639,8 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 // read by the chunk-local backward kernel; dv is written directly.
 // ===========================================================================
 constexpr uint32_t G_S0 = 0, G_DS = 32768, G_ODD = 65536, G_DV = 98304, G_T = 131072;
-constexpr uint32_t G_BAR = 139264, G_DBV = G_BAR + 64;
+constexpr uint32_t G_DT = 139264;  // delta^T [128 v][64 c], 16 KB
+constexpr uint32_t G_BAR = G_DT + 16384, G_DBV = G_BAR + 64;
 constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
 constexpr uint32_t GRAD_SMEM = G_DBV + 2304 + 1024;
 constexpr int kGradThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
@@ -693,8 +703,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         tma_load_3d(smem + G_ODD + 16384, &tm_do, bar_tma, 64, hv, trow);
         tma_load_2d(smem + G_ODD + 8192, &tm_dd, bar_tma, 0, row);
         tma_load_2d(smem + G_ODD + 24576, &tm_dd, bar_tma, 64, row);
-        tma_load_2d(smem + G_DV, &tm_d, bar_tma, 0, row);
-        tma_load_2d(smem + G_DV + 16384, &tm_d, bar_tma, 64, row);
+        tma_load_2d(smem + G_DT, &tm_d, bar_tma, 0, crow * kD);
         tma_load_3d(smem + G_DV + 8192, &tm_v, bar_tma, 0, hv, trow);
         tma_load_3d(smem + G_DV + 24576, &tm_v, bar_tma, 64, hv, trow);
         tma_load_2d(smem + G_T, &tm_t, bar_tma, 0, crow * kC);
@@ -704,7 +713,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
             const uint32_t s0 = smem_u32(smem + G_S0), ds = smem_u32(smem + G_DS);
             const uint32_t odd = smem_u32(smem + G_ODD), dvt = smem_u32(smem + G_DV);
-            const uint32_t tt = smem_u32(smem + G_T);
+            const uint32_t tt = smem_u32(smem + G_T), dt = smem_u32(smem + G_DT);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -714,8 +723,12 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                 const uint64_t ads = sdesc_mn_sw128(ds + kk * 2048, 16384);
                 mma_bf16(tmem + 0, as0, sdesc_sw128(odd + ko), id64 | kAMajorMN, kk > 0);
                 mma_bf16(tmem + 64, as0, sdesc_sw128(odd + 8192 + ko), id64 | kAMajorMN, kk > 0);
-                mma_bf16(tmem + 128, ads, sdesc_sw128(dvt + ko), id64 | kAMajorMN, kk > 0);
-                mma_bf16(tmem + 256, sdesc_sw128(odd + ko), sdesc_sw128(dvt + ko), id128, kk > 0);
+                // delta is stored transposed (rows v): B operand read MN-major
+                const uint64_t bdt = sdesc_mn_sw128(dt + kk * 2048, 16384);
+                mma_bf16(tmem + 128, ads, bdt, id64 | kAMajorMN | kBMajorMN, kk > 0);
+                mma_bf16(tmem + 256, sdesc_sw128(odd + ko), bdt, id64 | kBMajorMN, kk > 0);
+                mma_bf16(tmem + 320, sdesc_sw128(odd + ko), sdesc_sw128(dvt + 8192 + ko), id64,
+                         kk > 0);
             }
             // D5 = ddelta^T T: ddelta tile read MN-major (v blocks 16 KB apart), T MN-major
 #pragma unroll
@@ -1811,9 +1824,13 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         return KDA_ERR_CUDA;
     // chunk-start states, [BH*NT*V][K]: 64-column boxes of 128 rows (a dummy
     // map over W when no states are kept)
-    CUtensorMap mh;
+    // and delta, [BH*NT*V][C]: one box of 128 rows
+    if ((h_out == nullptr) != (delta_out == nullptr)) return KDA_ERR_INVALID_ARG;
+    CUtensorMap mh, mdl;
     if (!(h_out ? make_map(&mh, h_out, (uint64_t)BH * NT * kD, kD, 64, 128, true)
-                : make_map(&mh, w.W2, rows, kD, 64, 64, true)))
+                : make_map(&mh, w.W2, rows, kD, 64, 64, true)) ||
+        !(delta_out ? make_map(&mdl, delta_out, (uint64_t)BH * NT * kD, kC, 64, 128, true)
+                    : make_map(&mdl, w.W2, rows, kD, 64, 64, true)))
         return KDA_ERR_CUDA;
     ChainArgs args;
     args.B = d.B;
@@ -1833,7 +1850,8 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         // three roles, timed apart: forward (o), saving forward (o and the
         // chunk-start states), and the backward's recompute (states only)
         TimedLaunch tl(!h_out ? "tc_chain_fwd" : o ? "tc_chain_fwd_save" : "tc_chain_states", s);
-        chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, args);
+        chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, mdl,
+                                                               args);
     }
     return launch_status();
 }
@@ -1917,7 +1935,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
             !make_map(&mdh, w.dh2, srows, kD, 64, 128, true) ||
             !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
             !make_map(&mdd, w.dd2, rows, kD, 64, 64, true) ||
-            !make_map(&md, w.d2, rows, kD, 64, 64, true) ||
+            !make_map(&md, w.d2, srows, kC, 64, 128, true) ||
             !make_map_tok(&mv, v, (uint64_t)d.B * d.T, d.HV) ||
             !make_map(&mt, w.T2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
             return KDA_ERR_CUDA;
