@@ -49,18 +49,9 @@ struct SimtWsPtrs {
     float *hs, *dhs, *ddl, *dQh, *dWm, *dKb, *dgam, *dAqk, *dTv, *dbv, *dqh, *dkh;
 };
 void simt_ws_ptrs(const kda_dims& d, int for_bwd, void* ws, SimtWsPtrs* out);
-// Chunk-local backward (kgrad) and the GVA group sum, from the V-contraction
-// results already in the workspace (dQh, dWm, dKb, dgam, dAqk, dTv, dbv, Tm).
-kda_status simt_bwd_tail(const kda_dims& d, void* ws, const void* q, const void* k,
-                         const void* g, const void* beta, void* dq, void* dk, void* dg,
-                         void* dbeta, cudaStream_t s);
 // GVA reduction: dq[b,t,h] = sum over the value heads of group h of dqh (fp32).
 kda_status group_sum_launch(const kda_dims& d, const float* dqh, const float* dkh, void* dq,
                             void* dk, cudaStream_t s);
-// Chunk-local backward for bf16, K = V = 128, chunk 64 (register-tiled fp32).
-kda_status local_bwd_launch(const kda_dims& d, const SimtWsPtrs& p, const void* q,
-                            const void* k, const void* g, const void* beta, void* dq, void* dk,
-                            void* dg, void* dbeta, cudaStream_t s);
 kda_status simt_fwd(const kda_dims& d, const void* q, const void* k, const void* v,
                     const void* g, const void* beta, const float* h0, void* o, float* ht,
                     void* ws, cudaStream_t s);

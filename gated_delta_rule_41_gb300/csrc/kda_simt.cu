@@ -962,17 +962,6 @@ void simt_ws_ptrs(const kda_dims& kd, int for_bwd, void* ws, SimtWsPtrs* o) {
     o->dTv = w.dTv; o->dbv = w.dbv; o->dqh = w.dqh; o->dkh = w.dkh;
 }
 
-kda_status simt_bwd_tail(const kda_dims& kd, void* ws, const void* q, const void* k,
-                         const void* g, const void* beta, void* dq, void* dk, void* dg,
-                         void* dbeta, cudaStream_t s) {
-    const Dims d = make_dims(kd);
-    Ws w;
-    carve(d, 1, static_cast<char*>(ws), &w);
-    if (kd.dtype == KDA_BF16)
-        return simt_tail_t<__nv_bfloat16>(d, w, q, k, g, beta, dq, dk, dg, dbeta, s);
-    return simt_tail_t<float>(d, w, q, k, g, beta, dq, dk, dg, dbeta, s);
-}
-
 kda_status simt_bwd(const kda_dims& kd, const void* q, const void* k, const void* v,
                     const void* g, const void* beta, const float* h0, const void* dout,
                     const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
