@@ -649,7 +649,8 @@ struct GradArgs {
     int T, HV, NT;
     const __nv_bfloat16* beta;  // [B,T,HV]
     __nv_bfloat16* dv;          // [B,T,HV,V]
-    float *dQh, *dWm, *dKb, *dgam, *dAqk, *dTv, *dbv;
+    float *dQh, *dKb, *dgam, *dTv, *dbv;
+    __nv_bfloat16 *dW, *dAqk;  // bf16: the local backward uses them only as MMA operands
 };
 
 __global__ void __launch_bounds__(kGradThreads, 1)
@@ -771,7 +772,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             for (int j = 0; j < 32; ++j) a.dQh[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
             tmem_ld32(tmem + lane_off + 64 + cb * 32, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a.dWm[rb + (size_t)(cb * 32 + j) * kD + l] = -r[j];
+            for (int j = 0; j < 32; ++j)
+                a.dW[rb + (size_t)(cb * 32 + j) * kD + l] = __float2bfloat16_rn(-r[j]);
             tmem_ld32(tmem + lane_off + 128 + cb * 32, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j) a.dKb[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
@@ -780,22 +782,26 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                 const size_t cc = (size_t)crow * kC * kC;
                 const int c4 = (q < 2 ? 0 : 2) + half;
                 tmem_ld32(tmem + lane_off + 256 + c4 * 32, r);
-                float* dst;
-                int i;
-                if (q < 2) {
-                    i = l;
-                    dst = a.dAqk + cc + (size_t)i * kC + c4 * 32;
+                if (q < 2) {  // dAqk row i (bf16), masked to j <= i
+                    const int i = l;
+                    __nv_bfloat16* dst = a.dAqk + cc + (size_t)i * kC + c4 * 32;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = (c4 * 32 + j) <= i ? r[j] : 0.f;
-                } else {
-                    i = l - 64;
-                    dst = a.dTv + cc + (size_t)i * kC + (c4 - 2) * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8)
+                        *reinterpret_cast<uint4*>(dst + j) =
+                            make_uint4(pack_bf16(r[j], r[j + 1]), pack_bf16(r[j + 2], r[j + 3]),
+                                       pack_bf16(r[j + 4], r[j + 5]), pack_bf16(r[j + 6], r[j + 7]));
+                } else {  // dTv row i (fp32), masked to j < i
+                    const int i = l - 64;
+                    float* dst = a.dTv + cc + (size_t)i * kC + (c4 - 2) * 32;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = ((c4 - 2) * 32 + j) < i ? r[j] : 0.f;
-                }
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(dst + j) = make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) =
+                            make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+                }
             }
             // D5: lane = v, columns m = 32*cb .. 32*cb+31
             tmem_ld32(tmem + lane_off + 192 + cb * 32, r);
@@ -839,7 +845,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
 //   (3) T = (I + A)^{-1} (fp32, blocked forward substitution),
 //       W^T = Khat^T (T diag beta)^T, U^T = V^T (T diag beta)^T with Khat and
 //       V read MN-major from their tiles.
-// Writes W, Qh, U, Kb^T, Aqk, T (bf16 operand arrays), T (fp32) and gam.
+// Writes W, Qh, U, Kb, Aqk (bf16 operand arrays), T as bf16 high and low
+// parts (T2 + Tlo reproduce the fp32 T to about 16 bits) and gam.
 // ===========================================================================
 constexpr uint32_t I_K = 0, I_Q = 16384, I_G = 32768, I_V = 49152;   // TMA tiles, 16 KB each
 constexpr uint32_t I_LEFT = 65536;                                   // 128 rows x 128, 32 KB
@@ -867,8 +874,8 @@ struct IntraArgs {
     int T, H, HV, NT;
     float scale;
     const __nv_bfloat16* beta;
-    __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2;
-    float *Tm, *gam;
+    __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2, *Tlo;
+    float* gam;
 };
 
 template <int R>
@@ -1126,12 +1133,13 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         sT[(32 + i0 + 1) * kAS + jj] = -y1;
     }
     __syncthreads();
-    // T (fp32, bf16) to global; T*beta to the B-operand tile
+    // T (bf16 high and low parts) to global; T*beta to the B-operand tile
     for (int idx = tid; idx < kC * kC; idx += kIntraThreads) {
         const int i = idx >> 6, j = idx & 63;
         const float t = sT[i * kAS + j];
-        a.Tm[(size_t)crow * kC * kC + idx] = t;
-        a.T2[(size_t)crow * kC * kC + idx] = __float2bfloat16_rn(t);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(t);
+        a.T2[(size_t)crow * kC * kC + idx] = hi;
+        a.Tlo[(size_t)crow * kC * kC + idx] = __float2bfloat16_rn(t - __bfloat162float(hi));
         st(I_TB + sw128_offset(i, j), t * sBeta[j]);
     }
     fence_async_smem();
@@ -1197,7 +1205,7 @@ constexpr uint32_t LB_K = 0, LB_Q = 16384, LB_G = 32768;     // TMA tiles, read 
 constexpr uint32_t LB_DWY = 49152;    // [dW; Y] 128 rows x 128, 2 k-blocks of 16 KB
 constexpr uint32_t LB_T = 81920;      // T bf16 [64 r][64 m]
 constexpr uint32_t LB_DAQ = 90112;    // [dA_R; dAqk_R] rows 32R + 16s + u, 64 columns j
-constexpr uint32_t LB_DAQT = 106496;  // transposed: rows j, columns t'' = 32R + 16s + u
+// 106496 .. 122880: unused
 constexpr uint32_t LB_RIGHT = 122880; // Right_R tiles, 16(R+1) rows each
 constexpr uint32_t LB_LCOL = 163840;  // [beta k E; qs E] rows 32R + 16s + u, 128 c
 constexpr uint32_t LB_SMALL = 196608; // fp32 small arrays
@@ -1223,7 +1231,7 @@ __host__ __device__ constexpr uint32_t lb_dkb_row(int r) {
 struct LocalTcArgs {
     int T, H, HV, NT, G;
     float scale;
-    const float *Tm, *dW, *dQh, *dKb, *dAqk, *dTv, *dgam, *dbv;
+    const float *dQh, *dKb, *dTv, *dgam, *dbv;
     const __nv_bfloat16 *q, *k, *g, *beta;
     __nv_bfloat16 *dq, *dk, *dg, *dbeta;
     float *dqh, *dkh;
@@ -1232,7 +1240,12 @@ struct LocalTcArgs {
 __global__ void __launch_bounds__(kLocalTcThreads, 1)
 local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_g, LocalTcArgs a) {
+                    const __grid_constant__ CUtensorMap tm_g,
+                    const __grid_constant__ CUtensorMap tm_dw,    // dW bf16 [BH*T][128]
+                    const __grid_constant__ CUtensorMap tm_t,     // T high part [BH*NT*64][64]
+                    const __grid_constant__ CUtensorMap tm_tlo,   // T low part
+                    const __grid_constant__ CUtensorMap tm_daq,   // dAqk bf16, 16-row boxes
+                    LocalTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1258,24 +1271,12 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const size_t cc0 = ((size_t)bh * a.NT + n) * kC * kC;
     const uint32_t lane_off = (uint32_t)((c >> 5) * 32) << 16;
 
-    // fp32 inputs of the build, staged asynchronously (16-byte copies) in
-    // regions the build only writes in its second pass: dW in the Lcol area,
-    // T and dAqk in the Right area.
-    float* stW = reinterpret_cast<float*>(smem + LB_LCOL);          // [64][128]
-    float* stT = reinterpret_cast<float*>(smem + LB_RIGHT);         // [64][64]
-    float* stA = stT + kC * kC;                                     // [64][64]
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int ch = tid + e * kLocalTcThreads;  // 16-byte chunk of dW
-        cp_async16(stW + ch * 4, a.dW + row0 * kD + ch * 4);
-    }
+    // dTv (fp32) staged asynchronously; row i, 16-byte chunk qd lands in chunk
+    // qd ^ (i & 7), so a thread reading its own row's chunks meets no bank
+    // conflict within 8 lanes
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int ch = tid + e * kLocalTcThreads;
-        cp_async16(stT + ch * 4, a.Tm + cc0 + ch * 4);
-        cp_async16(stA + ch * 4, a.dAqk + cc0 + ch * 4);
-        // dTv row i, chunk qd lands in chunk qd ^ (i & 7): a thread reading
-        // its own row's chunks then meets no bank conflict within 8 lanes
         const int i = ch >> 4, qd = ch & 15;
         cp_async16(sDtv + i * kC + ((qd ^ (i & 7)) << 2), a.dTv + cc0 + ch * 4);
     }
@@ -1301,13 +1302,24 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     if (tid == 0) {
-        mbar_arrive_expect_tx(bar_tma, 3 * 16384);
+        // k, q, g tiles; dW into the top half of [dW; Y]; T (hi, lo) tiles;
+        // dAqk rows into the rows 32R + 16 + u of [dA; dAqk]
+        mbar_arrive_expect_tx(bar_tma, 3 * 16384 + 16384 + 2 * 8192 + 8192);
         tma_load_3d(smem + LB_K, &tm_k, bar_tma, 0, h, trow);
         tma_load_3d(smem + LB_K + 8192, &tm_k, bar_tma, 64, h, trow);
         tma_load_3d(smem + LB_Q, &tm_q, bar_tma, 0, h, trow);
         tma_load_3d(smem + LB_Q + 8192, &tm_q, bar_tma, 64, h, trow);
         tma_load_3d(smem + LB_G, &tm_g, bar_tma, 0, hv, trow);
         tma_load_3d(smem + LB_G + 8192, &tm_g, bar_tma, 64, hv, trow);
+        tma_load_2d(smem + LB_DWY, &tm_dw, bar_tma, 0, (int)row0);
+        tma_load_2d(smem + LB_DWY + 16384, &tm_dw, bar_tma, 64, (int)row0);
+        const int crow64 = (bh * a.NT + n) * kC;
+        tma_load_2d(smem + LB_T, &tm_t, bar_tma, 0, crow64);
+        tma_load_2d(smem + LB_TLO, &tm_tlo, bar_tma, 0, crow64);
+#pragma unroll
+        for (int RR = 0; RR < 4; ++RR)
+            tma_load_2d(smem + LB_DAQ + (32 * RR + 16) * 128, &tm_daq, bar_tma, 0,
+                        crow64 + 16 * RR);
     }
     bool ok = wait_bar_warp(bar_tma, 0, 41);
 
@@ -1347,25 +1359,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
     const float eGbR = __expf(Gb[R]), eLbR = __expf(Glast - Gb[R]);
 
-    // ---- build bf16 operands: pass 1 from the staged fp32 inputs ----
-    cp_async_wait_all16();
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-        const int r = 16 * R + u;
-        st(LB_DWY + (c >> 6) * 16384 + sw128_offset(r, cc), stW[r * kD + c]);
-        if (c < kC) {
-            const float t = stT[r * kC + c];
-            st(LB_T + sw128_offset(r, c), t);
-            st(LB_TLO + sw128_offset(r, c), t - __bfloat162float(__float2bfloat16_rn(t)));
-            const float dq_ = stA[r * kC + c];
-            st(LB_DAQ + sw128_offset(32 * R + 16 + u, c), dq_);
-            const int t2 = 32 * R + 16 + u;
-            st(LB_DAQT + (t2 >> 6) * 8192 + sw128_offset(c, t2 & 63), dq_);
-        }
-    }
-    __syncthreads();
-    // ---- pass 2: Y, Right_R, Lcol (overwrites the staging areas) ----
+    // ---- build bf16 operands: Y, Right_R, Lcol ----
     {
         float F[4];
 #pragma unroll
@@ -1393,6 +1387,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             st(LB_LCOL + cb16 + sw128_offset(32 * R + 16 + u, cc), qv * E);
         }
     }
+    cp_async_wait_all16();
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1505,7 +1500,6 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int j = 16 * R + e;
             const float v = j < i ? -r16[e] : 0.f;
             st(LB_DAQ + sw128_offset(t2, j), v);
-            st(LB_DAQT + (t2 >> 6) * 8192 + sw128_offset(j, t2 & 63), v);
         }
     }
     fence_async_smem();
@@ -1515,7 +1509,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     // ---- P5 (row side), P6 (column side) ----
     if (tid == 0 && ok) {
-        const uint32_t daq = smem_u32(smem + LB_DAQ), daqt = smem_u32(smem + LB_DAQT);
+        const uint32_t daq = smem_u32(smem + LB_DAQ);
         const uint32_t right = smem_u32(smem + LB_RIGHT), lcol = smem_u32(smem + LB_LCOL);
 #pragma unroll
         for (int RR = 0; RR < 4; ++RR) {
@@ -1525,18 +1519,17 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                          sdesc_mn_sw128(right + right_rel(RR) + kk * 2048, 2048u * (RR + 1)),
                          sdesc_sw128(daq + 4096u * RR + kk * 32), id, kk > 0);
         }
-        // one MMA per block R covers the pairs (R, J <= R): their column
-        // blocks J are consecutive rows of the transposed tile and consecutive
-        // TMEM columns
+        // one MMA per block R covers the pairs (R, J <= R): B is [dA; dAqk]
+        // read MN-major (N = its 64 columns j, K = its rows 32R..32R+31), so
+        // pair (R, J) lands in TMEM columns 256 + 64 R + 16 J (J > R unused)
 #pragma unroll
         for (int RR = 0; RR < 4; ++RR) {
-            const uint32_t id = idesc_bf16_f32(128, 16 * (RR + 1)) | kAMajorMN;
+            const uint32_t id = idesc_bf16_f32(128, 64) | kAMajorMN | kBMajorMN;
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
-                mma_bf16(tmem + 256 + 16 * pair_idx(RR, 0),
+                mma_bf16(tmem + 256 + 64 * RR,
                          sdesc_mn_sw128(lcol + 4096u * RR + kk * 2048, 16384),
-                         sdesc_sw128(daqt + (RR >> 1) * 8192 + (RR & 1) * 64 + kk * 32), id,
-                         kk > 0);
+                         sdesc_mn_sw128(daq + 4096u * RR + kk * 2048, 8192), id, kk > 0);
         }
         mma_commit(bar_m2);
     }
@@ -1568,7 +1561,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int u = 0; u < 16; ++u) cAQ[u] = 0.f;
         for (int Rp = R; Rp < 4; ++Rp) {
             float d6[16];
-            tmem_ld16(tmem + lane_off + 256 + 16 * pair_idx(Rp, R), d6);
+            tmem_ld16(tmem + lane_off + 256 + 64 * Rp + 16 * R, d6);
             const float f = Rp > R ? __expf(Gb[Rp] - Gb[R]) : 1.f;
 #pragma unroll
             for (int u = 0; u < 16; ++u) cAQ[u] += f * d6[u];
@@ -1696,7 +1689,7 @@ bool make_map_tok(CUtensorMap* m, const void* ptr, uint64_t BT, uint64_t heads) 
 
 struct TcWs {
     char* simt;  // SIMT workspace (fp32 quantities)
-    __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2;  // chain operands, T
+    __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2, *Tlo2;  // chain operands, T (hi, lo)
     __nv_bfloat16 *h2, *d2, *dh2, *dd2;              // backward only
 };
 
@@ -1717,6 +1710,7 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     x.Kb2 = bf(BH * T * kD);
     x.Aqk2 = bf(BH * NT * kC * kC);
     x.T2 = bf(BH * NT * kC * kC);
+    x.Tlo2 = bf(BH * NT * kC * kC);
     if (for_bwd) {
         x.h2 = bf(BH * NT * kD * kD);
         x.d2 = bf(BH * T * kD);
@@ -1753,7 +1747,7 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     a.Kb2 = w.Kb2;
     a.Aqk2 = w.Aqk2;
     a.T2 = w.T2;
-    a.Tm = p.Tm;
+    a.Tlo = w.Tlo2;
     a.gam = p.gam;
     if (cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)INTRA_SMEM) != cudaSuccess)
@@ -1766,13 +1760,17 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     return launch_status();
 }
 
-kda_status run_local_bwd_tc(const kda_dims& d, const SimtWsPtrs& p, const void* q,
-                            const void* k, const void* g, const void* beta, void* dq, void* dk,
-                            void* dg, void* dbeta, cudaStream_t s) {
+kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& p,
+                            const void* q, const void* k, const void* g, const void* beta,
+                            void* dq, void* dk, void* dg, void* dbeta, cudaStream_t s) {
     const uint64_t BT = (uint64_t)d.B * d.T;
-    CUtensorMap mk, mq, mg;
+    const uint64_t rows = (uint64_t)d.B * d.HV * d.T;  // [BH*T] and [BH*NT*64] alike
+    CUtensorMap mk, mq, mg, mdw, mt, mtl, mda;
     if (!make_map_tok(&mk, k, BT, d.H) || !make_map_tok(&mq, q, BT, d.H) ||
-        !make_map_tok(&mg, g, BT, d.HV))
+        !make_map_tok(&mg, g, BT, d.HV) || !make_map(&mdw, p.dWm, rows, kD, 64, 64, true) ||
+        !make_map(&mt, w.T2, rows, kC, 64, 64, true) ||
+        !make_map(&mtl, w.Tlo2, rows, kC, 64, 64, true) ||
+        !make_map(&mda, p.dAqk, rows, kC, 64, 16, true))
         return KDA_ERR_CUDA;
     LocalTcArgs a;
     a.T = d.T;
@@ -1781,11 +1779,8 @@ kda_status run_local_bwd_tc(const kda_dims& d, const SimtWsPtrs& p, const void* 
     a.NT = d.T / kC;
     a.G = d.HV / d.H;
     a.scale = d.scale;
-    a.Tm = p.Tm;
-    a.dW = p.dWm;
     a.dQh = p.dQh;
     a.dKb = p.dKb;
-    a.dAqk = p.dAqk;
     a.dTv = p.dTv;
     a.dgam = p.dgam;
     a.dbv = p.dbv;
@@ -1805,7 +1800,7 @@ kda_status run_local_bwd_tc(const kda_dims& d, const SimtWsPtrs& p, const void* 
     {
         TimedLaunch tl("tc_local_bwd", s);
         local_bwd_tc_kernel<<<dim3(d.T / kC, d.B * d.HV), kLocalTcThreads, LOCAL_TC_SMEM, s>>>(
-            mk, mq, mg, a);
+            mk, mq, mg, mdw, mt, mtl, mda, a);
     }
     return launch_status();
 }
@@ -1946,10 +1941,10 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.beta = static_cast<const __nv_bfloat16*>(beta);
         a.dv = static_cast<__nv_bfloat16*>(dv);
         a.dQh = p.dQh;
-        a.dWm = p.dWm;
+        a.dW = reinterpret_cast<__nv_bfloat16*>(p.dWm);  // bf16 in the fp32 array's space
         a.dKb = p.dKb;
         a.dgam = p.dgam;
-        a.dAqk = p.dAqk;
+        a.dAqk = reinterpret_cast<__nv_bfloat16*>(p.dAqk);
         a.dTv = p.dTv;
         a.dbv = p.dbv;
         if (cudaFuncSetAttribute(grad_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1961,7 +1956,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     if ((st = launch_status()) != KDA_OK) return st;
     SimtWsPtrs p;
     simt_ws_ptrs(d, 1, w.simt, &p);
-    if ((st = run_local_bwd_tc(d, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
+    if ((st = run_local_bwd_tc(d, w, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
     if (d.HV == d.H) return KDA_OK;
     return group_sum_launch(d, p.dqh, p.dkh, dq, dk, s);
 }
