@@ -643,7 +643,10 @@ constexpr uint32_t G_DT = 139264;  // delta^T [128 v][64 c], 16 KB
 constexpr uint32_t G_BAR = G_DT + 16384, G_DBV = G_BAR + 64;
 constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
 constexpr uint32_t GRAD_SMEM = G_DBV + 2304 + 1024;
-constexpr int kGradThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
+// 8 warps (two per SM sub-partition, so up to 255 registers a thread): lane 0
+// of warp 0 issues the TMA copies, lane 0 of warp 1 the MMAs, then all eight
+// run the epilogue
+constexpr int kGradThreads = 256;
 
 struct GradArgs {
     int T, HV, NT;
@@ -708,7 +711,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         tma_load_3d(smem + G_DV + 8192, &tm_v, bar_tma, 0, hv, trow);
         tma_load_3d(smem + G_DV + 24576, &tm_v, bar_tma, 64, hv, trow);
         tma_load_2d(smem + G_T, &tm_t, bar_tma, 0, crow * kC);
-    } else if (warp == 1 && lane == 0) {
+    }
+    if (warp == 1 && lane == 0) {
         if (wait_bar(bar_tma, 0, 21)) {
             tc_fence_after();
             const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
@@ -738,11 +742,13 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                          sdesc_mn_sw128(tt + kk * 2048, 8192), id64 | kAMajorMN | kBMajorMN,
                          kk > 0);
             mma_commit(bar_mma);
-            wait_bar(bar_mma, 0, 22);
         }
-    } else if (warp >= 2) {
-        // 8 epilogue warps: two per TMEM lane quadrant, splitting the columns.
-        const int q = warp & 3, half = (warp - 2) >> 2;
+    }
+    __syncwarp();
+    {
+        // all 8 warps, two per TMEM lane quadrant, splitting the columns (lane
+        // 0 of warps 0 and 1 issued the copies and the MMAs above)
+        const int q = warp & 3, half = warp >> 2;
         const int l = q * 32 + lane;  // TMEM lane: k for D1-D3, row for D4, v for D5
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         float r[32];
