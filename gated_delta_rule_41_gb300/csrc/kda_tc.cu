@@ -864,8 +864,34 @@ constexpr uint32_t I_A = I_TB + 8192;                                // fp32 [64
 constexpr uint32_t I_T = I_A + 64 * kAS * 4;                         // fp32 [64][kAS]
 constexpr uint32_t I_BETA = I_T + 64 * kAS * 4;                      // fp32 [64]
 constexpr uint32_t I_GX = I_BETA + 256;                              // fp32 [2][4][128]
-constexpr uint32_t I_BAR = I_GX + 4096;
+constexpr uint32_t I_SG = I_GX + 4096;     // G fp32 [64][128] for the operand build
+constexpr uint32_t I_SC = I_SG + 32768;    // exp(G_b), exp(G_last - G_b) [4][128]; F [6][128]
+constexpr uint32_t I_BAR = I_SC + 14 * 512;
 constexpr uint32_t INTRA_SMEM = I_BAR + 64 + 1024;
+static_assert(INTRA_SMEM <= 232448, "intra kernel exceeds the per-CTA shared memory limit");
+
+// slot of F(R, Rr) = exp(G_b(Rr) - G_b(R)) for Rr > R among the six pairs
+__host__ __device__ constexpr int f_slot(int R, int Rr) { return R * (7 - R) / 2 + (Rr - R - 1); }
+
+__device__ __forceinline__ void ld8f(const float* p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                      pack_bf16(x[6], x[7]));
+}
+__device__ __forceinline__ void unpack8(const uint4 v, float (&x)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
 constexpr int kIntraThreads = 512;
 constexpr uint32_t INTRA_TX = 4 * 16384;
 
@@ -916,6 +942,10 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     float* sBeta = reinterpret_cast<float*>(smem + I_BETA);
     float* sGtot = reinterpret_cast<float*>(smem + I_GX);   // [4][128] block sums
     float* sGb = sGtot + 4 * kD;                             // [4][128] G at block starts
+    float* sG = reinterpret_cast<float*>(smem + I_SG);      // [64][128]
+    float* sEGb = reinterpret_cast<float*>(smem + I_SC);    // [4][128]
+    float* sELb = sEGb + 4 * kD;                             // [4][128]
+    float* sF = sELb + 4 * kD;                               // [6][128]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x, bh = blockIdx.y;
@@ -981,41 +1011,79 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         Glast += t;
     }
 #pragma unroll
-    for (int u = 0; u < 16; ++u) G[u] += off;
+    for (int u = 0; u < 16; ++u) {
+        G[u] += off;
+        sG[(16 * R + u) * kD + c] = G[u];
+    }
     sGb[R * kD + c] = G[0];
     __syncthreads();
-    float Gb[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
-    if (R == 3) a.gam[(size_t)crow * kD + c] = __expf(Glast);
-
-    // ---- operands for rows 16R..16R+15: Left, Right_Rr (Rr >= R), Khat; Qh, Kb ----
     {
-        const float eGb = __expf(Gb[R]);            // exp(G_b)
-        const float eLb = __expf(Glast - Gb[R]);    // exp(G_last - G_b)
-        float F[4];                                 // exp(G_b(Rr) - G_b(R)), Rr >= R
+        float Gb[4];
 #pragma unroll
-        for (int Rr = 0; Rr < 4; ++Rr) F[Rr] = Rr > R ? __expf(Gb[Rr] - Gb[R]) : 1.f;
+        for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
+        if (R == 3) a.gam[(size_t)crow * kD + c] = __expf(Glast);
+        // per (block, channel) factors of the build
+        sEGb[R * kD + c] = __expf(Gb[R]);               // exp(G_b)
+        sELb[R * kD + c] = __expf(Glast - Gb[R]);       // exp(G_last - G_b)
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int r = 16 * R + u;
-            const float E = __expf(G[u] - Gb[R]);        // <= 1
-            const float Einv = __expf(Gb[R] - G[u]);     // in [1, e^75]
-            const float kv = ld(I_K, r), qv = a.scale * ld(I_Q, r);
-            st(I_LEFT + (c >> 6) * 16384 + sw128_offset(32 * R + u, cc), kv * E);
-            st(I_LEFT + (c >> 6) * 16384 + sw128_offset(32 * R + 16 + u, cc), qv * E);
-            const float ke = kv * Einv;
+        for (int Rr = 0; Rr < 4; ++Rr)
+            if (Rr > R) sF[f_slot(R, Rr) * kD + c] = __expf(Gb[Rr] - Gb[R]);
+    }
+    __syncthreads();
+
+    // ---- operands: Left, Right_Rr (Rr >= R), Khat in smem; Qh, Kb to global.
+    // A unit is one 8-channel chunk (16 bytes of bf16) of one row; thread t
+    // takes chunk t % 16 of rows t / 16 and 63 - t / 16, whose blocks R and
+    // 3 - R give every thread five Right copies. ----
+    {
+        const int oct = tid & 15, kb = oct >> 3, ch = oct & 7, c0 = oct * 8;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const int r = pass == 0 ? (tid >> 4) : 63 - (tid >> 4);
+            const int Rb = r >> 4, u = r & 15;
+            // rows r, 32 Rb + u and 32 Rb + 16 + u share r mod 8, hence the swizzle
+            const uint32_t co = (uint32_t)((ch ^ (r & 7)) << 4);
+            float g8[8], gb8[8], egb[8], elb[8], kv[8], qv[8], E[8], Ei[8], x[8];
+            ld8f(sG + r * kD + c0, g8);
+            ld8f(sGb + Rb * kD + c0, gb8);
+            ld8f(sEGb + Rb * kD + c0, egb);
+            ld8f(sELb + Rb * kD + c0, elb);
+            unpack8(*reinterpret_cast<const uint4*>(smem + I_K + kb * 8192 + r * 128 + co), kv);
+            unpack8(*reinterpret_cast<const uint4*>(smem + I_Q + kb * 8192 + r * 128 + co), qv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                qv[e] *= a.scale;
+                E[e] = __expf(g8[e] - gb8[e]);    // <= 1
+                Ei[e] = __expf(gb8[e] - g8[e]);   // in [1, e^75]
+            }
+            uint8_t* lk = smem + I_LEFT + kb * 16384 + (32 * Rb + u) * 128 + co;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = kv[e] * E[e];
+            *reinterpret_cast<uint4*>(lk) = pack8(x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = qv[e] * E[e];
+            *reinterpret_cast<uint4*>(lk + 16 * 128) = pack8(x);
 #pragma unroll
             for (int Rr = 0; Rr < 4; ++Rr) {
-                if (Rr < R) continue;
-                const uint32_t rows = 16u * (Rr + 1);
-                st(right_off(Rr) + (c >> 6) * (rows * 128u) + sw128_offset(r, cc), ke * F[Rr]);
+                if (Rr < Rb) continue;
+                float f8[8];
+                if (Rr > Rb) ld8f(sF + f_slot(Rb, Rr) * kD + c0, f8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = kv[e] * Ei[e] * (Rr > Rb ? f8[e] : 1.f);
+                *reinterpret_cast<uint4*>(smem + right_off(Rr) + kb * (16u * (Rr + 1) * 128u) +
+                                          r * 128 + co) = pack8(x);
             }
-            const float eG = eGb * E;                    // exp(G_r)
-            a.Q2[((size_t)row0 + r) * kD + c] = __float2bfloat16_rn(qv * eG);
-            a.Kb2[((size_t)row0 + r) * kD + c] = __float2bfloat16_rn(kv * eLb * Einv);
-            // Khat overwrites g's slot of this thread's own element (g already consumed)
-            st(I_KHAT + kbo + sw128_offset(r, cc), kv * eG);
+            const size_t go = ((size_t)row0 + r) * kD + c0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = qv[e] * egb[e] * E[e];        // qs exp(G)
+            *reinterpret_cast<uint4*>(a.Q2 + go) = pack8(x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = kv[e] * elb[e] * Ei[e];       // k exp(G_last - G)
+            *reinterpret_cast<uint4*>(a.Kb2 + go) = pack8(x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = kv[e] * egb[e] * E[e];        // Khat = k exp(G)
+            // Khat overwrites the consumed g tile
+            *reinterpret_cast<uint4*>(smem + I_KHAT + kb * 8192 + r * 128 + co) = pack8(x);
         }
     }
     fence_async_smem();
