@@ -138,12 +138,13 @@ __device__ __forceinline__ void tile_row_to_global(const uint8_t* tile, uint32_t
 
 // State step, columns k in [64 half, 64 half + 64): S^T (lane v) from TMEM --
 // or, for the first chunk, from `init` ([K][V] fp32, may be null = zeros) --
-// to k-block `half` of the bf16 K-major operand tile; the TMEM copy is scaled
-// by gam (per column k); arrive on `bar`; then, off the critical path, the
-// bf16 state to out[k][v].
+// to k-block `half` of the bf16 K-major operand tile, then arrive on
+// `bar_tile` (the products that read the tile may start); then the TMEM copy
+// is scaled by gam (per column k) and stored back, and the thread arrives on
+// `bar_tmem` (the products that accumulate into it may start).
 __device__ __forceinline__ void chain_state_step(uint32_t tS, uint8_t* tile, const float* gam,
                                                  bool first, const float* init, int v, int half,
-                                                 uint64_t* bar, __nv_bfloat16* out) {
+                                                 uint64_t* bar_tile, uint64_t* bar_tmem) {
     const int k0 = 64 * half;
     float r0[32], r1[32];
     if (first) {
@@ -161,6 +162,9 @@ __device__ __forceinline__ void chain_state_step(uint32_t tS, uint8_t* tile, con
     uint8_t* kt = tile + 16384 * half;
     store_row_bf16(kt, v, 0, r0, 1.f);
     store_row_bf16(kt, v, 32, r1, 1.f);
+    fence_async_smem();
+    tc_fence_before();  // earlier TMEM reads of this thread precede the MMAs it releases
+    mbar_arrive(bar_tile);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         r0[i] *= gam[k0 + i];
@@ -169,10 +173,8 @@ __device__ __forceinline__ void chain_state_step(uint32_t tS, uint8_t* tile, con
     tmem_st32_nw(tS + k0, r0);
     tmem_st32_nw(tS + k0 + 32, r1);
     tmem_wait_st();
-    fence_async_smem();
     tc_fence_before();
-    mbar_arrive(bar);
-    if (out) tile_row_to_global(kt, 16384, v, 0, 64, 1.f, out + (size_t)k0 * kD + v, kD);
+    mbar_arrive(bar_tmem);
 }
 
 // Delta step, columns c in [32 half, 32 half + 32) of 64: from TMEM (U - D if
@@ -227,7 +229,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     uint64_t* bar_D12 = full + 6;
     uint64_t* bar_D3 = full + 7;
     uint64_t* bar_fin = full + 8;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 9);
+    uint64_t* bar_Sx = full + 9;   // state rescaled in TMEM
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 10);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
@@ -244,6 +247,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         mbar_init(bar_D12, 1);
         mbar_init(bar_D3, 1);
         mbar_init(bar_fin, 1);
+        mbar_init(bar_Sx, kChainEpi);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -335,6 +339,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     tma_store_2d(&tm_dout, smem + OFF_DELTA, 0, (bh * NT + n) * kD);
                     bulk_commit_group();
                 }
+                if (!wait_bar(bar_Sx, n & 1, 10)) break;  // S^T rescaled by gam in TMEM
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // Kb tile [64 c][128 k] read MN-major (N = k)
                     mma_bf16(tmem + TM_S, dD + ((kk * 32) >> 4), dKb0 + so + ((kk * 2048) >> 4),
@@ -370,8 +376,18 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + OFF_GAM);
             chain_state_step(tmem + lane_off + TM_S, sS, gam, n == 0,
                              a.h0 ? a.h0 + (size_t)bh * kD * kD : nullptr, v, half, bar_S,
-                             nullptr);
+                             bar_Sx);
             return true;
+        };
+
+        // E3: output rows of chunk m (complete once D3 of chunk m has fired)
+        auto o_out = [&](int m) {
+            const uint32_t tO = (m & 1) ? TM_O1 : TM_O0;
+            tmem_ld32(tmem + lane_off + tO + half * 32, r);
+            __nv_bfloat16* op =
+                a.o + (((size_t)b * a.T + (size_t)m * kC + half * 32) * a.HV + hv) * kD + v;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) op[(size_t)i * a.HV * kD] = __float2bfloat16_rn(r[i]);
         };
 
         ok = e1(0);
@@ -384,6 +400,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 reinterpret_cast<const __nv_bfloat16*>(smem + s * STAGE_BYTES + OFF_U);
             chain_delta_step(tmem + lane_off + TM_W, sDelta, U, false, v, half, bar_delta, &empty[s],
                              nullptr);
+            // the previous chunk's output while this chunk's state update runs
+            if (a.o && n > 0) o_out(n - 1);
             if (!wait_bar_warp(bar_D3, n & 1, 9)) { ok = false; break; }
             tc_fence_after();
             if (n + 1 < NT) {
@@ -397,18 +415,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     for (int i = 0; i < 32; ++i) hp[(size_t)i * kD] = r[i];
                 }
             }
-            // E3: output rows of chunk n
-            const uint32_t tO = (n & 1) ? TM_O1 : TM_O0;
-#pragma unroll 1
-            for (int cb = half; a.o && cb < half + 1; ++cb) {
-                tmem_ld32(tmem + lane_off + tO + cb * 32, r);
-                __nv_bfloat16* op =
-                    a.o + (((size_t)b * a.T + (size_t)n * kC + cb * 32) * a.HV + hv) * kD + v;
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    op[(size_t)i * a.HV * kD] = __float2bfloat16_rn(r[i]);
-            }
         }
+        if (ok && a.o) o_out(NT - 1);
         (void)ok;
     }
 
@@ -461,7 +469,8 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
     uint64_t* bar_dd = full + 6;
     uint64_t* bar_D4 = full + 7;
     uint64_t* bar_fin = full + 8;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 9);
+    uint64_t* bar_Sx = full + 9;   // state rescaled in TMEM
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 10);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
@@ -478,6 +487,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
         mbar_init(bar_dd, 1);
         mbar_init(bar_D4, 1);
         mbar_init(bar_fin, 1);
+        mbar_init(bar_Sx, kChainEpi);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -554,6 +564,8 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                     mma_bf16(tmem + TM2_DD, dDO0 + so + ((kk * 2048) >> 4),
                              dAq0 + so + ((kk * 2048) >> 4), id64 | kAMajorMN | kBMajorMN, 1);
                 mma_commit(bar_dd);
+                if (!wait_bar(bar_Sx, i & 1, 20)) break;  // dS^T rescaled by gam in TMEM
+                tc_fence_after();
                 // dS^T += dO^T Qh
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -590,7 +602,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + RB_GAM);
             chain_state_step(tmem + lane_off + TM2_S, sS, gam, i == 0,
                              a.dht ? a.dht + (size_t)bh * kD * kD : nullptr, v, half, bar_S,
-                             nullptr);
+                             bar_Sx);
             return true;
         };
 
