@@ -1219,14 +1219,23 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         sT[(32 + i0 + 1) * kAS + jj] = -y1;
     }
     __syncthreads();
-    // T (bf16 high and low parts) to global; T*beta to the B-operand tile
-    for (int idx = tid; idx < kC * kC; idx += kIntraThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        const float t = sT[i * kAS + j];
-        const __nv_bfloat16 hi = __float2bfloat16_rn(t);
-        a.T2[(size_t)crow * kC * kC + idx] = hi;
-        a.Tlo[(size_t)crow * kC * kC + idx] = __float2bfloat16_rn(t - __bfloat162float(hi));
-        st(I_TB + sw128_offset(i, j), t * sBeta[j]);
+    // T (bf16 high and low parts) to global; T*beta to the B-operand tile.
+    // Thread t takes columns 8 (t % 8) .. + 7 of row t / 8.
+    {
+        const int i = tid >> 3, ch = tid & 7, j0 = ch * 8;
+        float t8[8], b8[8], x[8];
+        ld8f(sT + i * kAS + j0, t8);
+        ld8f(sBeta + j0, b8);
+        const uint4 hi = pack8(t8);
+        unpack8(hi, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = t8[e] - x[e];
+        const size_t go = (size_t)crow * kC * kC + (size_t)i * kC + j0;
+        *reinterpret_cast<uint4*>(a.T2 + go) = hi;
+        *reinterpret_cast<uint4*>(a.Tlo + go) = pack8(x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = t8[e] * b8[e];
+        *reinterpret_cast<uint4*>(smem + I_TB + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8(x);
     }
     fence_async_smem();
     tc_fence_before();
@@ -1445,11 +1454,9 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
     const float eGbR = __expf(Gb[R]), eLbR = __expf(Glast - Gb[R]);
 
-    // ---- build bf16 operands: Y, Right_R, Lcol ----
+    // ---- build bf16 operands: Y, Right_R (own block; the copies for later
+    // blocks follow while P1/P2 run), Lcol ----
     {
-        float F[4];
-#pragma unroll
-        for (int Rr = 0; Rr < 4; ++Rr) F[Rr] = Rr > R ? __expf(Gb[Rr] - Gb[R]) : 1.f;
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             const int r = 16 * R + u;
@@ -1459,15 +1466,9 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             const uint32_t cb16 = (c >> 6) * 16384;
             // Y rows of [dW; Y]
             st(LB_DWY + cb16 + sw128_offset(64 + r, cc), br * kv * eGbR * E);
-            // Right_Rr (Rr >= R)
-            const float ke = kv * Einv;
-#pragma unroll
-            for (int Rr = 0; Rr < 4; ++Rr) {
-                if (Rr < R) continue;
-                const uint32_t rows = 16u * (Rr + 1);
-                st(LB_RIGHT + right_rel(Rr) + (c >> 6) * (rows * 128u) + sw128_offset(r, cc),
-                   ke * F[Rr]);
-            }
+            // Right_R (this thread's block only)
+            st(LB_RIGHT + right_rel(R) + (c >> 6) * (16u * (R + 1) * 128u) + sw128_offset(r, cc),
+               kv * Einv);
             // Lcol rows 32R + u (beta k E) and 32R + 16 + u (qs E)
             st(LB_LCOL + cb16 + sw128_offset(32 * R + u, cc), br * kv * E);
             st(LB_LCOL + cb16 + sw128_offset(32 * R + 16 + u, cc), qv * E);
@@ -1493,6 +1494,26 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             mma_bf16(tmem + 64, sdesc_mn_sw128(dwy + kk * 2048, 16384),
                      sdesc_mn_sw128(tt + kk * 2048, 8192), id64 | kAMajorMN | kBMajorMN, kk > 0);
         mma_commit(bar_m1);
+    }
+    // Right_Rr rows of block R for Rr > R: Right_R scaled by exp(G_b(Rr) - G_b(R)),
+    // 16-byte units (6 block pairs x 16 rows x 16 chunks) spread over all
+    // threads while P1/P2 run
+#pragma unroll 1
+    for (int e = 0; e < 3; ++e) {
+        const int w = tid + e * kLocalTcThreads, pr = w >> 8, rem = w & 255;
+        const int Rs = pr < 3 ? 0 : pr < 5 ? 1 : 2;
+        const int Rd = pr < 3 ? pr + 1 : pr < 5 ? pr - 1 : 3;
+        const int r = 16 * Rs + (rem >> 4), oct = rem & 15, kb = oct >> 3, ch = oct & 7;
+        const uint32_t co = (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
+        float gs[8], gd[8], x[8];
+        ld8f(sGb + Rs * kD + oct * 8, gs);
+        ld8f(sGb + Rd * kD + oct * 8, gd);
+        unpack8(*reinterpret_cast<const uint4*>(smem + LB_RIGHT + right_rel(Rs) +
+                                                 kb * (16u * (Rs + 1) * 128u) + co), x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= __expf(gd[i] - gs[i]);
+        *reinterpret_cast<uint4*>(smem + LB_RIGHT + right_rel(Rd) + kb * (16u * (Rd + 1) * 128u) +
+                                  co) = pack8(x);
     }
     ok = ok && wait_bar_warp(bar_m1, 0, 42);
     tc_fence_after();
