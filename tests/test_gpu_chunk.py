@@ -142,6 +142,31 @@ def test_saved_backward_rejects_other_dims():
                           t["beta"][:, :64], t["do"][:, :64], saved=saved)
 
 
+@pytest.mark.parametrize("saved", [False, True])
+@pytest.mark.parametrize("B,T,H,HV", [(1, 64, 1, 1), (2, 192, 1, 4), (1, 320, 2, 2)])
+def test_tcgen05_chunk_counts_and_groups(B, T, H, HV, saved):
+    """Tensor-core path on one chunk, odd chunk counts and a GVA group of 4,
+    with an initial state and the final state, stateless and saved backward."""
+    w = I.Workload("tc_shapes", B, T, H, HV, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
+                   h0_std=0.1, seed=31 + T + HV)
+    inp = I.make_chunk_inputs(w)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    if saved:
+        o, ht, sv = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                      initial_state=t["h0"], output_final_state=True,
+                                      impl="tcgen05", save_for_backward=True)
+    else:
+        o, ht = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                  initial_state=t["h0"], output_final_state=True, impl="tcgen05")
+        sv = None
+    res = dict(o=o, ht=ht)
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                 initial_state=t["h0"], impl="tcgen05", saved=sv))
+    torch.cuda.synchronize()
+    kda.check()
+    compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
+
+
 def test_tcgen05_backward_refuses_final_state_gradient():
     w = I.Workload("bf16_dht", 1, 128, 1, 1, 128, 128, 64, torch.bfloat16, dht=True, seed=26)
     t = {n: (x.cuda() if x is not None else None) for n, x in I.make_chunk_inputs(w).items()}
