@@ -309,12 +309,6 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 if (!wait_bar(&full[s], (n >> 1) & 1, 3)) break;
                 if (!wait_bar(bar_S, n & 1, 4)) break;
                 tc_fence_after();
-                if (a.h_out) {  // S_n^T tile (rows v) as it stands to h_out, by TMA
-                    const int y = (bh * NT + n) * kD;
-                    tma_store_2d(&tm_hout, smem + OFF_S, 0, y);
-                    tma_store_2d(&tm_hout, smem + OFF_S + 16384, 64, y);
-                    bulk_commit_group();
-                }
                 const uint32_t tO = tmem + ((n & 1) ? TM_O1 : TM_O0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -323,10 +317,16 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     mma_bf16(tmem + TM_W, dS + ka, dW0 + so + kb, idesc64, kk > 0);
                 }
                 // the delta step rewrites the delta tile once D12 completes: the
-                // store of the previous delta must have read it (only this
-                // chunk's state store may still be reading)
-                if (a.h_out) bulk_wait_read_but1();
+                // previous delta's store must have read it
+                if (a.h_out) bulk_wait_read_all();
                 mma_commit(bar_D12);
+                // stores are issued after the products they would otherwise delay
+                if (a.h_out) {  // S_n^T tile (rows v) as it stands to h_out, by TMA
+                    const int y = (bh * NT + n) * kD;
+                    tma_store_2d(&tm_hout, smem + OFF_S, 0, y);
+                    tma_store_2d(&tm_hout, smem + OFF_S + 16384, 64, y);
+                    bulk_commit_group();
+                }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
@@ -335,24 +335,25 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 }
                 if (!wait_bar(bar_delta, n & 1, 5)) break;
                 tc_fence_after();
-                if (a.delta_out) {  // delta_n^T tile (rows v) to delta_out, by TMA
-                    tma_store_2d(&tm_dout, smem + OFF_DELTA, 0, (bh * NT + n) * kD);
-                    bulk_commit_group();
-                }
                 if (!wait_bar(bar_Sx, n & 1, 10)) break;  // S^T rescaled by gam in TMEM
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // Kb tile [64 c][128 k] read MN-major (N = k)
                     mma_bf16(tmem + TM_S, dD + ((kk * 32) >> 4), dKb0 + so + ((kk * 2048) >> 4),
                              idesc128 | kBMajorMN, 1);
+                // the next state step may start once the state update is done
+                // (and this chunk's state store has read the state tile); O_n
+                // is read only after the next chunk's D12, which also covers it
+                if (a.h_out) bulk_wait_read_all();
+                mma_commit(bar_D3);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tO, dD + ((kk * 32) >> 4), dAq0 + so + ((kk * 32) >> 4), idesc64, 1);
-                // the next state step rewrites the state tile once D3 completes
-                // (this chunk's delta store may still be reading its tile)
-                if (a.h_out) bulk_wait_read_but1();
-                mma_commit(bar_D3);
                 mma_commit(&empty[s]);
+                if (a.delta_out) {  // delta_n^T tile (rows v) to delta_out, by TMA
+                    tma_store_2d(&tm_dout, smem + OFF_DELTA, 0, (bh * NT + n) * kD);
+                    bulk_commit_group();
+                }
             }
             bulk_wait_all();
             // all issued MMAs complete before TMEM is released
@@ -416,7 +417,11 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 }
             }
         }
-        if (ok && a.o) o_out(NT - 1);
+        // the last chunk's output products are covered by the final commit only
+        if (ok && a.o && wait_bar_warp(bar_fin, 0, 6)) {
+            tc_fence_after();
+            o_out(NT - 1);
+        }
         (void)ok;
     }
 
