@@ -873,7 +873,10 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
 // ===========================================================================
 constexpr uint32_t I_K = 0, I_Q = 16384, I_G = 32768, I_V = 49152;   // TMA tiles, 16 KB each
 constexpr uint32_t I_LEFT = 65536;                                   // 128 rows x 128, 32 KB
-constexpr uint32_t I_R0 = 98304;   // Right_R: 16(R+1) rows x 128: 4, 8, 12, 16 KB
+// Right_0..Right_3 stacked as one 160-row operand (rows 0-15, 16-47, 48-95,
+// 96-159), per 64-channel block of 160 x 128 B = 20 KB
+constexpr uint32_t I_R0 = 98304;
+constexpr uint32_t kRightKb = 160 * 128;
 constexpr uint32_t I_KHAT = I_G;     // Khat overwrites the consumed g tile
 constexpr uint32_t I_TB = I_R0 + 40960;                              // T*beta, 64x64 bf16, 8 KB
 constexpr int kAS = 68;              // row stride (floats) of A and T: rows stay 16-byte aligned
@@ -912,12 +915,9 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&x)[8]) {
 constexpr int kIntraThreads = 512;
 constexpr uint32_t INTRA_TX = 4 * 16384;
 
-__host__ __device__ constexpr uint32_t right_off(int R) {  // byte offset of Right_R
-    return I_R0 + 2048u * (uint32_t)(R * (R + 1));         // sum_{J<R} 4096 (J+1)
-}
-__host__ __device__ constexpr uint32_t right_col(int R) {  // TMEM column of D_R
-    return 8u * (uint32_t)(R * (R + 1));                   // sum_{J<R} 16 (J+1)
-}
+// first row of Right_R in the stacked operand, which is also the first TMEM
+// column of D_R: sum_{J<R} 16 (J+1)
+__host__ __device__ constexpr uint32_t right_col(int R) { return 8u * (uint32_t)(R * (R + 1)); }
 
 struct IntraArgs {
     int T, H, HV, NT;
@@ -1087,8 +1087,9 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 if (Rr > Rb) ld8f(sF + f_slot(Rb, Rr) * kD + c0, f8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = kv[e] * Ei[e] * (Rr > Rb ? f8[e] : 1.f);
-                *reinterpret_cast<uint4*>(smem + right_off(Rr) + kb * (16u * (Rr + 1) * 128u) +
-                                          r * 128 + co) = pack8(x);
+                // right_col(Rr) is a multiple of 8: row r keeps its swizzle
+                *reinterpret_cast<uint4*>(smem + I_R0 + kb * kRightKb +
+                                          (right_col(Rr) + r) * 128 + co) = pack8(x);
             }
             const size_t go = ((size_t)row0 + r) * kD + c0;
 #pragma unroll
@@ -1108,21 +1109,15 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     __syncthreads();
     tc_fence_after();
 
-    // ---- (2) D_R = Left Right_R^T ----
+    // ---- (2) D_R = Left Right_R^T for all R at once: N = 160 over the stacked
+    // Right operand, D_R in TMEM columns right_col(R) .. + 16(R+1) ----
     if (tid == 0 && ok) {
-        const uint32_t left = smem_u32(smem + I_LEFT);
+        const uint32_t left = smem_u32(smem + I_LEFT), right = smem_u32(smem + I_R0);
+        const uint32_t id = idesc_bf16_f32(128, 160);
 #pragma unroll
-        for (int RR = 0; RR < 4; ++RR) {
-            const uint32_t rows = 16u * (RR + 1);
-            const uint32_t right = smem_u32(smem + right_off(RR));
-            const uint32_t id = idesc_bf16_f32(128, 16 * (RR + 1));
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + right_col(RR),
-                         sdesc_sw128(left + (kk >> 2) * 16384 + (kk & 3) * 32),
-                         sdesc_sw128(right + (kk >> 2) * (rows * 128u) + (kk & 3) * 32), id,
-                         kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16(tmem, sdesc_sw128(left + (kk >> 2) * 16384 + (kk & 3) * 32),
+                     sdesc_sw128(right + (kk >> 2) * kRightKb + (kk & 3) * 32), id, kk > 0);
         mma_commit(bar_a);
     }
     ok = ok && wait_bar_warp(bar_a, 0, 32);
