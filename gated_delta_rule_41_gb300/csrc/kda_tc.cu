@@ -743,8 +743,9 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                 // MN-major, K = v advancing 16 rows per step
                 const uint64_t as0 = sdesc_mn_sw128(s0 + kk * 2048, 16384);
                 const uint64_t ads = sdesc_mn_sw128(ds + kk * 2048, 16384);
-                mma_bf16(tmem + 0, as0, sdesc_sw128(odd + ko), id64 | kAMajorMN, kk > 0);
-                mma_bf16(tmem + 64, as0, sdesc_sw128(odd + 8192 + ko), id64 | kAMajorMN, kk > 0);
+                // S0 [dO; ddelta]^T in one N = 128 product: D1 (dQh^T) columns 0-63,
+                // D2 (dW^T) columns 64-127
+                mma_bf16(tmem + 0, as0, sdesc_sw128(odd + ko), id128 | kAMajorMN, kk > 0);
                 // delta is stored transposed (rows v): B operand read MN-major
                 const uint64_t bdt = sdesc_mn_sw128(dt + kk * 2048, 16384);
                 mma_bf16(tmem + 128, ads, bdt, id64 | kAMajorMN | kBMajorMN, kk > 0);
@@ -1298,14 +1299,16 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 // ===========================================================================
 constexpr uint32_t LB_K = 0, LB_Q = 16384, LB_G = 32768;     // TMA tiles, read up to the end
 constexpr uint32_t LB_DWY = 49152;    // [dW; Y] 128 rows x 128, 2 k-blocks of 16 KB
-constexpr uint32_t LB_T = 81920;      // T bf16 [64 r][64 m]
+// 81920 .. 90112: unused
 constexpr uint32_t LB_DAQ = 90112;    // [dA_R; dAqk_R] rows 32R + 16s + u, 64 columns j
-// 106496 .. 122880: unused
+// T as [T_hi; T_lo]: bf16 [64 r][64 m] each, adjacent so that one N = 128
+// operand covers both
+constexpr uint32_t LB_T = 106496, LB_TLO = LB_T + 8192;
 constexpr uint32_t LB_RIGHT = 122880; // Right_R tiles, 16(R+1) rows each
 constexpr uint32_t LB_LCOL = 163840;  // [beta k E; qs E] rows 32R + 16s + u, 128 c
 constexpr uint32_t LB_SMALL = 196608; // fp32 small arrays
-constexpr uint32_t LB_TLO = LB_SMALL + 8192;  // T low part, bf16 [64 r][64 m]
-constexpr uint32_t LB_DTV = LB_TLO + 8192;    // dTv fp32 [64][64], 16-byte chunks XOR-swizzled
+// LB_SMALL + 8192 .. + 16384: unused
+constexpr uint32_t LB_DTV = LB_SMALL + 16384;  // dTv fp32 [64][64], 16-byte chunks XOR-swizzled
 constexpr uint32_t LB_BAR = LB_DTV + 16384;
 // After P1/P2 the [dW; Y] area holds the split P3/P4 operands.  P3's A has
 // M = 128 rows of which only the first 64 matter: the hi tile's rows 64..127
@@ -1547,65 +1550,66 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // ---- P3: Y2 = dT T^T (TMEM columns 128..191) ----
+    // ---- P3: Y2 = dT T^T.  dT_hi [T_hi; T_lo]^T (N = 128) puts hi.hi in TMEM
+    // columns 128..191 and hi.lo in 192..255; dT_lo T_hi^T adds onto 128..191 ----
     if (tid == 0 && ok) {
         const uint32_t dth = smem_u32(smem + LB_DTH), dtl = smem_u32(smem + LB_DTL);
-        const uint32_t th = smem_u32(smem + LB_T), tl = smem_u32(smem + LB_TLO);
-        const uint32_t id = idesc_bf16_f32(128, 64);
+        const uint32_t th = smem_u32(smem + LB_T);
+        const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + 128, sdesc_sw128(dth + kk * 32), sdesc_sw128(th + kk * 32), id, kk > 0);
+            mma_bf16(tmem + 128, sdesc_sw128(dth + kk * 32), sdesc_sw128(th + kk * 32), id128,
+                     kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + 128, sdesc_sw128(dth + kk * 32), sdesc_sw128(tl + kk * 32), id, 1);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + 128, sdesc_sw128(dtl + kk * 32), sdesc_sw128(th + kk * 32), id, 1);
+            mma_bf16(tmem + 128, sdesc_sw128(dtl + kk * 32), sdesc_sw128(th + kk * 32), id64, 1);
         mma_commit(bar_m3);
     }
     ok = ok && wait_bar_warp(bar_m3, 0, 44);
     tc_fence_after();
     if (ok && c < kC) {
-        float r16[16];
+        float r16[16], s16[16];
         tmem_ld16(tmem + lane_off + 128 + 16 * R, r16);
+        tmem_ld16(tmem + lane_off + 192 + 16 * R, s16);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) split_st(LB_Y2H, LB_Y2L, sw128_offset(c, 16 * R + e), r16[e]);
+        for (int e = 0; e < 16; ++e)
+            split_st(LB_Y2H, LB_Y2L, sw128_offset(c, 16 * R + e), r16[e] + s16[e]);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // ---- P4: T^T Y2 (TMEM columns 0..63); T and Y2 both read MN-major. A
-    // spans M = 128: its second MN block (+8192 B) is don't-care data ----
+    // ---- P4: T^T Y2, T and Y2 read MN-major.  T_hi^T [Y2_hi | Y2_lo] (N = 128
+    // over the adjacent Y2 tiles) puts hi.hi in TMEM columns 256..319 and hi.lo
+    // in 320..383; T_lo^T Y2_hi adds onto 256..319.  A spans M = 128: its
+    // second MN block (+8192 B) is don't-care data ----
     if (tid == 0 && ok) {
         const uint32_t th = smem_u32(smem + LB_T), tl = smem_u32(smem + LB_TLO);
-        const uint32_t yh = smem_u32(smem + LB_Y2H), yl = smem_u32(smem + LB_Y2L);
-        const uint32_t id = idesc_bf16_f32(128, 64) | kAMajorMN | kBMajorMN;
+        const uint32_t yh = smem_u32(smem + LB_Y2H);
+        const uint32_t id64 = idesc_bf16_f32(128, 64) | kAMajorMN | kBMajorMN;
+        const uint32_t id128 = idesc_bf16_f32(128, 128) | kAMajorMN | kBMajorMN;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + 0, sdesc_mn_sw128(th + kk * 2048, 8192),
-                     sdesc_mn_sw128(yh + kk * 2048, 8192), id, kk > 0);
+            mma_bf16(tmem + 256, sdesc_mn_sw128(th + kk * 2048, 8192),
+                     sdesc_mn_sw128(yh + kk * 2048, 8192), id128, kk > 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + 0, sdesc_mn_sw128(th + kk * 2048, 8192),
-                     sdesc_mn_sw128(yl + kk * 2048, 8192), id, 1);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + 0, sdesc_mn_sw128(tl + kk * 2048, 8192),
-                     sdesc_mn_sw128(yh + kk * 2048, 8192), id, 1);
+            mma_bf16(tmem + 256, sdesc_mn_sw128(tl + kk * 2048, 8192),
+                     sdesc_mn_sw128(yh + kk * 2048, 8192), id64, 1);
         mma_commit(bar_m4);
     }
     ok = ok && wait_bar_warp(bar_m4, 0, 45);
     tc_fence_after();
     // dA = -mask_strict(T^T Y2) (bf16) into the row-side and column-side B tiles
     if (ok && c < kC) {
-        float r16[16];
-        tmem_ld16(tmem + lane_off + 16 * R, r16);
+        float r16[16], s16[16];
+        tmem_ld16(tmem + lane_off + 256 + 16 * R, r16);
+        tmem_ld16(tmem + lane_off + 320 + 16 * R, s16);
         const int i = c, t2 = 32 * (i >> 4) + (i & 15);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int j = 16 * R + e;
-            const float v = j < i ? -r16[e] : 0.f;
+            const float v = j < i ? -(r16[e] + s16[e]) : 0.f;
             st(LB_DAQ + sw128_offset(t2, j), v);
         }
     }
