@@ -53,9 +53,15 @@ def _src_hash(name):
 # keyed by kernel name: (bytes per launch at the benchmark workload, the
 # source file, that file's hash when captured).  A kernel whose source has
 # changed since reports traffic null.
-# tc_local_bwd: 488,422,656 B measured at B=1, T=8192 (2048 chunks), scaled
-# by the chunk count to the B=4 launch (8192 chunks).
-NCU_TRAFFIC = {"tc_local_bwd": (4 * 488422656, "kda_tc.cu", "62840bd45751")}
+# Measured at B=1, T=8192 (2048 chunks, inputs and workspace above L2),
+# scaled by the chunk count to the B=4 launch (8192 chunks).
+NCU_TRAFFIC = {
+    "tc_local_bwd": (4 * (354545408 + 78717696), "kda_tc.cu", "daa97945830f"),
+    "tc_intra": (4 * (134708224 + 133925376), "kda_tc.cu", "daa97945830f"),
+    "tc_grad_v": (4 * (285914112 + 205229056), "kda_tc.cu", "daa97945830f"),
+    "tc_chain_fwd_save": (4 * (152110080 + 91291648), "kda_tc.cu", "daa97945830f"),
+    "tc_chain_bwd": (4 * (152088832 + 65049600), "kda_tc.cu", "daa97945830f"),
+}
 
 
 def kernel_algo_bytes(name, w):
@@ -110,6 +116,21 @@ def kernel_algo_bytes(name, w):
     return None
 
 
+def kernel_entry(name, total_ms, launches, total_k, w, hbm):
+    """Per-kernel line: launches, time, share, algorithmic GB/s and its
+    fraction of the copy peak, and the measured DRAM bytes per launch."""
+    per = total_ms / launches
+    algo = kernel_algo_bytes(name, w)
+    e = {"launches": launches, "ms_per_launch": per, "share": total_ms / total_k}
+    if algo:
+        e["algo_gbs"] = algo / (per / 1e3) / 1e9
+        e["frac"] = e["algo_gbs"] / hbm
+    if name in NCU_TRAFFIC:
+        tb, src, h = NCU_TRAFFIC[name]
+        e["traffic"] = tb if _src_hash(src) == h else None
+    return e
+
+
 def start_clock_sampler():
     f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
     q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -117,7 +138,7 @@ def start_clock_sampler():
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     try:
         p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                              "-lms", "200"], stdout=f, stderr=subprocess.DEVNULL)
+                              "-lms", "50"], stdout=f, stderr=subprocess.DEVNULL)
     except OSError:
         p = None
     return p, f.name
@@ -265,7 +286,7 @@ def measure_decode(kda, dev, hbm):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05"])
@@ -435,7 +456,7 @@ def main():
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": int(sum(n for _, n in kernels.values())),
-        "kernels": {n: {"launches": c, "ms_per_launch": t / c, "share": t / total_k}
+        "kernels": {n: kernel_entry(n, t, c, total_k, w, hbm)
                     for n, (t, c) in sorted(kernels.items(), key=lambda x: -x[1][0])},
         "clocks": clocks,
     }
