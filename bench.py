@@ -101,14 +101,18 @@ def kernel_algo_bytes(name, w):
         ops = 4 * K * 2                          # W, Qh, U, Kb (bf16)
         cc = C * 2                               # one bf16 C x C row per token
         per = {
-            "tc_intra": qk + 2 * K * e + e + ops + 2 * cc + C * 4 + K * 4 // C,
+            # T out as bf16 high and low parts, like Aqk one C-row each
+            "tc_intra": qk + 2 * K * e + e + ops + 3 * cc + K * 4 // C,
             "tc_chain_fwd": ops + cc + K * 4 // C + V * e,
             "tc_chain_fwd_save": ops + cc + K * 4 // C + V * e + K * V * 2 // C + V * 2,
             "tc_chain_states": ops + cc + K * 4 // C + K * V * 2 // C + V * 2,
             "tc_chain_bwd": V * e + 3 * K * 2 + cc + K * 4 // C + K * V * 2 // C + V * 2,
+            # out: dv, dQh and dK (fp32), dW (bf16), dgam, dAqk (bf16), dTv (fp32), d(beta v)
             "tc_grad_v": (2 * K * V * 2 // C + V * e + 2 * V * 2 + V * e + cc + e)
-                         + (V * e + 3 * K * 4 + K * 4 // C + 2 * C * 4 + 4),
-            "tc_local_bwd": (C * 4 + 3 * K * 4 + 2 * C * 4 + K * 4 // C + 4 + qk + K * e + e)
+                         + (V * e + 2 * K * 4 + K * 2 + K * 4 // C + cc + C * 4 + 4),
+            # in: T (hi, lo), dW (bf16), dQh, dK (fp32), dAqk (bf16), dTv (fp32), ...
+            "tc_local_bwd": (2 * cc + K * 2 + 2 * K * 4 + cc + C * 4 + K * 4 // C + 4 + qk +
+                             K * e + e)
                             + (2 * K * (e if G == 1 else 4) + K * e + e),
         }
         if name in per:
