@@ -1257,21 +1257,17 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     ok = ok && wait_bar_warp(bar_w, 0, 33);
     tc_fence_after();
-    if (ok && warp < 8) {
-        // warps 0-3: W^T (lane = k); warps 4-7: U^T (lane = v)
+    if (ok) {
+        // W^T (lane = k, TMEM columns 0..63) and U^T (lane = v, 64..127): warp w
+        // takes lane quadrant w % 4 of W (w / 4 even) or U, rows 32 (w / 8) + 0..31
         float r[32];
-        const int q4 = warp & 3;
-        const uint32_t lo = (uint32_t)(q4 * 32) << 16;
+        const int q4 = warp & 3, isU = (warp >> 2) & 1, cb = warp >> 3;
         const int l = q4 * 32 + lane;
-        const uint32_t col = warp < 4 ? 0u : 64u;
-        __nv_bfloat16* dst = warp < 4 ? a.W2 : a.U2;
-#pragma unroll 1
-        for (int cb = 0; cb < 2; ++cb) {
-            tmem_ld32(tmem + lo + col + cb * 32, r);
+        tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + isU * 64 + cb * 32, r);
+        __nv_bfloat16* dst = isU ? a.U2 : a.W2;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                dst[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
-        }
+        for (int j = 0; j < 32; ++j)
+            dst[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
     }
     tc_fence_before();
     __syncthreads();
