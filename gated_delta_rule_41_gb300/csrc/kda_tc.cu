@@ -15,6 +15,7 @@
 // issues MMAs (one thread), warps 2-5 are the epilogue (one TMEM lane per
 // value column).  Every mbarrier wait is bounded: on expiry the kernel records
 // an error code in g_tc_error and unwinds.
+#include <algorithm>
 #include <mutex>
 
 #include "kda_common.cuh"
@@ -47,6 +48,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, int cod
         }
     }
     return true;
+}
+// Wait for a phase with the time bound only (also after another wait has
+// failed), for copies that must land before the CTA exits.
+__device__ __forceinline__ void wait_bar_drain(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kTimeoutCycles) return;
 }
 // Warp-uniform version: every lane waits, the warp proceeds only if all did.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, int code) {
@@ -878,18 +886,23 @@ constexpr uint32_t I_LEFT = 65536;                                   // 128 rows
 // 96-159), per 64-channel block of 160 x 128 B = 20 KB
 constexpr uint32_t I_R0 = 98304;
 constexpr uint32_t kRightKb = 160 * 128;
-constexpr uint32_t I_KHAT = I_G;     // Khat overwrites the consumed g tile
+constexpr uint32_t I_KHAT = I_G;     // Khat (the g tile itself goes to the G area I_SG)
 constexpr uint32_t I_TB = I_R0 + 40960;                              // T*beta, 64x64 bf16, 8 KB
 constexpr int kAS = 68;              // row stride (floats) of A and T: rows stay 16-byte aligned
 constexpr uint32_t I_A = I_TB + 8192;                                // fp32 [64][kAS]
 constexpr uint32_t I_T = I_A + 64 * kAS * 4;                         // fp32 [64][kAS]
 constexpr uint32_t I_BETA = I_T + 64 * kAS * 4;                      // fp32 [64]
 constexpr uint32_t I_GX = I_BETA + 256;                              // fp32 [2][4][128]
-constexpr uint32_t I_SG = I_GX + 4096;     // G fp32 [64][128] for the operand build
+// G fp32 [64][128] for the operand build; before that it receives the g tile
+// by TMA, whose 128-byte swizzle needs a 1024-byte aligned destination
+constexpr uint32_t I_SG = (I_GX + 4096 + 1023) & ~1023u;
 constexpr uint32_t I_SC = I_SG + 32768;    // exp(G_b), exp(G_last - G_b) [4][128]; F [6][128]
 constexpr uint32_t I_BAR = I_SC + 14 * 512;
 constexpr uint32_t INTRA_SMEM = I_BAR + 64 + 1024;
 static_assert(INTRA_SMEM <= 232448, "intra kernel exceeds the per-CTA shared memory limit");
+static_assert(I_K % 1024 == 0 && I_Q % 1024 == 0 && I_V % 1024 == 0 && I_SG % 1024 == 0 &&
+                  I_LEFT % 1024 == 0 && I_R0 % 1024 == 0 && I_TB % 1024 == 0 && I_G % 1024 == 0,
+              "128-byte swizzled tiles need 1024-byte aligned bases");
 
 // slot of F(R, Rr) = exp(G_b(Rr) - G_b(R)) for Rr > R among the six pairs
 __host__ __device__ constexpr int f_slot(int R, int Rr) { return R * (7 - R) / 2 + (Rr - R - 1); }
@@ -921,7 +934,7 @@ constexpr uint32_t INTRA_TX = 4 * 16384;
 __host__ __device__ constexpr uint32_t right_col(int R) { return 8u * (uint32_t)(R * (R + 1)); }
 
 struct IntraArgs {
-    int T, H, HV, NT;
+    int T, H, HV, NT, BH;
     float scale;
     const __nv_bfloat16* beta;
     __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2, *Tlo;
@@ -951,10 +964,11 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + I_BAR);
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + I_BAR);   // k, q, g tiles
     uint64_t* bar_a = bar_tma + 1;
     uint64_t* bar_w = bar_tma + 2;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    uint64_t* bar_v = bar_tma + 3;                                     // v tile
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 4);
     float* sA = reinterpret_cast<float*>(smem + I_A);
     float* sT = reinterpret_cast<float*>(smem + I_T);
     float* sBeta = reinterpret_cast<float*>(smem + I_BETA);
@@ -966,39 +980,86 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     float* sF = sELb + 4 * kD;                               // [6][128]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / a.HV, hv = bh % a.HV, h = hv / (a.HV / a.H);
-    const int trow = b * a.T + n * kC;        // token row in [B*T]
-    const int row0 = bh * a.T + n * kC;       // row in the [BH*T] workspace arrays
-    const int crow = bh * a.NT + n;           // chunk index
+    const int total = a.BH * a.NT;   // chunks; CTA i takes chunks i, i + grid, ...
+
+    // token row of chunk ch, its value head and key head
+    auto coords = [&](int ch, int& trow, int& hv, int& h) {
+        const int nn = ch % a.NT, bb = ch / a.NT;
+        hv = bb % a.HV;
+        h = hv / (a.HV / a.H);
+        trow = (bb / a.HV) * a.T + nn * kC;
+    };
+    // k, q, g tiles of chunk ch (g into the fp32 G area, which the build has
+    // finished reading) and, separately, its v tile
+    // thread 0's counts of issued and consumed loads (every load is waited for
+    // before the CTA exits)
+    int kqg_issued = 0, v_issued = 0, kqg_waited = 0, v_waited = 0;
+    auto issue_kqg = [&](int ch) {
+        int trow, hv, h;
+        coords(ch, trow, hv, h);
+        mbar_arrive_expect_tx(bar_tma, 3 * 16384);
+        tma_load_3d(smem + I_K, &tm_k, bar_tma, 0, h, trow);
+        tma_load_3d(smem + I_K + 8192, &tm_k, bar_tma, 64, h, trow);
+        tma_load_3d(smem + I_Q, &tm_q, bar_tma, 0, h, trow);
+        tma_load_3d(smem + I_Q + 8192, &tm_q, bar_tma, 64, h, trow);
+        tma_load_3d(smem + I_SG, &tm_g, bar_tma, 0, hv, trow);
+        tma_load_3d(smem + I_SG + 8192, &tm_g, bar_tma, 64, hv, trow);
+        ++kqg_issued;
+    };
+    auto issue_v = [&](int ch) {
+        int trow, hv, h;
+        coords(ch, trow, hv, h);
+        mbar_arrive_expect_tx(bar_v, 16384);
+        tma_load_3d(smem + I_V, &tm_v, bar_v, 0, hv, trow);
+        tma_load_3d(smem + I_V + 8192, &tm_v, bar_v, 64, hv, trow);
+        ++v_issued;
+    };
+    auto load_beta = [&](int ch) {
+        int trow, hv, h;
+        coords(ch, trow, hv, h);
+        return __bfloat162float(a.beta[((size_t)trow + tid) * a.HV + hv]);
+    };
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_a, 1);
         mbar_init(bar_w, 1);
+        mbar_init(bar_v, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
         tmem_alloc(tmem_holder, 256);
         tmem_relinquish();
     }
-    if (tid < kC) sBeta[tid] = __bfloat162float(a.beta[((size_t)trow + tid) * a.HV + hv]);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(bar_tma, INTRA_TX);
-        tma_load_3d(smem + I_K, &tm_k, bar_tma, 0, h, trow);
-        tma_load_3d(smem + I_K + 8192, &tm_k, bar_tma, 64, h, trow);
-        tma_load_3d(smem + I_Q, &tm_q, bar_tma, 0, h, trow);
-        tma_load_3d(smem + I_Q + 8192, &tm_q, bar_tma, 64, h, trow);
-        tma_load_3d(smem + I_G, &tm_g, bar_tma, 0, hv, trow);
-        tma_load_3d(smem + I_G + 8192, &tm_g, bar_tma, 64, hv, trow);
-        tma_load_3d(smem + I_V, &tm_v, bar_tma, 0, hv, trow);
-        tma_load_3d(smem + I_V + 8192, &tm_v, bar_tma, 64, hv, trow);
+    if (tid == 0 && (int)blockIdx.x < total) {
+        issue_kqg(blockIdx.x);
+        issue_v(blockIdx.x);
     }
-    bool ok = wait_bar_warp(bar_tma, 0, 31);
+    float beta_next = (tid < kC && (int)blockIdx.x < total) ? load_beta(blockIdx.x) : 0.f;
+    bool ok = true;
+
+#pragma unroll 1
+    for (int it = 0, chunk = blockIdx.x; chunk < total; ++it, chunk += gridDim.x) {
+    const uint32_t ph = it & 1;
+    const int next = chunk + gridDim.x;
+    const int n = chunk % a.NT, bh = chunk / a.NT;
+    const int b = bh / a.HV, hv = bh % a.HV;
+    const int row0 = bh * a.T + n * kC;       // row in the [BH*T] workspace arrays
+    const int crow = chunk;                   // chunk index
+    (void)b;
+    if (tid < kC) {
+        sBeta[tid] = beta_next;                                   // read after later barriers
+        if (next < total) beta_next = load_beta(next);            // in flight meanwhile
+    }
+    {
+        const bool got = wait_bar_warp(bar_tma, ph, 31);
+        if (got) ++kqg_waited;
+        ok = ok && got;
+    }
 
     // ---- (1) cumsum: thread (c, R) owns key channel c of row block R ----
     const int c = tid & (kD - 1), R = tid >> 7;
@@ -1015,7 +1076,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         float acc = 0.f;
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-            acc += fmaxf(ld(I_G, 16 * R + u), kGateFloor);
+            acc += fmaxf(ld(I_SG, 16 * R + u), kGateFloor);   // g tile in the G area
             G[u] = acc;
         }
         sGtot[R * kD + c] = acc;
@@ -1101,7 +1162,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             *reinterpret_cast<uint4*>(a.Kb2 + go) = pack8(x);
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = kv[e] * egb[e] * E[e];        // Khat = k exp(G)
-            // Khat overwrites the consumed g tile
             *reinterpret_cast<uint4*>(smem + I_KHAT + kb * 8192 + r * 128 + co) = pack8(x);
         }
     }
@@ -1109,6 +1169,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the k, q tiles and the G area are free: the next chunk's k, q, g load now
+    if (tid == 0 && next < total) issue_kqg(next);
 
     // ---- (2) D_R = Left Right_R^T for all R at once: N = 160 over the stacked
     // Right operand, D_R in TMEM columns right_col(R) .. + 16(R+1) ----
@@ -1121,7 +1183,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                      sdesc_sw128(right + (kk >> 2) * kRightKb + (kk & 3) * 32), id, kk > 0);
         mma_commit(bar_a);
     }
-    ok = ok && wait_bar_warp(bar_a, 0, 32);
+    ok = ok && wait_bar_warp(bar_a, ph, 32);
     tc_fence_after();
     if (ok && warp < 4) {
         // warp R reads block R: lanes 0-15 -> A rows, 16-31 -> Aqk rows
@@ -1242,7 +1304,9 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && ok) {
+    if (tid == 0 && ok && wait_bar(bar_v, ph, 34)) {
+        ++v_waited;
+        tc_fence_after();
         const uint32_t id = idesc_bf16_f32(128, 64) | kAMajorMN;
         const uint32_t kh = smem_u32(smem + I_KHAT), vt = smem_u32(smem + I_V);
         const uint32_t tb = smem_u32(smem + I_TB);
@@ -1255,7 +1319,9 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         }
         mma_commit(bar_w);
     }
-    ok = ok && wait_bar_warp(bar_w, 0, 33);
+    ok = ok && wait_bar_warp(bar_w, ph, 33);
+    // the v tile is free: the next chunk's v loads now
+    if (tid == 0 && next < total) issue_v(next);
     tc_fence_after();
     if (ok) {
         // W^T (lane = k, TMEM columns 0..63) and U^T (lane = v, 64..127): warp w
@@ -1268,6 +1334,17 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             dst[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
+    }
+    tc_fence_before();
+    const bool all_ok = __syncthreads_and(ok);
+    tc_fence_after();
+    if (!all_ok) break;
+    }  // chunk loop
+    // loads issued for chunks the loop did not reach (after an error) land
+    // before shared memory is released
+    if (tid == 0) {
+        for (; kqg_waited < kqg_issued; ++kqg_waited) wait_bar_drain(bar_tma, kqg_waited & 1);
+        for (; v_waited < v_issued; ++v_waited) wait_bar_drain(bar_v, v_waited & 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -1313,6 +1390,10 @@ constexpr uint32_t LB_DTH = LB_DWY, LB_DTL = LB_DWY + 8192;
 constexpr uint32_t LB_Y2H = LB_DWY + 16384, LB_Y2L = LB_DWY + 24576;
 constexpr uint32_t LOCAL_TC_SMEM = LB_BAR + 64 + 1024;
 static_assert(LOCAL_TC_SMEM <= 232448, "local backward exceeds the per-CTA shared memory limit");
+static_assert(LB_K % 1024 == 0 && LB_Q % 1024 == 0 && LB_G % 1024 == 0 && LB_DWY % 1024 == 0 &&
+                  LB_T % 1024 == 0 && LB_TLO % 1024 == 0 && LB_DAQ % 1024 == 0 &&
+                  LB_RIGHT % 1024 == 0 && LB_LCOL % 1024 == 0,
+              "128-byte swizzled tiles need 1024-byte aligned bases");
 constexpr int kLocalTcThreads = 512;
 
 __host__ __device__ constexpr uint32_t right_rel(int R) { return 2048u * (uint32_t)(R * (R + 1)); }
@@ -1762,6 +1843,19 @@ EncodeFn get_encoder() {
     return fn;
 }
 
+// SMs of the current device (cached per device), for persistent grids.
+int sm_count() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 1;
+    }
+    return cache[dev];
+}
+
 // 2-D bf16 map over a row-major [rows][cols] array with a box of
 // box_cols x box_rows.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
@@ -1846,6 +1940,7 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     a.H = d.H;
     a.HV = d.HV;
     a.NT = NT;
+    a.BH = BH;
     a.scale = d.scale;
     a.beta = static_cast<const __nv_bfloat16*>(beta);
     a.W2 = w.W2;
@@ -1861,7 +1956,9 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
         return KDA_ERR_CUDA;
     {
         TimedLaunch tl("tc_intra", s);
-        intra_tc_kernel<<<dim3(NT, BH), kIntraThreads, INTRA_SMEM, s>>>(mk, mq, mg, mv, a);
+        // persistent: one CTA per SM walks the chunks
+        const int grid = std::min(BH * NT, sm_count());
+        intra_tc_kernel<<<grid, kIntraThreads, INTRA_SMEM, s>>>(mk, mq, mg, mv, a);
     }
     *gam_out = p.gam;
     return launch_status();
