@@ -668,13 +668,12 @@ constexpr uint32_t G_DT = 139264;  // delta^T [128 v][64 c], 16 KB
 constexpr uint32_t G_BAR = G_DT + 16384, G_DBV = G_BAR + 64;
 constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
 constexpr uint32_t GRAD_SMEM = G_DBV + 2304 + 1024;
-// 8 warps (two per SM sub-partition, so up to 255 registers a thread): lane 0
-// of warp 0 issues the TMA copies, lane 0 of warp 1 the MMAs, then all eight
-// run the epilogue
+// 8 warps (two per SM sub-partition, so up to 255 registers a thread): thread
+// 0 issues the TMA copies and the MMAs, then all eight run the epilogue
 constexpr int kGradThreads = 256;
 
 struct GradArgs {
-    int T, HV, NT;
+    int T, HV, NT, BH;
     const __nv_bfloat16* beta;  // [B,T,HV]
     __nv_bfloat16* dv;          // [B,T,HV,V]
     float *dQh, *dKb, *dgam, *dTv, *dbv;
@@ -689,26 +688,55 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + G_BAR);
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + G_BAR);   // all tiles but v
     uint64_t* bar_mma = bar_tma + 1;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 2);
+    uint64_t* bar_v = bar_tma + 2;                                     // v tile
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 3);
     float* dbv_part = reinterpret_cast<float*>(smem + G_DBV);  // [4 lane quadrants][64]
     float* beta_s = dbv_part + 4 * 64;                          // [64]
     float* dg_part = beta_s + 64;                               // [2 halves][128]
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / a.HV, hv = bh % a.HV;
-    const int NT = a.NT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NT = a.NT, total = a.BH * NT;   // CTA i takes chunks i, i + grid, ...
 
-    if (threadIdx.x == 0) {
+    // thread 0's counts of issued and consumed loads (every load is waited for
+    // before the CTA exits)
+    int main_issued = 0, v_issued = 0, main_waited = 0, v_waited = 0;
+    auto issue_main = [&](int ch) {   // states, state gradients, [dO; ddelta], delta^T, T
+        const int nn = ch % NT, bb = ch / NT, hvv = bb % a.HV;
+        const int rw = bb * a.T + nn * kC, tr = (bb / a.HV) * a.T + nn * kC;
+        mbar_arrive_expect_tx(bar_tma, GRAD_TX - 16384);
+        tma_load_2d(smem + G_S0, &tm_h, bar_tma, 0, ch * kD);
+        tma_load_2d(smem + G_S0 + 16384, &tm_h, bar_tma, 64, ch * kD);
+        tma_load_2d(smem + G_DS, &tm_dh, bar_tma, 0, ch * kD);
+        tma_load_2d(smem + G_DS + 16384, &tm_dh, bar_tma, 64, ch * kD);
+        tma_load_3d(smem + G_ODD, &tm_do, bar_tma, 0, hvv, tr);
+        tma_load_3d(smem + G_ODD + 16384, &tm_do, bar_tma, 64, hvv, tr);
+        tma_load_2d(smem + G_ODD + 8192, &tm_dd, bar_tma, 0, rw);
+        tma_load_2d(smem + G_ODD + 24576, &tm_dd, bar_tma, 64, rw);
+        tma_load_2d(smem + G_DT, &tm_d, bar_tma, 0, ch * kD);
+        tma_load_2d(smem + G_T, &tm_t, bar_tma, 0, ch * kC);
+        ++main_issued;
+    };
+    auto issue_v = [&](int ch) {
+        const int nn = ch % NT, bb = ch / NT, hvv = bb % a.HV;
+        const int tr = (bb / a.HV) * a.T + nn * kC;
+        mbar_arrive_expect_tx(bar_v, 16384);
+        tma_load_3d(smem + G_DV + 8192, &tm_v, bar_v, 0, hvv, tr);
+        tma_load_3d(smem + G_DV + 24576, &tm_v, bar_v, 64, hvv, tr);
+        ++v_issued;
+    };
+    auto load_beta = [&](int ch) {
+        const int nn = ch % NT, bb = ch / NT;
+        return __bfloat162float(
+            a.beta[((size_t)(bb / a.HV) * a.T + (size_t)nn * kC + tid) * a.HV + bb % a.HV]);
+    };
+
+    if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_v, 1);
         fence_mbar_init();
-    }
-    if (threadIdx.x < 64) {
-        beta_s[threadIdx.x] = __bfloat162float(
-            a.beta[((size_t)b * a.T + (size_t)n * kC + threadIdx.x) * a.HV + hv]);
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, 512);
@@ -718,67 +746,68 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const int row = bh * a.T + n * kC;
-    const int crow = bh * NT + n;
-    const int trow = b * a.T + n * kC;
+    if (tid == 0 && (int)blockIdx.x < total) {
+        issue_main(blockIdx.x);
+        issue_v(blockIdx.x);
+    }
+    float beta_next = (tid < kC && (int)blockIdx.x < total) ? load_beta(blockIdx.x) : 0.f;
+    bool ok = true;
 
-    if (warp == 0 && lane == 0) {
-        mbar_arrive_expect_tx(bar_tma, GRAD_TX);
-        tma_load_2d(smem + G_S0, &tm_h, bar_tma, 0, crow * kD);
-        tma_load_2d(smem + G_S0 + 16384, &tm_h, bar_tma, 64, crow * kD);
-        tma_load_2d(smem + G_DS, &tm_dh, bar_tma, 0, crow * kD);
-        tma_load_2d(smem + G_DS + 16384, &tm_dh, bar_tma, 64, crow * kD);
-        tma_load_3d(smem + G_ODD, &tm_do, bar_tma, 0, hv, trow);
-        tma_load_3d(smem + G_ODD + 16384, &tm_do, bar_tma, 64, hv, trow);
-        tma_load_2d(smem + G_ODD + 8192, &tm_dd, bar_tma, 0, row);
-        tma_load_2d(smem + G_ODD + 24576, &tm_dd, bar_tma, 64, row);
-        tma_load_2d(smem + G_DT, &tm_d, bar_tma, 0, crow * kD);
-        tma_load_3d(smem + G_DV + 8192, &tm_v, bar_tma, 0, hv, trow);
-        tma_load_3d(smem + G_DV + 24576, &tm_v, bar_tma, 64, hv, trow);
-        tma_load_2d(smem + G_T, &tm_t, bar_tma, 0, crow * kC);
-    }
-    if (warp == 1 && lane == 0) {
-        if (wait_bar(bar_tma, 0, 21)) {
-            tc_fence_after();
-            const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
-            const uint32_t s0 = smem_u32(smem + G_S0), ds = smem_u32(smem + G_DS);
-            const uint32_t odd = smem_u32(smem + G_ODD), dvt = smem_u32(smem + G_DV);
-            const uint32_t tt = smem_u32(smem + G_T), dt = smem_u32(smem + G_DT);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                // S0 and dS are stored transposed (rows v): A operands read
-                // MN-major, K = v advancing 16 rows per step
-                const uint64_t as0 = sdesc_mn_sw128(s0 + kk * 2048, 16384);
-                const uint64_t ads = sdesc_mn_sw128(ds + kk * 2048, 16384);
-                // S0 [dO; ddelta]^T in one N = 128 product: D1 (dQh^T) columns 0-63,
-                // D2 (dW^T) columns 64-127
-                mma_bf16(tmem + 0, as0, sdesc_sw128(odd + ko), id128 | kAMajorMN, kk > 0);
-                // delta is stored transposed (rows v): B operand read MN-major
-                const uint64_t bdt = sdesc_mn_sw128(dt + kk * 2048, 16384);
-                mma_bf16(tmem + 128, ads, bdt, id64 | kAMajorMN | kBMajorMN, kk > 0);
-                mma_bf16(tmem + 256, sdesc_sw128(odd + ko), bdt, id64 | kBMajorMN, kk > 0);
-                mma_bf16(tmem + 320, sdesc_sw128(odd + ko), sdesc_sw128(dvt + 8192 + ko), id64,
-                         kk > 0);
-            }
-            // D5 = ddelta^T T: ddelta tile read MN-major (v blocks 16 KB apart), T MN-major
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 192, sdesc_mn_sw128(odd + 8192 + kk * 2048, 16384),
-                         sdesc_mn_sw128(tt + kk * 2048, 8192), id64 | kAMajorMN | kBMajorMN,
-                         kk > 0);
-            mma_commit(bar_mma);
+#pragma unroll 1
+    for (int it = 0, chunk = blockIdx.x; chunk < total; ++it, chunk += gridDim.x) {
+        const uint32_t ph = it & 1;
+        const int next = chunk + gridDim.x;
+        const int n = chunk % NT, bh = chunk / NT;
+        const int b = bh / a.HV, hv = bh % a.HV;
+        const int row = bh * a.T + n * kC;
+        const int crow = chunk;
+        const int trow = b * a.T + n * kC;
+        if (tid < kC) {
+            beta_s[tid] = beta_next;                          // read after later barriers
+            if (next < total) beta_next = load_beta(next);    // in flight meanwhile
         }
-    }
-    __syncwarp();
-    {
-        // all 8 warps, two per TMEM lane quadrant, splitting the columns (lane
-        // 0 of warps 0 and 1 issued the copies and the MMAs above)
+        if (tid == 0) {   // the thread that issues the loads also issues the products
+            if (wait_bar(bar_tma, ph, 21) && wait_bar(bar_v, ph, 25)) {
+                ++main_waited;
+                ++v_waited;
+                tc_fence_after();
+                const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
+                const uint32_t s0 = smem_u32(smem + G_S0), ds = smem_u32(smem + G_DS);
+                const uint32_t odd = smem_u32(smem + G_ODD), dvt = smem_u32(smem + G_DV);
+                const uint32_t tt = smem_u32(smem + G_T), dt = smem_u32(smem + G_DT);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    // S0 and dS are stored transposed (rows v): A operands read
+                    // MN-major, K = v advancing 16 rows per step
+                    const uint64_t as0 = sdesc_mn_sw128(s0 + kk * 2048, 16384);
+                    const uint64_t ads = sdesc_mn_sw128(ds + kk * 2048, 16384);
+                    // S0 [dO; ddelta]^T in one N = 128 product: D1 (dQh^T) columns
+                    // 0-63, D2 (dW^T) columns 64-127
+                    mma_bf16(tmem + 0, as0, sdesc_sw128(odd + ko), id128 | kAMajorMN, kk > 0);
+                    // delta is stored transposed (rows v): B operand read MN-major
+                    const uint64_t bdt = sdesc_mn_sw128(dt + kk * 2048, 16384);
+                    mma_bf16(tmem + 128, ads, bdt, id64 | kAMajorMN | kBMajorMN, kk > 0);
+                    mma_bf16(tmem + 256, sdesc_sw128(odd + ko), bdt, id64 | kBMajorMN, kk > 0);
+                    mma_bf16(tmem + 320, sdesc_sw128(odd + ko), sdesc_sw128(dvt + 8192 + ko),
+                             id64, kk > 0);
+                }
+                // D5 = ddelta^T T: ddelta tile read MN-major (v blocks 16 KB apart), T MN-major
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + 192, sdesc_mn_sw128(odd + 8192 + kk * 2048, 16384),
+                             sdesc_mn_sw128(tt + kk * 2048, 8192), id64 | kAMajorMN | kBMajorMN,
+                             kk > 0);
+                mma_commit(bar_mma);
+            }
+        }
+        __syncwarp();
+        // all 8 warps, two per TMEM lane quadrant, splitting the columns
         const int q = warp & 3, half = warp >> 2;
         const int l = q * 32 + lane;  // TMEM lane: k for D1-D3, row for D4, v for D5
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         float r[32];
-        bool ok = wait_bar_warp(bar_tma, 0, 23);
+        ok = ok && wait_bar_warp(bar_tma, ph, 23);
         // dgam[k] = sum_v dS[v][k] S0[v][k] from the bf16 tiles (independent of
         // the MMAs); thread (k = l, half) sums rows v in [64 half, 64 half + 64)
         {
@@ -794,9 +823,15 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             }
             dg_part[half * kD + l] = acc;
         }
-        ok = ok && wait_bar_warp(bar_mma, 0, 24);
+        ok = ok && wait_bar_warp(bar_mma, ph, 24);
+        // every tile but v has been read (products and dgam): the next chunk's
+        // loads start while this chunk's results leave
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0 && ok && next < total) issue_main(next);
         if (ok) {
-            tc_fence_after();
             const size_t rb = (size_t)row * kD;
             const int cb = half;  // columns 32*cb .. 32*cb+31 of D1-D3 and D5
             tmem_ld32(tmem + lane_off + 0 + cb * 32, r);
@@ -848,17 +883,31 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             // dbv[m] = sum over v of r: lane j ends with row cb*32 + j of this quadrant
             dbv_part[q * 64 + cb * 32 + lane] = warp_sum_scatter<32>(r);
         }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // the v tile has been read: the next chunk's v loads now
+        if (tid == 0 && ok && next < total) issue_v(next);
+        if (tid < kD)
+            a.dgam[(size_t)crow * kD + tid] = dg_part[tid] + dg_part[kD + tid];
+        if (tid < 64) {
+            const int m = tid;
+            a.dbv[(size_t)row + m] =
+                (dbv_part[m] + dbv_part[64 + m]) + (dbv_part[128 + m] + dbv_part[192 + m]);
+        }
+        // partial sums, beta and TMEM are reused by the next chunk
+        if (!__syncthreads_and(ok)) break;
+    }
+    // loads issued for chunks the loop did not reach (after an error) land
+    // before shared memory is released
+    if (tid == 0) {
+        for (; main_waited < main_issued; ++main_waited) wait_bar_drain(bar_tma, main_waited & 1);
+        for (; v_waited < v_issued; ++v_waited) wait_bar_drain(bar_v, v_waited & 1);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (threadIdx.x < kD)
-        a.dgam[(size_t)crow * kD + threadIdx.x] = dg_part[threadIdx.x] + dg_part[kD + threadIdx.x];
-    if (threadIdx.x < 64) {
-        const int m = threadIdx.x;
-        a.dbv[(size_t)row + m] =
-            (dbv_part[m] + dbv_part[64 + m]) + (dbv_part[128 + m] + dbv_part[192 + m]);
-    }
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -2142,6 +2191,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.T = d.T;
         a.HV = d.HV;
         a.NT = NT;
+        a.BH = BH;
         a.beta = static_cast<const __nv_bfloat16*>(beta);
         a.dv = static_cast<__nv_bfloat16*>(dv);
         a.dQh = p.dQh;
@@ -2155,7 +2205,9 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                                  (int)GRAD_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
         TimedLaunch tl("tc_grad_v", s);
-        grad_v_kernel<<<dim3(NT, BH), kGradThreads, GRAD_SMEM, s>>>(mh, mdh, mdo, mdd, md, mv, mt, a);
+        // persistent: one CTA per SM walks the chunks
+        grad_v_kernel<<<std::min(BH * NT, sm_count()), kGradThreads, GRAD_SMEM, s>>>(
+            mh, mdh, mdo, mdd, md, mv, mt, a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     SimtWsPtrs p;
