@@ -1453,7 +1453,7 @@ __host__ __device__ constexpr uint32_t lb_dkb_row(int r) {
 }
 
 struct LocalTcArgs {
-    int T, H, HV, NT, G;
+    int T, H, HV, NT, G, BH;
     float scale;
     const float *dQh, *dKb, *dTv, *dgam, *dbv;
     const __nv_bfloat16 *q, *k, *g, *beta;
@@ -1478,7 +1478,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint64_t* bar_m2 = bar_tma + 2;
     uint64_t* bar_m3 = bar_tma + 3;
     uint64_t* bar_m4 = bar_tma + 4;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 5);
+    uint64_t* bar_g = bar_tma + 5;   // g tile (loaded apart from the others)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 6);
     float* sBeta = reinterpret_cast<float*>(smem + LB_SMALL);   // [64]
     float* sDbp = sBeta + 64;                                   // [4 lane quadrants][64]
     float* sGtot = sDbp + 4 * 64;                               // [4][128]
@@ -1488,23 +1489,57 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = tid & (kD - 1), R = tid >> 7;
-    const int n = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / a.HV, hv = bh % a.HV, h = hv / a.G;
-    const int trow = b * a.T + n * kC;
-    const size_t row0 = (size_t)bh * a.T + (size_t)n * kC;
-    const size_t cc0 = ((size_t)bh * a.NT + n) * kC * kC;
     const uint32_t lane_off = (uint32_t)((c >> 5) * 32) << 16;
+    const int total = a.BH * a.NT;   // chunks; CTA i takes chunks i, i + grid, ...
 
-    // dTv (fp32) staged asynchronously; row i, 16-byte chunk qd lands in chunk
-    // qd ^ (i & 7), so a thread reading its own row's chunks meets no bank
-    // conflict within 8 lanes
+    // thread 0's counts of issued and consumed loads (every load is waited for
+    // before the CTA exits)
+    int main_issued = 0, g_issued = 0, main_waited = 0, g_waited = 0;
+    // k, q tiles; dW into the top half of [dW; Y]; T (hi, lo) tiles; dAqk rows
+    // into the rows 32R + 16 + u of [dA; dAqk]
+    auto issue_main = [&](int ch) {
+        const int nn = ch % a.NT, bb = ch / a.NT, hvv = bb % a.HV, hh = hvv / a.G;
+        const int tr = (bb / a.HV) * a.T + nn * kC, rw = bb * a.T + nn * kC, c64 = ch * kC;
+        mbar_arrive_expect_tx(bar_tma, 2 * 16384 + 16384 + 2 * 8192 + 8192);
+        tma_load_3d(smem + LB_K, &tm_k, bar_tma, 0, hh, tr);
+        tma_load_3d(smem + LB_K + 8192, &tm_k, bar_tma, 64, hh, tr);
+        tma_load_3d(smem + LB_Q, &tm_q, bar_tma, 0, hh, tr);
+        tma_load_3d(smem + LB_Q + 8192, &tm_q, bar_tma, 64, hh, tr);
+        tma_load_2d(smem + LB_DWY, &tm_dw, bar_tma, 0, rw);
+        tma_load_2d(smem + LB_DWY + 16384, &tm_dw, bar_tma, 64, rw);
+        tma_load_2d(smem + LB_T, &tm_t, bar_tma, 0, c64);
+        tma_load_2d(smem + LB_TLO, &tm_tlo, bar_tma, 0, c64);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int ch = tid + e * kLocalTcThreads;
-        const int i = ch >> 4, qd = ch & 15;
-        cp_async16(sDtv + i * kC + ((qd ^ (i & 7)) << 2), a.dTv + cc0 + ch * 4);
-    }
-    cp_async_commit();
+        for (int RR = 0; RR < 4; ++RR)
+            tma_load_2d(smem + LB_DAQ + (32 * RR + 16) * 128, &tm_daq, bar_tma, 0, c64 + 16 * RR);
+        ++main_issued;
+    };
+    auto issue_g = [&](int ch) {
+        const int nn = ch % a.NT, bb = ch / a.NT, hvv = bb % a.HV;
+        const int tr = (bb / a.HV) * a.T + nn * kC;
+        mbar_arrive_expect_tx(bar_g, 16384);
+        tma_load_3d(smem + LB_G, &tm_g, bar_g, 0, hvv, tr);
+        tma_load_3d(smem + LB_G + 8192, &tm_g, bar_g, 64, hvv, tr);
+        ++g_issued;
+    };
+    // dTv (fp32) staged asynchronously by every thread; row i, 16-byte chunk
+    // qd lands in chunk qd ^ (i & 7), so a thread reading its own row's chunks
+    // meets no bank conflict within 8 lanes
+    auto issue_dtv = [&](int ch) {
+        const size_t cc = (size_t)ch * kC * kC;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int w = tid + e * kLocalTcThreads;
+            const int i = w >> 4, qd = w & 15;
+            cp_async16(sDtv + i * kC + ((qd ^ (i & 7)) << 2), a.dTv + cc + w * 4);
+        }
+        cp_async_commit();
+    };
+    auto load_beta = [&](int ch) {
+        const int nn = ch % a.NT, bb = ch / a.NT;
+        return __bfloat162float(
+            a.beta[((size_t)(bb / a.HV) * a.T + (size_t)nn * kC + tid) * a.HV + bb % a.HV]);
+    };
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
@@ -1512,40 +1547,45 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         mbar_init(bar_m2, 1);
         mbar_init(bar_m3, 1);
         mbar_init(bar_m4, 1);
+        mbar_init(bar_g, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
         tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
     }
-    if (tid < kC) {
-        sBeta[tid] = __bfloat162float(a.beta[((size_t)trow + tid) * a.HV + hv]);
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    if (tid == 0) {
-        // k, q, g tiles; dW into the top half of [dW; Y]; T (hi, lo) tiles;
-        // dAqk rows into the rows 32R + 16 + u of [dA; dAqk]
-        mbar_arrive_expect_tx(bar_tma, 3 * 16384 + 16384 + 2 * 8192 + 8192);
-        tma_load_3d(smem + LB_K, &tm_k, bar_tma, 0, h, trow);
-        tma_load_3d(smem + LB_K + 8192, &tm_k, bar_tma, 64, h, trow);
-        tma_load_3d(smem + LB_Q, &tm_q, bar_tma, 0, h, trow);
-        tma_load_3d(smem + LB_Q + 8192, &tm_q, bar_tma, 64, h, trow);
-        tma_load_3d(smem + LB_G, &tm_g, bar_tma, 0, hv, trow);
-        tma_load_3d(smem + LB_G + 8192, &tm_g, bar_tma, 64, hv, trow);
-        tma_load_2d(smem + LB_DWY, &tm_dw, bar_tma, 0, (int)row0);
-        tma_load_2d(smem + LB_DWY + 16384, &tm_dw, bar_tma, 64, (int)row0);
-        const int crow64 = (bh * a.NT + n) * kC;
-        tma_load_2d(smem + LB_T, &tm_t, bar_tma, 0, crow64);
-        tma_load_2d(smem + LB_TLO, &tm_tlo, bar_tma, 0, crow64);
-#pragma unroll
-        for (int RR = 0; RR < 4; ++RR)
-            tma_load_2d(smem + LB_DAQ + (32 * RR + 16) * 128, &tm_daq, bar_tma, 0,
-                        crow64 + 16 * RR);
+    if ((int)blockIdx.x < total) {
+        if (tid == 0) {
+            issue_g(blockIdx.x);
+            issue_main(blockIdx.x);
+        }
+        issue_dtv(blockIdx.x);
     }
-    bool ok = wait_bar_warp(bar_tma, 0, 41);
+    float beta_next = (tid < kC && (int)blockIdx.x < total) ? load_beta(blockIdx.x) : 0.f;
+    bool ok = true;
+
+#pragma unroll 1
+    for (int it = 0, chunk = blockIdx.x; chunk < total; ++it, chunk += gridDim.x) {
+    const uint32_t ph = it & 1;
+    const int next = chunk + gridDim.x;
+    const int n = chunk % a.NT, bh = chunk / a.NT;
+    const int b = bh / a.HV, hv = bh % a.HV;
+    const int trow = b * a.T + n * kC;
+    const size_t row0 = (size_t)bh * a.T + (size_t)n * kC;
+    const size_t cc0 = (size_t)chunk * kC * kC;
+    if (tid < kC) {
+        sBeta[tid] = beta_next;                          // read after later barriers
+        if (next < total) beta_next = load_beta(next);   // in flight meanwhile
+    }
+    {
+        const bool got = wait_bar_warp(bar_g, ph, 46);
+        if (got) ++g_waited;
+        ok = ok && got;
+    }
 
     const uint32_t kbo = (c >> 6) * 8192, cc = c & 63;
     auto ldt = [&](uint32_t tile, int r) {
@@ -1555,18 +1595,23 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     auto st = [&](uint32_t off, float x) {
         *reinterpret_cast<__nv_bfloat16*>(smem + off) = __float2bfloat16_rn(x);
     };
-    // ---- cumsum (thread (c, R): rows 16R..16R+15 of channel c) ----
+    // ---- cumsum (thread (c, R): rows 16R..16R+15 of channel c); the gate mask
+    // [g >= -5] of the rows is kept for dg, so the g tile is free afterwards ----
     float G[16];
+    uint32_t gmask = 0;
     {
         float acc = 0.f;
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-            acc += fmaxf(ldt(LB_G, 16 * R + u), kGateFloor);
+            const float gv = ldt(LB_G, 16 * R + u);
+            gmask |= (gv >= kGateFloor ? 1u : 0u) << u;
+            acc += fmaxf(gv, kGateFloor);
             G[u] = acc;
         }
         sGtot[R * kD + c] = acc;
     }
     __syncthreads();
+    if (tid == 0 && next < total) issue_g(next);   // the next chunk's g tile
     float off = 0.f, Glast = 0.f;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
@@ -1582,6 +1627,11 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
     for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
     const float eGbR = __expf(Gb[R]), eLbR = __expf(Glast - Gb[R]);
+    {
+        const bool got = wait_bar_warp(bar_tma, ph, 41);
+        if (got) ++main_waited;
+        ok = ok && got;
+    }
 
     // ---- build bf16 operands: Y, Right_R (own block; the copies for later
     // blocks follow while P1/P2 run), Lcol ----
@@ -1644,7 +1694,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         *reinterpret_cast<uint4*>(smem + LB_RIGHT + right_rel(Rd) + kb * (16u * (Rd + 1) * 128u) +
                                   co) = pack8(x);
     }
-    ok = ok && wait_bar_warp(bar_m1, 0, 42);
+    ok = ok && wait_bar_warp(bar_m1, ph, 42);
     tc_fence_after();
     // Epilogues below run in the warps of TMEM quadrants 0 and 1 (c < 64):
     // thread (c, R) owns row c of a 64 x 64 result, columns 16R..16R+15.
@@ -1691,7 +1741,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             mma_bf16(tmem + 128, sdesc_sw128(dtl + kk * 32), sdesc_sw128(th + kk * 32), id64, 1);
         mma_commit(bar_m3);
     }
-    ok = ok && wait_bar_warp(bar_m3, 0, 44);
+    ok = ok && wait_bar_warp(bar_m3, ph, 44);
     tc_fence_after();
     if (ok && c < kC) {
         float r16[16], s16[16];
@@ -1724,7 +1774,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                      sdesc_mn_sw128(yh + kk * 2048, 8192), id64, 1);
         mma_commit(bar_m4);
     }
-    ok = ok && wait_bar_warp(bar_m4, 0, 45);
+    ok = ok && wait_bar_warp(bar_m4, ph, 45);
     tc_fence_after();
     // dA = -mask_strict(T^T Y2) (bf16) into the row-side and column-side B tiles
     if (ok && c < kC) {
@@ -1780,7 +1830,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         cp_async16(smem + lb_dkb_row(r) + c4 * 4, a.dKb + (row0 + r) * kD + c4);
     }
     cp_async_commit();
-    ok = ok && wait_bar_warp(bar_m2, 0, 43);
+    ok = ok && wait_bar_warp(bar_m2, ph, 43);
     tc_fence_after();
     cp_async_wait_all16();
     __syncthreads();
@@ -1847,9 +1897,16 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int u = 0; u < 16; ++u) bsum += dG[u];
     sGtot[R * kD + c] = bsum;
     sLast[R * kD + c] = lastp;
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // k, q, [dW; Y], T, [dA; dAqk] and the staging areas have been read: the
+    // next chunk's loads start while this chunk's tail runs
+    if (next < total && ok) {
+        if (tid == 0) issue_main(next);
+        issue_dtv(next);
+    }
     {
         // dG_last += sum_r dKb_r Kb_r + dgam gam; it enters every row's suffix sum
         float extra = a.dgam[((size_t)bh * a.NT + n) * kD + c] * __expf(Glast);
@@ -1862,13 +1919,28 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             run += dG[u];
             const int t = 16 * R + u;
             const size_t ig = (((size_t)trow + t) * a.HV + hv) * kD + c;
-            a.dg[ig] = __float2bfloat16_rn(ldt(LB_G, t) >= kGateFloor ? run : 0.f);
+            a.dg[ig] = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
         }
     }
     if (tid < kC)
         a.dbeta[((size_t)trow + tid) * a.HV + hv] =
             __float2bfloat16_rn((sDbp[tid] + sDbp[64 + tid]) + (sDbp[128 + tid] + sDbp[192 + tid]) +
                                 a.dbv[row0 + tid]);
+    // partial sums, beta and TMEM are reused by the next chunk
+    tc_fence_before();
+    if (!__syncthreads_and(ok)) break;
+    tc_fence_after();
+    }  // chunk loop
+    // loads issued for chunks the loop did not reach (after an error) land
+    // before shared memory is released
+    cp_async_wait_all16();
+    if (tid == 0) {
+        for (; main_waited < main_issued; ++main_waited) wait_bar_drain(bar_tma, main_waited & 1);
+        for (; g_waited < g_issued; ++g_waited) wait_bar_drain(bar_g, g_waited & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
@@ -2031,6 +2103,7 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
     a.HV = d.HV;
     a.NT = d.T / kC;
     a.G = d.HV / d.H;
+    a.BH = d.B * d.HV;
     a.scale = d.scale;
     a.dQh = p.dQh;
     a.dKb = p.dKb;
@@ -2052,8 +2125,9 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
         return KDA_ERR_CUDA;
     {
         TimedLaunch tl("tc_local_bwd", s);
-        local_bwd_tc_kernel<<<dim3(d.T / kC, d.B * d.HV), kLocalTcThreads, LOCAL_TC_SMEM, s>>>(
-            mk, mq, mg, mdw, mt, mtl, mda, a);
+        // persistent: one CTA per SM walks the chunks
+        local_bwd_tc_kernel<<<std::min(a.BH * a.NT, sm_count()), kLocalTcThreads, LOCAL_TC_SMEM,
+                              s>>>(mk, mq, mg, mdw, mt, mtl, mda, a);
     }
     return launch_status();
 }
