@@ -1493,8 +1493,13 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int total = a.BH * a.NT;   // chunks; CTA i takes chunks i, i + grid, ...
 
     // thread 0's counts of issued and consumed loads (every load is waited for
-    // before the CTA exits)
-    int main_issued = 0, g_issued = 0, main_waited = 0, g_waited = 0;
+    // before the CTA exits), kept in shared memory so that they hold no
+    // register in the other threads
+    int* cnt = reinterpret_cast<int*>(sLast + 4 * kD);   // [main issued, g issued, main, g waited]
+    int& main_issued = cnt[0];
+    int& g_issued = cnt[1];
+    int& main_waited = cnt[2];
+    int& g_waited = cnt[3];
     // k, q tiles; dW into the top half of [dW; Y]; T (hi, lo) tiles; dAqk rows
     // into the rows 32R + 16 + u of [dA; dAqk]
     auto issue_main = [&](int ch) {
@@ -1549,6 +1554,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         mbar_init(bar_m4, 1);
         mbar_init(bar_g, 1);
         fence_mbar_init();
+        cnt[0] = cnt[1] = cnt[2] = cnt[3] = 0;
     }
     if (warp == 0) {
         tmem_alloc(tmem_holder, 512);
@@ -1583,7 +1589,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     {
         const bool got = wait_bar_warp(bar_g, ph, 46);
-        if (got) ++g_waited;
+        if (got && tid == 0) ++g_waited;
         ok = ok && got;
     }
 
@@ -1629,7 +1635,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const float eGbR = __expf(Gb[R]), eLbR = __expf(Glast - Gb[R]);
     {
         const bool got = wait_bar_warp(bar_tma, ph, 41);
-        if (got) ++main_waited;
+        if (got && tid == 0) ++main_waited;
         ok = ok && got;
     }
 
