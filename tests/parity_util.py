@@ -2,6 +2,8 @@
 the float64 oracle on the same (dtype-rounded) inputs, whole or per head."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -24,6 +26,10 @@ def assert_close(name, got, ref, dtype):
     bound = atol + rtol * np.abs(ref)
     bad = err > bound
     fro = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30)
+    if os.environ.get("KDA_PARITY_REPORT"):
+        # worst error as a fraction of its bound: the margin left in the bar
+        print(f"[parity] {name}: worst err/bound {float(np.max(err / bound)):.3f}, "
+              f"max abs err {float(err.max()):.3g}, rel fro err {fro:.3g}")
     if bad.any():
         idx = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(
