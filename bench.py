@@ -394,29 +394,64 @@ def main():
     value = world * w.tokens / (ms / 1e3)
 
     # ---- end to end: pinned host buffers, copies inside the timed region ----
-    h_in = {n: inp[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "do")}
-    h_out = {n: torch.empty_like(x, device="cpu").pin_memory()
-             for n, x in (("o", o), ("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta))}
-    d_in = {n: torch.empty_like(inp[n]) for n in h_in}
+    # Each step copies its inputs host -> device and its outputs device -> host.
+    # The copies run on their own streams, double-buffered on the device, so
+    # that step i's inputs arrive and step i-1's outputs leave while step i-1
+    # (i) computes; events order every reuse of a buffer.
+    names_in = ("q", "k", "v", "g", "beta", "do")
+    h_in = {n: inp[n].cpu().pin_memory() for n in names_in}
+    outs = (("o", v), ("dq", q), ("dk", k), ("dv", v), ("dg", g), ("dbeta", beta))
+    h_out = {n: torch.empty_like(x, device="cpu").pin_memory() for n, x in outs}
+    d_in = [{n: torch.empty_like(inp[n]) for n in names_in} for _ in range(2)]
+    d_out = [{n: torch.empty_like(x) for n, x in outs} for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in h_in.values())
     d2h = sum(x.numel() * x.element_size() for x in h_out.values())
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    ev_in, ev_comp, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for e_ in ev_comp + ev_out:
+        e_.record(stream)
 
-    def e2e_step():
-        for n in h_in:
-            d_in[n].copy_(h_in[n], non_blocking=True)
-        fwd_bwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"], d_in["do"])
-        h_out["o"].copy_(o, non_blocking=True)
-        for n in ("dq", "dk", "dv", "dg", "dbeta"):
-            h_out[n].copy_(grads[n], non_blocking=True)
+    def e2e_step(i):
+        j = i & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_comp[j])            # step i-2 has read this input set
+            for n in names_in:
+                d_in[j][n].copy_(h_in[n], non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])               # step i-2's outputs have left
+        x, y = d_in[j], d_out[j]
+        if saving:
+            _, _, sv = kda.chunk_kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                         chunk_size=w.chunk, impl=args.path, workspace=ws_b,
+                                         out=y["o"], save_for_backward=True)
+            kda.chunk_kda_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"],
+                              chunk_size=w.chunk, impl=args.path, grads=y, saved=sv)
+        else:
+            kda.chunk_kda_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], chunk_size=w.chunk,
+                              impl=args.path, workspace=ws_f, out=y["o"])
+            kda.chunk_kda_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"],
+                              chunk_size=w.chunk, impl=args.path, workspace=ws_b, grads=y)
+        ev_comp[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[j])
+            for n in h_out:
+                h_out[n].copy_(y[n], non_blocking=True)
+            ev_out[j].record(s_out)
 
-    e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_event(ev_out[(args.steps - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
