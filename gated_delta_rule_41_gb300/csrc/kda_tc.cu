@@ -1234,20 +1234,23 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     ok = ok && wait_bar_warp(bar_a, ph, 32);
     tc_fence_after();
-    if (ok && warp < 4) {
-        // warp R reads block R: lanes 0-15 -> A rows, 16-31 -> Aqk rows
+    if (ok && warp < 8) {
+        // warps R and R + 4 read block R (TMEM quadrant R); lanes 0-15 of warp R
+        // write its A rows, lanes 16-31 of warp R + 4 its Aqk rows, so that no
+        // warp runs both branches
+        const int Rq = warp & 3;
         float d[64];
-        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + right_col(warp);
-        if (warp == 0) intra_read_block<0>(taddr, d);
-        else if (warp == 1) intra_read_block<1>(taddr, d);
-        else if (warp == 2) intra_read_block<2>(taddr, d);
+        const uint32_t taddr = tmem + ((uint32_t)(Rq * 32) << 16) + right_col(Rq);
+        if (Rq == 0) intra_read_block<0>(taddr, d);
+        else if (Rq == 1) intra_read_block<1>(taddr, d);
+        else if (Rq == 2) intra_read_block<2>(taddr, d);
         else intra_read_block<3>(taddr, d);
-        const int u = lane & 15, i = 16 * warp + u;
-        if (lane < 16) {
+        const int u = lane & 15, i = 16 * Rq + u;
+        if (warp < 4 && lane < 16) {
             const float bi = sBeta[i];
 #pragma unroll
             for (int j = 0; j < kC; ++j) sA[i * kAS + j] = j < i ? bi * d[j] : 0.f;
-        } else {
+        } else if (warp >= 4 && lane >= 16) {
             __nv_bfloat16* ap = a.Aqk2 + ((size_t)crow * kC + i) * kC;
 #pragma unroll
             for (int j = 0; j < kC; j += 8) {
