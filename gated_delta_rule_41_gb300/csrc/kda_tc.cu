@@ -1785,6 +1785,16 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     ok = ok && wait_bar_warp(bar_m4, ph, 45);
     tc_fence_after();
+    // stage the assembly's fp32 inputs dQh (into the [dW; Y] area) and dKb
+    // (rows 0..31 into the dTv area, 32..47 into T, 48..63 into T's low part):
+    // all of them were last read by P4
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int ch = tid + e * kLocalTcThreads, r = ch >> 5, c4 = (ch & 31) * 4;
+        cp_async16(smem + LB_DWY + r * 512 + c4 * 4, a.dQh + (row0 + r) * kD + c4);
+        cp_async16(smem + lb_dkb_row(r) + c4 * 4, a.dKb + (row0 + r) * kD + c4);
+    }
+    cp_async_commit();
     // dA = -mask_strict(T^T Y2) (bf16) into the row-side and column-side B tiles
     if (ok && c < kC) {
         float r16[16], s16[16];
@@ -1829,16 +1839,6 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         mma_commit(bar_m2);
     }
-    // stage the assembly's fp32 inputs dQh (into the [dW; Y] area) and dKb
-    // (rows 0..31 into the dTv area, 32..47 into T, 48..63 into T's low part):
-    // all of them were last read by P4
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int ch = tid + e * kLocalTcThreads, r = ch >> 5, c4 = (ch & 31) * 4;
-        cp_async16(smem + LB_DWY + r * 512 + c4 * 4, a.dQh + (row0 + r) * kD + c4);
-        cp_async16(smem + lb_dkb_row(r) + c4 * 4, a.dKb + (row0 + r) * kD + c4);
-    }
-    cp_async_commit();
     ok = ok && wait_bar_warp(bar_m2, ph, 43);
     tc_fence_after();
     cp_async_wait_all16();
