@@ -1299,7 +1299,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     // X = A_10 T_00 into A's unused upper block (rows 0..31, columns 32..63)
     {
         const int jj = lane, i0 = 2 * warp;
-        float x0 = 0.f, x1 = 0.f;
+        float x0 = 0.f, x1 = 0.f, y0 = 0.f, y1 = 0.f;   // two chains per row
         const float* a0 = sA + (32 + i0) * kAS;
         const float* a1 = a0 + kAS;
 #pragma unroll
@@ -1308,17 +1308,23 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             const float4 q = *reinterpret_cast<const float4*>(a1 + m);
             const float t0 = sT[m * kAS + jj], t1 = sT[(m + 1) * kAS + jj];
             const float t2 = sT[(m + 2) * kAS + jj], t3 = sT[(m + 3) * kAS + jj];
-            x0 += p.x * t0 + p.y * t1 + p.z * t2 + p.w * t3;
-            x1 += q.x * t0 + q.y * t1 + q.z * t2 + q.w * t3;
+            x0 = fmaf(p.x, t0, x0);
+            y0 = fmaf(p.y, t1, y0);
+            x1 = fmaf(q.x, t0, x1);
+            y1 = fmaf(q.y, t1, y1);
+            x0 = fmaf(p.z, t2, x0);
+            y0 = fmaf(p.w, t3, y0);
+            x1 = fmaf(q.z, t2, x1);
+            y1 = fmaf(q.w, t3, y1);
         }
-        sA[i0 * kAS + 32 + jj] = x0;
-        sA[(i0 + 1) * kAS + 32 + jj] = x1;
+        sA[i0 * kAS + 32 + jj] = x0 + y0;
+        sA[(i0 + 1) * kAS + 32 + jj] = x1 + y1;
     }
     __syncthreads();
     // T_10 = -T_11 X
     {
         const int jj = lane, i0 = 2 * warp;
-        float y0 = 0.f, y1 = 0.f;
+        float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;   // two chains per row
         const float* r0 = sT + (32 + i0) * kAS + 32;
         const float* r1 = r0 + kAS;
 #pragma unroll
@@ -1327,11 +1333,17 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             const float4 q = *reinterpret_cast<const float4*>(r1 + m);
             const float x0 = sA[m * kAS + 32 + jj], x1 = sA[(m + 1) * kAS + 32 + jj];
             const float x2 = sA[(m + 2) * kAS + 32 + jj], x3 = sA[(m + 3) * kAS + 32 + jj];
-            y0 += p.x * x0 + p.y * x1 + p.z * x2 + p.w * x3;
-            y1 += q.x * x0 + q.y * x1 + q.z * x2 + q.w * x3;
+            y0 = fmaf(p.x, x0, y0);
+            z0 = fmaf(p.y, x1, z0);
+            y1 = fmaf(q.x, x0, y1);
+            z1 = fmaf(q.y, x1, z1);
+            y0 = fmaf(p.z, x2, y0);
+            z0 = fmaf(p.w, x3, z0);
+            y1 = fmaf(q.z, x2, y1);
+            z1 = fmaf(q.w, x3, z1);
         }
-        sT[(32 + i0) * kAS + jj] = -y0;
-        sT[(32 + i0 + 1) * kAS + jj] = -y1;
+        sT[(32 + i0) * kAS + jj] = -(y0 + z0);
+        sT[(32 + i0 + 1) * kAS + jj] = -(y1 + z1);
     }
     __syncthreads();
     // T (bf16 high and low parts) to global; T*beta to the B-operand tile.
