@@ -56,11 +56,11 @@ def _src_hash(name):
 # Measured at B=1, T=8192 (2048 chunks, inputs and workspace above L2),
 # scaled by the chunk count to the B=4 launch (8192 chunks).
 NCU_TRAFFIC = {
-    "tc_local_bwd": (4 * (354545408 + 78717696), "kda_tc.cu", "daa97945830f"),
-    "tc_intra": (4 * (134708224 + 133925376), "kda_tc.cu", "daa97945830f"),
-    "tc_grad_v": (4 * (285914112 + 205229056), "kda_tc.cu", "daa97945830f"),
-    "tc_chain_fwd_save": (4 * (152110080 + 91291648), "kda_tc.cu", "daa97945830f"),
-    "tc_chain_bwd": (4 * (152088832 + 65049600), "kda_tc.cu", "daa97945830f"),
+    "tc_local_bwd": (4 * (354624256 + 78924800), "kda_tc.cu", "091c58e33e8c"),
+    "tc_intra": (4 * (134799872 + 132511232), "kda_tc.cu", "091c58e33e8c"),
+    "tc_grad_v": (4 * (286091520 + 199869952), "kda_tc.cu", "091c58e33e8c"),
+    "tc_chain_fwd_save": (4 * (152091648 + 90978560), "kda_tc.cu", "091c58e33e8c"),
+    "tc_chain_bwd": (4 * (152133376 + 63938560), "kda_tc.cu", "091c58e33e8c"),
 }
 
 
