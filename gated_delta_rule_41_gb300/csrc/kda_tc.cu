@@ -1718,12 +1718,19 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     ok = ok && wait_bar_warp(bar_m1, ph, 42);
     tc_fence_after();
     // Epilogues below run in the warps of TMEM quadrants 0 and 1 (c < 64):
-    // thread (c, R) owns row c of a 64 x 64 result, columns 16R..16R+15.
-    auto split_st = [&](uint32_t hi, uint32_t lo, uint32_t off, float x) {
-        const __nv_bfloat16 h16 = __float2bfloat16_rn(x);
-        *reinterpret_cast<__nv_bfloat16*>(smem + hi + off) = h16;
-        *reinterpret_cast<__nv_bfloat16*>(smem + lo + off) =
-            __float2bfloat16_rn(x - __bfloat162float(h16));
+    // thread (c, R) owns row c of a 64 x 64 result, columns 16R..16R+15,
+    // written as two 16-byte units per tile (a warp's 32 rows then fill all
+    // banks; single bf16 stores down a column would conflict 4 ways).
+    // split8 stores x as bf16 hi + lo parts at byte offset off of two tiles.
+    auto split8 = [&](uint32_t hi, uint32_t lo, uint32_t off, const float (&x)[8]) {
+        float h[8], l[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            h[e] = __bfloat162float(__float2bfloat16_rn(x[e]));
+            l[e] = x[e] - h[e];
+        }
+        *reinterpret_cast<uint4*>(smem + hi + off) = pack8(h);
+        *reinterpret_cast<uint4*>(smem + lo + off) = pack8(l);
     };
     // ---- dT = mask_strict(beta_m dTv + dW Y^T), split hi + lo ----
     if (ok && c < kC) {
@@ -1731,16 +1738,21 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         tmem_ld16(tmem + lane_off + 16 * R, r16);
         const int i = c;
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const float4 t4 =
-                *reinterpret_cast<const float4*>(sDtv + i * kC + (((4 * R + x) ^ (i & 7)) << 2));
-            const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+        for (int hh = 0; hh < 2; ++hh) {
+            float x8[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = 16 * R + 4 * x + e;
-                split_st(LB_DTH, LB_DTL, sw128_offset(i, m),
-                         m < i ? sBeta[m] * tv[e] + r16[4 * x + e] : 0.f);
+            for (int x = 0; x < 2; ++x) {
+                const int q4 = 4 * R + 2 * hh + x;
+                const float4 t4 =
+                    *reinterpret_cast<const float4*>(sDtv + i * kC + ((q4 ^ (i & 7)) << 2));
+                const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = 4 * q4 + e;
+                    x8[4 * x + e] = m < i ? sBeta[m] * tv[e] + r16[8 * hh + 4 * x + e] : 0.f;
+                }
             }
+            split8(LB_DTH, LB_DTL, sw128_offset(i, 16 * R + 8 * hh), x8);
         }
     }
     fence_async_smem();
@@ -1769,8 +1781,12 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         tmem_ld16(tmem + lane_off + 128 + 16 * R, r16);
         tmem_ld16(tmem + lane_off + 192 + 16 * R, s16);
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-            split_st(LB_Y2H, LB_Y2L, sw128_offset(c, 16 * R + e), r16[e] + s16[e]);
+        for (int hh = 0; hh < 2; ++hh) {
+            float x8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x8[e] = r16[8 * hh + e] + s16[8 * hh + e];
+            split8(LB_Y2H, LB_Y2L, sw128_offset(c, 16 * R + 8 * hh), x8);
+        }
     }
     fence_async_smem();
     tc_fence_before();
@@ -1814,10 +1830,14 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         tmem_ld16(tmem + lane_off + 320 + 16 * R, s16);
         const int i = c, t2 = 32 * (i >> 4) + (i & 15);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int j = 16 * R + e;
-            const float v = j < i ? -(r16[e] + s16[e]) : 0.f;
-            st(LB_DAQ + sw128_offset(t2, j), v);
+        for (int hh = 0; hh < 2; ++hh) {
+            float x8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = 16 * R + 8 * hh + e;
+                x8[e] = j < i ? -(r16[8 * hh + e] + s16[8 * hh + e]) : 0.f;
+            }
+            *reinterpret_cast<uint4*>(smem + LB_DAQ + sw128_offset(t2, 16 * R + 8 * hh)) = pack8(x8);
         }
     }
     fence_async_smem();
