@@ -68,13 +68,18 @@ constexpr uint32_t OFF_Q = 16384;      // same for Qh
 constexpr uint32_t OFF_KBT = 32768;    // Kb: 64 rows (c) x 128 bf16 (k), 2 k-blocks
 constexpr uint32_t OFF_AQK = 49152;    // Aqk: 64 rows x 64 bf16
 constexpr uint32_t OFF_U = 57344;      // U: 64 x 128 bf16, row-major, unswizzled
-constexpr uint32_t OFF_GAM = 73728;    // gam: 128 fp32
-constexpr uint32_t STAGE_BYTES = 74752;
-constexpr uint32_t STAGE_TX = 16384 * 2 + 16384 + 8192 + 16384 + 512;
-constexpr uint32_t OFF_S = 2 * STAGE_BYTES;    // S^T operand: 128 rows x 128 bf16 (2 k-blocks)
-constexpr uint32_t OFF_DELTA = OFF_S + 32768;  // delta^T operand: 128 rows x 64 bf16
-constexpr uint32_t OFF_BAR = OFF_DELTA + 16384;
+constexpr uint32_t STAGE_BYTES = 73728;
+constexpr uint32_t STAGE_TX = 16384 * 2 + 16384 + 8192 + 16384 + 512;   // tiles + gam
+// S^T operand tiles (128 rows x 128 bf16, 2 k-blocks), one per chunk parity:
+// the state store of chunk n may still be reading its tile while the state
+// of chunk n + 1 is written to the other
+constexpr uint32_t OFF_S = 2 * STAGE_BYTES;
+constexpr uint32_t S_TILE = 32768;
+constexpr uint32_t OFF_DELTA = OFF_S + 2 * S_TILE;  // delta^T operand: 128 rows x 64 bf16
+constexpr uint32_t OFF_GAM = OFF_DELTA + 16384;     // gam (128 fp32) of each stage, 512 B apart
+constexpr uint32_t OFF_BAR = OFF_GAM + 1024;
 constexpr uint32_t CHAIN_SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
+static_assert(CHAIN_SMEM <= 232448, "chain kernels exceed the per-CTA shared memory limit");
 
 // TMA warp, MMA warp, 8 epilogue warps (two per TMEM lane quadrant)
 constexpr int kChainThreads = 320, kChainEpi = 256;
@@ -144,17 +149,16 @@ __device__ __forceinline__ void tile_row_to_global(const uint8_t* tile, uint32_t
 // The chains' epilogue has two threads per value column v (TMEM lane); each
 // takes one half of the columns of a step.
 
-// State step, columns k in [64 half, 64 half + 64): S^T (lane v) from TMEM --
-// or, for the first chunk, from `init` ([K][V] fp32, may be null = zeros) --
-// to k-block `half` of the bf16 K-major operand tile, then arrive on
-// `bar_tile` (the products that read the tile may start); then the TMEM copy
-// is scaled by gam (per column k) and stored back, and the thread arrives on
-// `bar_tmem` (the products that accumulate into it may start).
-__device__ __forceinline__ void chain_state_step(uint32_t tS, uint8_t* tile, const float* gam,
-                                                 bool first, const float* init, int v, int half,
-                                                 uint64_t* bar_tile, uint64_t* bar_tmem) {
+// State step, columns k in [64 half, 64 half + 64), in two parts.  First:
+// S^T (lane v) from TMEM -- or, for the first chunk, from `init` ([K][V]
+// fp32, may be null = zeros) -- into r0, r1 and to k-block `half` of the bf16
+// K-major operand tile, then arrive on `bar_tile` (the products that read
+// the tile may start).
+__device__ __forceinline__ void chain_state_tile(uint32_t tS, uint8_t* tile, bool first,
+                                                 const float* init, int v, int half,
+                                                 uint64_t* bar_tile, float (&r0)[32],
+                                                 float (&r1)[32]) {
     const int k0 = 64 * half;
-    float r0[32], r1[32];
     if (first) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -173,6 +177,14 @@ __device__ __forceinline__ void chain_state_step(uint32_t tS, uint8_t* tile, con
     fence_async_smem();
     tc_fence_before();  // earlier TMEM reads of this thread precede the MMAs it releases
     mbar_arrive(bar_tile);
+}
+// Second part (gam is in the chunk's stage): the TMEM copy is scaled by gam
+// (per column k) and stored back, then the thread arrives on `bar_tmem` (the
+// products that accumulate into it may start).
+__device__ __forceinline__ void chain_state_rescale(uint32_t tS, const float* gam, int half,
+                                                    uint64_t* bar_tmem, float (&r0)[32],
+                                                    float (&r1)[32]) {
+    const int k0 = 64 * half;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         r0[i] *= gam[k0 + i];
@@ -185,28 +197,28 @@ __device__ __forceinline__ void chain_state_step(uint32_t tS, uint8_t* tile, con
     mbar_arrive(bar_tmem);
 }
 
-// Delta step, columns c in [32 half, 32 half + 32) of 64: from TMEM (U - D if
-// U is given) to the bf16 K-major operand tile (negated if `neg_tile`),
-// arrive on bar1 and bar2, then the true-sign bf16 values to out[c][v] (row
-// stride kD) if given.
-__device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile,
-                                                 const __nv_bfloat16* U, bool neg_tile, int v,
-                                                 int half, uint64_t* bar1, uint64_t* bar2,
-                                                 __nv_bfloat16* out) {
+// Delta step, columns c in [32 half, 32 half + 32) of 64: from TMEM (u - D if
+// u is given: the 32 values U[c][v], read before the products completed) to
+// the bf16 K-major operand tile (negated if `neg_tile`), arrive on bar1 and
+// bar2 (if given), then the true-sign bf16 values to out[c][v] (row stride
+// kD) if given.
+__device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile, const float* u,
+                                                 bool neg_tile, int v, int half, uint64_t* bar1,
+                                                 uint64_t* bar2, __nv_bfloat16* out) {
     const int c0 = 32 * half;
     float d0[32];
     tmem_ld32_nw(tD + c0, d0);
     tmem_wait_ld_dep(d0);
-    if (U) {
+    if (u) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) d0[i] = __bfloat162float(U[(c0 + i) * kD + v]) - d0[i];
+        for (int i = 0; i < 32; ++i) d0[i] = u[i] - d0[i];
     }
     const float sg = neg_tile ? -1.f : 1.f;
     store_row_bf16(tile, v, c0, d0, sg);
     fence_async_smem();
     tc_fence_before();
     mbar_arrive(bar1);
-    mbar_arrive(bar2);
+    if (bar2) mbar_arrive(bar2);
     if (out) tile_row_to_global(tile, 0, v, c0, 32, sg, out + v, kD);
 }
 
@@ -226,7 +238,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_aqk,
                  const __grid_constant__ CUtensorMap tm_u,
                  const __grid_constant__ CUtensorMap tm_hout,
-                 const __grid_constant__ CUtensorMap tm_dout, ChainArgs a) {
+                 const __grid_constant__ CUtensorMap tm_dout,
+                 const __grid_constant__ CUtensorMap tm_o, ChainArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -238,7 +251,9 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     uint64_t* bar_D3 = full + 7;
     uint64_t* bar_fin = full + 8;
     uint64_t* bar_Sx = full + 9;   // state rescaled in TMEM
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 10);
+    uint64_t* bar_o = full + 10;   // [2] the epilogue is done with a stage (and its U area)
+    uint64_t* bar_u = full + 12;   // every epilogue thread has read its U values
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 13);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
@@ -248,14 +263,17 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(&empty[0], kChainEpi + 1);
-        mbar_init(&empty[1], kChainEpi + 1);
+        mbar_init(&empty[0], 1);
+        mbar_init(&empty[1], 1);
         mbar_init(bar_S, kChainEpi);
         mbar_init(bar_delta, kChainEpi);
         mbar_init(bar_D12, 1);
         mbar_init(bar_D3, 1);
         mbar_init(bar_fin, 1);
         mbar_init(bar_Sx, kChainEpi);
+        mbar_init(&bar_o[0], kChainEpi);
+        mbar_init(&bar_o[1], kChainEpi);
+        mbar_init(bar_u, kChainEpi);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -275,10 +293,27 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             prefetch_tmap(&tm_kbt);
             prefetch_tmap(&tm_aqk);
             prefetch_tmap(&tm_u);
+            // Hands back the stage of epilogue iteration j (its U area then
+            // holds the output tile of chunk j - 1, stored here by TMA; its
+            // source must be read before the stage is refilled).
+            auto drain_o = [&](int j) -> bool {
+                const int sj = j & 1;
+                if (!wait_bar(&bar_o[sj], (j >> 1) & 1, 21)) return false;
+                if (a.o && j >= 1) {
+                    const int z = b * a.T + (j - 1) * kC;
+                    const uint8_t* tile = smem + sj * STAGE_BYTES + OFF_U;
+                    tma_store_3d(&tm_o, tile, 0, hv, z);
+                    tma_store_3d(&tm_o, tile + 8192, 64, hv, z);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                }
+                return true;
+            };
             int issued = 0;
             for (int n = 0; n < NT; ++n) {
                 const int s = n & 1;
                 if (!wait_bar(&empty[s], ((n >> 1) & 1) ^ 1, 1)) break;
+                if (n >= 2 && !drain_o(n - 2)) break;
                 uint8_t* st = smem + s * STAGE_BYTES;
                 mbar_arrive_expect_tx(&full[s], STAGE_TX);
                 const int row = bh * a.T + n * kC;
@@ -291,9 +326,27 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 tma_load_2d(st + OFF_KBT + 8192, &tm_kbt, &full[s], 64, row);
                 tma_load_2d(st + OFF_AQK, &tm_aqk, &full[s], 0, crow * kC);
                 tma_load_2d(st + OFF_U, &tm_u, &full[s], 0, row);
-                bulk_load(st + OFF_GAM, a.gam + (size_t)crow * kD, 512, &full[s]);
+                bulk_load(smem + OFF_GAM + s * 512, a.gam + (size_t)crow * kD, 512, &full[s]);
                 issued = n + 1;
+                // the chunk two ahead into L2, so that its stage load (issued
+                // once this one is consumed) does not wait on DRAM
+                if (n + 2 < NT) {
+                    const int row2 = row + 2 * kC, crow2 = crow + 2;
+                    tma_prefetch_2d(&tm_w, 0, row2);
+                    tma_prefetch_2d(&tm_w, 64, row2);
+                    tma_prefetch_2d(&tm_q, 0, row2);
+                    tma_prefetch_2d(&tm_q, 64, row2);
+                    tma_prefetch_2d(&tm_kbt, 0, row2);
+                    tma_prefetch_2d(&tm_kbt, 64, row2);
+                    tma_prefetch_2d(&tm_aqk, 0, crow2 * kC);
+                    tma_prefetch_2d(&tm_u, 0, row2);
+                    bulk_prefetch_l2(a.gam + (size_t)crow2 * kD, 512);
+                }
             }
+            // the epilogue's last two iterations (after an error, skipped)
+            for (int j = NT - 2 < 0 ? 0 : NT - 2; issued == NT && j < NT; ++j)
+                if (!drain_o(j)) break;
+            bulk_wait_all();
             // do not leave copies in flight: wait for the last stages issued
             for (int n = issued - 2 < 0 ? 0 : issued - 2; n < issued; ++n)
                 wait_bar(&full[n & 1], (n >> 1) & 1, 2);
@@ -318,11 +371,12 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 if (!wait_bar(bar_S, n & 1, 4)) break;
                 tc_fence_after();
                 const uint32_t tO = tmem + ((n & 1) ? TM_O1 : TM_O0);
+                const uint64_t dSn = dS + (uint64_t)((n & 1) * (S_TILE >> 4));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
                     const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_bf16(tmem + TM_W, dS + ka, dW0 + so + kb, idesc64, kk > 0);
+                    mma_bf16(tmem + TM_W, dSn + ka, dW0 + so + kb, idesc64, kk > 0);
                 }
                 // the delta step rewrites the delta tile once D12 completes: the
                 // previous delta's store must have read it
@@ -331,15 +385,10 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 // stores are issued after the products they would otherwise delay
                 if (a.h_out) {  // S_n^T tile (rows v) as it stands to h_out, by TMA
                     const int y = (bh * NT + n) * kD;
-                    tma_store_2d(&tm_hout, smem + OFF_S, 0, y);
-                    tma_store_2d(&tm_hout, smem + OFF_S + 16384, 64, y);
+                    uint8_t* tile = smem + OFF_S + (n & 1) * S_TILE;
+                    tma_store_2d(&tm_hout, tile, 0, y);
+                    tma_store_2d(&tm_hout, tile + 16384, 64, y);
                     bulk_commit_group();
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_bf16(tO, dS + ka, dQ0 + so + kb, idesc64, kk > 0);
                 }
                 if (!wait_bar(bar_delta, n & 1, 5)) break;
                 tc_fence_after();
@@ -350,10 +399,20 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     mma_bf16(tmem + TM_S, dD + ((kk * 32) >> 4), dKb0 + so + ((kk * 2048) >> 4),
                              idesc128 | kBMajorMN, 1);
                 // the next state step may start once the state update is done
-                // (and this chunk's state store has read the state tile); O_n
-                // is read only after the next chunk's D12, which also covers it
-                if (a.h_out) bulk_wait_read_all();
+                // and the previous chunk's state store (groups: its state,
+                // its delta, this chunk's state) has read the tile it will
+                // rewrite; O_n is read only after the next chunk's D12, which
+                // also covers it
+                if (a.h_out) bulk_wait_read_but2();
                 mma_commit(bar_D3);
+                // O_n = S_n Qh^T + delta Aqk^T, behind the state update (the
+                // S tile of parity n is rewritten only after the next D3)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    mma_bf16(tO, dSn + ka, dQ0 + so + kb, idesc64, kk > 0);
+                }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tO, dD + ((kk * 32) >> 4), dAq0 + so + ((kk * 32) >> 4), idesc64, 1);
@@ -373,23 +432,36 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         const int q = warp & 3, half = (warp - 2) >> 2;
         const int v = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        uint8_t* sS = smem + OFF_S;
         uint8_t* sDelta = smem + OFF_DELTA;
         float r[32];
         bool ok = true;
 
-        // E1: S_n -> bf16 operand tile; TMEM copy scaled by gam_n.
+        // E1: S_n -> bf16 operand tile (of parity n); then, once chunk n's
+        // stage (gam) has landed, the TMEM copy scaled by gam_n.
         auto e1 = [&](int n) -> bool {
             const int s = n & 1;
+            float r0[32], r1[32];
+            chain_state_tile(tmem + lane_off + TM_S, smem + OFF_S + s * S_TILE, n == 0,
+                             a.h0 ? a.h0 + (size_t)bh * kD * kD : nullptr, v, half, bar_S, r0, r1);
             if (!wait_bar_warp(&full[s], (n >> 1) & 1, 7)) return false;
-            const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + OFF_GAM);
-            chain_state_step(tmem + lane_off + TM_S, sS, gam, n == 0,
-                             a.h0 ? a.h0 + (size_t)bh * kD * kD : nullptr, v, half, bar_S,
-                             bar_Sx);
+            chain_state_rescale(tmem + lane_off + TM_S,
+                                reinterpret_cast<const float*>(smem + OFF_GAM + s * 512), half,
+                                bar_Sx, r0, r1);
             return true;
         };
 
-        // E3: output rows of chunk m (complete once D3 of chunk m has fired)
+        // E3: output rows of chunk m into a 128B-swizzled pair of [64 t][64 v]
+        // tiles at dst (a warp's lanes fill 64 contiguous bytes of one row)
+        auto o_tile = [&](int m, uint8_t* dst) {
+            const uint32_t tO = (m & 1) ? TM_O1 : TM_O0;
+            tmem_ld32(tmem + lane_off + tO + half * 32, r);
+            uint8_t* box = dst + (v >> 6) * 8192;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                *reinterpret_cast<__nv_bfloat16*>(box + sw128_offset(32 * half + i, v & 63)) =
+                    __float2bfloat16_rn(r[i]);
+        };
+        // the last chunk's output rows straight to global memory
         auto o_out = [&](int m) {
             const uint32_t tO = (m & 1) ? TM_O1 : TM_O0;
             tmem_ld32(tmem + lane_off + tO + half * 32, r);
@@ -402,15 +474,29 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         ok = e1(0);
         for (int n = 0; ok && n < NT; ++n) {
             const int s = n & 1;
-            // E2: delta^T = U^T - S^T W^T  -> bf16 operand tile
+            // E2: delta^T = U^T - S^T W^T  -> bf16 operand tile.  U (in the
+            // stage since E1 of this chunk) is read while the products run.
+            float u[32];
+            {
+                const __nv_bfloat16* U =
+                    reinterpret_cast<const __nv_bfloat16*>(smem + s * STAGE_BYTES + OFF_U);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) u[i] = __bfloat162float(U[(32 * half + i) * kD + v]);
+            }
             if (!wait_bar_warp(bar_D12, n & 1, 8)) { ok = false; break; }
             tc_fence_after();
-            const __nv_bfloat16* U =
-                reinterpret_cast<const __nv_bfloat16*>(smem + s * STAGE_BYTES + OFF_U);
-            chain_delta_step(tmem + lane_off + TM_W, sDelta, U, false, v, half, bar_delta, &empty[s],
+            chain_delta_step(tmem + lane_off + TM_W, sDelta, u, false, v, half, bar_delta, nullptr,
                              nullptr);
-            // the previous chunk's output while this chunk's state update runs
-            if (a.o && n > 0) o_out(n - 1);
+            // the previous chunk's output, while this chunk's state update
+            // runs, into the U area of this chunk's stage once every thread
+            // has read its U values; the TMA thread stores it
+            if (a.o) {
+                mbar_arrive(bar_u);
+                if (!wait_bar_warp(bar_u, n & 1, 22)) { ok = false; break; }
+                if (n > 0) o_tile(n - 1, smem + s * STAGE_BYTES + OFF_U);
+                fence_async_smem();
+            }
+            mbar_arrive(&bar_o[s]);
             if (!wait_bar_warp(bar_D3, n & 1, 9)) { ok = false; break; }
             tc_fence_after();
             if (n + 1 < NT) {
@@ -455,7 +541,6 @@ constexpr uint32_t RB_Q = 16384;     // Qh [64 t][128 k]
 constexpr uint32_t RB_W = 32768;     // W  [64 r][128 k]
 constexpr uint32_t RB_KBT = 49152;   // Kb [64 r][128 k]
 constexpr uint32_t RB_AQK = 65536;   // Aqk [64 t][64 r]
-constexpr uint32_t RB_GAM = 73728;
 constexpr uint32_t TM2_S = 0, TM2_DD = 128, TM2_COLS = 256;
 
 struct ChainBwdArgs {
@@ -537,8 +622,22 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 tma_load_2d(st + RB_KBT, &tm_kbt, &full[s], 0, row);
                 tma_load_2d(st + RB_KBT + 8192, &tm_kbt, &full[s], 64, row);
                 tma_load_2d(st + RB_AQK, &tm_aqk, &full[s], 0, crow * kC);
-                bulk_load(st + RB_GAM, a.gam + (size_t)crow * kD, 512, &full[s]);
+                bulk_load(smem + OFF_GAM + s * 512, a.gam + (size_t)crow * kD, 512, &full[s]);
                 issued = i + 1;
+                // the chunk two ahead (n - 2) into L2
+                if (n >= 2) {
+                    const int row2 = row - 2 * kC, crow2 = crow - 2, trow2 = trow - 2 * kC;
+                    tma_prefetch_3d(&tm_do, 0, hv, trow2);
+                    tma_prefetch_3d(&tm_do, 64, hv, trow2);
+                    tma_prefetch_2d(&tm_q, 0, row2);
+                    tma_prefetch_2d(&tm_q, 64, row2);
+                    tma_prefetch_2d(&tm_w, 0, row2);
+                    tma_prefetch_2d(&tm_w, 64, row2);
+                    tma_prefetch_2d(&tm_kbt, 0, row2);
+                    tma_prefetch_2d(&tm_kbt, 64, row2);
+                    tma_prefetch_2d(&tm_aqk, 0, crow2 * kC);
+                    bulk_prefetch_l2(a.gam + (size_t)crow2 * kD, 512);
+                }
             }
             for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
                 wait_bar(&full[i & 1], (i >> 1) & 1, 12);
@@ -560,16 +659,18 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 if (!wait_bar(&full[s], (i >> 1) & 1, 13)) break;
                 if (!wait_bar(bar_S, i & 1, 14)) break;
                 tc_fence_after();
-                {  // dS^T tile (rows v) of chunk n = NT-1-i to dh_out, by TMA
+                const uint64_t dSi = dS + (uint64_t)((i & 1) * (S_TILE >> 4));
+                {  // dS^T tile (rows v, parity i) of chunk n = NT-1-i to dh_out, by TMA
                     const int y = (bh * NT + (NT - 1 - i)) * kD;
-                    tma_store_2d(&tm_dhout, smem + OFF_S, 0, y);
-                    tma_store_2d(&tm_dhout, smem + OFF_S + 16384, 64, y);
+                    uint8_t* tile = smem + OFF_S + (i & 1) * S_TILE;
+                    tma_store_2d(&tm_dhout, tile, 0, y);
+                    tma_store_2d(&tm_dhout, tile + 16384, 64, y);
                     bulk_commit_group();
                 }
                 // ddelta^T = dS^T Kb^T  (B = Kb tile [64 r][128 k], K-major)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + TM2_DD, dS + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                    mma_bf16(tmem + TM2_DD, dSi + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
                              dKb0 + so + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), id64, kk > 0);
                 // ddelta^T += dO^T Aqk
 #pragma unroll
@@ -591,7 +692,9 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + TM2_S, dD + ((kk * 32) >> 4), dW0 + so + ((kk * 2048) >> 4),
                              id128 | kBMajorMN, 1);
-                bulk_wait_read_all();  // the next state step rewrites the tile
+                // the next state step rewrites the tile of the previous chunk's
+                // store: all but this chunk's store have read their tiles
+                bulk_wait_read_but1();
                 mma_commit(bar_D4);
                 mma_commit(&empty[s]);
             }
@@ -603,19 +706,22 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
         const int q = warp & 3, half = (warp - 2) >> 2;
         const int v = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        uint8_t* sS = smem + OFF_S;
         uint8_t* sDelta = smem + OFF_DELTA;
         float r[32];
         bool ok = true;
 
-        // E1: dS (end of chunk n) -> bf16 operand tile and dh_out; TMEM copy scaled by gam_n.
+        // E1: dS (end of chunk n) -> bf16 operand tile (of parity i); then,
+        // once the chunk's stage (gam) has landed, the TMEM copy scaled by gam_n.
         auto e1 = [&](int i) -> bool {
-            const int n = NT - 1 - i, s = i & 1;
+            const int s = i & 1;
+            float r0[32], r1[32];
+            chain_state_tile(tmem + lane_off + TM2_S, smem + OFF_S + s * S_TILE, i == 0,
+                             a.dht ? a.dht + (size_t)bh * kD * kD : nullptr, v, half, bar_S, r0,
+                             r1);
             if (!wait_bar_warp(&full[s], (i >> 1) & 1, 17)) return false;
-            const float* gam = reinterpret_cast<const float*>(smem + s * STAGE_BYTES + RB_GAM);
-            chain_state_step(tmem + lane_off + TM2_S, sS, gam, i == 0,
-                             a.dht ? a.dht + (size_t)bh * kD * kD : nullptr, v, half, bar_S,
-                             bar_Sx);
+            chain_state_rescale(tmem + lane_off + TM2_S,
+                                reinterpret_cast<const float*>(smem + OFF_GAM + s * 512), half,
+                                bar_Sx, r0, r1);
             return true;
         };
 
@@ -1249,7 +1355,10 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         if (warp < 4 && lane < 16) {
             const float bi = sBeta[i];
 #pragma unroll
-            for (int j = 0; j < kC; ++j) sA[i * kAS + j] = j < i ? bi * d[j] : 0.f;
+            for (int j = 0; j < kC; j += 4)
+                *reinterpret_cast<float4*>(sA + i * kAS + j) =
+                    make_float4(j < i ? bi * d[j] : 0.f, j + 1 < i ? bi * d[j + 1] : 0.f,
+                                j + 2 < i ? bi * d[j + 2] : 0.f, j + 3 < i ? bi * d[j + 3] : 0.f);
         } else if (warp >= 4 && lane >= 16) {
             __nv_bfloat16* ap = a.Aqk2 + ((size_t)crow * kC + i) * kC;
 #pragma unroll
@@ -2189,11 +2298,15 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     // map over W when no states are kept)
     // and delta, [BH*NT*V][C]: one box of 128 rows
     if ((h_out == nullptr) != (delta_out == nullptr)) return KDA_ERR_INVALID_ARG;
-    CUtensorMap mh, mdl;
+    CUtensorMap mh, mdl, mo;
     if (!(h_out ? make_map(&mh, h_out, (uint64_t)BH * NT * kD, kD, 64, 128, true)
                 : make_map(&mh, w.W2, rows, kD, 64, 64, true)) ||
         !(delta_out ? make_map(&mdl, delta_out, (uint64_t)BH * NT * kD, kC, 64, 128, true)
                     : make_map(&mdl, w.W2, rows, kD, 64, 64, true)))
+        return KDA_ERR_CUDA;
+    // the output o [B*T][HV][V] in [64 t][64 v] boxes (a dummy map over W when
+    // there is no output)
+    if (!(o ? make_map_tok(&mo, o, (uint64_t)d.B * d.T, d.HV) : make_map_tok(&mo, w.W2, rows, 1)))
         return KDA_ERR_CUDA;
     ChainArgs args;
     args.B = d.B;
@@ -2213,7 +2326,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         // three roles, timed apart: forward (o), saving forward (o and the
         // chunk-start states), and the backward's recompute (states only)
         TimedLaunch tl(!h_out ? "tc_chain_fwd" : o ? "tc_chain_fwd_save" : "tc_chain_states", s);
-        chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, mdl,
+        chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, mdl, mo,
                                                                args);
     }
     return launch_status();
