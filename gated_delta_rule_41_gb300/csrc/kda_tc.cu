@@ -127,25 +127,6 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* base, int v, int col0, c
     }
 }
 
-// Copies columns [col0, col0 + ncols) of row v of a K-major bf16 tile
-// (64-column k-blocks `kb_stride` bytes apart) to out[c * ld] for each
-// column c, times `sign`.  col0 and ncols are multiples of 8.
-__device__ __forceinline__ void tile_row_to_global(const uint8_t* tile, uint32_t kb_stride, int v,
-                                                   int col0, int ncols, float sign,
-                                                   __nv_bfloat16* out, size_t ld) {
-    for (int c8 = col0 / 8; c8 < (col0 + ncols) / 8; ++c8) {
-        const uint4 x = *reinterpret_cast<const uint4*>(
-            tile + (c8 >> 3) * kb_stride + sw128_offset(v, (c8 & 7) * 8));
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float2 f = __bfloat1622float2(h2[u]);
-            out[(size_t)(c8 * 8 + 2 * u) * ld] = __float2bfloat16_rn(sign * f.x);
-            out[(size_t)(c8 * 8 + 2 * u + 1) * ld] = __float2bfloat16_rn(sign * f.y);
-        }
-    }
-}
-
 // The chains' epilogue has two threads per value column v (TMEM lane); each
 // takes one half of the columns of a step.
 
@@ -200,11 +181,11 @@ __device__ __forceinline__ void chain_state_rescale(uint32_t tS, const float* ga
 // Delta step, columns c in [32 half, 32 half + 32) of 64: from TMEM (u - D if
 // u is given: the 32 values U[c][v], read before the products completed) to
 // the bf16 K-major operand tile (negated if `neg_tile`), arrive on bar1 and
-// bar2 (if given), then the true-sign bf16 values to out[c][v] (row stride
-// kD) if given.
+// bar2 (if given), then, if `gtile` is given, the true-sign bf16 values into
+// it as a 128B-swizzled pair of [64 c][64 v] tiles (for a TMA store).
 __device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile, const float* u,
                                                  bool neg_tile, int v, int half, uint64_t* bar1,
-                                                 uint64_t* bar2, __nv_bfloat16* out) {
+                                                 uint64_t* bar2, uint8_t* gtile) {
     const int c0 = 32 * half;
     float d0[32];
     tmem_ld32_nw(tD + c0, d0);
@@ -219,7 +200,14 @@ __device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile, con
     tc_fence_before();
     mbar_arrive(bar1);
     if (bar2) mbar_arrive(bar2);
-    if (out) tile_row_to_global(tile, 0, v, c0, 32, sg, out + v, kD);
+    if (gtile) {
+        uint8_t* box = gtile + (v >> 6) * 8192;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<__nv_bfloat16*>(box + sw128_offset(c0 + i, v & 63)) =
+                __float2bfloat16_rn(d0[i]);
+        fence_async_smem();
+    }
 }
 
 struct ChainArgs {
@@ -549,14 +537,14 @@ struct ChainBwdArgs {
     const float* dht;            // [BH][K][V] or null
     float* dh0;                  // [BH][K][V] or null
     __nv_bfloat16* dh_out;       // [BH][NT][V][K] (transposed)
-    __nv_bfloat16* dd_out;       // [BH*T][V]
 };
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kbt,
                  const __grid_constant__ CUtensorMap tm_aqk,
-                 const __grid_constant__ CUtensorMap tm_dhout, ChainBwdArgs a) {
+                 const __grid_constant__ CUtensorMap tm_dhout,
+                 const __grid_constant__ CUtensorMap tm_dd, ChainBwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -568,7 +556,8 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
     uint64_t* bar_D4 = full + 7;
     uint64_t* bar_fin = full + 8;
     uint64_t* bar_Sx = full + 9;   // state rescaled in TMEM
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 10);
+    uint64_t* bar_o = full + 10;   // [2] the epilogue is done with a stage (ddelta tile in it)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 12);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x;
@@ -578,14 +567,16 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(&empty[0], kChainEpi + 1);
-        mbar_init(&empty[1], kChainEpi + 1);
+        mbar_init(&empty[0], 1);
+        mbar_init(&empty[1], 1);
         mbar_init(bar_S, kChainEpi);
         mbar_init(bar_delta, kChainEpi);
         mbar_init(bar_dd, 1);
         mbar_init(bar_D4, 1);
         mbar_init(bar_fin, 1);
         mbar_init(bar_Sx, kChainEpi);
+        mbar_init(&bar_o[0], kChainEpi);
+        mbar_init(&bar_o[1], kChainEpi);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -604,10 +595,25 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             prefetch_tmap(&tm_w);
             prefetch_tmap(&tm_kbt);
             prefetch_tmap(&tm_aqk);
+            // Hands back the stage of epilogue iteration j: its Kb area (free
+            // once ddelta's products completed) then holds ddelta of chunk
+            // NT-1-j, stored here by TMA before the stage is refilled.
+            auto drain_dd = [&](int j) -> bool {
+                const int sj = j & 1;
+                if (!wait_bar(&bar_o[sj], (j >> 1) & 1, 23)) return false;
+                const int y = bh * a.T + (NT - 1 - j) * kC;
+                const uint8_t* tile = smem + sj * STAGE_BYTES + RB_KBT;
+                tma_store_2d(&tm_dd, tile, 0, y);
+                tma_store_2d(&tm_dd, tile + 8192, 64, y);
+                bulk_commit_group();
+                bulk_wait_read_all();
+                return true;
+            };
             int issued = 0;
             for (int i = 0; i < NT; ++i) {
                 const int n = NT - 1 - i, s = i & 1;
                 if (!wait_bar(&empty[s], ((i >> 1) & 1) ^ 1, 11)) break;
+                if (i >= 2 && !drain_dd(i - 2)) break;
                 uint8_t* st = smem + s * STAGE_BYTES;
                 mbar_arrive_expect_tx(&full[s], STAGE_TX);
                 const int row = bh * a.T + n * kC;
@@ -639,6 +645,10 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                     bulk_prefetch_l2(a.gam + (size_t)crow2 * kD, 512);
                 }
             }
+            // the epilogue's last two iterations (after an error, skipped)
+            for (int j = NT - 2 < 0 ? 0 : NT - 2; issued == NT && j < NT; ++j)
+                if (!drain_dd(j)) break;
+            bulk_wait_all();
             for (int i = issued - 2 < 0 ? 0 : issued - 2; i < issued; ++i)
                 wait_bar(&full[i & 1], (i >> 1) & 1, 12);
         }
@@ -727,12 +737,14 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 
         ok = e1(0);
         for (int i = 0; ok && i < NT; ++i) {
-            const int n = NT - 1 - i, s = i & 1;
+            const int s = i & 1;
             if (!wait_bar_warp(bar_dd, i & 1, 18)) { ok = false; break; }
             tc_fence_after();
-            // -ddelta^T to the operand tile; ddelta (true sign) to dd_out
+            // -ddelta^T to the operand tile; ddelta (true sign) into the
+            // stage's Kb area, which the TMA thread stores
             chain_delta_step(tmem + lane_off + TM2_DD, sDelta, nullptr, true, v, half, bar_delta,
-                             &empty[s], a.dd_out + ((size_t)bh * a.T + (size_t)n * kC) * kD);
+                             nullptr, smem + s * STAGE_BYTES + RB_KBT);
+            mbar_arrive(&bar_o[s]);
             if (!wait_bar_warp(bar_D4, i & 1, 19)) { ok = false; break; }
             tc_fence_after();
             if (i + 1 < NT) {
@@ -1082,7 +1094,6 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&x)[8]) {
     }
 }
 constexpr int kIntraThreads = 512;
-constexpr uint32_t INTRA_TX = 4 * 16384;
 
 // first row of Right_R in the stacked operand, which is also the first TMEM
 // column of D_R: sum_{J<R} 16 (J+1)
@@ -1202,10 +1213,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const uint32_t ph = it & 1;
     const int next = chunk + gridDim.x;
     const int n = chunk % a.NT, bh = chunk / a.NT;
-    const int b = bh / a.HV, hv = bh % a.HV;
     const int row0 = bh * a.T + n * kC;       // row in the [BH*T] workspace arrays
     const int crow = chunk;                   // chunk index
-    (void)b;
     if (tid < kC) {
         sBeta[tid] = beta_next;                                   // read after later barriers
         if (next < total) beta_next = load_beta(next);            // in flight meanwhile
@@ -1222,9 +1231,6 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     auto ld = [&](uint32_t tile, int r) {
         return __bfloat162float(
             *reinterpret_cast<const __nv_bfloat16*>(smem + tile + kbo + sw128_offset(r, cc)));
-    };
-    auto st = [&](uint32_t off, float x) {
-        *reinterpret_cast<__nv_bfloat16*>(smem + off) = __float2bfloat16_rn(x);
     };
     float G[16];
     {
@@ -1570,7 +1576,6 @@ static_assert(LB_K % 1024 == 0 && LB_Q % 1024 == 0 && LB_G % 1024 == 0 && LB_DWY
 constexpr int kLocalTcThreads = 512;
 
 __host__ __device__ constexpr uint32_t right_rel(int R) { return 2048u * (uint32_t)(R * (R + 1)); }
-__host__ __device__ constexpr int pair_idx(int R, int J) { return R * (R + 1) / 2 + J; }
 // fp32 dKb row r (512 bytes) in the assembly, staged in three freed areas
 __host__ __device__ constexpr uint32_t lb_dkb_row(int r) {
     return r < 32 ? LB_DTV + 512u * r : r < 48 ? LB_T + 512u * (r - 32) : LB_TLO + 512u * (r - 48);
@@ -1706,7 +1711,6 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int b = bh / a.HV, hv = bh % a.HV;
     const int trow = b * a.T + n * kC;
     const size_t row0 = (size_t)bh * a.T + (size_t)n * kC;
-    const size_t cc0 = (size_t)chunk * kC * kC;
     if (tid < kC) {
         sBeta[tid] = beta_next;                          // read after later barriers
         if (next < total) beta_next = load_beta(next);   // in flight meanwhile
@@ -2376,13 +2380,14 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     const uint64_t rows = (uint64_t)BH * d.T;
     // reverse chain
     {
-        CUtensorMap mdo, mq, mw, mk, ma, mdh;
+        CUtensorMap mdo, mq, mw, mk, ma, mdh, mddst;
         if (!make_map(&mdh, w.dh2, (uint64_t)BH * NT * kD, kD, 64, 128, true) ||
             !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
             !make_map(&mq, w.Q2, rows, kD, 64, 64, true) ||
             !make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
             !make_map(&mk, w.Kb2, rows, kD, 64, 64, true) ||
-            !make_map(&ma, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
+            !make_map(&ma, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true) ||
+            !make_map(&mddst, w.dd2, rows, kD, 64, 64, true))   // ddelta [BH*T][V]
             return KDA_ERR_CUDA;
         ChainBwdArgs a;
         a.B = d.B;
@@ -2393,12 +2398,12 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.dht = dht;
         a.dh0 = dh0;
         a.dh_out = w.dh2;
-        a.dd_out = w.dd2;
         if (cudaFuncSetAttribute(chain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)CHAIN_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
         TimedLaunch tl("tc_chain_bwd", s);
-        chain_bwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, mdh, a);
+        chain_bwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, mdh, mddst,
+                                                               a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     // contractions over V
