@@ -12,9 +12,10 @@
 //     S^T   = diag(gam) S^T + delta^T Kb       (gam applied by the epilogue)
 // Per-chunk operands (W, Qh, Kb, Aqk, U as bf16; gam fp32) arrive by TMA
 // into a two-stage ring.  Warp roles: warp 0 issues TMA, warp 1 owns TMEM and
-// issues MMAs (one thread), warps 2-5 are the epilogue (one TMEM lane per
-// value column).  Every mbarrier wait is bounded: on expiry the kernel records
-// an error code in g_tc_error and unwinds.
+// issues MMAs (one thread), warps 2-9 are the epilogue (two threads per TMEM
+// lane = value column, each taking half of its columns).  Every mbarrier wait
+// is bounded: on expiry the kernel records an error code in g_tc_error and
+// unwinds.
 #include <algorithm>
 #include <mutex>
 
@@ -166,10 +167,19 @@ __device__ __forceinline__ void chain_state_rescale(uint32_t tS, const float* ga
                                                     uint64_t* bar_tmem, float (&r0)[32],
                                                     float (&r1)[32]) {
     const int k0 = 64 * half;
+    // gam is 16-byte aligned: 16 broadcast float4 loads instead of 64 scalar
+    const float4* g4 = reinterpret_cast<const float4*>(gam + k0);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        r0[i] *= gam[k0 + i];
-        r1[i] *= gam[k0 + 32 + i];
+    for (int i = 0; i < 8; ++i) {
+        const float4 a = g4[i], b = g4[8 + i];
+        r0[4 * i] *= a.x;
+        r0[4 * i + 1] *= a.y;
+        r0[4 * i + 2] *= a.z;
+        r0[4 * i + 3] *= a.w;
+        r1[4 * i] *= b.x;
+        r1[4 * i + 1] *= b.y;
+        r1[4 * i + 2] *= b.z;
+        r1[4 * i + 3] *= b.w;
     }
     tmem_st32_nw(tS + k0, r0);
     tmem_st32_nw(tS + k0 + 32, r1);
