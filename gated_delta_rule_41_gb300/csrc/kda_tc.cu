@@ -4,11 +4,13 @@
 // Forward state pass ("chain") of the chunk form (K3 README, table 实现路线表,
 // row L2, step (4): the state passed between chunks).  One CTA per (b, hv)
 // walks the chunks in order and keeps the K x V state S on chip, as fp32 in
-// tensor memory.  Everything is computed transposed so that the MMA M
-// dimension is the value dimension (128 rows = 128 TMEM lanes):
+// tensor memory.  The state products are computed transposed so that the
+// MMA M dimension is the value dimension (128 rows = 128 TMEM lanes); the
+// output is computed row-major:
 //     D12W  = S^T W^T            (M=128 v, N=64 rows, K=128 k)
 //     delta^T = U^T - D12W       (epilogue, fp32 -> bf16 operand in smem)
-//     O^T   = S^T Qh^T + delta^T Aqk^T
+//     O     = Qh S + Aqk delta      (M=128 over the 64 rows of Qh / Aqk and
+//                                     64 don't-care rows, N=128 v: row-major)
 //     S^T   = diag(gam) S^T + delta^T Kb       (gam applied by the epilogue)
 // Per-chunk operands (W, Qh, Kb, Aqk, U as bf16; gam fp32) arrive by TMA
 // into a two-stage ring.  Warp roles: warp 0 issues TMA, warp 1 owns TMEM and
@@ -86,7 +88,7 @@ static_assert(CHAIN_SMEM <= 232448, "chain kernels exceed the per-CTA shared mem
 constexpr int kChainThreads = 320, kChainEpi = 256;
 
 // TMEM columns
-constexpr uint32_t TM_S = 0, TM_W = 128, TM_O0 = 192, TM_O1 = 256, TM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_W = 128, TM_O0 = 192, TM_O1 = 320, TM_COLS = 512;
 
 // Sums each of N (16 or 32) per-lane values over the 32 lanes of a warp with
 // N - 1 + (32 / N - 1) shuffles (a reduce-scatter butterfly: at offset o a
@@ -111,6 +113,27 @@ __device__ __forceinline__ float warp_sum_scatter(float (&v)[N]) {
 #pragma unroll
     for (; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
     return v[0];
+}
+
+// eight fp32 <-> eight bf16 (16 bytes)
+__device__ __forceinline__ void ld8f(const float* p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                      pack_bf16(x[6], x[7]));
+}
+__device__ __forceinline__ void unpack8(const uint4 v, float (&x)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
 }
 
 // ---- epilogue steps shared by the two chains (thread <-> value column v) ----
@@ -403,17 +426,20 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 // also covers it
                 if (a.h_out) bulk_wait_read_but2();
                 mma_commit(bar_D3);
-                // O_n = S_n Qh^T + delta Aqk^T, behind the state update (the
-                // S tile of parity n is rewritten only after the next D3)
+                // O_n = Qh S_n + Aqk delta (rows t in TMEM lanes 0..63, columns
+                // v), behind the state update (the S tile of parity n is
+                // rewritten only after the next D3).  A = the Qh and Aqk tiles
+                // with M = 128: their rows 64..127 are the next 64 rows of the
+                // stage, don't-care; B = the S^T and delta^T tiles (N = v).
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
                     const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_bf16(tO, dSn + ka, dQ0 + so + kb, idesc64, kk > 0);
+                    mma_bf16(tO, dQ0 + so + kb, dSn + ka, idesc128, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tO, dD + ((kk * 32) >> 4), dAq0 + so + ((kk * 32) >> 4), idesc64, 1);
+                    mma_bf16(tO, dAq0 + so + ((kk * 32) >> 4), dD + ((kk * 32) >> 4), idesc128, 1);
                 mma_commit(&empty[s]);
                 if (a.delta_out) {  // delta_n^T tile (rows v) to delta_out, by TMA
                     tma_store_2d(&tm_dout, smem + OFF_DELTA, 0, (bh * NT + n) * kD);
@@ -448,25 +474,51 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             return true;
         };
 
-        // E3: output rows of chunk m into a 128B-swizzled pair of [64 t][64 v]
-        // tiles at dst (a warp's lanes fill 64 contiguous bytes of one row)
-        auto o_tile = [&](int m, uint8_t* dst) {
+        // E3: output rows of chunk m (row t = TMEM lane, warps of lanes 0..63;
+        // thread (t, half) holds columns v in [64 half, 64 half + 64)) into a
+        // 128B-swizzled pair of [64 t][64 v] tiles at dst, or, for the last
+        // chunk, straight to global memory
+        auto o_rows = [&](int m, float (&x0)[32], float (&x1)[32]) {
             const uint32_t tO = (m & 1) ? TM_O1 : TM_O0;
-            tmem_ld32(tmem + lane_off + tO + half * 32, r);
-            uint8_t* box = dst + (v >> 6) * 8192;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                *reinterpret_cast<__nv_bfloat16*>(box + sw128_offset(32 * half + i, v & 63)) =
-                    __float2bfloat16_rn(r[i]);
+            tmem_ld32_nw(tmem + lane_off + tO + half * 64, x0);
+            tmem_ld32_nw(tmem + lane_off + tO + half * 64 + 32, x1);
+            tmem_wait_ld_dep(x0);
+            tmem_wait_ld_dep(x1);
         };
-        // the last chunk's output rows straight to global memory
-        auto o_out = [&](int m) {
-            const uint32_t tO = (m & 1) ? TM_O1 : TM_O0;
-            tmem_ld32(tmem + lane_off + tO + half * 32, r);
-            __nv_bfloat16* op =
-                a.o + (((size_t)b * a.T + (size_t)m * kC + half * 32) * a.HV + hv) * kD + v;
+        auto o_tile = [&](int m, uint8_t* dst) {
+            if (q >= 2) return;
+            float x1[32];
+            o_rows(m, r, x1);
+            uint8_t* box = dst + half * 8192;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) op[(size_t)i * a.HV * kD] = __float2bfloat16_rn(r[i]);
+            for (int j = 0; j < 4; ++j) {
+                float e0[8], e1v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    e0[i] = r[8 * j + i];
+                    e1v[i] = x1[8 * j + i];
+                }
+                *reinterpret_cast<uint4*>(box + sw128_offset(v, 8 * j)) = pack8(e0);
+                *reinterpret_cast<uint4*>(box + sw128_offset(v, 32 + 8 * j)) = pack8(e1v);
+            }
+        };
+        auto o_out = [&](int m) {
+            if (q >= 2) return;
+            float x1[32];
+            o_rows(m, r, x1);
+            __nv_bfloat16* op =
+                a.o + (((size_t)b * a.T + (size_t)m * kC + v) * a.HV + hv) * kD + half * 64;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float e0[8], e1v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    e0[i] = r[8 * j + i];
+                    e1v[i] = x1[8 * j + i];
+                }
+                *reinterpret_cast<uint4*>(op + 8 * j) = pack8(e0);
+                *reinterpret_cast<uint4*>(op + 32 + 8 * j) = pack8(e1v);
+            }
         };
 
         ok = e1(0);
@@ -1084,25 +1136,6 @@ static_assert(I_K % 1024 == 0 && I_Q % 1024 == 0 && I_V % 1024 == 0 && I_SG % 10
 // slot of F(R, Rr) = exp(G_b(Rr) - G_b(R)) for Rr > R among the six pairs
 __host__ __device__ constexpr int f_slot(int R, int Rr) { return R * (7 - R) / 2 + (Rr - R - 1); }
 
-__device__ __forceinline__ void ld8f(const float* p, float (&x)[8]) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                      pack_bf16(x[6], x[7]));
-}
-__device__ __forceinline__ void unpack8(const uint4 v, float (&x)[8]) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
-}
 constexpr int kIntraThreads = 512;
 
 // first row of Right_R in the stacked operand, which is also the first TMEM
