@@ -2063,12 +2063,15 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             const float dQh = *reinterpret_cast<const float*>(smem + LB_DWY + t * 512 + c * 4);
             const float dKb = *reinterpret_cast<const float*>(smem + lb_dkb_row(t) + c * 4);
             const float sa = sAQ[u] * E, sq = sAQ[16 + u] * E, caq = cAQ[u] * Einv;
-            const float dkv = br * dKbeta * eG + dKb * eL + br * sa + caq;
-            const float dqs = dQh * eG + sq;
-            dG[u] = dKbeta * br * kr * eG + dQh * qr * eG - dKb * kr * eL + br * kr * sa +
-                    qr * sq - kr * caq;
-            lastp += dKb * kr * eL;
-            dbps[u] = dKbeta * kr * eG + kr * sa;
+            // with p = dKbeta eG + sa (the factor beta multiplies) and l = dKb eL:
+            // dk = beta p + l + caq, dqs = dQh eG + sq,
+            // dG = k (beta p - l - caq) + qs dqs, dbeta partial = k p
+            const float pb = fmaf(dKbeta, eG, sa), l = dKb * eL, bp = br * pb;
+            const float dkv = bp + l + caq;
+            const float dqs = fmaf(dQh, eG, sq);
+            dG[u] = fmaf(qr, dqs, kr * (bp - l - caq));
+            lastp = fmaf(kr, l, lastp);
+            dbps[u] = kr * pb;
             const size_t io = (((size_t)trow + t) * a.HV + hv) * kD + c;
             if (a.G == 1) {
                 a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
