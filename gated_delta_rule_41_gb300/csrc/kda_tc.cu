@@ -1359,13 +1359,15 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             const size_t go = ((size_t)row0 + r) * kD + c0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = qv[e] * egb[e] * E[e];        // qs exp(G)
+            for (int e = 0; e < 8; ++e) egb[e] *= E[e];                      // exp(G)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = qv[e] * egb[e];               // qs exp(G)
             *reinterpret_cast<uint4*>(a.Q2 + go) = pack8(x);
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = kv[e] * elb[e] * Ei[e];       // k exp(G_last - G)
             *reinterpret_cast<uint4*>(a.Kb2 + go) = pack8(x);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = kv[e] * egb[e] * E[e];        // Khat = k exp(G)
+            for (int e = 0; e < 8; ++e) x[e] = kv[e] * egb[e];               // Khat = k exp(G)
             *reinterpret_cast<uint4*>(smem + I_KHAT + kb * 8192 + r * 128 + co) = pack8(x);
         }
     }
@@ -2085,6 +2087,9 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
         for (int u = 0; u < 16; ++u) dG[u] = 0.f;
     }
+    // the tail's global inputs, in flight while the partial sums are formed
+    const float dgam_c = a.dgam[((size_t)bh * a.NT + n) * kD + c];
+    const float dbv_t = tid < kC ? a.dbv[row0 + tid] : 0.f;
     // dbeta partials of rows 16R..16R+15 over this warp's 32 channels: lane
     // pair (2u, 2u+1) ends with row 16R + u
     {
@@ -2109,7 +2114,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     {
         // dG_last += sum_r dKb_r Kb_r + dgam gam; it enters every row's suffix sum
-        float extra = a.dgam[((size_t)bh * a.NT + n) * kD + c] * __expf(Glast);
+        float extra = dgam_c * __expf(Glast);
 #pragma unroll
         for (int p = 0; p < 4; ++p) extra += sLast[p * kD + c];
         float run = extra;
@@ -2125,7 +2130,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (tid < kC)
         a.dbeta[((size_t)trow + tid) * a.HV + hv] =
             __float2bfloat16_rn((sDbp[tid] + sDbp[64 + tid]) + (sDbp[128 + tid] + sDbp[192 + tid]) +
-                                a.dbv[row0 + tid]);
+                                dbv_t);
     // partial sums, beta and TMEM are reused by the next chunk
     tc_fence_before();
     if (!__syncthreads_and(ok)) break;
