@@ -1456,55 +1456,41 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         }
     }
     __syncthreads();
-    // X = A_10 T_00 into A's unused upper block (rows 0..31, columns 32..63)
-    {
-        const int jj = lane, i0 = 2 * warp;
-        float x0 = 0.f, x1 = 0.f, y0 = 0.f, y1 = 0.f;   // two chains per row
-        const float* a0 = sA + (32 + i0) * kAS;
-        const float* a1 = a0 + kAS;
+    // The two 32 x 32 x 32 products below: the first 256 threads, thread
+    // (rp, cp) owning rows 2rp, 2rp + 1 and columns 2cp, 2cp + 1 of C =
+    // sign A B (row stride kAS everywhere).  Per four k: two float4 loads of
+    // A rows (shared by a half-warp) and four float2 loads of B (shared by the
+    // two half-warps) feed 16 FMAs.
+    auto mm32 = [&](const float* A, const float* B, float* C, float sign) {
+        if (tid < 256) {
+            const int rp = 2 * warp + (lane >> 4), cp = lane & 15;
+            const int i0 = 2 * rp, j0 = 2 * cp;
+            const float* a0 = A + i0 * kAS;
+            const float* a1 = a0 + kAS;
+            float c00 = 0.f, c01 = 0.f, c10 = 0.f, c11 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 32; m += 4) {
-            const float4 p = *reinterpret_cast<const float4*>(a0 + m);
-            const float4 q = *reinterpret_cast<const float4*>(a1 + m);
-            const float t0 = sT[m * kAS + jj], t1 = sT[(m + 1) * kAS + jj];
-            const float t2 = sT[(m + 2) * kAS + jj], t3 = sT[(m + 3) * kAS + jj];
-            x0 = fmaf(p.x, t0, x0);
-            y0 = fmaf(p.y, t1, y0);
-            x1 = fmaf(q.x, t0, x1);
-            y1 = fmaf(q.y, t1, y1);
-            x0 = fmaf(p.z, t2, x0);
-            y0 = fmaf(p.w, t3, y0);
-            x1 = fmaf(q.z, t2, x1);
-            y1 = fmaf(q.w, t3, y1);
+            for (int m = 0; m < 32; m += 4) {
+                const float4 p = *reinterpret_cast<const float4*>(a0 + m);
+                const float4 q = *reinterpret_cast<const float4*>(a1 + m);
+                const float pa[4] = {p.x, p.y, p.z, p.w}, qa[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 bv = *reinterpret_cast<const float2*>(B + (m + e) * kAS + j0);
+                    c00 = fmaf(pa[e], bv.x, c00);
+                    c01 = fmaf(pa[e], bv.y, c01);
+                    c10 = fmaf(qa[e], bv.x, c10);
+                    c11 = fmaf(qa[e], bv.y, c11);
+                }
+            }
+            *reinterpret_cast<float2*>(C + i0 * kAS + j0) = make_float2(sign * c00, sign * c01);
+            *reinterpret_cast<float2*>(C + (i0 + 1) * kAS + j0) = make_float2(sign * c10, sign * c11);
         }
-        sA[i0 * kAS + 32 + jj] = x0 + y0;
-        sA[(i0 + 1) * kAS + 32 + jj] = x1 + y1;
-    }
+    };
+    // X = A_10 T_00 into A's unused upper block (rows 0..31, columns 32..63)
+    mm32(sA + 32 * kAS, sT, sA + 32, 1.f);
     __syncthreads();
     // T_10 = -T_11 X
-    {
-        const int jj = lane, i0 = 2 * warp;
-        float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;   // two chains per row
-        const float* r0 = sT + (32 + i0) * kAS + 32;
-        const float* r1 = r0 + kAS;
-#pragma unroll
-        for (int m = 0; m < 32; m += 4) {
-            const float4 p = *reinterpret_cast<const float4*>(r0 + m);
-            const float4 q = *reinterpret_cast<const float4*>(r1 + m);
-            const float x0 = sA[m * kAS + 32 + jj], x1 = sA[(m + 1) * kAS + 32 + jj];
-            const float x2 = sA[(m + 2) * kAS + 32 + jj], x3 = sA[(m + 3) * kAS + 32 + jj];
-            y0 = fmaf(p.x, x0, y0);
-            z0 = fmaf(p.y, x1, z0);
-            y1 = fmaf(q.x, x0, y1);
-            z1 = fmaf(q.y, x1, z1);
-            y0 = fmaf(p.z, x2, y0);
-            z0 = fmaf(p.w, x3, z0);
-            y1 = fmaf(q.z, x2, y1);
-            z1 = fmaf(q.w, x3, z1);
-        }
-        sT[(32 + i0) * kAS + jj] = -(y0 + z0);
-        sT[(32 + i0 + 1) * kAS + jj] = -(y1 + z1);
-    }
+    mm32(sT + 32 * kAS + 32, sA + 32, sT + 32 * kAS, -1.f);
     __syncthreads();
     // T (bf16 high and low parts) to global; T*beta to the B-operand tile.
     // Thread t takes columns 8 (t % 8) .. + 7 of row t / 8.
