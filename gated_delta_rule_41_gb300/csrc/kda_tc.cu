@@ -1425,17 +1425,19 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     __syncthreads();
 
-    // ---- (3) T = (I + A)^{-1}, A strictly lower: two 32 x 32 diagonal blocks by
-    // forward substitution (thread (RB, jj) keeps column jj of block RB in
-    // registers), then T_10 = -T_11 (A_10 T_00).  A's entries on and above the
-    // diagonal are stored zeros, so the dot products run over whole float4s. ----
+    // ---- (3) T = (I + A)^{-1}, A strictly lower, in three levels: the four
+    // 16 x 16 diagonal blocks by forward substitution (thread (B, jj) keeps
+    // column jj of block B in registers); each 32 x 32 diagonal block as
+    // [[T_a, 0], [-T_b (A_ba T_a), T_b]]; then T_10 = -T_11 (A_10 T_00).  A's
+    // entries on and above the diagonal are stored zeros, so the dot products
+    // run over whole float4s. ----
     if (tid < 64) {
-        const int RB = tid >> 5, jj = tid & 31, o = 32 * RB;
-        float t[32];
+        const int o = 16 * (tid >> 4), jj = tid & 15;
+        float t[16];
 #pragma unroll
-        for (int m = 0; m < 32; ++m) t[m] = m == jj ? 1.f : 0.f;
+        for (int m = 0; m < 16; ++m) t[m] = m == jj ? 1.f : 0.f;
 #pragma unroll
-        for (int ii = 1; ii < 32; ++ii) {
+        for (int ii = 1; ii < 16; ++ii) {
             const float* arow = sA + (o + ii) * kAS + o;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1449,11 +1451,44 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             if (ii > jj) t[ii] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
         }
 #pragma unroll
-        for (int m = 0; m < 32; ++m) sT[(o + m) * kAS + o + jj] = t[m];
-        if (RB == 1) {
+        for (int m = 0; m < 16; ++m) sT[(o + m) * kAS + o + jj] = t[m];
+    }
+    __syncthreads();
+    // 32-level, thread (RB, i, j) of all 512: Y = A_ba T_a into A's unused
+    // block above the diagonal (rows o + i, columns o + 16 + j); T's blocks
+    // above the diagonal (that one, and T_01) are zero
+    {
+        const int RB = tid >> 8, i = (tid >> 4) & 15, j = tid & 15, o = 32 * RB;
+        const float* arow = sA + (o + 16 + i) * kAS + o;
+        float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 32; ++m) sT[m * kAS + 32 + jj] = 0.f;   // T_01 = 0
+        for (int m = 0; m < 16; m += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(arow + m);
+            y0 = fmaf(a4.x, sT[(o + m) * kAS + o + j], y0);
+            y1 = fmaf(a4.y, sT[(o + m + 1) * kAS + o + j], y1);
+            y0 = fmaf(a4.z, sT[(o + m + 2) * kAS + o + j], y0);
+            y1 = fmaf(a4.w, sT[(o + m + 3) * kAS + o + j], y1);
         }
+        sA[(o + i) * kAS + o + 16 + j] = y0 + y1;
+        sT[(o + i) * kAS + o + 16 + j] = 0.f;
+        sT[(tid >> 5) * kAS + 32 + (tid & 31)] = 0.f;   // T_01, rows 0..15
+        sT[(16 + (tid >> 5)) * kAS + 32 + (tid & 31)] = 0.f;   // rows 16..31
+    }
+    __syncthreads();
+    // T_ba = -T_b Y
+    {
+        const int RB = tid >> 8, i = (tid >> 4) & 15, j = tid & 15, o = 32 * RB;
+        const float* trow = sT + (o + 16 + i) * kAS + o + 16;
+        float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+            const float4 t4 = *reinterpret_cast<const float4*>(trow + m);
+            y0 = fmaf(t4.x, sA[(o + m) * kAS + o + 16 + j], y0);
+            y1 = fmaf(t4.y, sA[(o + m + 1) * kAS + o + 16 + j], y1);
+            y0 = fmaf(t4.z, sA[(o + m + 2) * kAS + o + 16 + j], y0);
+            y1 = fmaf(t4.w, sA[(o + m + 3) * kAS + o + 16 + j], y1);
+        }
+        sT[(o + 16 + i) * kAS + o + j] = -(y0 + y1);
     }
     __syncthreads();
     // The two 32 x 32 x 32 products below: the first 256 threads, thread
