@@ -871,7 +871,10 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + G_BAR);   // all tiles but v
     uint64_t* bar_mma = bar_tma + 1;
     uint64_t* bar_v = bar_tma + 2;                                     // v tile
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    uint64_t* bar_sd = bar_tma + 3;    // S0 and dS tiles
+    uint64_t* bar_s = bar_tma + 4;     // the products that read S0 and dS are done
+    uint64_t* bar_dg = bar_tma + 5;    // every thread is done reading S0 and dS
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 6);
     float* dbv_part = reinterpret_cast<float*>(smem + G_DBV);  // [4 lane quadrants][64]
     float* beta_s = dbv_part + 4 * 64;                          // [64]
     float* dg_part = beta_s + 64;                               // [2 halves][128]
@@ -882,14 +885,19 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     // thread 0's counts of issued and consumed loads (every load is waited for
     // before the CTA exits)
     int main_issued = 0, v_issued = 0, main_waited = 0, v_waited = 0;
-    auto issue_main = [&](int ch) {   // states, state gradients, [dO; ddelta], delta^T, T
+    int sd_issued = 0, sd_waited = 0;
+    auto issue_sd = [&](int ch) {     // states, state gradients
+        mbar_arrive_expect_tx(bar_sd, 65536);
+        tma_load_2d(smem + G_S0, &tm_h, bar_sd, 0, ch * kD);
+        tma_load_2d(smem + G_S0 + 16384, &tm_h, bar_sd, 64, ch * kD);
+        tma_load_2d(smem + G_DS, &tm_dh, bar_sd, 0, ch * kD);
+        tma_load_2d(smem + G_DS + 16384, &tm_dh, bar_sd, 64, ch * kD);
+        ++sd_issued;
+    };
+    auto issue_main = [&](int ch) {   // [dO; ddelta], delta^T, T
         const int nn = ch % NT, bb = ch / NT, hvv = bb % a.HV;
         const int rw = bb * a.T + nn * kC, tr = (bb / a.HV) * a.T + nn * kC;
-        mbar_arrive_expect_tx(bar_tma, GRAD_TX - 16384);
-        tma_load_2d(smem + G_S0, &tm_h, bar_tma, 0, ch * kD);
-        tma_load_2d(smem + G_S0 + 16384, &tm_h, bar_tma, 64, ch * kD);
-        tma_load_2d(smem + G_DS, &tm_dh, bar_tma, 0, ch * kD);
-        tma_load_2d(smem + G_DS + 16384, &tm_dh, bar_tma, 64, ch * kD);
+        mbar_arrive_expect_tx(bar_tma, GRAD_TX - 16384 - 65536);
         tma_load_3d(smem + G_ODD, &tm_do, bar_tma, 0, hvv, tr);
         tma_load_3d(smem + G_ODD + 16384, &tm_do, bar_tma, 64, hvv, tr);
         tma_load_2d(smem + G_ODD + 8192, &tm_dd, bar_tma, 0, rw);
@@ -916,6 +924,9 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_v, 1);
+        mbar_init(bar_sd, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_dg, kGradThreads);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -927,6 +938,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     if (tid == 0 && (int)blockIdx.x < total) {
+        issue_sd(blockIdx.x);
         issue_main(blockIdx.x);
         issue_v(blockIdx.x);
     }
@@ -947,7 +959,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             if (next < total) beta_next = load_beta(next);    // in flight meanwhile
         }
         if (tid == 0) {   // the thread that issues the loads also issues the products
-            if (wait_bar(bar_tma, ph, 21) && wait_bar(bar_v, ph, 25)) {
+            if (wait_bar(bar_sd, ph, 26) && wait_bar(bar_tma, ph, 21) && wait_bar(bar_v, ph, 25)) {
+                ++sd_waited;
                 ++main_waited;
                 ++v_waited;
                 tc_fence_after();
@@ -955,6 +968,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                 const uint32_t s0 = smem_u32(smem + G_S0), ds = smem_u32(smem + G_DS);
                 const uint32_t odd = smem_u32(smem + G_ODD), dvt = smem_u32(smem + G_DV);
                 const uint32_t tt = smem_u32(smem + G_T), dt = smem_u32(smem + G_DT);
+                // the products that read S0 and dS first, so that their tiles
+                // can be refilled while the others run
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -968,6 +983,12 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                     // delta is stored transposed (rows v): B operand read MN-major
                     const uint64_t bdt = sdesc_mn_sw128(dt + kk * 2048, 16384);
                     mma_bf16(tmem + 128, ads, bdt, id64 | kAMajorMN | kBMajorMN, kk > 0);
+                }
+                mma_commit(bar_s);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint64_t bdt = sdesc_mn_sw128(dt + kk * 2048, 16384);
                     mma_bf16(tmem + 256, sdesc_sw128(odd + ko), bdt, id64 | kBMajorMN, kk > 0);
                     mma_bf16(tmem + 320, sdesc_sw128(odd + ko), sdesc_sw128(dvt + 8192 + ko),
                              id64, kk > 0);
@@ -987,7 +1008,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         const int l = q * 32 + lane;  // TMEM lane: k for D1-D3, row for D4, v for D5
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         float r[32];
-        ok = ok && wait_bar_warp(bar_tma, ph, 23);
+        ok = ok && wait_bar_warp(bar_sd, ph, 23);
         // dgam[k] = sum_v dS[v][k] S0[v][k] from the bf16 tiles (independent of
         // the MMAs); thread (k = l, half) sums rows v in [64 half, 64 half + 64)
         {
@@ -1003,9 +1024,19 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             }
             dg_part[half * kD + l] = acc;
         }
+        // S0 and dS are free once every thread has read them and their
+        // products are done: the next chunk's copies start now
+        fence_async_smem();
+        mbar_arrive(bar_dg);
+        if (tid == 0 && ok && next < total) {
+            if (wait_bar(bar_s, ph, 27) && wait_bar(bar_dg, ph, 28))
+                issue_sd(next);
+            else
+                ok = false;
+        }
         ok = ok && wait_bar_warp(bar_mma, ph, 24);
-        // every tile but v has been read (products and dgam): the next chunk's
-        // loads start while this chunk's results leave
+        // [dO; ddelta], delta^T and T have been read by the products: the
+        // next chunk's copies of them start while this chunk's results leave
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -1082,6 +1113,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     // loads issued for chunks the loop did not reach (after an error) land
     // before shared memory is released
     if (tid == 0) {
+        for (; sd_waited < sd_issued; ++sd_waited) wait_bar_drain(bar_sd, sd_waited & 1);
         for (; main_waited < main_issued; ++main_waited) wait_bar_drain(bar_tma, main_waited & 1);
         for (; v_waited < v_issued; ++v_waited) wait_bar_drain(bar_v, v_waited & 1);
     }
