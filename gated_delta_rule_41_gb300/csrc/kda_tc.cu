@@ -1035,13 +1035,13 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                 ok = false;
         }
         ok = ok && wait_bar_warp(bar_mma, ph, 24);
-        // [dO; ddelta], delta^T and T have been read by the products: the
-        // next chunk's copies of them start while this chunk's results leave
-        fence_async_smem();
+        // [dO; ddelta], delta^T and T are read only by the products, which are
+        // done: the next chunk's copies of them start while this chunk's
+        // results leave
+        if (tid == 0 && ok && next < total) issue_main(next);
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0 && ok && next < total) issue_main(next);
         if (ok) {
             const size_t rb = (size_t)row * kD;
             const int cb = half;  // columns 32*cb .. 32*cb+31 of D1-D3 and D5
