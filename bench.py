@@ -56,11 +56,11 @@ def _src_hash(name):
 # Measured at B=1, T=8192 (2048 chunks, inputs and workspace above L2),
 # scaled by the chunk count to the B=4 launch (8192 chunks).
 NCU_TRAFFIC = {
-    "tc_local_bwd": (4 * (354624256 + 78924800), "kda_tc.cu", "091c58e33e8c"),
-    "tc_intra": (4 * (134799872 + 132511232), "kda_tc.cu", "091c58e33e8c"),
-    "tc_grad_v": (4 * (286091520 + 199869952), "kda_tc.cu", "091c58e33e8c"),
-    "tc_chain_fwd_save": (4 * (152091648 + 90978560), "kda_tc.cu", "091c58e33e8c"),
-    "tc_chain_bwd": (4 * (152133376 + 63938560), "kda_tc.cu", "091c58e33e8c"),
+    "tc_local_bwd": (4 * (354916608 + 79097344), "kda_tc.cu", "f3e1de5729e7"),
+    "tc_intra": (4 * (134690816 + 132693248), "kda_tc.cu", "f3e1de5729e7"),
+    "tc_grad_v": (4 * (286017792 + 197427200), "kda_tc.cu", "f3e1de5729e7"),
+    "tc_chain_fwd_save": (4 * (152090624 + 91252992), "kda_tc.cu", "f3e1de5729e7"),
+    "tc_chain_bwd": (4 * (152093952 + 64608512), "kda_tc.cu", "f3e1de5729e7"),
 }
 
 
