@@ -126,6 +126,9 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
     return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                       pack_bf16(x[6], x[7]));
 }
+__device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
 __device__ __forceinline__ void unpack8(const uint4 v, float (&x)[8]) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -1824,9 +1827,6 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         return __bfloat162float(
             *reinterpret_cast<const __nv_bfloat16*>(smem + tile + kbo + sw128_offset(r, cc)));
     };
-    auto st = [&](uint32_t off, float x) {
-        *reinterpret_cast<__nv_bfloat16*>(smem + off) = __float2bfloat16_rn(x);
-    };
     // ---- cumsum (thread (c, R): rows 16R..16R+15 of channel c); the gate mask
     // [g >= -5] of the rows is kept for dg, so the g tile is free afterwards ----
     float G[16];
@@ -1866,23 +1866,74 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
 
     // ---- build bf16 operands: Y, Right_R (own block; the copies for later
-    // blocks follow while P1/P2 run), Lcol ----
+    // blocks follow while P1/P2 run), Lcol.  The G values of a quad of lanes
+    // (channels cq..cq+3) are first transposed within the quad, so that lane
+    // s of the quad owns rows 16R + 4s .. + 3 of all four channels: every
+    // load and store then moves four channels (8 bytes) at once. ----
     {
+        const int s4 = lane & 3, cq = c - s4;
+        // GT[4 i + j]: channel cq + i, row 16R + 4 s4 + j.  A 4 x 4 transpose of
+        // 4-row blocks across the quad: at stage m, of each block pair
+        // (b, b ^ m) a lane keeps the one on its side of bit m and receives the
+        // partner's other one.
+        float GT[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int r = 16 * R + u;
-            const float E = __expf(G[u] - Gb[R]);
-            const float Einv = __expf(Gb[R] - G[u]);
-            const float kv = ldt(LB_K, r), qv = a.scale * ldt(LB_Q, r), br = sBeta[r];
-            const uint32_t cb16 = (c >> 6) * 16384;
-            // Y rows of [dW; Y]
-            st(LB_DWY + cb16 + sw128_offset(64 + r, cc), br * kv * eGbR * E);
-            // Right_R (this thread's block only)
-            st(LB_RIGHT + right_rel(R) + (c >> 6) * (16u * (R + 1) * 128u) + sw128_offset(r, cc),
-               kv * Einv);
-            // Lcol rows 32R + u (beta k E) and 32R + 16 + u (qs E)
-            st(LB_LCOL + cb16 + sw128_offset(32 * R + u, cc), br * kv * E);
-            st(LB_LCOL + cb16 + sw128_offset(32 * R + 16 + u, cc), qv * E);
+        for (int u = 0; u < 16; ++u) GT[u] = G[u];
+#pragma unroll
+        for (int m = 1; m <= 2; m <<= 1) {
+            const bool up = (s4 & m) != 0;
+#pragma unroll
+            for (int b0 = 0; b0 < 4; ++b0) {
+                if (b0 & m) continue;
+                const int b1 = b0 ^ m;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float send = up ? GT[4 * b0 + k] : GT[4 * b1 + k];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+                    if (up)
+                        GT[4 * b0 + k] = recv;
+                    else
+                        GT[4 * b1 + k] = recv;
+                }
+            }
+        }
+        const float4 gb4 = *reinterpret_cast<const float4*>(sGb + R * kD + cq);
+        const float gbq[4] = {gb4.x, gb4.y, gb4.z, gb4.w};
+        float egb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) egb[i] = __expf(gbq[i]);
+        const float4 bt4 = *reinterpret_cast<const float4*>(sBeta + 16 * R + 4 * s4);
+        const float btq[4] = {bt4.x, bt4.y, bt4.z, bt4.w};
+        const uint32_t kbq = (cq >> 6) * 8192, cb16 = (cq >> 6) * 16384, ccq = cq & 63;
+        const uint32_t rbase = LB_RIGHT + right_rel(R) + (cq >> 6) * (16u * (R + 1) * 128u);
+        auto st4 = [&](uint32_t off, const float (&x)[4]) {
+            *reinterpret_cast<uint2*>(smem + off) =
+                make_uint2(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]));
+        };
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int u = 4 * s4 + j, r = 16 * R + u;
+            const uint32_t so = sw128_offset(r, ccq);
+            const uint2 k2 = *reinterpret_cast<const uint2*>(smem + LB_K + kbq + so);
+            const uint2 q2 = *reinterpret_cast<const uint2*>(smem + LB_Q + kbq + so);
+            const float2 k01 = unpack_bf16(k2.x), k23 = unpack_bf16(k2.y);
+            const float2 q01 = unpack_bf16(q2.x), q23 = unpack_bf16(q2.y);
+            const float kv[4] = {k01.x, k01.y, k23.x, k23.y};
+            const float qv[4] = {q01.x, q01.y, q23.x, q23.y};
+            float y[4], rt[4], l1[4], l2[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float E = __expf(GT[4 * i + j] - gbq[i]);
+                const float Einv = __expf(gbq[i] - GT[4 * i + j]);
+                l1[i] = btq[j] * kv[i] * E;             // beta k E
+                y[i] = l1[i] * egb[i];                  // Y = beta k exp(G)
+                rt[i] = kv[i] * Einv;                   // Right_R
+                l2[i] = a.scale * qv[i] * E;            // qs E
+            }
+            st4(LB_DWY + cb16 + sw128_offset(64 + r, ccq), y);   // Y rows of [dW; Y]
+            st4(rbase + so, rt);
+            st4(LB_LCOL + cb16 + sw128_offset(32 * R + u, ccq), l1);
+            st4(LB_LCOL + cb16 + sw128_offset(32 * R + 16 + u, ccq), l2);
         }
     }
     cp_async_wait_all16();
