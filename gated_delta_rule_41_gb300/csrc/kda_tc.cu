@@ -1660,7 +1660,8 @@ constexpr uint32_t LB_T = 106496, LB_TLO = LB_T + 8192;
 constexpr uint32_t LB_RIGHT = 122880; // Right_R tiles, 16(R+1) rows each
 constexpr uint32_t LB_LCOL = 163840;  // [beta k E; qs E] rows 32R + 16s + u, 128 c
 constexpr uint32_t LB_SMALL = 196608; // fp32 small arrays
-// LB_SMALL + 8192 .. + 16384: unused
+constexpr uint32_t LB_F = LB_SMALL + 8192;   // F [6 block pairs][128] fp32
+// LB_F + 3072 .. LB_SMALL + 16384: unused
 constexpr uint32_t LB_DTV = LB_SMALL + 16384;  // dTv fp32 [64][64], 16-byte chunks XOR-swizzled
 constexpr uint32_t LB_BAR = LB_DTV + 16384;
 // After P1/P2 the [dW; Y] area holds the split P3/P4 operands.  P3's A has
@@ -1859,6 +1860,14 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
     for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
     const float eGbR = __expf(Gb[R]), eLbR = __expf(Glast - Gb[R]);
+    // F(R, Rd) = exp(G_b(Rd) - G_b(R)) for the later blocks Rd, per channel: the
+    // factors of the Right copies below
+    {
+        float* sF = reinterpret_cast<float*>(smem + LB_F);
+#pragma unroll
+        for (int Rd = 1; Rd < 4; ++Rd)
+            if (Rd > R) sF[f_slot(R, Rd) * kD + c] = __expf(Gb[Rd] - Gb[R]);
+    }
     {
         const bool got = wait_bar_warp(bar_tma, ph, 41);
         if (got && tid == 0) ++main_waited;
@@ -1957,9 +1966,9 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                      sdesc_mn_sw128(tt + kk * 2048, 8192), id64 | kAMajorMN | kBMajorMN, kk > 0);
         mma_commit(bar_m1);
     }
-    // Right_Rr rows of block R for Rr > R: Right_R scaled by exp(G_b(Rr) - G_b(R)),
-    // 16-byte units (6 block pairs x 16 rows x 16 chunks) spread over all
-    // threads while P1/P2 run
+    // Right_Rr rows of block R for Rr > R: Right_R scaled by F(R, Rr), 16-byte
+    // units (6 block pairs x 16 rows x 16 chunks) spread over all threads
+    // while P1/P2 run; pair pr is F's slot
 #pragma unroll 1
     for (int e = 0; e < 3; ++e) {
         const int w = tid + e * kLocalTcThreads, pr = w >> 8, rem = w & 255;
@@ -1967,13 +1976,12 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int Rd = pr < 3 ? pr + 1 : pr < 5 ? pr - 1 : 3;
         const int r = 16 * Rs + (rem >> 4), oct = rem & 15, kb = oct >> 3, ch = oct & 7;
         const uint32_t co = (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
-        float gs[8], gd[8], x[8];
-        ld8f(sGb + Rs * kD + oct * 8, gs);
-        ld8f(sGb + Rd * kD + oct * 8, gd);
+        float f8[8], x[8];
+        ld8f(reinterpret_cast<const float*>(smem + LB_F) + pr * kD + oct * 8, f8);
         unpack8(*reinterpret_cast<const uint4*>(smem + LB_RIGHT + right_rel(Rs) +
                                                  kb * (16u * (Rs + 1) * 128u) + co), x);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] *= __expf(gd[i] - gs[i]);
+        for (int i = 0; i < 8; ++i) x[i] *= f8[i];
         *reinterpret_cast<uint4*>(smem + LB_RIGHT + right_rel(Rd) + kb * (16u * (Rd + 1) * 128u) +
                                   co) = pack8(x);
     }
