@@ -56,11 +56,11 @@ def _src_hash(name):
 # Measured at B=1, T=8192 (2048 chunks, inputs and workspace above L2),
 # scaled by the chunk count to the B=4 launch (8192 chunks).
 NCU_TRAFFIC = {
-    "tc_local_bwd": (4 * (354916608 + 79097344), "kda_tc.cu", "f3e1de5729e7"),
-    "tc_intra": (4 * (134690816 + 132693248), "kda_tc.cu", "f3e1de5729e7"),
-    "tc_grad_v": (4 * (286017792 + 197427200), "kda_tc.cu", "f3e1de5729e7"),
-    "tc_chain_fwd_save": (4 * (152090624 + 91252992), "kda_tc.cu", "f3e1de5729e7"),
-    "tc_chain_bwd": (4 * (152093952 + 64608512), "kda_tc.cu", "f3e1de5729e7"),
+    "tc_local_bwd": (4 * (354968832 + 78607360), "kda_tc.cu", "72b41d331d5e"),
+    "tc_intra": (4 * (134708736 + 132661504), "kda_tc.cu", "72b41d331d5e"),
+    "tc_grad_v": (4 * (286032640 + 197711360), "kda_tc.cu", "72b41d331d5e"),
+    "tc_chain_fwd_save": (4 * (152248320 + 91040768), "kda_tc.cu", "72b41d331d5e"),
+    "tc_chain_bwd": (4 * (152090368 + 64567040), "kda_tc.cu", "72b41d331d5e"),
 }
 
 
