@@ -143,10 +143,13 @@ def test_saved_backward_rejects_other_dims():
 
 
 @pytest.mark.parametrize("saved", [False, True])
-@pytest.mark.parametrize("B,T,H,HV", [(1, 64, 1, 1), (2, 192, 1, 4), (1, 320, 2, 2)])
+@pytest.mark.parametrize("B,T,H,HV", [(1, 64, 1, 1), (1, 128, 1, 1), (2, 192, 1, 4),
+                                      (1, 256, 1, 2), (1, 320, 2, 2)])
 def test_tcgen05_chunk_counts_and_groups(B, T, H, HV, saved):
-    """Tensor-core path on one chunk, odd chunk counts and a GVA group of 4,
-    with an initial state and the final state, stateless and saved backward."""
+    """Tensor-core path on one chunk, odd and even chunk counts (the state
+    passes alternate two state tiles and two stages) and GVA groups of 2 and
+    4, with an initial state and the final state, stateless and saved
+    backward."""
     w = I.Workload("tc_shapes", B, T, H, HV, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
                    h0_std=0.1, seed=31 + T + HV)
     inp = I.make_chunk_inputs(w)
