@@ -50,18 +50,30 @@ def _src_hash(name):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
-# keyed by kernel name: (bytes per launch at the benchmark workload, the
-# source file, that file's hash when captured).  A kernel whose source has
-# changed since reports traffic null.
-# Measured at B=1, T=8192 (2048 chunks, inputs and workspace above L2),
-# scaled by the chunk count to the B=4 launch (8192 chunks).
+# keyed by kernel name: (bytes per launch at the capture workload, the source
+# file, that file's hash when captured).  A kernel whose source has changed
+# since reports traffic null.  Captured at B=1, T=8192, HV=16 (2048 chunks,
+# inputs and workspace above L2); the traffic grows with the chunk count, so a
+# launch at another size reports the bytes scaled by its head-tokens.
+NCU_TRAFFIC_HEAD_TOKENS = 1 * 8192 * 16
 NCU_TRAFFIC = {
-    "tc_local_bwd": (4 * (354968832 + 78607360), "kda_tc.cu", "72b41d331d5e"),
-    "tc_intra": (4 * (134708736 + 132661504), "kda_tc.cu", "72b41d331d5e"),
-    "tc_grad_v": (4 * (286032640 + 197711360), "kda_tc.cu", "72b41d331d5e"),
-    "tc_chain_fwd_save": (4 * (152248320 + 91040768), "kda_tc.cu", "72b41d331d5e"),
-    "tc_chain_bwd": (4 * (152090368 + 64567040), "kda_tc.cu", "72b41d331d5e"),
+    "tc_local_bwd": (354968832 + 78607360, "kda_tc.cu", "72b41d331d5e"),
+    "tc_intra": (134708736 + 132661504, "kda_tc.cu", "72b41d331d5e"),
+    "tc_grad_v": (286032640 + 197711360, "kda_tc.cu", "72b41d331d5e"),
+    "tc_chain_fwd_save": (152248320 + 91040768, "kda_tc.cu", "72b41d331d5e"),
+    "tc_chain_bwd": (152090368 + 64567040, "kda_tc.cu", "72b41d331d5e"),
 }
+
+
+def ncu_traffic(name, w):
+    """Measured DRAM bytes per launch of kernel `name` at workload w, or None
+    when there is no capture of its current source."""
+    if name not in NCU_TRAFFIC:
+        return None
+    tb, src, h = NCU_TRAFFIC[name]
+    if _src_hash(src) != h:
+        return None
+    return int(round(tb * (w.B * w.T * w.HV) / NCU_TRAFFIC_HEAD_TOKENS))
 
 
 def kernel_algo_bytes(name, w):
@@ -130,8 +142,7 @@ def kernel_entry(name, total_ms, launches, total_k, w, hbm):
         e["algo_gbs"] = algo / (per / 1e3) / 1e9
         e["frac"] = e["algo_gbs"] / hbm
     if name in NCU_TRAFFIC:
-        tb, src, h = NCU_TRAFFIC[name]
-        e["traffic"] = tb if _src_hash(src) == h else None
+        e["traffic"] = ncu_traffic(name, w)
     return e
 
 
@@ -474,10 +485,7 @@ def main():
     per_launch_ms = dom_ms / dom_n
     algo = kernel_algo_bytes(dom, w)
     achieved = algo / (per_launch_ms / 1e3) / 1e9 if algo else None
-    traffic = None
-    if dom in NCU_TRAFFIC:
-        tb, src, h = NCU_TRAFFIC[dom]
-        traffic = tb if _src_hash(src) == h else None
+    traffic = ncu_traffic(dom, w)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
                 "unit": "GB/s", "frac": (achieved / hbm) if achieved else None,
                 "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs, copy bandwidth)",
