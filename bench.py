@@ -80,7 +80,7 @@ def kernel_algo_bytes(name, w):
     """Algorithmic bytes one launch of kernel `name` must move at workload w.
 
     Inputs are counted once at their dtype, outputs once, fp32 workspace
-    intermediates once each way (per-kernel rooflines)."""
+    intermediates once each way."""
     B, T, H, HV, K, V, C = w.B, w.T, w.H, w.HV, w.K, w.V, w.chunk
     e = 2 if str(w.dtype).endswith("bfloat16") else 4
     BH, NT = B * HV, T // C

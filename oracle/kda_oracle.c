@@ -26,7 +26,7 @@
  *       hv / G; dq/dk summed back over the group), scale 1/sqrt(K) applied to
  *       q at entry, g clamped before exp with lower bound -5.
  *
- *   Readings taken where the pages are open (each is listed in the design doc):
+ *   Readings taken where the pages are open:
  *     - k reads the decayed state diag(a_t) S_{t-1} (the row-L1 formula
  *       applies exp(g) first and then writes "k_t.S" of that product).
  *     - beta is one scalar per token and value head, used as given.

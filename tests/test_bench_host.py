@@ -1,0 +1,62 @@
+"""Host logic of bench.py: the algorithmic bytes per launch (the roofline
+numerators) and the scaling of the measured DRAM traffic.  No GPU."""
+import dataclasses
+import importlib.util
+import os
+
+import pytest
+
+from gated_delta_rule_41_gb300 import inputs as I
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_host", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+# bytes per head-token of each tensor-core kernel's own inputs and outputs at
+# K = V = 128, chunk 64, bf16, one value head per key head
+PER_HEAD_TOKEN = {
+    "tc_intra": 2442,
+    "tc_chain_fwd": 1416,
+    "tc_chain_fwd_save": 2184,
+    "tc_chain_states": 1928,
+    "tc_chain_bwd": 1928,
+    "tc_grad_v": 4110,
+    "tc_local_bwd": 3472,
+}
+
+
+@pytest.mark.parametrize("name", sorted(PER_HEAD_TOKEN))
+def test_tc_algorithmic_bytes_per_head_token(bench, name):
+    w = I.TRAIN_BF16
+    head_tokens = w.B * w.T * w.HV
+    assert bench.kernel_algo_bytes(name, w) == PER_HEAD_TOKEN[name] * head_tokens
+
+
+def test_tc_algorithmic_bytes_scale_with_the_workload(bench):
+    w = I.TRAIN_BF16
+    half = dataclasses.replace(w, B=w.B // 2)
+    for name in PER_HEAD_TOKEN:
+        assert 2 * bench.kernel_algo_bytes(name, half) == bench.kernel_algo_bytes(name, w)
+
+
+def test_measured_traffic_scales_with_head_tokens(bench):
+    w = I.TRAIN_BF16
+    for name, (tb, src, h) in bench.NCU_TRAFFIC.items():
+        got = bench.ncu_traffic(name, w)
+        if bench._src_hash(src) != h:
+            assert got is None   # source changed since the capture
+            continue
+        assert got == round(tb * w.B * w.T * w.HV / bench.NCU_TRAFFIC_HEAD_TOKENS)
+    assert bench.ncu_traffic("no_such_kernel", w) is None
+
+
+def test_measured_traffic_is_dropped_for_a_changed_source(bench, monkeypatch):
+    monkeypatch.setattr(bench, "_src_hash", lambda src: "0" * 12)
+    assert all(bench.ncu_traffic(n, I.TRAIN_BF16) is None for n in bench.NCU_TRAFFIC)
