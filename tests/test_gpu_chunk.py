@@ -246,6 +246,31 @@ def test_train_shape_full_size_sampled_heads(impl):
         assert torch.isfinite(res[n].float()).all(), n
 
 
+def test_train_shape_full_size_saved_sampled_heads():
+    """The configuration the benchmark times: a saving forward, then the
+    backward from its workspace, at the full training size (AUTO takes the
+    tensor cores), on sampled heads against the oracle."""
+    w = I.TRAIN_BF16
+    heads = [(0, 3), (2, 12)]
+    inp = I.make_chunk_inputs(w, device="cuda")
+    o, ht, sv = kda.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                  initial_state=inp["h0"], output_final_state=True,
+                                  chunk_size=w.chunk, save_for_backward=True)
+    res = dict(o=o, ht=ht)
+    res.update(kda.chunk_kda_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["do"],
+                                 dht=inp["dht"], initial_state=inp["h0"], chunk_size=w.chunk,
+                                 saved=sv))
+    torch.cuda.synchronize()
+    kda.check()
+    refs = oracle_chunk(inp, True, heads=heads)
+    for (b, hv), ref in zip(heads, refs):
+        sl = lambda x: x[b:b + 1, :, hv:hv + 1]
+        assert_close(f"o[{b},{hv}]", sl(res["o"]), ref["o"], w.dtype)
+        assert_close(f"ht[{b},{hv}]", res["ht"][b:b + 1, hv:hv + 1], ref["ht"], w.dtype)
+        for n in GRADS:
+            assert_close(f"{n}[{b},{hv}]", sl(res[n]), ref[n], w.dtype)
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_long_context_full_size_sampled_heads(impl):
     _sampled(I.LONG_BF16, [(0, 0), (0, 31)], impl, backward=False)
