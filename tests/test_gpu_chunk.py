@@ -276,6 +276,25 @@ def test_long_context_full_size_sampled_heads(impl):
     _sampled(I.LONG_BF16, [(0, 0), (0, 31)], impl, backward=False)
 
 
+@pytest.mark.parametrize("impl,K,dtype", [("simt", 64, torch.bfloat16), ("simt", 64, torch.float32),
+                                           ("tcgen05", 128, torch.bfloat16)])
+def test_96_heads_sampled(impl, K, dtype):
+    """H = HV = 96 heads, head dim 64 (CUDA-core path) and 128 (tensor cores),
+    with an initial state, on sampled heads against the oracle."""
+    w = I.Workload("heads96", 1, 256, 96, 96, K, K, 64, dtype, g_sigma=2.0, h0_std=0.1,
+                   seed=41 + K)
+    inp = I.make_chunk_inputs(w, device="cuda")
+    res = run_gpu(inp, w, impl)
+    heads = [(0, 0), (0, 47), (0, 95)]
+    refs = oracle_chunk(inp, True, heads=heads)
+    for (b, hv), ref in zip(heads, refs):
+        sl = lambda x: x[b:b + 1, :, hv:hv + 1]
+        assert_close(f"o[{hv}]", sl(res["o"]), ref["o"], w.dtype)
+        assert_close(f"ht[{hv}]", res["ht"][b:b + 1, hv:hv + 1], ref["ht"], w.dtype)
+        for n in GRADS:
+            assert_close(f"{n}[{hv}]", sl(res[n]), ref[n], w.dtype)
+
+
 def test_impls_agree_train_shape_subset():
     """The SIMT and tensor-core paths agree with each other on a slice of the
     training workload (T = 1024)."""
