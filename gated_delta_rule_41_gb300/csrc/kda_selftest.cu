@@ -34,24 +34,11 @@ bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// MN-major operand descriptor with the 128-byte swizzle: for each K index a
-// 128-byte row of 64 consecutive M/N elements, 8 K-rows per 1024-byte atom.
-// `mn_stride` = bytes between consecutive 64-element M/N blocks, `k_stride`
-// = bytes between consecutive 8-row K groups.
-__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
 // 128 threads.  smem (160 KB, so that any stride reading stays in bounds):
 // A tile at 0 (16 KB), B tile at 64 KB (up to 16 KB), barriers at 144 KB.
-// flags: bit0 TMA staging, bit1 A MN-major, bit2 B MN-major, bit3 swap the
-// two stride fields of the MN-major descriptors.
+// flags: bit0 TMA staging, bit1 A MN-major, bit2 B MN-major.  MN-major
+// operands use the chunk kernels' descriptor (64-element M/N blocks 8 KB
+// apart, 8-row K groups 1 KB apart).
 __global__ void __launch_bounds__(128, 1)
 selftest_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
                 const __nv_bfloat16* __restrict__ A, const __nv_bfloat16* __restrict__ B,
@@ -59,8 +46,7 @@ selftest_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int use_tma = flags & 1, a_mn = (flags >> 1) & 1, b_mn = (flags >> 2) & 1,
-              swap = (flags >> 3) & 1;
+    const int use_tma = flags & 1, a_mn = (flags >> 1) & 1, b_mn = (flags >> 2) & 1;
     uint8_t* sA = smem;
     uint8_t* sB = smem + 65536;
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + 147456);
@@ -124,11 +110,10 @@ selftest_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ 
         tc_fence_after();
         const uint32_t idesc =
             idesc_bf16_f32(128, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
-        const uint32_t lbo = swap ? 1024u : 8192u, sbo = swap ? 8192u : 1024u;
         for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = a_mn ? sdesc_mn_sw128(smem_u32(sA) + kk * 2048, lbo, sbo)
+            const uint64_t ad = a_mn ? sdesc_mn_sw128(smem_u32(sA) + kk * 2048, 8192)
                                      : sdesc_sw128(smem_u32(sA) + kk * 32);
-            const uint64_t bd = b_mn ? sdesc_mn_sw128(smem_u32(sB) + kk * 2048, lbo, sbo)
+            const uint64_t bd = b_mn ? sdesc_mn_sw128(smem_u32(sB) + kk * 2048, 8192)
                                      : sdesc_sw128(smem_u32(sB) + kk * 32);
             mma_bf16(tmem, ad, bd, idesc, kk > 0);
         }
@@ -163,7 +148,7 @@ selftest_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ 
 extern "C" kda_status kda_selftest_mma(const void* A, const void* B, float* D, int N, int flags,
                                        int* status, void* stream) {
     using namespace kda;
-    if (!A || !B || !D || !status || (N != 64 && N != 128) || flags < 0 || flags > 15)
+    if (!A || !B || !D || !status || (N != 64 && N != 128) || flags < 0 || flags > 7)
         return KDA_ERR_INVALID_ARG;
     const bool a_mn = (flags >> 1) & 1, b_mn = (flags >> 2) & 1;
     if ((a_mn || b_mn) && !(flags & 1)) return KDA_ERR_INVALID_ARG;  // MN-major needs TMA

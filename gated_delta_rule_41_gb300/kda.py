@@ -237,13 +237,13 @@ def timing_read() -> dict:
     return out
 
 
-def selftest_mma(A, B, use_tma=True, a_mn=False, b_mn=False, swap=False, stream=None):
+def selftest_mma(A, B, use_tma=True, a_mn=False, b_mn=False, stream=None):
     """D = A @ B^T through one tcgen05 MMA chain.  A [128,64] and B [N,64] bf16
     (K-major), or, with a_mn / b_mn, A^T [64,128] / B^T [64,N] (MN-major)."""
     lib = load_library()
     _check_dev(A, B)
     N = B.shape[1] if b_mn else B.shape[0]
-    flags = int(use_tma) | (int(a_mn) << 1) | (int(b_mn) << 2) | (int(swap) << 3)
+    flags = int(use_tma) | (int(a_mn) << 1) | (int(b_mn) << 2)
     D = torch.zeros(128, N, dtype=torch.float32, device=A.device)
     status = torch.zeros(1, dtype=torch.int32, device=A.device)
     st = lib.kda_selftest_mma(_ptr(A), _ptr(B), _ptr(D), N, flags, _ptr(status),

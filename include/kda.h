@@ -158,15 +158,21 @@ kda_status kda_recurrent_step(const kda_dims* dims, const void* q, const void* k
  *   Arguments and results are those of kda_chunk_fwd without the workspace;
  *   dims->impl is ignored and the SIMT kernels run.  Their scratch lives in a
  *   file-scope device array of 32 MiB that every GPU loading the library
- *   keeps until the process exits.  Sizes whose scratch would exceed 32 MiB
- *   are rejected with KDA_ERR_WORKSPACE before anything is enqueued (about
- *   B*HV*T*(4K+2V)*4 bytes plus two 64x64 fp32 matrices per chunk and head).
+ *   keeps until the process exits.  The scratch a call needs is
+ *   kda_chunk_workspace_bytes of the same dims with impl = KDA_IMPL_SIMT and
+ *   for_bwd = 0; calls that need more than 32 MiB are rejected with
+ *   KDA_ERR_WORKSPACE before anything is enqueued.
  *   The function calls no cudaMalloc, cudaFree or allocating library routine.
- *   Its first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress with that device current); make that first call
- *   before any stream capture.  Every call shares the one array and nothing in
- *   it needs to start at zero; calls whose work overlaps on the GPU (several
- *   streams, several host threads) race on it, so serialise them. */
+ *   It finds the array's device address with cudaGetSymbolAddress (with the
+ *   calling device current) on every call made outside stream capture, so a
+ *   device reset is picked up; a call made while `stream` is captured uses
+ *   the address found by the last call outside capture on that device, and
+ *   fails with KDA_ERR_CUDA if there was none.  Any call that passes the
+ *   size check (an empty problem included) does that look-up: make one on
+ *   each device before capturing.  Every call shares the one array and
+ *   nothing in it needs to start at zero; calls whose work overlaps on the
+ *   GPU (several streams, several host threads) race on it, so serialise
+ *   them. */
 kda_status kda_chunk_fwd_noalloc(const kda_dims* dims, const void* q, const void* k,
                                  const void* v, const void* g, const void* beta, const float* h0,
                                  void* o, int output_final_state, float* ht, void* stream);
@@ -194,9 +200,9 @@ int kda_timing_entry(int i, char* name, int name_len, double* total_ms, long* la
  * all device pointers) with one tcgen05 MMA chain from 128B-swizzled
  * shared-memory tiles.  flags: bit 0 stage by TMA (else by thread stores);
  * bit 1 A is given K-minor, i.e. as A^T [64][128] row-major (MN-major
- * operand, TMA only); bit 2 B likewise as B^T [64][N]; bit 3 swap the two
- * stride fields of the MN-major descriptor.  *status (device int,
- * caller-zeroed) is set to 1 if a bounded device wait expired. */
+ * operand, TMA only); bit 2 B likewise as B^T [64][N].  Other bits are
+ * rejected with KDA_ERR_INVALID_ARG.  *status (device int, caller-zeroed) is
+ * set to 1 if a bounded device wait expired. */
 kda_status kda_selftest_mma(const void* A, const void* B, float* D, int N, int flags,
                             int* status, void* stream);
 

@@ -196,6 +196,34 @@ def test_clamp_active_below_minus_five(impl):
     assert torch.all(res["dg"].float().cpu()[inp["g"].float() < -5] == 0)
 
 
+@pytest.mark.parametrize("saved", [False, True])
+def test_tcgen05_clamp_below_minus_five(saved):
+    """The tensor-core kernels at K = V = 128 on gates far below -5 (down to
+    about -15) plus a block of exact -5 values: the in-kernel clamp must hold
+    every in-chunk decay factor in range, and dg must vanish where g < -5
+    (the K3 README's lower bound of -5 on the log-decay, row "exp 下溢")."""
+    w = I.Workload("clamp_tc", 1, 256, 2, 2, 128, 128, 64, torch.bfloat16, g_mu=3.0,
+                   g_sigma=3.0, h0_std=0.1, seed=24)
+    inp = I.make_chunk_inputs(w, g_floor=None)
+    g = inp["g"].float()
+    g[:, 64:72] = -5.0  # exact boundary values, inside the second chunk
+    inp["g"] = g.to(w.dtype)
+    below = inp["g"].float() < -5
+    assert below.float().mean() > 0.2 and inp["g"].float().min() < -12
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    out = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
+                            output_final_state=True, impl="tcgen05", save_for_backward=saved)
+    o, ht = out[0], out[1]
+    res = dict(o=o, ht=ht)
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                 initial_state=t["h0"], impl="tcgen05",
+                                 saved=out[2] if saved else None))
+    torch.cuda.synchronize()
+    kda.check()
+    compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
+    assert torch.all(res["dg"].float().cpu()[below] == 0)
+
+
 def test_ragged_value_width_simt():
     """V not a multiple of the 32-column tile, small K."""
     w = I.Workload("ragged_v", 1, 64, 1, 2, 16, 40, 32, torch.float32, h0_std=0.5, dht=True,

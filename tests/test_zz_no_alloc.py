@@ -1,5 +1,6 @@
 """The allocation-free forward (kda_chunk_fwd_noalloc) against the regular
-workspace forward (kda_chunk_fwd with the SIMT kernels), through the C ABI.
+workspace forward (kda_chunk_fwd with the SIMT kernels) and against the
+float64 oracle, through the C ABI.
 
 It exists for callers that cannot allocate device memory where they run the
 scan (graph capture, fixed memory pools); its scratch is a 32 MiB device
@@ -12,7 +13,7 @@ import torch
 import gated_delta_rule_41_gb300 as kda
 from gated_delta_rule_41_gb300 import inputs as I
 from gated_delta_rule_41_gb300.kda import _ptr, _stream, make_dims, KdaDims
-from parity_util import assert_close
+from parity_util import assert_close, oracle_chunk
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +54,10 @@ def test_noalloc_forward_matches_workspace_forward_twice(lib):
         kda.check()
         assert_close("o", o, o_ref.double().cpu().numpy(), w.dtype)
         assert_close("ht", ht, ht_ref.double().cpu().numpy(), w.dtype)
+        ref = oracle_chunk({n: (x.cpu() if x is not None else None) for n, x in t.items()},
+                           False)
+        assert_close("o vs oracle", o, ref["o"], w.dtype)
+        assert_close("ht vs oracle", ht, ref["ht"], w.dtype)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
