@@ -62,7 +62,11 @@ NCU_TRAFFIC = {
     "tc_grad_v": (286032640 + 197711360, "kda_tc.cu", "72b41d331d5e"),
     "tc_chain_fwd_save": (152248320 + 91040768, "kda_tc.cu", "72b41d331d5e"),
     "tc_chain_bwd": (152090368 + 64567040, "kda_tc.cu", "72b41d331d5e"),
+    "tc_chain_fwd": (152121344 + 20483072, "kda_tc.cu", "72b41d331d5e"),
 }
+# decode_kernel: dram read + write per launch at the decode workload (B=256,
+# HV=16, K=V=128), its source file and that file's hash when captured
+NCU_DECODE_TRAFFIC = (272689408 + 205644032, "kda_decode.cu", "9487616a3015")
 
 
 def ncu_traffic(name, w):
@@ -132,15 +136,46 @@ def kernel_algo_bytes(name, w):
     return None
 
 
+def kernel_method_bytes(name, w):
+    """The method's own bytes (the per-head-token budget of the fused path)
+    that one launch of kernel `name` moves: the tensors of the method it
+    reads or writes, each counted once at its dtype, and the fp32
+    chunk-boundary states at the budget's one write and one read.  Workspace
+    intermediates of this design do not count.  Summed over a step's kernels
+    this is exactly the step's budget (1282 + 4356 B per head-token at
+    K = V = 128, bf16, one value head per key head)."""
+    B, T, H, HV, K, V, C = w.B, w.T, w.H, w.HV, w.K, w.V, w.chunk
+    e = 2 if str(w.dtype).endswith("bfloat16") else 4
+    G = HV // H
+    qk = K * e // G                      # q or k, per value head
+    states = K * V * 4 // C              # fp32 chunk-boundary state, per head-token
+    per = {
+        "tc_intra": 2 * qk + V * e + K * e + e,          # q, k, v, g, beta in
+        "tc_chain_fwd": V * e,                           # o out
+        "tc_chain_fwd_save": V * e + states,             # o out, states written
+        "tc_chain_bwd": V * e,                           # do in
+        "tc_grad_v": V * e + states + V * e,             # v in, states read, dv out
+        "tc_local_bwd": 2 * (2 * qk + K * e + e),        # q, k, g, beta in; dq, dk, dg, dbeta out
+    }
+    return B * HV * T * per[name] if name in per else None
+
+
 def kernel_entry(name, total_ms, launches, total_k, w, hbm):
-    """Per-kernel line: launches, time, share, algorithmic GB/s and its
-    fraction of the copy peak, and the measured DRAM bytes per launch."""
+    """Per-kernel line: launches, time, share; the method's bytes it moves and
+    their rate against the copy peak; its own design bytes (inputs and outputs
+    including workspace intermediates) and their rate; and the measured DRAM
+    bytes per launch."""
     per = total_ms / launches
-    algo = kernel_algo_bytes(name, w)
     e = {"launches": launches, "ms_per_launch": per, "share": total_ms / total_k}
-    if algo:
-        e["algo_gbs"] = algo / (per / 1e3) / 1e9
-        e["frac"] = e["algo_gbs"] / hbm
+    method = kernel_method_bytes(name, w)
+    if method:
+        e["method_bytes"] = method
+        e["method_gbs"] = method / (per / 1e3) / 1e9
+        e["frac"] = e["method_gbs"] / hbm
+    design = kernel_algo_bytes(name, w)
+    if design:
+        e["design_bytes"] = design
+        e["design_gbs"] = design / (per / 1e3) / 1e9
     if name in NCU_TRAFFIC:
         e["traffic"] = ncu_traffic(name, w)
     return e
@@ -230,6 +265,12 @@ def oracle_whole(w, inp_cpu, min_seconds=10.0, max_passes=4):
 
 
 def reference_arm(args, w):
+    """The oracle as it stands, timed on the host cores: each step runs it
+    (forward + backward) on a bounded sample of the workload -- the first
+    `tsample` tokens of `nheads` heads -- and the line's value scales that
+    sample's throughput to whole-workload tokens/s (the oracle's cost is
+    linear in heads and in tokens).  ms_per_step is the time a sample step
+    actually took."""
     import torch as _t  # noqa: F401
     from gated_delta_rule_41_gb300 import inputs as I
     import oracle
@@ -239,16 +280,21 @@ def reference_arm(args, w):
     tsample = 1024
     for _ in range(args.warmup):
         oracle_sample(w, inp, nheads, tsample)
-    vals = []
+    vals, secs = [], []
     for _ in range(args.steps):
         v, dt, cores = oracle_sample(w, inp, nheads, tsample)
         vals.append(v)
+        secs.append(dt)
     value = statistics.median(vals)
-    sample = (f"per step: first {tsample} of T={w.T} tokens of {nheads} of {w.B * w.HV} "
-              f"heads, forward+backward, scaled to the whole workload")
+    sample = (f"per step: the first {tsample} of T={w.T} tokens of {nheads} of {w.B * w.HV} "
+              f"heads, forward+backward ({nheads * tsample} head-tokens of "
+              f"{w.B * w.HV * w.T}); value = that throughput scaled to the whole workload")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": w.tokens / value * 1e3, "higher_is_better": True,
+            "ms_per_step": statistics.median(secs) * 1e3,
+            "ms_per_step_note": "seconds of one sample step as timed (not the whole workload)",
+            "whole_workload_ms_extrapolated": w.tokens / value * 1e3,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w, "oracle"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
@@ -264,6 +310,65 @@ def workload_config(w, path, bwd="saved"):
             "l2": f"inputs larger than L2 (q, k, v, g = {4 * w.B * w.T * w.HV * w.K * 2 >> 20} MiB "
                   f"bf16; no flush needed)",
             "parallelism": "one independent replica per rank"}
+
+
+def fwd_method_bytes(w, final_state):
+    """The forward's own bytes for workload w: q, k (once per key head), v, g,
+    beta read and o written, at the input dtype; plus the fp32 final state
+    when it is returned."""
+    e = 2 if str(w.dtype).endswith("bfloat16") else 4
+    per = 2 * w.K * e // (w.HV // w.H) + w.V * e + w.K * e + e + w.V * e
+    b = w.B * w.T * w.HV * per
+    if final_state:
+        b += w.B * w.HV * w.K * w.V * 4
+    return b
+
+
+def measure_forward(kda, w, dev, hbm, steps, warmup, path):
+    """Forward only (kda_chunk_fwd, nothing kept for a backward) on workload
+    w, inputs resident, timed with CUDA events on the launching stream; its
+    HBM roofline on the method's bytes and the per-kernel split."""
+    from gated_delta_rule_41_gb300 import inputs as I
+    inp = I.make_chunk_inputs(w, device=dev)
+    q, k, v, g, beta = (inp[n] for n in ("q", "k", "v", "g", "beta"))
+    dims = kda.kda.make_dims(q, v, w.chunk, None, path)
+    ws = torch.empty(max(1, kda.workspace_bytes(dims, False)), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(v)
+    ht = (torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32, device=dev)
+          if w.final_state else None)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        kda.chunk_kda_fwd(q, k, v, g, beta, chunk_size=w.chunk, impl=path, workspace=ws, out=o,
+                          output_final_state=w.final_state, final_state=ht)
+
+    for _ in range(max(warmup, 3)):
+        fwd()
+    torch.cuda.synchronize()
+    kda.check()
+    kda.timing_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fwd()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    kernels = kda.timing_read()
+    kda.timing_enable(False)
+    kda.check()
+    ms = e0.elapsed_time(e1) / steps
+    method = fwd_method_bytes(w, w.final_state)
+    gbs = method / (ms / 1e3) / 1e9
+    total_k = sum(t for t, _ in kernels.values()) or 1.0
+    l2 = 4 * w.B * w.T * w.HV * w.K * 2 >> 20
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K, "V": w.V,
+            "chunk": w.chunk, "final_state": w.final_state, "tokens_per_s": w.tokens / (ms / 1e3),
+            "ms_per_step": ms, "steps": steps, "method_bytes": method, "achieved_gbs": gbs,
+            "peak_gbs": hbm, "frac": gbs / hbm, "bound": "hbm",
+            "gpu_launches_per_step": sum(n for _, n in kernels.values()) / steps,
+            "l2": f"inputs larger than L2 (q, k, v, g = {l2} MiB); no flush needed",
+            "kernels": {n: {"ms_per_launch": t / c, "launches": c, "share": t / total_k}
+                        for n, (t, c) in sorted(kernels.items(), key=lambda x: -x[1][0])}}
 
 
 def measure_decode(kda, dev, hbm):
@@ -289,7 +394,9 @@ def measure_decode(kda, dev, hbm):
     io = w.B * (2 * w.H * w.K + w.HV * (w.V + w.K + 1) + w.HV * w.V) * el
     bytes_ = 2 * state.numel() * 4 + io
     gbs = bytes_ / (ms / 1e3) / 1e9
+    tb, src, h = NCU_DECODE_TRAFFIC
     return {"workload": w.name, "ms_per_step": ms, "bytes_per_step": bytes_,
+            "traffic": tb if _src_hash(src) == h else None,
             "achieved_gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm, "bound": "hbm",
             "note": "state read once and written once per step; state (256 MiB) > L2"}
 
@@ -313,6 +420,9 @@ def main():
                     help="override the batch (profiling / sweeps; default: the workload's)")
     ap.add_argument("--T", type=int, default=None,
                     help="override the sequence length (profiling / sweeps)")
+    ap.add_argument("--part", default="all", choices=["all", "step", "fwd", "long", "decode"],
+                    help="profiling: run only the fwd+bwd step, the forward-only line, the "
+                         "long-context forward or the decode leg (default: all, one JSON line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -345,6 +455,20 @@ def main():
     from gated_delta_rule_41_gb300 import build as kbuild
     kbuild.build()
     import gated_delta_rule_41_gb300 as kda
+
+    hbm, tf, tf_sus, peak_src = _peaks()
+    if args.part in ("fwd", "long", "decode"):
+        # one part alone (for a profiler): its own line, no step
+        if args.part == "decode":
+            part = measure_decode(kda, dev, hbm)
+        else:
+            pw = w if args.part == "fwd" else I.LONG_BF16
+            part = measure_forward(kda, pw, dev, hbm, args.steps, args.warmup, args.path)
+        if rank == 0:
+            print(json.dumps({"part": args.part, **part}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     inp = I.make_chunk_inputs(w, device=dev, seed=w.seed + rank)
     q, k, v, g, beta, do = (inp[n] for n in ("q", "k", "v", "g", "beta", "do"))
@@ -477,19 +601,25 @@ def main():
             dist.destroy_process_group()
         return
 
-    # ---- roofline of the dominant kernel ----
-    hbm, tf, tf_sus, peak_src = _peaks()
+    # ---- roofline of the dominant kernel, on the method's bytes ----
+    # The numerator is what the method itself must move through this kernel
+    # (kernel_method_bytes: its share of the 5638 B per head-token budget),
+    # not the design's workspace intermediates (reported as design_bytes).
     total_k = sum(t for t, _ in kernels.values()) or 1.0
     dom = max(kernels, key=lambda n: kernels[n][0])
     dom_ms, dom_n = kernels[dom]
     per_launch_ms = dom_ms / dom_n
-    algo = kernel_algo_bytes(dom, w)
-    achieved = algo / (per_launch_ms / 1e3) / 1e9 if algo else None
+    method = kernel_method_bytes(dom, w)
+    achieved = method / (per_launch_ms / 1e3) / 1e9 if method else None
     traffic = ncu_traffic(dom, w)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
                 "unit": "GB/s", "frac": (achieved / hbm) if achieved else None,
                 "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs, copy bandwidth)",
-                "algo_bytes_per_launch": algo, "ms_per_launch": per_launch_ms}
+                "method_bytes_per_launch": method, "design_bytes_per_launch":
+                kernel_algo_bytes(dom, w), "ms_per_launch": per_launch_ms,
+                "note": "achieved = the method's bytes this kernel moves (its share of the "
+                        "per-head-token budget) / its CUDA-event time; traffic = ncu DRAM "
+                        "bytes per launch (null if its source changed since the capture)"}
     step_bytes = w.B * w.T * w.HV * (FWD_BYTES_PER_HEAD_TOKEN + BWD_BYTES_PER_HEAD_TOKEN)
     step_roof_ms = step_bytes / (hbm * 1e9) * 1e3
     line = {
@@ -499,17 +629,28 @@ def main():
         "data": "synthetic", "config": workload_config(w, args.path, args.bwd),
         "roofline": roofline,
         "step_roofline": {"bytes": step_bytes, "roofline_ms": step_roof_ms,
-                          "frac": step_roof_ms / ms, "note": "whole fwd+bwd step at HBM peak"},
+                          "achieved_gbs": step_bytes / (ms / 1e3) / 1e9,
+                          "frac": step_roof_ms / ms, "peak": hbm,
+                          "note": "whole fwd+bwd step: 5638 B per head-token at the copy peak"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "via": "the Python binding (kda.chunk_kda_fwd / chunk_kda_bwd); torch copies "
+                       "pinned host buffers to and from the device, the C ABI takes device "
+                       "pointers"},
         "gpu_launches": int(sum(n for _, n in kernels.values())),
         "kernels": {n: kernel_entry(n, t, c, total_k, w, hbm)
                     for n, (t, c) in sorted(kernels.items(), key=lambda x: -x[1][0])},
         "clocks": clocks,
     }
-    if world == 1:
+    if world == 1 and args.part == "all":
+        # forward only (inference): the training shape, and the long-context
+        # forward with its final state
+        line["forward"] = measure_forward(kda, w, dev, hbm, max(5, args.steps), 3, args.path)
+        line["long_context_forward"] = measure_forward(kda, I.LONG_BF16, dev, hbm, 3, 3,
+                                                       args.path)
+    if world == 1 and args.part == "all":
         line["decode"] = measure_decode(kda, dev, hbm)
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and args.part == "all":
         import oracle
         oracle.build()
         inp_cpu = {n: inp[n].cpu() for n in ("q", "k", "v", "g", "beta", "do")}

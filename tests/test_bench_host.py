@@ -60,3 +60,25 @@ def test_measured_traffic_scales_with_head_tokens(bench):
 def test_measured_traffic_is_dropped_for_a_changed_source(bench, monkeypatch):
     monkeypatch.setattr(bench, "_src_hash", lambda src: "0" * 12)
     assert all(bench.ncu_traffic(n, I.TRAIN_BF16) is None for n in bench.NCU_TRAFFIC)
+
+
+def test_method_bytes_of_a_step_sum_to_the_budget(bench):
+    """The method bytes attributed to the kernels of one fwd+bwd step (saving
+    forward + backward from its workspace) add up to the per-head-token
+    budget: 1282 B forward + 4356 B backward at K = V = 128, bf16."""
+    w = I.TRAIN_BF16
+    step = ["tc_intra", "tc_chain_fwd_save", "tc_chain_bwd", "tc_grad_v", "tc_local_bwd"]
+    total = sum(bench.kernel_method_bytes(n, w) for n in step)
+    assert total == (1282 + 4356) * w.B * w.T * w.HV
+    assert bench.kernel_method_bytes("tc_local_bwd", w) == 1540 * w.B * w.T * w.HV
+
+
+def test_forward_method_bytes(bench):
+    w = I.TRAIN_BF16
+    assert bench.fwd_method_bytes(w, False) == 1282 * w.B * w.T * w.HV
+    lw = I.LONG_BF16
+    assert bench.fwd_method_bytes(lw, True) == (1282 * lw.B * lw.T * lw.HV
+                                                + lw.B * lw.HV * lw.K * lw.V * 4)
+    # GVA: q and k are read once per key head
+    g = dataclasses.replace(w, H=w.HV // 2)
+    assert bench.fwd_method_bytes(g, False) == (1282 - 256) * w.B * w.T * w.HV
