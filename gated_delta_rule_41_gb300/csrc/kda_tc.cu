@@ -1127,51 +1127,59 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
 }
 
 // ===========================================================================
-// Intra-chunk quantities on tensor cores, one CTA (512 threads) per (chunk,
-// head): K3 row L2 steps (1)-(3) plus the operands of the state passes.
-//   (1) G = cumsum(max(g,-5)) per key channel (thread (c, R) owns channel c
-//       of the 16-row block R; block sums are exchanged through smem).
+// Intra-chunk quantities on tensor cores (K3 row L2 steps (1)-(3) plus the
+// operands of the state passes), one chunk of one head at a time per CTA of
+// 256 threads.  Shared memory stays under half an SM's, so two CTAs share an
+// SM and one's dependent phases (barriers, MMA and TMA waits, the triangular
+// inverse) overlap the other's work.
+//   (1) G_rel = cumsum of max(g, -5) inside each 16-row block, as one MMA:
+//       a constant 0/1 matrix (row r has ones at 16 floor(r/16) < r' <= r)
+//       times the clamped g tile.  The product has M = 128: rows 64-127
+//       repeat rows 0-63, so every TMEM lane quadrant holds a copy of the
+//       chunk's rows.  Block offsets G_b (G at each block's first row) and
+//       G_last follow from the block ends and block-start gates.
 //   (2) A, Aqk: the pairwise decay exp(G_i - G_j) is factored per 16-row
 //       block R with reference row b = 16R:  exp(G_i - G_b) <= 1 on the left,
 //       exp(G_b - G_j) on the right (<= 1 for earlier blocks, <= e^75 inside
 //       the block since g >= -5), so no factor overflows fp32/bf16.
-//       D_R = Left Right_R^T (M=128, N=16(R+1), K=128), where Left row
-//       32R + 16s + u holds token 16R+u (s=0: k, s=1: scale*q) times
-//       exp(G - G_b), so TMEM warp quadrant R holds exactly block R's rows.
+//       D_R = Left Right_R^T (M=128, N=16(R+1)), where Left row 32R + 16s + u
+//       holds token 16R+u (s=0: k, s=1: q) times exp(G - G_b), so TMEM warp
+//       quadrant R holds exactly block R's rows.  The product runs in two
+//       64-channel halves through one Left/Right buffer.
 //   (3) T = (I + A)^{-1} (fp32, blocked forward substitution),
-//       W^T = Khat^T (T diag beta)^T, U^T = V^T (T diag beta)^T with Khat and
-//       V read MN-major from their tiles.
-// Writes W, Qh, U, Kb, Aqk (bf16 operand arrays), T as bf16 high and low
-// parts (T2 + Tlo reproduce the fp32 T to about 16 bits) and gam.
+//       W = (T diag beta) Khat and U = (T diag beta) V as row-major products
+//       (M = 128: the T diag beta operand is stored twice), Khat and V read
+//       MN-major from their tiles.
+// Elementwise work runs with one thread per (row, 32 key channels); Qh and
+// Kb are written in place over the q and k tiles.  Every output leaves
+// through a TMA store of its shared-memory tile (W, Qh, U, Kb, Aqk) or as
+// 16-byte rows (T as bf16 high and low parts, when asked for) and gam.
 // ===========================================================================
-constexpr uint32_t I_K = 0, I_Q = 16384, I_G = 32768, I_V = 49152;   // TMA tiles, 16 KB each
-constexpr uint32_t I_LEFT = 65536;                                   // 128 rows x 128, 32 KB
-// Right_0..Right_3 stacked as one 160-row operand (rows 0-15, 16-47, 48-95,
-// 96-159), per 64-channel block of 160 x 128 B = 20 KB
-constexpr uint32_t I_R0 = 98304;
-constexpr uint32_t kRightKb = 160 * 128;
-constexpr uint32_t I_KHAT = I_G;     // Khat (the g tile itself goes to the G area I_SG)
-constexpr uint32_t I_TB = I_R0 + 40960;                              // T*beta, 64x64 bf16, 8 KB
+constexpr uint32_t J_L = 0;          // [128][64] bf16 block-lower-triangular ones (constant)
+constexpr uint32_t J_K = 16384;      // k tile -> Kb (in place) -> Aqk staging
+constexpr uint32_t J_Q = 32768;      // q tile -> Qh (in place) -> v tile -> U staging
+constexpr uint32_t J_G = 49152;      // g tile (clamped in place) -> Khat -> W staging
+constexpr uint32_t J_LR = 65536;     // Left half [128][64] + Right half [160][64]; then A, T
+constexpr uint32_t J_RIGHT = J_LR + 16384;
 constexpr int kAS = 68;              // row stride (floats) of A and T: rows stay 16-byte aligned
-constexpr uint32_t I_A = I_TB + 8192;                                // fp32 [64][kAS]
-constexpr uint32_t I_T = I_A + 64 * kAS * 4;                         // fp32 [64][kAS]
-constexpr uint32_t I_BETA = I_T + 64 * kAS * 4;                      // fp32 [64]
-constexpr uint32_t I_GX = I_BETA + 256;                              // fp32 [2][4][128]
-// G fp32 [64][128] for the operand build; before that it receives the g tile
-// by TMA, whose 128-byte swizzle needs a 1024-byte aligned destination
-constexpr uint32_t I_SG = (I_GX + 4096 + 1023) & ~1023u;
-constexpr uint32_t I_SC = I_SG + 32768;    // exp(G_b), exp(G_last - G_b) [4][128]; F [6][128]
-constexpr uint32_t I_BAR = I_SC + 14 * 512;
-constexpr uint32_t INTRA_SMEM = I_BAR + 64 + 1024;
-static_assert(INTRA_SMEM <= 232448, "intra kernel exceeds the per-CTA shared memory limit");
-static_assert(I_K % 1024 == 0 && I_Q % 1024 == 0 && I_V % 1024 == 0 && I_SG % 1024 == 0 &&
-                  I_LEFT % 1024 == 0 && I_R0 % 1024 == 0 && I_TB % 1024 == 0 && I_G % 1024 == 0,
+constexpr uint32_t J_A = J_LR;                       // fp32 [64][kAS]
+constexpr uint32_t J_T = J_LR + 64 * kAS * 4;        // fp32 [64][kAS]
+constexpr uint32_t J_TB = J_LR;      // T diag(beta), bf16 [128][64] (rows 64-127 repeat), over A
+constexpr uint32_t J_SCR = J_LR;     // block ends and block-start gates, fp32 [2][4][128]
+constexpr uint32_t J_BETA = J_LR + 36864;            // fp32 [64]
+constexpr uint32_t J_C = J_BETA + 256;               // exp(G_b) [4][128], exp(G_last-G_b) [4][128], F [6][128]
+constexpr uint32_t J_BAR = J_C + 14 * 512;
+constexpr uint32_t INTRA_SMEM = J_BAR + 64 + 1024;
+static_assert(J_T + 64 * kAS * 4 <= J_BETA, "A and T overflow the Left/Right area");
+static_assert(INTRA_SMEM <= 115712, "two intra CTAs must fit one SM's shared memory");
+static_assert(J_L % 1024 == 0 && J_K % 1024 == 0 && J_Q % 1024 == 0 && J_G % 1024 == 0 &&
+                  J_LR % 1024 == 0 && J_RIGHT % 1024 == 0,
               "128-byte swizzled tiles need 1024-byte aligned bases");
 
 // slot of F(R, Rr) = exp(G_b(Rr) - G_b(R)) for Rr > R among the six pairs
 __host__ __device__ constexpr int f_slot(int R, int Rr) { return R * (7 - R) / 2 + (Rr - R - 1); }
 
-constexpr int kIntraThreads = 512;
+constexpr int kIntraThreads = 256;
 
 // first row of Right_R in the stacked operand, which is also the first TMEM
 // column of D_R: sum_{J<R} 16 (J+1)
@@ -1181,7 +1189,7 @@ struct IntraArgs {
     int T, H, HV, NT, BH;
     float scale;
     const __nv_bfloat16* beta;
-    __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2, *Tlo;
+    __nv_bfloat16 *T2, *Tlo;   // null: T is not kept (plain forward)
     float* gam;
 };
 
@@ -1201,30 +1209,41 @@ __device__ __forceinline__ void intra_read_block(uint32_t taddr, float* out /* 6
     for (int j = N; j < 64; ++j) out[j] = 0.f;
 }
 
-__global__ void __launch_bounds__(kIntraThreads, 1)
+__global__ void __launch_bounds__(kIntraThreads, 2)
 intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
-                IntraArgs a) {
+                const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_q2,
+                const __grid_constant__ CUtensorMap tm_u2, const __grid_constant__ CUtensorMap tm_kb2,
+                const __grid_constant__ CUtensorMap tm_aqk2, IntraArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + I_BAR);   // k, q, g tiles
-    uint64_t* bar_a = bar_tma + 1;
-    uint64_t* bar_w = bar_tma + 2;
-    uint64_t* bar_v = bar_tma + 3;                                     // v tile
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 4);
-    float* sA = reinterpret_cast<float*>(smem + I_A);
-    float* sT = reinterpret_cast<float*>(smem + I_T);
-    float* sBeta = reinterpret_cast<float*>(smem + I_BETA);
-    float* sGtot = reinterpret_cast<float*>(smem + I_GX);   // [4][128] block sums
-    float* sGb = sGtot + 4 * kD;                             // [4][128] G at block starts
-    float* sG = reinterpret_cast<float*>(smem + I_SG);      // [64][128]
-    float* sEGb = reinterpret_cast<float*>(smem + I_SC);    // [4][128]
-    float* sELb = sEGb + 4 * kD;                             // [4][128]
-    float* sF = sELb + 4 * kD;                               // [6][128]
+    uint64_t* bar_kqg = reinterpret_cast<uint64_t*>(smem + J_BAR);   // k, q, g tiles
+    uint64_t* bar_v = bar_kqg + 1;                                     // v tile
+    uint64_t* bar_g = bar_kqg + 2;                                     // G_rel product
+    uint64_t* bar_a0 = bar_kqg + 3;                                    // D, channels 0-63
+    uint64_t* bar_a1 = bar_kqg + 4;                                    // D, channels 64-127
+    uint64_t* bar_w = bar_kqg + 5;                                     // W and U products
+    uint64_t* bar_fin = bar_kqg + 6;                                   // every product issued
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_kqg + 7);
+    float* sA = reinterpret_cast<float*>(smem + J_A);
+    float* sT = reinterpret_cast<float*>(smem + J_T);
+    float* sBeta = reinterpret_cast<float*>(smem + J_BETA);
+    float* sGend = reinterpret_cast<float*>(smem + J_SCR);   // [4][128] G_rel at block ends
+    float* sG0 = sGend + 4 * kD;                              // [4][128] clamped g at block starts
+    float* sEGb = reinterpret_cast<float*>(smem + J_C);      // [4][128] exp(G_b)
+    float* sELb = sEGb + 4 * kD;                              // [4][128] exp(G_last - G_b)
+    float* sF = sELb + 4 * kD;                                // [6][128]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int total = a.BH * a.NT;   // chunks; CTA i takes chunks i, i + grid, ...
+    // elementwise role: chunk row r (TMEM lane quadrant qd holds rows
+    // 32 (qd & 1) .. + 31) and channel quarter jq: channels 16 jq .. + 15 and
+    // 64 + 16 jq .. + 15
+    const int qd = warp & 3;
+    const int r = 32 * (qd & 1) + lane, R = r >> 4, u = r & 15;
+    const int jq = (qd >> 1) + 2 * (warp >> 2);
+    const uint32_t tlane = (uint32_t)(32 * qd) << 16;
 
     // token row of chunk ch, its value head and key head
     auto coords = [&](int ch, int& trow, int& hv, int& h) {
@@ -1233,30 +1252,41 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         h = hv / (a.HV / a.H);
         trow = (bb / a.HV) * a.T + nn * kC;
     };
-    // k, q, g tiles of chunk ch (g into the fp32 G area, which the build has
-    // finished reading) and, separately, its v tile
     // thread 0's counts of issued and consumed loads (every load is waited for
     // before the CTA exits)
     int kqg_issued = 0, v_issued = 0, kqg_waited = 0, v_waited = 0;
     auto issue_kqg = [&](int ch) {
         int trow, hv, h;
         coords(ch, trow, hv, h);
-        mbar_arrive_expect_tx(bar_tma, 3 * 16384);
-        tma_load_3d(smem + I_K, &tm_k, bar_tma, 0, h, trow);
-        tma_load_3d(smem + I_K + 8192, &tm_k, bar_tma, 64, h, trow);
-        tma_load_3d(smem + I_Q, &tm_q, bar_tma, 0, h, trow);
-        tma_load_3d(smem + I_Q + 8192, &tm_q, bar_tma, 64, h, trow);
-        tma_load_3d(smem + I_SG, &tm_g, bar_tma, 0, hv, trow);
-        tma_load_3d(smem + I_SG + 8192, &tm_g, bar_tma, 64, hv, trow);
+        mbar_arrive_expect_tx(bar_kqg, 3 * 16384);
+        tma_load_3d(smem + J_K, &tm_k, bar_kqg, 0, h, trow);
+        tma_load_3d(smem + J_K + 8192, &tm_k, bar_kqg, 64, h, trow);
+        tma_load_3d(smem + J_Q, &tm_q, bar_kqg, 0, h, trow);
+        tma_load_3d(smem + J_Q + 8192, &tm_q, bar_kqg, 64, h, trow);
+        tma_load_3d(smem + J_G, &tm_g, bar_kqg, 0, hv, trow);
+        tma_load_3d(smem + J_G + 8192, &tm_g, bar_kqg, 64, hv, trow);
         ++kqg_issued;
     };
     auto issue_v = [&](int ch) {
         int trow, hv, h;
         coords(ch, trow, hv, h);
         mbar_arrive_expect_tx(bar_v, 16384);
-        tma_load_3d(smem + I_V, &tm_v, bar_v, 0, hv, trow);
-        tma_load_3d(smem + I_V + 8192, &tm_v, bar_v, 64, hv, trow);
+        tma_load_3d(smem + J_Q, &tm_v, bar_v, 0, hv, trow);
+        tma_load_3d(smem + J_Q + 8192, &tm_v, bar_v, 64, hv, trow);
         ++v_issued;
+    };
+    // the chunk's tiles into L2 ahead of their loads
+    auto prefetch = [&](int ch) {
+        int trow, hv, h;
+        coords(ch, trow, hv, h);
+        tma_prefetch_3d(&tm_k, 0, h, trow);
+        tma_prefetch_3d(&tm_k, 64, h, trow);
+        tma_prefetch_3d(&tm_q, 0, h, trow);
+        tma_prefetch_3d(&tm_q, 64, h, trow);
+        tma_prefetch_3d(&tm_g, 0, hv, trow);
+        tma_prefetch_3d(&tm_g, 64, hv, trow);
+        tma_prefetch_3d(&tm_v, 0, hv, trow);
+        tma_prefetch_3d(&tm_v, 64, hv, trow);
     };
     auto load_beta = [&](int ch) {
         int trow, hv, h;
@@ -1265,23 +1295,38 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     };
 
     if (tid == 0) {
-        mbar_init(bar_tma, 1);
-        mbar_init(bar_a, 1);
-        mbar_init(bar_w, 1);
-        mbar_init(bar_v, 1);
+        for (int i = 0; i < 7; ++i) mbar_init(bar_kqg + i, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
         tmem_alloc(tmem_holder, 256);
         tmem_relinquish();
     }
+    // the constant block-lower-triangular operand: row i (token r = i & 63)
+    // has ones at 16 floor(r / 16) < r' <= r; thread t fills four 8-column units
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+        const int unit = tid + 256 * k4, i = unit >> 3, o = unit & 7, rr = i & 63;
+        const int lo = (rr & ~15) + 1;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = 8 * o + e;
+            x[e] = (c >= lo && c <= rr) ? 1.f : 0.f;
+        }
+        *reinterpret_cast<uint4*>(smem + J_L + sw128_offset(i, 8 * o)) = pack8(x);
+    }
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     if (tid == 0 && (int)blockIdx.x < total) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_g);
+        prefetch_tmap(&tm_v);
         issue_kqg(blockIdx.x);
-        issue_v(blockIdx.x);
     }
     float beta_next = (tid < kC && (int)blockIdx.x < total) ? load_beta(blockIdx.x) : 0.f;
     bool ok = true;
@@ -1293,143 +1338,198 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int n = chunk % a.NT, bh = chunk / a.NT;
     const int row0 = bh * a.T + n * kC;       // row in the [BH*T] workspace arrays
     const int crow = chunk;                   // chunk index
+    if (tid == 0 && next < total) prefetch(next);
     if (tid < kC) {
         sBeta[tid] = beta_next;                                   // read after later barriers
         if (next < total) beta_next = load_beta(next);            // in flight meanwhile
     }
     {
-        const bool got = wait_bar_warp(bar_tma, ph, 31);
-        if (got) ++kqg_waited;
+        const bool got = wait_bar_warp(bar_kqg, ph, 31);
+        if (got && tid == 0) ++kqg_waited;
         ok = ok && got;
     }
 
-    // ---- (1) cumsum: thread (c, R) owns key channel c of row block R ----
-    const int c = tid & (kD - 1), R = tid >> 7;
-    const uint32_t kbo = (c >> 6) * 8192, cc = c & 63;
-    auto ld = [&](uint32_t tile, int r) {
-        return __bfloat162float(
-            *reinterpret_cast<const __nv_bfloat16*>(smem + tile + kbo + sw128_offset(r, cc)));
-    };
-    float G[16];
+    // ---- (1) clamp the g tile in place (1024 units of 8 bf16) ----
     {
-        float acc = 0.f;
+        const __nv_bfloat162 floor2 = __floats2bfloat162_rn(kGateFloor, kGateFloor);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            acc += fmaxf(ld(I_SG, 16 * R + u), kGateFloor);   // g tile in the G area
-            G[u] = acc;
-        }
-        sGtot[R * kD + c] = acc;
-    }
-    __syncthreads();
-    float off = 0.f, Glast = 0.f;
+        for (int k4 = 0; k4 < 4; ++k4) {
+            uint4* p = reinterpret_cast<uint4*>(smem + J_G) + tid + 256 * k4;
+            uint4 v4 = *p;
+            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&v4);
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const float t = sGtot[p * kD + c];
-        if (p < R) off += t;
-        Glast += t;
-    }
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-        G[u] += off;
-        sG[(16 * R + u) * kD + c] = G[u];
-    }
-    sGb[R * kD + c] = G[0];
-    __syncthreads();
-    {
-        float Gb[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) Gb[p] = sGb[p * kD + c];
-        if (R == 3) a.gam[(size_t)crow * kD + c] = __expf(Glast);
-        // per (block, channel) factors of the build
-        sEGb[R * kD + c] = __expf(Gb[R]);               // exp(G_b)
-        sELb[R * kD + c] = __expf(Glast - Gb[R]);       // exp(G_last - G_b)
-#pragma unroll
-        for (int Rr = 0; Rr < 4; ++Rr)
-            if (Rr > R) sF[f_slot(R, Rr) * kD + c] = __expf(Gb[Rr] - Gb[R]);
-    }
-    __syncthreads();
-
-    // ---- operands: Left, Right_Rr (Rr >= R), Khat in smem; Qh, Kb to global.
-    // A unit is one 8-channel chunk (16 bytes of bf16) of one row; thread t
-    // takes chunk t % 16 of rows t / 16 and 63 - t / 16, whose blocks R and
-    // 3 - R give every thread five Right copies. ----
-    {
-        const int oct = tid & 15, kb = oct >> 3, ch = oct & 7, c0 = oct * 8;
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-            const int r = pass == 0 ? (tid >> 4) : 63 - (tid >> 4);
-            const int Rb = r >> 4, u = r & 15;
-            // rows r, 32 Rb + u and 32 Rb + 16 + u share r mod 8, hence the swizzle
-            const uint32_t co = (uint32_t)((ch ^ (r & 7)) << 4);
-            float g8[8], gb8[8], egb[8], elb[8], kv[8], qv[8], E[8], Ei[8], x[8];
-            ld8f(sG + r * kD + c0, g8);
-            ld8f(sGb + Rb * kD + c0, gb8);
-            ld8f(sEGb + Rb * kD + c0, egb);
-            ld8f(sELb + Rb * kD + c0, elb);
-            unpack8(*reinterpret_cast<const uint4*>(smem + I_K + kb * 8192 + r * 128 + co), kv);
-            unpack8(*reinterpret_cast<const uint4*>(smem + I_Q + kb * 8192 + r * 128 + co), qv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                qv[e] *= a.scale;
-                E[e] = __expf(g8[e] - gb8[e]);    // <= 1
-                Ei[e] = __expf(gb8[e] - g8[e]);   // in [1, e^75]
-            }
-            uint8_t* lk = smem + I_LEFT + kb * 16384 + (32 * Rb + u) * 128 + co;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = kv[e] * E[e];
-            *reinterpret_cast<uint4*>(lk) = pack8(x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = qv[e] * E[e];
-            *reinterpret_cast<uint4*>(lk + 16 * 128) = pack8(x);
-#pragma unroll
-            for (int Rr = 0; Rr < 4; ++Rr) {
-                if (Rr < Rb) continue;
-                float f8[8];
-                if (Rr > Rb) ld8f(sF + f_slot(Rb, Rr) * kD + c0, f8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = kv[e] * Ei[e] * (Rr > Rb ? f8[e] : 1.f);
-                // right_col(Rr) is a multiple of 8: row r keeps its swizzle
-                *reinterpret_cast<uint4*>(smem + I_R0 + kb * kRightKb +
-                                          (right_col(Rr) + r) * 128 + co) = pack8(x);
-            }
-            const size_t go = ((size_t)row0 + r) * kD + c0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) egb[e] *= E[e];                      // exp(G)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = qv[e] * egb[e];               // qs exp(G)
-            *reinterpret_cast<uint4*>(a.Q2 + go) = pack8(x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = kv[e] * elb[e] * Ei[e];       // k exp(G_last - G)
-            *reinterpret_cast<uint4*>(a.Kb2 + go) = pack8(x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = kv[e] * egb[e];               // Khat = k exp(G)
-            *reinterpret_cast<uint4*>(smem + I_KHAT + kb * 8192 + r * 128 + co) = pack8(x);
+            for (int e = 0; e < 4; ++e) h2[e] = __hmax2(h2[e], floor2);
+            *p = v4;
         }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the k, q tiles and the G area are free: the next chunk's k, q, g load now
-    if (tid == 0 && next < total) issue_kqg(next);
-
-    // ---- (2) D_R = Left Right_R^T for all R at once: N = 160 over the stacked
-    // Right operand, D_R in TMEM columns right_col(R) .. + 16(R+1) ----
+    // G_rel = Lrel . gclamp: M = 128 (rows 64-127 repeat), N = 128 channels, K = 64 rows
     if (tid == 0 && ok) {
-        const uint32_t left = smem_u32(smem + I_LEFT), right = smem_u32(smem + I_R0);
-        const uint32_t id = idesc_bf16_f32(128, 160);
+        const uint32_t id = idesc_bf16_f32(128, 128) | kBMajorMN;
+        const uint32_t l = smem_u32(smem + J_L), gt = smem_u32(smem + J_G);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(tmem, sdesc_sw128(left + (kk >> 2) * 16384 + (kk & 3) * 32),
-                     sdesc_sw128(right + (kk >> 2) * kRightKb + (kk & 3) * 32), id, kk > 0);
-        mma_commit(bar_a);
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem, sdesc_sw128(l + kk * 32), sdesc_mn_sw128(gt + kk * 2048, 8192), id,
+                     kk > 0);
+        mma_commit(bar_g);
     }
-    ok = ok && wait_bar_warp(bar_a, ph, 32);
+    ok = ok && wait_bar_warp(bar_g, ph, 35);
     tc_fence_after();
-    if (ok && warp < 8) {
+    // this thread's 32 block-relative cumsums
+    float Gr[32];
+    {
+        float x[16];
+        tmem_ld16(tmem + tlane + 16 * jq, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) Gr[e] = x[e];
+        tmem_ld16(tmem + tlane + 64 + 16 * jq, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) Gr[16 + e] = x[e];
+    }
+    // block ends and block-start gates for the per-block constants
+    if (u == 15) {
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            *reinterpret_cast<float4*>(sGend + R * kD + 16 * jq + e) =
+                make_float4(Gr[e], Gr[e + 1], Gr[e + 2], Gr[e + 3]);
+            *reinterpret_cast<float4*>(sGend + R * kD + 64 + 16 * jq + e) =
+                make_float4(Gr[16 + e], Gr[17 + e], Gr[18 + e], Gr[19 + e]);
+        }
+    } else if (u == 0) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float x[8];
+                unpack8(*reinterpret_cast<const uint4*>(smem + J_G + hh * 8192 +
+                                                        sw128_offset(r, 16 * jq + 8 * e)),
+                        x);
+                float* dst = sG0 + R * kD + 64 * hh + 16 * jq + 8 * e;
+                *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // per (block, channel) constants: thread (c, part) with c = tid % 128
+    {
+        const int c = tid & (kD - 1);
+        float gb[4];
+        gb[0] = sG0[c];
+#pragma unroll
+        for (int p = 1; p < 4; ++p) gb[p] = gb[p - 1] + sGend[(p - 1) * kD + c] + sG0[p * kD + c];
+        const float glast = gb[3] + sGend[3 * kD + c];
+        if (tid < kD) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                sEGb[p * kD + c] = __expf(gb[p]);
+                sELb[p * kD + c] = __expf(glast - gb[p]);
+            }
+            a.gam[(size_t)crow * kD + c] = __expf(glast);
+        } else {
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int pr = p + 1; pr < 4; ++pr) sF[f_slot(p, pr) * kD + c] = __expf(gb[pr] - gb[p]);
+        }
+    }
+    __syncthreads();
+
+    // ---- operands, in two 64-channel halves through one Left/Right buffer:
+    // Left (k E, q E), Right_Rr (Rr >= R), Khat into the g area, Qh and Kb in
+    // place over the q and k tiles ----
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        if (hh == 1) {
+            // the first half's product has read the Left/Right buffer
+            ok = ok && wait_bar_warp(bar_a0, ph, 36);
+            tc_fence_after();
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int o = 2 * jq + e;                 // 8-channel unit within the half
+            const int c0 = 64 * hh + 8 * o;           // first channel
+            const uint32_t tile_off = hh * 8192 + sw128_offset(r, 8 * o);
+            float kv[8], qv[8], egb[8], elb[8], E[8], Ei[8], x[8];
+            unpack8(*reinterpret_cast<const uint4*>(smem + J_K + tile_off), kv);
+            unpack8(*reinterpret_cast<const uint4*>(smem + J_Q + tile_off), qv);
+            ld8f(sEGb + R * kD + c0, egb);
+            ld8f(sELb + R * kD + c0, elb);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float gr = Gr[16 * hh + 8 * e + i];
+                E[i] = __expf(gr);       // exp(G - G_b) <= 1
+                Ei[i] = __expf(-gr);     // exp(G_b - G) in [1, e^75]
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = kv[i] * E[i];
+            *reinterpret_cast<uint4*>(smem + J_LR + sw128_offset(32 * R + u, 8 * o)) = pack8(x);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = qv[i] * E[i];
+            *reinterpret_cast<uint4*>(smem + J_LR + sw128_offset(32 * R + 16 + u, 8 * o)) = pack8(x);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) Ei[i] *= kv[i];                       // k exp(G_b - G)
+            *reinterpret_cast<uint4*>(smem + J_RIGHT + sw128_offset(right_col(R) + r, 8 * o)) =
+                pack8(Ei);
+#pragma unroll
+            for (int Rr = 1; Rr < 4; ++Rr) {
+                if (Rr <= R) continue;
+                float f8[8];
+                ld8f(sF + f_slot(R, Rr) * kD + c0, f8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = Ei[i] * f8[i];
+                *reinterpret_cast<uint4*>(smem + J_RIGHT + sw128_offset(right_col(Rr) + r, 8 * o)) =
+                    pack8(x);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = kv[i] * E[i] * egb[i];          // Khat = k exp(G)
+            *reinterpret_cast<uint4*>(smem + J_G + tile_off) = pack8(x);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = qv[i] * E[i] * egb[i] * a.scale;  // Qh
+            *reinterpret_cast<uint4*>(smem + J_Q + tile_off) = pack8(x);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = Ei[i] * elb[i];                 // Kb = k exp(G_last - G)
+            *reinterpret_cast<uint4*>(smem + J_K + tile_off) = pack8(x);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0 && ok) {
+            // D (+)= Left_h Right_h^T over this half's 64 channels, N = 160
+            const uint32_t left = smem_u32(smem + J_LR), right = smem_u32(smem + J_RIGHT);
+            const uint32_t id = idesc_bf16_f32(128, 160);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem, sdesc_sw128(left + kk * 32), sdesc_sw128(right + kk * 32), id,
+                         (hh > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(hh == 0 ? bar_a0 : bar_a1);
+            if (hh == 1) {
+                // Qh and Kb are complete: out by TMA
+                tma_store_2d(&tm_q2, smem + J_Q, 0, row0);
+                tma_store_2d(&tm_q2, smem + J_Q + 8192, 64, row0);
+                tma_store_2d(&tm_kb2, smem + J_K, 0, row0);
+                tma_store_2d(&tm_kb2, smem + J_K + 8192, 64, row0);
+                bulk_commit_group();
+            }
+        }
+    }
+    ok = ok && wait_bar_warp(bar_a1, ph, 32);
+    tc_fence_after();
+    if (tid == 0) {
+        // the Qh and Kb stores have read their tiles: the v tile loads into
+        // the q area, and the k area takes the Aqk staging tile
+        bulk_wait_read_all();
+        if (ok) issue_v(chunk);
+    }
+    __syncthreads();
+    if (ok) {
         // warps R and R + 4 read block R (TMEM quadrant R); lanes 0-15 of warp R
-        // write its A rows, lanes 16-31 of warp R + 4 its Aqk rows, so that no
-        // warp runs both branches
+        // write its A rows, lanes 16-31 of warp R + 4 its Aqk rows
         const int Rq = warp & 3;
         float d[64];
         const uint32_t taddr = tmem + ((uint32_t)(Rq * 32) << 16) + right_col(Rq);
@@ -1437,7 +1537,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         else if (Rq == 1) intra_read_block<1>(taddr, d);
         else if (Rq == 2) intra_read_block<2>(taddr, d);
         else intra_read_block<3>(taddr, d);
-        const int u = lane & 15, i = 16 * Rq + u;
+        const int uu = lane & 15, i = 16 * Rq + uu;
         if (warp < 4 && lane < 16) {
             const float bi = sBeta[i];
 #pragma unroll
@@ -1446,19 +1546,23 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     make_float4(j < i ? bi * d[j] : 0.f, j + 1 < i ? bi * d[j + 1] : 0.f,
                                 j + 2 < i ? bi * d[j + 2] : 0.f, j + 3 < i ? bi * d[j + 3] : 0.f);
         } else if (warp >= 4 && lane >= 16) {
-            __nv_bfloat16* ap = a.Aqk2 + ((size_t)crow * kC + i) * kC;
 #pragma unroll
             for (int j = 0; j < kC; j += 8) {
-                uint4 pk;
-                pk.x = pack_bf16(j + 0 <= i ? d[j + 0] : 0.f, j + 1 <= i ? d[j + 1] : 0.f);
-                pk.y = pack_bf16(j + 2 <= i ? d[j + 2] : 0.f, j + 3 <= i ? d[j + 3] : 0.f);
-                pk.z = pack_bf16(j + 4 <= i ? d[j + 4] : 0.f, j + 5 <= i ? d[j + 5] : 0.f);
-                pk.w = pack_bf16(j + 6 <= i ? d[j + 6] : 0.f, j + 7 <= i ? d[j + 7] : 0.f);
-                *reinterpret_cast<uint4*>(ap + j) = pk;
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = (j + e <= i) ? a.scale * d[j + e] : 0.f;
+                *reinterpret_cast<uint4*>(smem + J_K + sw128_offset(i, j)) = pack8(x);
             }
         }
     }
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && ok) {
+        tma_store_2d(&tm_aqk2, smem + J_K, 0, crow * kC);
+        bulk_commit_group();
+    }
 
     // ---- (3) T = (I + A)^{-1}, A strictly lower, in three levels: the four
     // 16 x 16 diagonal blocks by forward substitution (thread (B, jj) keeps
@@ -1489,72 +1593,79 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         for (int m = 0; m < 16; ++m) sT[(o + m) * kAS + o + jj] = t[m];
     }
     __syncthreads();
-    // 32-level, thread (RB, i, j) of all 512: Y = A_ba T_a into A's unused
-    // block above the diagonal (rows o + i, columns o + 16 + j); T's blocks
-    // above the diagonal (that one, and T_01) are zero
+    // 32-level, thread (i, j) for both diagonal 32-blocks RB: Y = A_ba T_a into
+    // A's unused block above the diagonal (rows o + i, columns o + 16 + j);
+    // T's blocks above the diagonal (that one, and T_01) are zero
     {
-        const int RB = tid >> 8, i = (tid >> 4) & 15, j = tid & 15, o = 32 * RB;
-        const float* arow = sA + (o + 16 + i) * kAS + o;
-        float y0 = 0.f, y1 = 0.f;
+        const int i = tid >> 4, j = tid & 15;
 #pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(arow + m);
-            y0 = fmaf(a4.x, sT[(o + m) * kAS + o + j], y0);
-            y1 = fmaf(a4.y, sT[(o + m + 1) * kAS + o + j], y1);
-            y0 = fmaf(a4.z, sT[(o + m + 2) * kAS + o + j], y0);
-            y1 = fmaf(a4.w, sT[(o + m + 3) * kAS + o + j], y1);
+        for (int RB = 0; RB < 2; ++RB) {
+            const int o = 32 * RB;
+            const float* arow = sA + (o + 16 + i) * kAS + o;
+            float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(arow + m);
+                y0 = fmaf(a4.x, sT[(o + m) * kAS + o + j], y0);
+                y1 = fmaf(a4.y, sT[(o + m + 1) * kAS + o + j], y1);
+                y0 = fmaf(a4.z, sT[(o + m + 2) * kAS + o + j], y0);
+                y1 = fmaf(a4.w, sT[(o + m + 3) * kAS + o + j], y1);
+            }
+            sA[(o + i) * kAS + o + 16 + j] = y0 + y1;
+            sT[(o + i) * kAS + o + 16 + j] = 0.f;
         }
-        sA[(o + i) * kAS + o + 16 + j] = y0 + y1;
-        sT[(o + i) * kAS + o + 16 + j] = 0.f;
-        sT[(tid >> 5) * kAS + 32 + (tid & 31)] = 0.f;   // T_01, rows 0..15
-        sT[(16 + (tid >> 5)) * kAS + 32 + (tid & 31)] = 0.f;   // rows 16..31
+#pragma unroll
+        for (int rr = 0; rr < 32; rr += 8)   // T_01, rows 0..31, columns 32..63
+            sT[(rr + (tid >> 5)) * kAS + 32 + (tid & 31)] = 0.f;
     }
     __syncthreads();
     // T_ba = -T_b Y
     {
-        const int RB = tid >> 8, i = (tid >> 4) & 15, j = tid & 15, o = 32 * RB;
-        const float* trow = sT + (o + 16 + i) * kAS + o + 16;
-        float y0 = 0.f, y1 = 0.f;
+        const int i = tid >> 4, j = tid & 15;
 #pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-            const float4 t4 = *reinterpret_cast<const float4*>(trow + m);
-            y0 = fmaf(t4.x, sA[(o + m) * kAS + o + 16 + j], y0);
-            y1 = fmaf(t4.y, sA[(o + m + 1) * kAS + o + 16 + j], y1);
-            y0 = fmaf(t4.z, sA[(o + m + 2) * kAS + o + 16 + j], y0);
-            y1 = fmaf(t4.w, sA[(o + m + 3) * kAS + o + 16 + j], y1);
+        for (int RB = 0; RB < 2; ++RB) {
+            const int o = 32 * RB;
+            const float* trow = sT + (o + 16 + i) * kAS + o + 16;
+            float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m += 4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(trow + m);
+                y0 = fmaf(t4.x, sA[(o + m) * kAS + o + 16 + j], y0);
+                y1 = fmaf(t4.y, sA[(o + m + 1) * kAS + o + 16 + j], y1);
+                y0 = fmaf(t4.z, sA[(o + m + 2) * kAS + o + 16 + j], y0);
+                y1 = fmaf(t4.w, sA[(o + m + 3) * kAS + o + 16 + j], y1);
+            }
+            sT[(o + 16 + i) * kAS + o + j] = -(y0 + y1);
         }
-        sT[(o + 16 + i) * kAS + o + j] = -(y0 + y1);
     }
     __syncthreads();
-    // The two 32 x 32 x 32 products below: the first 256 threads, thread
-    // (rp, cp) owning rows 2rp, 2rp + 1 and columns 2cp, 2cp + 1 of C =
-    // sign A B (row stride kAS everywhere).  Per four k: two float4 loads of
-    // A rows (shared by a half-warp) and four float2 loads of B (shared by the
-    // two half-warps) feed 16 FMAs.
+    // The two 32 x 32 x 32 products below: thread (rp, cp) owns rows 2rp,
+    // 2rp + 1 and columns 2cp, 2cp + 1 of C = sign A B (row stride kAS
+    // everywhere).  Per four k: two float4 loads of A rows (shared by a
+    // half-warp) and four float2 loads of B (shared by the two half-warps)
+    // feed 16 FMAs.
     auto mm32 = [&](const float* A, const float* B, float* C, float sign) {
-        if (tid < 256) {
-            const int rp = 2 * warp + (lane >> 4), cp = lane & 15;
-            const int i0 = 2 * rp, j0 = 2 * cp;
-            const float* a0 = A + i0 * kAS;
-            const float* a1 = a0 + kAS;
-            float c00 = 0.f, c01 = 0.f, c10 = 0.f, c11 = 0.f;
+        const int rp = 2 * warp + (lane >> 4), cp = lane & 15;
+        const int i0 = 2 * rp, j0 = 2 * cp;
+        const float* a0 = A + i0 * kAS;
+        const float* a1 = a0 + kAS;
+        float c00 = 0.f, c01 = 0.f, c10 = 0.f, c11 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 32; m += 4) {
-                const float4 p = *reinterpret_cast<const float4*>(a0 + m);
-                const float4 q = *reinterpret_cast<const float4*>(a1 + m);
-                const float pa[4] = {p.x, p.y, p.z, p.w}, qa[4] = {q.x, q.y, q.z, q.w};
+        for (int m = 0; m < 32; m += 4) {
+            const float4 p = *reinterpret_cast<const float4*>(a0 + m);
+            const float4 q = *reinterpret_cast<const float4*>(a1 + m);
+            const float pa[4] = {p.x, p.y, p.z, p.w}, qa[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 bv = *reinterpret_cast<const float2*>(B + (m + e) * kAS + j0);
-                    c00 = fmaf(pa[e], bv.x, c00);
-                    c01 = fmaf(pa[e], bv.y, c01);
-                    c10 = fmaf(qa[e], bv.x, c10);
-                    c11 = fmaf(qa[e], bv.y, c11);
-                }
+            for (int e = 0; e < 4; ++e) {
+                const float2 bv = *reinterpret_cast<const float2*>(B + (m + e) * kAS + j0);
+                c00 = fmaf(pa[e], bv.x, c00);
+                c01 = fmaf(pa[e], bv.y, c01);
+                c10 = fmaf(qa[e], bv.x, c10);
+                c11 = fmaf(qa[e], bv.y, c11);
             }
-            *reinterpret_cast<float2*>(C + i0 * kAS + j0) = make_float2(sign * c00, sign * c01);
-            *reinterpret_cast<float2*>(C + (i0 + 1) * kAS + j0) = make_float2(sign * c10, sign * c11);
         }
+        *reinterpret_cast<float2*>(C + i0 * kAS + j0) = make_float2(sign * c00, sign * c01);
+        *reinterpret_cast<float2*>(C + (i0 + 1) * kAS + j0) = make_float2(sign * c10, sign * c11);
     };
     // X = A_10 T_00 into A's unused upper block (rows 0..31, columns 32..63)
     mm32(sA + 32 * kAS, sT, sA + 32, 1.f);
@@ -1562,69 +1673,104 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     // T_10 = -T_11 X
     mm32(sT + 32 * kAS + 32, sA + 32, sT + 32 * kAS, -1.f);
     __syncthreads();
-    // T (bf16 high and low parts) to global; T*beta to the B-operand tile.
-    // Thread t takes columns 8 (t % 8) .. + 7 of row t / 8.
-    {
-        const int i = tid >> 3, ch = tid & 7, j0 = ch * 8;
+    // T (bf16 high and low parts) to global when kept; T*beta, twice, to the
+    // A operand of the W and U products (over A, whose last reader was the
+    // product above).  Thread t takes columns 8 (t % 8) .. + 7 of rows t / 8
+    // and t / 8 + 32.
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int i = (tid >> 3) + 32 * half, ch = tid & 7, j0 = ch * 8;
         float t8[8], b8[8], x[8];
         ld8f(sT + i * kAS + j0, t8);
         ld8f(sBeta + j0, b8);
-        const uint4 hi = pack8(t8);
-        unpack8(hi, x);
+        if (a.T2) {
+            const uint4 hi = pack8(t8);
+            unpack8(hi, x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = t8[e] - x[e];
-        const size_t go = (size_t)crow * kC * kC + (size_t)i * kC + j0;
-        *reinterpret_cast<uint4*>(a.T2 + go) = hi;
-        *reinterpret_cast<uint4*>(a.Tlo + go) = pack8(x);
+            for (int e = 0; e < 8; ++e) x[e] = t8[e] - x[e];
+            const size_t go = (size_t)crow * kC * kC + (size_t)i * kC + j0;
+            *reinterpret_cast<uint4*>(a.T2 + go) = hi;
+            *reinterpret_cast<uint4*>(a.Tlo + go) = pack8(x);
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = t8[e] * b8[e];
-        *reinterpret_cast<uint4*>(smem + I_TB + i * 128 + ((ch ^ (i & 7)) << 4)) = pack8(x);
+        const uint4 pk = pack8(x);
+        *reinterpret_cast<uint4*>(smem + J_TB + sw128_offset(i, j0)) = pk;
+        *reinterpret_cast<uint4*>(smem + J_TB + sw128_offset(64 + i, j0)) = pk;
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // W = (T beta) Khat into TMEM columns 0..127, U = (T beta) V into 128..255
+    // (rows t in lanes 0..63, repeated in 64..127)
     if (tid == 0 && ok && wait_bar(bar_v, ph, 34)) {
         ++v_waited;
         tc_fence_after();
-        const uint32_t id = idesc_bf16_f32(128, 64) | kAMajorMN;
-        const uint32_t kh = smem_u32(smem + I_KHAT), vt = smem_u32(smem + I_V);
-        const uint32_t tb = smem_u32(smem + I_TB);
+        const uint32_t id = idesc_bf16_f32(128, 128) | kBMajorMN;
+        const uint32_t tb = smem_u32(smem + J_TB), kh = smem_u32(smem + J_G),
+                       vt = smem_u32(smem + J_Q);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            mma_bf16(tmem + 0, sdesc_mn_sw128(kh + kk * 2048, 8192), sdesc_sw128(tb + kk * 32), id,
+            mma_bf16(tmem + 0, sdesc_sw128(tb + kk * 32), sdesc_mn_sw128(kh + kk * 2048, 8192), id,
                      kk > 0);
-            mma_bf16(tmem + 64, sdesc_mn_sw128(vt + kk * 2048, 8192), sdesc_sw128(tb + kk * 32), id,
-                     kk > 0);
+            mma_bf16(tmem + 128, sdesc_sw128(tb + kk * 32), sdesc_mn_sw128(vt + kk * 2048, 8192),
+                     id, kk > 0);
         }
         mma_commit(bar_w);
     }
     ok = ok && wait_bar_warp(bar_w, ph, 33);
-    // the v tile is free: the next chunk's v loads now
-    if (tid == 0 && next < total) issue_v(next);
     tc_fence_after();
     if (ok) {
-        // W^T (lane = k, TMEM columns 0..63) and U^T (lane = v, 64..127): warp w
-        // takes lane quadrant w % 4 of W (w / 4 even) or U, rows 32 (w / 8) + 0..31
-        float r[32];
-        const int q4 = warp & 3, isU = (warp >> 2) & 1, cb = warp >> 3;
-        const int l = q4 * 32 + lane;
-        tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + isU * 64 + cb * 32, r);
-        __nv_bfloat16* dst = isU ? a.U2 : a.W2;
+        // quadrants 0, 1 read W rows into the g area (Khat's last reader was
+        // the product), quadrants 2, 3 U rows into the q area (v's); warp
+        // w / 4 takes the 64-column half
+        const int isU = qd >> 1, cb = warp >> 2;
+        float x0[32], x1[32];
+        const uint32_t src = tmem + tlane + isU * 128 + cb * 64;
+        tmem_ld32_nw(src, x0);
+        tmem_ld32_nw(src + 32, x1);
+        tmem_wait_ld_dep(x0);
+        tmem_wait_ld_dep(x1);
+        uint8_t* box = smem + (isU ? J_Q : J_G) + cb * 8192;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            dst[((size_t)row0 + cb * 32 + j) * kD + l] = __float2bfloat16_rn(r[j]);
+        for (int j = 0; j < 4; ++j) {
+            float e0[8], e1[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                e0[i] = x0[8 * j + i];
+                e1[i] = x1[8 * j + i];
+            }
+            *reinterpret_cast<uint4*>(box + sw128_offset(r, 8 * j)) = pack8(e0);
+            *reinterpret_cast<uint4*>(box + sw128_offset(r, 32 + 8 * j)) = pack8(e1);
+        }
     }
+    fence_async_smem();
     tc_fence_before();
     const bool all_ok = __syncthreads_and(ok);
     tc_fence_after();
+    if (tid == 0 && all_ok) {
+        tma_store_2d(&tm_w2, smem + J_G, 0, row0);
+        tma_store_2d(&tm_w2, smem + J_G + 8192, 64, row0);
+        tma_store_2d(&tm_u2, smem + J_Q, 0, row0);
+        tma_store_2d(&tm_u2, smem + J_Q + 8192, 64, row0);
+        bulk_commit_group();
+        // the tiles (and the Aqk staging tile) are read before the next
+        // chunk's loads overwrite them
+        bulk_wait_read_all();
+        if (next < total) issue_kqg(next);
+    }
     if (!all_ok) break;
     }  // chunk loop
     // loads issued for chunks the loop did not reach (after an error) land
-    // before shared memory is released
+    // before shared memory is released, and every store has completed
     if (tid == 0) {
-        for (; kqg_waited < kqg_issued; ++kqg_waited) wait_bar_drain(bar_tma, kqg_waited & 1);
+        for (; kqg_waited < kqg_issued; ++kqg_waited) wait_bar_drain(bar_kqg, kqg_waited & 1);
         for (; v_waited < v_issued; ++v_waited) wait_bar_drain(bar_v, v_waited & 1);
+        bulk_wait_all();
+        // every issued product completes before TMEM is released
+        mma_commit(bar_fin);
+        wait_bar_drain(bar_fin, 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -2360,18 +2506,26 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     return off;
 }
 
-// Intra-chunk quantities on tensor cores, written straight into the operand
-// arrays (and T, gam into the fp32 workspace arrays the backward tail reads).
+// Intra-chunk quantities on tensor cores, stored by TMA into the operand
+// arrays (and gam, and T when kept, into the arrays the backward reads).
+// keep_T: also write T as bf16 high and low parts (the backward needs them;
+// the plain forward does not).
 kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const void* k,
-                        const void* v, const void* g, const void* beta, cudaStream_t s,
-                        float** gam_out) {
+                        const void* v, const void* g, const void* beta, bool keep_T,
+                        cudaStream_t s, float** gam_out) {
     SimtWsPtrs p;
     simt_ws_ptrs(d, 0, w.simt, &p);
     const int BH = d.B * d.HV, NT = d.T / kC;
     const uint64_t BT = (uint64_t)d.B * d.T;
-    CUtensorMap mk, mq, mg, mv;
+    const uint64_t rows = (uint64_t)BH * d.T;
+    CUtensorMap mk, mq, mg, mv, mw2, mq2, mu2, mkb2, ma2;
     if (!make_map_tok(&mk, k, BT, d.H) || !make_map_tok(&mq, q, BT, d.H) ||
-        !make_map_tok(&mg, g, BT, d.HV) || !make_map_tok(&mv, v, BT, d.HV))
+        !make_map_tok(&mg, g, BT, d.HV) || !make_map_tok(&mv, v, BT, d.HV) ||
+        !make_map(&mw2, w.W2, rows, kD, 64, 64, true) ||
+        !make_map(&mq2, w.Q2, rows, kD, 64, 64, true) ||
+        !make_map(&mu2, w.U2, rows, kD, 64, 64, true) ||
+        !make_map(&mkb2, w.Kb2, rows, kD, 64, 64, true) ||
+        !make_map(&ma2, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
         return KDA_ERR_CUDA;
     IntraArgs a;
     a.T = d.T;
@@ -2381,22 +2535,18 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     a.BH = BH;
     a.scale = d.scale;
     a.beta = static_cast<const __nv_bfloat16*>(beta);
-    a.W2 = w.W2;
-    a.Q2 = w.Q2;
-    a.U2 = w.U2;
-    a.Kb2 = w.Kb2;
-    a.Aqk2 = w.Aqk2;
-    a.T2 = w.T2;
-    a.Tlo = w.Tlo2;
+    a.T2 = keep_T ? w.T2 : nullptr;
+    a.Tlo = keep_T ? w.Tlo2 : nullptr;
     a.gam = p.gam;
     if (cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)INTRA_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
     {
         TimedLaunch tl("tc_intra", s);
-        // persistent: one CTA per SM walks the chunks
-        const int grid = std::min(BH * NT, sm_count());
-        intra_tc_kernel<<<grid, kIntraThreads, INTRA_SMEM, s>>>(mk, mq, mg, mv, a);
+        // persistent: two CTAs per SM walk the chunks
+        const int grid = std::min(BH * NT, 2 * sm_count());
+        intra_tc_kernel<<<grid, kIntraThreads, INTRA_SMEM, s>>>(mk, mq, mg, mv, mw2, mq2, mu2,
+                                                                 mkb2, ma2, a);
     }
     *gam_out = p.gam;
     return launch_status();
@@ -2516,7 +2666,7 @@ kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v
     TcWs w;
     tc_carve(d, save ? 1 : 0, static_cast<char*>(ws), &w);
     float* gam = nullptr;
-    kda_status st = run_intra_tc(d, w, q, k, v, g, beta, s, &gam);
+    kda_status st = run_intra_tc(d, w, q, k, v, g, beta, save, s, &gam);
     if (st != KDA_OK) return st;
     return run_chain_fwd(d, w, gam, h0, o, ht, save ? w.h2 : nullptr, save ? w.d2 : nullptr, s);
 }
@@ -2534,7 +2684,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         simt_ws_ptrs(d, 0, w.simt, &p0);  // where the intra kernel left gam
         gam = p0.gam;
     } else {
-        if ((st = run_intra_tc(d, w, q, k, v, g, beta, s, &gam)) != KDA_OK) return st;
+        if ((st = run_intra_tc(d, w, q, k, v, g, beta, true, s, &gam)) != KDA_OK) return st;
         // forward recompute: chunk-start states and delta
         if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s)) != KDA_OK)
             return st;
