@@ -49,9 +49,10 @@ struct SimtWsPtrs {
     float *hs, *dhs, *ddl, *dQh, *dWm, *dKb, *dgam, *dAqk, *dTv, *dbv, *dqh, *dkh;
 };
 void simt_ws_ptrs(const kda_dims& d, int for_bwd, void* ws, SimtWsPtrs* out);
-// GVA reduction: dq[b,t,h] = sum over the value heads of group h of dqh (fp32).
-kda_status group_sum_launch(const kda_dims& d, const float* dqh, const float* dkh, void* dq,
-                            void* dk, cudaStream_t s);
+// GVA reduction: dq[b,t,h] = sum over the value heads of group h of dqh (fp32);
+// with d.qk_l2norm, then mapped from the normalised to the raw q (k, alike).
+kda_status group_sum_launch(const kda_dims& d, const float* dqh, const float* dkh,
+                            const void* q, const void* k, void* dq, void* dk, cudaStream_t s);
 kda_status simt_fwd(const kda_dims& d, const void* q, const void* k, const void* v,
                     const void* g, const void* beta, const float* h0, void* o, float* ht,
                     void* ws, cudaStream_t s);

@@ -19,9 +19,12 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 
+constexpr float kNormEps = 1e-12f;
+
 // Fast path: K, V multiples of 4 with (V/4) threads per row.  Each thread
-// owns 4 consecutive columns of ROWS rows.
-template <typename Tin, int K, int V>
+// owns 4 consecutive columns of ROWS rows.  QKN: q and k are L2-normalised
+// over K first (x / max(|x|, 1e-12)).
+template <typename Tin, int K, int V, bool QKN>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* __restrict__ k,
               const Tin* __restrict__ v, const Tin* __restrict__ g,
@@ -35,6 +38,7 @@ decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* 
     __shared__ float s_red[2][RP][V];
     __shared__ float s_e[V];
     __shared__ float s_kq[K / 32];
+    __shared__ float s_nk[K / 32], s_nq[K / 32];
 
     const int bh = blockIdx.x;
     const int b = bh / HV, hv = bh % HV, h = hv / (HV / H);
@@ -48,10 +52,40 @@ decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* 
     for (int i = 0; i < ROWS; ++i) s[i] = __ldcs(S4 + (size_t)(row0 + i * RP) * TPR + col4);
 
     const size_t qk_off = ((size_t)b * H + h) * K;
+    float kk = 0.f, qq = 0.f;
+    if (QKN) {
+        if (tid < K) {
+            kk = to_f(k[qk_off + tid]);
+            qq = to_f(q[qk_off + tid]);
+            float nk = kk * kk, nq = qq * qq;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                nk += __shfl_xor_sync(0xffffffffu, nk, off);
+                nq += __shfl_xor_sync(0xffffffffu, nq, off);
+            }
+            if ((tid & 31) == 0) {
+                s_nk[tid >> 5] = nk;
+                s_nq[tid >> 5] = nq;
+            }
+        }
+        __syncthreads();
+        if (tid < K) {
+            float nk = 0.f, nq = 0.f;
+#pragma unroll
+            for (int w = 0; w < K / 32; ++w) {
+                nk += s_nk[w];
+                nq += s_nq[w];
+            }
+            kk *= 1.f / fmaxf(sqrtf(nk), kNormEps);
+            qq *= scale / fmaxf(sqrtf(nq), kNormEps);
+        }
+    }
     if (tid < K) {  // K is a multiple of 32: these warps are fully active
         const float a = __expf(fmaxf(to_f(g[(size_t)bh * K + tid]), kGateFloor));
-        const float kk = to_f(k[qk_off + tid]);
-        const float qq = scale * to_f(q[qk_off + tid]);
+        if (!QKN) {
+            kk = to_f(k[qk_off + tid]);
+            qq = scale * to_f(q[qk_off + tid]);
+        }
         s_a[tid] = a;
         s_k[tid] = kk;
         s_ka[tid] = a * kk;
@@ -109,7 +143,7 @@ decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* 
 // Any K, V <= 128: one thread per value column, two passes over the state.
 template <typename Tin>
 __global__ void __launch_bounds__(128)
-decode_kernel_generic(int H, int HV, int K, int V, float scale, const Tin* __restrict__ q,
+decode_kernel_generic(int H, int HV, int K, int V, float scale, int qkn, const Tin* __restrict__ q,
                       const Tin* __restrict__ k, const Tin* __restrict__ v,
                       const Tin* __restrict__ g, const Tin* __restrict__ beta,
                       float* __restrict__ state, Tin* __restrict__ o) {
@@ -124,6 +158,16 @@ decode_kernel_generic(int H, int HV, int K, int V, float scale, const Tin* __res
         s_q[c] = scale * to_f(q[qk_off + c]);
     }
     __syncthreads();
+    float ik = 1.f, iq = 1.f;   // with qkn: the inverse norms of k and q
+    if (qkn) {
+        float nk = 0.f, nq = 0.f;
+        for (int c = 0; c < K; ++c) {
+            nk = fmaf(s_k[c], s_k[c], nk);
+            nq = fmaf(s_q[c], s_q[c], nq);
+        }
+        ik = 1.f / fmaxf(sqrtf(nk), kNormEps);
+        iq = 1.f / fmaxf(sqrtf(nq) / scale, kNormEps);
+    }
     if (j >= V) return;
     float* S = state + (size_t)bh * K * V;
     float sk = 0.f, sq = 0.f, kq = 0.f;
@@ -133,12 +177,15 @@ decode_kernel_generic(int H, int HV, int K, int V, float scale, const Tin* __res
         sq += s_q[c] * sv;
         kq += s_k[c] * s_q[c];
     }
+    sk *= ik;
+    sq *= iq;
+    kq *= ik * iq;
     const float bt = to_f(beta[bh]);
     const float e = to_f(v[(size_t)bh * V + j]) - sk;
     o[(size_t)bh * V + j] = from_f<Tin>(sq + bt * kq * e);
     for (int c = 0; c < K; ++c) {
         float* p = S + (size_t)c * V + j;
-        *p = s_a[c] * *p + bt * s_k[c] * e;
+        *p = s_a[c] * *p + bt * (ik * s_k[c]) * e;
     }
 }
 
@@ -154,15 +201,24 @@ kda_status decode_dispatch(const kda_dims& d, const void* q, const void* k, cons
     auto* bb = static_cast<const Tin*>(beta);
     auto* oo = static_cast<Tin*>(o);
     TimedLaunch tl("decode_step", s);
+    const bool qkn = d.qk_l2norm != 0;
     if (d.K == 128 && d.V == 128) {
-        decode_kernel<Tin, 128, 128><<<nb, kDecodeThreads, 0, s>>>(d.H, d.HV, d.scale, qq, kk, vv,
-                                                                   gg, bb, state, oo);
+        if (qkn)
+            decode_kernel<Tin, 128, 128, true><<<nb, kDecodeThreads, 0, s>>>(
+                d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
+        else
+            decode_kernel<Tin, 128, 128, false><<<nb, kDecodeThreads, 0, s>>>(
+                d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
     } else if (d.K == 64 && d.V == 64) {
-        decode_kernel<Tin, 64, 64><<<nb, kDecodeThreads, 0, s>>>(d.H, d.HV, d.scale, qq, kk, vv,
-                                                                 gg, bb, state, oo);
+        if (qkn)
+            decode_kernel<Tin, 64, 64, true><<<nb, kDecodeThreads, 0, s>>>(
+                d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
+        else
+            decode_kernel<Tin, 64, 64, false><<<nb, kDecodeThreads, 0, s>>>(
+                d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
     } else {
-        decode_kernel_generic<Tin><<<nb, 128, 0, s>>>(d.H, d.HV, d.K, d.V, d.scale, qq, kk, vv,
-                                                      gg, bb, state, oo);
+        decode_kernel_generic<Tin><<<nb, 128, 0, s>>>(d.H, d.HV, d.K, d.V, d.scale, qkn ? 1 : 0,
+                                                      qq, kk, vv, gg, bb, state, oo);
     }
     return launch_status();
 }

@@ -51,12 +51,14 @@ struct Ws {
 struct Dims {
     int B, T, H, HV, K, V, C, NT, G;
     float scale;
+    int qkn;   // L2-normalise q and k over K inside the kernels
 };
 
 Dims make_dims(const kda_dims& d) {
     Dims r;
     r.B = d.B; r.T = d.T; r.H = d.H; r.HV = d.HV; r.K = d.K; r.V = d.V;
     r.C = d.chunk_size; r.NT = d.T / d.chunk_size; r.G = d.HV / d.H; r.scale = d.scale;
+    r.qkn = d.qk_l2norm != 0;
     return r;
 }
 
@@ -101,6 +103,36 @@ __device__ __forceinline__ size_t tok_idx(const Dims& d, int b, int t, int head,
     return (((size_t)b * d.T + t) * nheads + head) * width;
 }
 
+// L2 normalisation of q and k rows in place: kS holds k, qS holds scale * q
+// (C rows of K floats, row stride KP).  Afterwards kS holds k / max(|k|, eps)
+// and qS holds scale * q / max(|q|, eps).  One warp per row.
+constexpr float kNormEps = 1e-12f;
+
+__device__ __forceinline__ void l2norm_rows(float* kS, float* qS, int C, int K, int KP,
+                                            float scale) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int r = warp; r < C; r += kThreads / 32) {
+        float sk = 0.f, sq = 0.f;
+        for (int c = lane; c < K; c += 32) {
+            const float kv = kS[r * KP + c], qv = qS[r * KP + c];
+            sk = fmaf(kv, kv, sk);
+            sq = fmaf(qv, qv, sq);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sk += __shfl_xor_sync(0xffffffffu, sk, off);
+            sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        }
+        // |q| = |scale q| / scale
+        const float ik = 1.f / fmaxf(sqrtf(sk), kNormEps);
+        const float iq = 1.f / fmaxf(sqrtf(sq) / scale, kNormEps);
+        for (int c = lane; c < K; c += 32) {
+            kS[r * KP + c] *= ik;
+            qS[r * KP + c] *= iq;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // intra: per (chunk, head)
 // smem: k[C][K+1], qs[C][K+1], G[C][K+1], A[C][C+1], Tm[C][C+1], beta[C]
@@ -136,6 +168,10 @@ intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     }
     for (int r = tid; r < C; r += kThreads) bS[r] = to_f(beta[((size_t)b * d.T + t0 + r) * d.HV + hv]);
     __syncthreads();
+    if (d.qkn) {
+        l2norm_rows(kS, qS, C, K, KP, d.scale);
+        __syncthreads();
+    }
     for (int c = tid; c < K; c += kThreads) {  // (1) in-chunk cumsum
         float acc = 0.f;
         for (int r = 0; r < C; ++r) {
@@ -562,6 +598,10 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
         dbS[r] = w.dbv[row0 + r];
     }
     __syncthreads();
+    if (d.qkn) {
+        l2norm_rows(kS, qS, C, K, KP, d.scale);
+        __syncthreads();
+    }
     for (int c = tid; c < K; c += kThreads) {
         float acc = 0.f;
         for (int r = 0; r < C; ++r) {
@@ -802,26 +842,78 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     }
 }
 
-// dq[b,t,h,:] = sum over the G value heads of the group; cast to the dtype.
+// dq[b,t,h,:] = sum over the G value heads of the group (and the same for
+// dk); with qkn, the sum is the gradient with respect to the normalised q
+// (k), and the row is mapped back to the raw q (k):
+//     dx = (dn - n <n, dn>) / max(|x|, eps),   n = x / max(|x|, eps).
+// One warp per (b, t, h) row, K <= 128 (four channels per lane); cast to the dtype.
 template <typename Tin>
 __global__ void group_sum_kernel(Dims d, const float* __restrict__ dqh,
-                                 const float* __restrict__ dkh, Tin* __restrict__ dq,
+                                 const float* __restrict__ dkh, const Tin* __restrict__ q,
+                                 const Tin* __restrict__ k, Tin* __restrict__ dq,
                                  Tin* __restrict__ dk) {
-    const size_t total = (size_t)d.B * d.T * d.H * d.K;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
-         i += (size_t)gridDim.x * blockDim.x) {
-        const int c = i % d.K;
-        const size_t bth = i / d.K;  // (b*T + t)*H + h
-        const int h = bth % d.H;
-        const size_t bt = bth / d.H;
-        float sq = 0.f, sk = 0.f;
-        for (int u = 0; u < d.G; ++u) {
-            const size_t j = (bt * d.HV + (size_t)h * d.G + u) * d.K + c;
-            sq += dqh[j];
-            sk += dkh[j];
+    const int lane = threadIdx.x & 31;
+    const size_t rows = (size_t)d.B * d.T * d.H;
+    const size_t wstep = (size_t)gridDim.x * (blockDim.x >> 5);
+    for (size_t row = blockIdx.x * (size_t)(blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+         row += wstep) {
+        const int h = row % d.H;
+        const size_t bt = row / d.H;
+        float sq[4], sk[4], xq[4], xk[4];
+        float nq = 0.f, nk = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = lane + 32 * e;
+            sq[e] = sk[e] = xq[e] = xk[e] = 0.f;
+            if (c < d.K) {
+                for (int u = 0; u < d.G; ++u) {
+                    const size_t j = (bt * d.HV + (size_t)h * d.G + u) * d.K + c;
+                    sq[e] += dqh[j];
+                    sk[e] += dkh[j];
+                }
+                if (d.qkn) {
+                    xq[e] = to_f(q[row * d.K + c]);
+                    xk[e] = to_f(k[row * d.K + c]);
+                    nq = fmaf(xq[e], xq[e], nq);
+                    nk = fmaf(xk[e], xk[e], nk);
+                }
+            }
         }
-        dq[i] = from_f<Tin>(sq);
-        dk[i] = from_f<Tin>(sk);
+        if (d.qkn) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                nq += __shfl_xor_sync(0xffffffffu, nq, off);
+                nk += __shfl_xor_sync(0xffffffffu, nk, off);
+            }
+            const float iq = 1.f / fmaxf(sqrtf(nq), kNormEps);
+            const float ik = 1.f / fmaxf(sqrtf(nk), kNormEps);
+            float pq = 0.f, pk = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                xq[e] *= iq;   // normalised rows
+                xk[e] *= ik;
+                pq = fmaf(xq[e], sq[e], pq);
+                pk = fmaf(xk[e], sk[e], pk);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                pq += __shfl_xor_sync(0xffffffffu, pq, off);
+                pk += __shfl_xor_sync(0xffffffffu, pk, off);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sq[e] = (sq[e] - xq[e] * pq) * iq;
+                sk[e] = (sk[e] - xk[e] * pk) * ik;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = lane + 32 * e;
+            if (c < d.K) {
+                dq[row * d.K + c] = from_f<Tin>(sq[e]);
+                dk[row * d.K + c] = from_f<Tin>(sk[e]);
+            }
+        }
     }
 }
 
@@ -899,12 +991,13 @@ kda_status simt_tail_t(const Dims& d, const Ws& w, const void* q, const void* k,
             static_cast<Tin*>(dbeta));
     }
     if ((st = launch_status()) != KDA_OK) return st;
-    const size_t total = (size_t)d.B * d.T * d.H * d.K;
-    const int nblk = (int)std::min<size_t>((total + 255) / 256, 152 * 16);
+    const size_t rows = (size_t)d.B * d.T * d.H;
+    const int nblk = (int)std::min<size_t>((rows + 7) / 8, 152 * 16);
     {
         TimedLaunch tl("simt_group_sum", s);
-        group_sum_kernel<Tin><<<nblk, 256, 0, s>>>(d, w.dqh, w.dkh, static_cast<Tin*>(dq),
-                                                   static_cast<Tin*>(dk));
+        group_sum_kernel<Tin><<<nblk, 256, 0, s>>>(d, w.dqh, w.dkh, static_cast<const Tin*>(q),
+                                                   static_cast<const Tin*>(k),
+                                                   static_cast<Tin*>(dq), static_cast<Tin*>(dk));
     }
     return launch_status();
 }
@@ -937,17 +1030,20 @@ kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, 
 }
 }  // namespace
 
-kda_status group_sum_launch(const kda_dims& kd, const float* dqh, const float* dkh, void* dq,
-                            void* dk, cudaStream_t s) {
+kda_status group_sum_launch(const kda_dims& kd, const float* dqh, const float* dkh,
+                            const void* q, const void* k, void* dq, void* dk, cudaStream_t s) {
     const Dims d = make_dims(kd);
-    const size_t total = (size_t)d.B * d.T * d.H * d.K;
-    const int nblk = (int)std::min<size_t>((total + 255) / 256, 152 * 16);
+    const size_t rows = (size_t)d.B * d.T * d.H;
+    const int nblk = (int)std::min<size_t>((rows + 7) / 8, 152 * 16);
     TimedLaunch tl("group_sum", s);
     if (kd.dtype == KDA_BF16)
         group_sum_kernel<__nv_bfloat16><<<nblk, 256, 0, s>>>(
-            d, dqh, dkh, static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk));
+            d, dqh, dkh, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+            static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk));
     else
-        group_sum_kernel<float><<<nblk, 256, 0, s>>>(d, dqh, dkh, static_cast<float*>(dq),
+        group_sum_kernel<float><<<nblk, 256, 0, s>>>(d, dqh, dkh, static_cast<const float*>(q),
+                                                     static_cast<const float*>(k),
+                                                     static_cast<float*>(dq),
                                                      static_cast<float*>(dk));
     return launch_status();
 }

@@ -139,6 +139,28 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&x)[8]) {
     }
 }
 
+// L2-normalises each of the 64 rows of a [64][128] bf16 token tile (two
+// 64-column 128B-swizzled boxes, 8 KB apart) in place: x / max(|x|, 1e-12),
+// the squares summed in fp32.  nthreads (256 or 512) threads; sixteen
+// consecutive lanes share a row, one 8-channel unit each.
+__device__ __forceinline__ void l2norm_tile_rows(uint8_t* tile, int tid, int nthreads) {
+    for (int unit = tid; unit < 64 * 16; unit += nthreads) {
+        const int row = unit >> 4, o = unit & 15;
+        uint4* p = reinterpret_cast<uint4*>(tile + (o >> 3) * 8192 + sw128_offset(row, 8 * (o & 7)));
+        float x[8];
+        unpack8(*p, x);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= inv;
+        *p = pack8(x);
+    }
+}
+
 // ---- epilogue steps shared by the two chains (thread <-> value column v) ----
 
 __device__ __forceinline__ void store_row_bf16(uint8_t* base, int v, int col0, const float (&r)[32],
@@ -1188,6 +1210,7 @@ __host__ __device__ constexpr uint32_t right_col(int R) { return 8u * (uint32_t)
 struct IntraArgs {
     int T, H, HV, NT, BH;
     float scale;
+    int qkn;                   // L2-normalise the q and k tiles first
     const __nv_bfloat16* beta;
     __nv_bfloat16 *T2, *Tlo;   // null: T is not kept (plain forward)
     float* gam;
@@ -1349,7 +1372,12 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         ok = ok && got;
     }
 
-    // ---- (1) clamp the g tile in place (1024 units of 8 bf16) ----
+    // ---- (1) clamp the g tile in place (1024 units of 8 bf16); with qkn,
+    // normalise the rows of the k and q tiles in place ----
+    if (a.qkn) {
+        l2norm_tile_rows(smem + J_K, tid, kIntraThreads);
+        l2norm_tile_rows(smem + J_Q, tid, kIntraThreads);
+    }
     {
         const __nv_bfloat162 floor2 = __floats2bfloat162_rn(kGateFloor, kGateFloor);
 #pragma unroll
@@ -1832,6 +1860,7 @@ __host__ __device__ constexpr uint32_t lb_dkb_row(int r) {
 struct LocalTcArgs {
     int T, H, HV, NT, G, BH;
     float scale;
+    int qkn;   // L2-normalise the q and k tiles first; dq, dk then go out as fp32
     const float *dQh, *dKb, *dTv, *dgam, *dbv;
     const __nv_bfloat16 *q, *k, *g, *beta;
     __nv_bfloat16 *dq, *dk, *dg, *dbeta;
@@ -2018,6 +2047,11 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const bool got = wait_bar_warp(bar_tma, ph, 41);
         if (got && tid == 0) ++main_waited;
         ok = ok && got;
+    }
+    if (a.qkn) {
+        l2norm_tile_rows(smem + LB_K, tid, kLocalTcThreads);
+        l2norm_tile_rows(smem + LB_Q, tid, kLocalTcThreads);
+        __syncthreads();
     }
 
     // ---- build bf16 operands: Y, Right_R (own block; the copies for later
@@ -2333,7 +2367,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             lastp = fmaf(kr, l, lastp);
             dbps[u] = kr * pb;
             const size_t io = (((size_t)trow + t) * a.HV + hv) * kD + c;
-            if (a.G == 1) {
+            if (a.G == 1 && !a.qkn) {
                 a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
                 a.dk[io] = __float2bfloat16_rn(dkv);
             } else {
@@ -2534,6 +2568,7 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     a.NT = NT;
     a.BH = BH;
     a.scale = d.scale;
+    a.qkn = d.qk_l2norm != 0;
     a.beta = static_cast<const __nv_bfloat16*>(beta);
     a.T2 = keep_T ? w.T2 : nullptr;
     a.Tlo = keep_T ? w.Tlo2 : nullptr;
@@ -2572,6 +2607,7 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
     a.G = d.HV / d.H;
     a.BH = d.B * d.HV;
     a.scale = d.scale;
+    a.qkn = d.qk_l2norm != 0;
     a.dQh = p.dQh;
     a.dKb = p.dKb;
     a.dTv = p.dTv;
@@ -2759,8 +2795,8 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     SimtWsPtrs p;
     simt_ws_ptrs(d, 1, w.simt, &p);
     if ((st = run_local_bwd_tc(d, w, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
-    if (d.HV == d.H) return KDA_OK;
-    return group_sum_launch(d, p.dqh, p.dkh, dq, dk, s);
+    if (d.HV == d.H && !d.qk_l2norm) return KDA_OK;
+    return group_sum_launch(d, p.dqh, p.dkh, q, k, dq, dk, s);
 }
 
 kda_status tc_take_error(cudaStream_t s) {

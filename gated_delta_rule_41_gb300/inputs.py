@@ -96,17 +96,21 @@ def _l2norm(x: torch.Tensor) -> torch.Tensor:
 
 
 def make_chunk_inputs(w: Workload, device="cpu", g_floor: Optional[float] = -5.0,
-                      T: Optional[int] = None, seed: Optional[int] = None) -> dict:
+                      T: Optional[int] = None, seed: Optional[int] = None,
+                      normalize_qk: bool = True) -> dict:
     """Draw q, k, v, g, beta (w.dtype), h0 (float32 or None), do (w.dtype), dht.
 
     ``T`` and ``seed`` override the workload's (used for ragged / scaled cases).
+    ``normalize_qk=False`` leaves q and k as raw N(0,1) draws (for the kernels'
+    own L2 normalisation).
     """
     T = w.T if T is None else T
     gen = _gen(w.seed if seed is None else seed, device)
     f32 = dict(dtype=torch.float32, device=device, generator=gen)
     B, H, HV, K, V = w.B, w.H, w.HV, w.K, w.V
-    q = _l2norm(torch.randn(B, T, H, K, **f32))
-    k = _l2norm(torch.randn(B, T, H, K, **f32))
+    nrm = _l2norm if normalize_qk else (lambda x: x)
+    q = nrm(torch.randn(B, T, H, K, **f32))
+    k = nrm(torch.randn(B, T, H, K, **f32))
     v = torch.randn(B, T, HV, V, **f32)
     beta = torch.sigmoid(torch.randn(B, T, HV, **f32))
     g = -torch.nn.functional.softplus(torch.randn(B, T, HV, K, **f32) * w.g_sigma + w.g_mu)
@@ -121,7 +125,7 @@ def make_chunk_inputs(w: Workload, device="cpu", g_floor: Optional[float] = -5.0
 
 
 def make_decode_inputs(w: DecodeWorkload, device="cpu", steps: Optional[int] = None,
-                       B: Optional[int] = None) -> dict:
+                       B: Optional[int] = None, normalize_qk: bool = True) -> dict:
     """Per-step q,k [S,B,H,K]; v [S,B,HV,V]; g [S,B,HV,K]; beta [S,B,HV]; state0."""
     steps = w.steps if steps is None else steps
     B = w.B if B is None else B
@@ -129,8 +133,9 @@ def make_decode_inputs(w: DecodeWorkload, device="cpu", steps: Optional[int] = N
     f32 = dict(dtype=torch.float32, device=device, generator=gen)
     H, HV, K, V = w.H, w.HV, w.K, w.V
     state = torch.randn(B, HV, K, V, **f32) * w.state_std
-    q = _l2norm(torch.randn(steps, B, H, K, **f32))
-    k = _l2norm(torch.randn(steps, B, H, K, **f32))
+    nrm = _l2norm if normalize_qk else (lambda x: x)
+    q = nrm(torch.randn(steps, B, H, K, **f32))
+    k = nrm(torch.randn(steps, B, H, K, **f32))
     v = torch.randn(steps, B, HV, V, **f32)
     beta = torch.sigmoid(torch.randn(steps, B, HV, **f32))
     g = (-torch.nn.functional.softplus(torch.randn(steps, B, HV, K, **f32) * w.g_sigma

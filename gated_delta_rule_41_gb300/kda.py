@@ -32,7 +32,7 @@ class KdaDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("HV", ctypes.c_int), ("K", ctypes.c_int), ("V", ctypes.c_int),
                 ("chunk_size", ctypes.c_int), ("scale", ctypes.c_float),
-                ("dtype", ctypes.c_int), ("impl", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("impl", ctypes.c_int), ("qk_l2norm", ctypes.c_int)]
 
 
 _lib = None
@@ -106,12 +106,12 @@ def _check_dev(*ts):
             raise KdaError(1, "tensors must be contiguous CUDA tensors")
 
 
-def make_dims(q, v, chunk_size=64, scale=None, impl="auto") -> KdaDims:
+def make_dims(q, v, chunk_size=64, scale=None, impl="auto", qk_l2norm=False) -> KdaDims:
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
     return KdaDims(B, T, H, HV, K, V, chunk_size,
                    float(K ** -0.5 if scale is None else scale), _dtype_code(q.dtype),
-                   IMPLS[impl])
+                   IMPLS[impl], int(bool(qk_l2norm)))
 
 
 def workspace_bytes(dims: KdaDims, for_bwd: bool) -> int:
@@ -144,12 +144,13 @@ class SavedForward:
 
 def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
                   chunk_size=64, impl="auto", workspace=None, out=None, final_state=None,
-                  stream=None, save_for_backward=False):
+                  stream=None, save_for_backward=False, use_qk_l2norm_in_kernel=False):
     """Chunked KDA forward.  Returns (o, final_state or None), plus a
-    ``SavedForward`` when ``save_for_backward`` is set."""
+    ``SavedForward`` when ``save_for_backward`` is set.  With
+    ``use_qk_l2norm_in_kernel`` the kernels L2-normalise q and k themselves."""
     lib = load_library()
     _check_dev(q, k, v, g, beta, initial_state)
-    dims = make_dims(q, v, chunk_size, scale, impl)
+    dims = make_dims(q, v, chunk_size, scale, impl, use_qk_l2norm_in_kernel)
     o = torch.empty_like(v) if out is None else out
     ht = None
     if output_final_state:
@@ -168,13 +169,15 @@ def chunk_kda_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final
 
 def chunk_kda_bwd(q, k, v, g, beta, do, dht=None, scale=None, initial_state=None,
                   chunk_size=64, impl="auto", workspace=None, grads=None, stream=None,
-                  saved=None):
+                  saved=None, use_qk_l2norm_in_kernel=False):
     """Backward of chunk_kda_fwd.  Returns dict dq, dk, dv, dg, dbeta, dh0.
     With ``saved`` (from a saving forward on the same inputs) the tensor-core
-    kernels start from the saved intermediates instead of recomputing them."""
+    kernels start from the saved intermediates instead of recomputing them.
+    With ``use_qk_l2norm_in_kernel``, dq and dk are the gradients with respect
+    to the raw (unnormalised) q and k."""
     lib = load_library()
     _check_dev(q, k, v, g, beta, do, dht, initial_state)
-    dims = make_dims(q, v, chunk_size, scale, impl)
+    dims = make_dims(q, v, chunk_size, scale, impl, use_qk_l2norm_in_kernel)
     if grads is None:
         grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                      dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
@@ -182,9 +185,9 @@ def chunk_kda_bwd(q, k, v, g, beta, do, dht=None, scale=None, initial_state=None
                                       device=q.device) if initial_state is not None else None))
     if saved is not None:
         if (saved.dims.B, saved.dims.T, saved.dims.H, saved.dims.HV, saved.dims.K, saved.dims.V,
-                saved.dims.chunk_size, saved.dims.impl) != (dims.B, dims.T, dims.H, dims.HV,
-                                                          dims.K, dims.V, dims.chunk_size,
-                                                          dims.impl):
+                saved.dims.chunk_size, saved.dims.impl, saved.dims.qk_l2norm) != (
+                    dims.B, dims.T, dims.H, dims.HV, dims.K, dims.V, dims.chunk_size, dims.impl,
+                    dims.qk_l2norm):
             raise KdaError(1, "chunk_kda_bwd: saved forward has other dims")
         ws, nws, fn, what = saved.workspace, saved.nbytes, lib.kda_chunk_bwd_saved, \
             "kda_chunk_bwd_saved"
@@ -199,7 +202,8 @@ def chunk_kda_bwd(q, k, v, g, beta, do, dht=None, scale=None, initial_state=None
     return grads
 
 
-def recurrent_step(q, k, v, g, beta, state, scale=None, out=None, stream=None):
+def recurrent_step(q, k, v, g, beta, state, scale=None, out=None, stream=None,
+                   use_qk_l2norm_in_kernel=False):
     """One decode token: q,k [B,H,K]; v [B,HV,V]; g [B,HV,K]; beta [B,HV];
     ``state`` [B,HV,K,V] float32 updated in place.  Returns o [B,HV,V]."""
     lib = load_library()
@@ -207,7 +211,7 @@ def recurrent_step(q, k, v, g, beta, state, scale=None, out=None, stream=None):
     B, H, K = q.shape
     HV, V = v.shape[1], v.shape[2]
     dims = KdaDims(B, 1, H, HV, K, V, 64, float(K ** -0.5 if scale is None else scale),
-                   _dtype_code(q.dtype), 0)
+                   _dtype_code(q.dtype), 0, int(bool(use_qk_l2norm_in_kernel)))
     o = torch.empty_like(v) if out is None else out
     st = lib.kda_recurrent_step(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                 _ptr(beta), _ptr(state), _ptr(o), _stream(stream))

@@ -87,6 +87,13 @@ typedef struct {
     float scale;      /* multiplies q; pass 1/sqrt(K) for the standard scale */
     kda_dtype dtype;
     kda_impl impl;
+    /* Nonzero: the kernels L2-normalise q and k over K, per token and head,
+     * before use: x_n = x / max(||x||_2, 1e-12), in fp32 (the "q/k L2-norm"
+     * variant of the K3 README's test-status table, row L3/L4).  Results are
+     * those of the scan on the normalised q, k; dq and dk are the gradients
+     * with respect to the raw q, k: dx = (dx_n - x_n <x_n, dx_n>) / max(||x||, 1e-12).
+     * Zero: q and k are used as given (a caller that normalises them itself). */
+    int qk_l2norm;
 } kda_dims;
 
 /* Bytes of device workspace that kda_chunk_fwd (for_bwd = 0) or

@@ -58,12 +58,14 @@ def _load():
             lib.kda_oracle_fwd_recurrent.argtypes = [i] * 6 + [d] + [p] * 8
             lib.kda_oracle_bwd_recurrent.argtypes = [i] * 6 + [d] + [p] * 14
             lib.kda_oracle_fwd_chunked.argtypes = [i] * 6 + [d, i] + [p] * 8
+            lib.kda_oracle_l2norm.argtypes = [ctypes.c_long, i, p, p]
+            lib.kda_oracle_l2norm_bwd.argtypes = [ctypes.c_long, i, p, p, p]
             lib.kda_oracle_chunk_wy.argtypes = [i] * 3 + [p] * 11
             lib.kda_oracle_step.argtypes = [i] * 5 + [d] + [p] * 7
             lib.kda_oracle_num_threads.restype = i
             for f in ("kda_oracle_fwd_recurrent", "kda_oracle_bwd_recurrent",
                       "kda_oracle_fwd_chunked", "kda_oracle_chunk_wy",
-                      "kda_oracle_step"):
+                      "kda_oracle_step", "kda_oracle_l2norm", "kda_oracle_l2norm_bwd"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -163,6 +165,24 @@ def step(q, k, v, g, beta, state, scale=None):
     _load().kda_oracle_step(B, H, HV, K, V, scale, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                             _ptr(beta), _ptr(state), _ptr(o))
     return o
+
+
+def l2norm(x):
+    """x / max(||x||_2, 1e-12) over the last axis (float64)."""
+    x = _f64(x)
+    y = np.zeros_like(x)
+    K = x.shape[-1]
+    _load().kda_oracle_l2norm(x.size // K if K else 0, K, _ptr(x), _ptr(y))
+    return y
+
+
+def l2norm_bwd(x, dy):
+    """Gradient with respect to x of <dy, l2norm(x)> (last axis, float64)."""
+    x, dy = _f64(x), _f64(dy)
+    dx = np.zeros_like(x)
+    K = x.shape[-1]
+    _load().kda_oracle_l2norm_bwd(x.size // K if K else 0, K, _ptr(x), _ptr(dy), _ptr(dx))
+    return dx
 
 
 def head_slice(x, b, head, kind):

@@ -44,6 +44,8 @@
  *                              U, Aqk), exposed for the WY pins.
  *   kda_oracle_step            one decode token applied in place (row L6,
  *                              state [B,HV,K,V]).
+ *   kda_oracle_l2norm(_bwd)    x / max(||x||, 1e-12) per row and its
+ *                              backward (the q/k L2-norm variant).
  *
  * Layouts (row-major, contiguous):
  *   q, k      [B,T,H,K]     v, o   [B,T,HV,V]     g  [B,T,HV,K]
@@ -473,5 +475,43 @@ void kda_oracle_step(int B, int H, int HV, int K, int V, double scale, const dou
         token_step(K, V, scale, q + ((size_t)b * H + h) * K, k + ((size_t)b * H + h) * K,
                    v + (size_t)bh * V, g + (size_t)bh * K, beta[bh],
                    state + (size_t)bh * K * V, o + (size_t)bh * V, NULL);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* L2 normalisation of q and k over K, and its backward (the "q/k L2-norm"   */
+/* variant of the K3 README's test-status table, row L3/L4).  The pages give */
+/* no formula beyond the name; the plain reading is x / ||x||_2 per token    */
+/* and head, with the norm floored at 1e-12 so that a zero row maps to zero. */
+/*   y  = x / max(||x||, eps)                                               */
+/*   dx = (dy - y <y, dy>) / ||x||       where ||x|| > eps                   */
+/*   dx = dy / eps                       where the floor is active           */
+/* rows vectors of length K, contiguous.                                     */
+/* ------------------------------------------------------------------------ */
+void kda_oracle_l2norm(long rows, int K, const double* x, double* y) {
+    for (long r = 0; r < rows; ++r) {
+        const double* xr = x + (size_t)r * K;
+        double ss = 0.0;
+        for (int c = 0; c < K; ++c) ss += xr[c] * xr[c];
+        double n = sqrt(ss);
+        double den = n > 1e-12 ? n : 1e-12;
+        for (int c = 0; c < K; ++c) y[(size_t)r * K + c] = xr[c] / den;
+    }
+}
+
+void kda_oracle_l2norm_bwd(long rows, int K, const double* x, const double* dy, double* dx) {
+    for (long r = 0; r < rows; ++r) {
+        const double* xr = x + (size_t)r * K;
+        const double* dyr = dy + (size_t)r * K;
+        double ss = 0.0;
+        for (int c = 0; c < K; ++c) ss += xr[c] * xr[c];
+        double n = sqrt(ss);
+        if (n > 1e-12) {
+            double dot = 0.0;
+            for (int c = 0; c < K; ++c) dot += (xr[c] / n) * dyr[c];
+            for (int c = 0; c < K; ++c) dx[(size_t)r * K + c] = (dyr[c] - (xr[c] / n) * dot) / n;
+        } else {
+            for (int c = 0; c < K; ++c) dx[(size_t)r * K + c] = dyr[c] / 1e-12;
+        }
     }
 }

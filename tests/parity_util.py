@@ -39,13 +39,28 @@ def assert_close(name, got, ref, dtype):
     return float(err.max()), float(fro)
 
 
-def oracle_chunk(inp, want_bwd, heads=None):
+def oracle_chunk(inp, want_bwd, heads=None, qk_l2norm=False):
     """Run the oracle on the inputs dict (torch, any device).
 
     heads=None: all heads.  Otherwise a list of (b, hv); results are returned
     per head as dicts of arrays shaped like the one-head slices [1,T,1,X].
     Only valid per head when H == HV (no GVA group sums needed).
+    qk_l2norm: q and k are L2-normalised first (oracle.l2norm) and dq, dk are
+    mapped back to the raw q, k (oracle.l2norm_bwd).
     """
+    if qk_l2norm:
+        qr, kr = to_f64(inp["q"]), to_f64(inp["k"])
+        normed = dict(inp, q=torch.from_numpy(oracle.l2norm(qr)),
+                      k=torch.from_numpy(oracle.l2norm(kr)))
+        res = oracle_chunk(normed, want_bwd, heads)
+        if want_bwd and heads is None:
+            res["dq"], res["dk"] = oracle.l2norm_bwd(qr, res["dq"]), oracle.l2norm_bwd(kr, res["dk"])
+        elif want_bwd:
+            for (b, hv), r in zip(heads, res):
+                sl = lambda x: x[b:b + 1, :, hv:hv + 1]
+                r["dq"], r["dk"] = (oracle.l2norm_bwd(sl(qr), r["dq"]),
+                                    oracle.l2norm_bwd(sl(kr), r["dk"]))
+        return res
     q, k, v, g, beta = (to_f64(inp[n]) for n in ("q", "k", "v", "g", "beta"))
     h0 = to_f64(inp.get("h0"))
     do = to_f64(inp.get("do"))

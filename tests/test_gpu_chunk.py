@@ -224,6 +224,45 @@ def test_tcgen05_clamp_below_minus_five(saved):
     assert torch.all(res["dg"].float().cpu()[below] == 0)
 
 
+@pytest.mark.parametrize("impl,saved", [("simt", False), ("tcgen05", False), ("tcgen05", True)])
+@pytest.mark.parametrize("H,HV", [(2, 2), (1, 2)])
+def test_qk_l2norm_in_kernel(impl, saved, H, HV):
+    """The kernels L2-normalise raw q and k themselves (the K3 README's "q/k
+    L2-norm" variant): outputs are the scan of the normalised q, k, and dq, dk
+    are gradients with respect to the raw q, k (after the GVA group sum)."""
+    w = I.Workload("qkn", 2, 192, H, HV, 128, 128, 64, torch.bfloat16, g_sigma=2.0, h0_std=0.1,
+                   seed=51 + H + HV)
+    inp = I.make_chunk_inputs(w, normalize_qk=False)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    out = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
+                            output_final_state=True, impl=impl, save_for_backward=saved,
+                            use_qk_l2norm_in_kernel=True)
+    res = dict(o=out[0], ht=out[1])
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                 initial_state=t["h0"], impl=impl,
+                                 saved=out[2] if saved else None, use_qk_l2norm_in_kernel=True))
+    torch.cuda.synchronize()
+    kda.check()
+    compare_all(res, oracle_chunk(inp, True, qk_l2norm=True), w, with_h0=True)
+
+
+def test_qk_l2norm_in_kernel_fp32_gva_with_final_state_gradient():
+    w = I.Workload("qkn_fp32", 2, 64, 2, 4, 16, 16, 16, torch.float32, g_sigma=2.0, h0_std=0.3,
+                   dht=True, seed=55)
+    inp = I.make_chunk_inputs(w, normalize_qk=False)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    o, ht = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
+                              output_final_state=True, chunk_size=w.chunk,
+                              use_qk_l2norm_in_kernel=True)
+    res = dict(o=o, ht=ht)
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                 dht=t["dht"], initial_state=t["h0"], chunk_size=w.chunk,
+                                 use_qk_l2norm_in_kernel=True))
+    torch.cuda.synchronize()
+    kda.check()
+    compare_all(res, oracle_chunk(inp, True, qk_l2norm=True), w, with_h0=True)
+
+
 def test_ragged_value_width_simt():
     """V not a multiple of the 32-column tile, small K."""
     w = I.Workload("ragged_v", 1, 64, 1, 2, 16, 40, 32, torch.float32, h0_std=0.5, dht=True,

@@ -65,3 +65,26 @@ def test_decode_matches_chunk_scan():
     torch.cuda.synchronize()
     torch.testing.assert_close(torch.stack(outs, 1), o, atol=1e-4, rtol=0)
     torch.testing.assert_close(state, ht, atol=1e-4, rtol=0)
+
+
+@pytest.mark.parametrize("K,V,H,HV,dtype", [(128, 128, 2, 4, torch.bfloat16),
+                                             (64, 64, 2, 2, torch.float32),
+                                             (32, 48, 1, 3, torch.float32)])
+def test_decode_qk_l2norm_in_kernel(K, V, H, HV, dtype):
+    """Raw q and k, L2-normalised by the decode kernel (fast and generic
+    paths) against the oracle step on the normalised q, k."""
+    w = I.DecodeWorkload("dec_qkn", 3, H, HV, K, V, 8, dtype, seed=33)
+    inp = I.make_decode_inputs(w, normalize_qk=False)
+    state = inp["state"].cuda().contiguous()
+    d = {n: inp[n].cuda() for n in ("q", "k", "v", "g", "beta")}
+    ref_state = to_f64(inp["state"]).copy()
+    for s in range(w.steps):
+        o = kda.recurrent_step(d["q"][s], d["k"][s], d["v"][s], d["g"][s], d["beta"][s], state,
+                               use_qk_l2norm_in_kernel=True)
+        o_ref = oracle.step(oracle.l2norm(to_f64(inp["q"][s])), oracle.l2norm(to_f64(inp["k"][s])),
+                            to_f64(inp["v"][s]), to_f64(inp["g"][s]), to_f64(inp["beta"][s]),
+                            ref_state)
+        assert_close(f"o step {s}", o, o_ref, dtype)
+    torch.cuda.synchronize()
+    kda.check()
+    assert_close("state", state, ref_state, dtype)
