@@ -7,7 +7,8 @@ else.  The library is loaded on first use; if it is missing, every call
 raises instead of falling back to another implementation.
 """
 from .kda import (  # noqa: F401
-    KdaError, SavedForward, chunk_kda_fwd, chunk_kda_bwd, recurrent_step, workspace_bytes,
+    KdaError, SavedForward, chunk_kda_fwd, chunk_kda_bwd, chunk_kda_fwd_varlen,
+    chunk_kda_bwd_varlen, recurrent_step, workspace_bytes,
     library_path,
     load_library, check, timing_enable, timing_read,
 )

@@ -84,6 +84,28 @@ kda_status copy_or_zero(const kda_dims& d, float* dst, const float* src, cudaStr
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// Variable-length batches: dims as for kda_chunk_fwd except B == 1 and no
+// T % chunk_size rule; the sequences run on the SIMT kernels.
+kda_status check_varlen_dims(const kda_dims* d, int nseq) {
+    if (!d) return KDA_ERR_INVALID_ARG;
+    kda_dims t = *d;
+    t.T = 0;   // T % chunk_size does not apply
+    kda_status st = check_common(&t, true);
+    if (st != KDA_OK) return st;
+    if (d->T < 0 || d->B != 1 || nseq < 1) return KDA_ERR_SHAPE;
+    if ((long long)nseq * d->HV > 65535) return KDA_ERR_UNSUPPORTED;
+    if (d->impl == KDA_IMPL_TCGEN05 || !simt_supported(*d)) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+kda_status check_varlen(const kda_dims* d, const int* cu, int nseq) {
+    const kda_status st = check_varlen_dims(d, nseq);
+    if (st != KDA_OK) return st;
+    if (!cu) return KDA_ERR_INVALID_ARG;
+    if (!aligned(cu, 4)) return KDA_ERR_ALIGNMENT;
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -191,6 +213,50 @@ kda_status kda_chunk_bwd_saved(const kda_dims* d, const void* q, const void* k, 
                      workspace_bytes, stream, true);
 }
 
+size_t kda_chunk_workspace_bytes_varlen(const kda_dims* d, int num_seqs, int for_bwd) {
+    if (check_varlen_dims(d, num_seqs) != KDA_OK) return 0;
+    return simt_varlen_workspace_bytes(*d, num_seqs, for_bwd ? 1 : 0);
+}
+
+kda_status kda_chunk_fwd_varlen(const kda_dims* d, const int* cu_seqlens, int num_seqs,
+                                const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, const float* h0, void* o,
+                                int output_final_state, float* ht, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    kda_status st = check_varlen(d, cu_seqlens, num_seqs);
+    if (st != KDA_OK) return st;
+    if (output_final_state && !ht) return KDA_ERR_INVALID_ARG;
+    const bool empty = d->T == 0;
+    if ((st = check_ptrs(empty, elem_bytes(*d), {q, k, v, g, beta, o},
+                         {h0, output_final_state ? ht : nullptr})) != KDA_OK)
+        return st;
+    const size_t need = simt_varlen_workspace_bytes(*d, num_seqs, 0);
+    if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_ALIGNMENT;
+    return simt_fwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, o,
+                           output_final_state ? ht : nullptr, workspace,
+                           static_cast<cudaStream_t>(stream));
+}
+
+kda_status kda_chunk_bwd_varlen(const kda_dims* d, const int* cu_seqlens, int num_seqs,
+                                const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, const float* h0, const void* dout,
+                                const float* dht, void* dq, void* dk, void* dv, void* dg,
+                                void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    kda_status st = check_varlen(d, cu_seqlens, num_seqs);
+    if (st != KDA_OK) return st;
+    const bool empty = d->T == 0;
+    if ((st = check_ptrs(empty, elem_bytes(*d), {q, k, v, g, beta, dout, dq, dk, dv, dg, dbeta},
+                         {h0, dht, dh0})) != KDA_OK)
+        return st;
+    const size_t need = simt_varlen_workspace_bytes(*d, num_seqs, 1);
+    if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_ALIGNMENT;
+    return simt_bwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, dout, dht, dq, dk, dv,
+                           dg, dbeta, dh0, workspace, static_cast<cudaStream_t>(stream));
+}
+
 kda_status kda_recurrent_step(const kda_dims* d, const void* q, const void* k, const void* v,
                               const void* g, const void* beta, float* state, void* o,
                               void* stream) {
@@ -209,6 +275,7 @@ kda_status kda_check(void* stream) {
         return KDA_ERR_CUDA;
     kda_status st = tc_take_error(static_cast<cudaStream_t>(stream));
     if (st != KDA_OK) return st;
+    if ((st = simt_take_error(static_cast<cudaStream_t>(stream))) != KDA_OK) return st;
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -61,6 +61,21 @@ kda_status simt_bwd(const kda_dims& d, const void* q, const void* k, const void*
                     const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
                     float* dh0, void* ws, cudaStream_t s);
 
+// Packed variable-length sequences on the SIMT kernels (B == 1; cu_seqlens
+// [nseq + 1] on the device; states [nseq][HV][K][V]).
+size_t simt_varlen_workspace_bytes(const kda_dims& d, int nseq, int for_bwd);
+kda_status simt_fwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q,
+                           const void* k, const void* v, const void* g, const void* beta,
+                           const float* h0, void* o, float* ht, void* ws, cudaStream_t s);
+kda_status simt_bwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q,
+                           const void* k, const void* v, const void* g, const void* beta,
+                           const float* h0, const void* dout, const float* dht, void* dq,
+                           void* dk, void* dv, void* dg, void* dbeta, float* dh0, void* ws,
+                           cudaStream_t s);
+// Reads and clears the device error word of the SIMT kernels (invalid
+// cu_seqlens: KDA_ERR_SHAPE).
+kda_status simt_take_error(cudaStream_t s);
+
 bool tc_supported(const kda_dims& d);
 size_t tc_workspace_bytes(const kda_dims& d, int for_bwd);
 // save: also keep the chunk-start states and delta in a backward-sized

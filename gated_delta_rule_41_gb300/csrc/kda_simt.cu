@@ -52,13 +52,37 @@ struct Dims {
     int B, T, H, HV, K, V, C, NT, G;
     float scale;
     int qkn;   // L2-normalise q and k over K inside the kernels
+    // Variable-length sequences (B == 1, sequences packed along T): ctab
+    // [NT][2] holds each chunk's first token and number of valid rows (0 for
+    // an unused slot), sfirst [nseq + 1] each sequence's first chunk.  T is
+    // then NT * C (the workspace's padded length) and Tr the real token
+    // count.  ctab == nullptr: fixed-length batches, Tr == T.
+    int Tr;
+    const int* ctab;
+    const int* sfirst;
+    int NS;   // rows of the state arrays: B * HV, or nseq * HV with a chunk table
 };
+
+// Chunk n of head row bh: batch b, first token t0 and valid rows len (len <
+// C only for the last chunk of a variable-length sequence; 0 for an unused
+// chunk-table slot).  With a chunk table the head row is hv (B == 1).
+struct ChunkRef {
+    int b, t0, len;
+};
+__device__ __forceinline__ ChunkRef chunk_ref(const Dims& d, int bh, int n) {
+    if (!d.ctab) return ChunkRef{bh / d.HV, n * d.C, d.C};
+    return ChunkRef{0, d.ctab[2 * n], d.ctab[2 * n + 1]};
+}
 
 Dims make_dims(const kda_dims& d) {
     Dims r;
     r.B = d.B; r.T = d.T; r.H = d.H; r.HV = d.HV; r.K = d.K; r.V = d.V;
     r.C = d.chunk_size; r.NT = d.T / d.chunk_size; r.G = d.HV / d.H; r.scale = d.scale;
     r.qkn = d.qk_l2norm != 0;
+    r.Tr = d.T;
+    r.ctab = nullptr;
+    r.sfirst = nullptr;
+    r.NS = d.B * d.HV;
     return r;
 }
 
@@ -146,7 +170,9 @@ __global__ void __launch_bounds__(kThreads)
 intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
              const Tin* __restrict__ v, const Tin* __restrict__ g, const Tin* __restrict__ beta) {
     const int n = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / d.HV, hv = bh % d.HV, h = hv / d.G;
+    const ChunkRef cr = chunk_ref(d, bh, n);
+    if (cr.len <= 0) return;
+    const int b = cr.b, hv = bh % d.HV, h = hv / d.G;
     const int C = d.C, K = d.K, V = d.V, KP = K + 1, CP = C + 1;
     const int tid = threadIdx.x;
     extern __shared__ float sm[];
@@ -156,17 +182,21 @@ intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     float* A = GS + C * KP;
     float* Tm = A + C * CP;
     float* bS = Tm + C * CP;
-    const int t0 = n * C;
+    const int t0 = cr.t0, len = cr.len;
 
+    // rows past a sequence's end enter as q = k = v = 0, g = 0, beta = 0:
+    // they leave the state unchanged and their outputs are not written
     for (int i = tid; i < C * K; i += kThreads) {
         const int r = i / K, c = i % K;
+        const bool on = r < len;
         const size_t iq = tok_idx(d, b, t0 + r, h, d.H, K) + c;
         const size_t ig = tok_idx(d, b, t0 + r, hv, d.HV, K) + c;
-        kS[r * KP + c] = to_f(k[iq]);
-        qS[r * KP + c] = d.scale * to_f(q[iq]);
-        GS[r * KP + c] = fmaxf(to_f(g[ig]), kGateFloor);
+        kS[r * KP + c] = on ? to_f(k[iq]) : 0.f;
+        qS[r * KP + c] = on ? d.scale * to_f(q[iq]) : 0.f;
+        GS[r * KP + c] = on ? fmaxf(to_f(g[ig]), kGateFloor) : 0.f;
     }
-    for (int r = tid; r < C; r += kThreads) bS[r] = to_f(beta[((size_t)b * d.T + t0 + r) * d.HV + hv]);
+    for (int r = tid; r < C; r += kThreads)
+        bS[r] = r < len ? to_f(beta[((size_t)b * d.T + t0 + r) * d.HV + hv]) : 0.f;
     __syncthreads();
     if (d.qkn) {
         l2norm_rows(kS, qS, C, K, KP, d.scale);
@@ -213,7 +243,7 @@ intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
 
     float* Tm_g = w.Tm + ((size_t)bh * d.NT + n) * C * C;
     for (int p = tid; p < C * C; p += kThreads) Tm_g[p] = Tm[(p / C) * CP + p % C];
-    const size_t row0 = (size_t)bh * d.T + t0;
+    const size_t row0 = (size_t)bh * d.T + (size_t)n * C;
     for (int i = tid; i < C * K; i += kThreads) {
         const int r = i / K, c = i % K;
         const float G = GS[r * KP + c], gl = GS[(C - 1) * KP + c];
@@ -235,7 +265,7 @@ intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     for (int i = tid; i < C * V; i += kThreads) {
         const int r = i / V, j = i % V;
         float acc = 0.f;
-        for (int m = 0; m <= r; ++m)
+        for (int m = 0; m <= r && m < len; ++m)
             acc += Tm[r * CP + m] * bS[m] * to_f(v[tok_idx(d, b, t0 + m, hv, d.HV, V) + j]);
         w.U[(row0 + r) * V + j] = acc;
     }
@@ -255,8 +285,12 @@ template <typename Tout>
 __global__ void __launch_bounds__(kThreads)
 state_fwd_kernel(Dims d, Ws w, const float* __restrict__ h0, Tout* __restrict__ o,
                  float* __restrict__ ht, int mode) {
+    // bh: the state's row (b, hv), or (sequence, hv) with a chunk table;
+    // bw: the head row of the workspace arrays
     const int vt = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / d.HV, hv = bh % d.HV;
+    const int hv = bh % d.HV, bw = d.ctab ? hv : bh;
+    const int nfirst = d.ctab ? d.sfirst[bh / d.HV] : 0;
+    const int nend = d.ctab ? d.sfirst[bh / d.HV + 1] : d.NT;
     const int C = d.C, K = d.K, V = d.V;
     const int j0 = vt * kVT;
     const int VT = min(kVT, V - j0);
@@ -275,22 +309,23 @@ state_fwd_kernel(Dims d, Ws w, const float* __restrict__ h0, Tout* __restrict__ 
         const int c = i / kVT, j = i % kVT;
         S[i] = (h0 && j < VT) ? h0[((size_t)bh * K + c) * V + j0 + j] : 0.f;
     }
-    for (int n = 0; n < d.NT; ++n) {
+    for (int n = nfirst; n < nend; ++n) {
         __syncthreads();
-        const size_t row0 = (size_t)bh * d.T + (size_t)n * C;
+        const ChunkRef cr = chunk_ref(d, bw, n);
+        const size_t row0 = (size_t)bw * d.T + (size_t)n * C;
         for (int i = tid; i < C * K; i += kThreads) {
             Ws_[i] = w.W[row0 * K + i];
             Qs[i] = w.Qh[row0 * K + i];
             Kbs[i] = w.Kb[row0 * K + i];
         }
-        for (int i = tid; i < C * C; i += kThreads) As[i] = w.Aqk[((size_t)bh * d.NT + n) * C * C + i];
-        for (int c = tid; c < K; c += kThreads) gs[c] = w.gam[((size_t)bh * d.NT + n) * K + c];
+        for (int i = tid; i < C * C; i += kThreads) As[i] = w.Aqk[((size_t)bw * d.NT + n) * C * C + i];
+        for (int c = tid; c < K; c += kThreads) gs[c] = w.gam[((size_t)bw * d.NT + n) * K + c];
         for (int i = tid; i < C * kVT; i += kThreads) {
             const int r = i / kVT, j = i % kVT;
             Us[i] = j < VT ? w.U[(row0 + r) * V + j0 + j] : 0.f;
         }
         if (mode & 2) {
-            float* hs = w.hs + ((size_t)bh * d.NT + n) * K * V;
+            float* hs = w.hs + ((size_t)bw * d.NT + n) * K * V;
             for (int i = tid; i < K * kVT; i += kThreads) {
                 const int c = i / kVT, j = i % kVT;
                 if (j < VT) hs[(size_t)c * V + j0 + j] = S[i];
@@ -311,7 +346,8 @@ state_fwd_kernel(Dims d, Ws w, const float* __restrict__ h0, Tout* __restrict__ 
                 float acc = 0.f;
                 for (int c = 0; c < K; ++c) acc += Qs[r * K + c] * S[c * kVT + lane];
                 for (int m = 0; m <= r; ++m) acc += As[r * C + m] * Ds[m * kVT + lane];
-                if (lane < VT) o[tok_idx(d, b, n * C + r, hv, d.HV, V) + j0 + lane] = from_f<Tout>(acc);
+                if (lane < VT && r < cr.len)
+                    o[tok_idx(d, cr.b, cr.t0 + r, hv, d.HV, V) + j0 + lane] = from_f<Tout>(acc);
             }
         }
         __syncthreads();
@@ -340,7 +376,9 @@ __global__ void __launch_bounds__(kThreads)
 state_bwd_kernel(Dims d, Ws w, const Tin* __restrict__ dout, const float* __restrict__ dht,
                  float* __restrict__ dh0) {
     const int vt = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / d.HV, hv = bh % d.HV;
+    const int hv = bh % d.HV, bw = d.ctab ? hv : bh;
+    const int nfirst = d.ctab ? d.sfirst[bh / d.HV] : 0;
+    const int nend = d.ctab ? d.sfirst[bh / d.HV + 1] : d.NT;
     const int C = d.C, K = d.K, V = d.V;
     const int j0 = vt * kVT;
     const int VT = min(kVT, V - j0);
@@ -359,22 +397,25 @@ state_bwd_kernel(Dims d, Ws w, const Tin* __restrict__ dout, const float* __rest
         const int c = i / kVT, j = i % kVT;
         dS[i] = (dht && j < VT) ? dht[((size_t)bh * K + c) * V + j0 + j] : 0.f;
     }
-    for (int n = d.NT - 1; n >= 0; --n) {
+    for (int n = nend - 1; n >= nfirst; --n) {
         __syncthreads();
-        const size_t row0 = (size_t)bh * d.T + (size_t)n * C;
+        const ChunkRef cr = chunk_ref(d, bw, n);
+        const size_t row0 = (size_t)bw * d.T + (size_t)n * C;
         for (int i = tid; i < C * K; i += kThreads) {
             Ws_[i] = w.W[row0 * K + i];
             Qs[i] = w.Qh[row0 * K + i];
             Kbs[i] = w.Kb[row0 * K + i];
         }
-        for (int i = tid; i < C * C; i += kThreads) As[i] = w.Aqk[((size_t)bh * d.NT + n) * C * C + i];
-        for (int c = tid; c < K; c += kThreads) gs[c] = w.gam[((size_t)bh * d.NT + n) * K + c];
+        for (int i = tid; i < C * C; i += kThreads) As[i] = w.Aqk[((size_t)bw * d.NT + n) * C * C + i];
+        for (int c = tid; c < K; c += kThreads) gs[c] = w.gam[((size_t)bw * d.NT + n) * K + c];
         for (int i = tid; i < C * kVT; i += kThreads) {
             const int r = i / kVT, j = i % kVT;
-            dOs[i] = j < VT ? to_f(dout[tok_idx(d, b, n * C + r, hv, d.HV, V) + j0 + j]) : 0.f;
+            dOs[i] = (j < VT && r < cr.len)
+                         ? to_f(dout[tok_idx(d, cr.b, cr.t0 + r, hv, d.HV, V) + j0 + j])
+                         : 0.f;
         }
         {
-            float* dh = w.dhs + ((size_t)bh * d.NT + n) * K * V;
+            float* dh = w.dhs + ((size_t)bw * d.NT + n) * K * V;
             for (int i = tid; i < K * kVT; i += kThreads) {
                 const int c = i / kVT, j = i % kVT;
                 if (j < VT) dh[(size_t)c * V + j0 + j] = dS[i];
@@ -425,7 +466,9 @@ __global__ void __launch_bounds__(kThreads)
 vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ beta,
              const Tin* __restrict__ dout, Tin* __restrict__ dv) {
     const int n = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / d.HV, hv = bh % d.HV;
+    const ChunkRef cr = chunk_ref(d, bh, n);
+    if (cr.len <= 0) return;
+    const int b = cr.b, hv = bh % d.HV, t0 = cr.t0, len = cr.len;
     const int C = d.C, K = d.K, V = d.V, CP = C + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     extern __shared__ float sm[];
@@ -444,7 +487,7 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
     const float* dh = w.dhs + ((size_t)bh * d.NT + n) * K * V;
     for (int p = tid; p < C * C; p += kThreads) Tm[(p / C) * CP + p % C] = w.Tm[((size_t)bh * d.NT + n) * C * C + p];
     for (int r = tid; r < C; r += kThreads) {
-        bS[r] = to_f(beta[((size_t)b * d.T + n * C + r) * d.HV + hv]);
+        bS[r] = r < len ? to_f(beta[((size_t)b * d.T + t0 + r) * d.HV + hv]) : 0.f;
         dbv[r] = 0.f;
     }
 
@@ -473,9 +516,9 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
             const bool ok = j < VS;
             dls[r * kVSP + j] = ok ? w.dlt[(row0 + r) * V + j0 + j] : 0.f;
             dds[r * kVSP + j] = ok ? w.ddl[(row0 + r) * V + j0 + j] : 0.f;
-            const size_t it = tok_idx(d, b, n * C + r, hv, d.HV, V) + j0 + j;
-            dOs[r * kVSP + j] = ok ? to_f(dout[it]) : 0.f;
-            vs[r * kVSP + j] = ok ? to_f(v[it]) : 0.f;
+            const size_t it = tok_idx(d, b, t0 + r, hv, d.HV, V) + j0 + j;
+            dOs[r * kVSP + j] = ok && r < len ? to_f(dout[it]) : 0.f;
+            vs[r * kVSP + j] = ok && r < len ? to_f(v[it]) : 0.f;
         }
         __syncthreads();
         // C x K contractions
@@ -512,8 +555,8 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
         for (int m = warp; m < C; m += kThreads / 32) {
             float acc = 0.f;
             for (int i = m; i < C; ++i) acc += Tm[i * CP + m] * dds[i * kVSP + lane];
-            if (lane < VS)
-                dv[tok_idx(d, b, n * C + m, hv, d.HV, V) + j0 + lane] = from_f<Tin>(bS[m] * acc);
+            if (lane < VS && m < len)
+                dv[tok_idx(d, b, t0 + m, hv, d.HV, V) + j0 + lane] = from_f<Tin>(bS[m] * acc);
             float pb = lane < VS ? acc * vs[m * kVSP + lane] : 0.f;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, off);
@@ -560,7 +603,9 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
              const Tin* __restrict__ g, const Tin* __restrict__ beta, Tin* __restrict__ dg,
              Tin* __restrict__ dbeta) {
     const int n = blockIdx.x, bh = blockIdx.y;
-    const int b = bh / d.HV, hv = bh % d.HV, h = hv / d.G;
+    const ChunkRef cr = chunk_ref(d, bh, n);
+    if (cr.len <= 0) return;
+    const int b = cr.b, hv = bh % d.HV, h = hv / d.G, len = cr.len;
     const int C = d.C, K = d.K, KP = K + 1, CP = C + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     extern __shared__ float sm[];
@@ -577,16 +622,18 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     float* Fb = dbS + C;              // Fb[fidx(R,J)*K + c] = exp(G_bR - G_bJ), J <= R
     float* eGbS = Fb + 10 * K;        // eGbS[R*K + c] = exp(G_bR)
     float* eLbS = eGbS + 4 * K;       // eLbS[R*K + c] = exp(G_last - G_bR)
-    const int t0 = n * C;
-    const size_t row0 = (size_t)bh * d.T + t0;
+    const int t0 = cr.t0;
+    const size_t row0 = (size_t)bh * d.T + (size_t)n * C;
     const size_t cc0 = ((size_t)bh * d.NT + n) * C * C;
 
     for (int i = tid; i < C * K; i += kThreads) {
         const int r = i / K, c = i % K;
+        const bool on = r < len;
         const size_t iq = tok_idx(d, b, t0 + r, h, d.H, K) + c;
-        kS[r * KP + c] = to_f(k[iq]);
-        qS[r * KP + c] = d.scale * to_f(q[iq]);
-        GS[r * KP + c] = fmaxf(to_f(g[tok_idx(d, b, t0 + r, hv, d.HV, K) + c]), kGateFloor);
+        kS[r * KP + c] = on ? to_f(k[iq]) : 0.f;
+        qS[r * KP + c] = on ? d.scale * to_f(q[iq]) : 0.f;
+        GS[r * KP + c] =
+            on ? fmaxf(to_f(g[tok_idx(d, b, t0 + r, hv, d.HV, K) + c]), kGateFloor) : 0.f;
         X[r * KP + c] = w.dWm[(row0 + r) * K + c];
     }
     for (int p = tid; p < C * C; p += kThreads) {
@@ -594,7 +641,7 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
         dAq[(p / C) * CP + p % C] = w.dAqk[cc0 + p];
     }
     for (int r = tid; r < C; r += kThreads) {
-        bS[r] = to_f(beta[((size_t)b * d.T + t0 + r) * d.HV + hv]);
+        bS[r] = r < len ? to_f(beta[((size_t)b * d.T + t0 + r) * d.HV + hv]) : 0.f;
         dbS[r] = w.dbv[row0 + r];
     }
     __syncthreads();
@@ -799,8 +846,10 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
             dGr[u] = dKbeta * br * kr * eG + dQh * qr * eG - dKb * kr * eL + br * kr * sA +
                      qr * sQ - kr * (cA + cQ);
             dbr[u] = dKbeta * kr * eG + kr * sA;
-            w.dqh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = d.scale * dqs;
-            w.dkh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = dk;
+            if (r < len) {
+                w.dqh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = d.scale * dqs;
+                w.dkh[tok_idx(d, b, t0 + r, hv, d.HV, K) + c] = dk;
+            }
         }
     }
     __syncthreads();
@@ -828,7 +877,8 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
         for (int c = lane; c < K; c += 32) acc += X[r * KP + c];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) dbeta[((size_t)b * d.T + t0 + r) * d.HV + hv] = from_f<Tin>(acc + dbS[r]);
+        if (lane == 0 && r < len)
+            dbeta[((size_t)b * d.T + t0 + r) * d.HV + hv] = from_f<Tin>(acc + dbS[r]);
     }
     __syncthreads();
     // dg_s = [g_s >= -5] sum_{r >= s} dG_r
@@ -836,8 +886,10 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
         float acc = 0.f;
         for (int r = C - 1; r >= 0; --r) {
             acc += Y[r * KP + c];
-            const size_t ig = tok_idx(d, b, t0 + r, hv, d.HV, K) + c;
-            dg[ig] = from_f<Tin>(to_f(g[ig]) >= kGateFloor ? acc : 0.f);
+            if (r < len) {
+                const size_t ig = tok_idx(d, b, t0 + r, hv, d.HV, K) + c;
+                dg[ig] = from_f<Tin>(to_f(g[ig]) >= kGateFloor ? acc : 0.f);
+            }
         }
     }
 }
@@ -853,7 +905,7 @@ __global__ void group_sum_kernel(Dims d, const float* __restrict__ dqh,
                                  const Tin* __restrict__ k, Tin* __restrict__ dq,
                                  Tin* __restrict__ dk) {
     const int lane = threadIdx.x & 31;
-    const size_t rows = (size_t)d.B * d.T * d.H;
+    const size_t rows = (size_t)d.B * d.Tr * d.H;
     const size_t wstep = (size_t)gridDim.x * (blockDim.x >> 5);
     for (size_t row = blockIdx.x * (size_t)(blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
          row += wstep) {
@@ -917,6 +969,43 @@ __global__ void group_sum_kernel(Dims d, const float* __restrict__ dqh,
     }
 }
 
+// Chunk table of packed variable-length sequences.  Sequence s spans tokens
+// [cu[s], cu[s+1]) and is cut into ceil(len / C) chunks, the last one
+// partial.  cu must start at 0, end at T and not decrease; then the chunks
+// number at most ceil(T / C) + nseq = NT.  Otherwise the error is recorded in
+// g_simt_error (reported by kda_check) and no sequence gets a chunk, so no
+// kernel reads or writes out of bounds.  One block: thread 0 checks cu and
+// forms the prefix of the chunk counts, all threads fill the table.
+__device__ int g_simt_error = 0;
+
+__global__ void varlen_table_kernel(const int* __restrict__ cu, int nseq, int T, int C, int NT,
+                                    int* __restrict__ ctab, int* __restrict__ sfirst) {
+    if (threadIdx.x == 0) {
+        bool ok = cu[0] == 0 && cu[nseq] == T;
+        for (int s = 0; s < nseq; ++s) ok = ok && cu[s + 1] >= cu[s];
+        int total = 0;
+        for (int s = 0; s < nseq; ++s) {
+            sfirst[s] = total;
+            if (ok) total += (cu[s + 1] - cu[s] + C - 1) / C;
+        }
+        sfirst[nseq] = total;
+        if (!ok) atomicCAS(&g_simt_error, 0, 1);
+    }
+    __syncthreads();
+    for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+        const int first = sfirst[s], end = sfirst[s + 1];   // empty unless cu is valid
+        for (int j = first; j < end; ++j) {
+            const int t0 = cu[s] + (j - first) * C;
+            ctab[2 * j] = t0;
+            ctab[2 * j + 1] = min(C, cu[s + 1] - t0);
+        }
+    }
+    for (int j = sfirst[nseq] + threadIdx.x; j < NT; j += blockDim.x) {
+        ctab[2 * j] = 0;
+        ctab[2 * j + 1] = 0;
+    }
+}
+
 template <typename F>
 kda_status set_smem(F* kernel, size_t bytes) {
     if (bytes > 227 * 1024) return KDA_ERR_UNSUPPORTED;
@@ -951,7 +1040,7 @@ kda_status run_forward_parts(const Dims& d, const Ws& w, const void* q, const vo
     if ((st = set_smem(state_fwd_kernel<Tin>, sf)) != KDA_OK) return st;
     {
         TimedLaunch tl("simt_state_fwd", s);
-        state_fwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, d.B * d.HV), kThreads, sf, s>>>(
+        state_fwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, d.NS), kThreads, sf, s>>>(
             d, w, h0, static_cast<Tin*>(o), ht, mode);
     }
     return launch_status();
@@ -991,8 +1080,9 @@ kda_status simt_tail_t(const Dims& d, const Ws& w, const void* q, const void* k,
             static_cast<Tin*>(dbeta));
     }
     if ((st = launch_status()) != KDA_OK) return st;
-    const size_t rows = (size_t)d.B * d.T * d.H;
+    const size_t rows = (size_t)d.B * d.Tr * d.H;
     const int nblk = (int)std::min<size_t>((rows + 7) / 8, 152 * 16);
+    if (nblk == 0) return KDA_OK;
     {
         TimedLaunch tl("simt_group_sum", s);
         group_sum_kernel<Tin><<<nblk, 256, 0, s>>>(d, w.dqh, w.dkh, static_cast<const Tin*>(q),
@@ -1015,7 +1105,7 @@ kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, 
     const int BH = d.B * d.HV;
     {
         TimedLaunch tl("simt_state_bwd", s);
-        state_bwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, BH), kThreads, sb, s>>>(
+        state_bwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, d.NS), kThreads, sb, s>>>(
             d, w, static_cast<const Tin*>(dout), dht, dh0);
     }
     if ((st = launch_status()) != KDA_OK) return st;
@@ -1029,6 +1119,89 @@ kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, 
     return simt_tail_t<Tin>(d, w, q, k, g, beta, dq, dk, dg, dbeta, s);
 }
 }  // namespace
+
+namespace {
+// Kernel dims of a packed variable-length batch: B = 1, T padded to the
+// chunk-table bound ceil(T / C) + nseq chunks, Tr the real token count.
+Dims varlen_dims(const kda_dims& kd, int nseq) {
+    Dims d = make_dims(kd);
+    d.NT = (kd.T + d.C - 1) / d.C + nseq;
+    d.T = d.NT * d.C;
+    d.Tr = kd.T;
+    d.NS = nseq * d.HV;
+    return d;
+}
+
+// The SIMT workspace of the padded batch, then the chunk table [NT][2] and
+// the sequences' first chunks [nseq + 1].
+size_t varlen_carve(const kda_dims& kd, int nseq, int for_bwd, char* base, Ws* w, Dims* out) {
+    Dims d = varlen_dims(kd, nseq);
+    size_t off = carve(d, for_bwd, base, w);
+    int* ctab = base ? reinterpret_cast<int*>(base + off) : nullptr;
+    off += align256((size_t)d.NT * 2 * sizeof(int));
+    int* sfirst = base ? reinterpret_cast<int*>(base + off) : nullptr;
+    off += align256((size_t)(nseq + 1) * sizeof(int));
+    d.ctab = ctab;
+    d.sfirst = sfirst;
+    if (out) *out = d;
+    return off;
+}
+
+kda_status varlen_table(const Dims& d, const int* cu, int nseq, cudaStream_t s) {
+    varlen_table_kernel<<<1, 256, 0, s>>>(cu, nseq, d.Tr, d.C, d.NT, const_cast<int*>(d.ctab),
+                                          const_cast<int*>(d.sfirst));
+    return launch_status();
+}
+}  // namespace
+
+size_t simt_varlen_workspace_bytes(const kda_dims& kd, int nseq, int for_bwd) {
+    return varlen_carve(kd, nseq, for_bwd, nullptr, nullptr, nullptr);
+}
+
+kda_status simt_fwd_varlen(const kda_dims& kd, const int* cu, int nseq, const void* q,
+                           const void* k, const void* v, const void* g, const void* beta,
+                           const float* h0, void* o, float* ht, void* ws, cudaStream_t s) {
+    Ws w;
+    Dims d;
+    varlen_carve(kd, nseq, 0, static_cast<char*>(ws), &w, &d);
+    kda_status st = varlen_table(d, cu, nseq, s);
+    if (st != KDA_OK) return st;
+    if (kd.dtype == KDA_BF16)
+        return run_forward_parts<__nv_bfloat16>(d, w, q, k, v, g, beta, h0, o, ht, 1, s);
+    return run_forward_parts<float>(d, w, q, k, v, g, beta, h0, o, ht, 1, s);
+}
+
+kda_status simt_bwd_varlen(const kda_dims& kd, const int* cu, int nseq, const void* q,
+                           const void* k, const void* v, const void* g, const void* beta,
+                           const float* h0, const void* dout, const float* dht, void* dq,
+                           void* dk, void* dv, void* dg, void* dbeta, float* dh0, void* ws,
+                           cudaStream_t s) {
+    Ws w;
+    Dims d;
+    varlen_carve(kd, nseq, 1, static_cast<char*>(ws), &w, &d);
+    kda_status st = varlen_table(d, cu, nseq, s);
+    if (st != KDA_OK) return st;
+    if (kd.dtype == KDA_BF16)
+        return simt_bwd_t<__nv_bfloat16>(d, w, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg,
+                                         dbeta, dh0, s);
+    return simt_bwd_t<float>(d, w, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0,
+                             s);
+}
+
+kda_status simt_take_error(cudaStream_t s) {
+    int err = 0;
+    if (cudaMemcpyFromSymbolAsync(&err, g_simt_error, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                  s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (err == 0) return KDA_OK;
+    const int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_simt_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return KDA_ERR_CUDA;
+    cudaStreamSynchronize(s);
+    return KDA_ERR_SHAPE;
+}
 
 kda_status group_sum_launch(const kda_dims& kd, const float* dqh, const float* dkh,
                             const void* q, const void* k, void* dq, void* dk, cudaStream_t s) {

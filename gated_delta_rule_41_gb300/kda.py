@@ -62,6 +62,12 @@ def load_library():
         for name in ("kda_chunk_bwd", "kda_chunk_bwd_saved"):
             getattr(lib, name).argtypes = [D] + [P] * 15 + [S, P]
             getattr(lib, name).restype = I
+        lib.kda_chunk_workspace_bytes_varlen.argtypes = [D, I, I]
+        lib.kda_chunk_workspace_bytes_varlen.restype = S
+        lib.kda_chunk_fwd_varlen.argtypes = [D, P, I, P, P, P, P, P, P, P, I, P, P, S, P]
+        lib.kda_chunk_fwd_varlen.restype = I
+        lib.kda_chunk_bwd_varlen.argtypes = [D, P, I] + [P] * 15 + [S, P]
+        lib.kda_chunk_bwd_varlen.restype = I
         lib.kda_recurrent_step.argtypes = [D] + [P] * 8
         lib.kda_recurrent_step.restype = I
         lib.kda_check.argtypes = [P]
@@ -199,6 +205,65 @@ def chunk_kda_bwd(q, k, v, g, beta, do, dht=None, scale=None, initial_state=None
             _ptr(grads["dv"]), _ptr(grads["dg"]), _ptr(grads["dbeta"]), _ptr(grads.get("dh0")),
             _ptr(ws), nws, _stream(stream))
     _raise(st, what)
+    return grads
+
+
+def _check_cu(cu_seqlens):
+    if (cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1
+            or not cu_seqlens.is_contiguous()):
+        raise KdaError(1, "cu_seqlens must be a contiguous 1-D int32 CUDA tensor")
+    return cu_seqlens.numel() - 1
+
+
+def chunk_kda_fwd_varlen(q, k, v, g, beta, cu_seqlens, scale=None, initial_state=None,
+                         output_final_state=False, chunk_size=64, impl="auto", workspace=None,
+                         out=None, final_state=None, stream=None, use_qk_l2norm_in_kernel=False):
+    """Forward over sequences packed along T: q, k [1,T,H,K]; v [1,T,HV,V];
+    g [1,T,HV,K]; beta [1,T,HV]; ``cu_seqlens`` int32 [N+1] on the device.
+    ``initial_state`` / the final state are [N,HV,K,V].  Returns (o, ht)."""
+    lib = load_library()
+    _check_dev(q, k, v, g, beta, initial_state)
+    nseq = _check_cu(cu_seqlens)
+    dims = make_dims(q, v, chunk_size, scale, impl, use_qk_l2norm_in_kernel)
+    o = torch.empty_like(v) if out is None else out
+    ht = None
+    if output_final_state:
+        ht = (torch.empty(nseq, dims.HV, dims.K, dims.V, dtype=torch.float32, device=q.device)
+              if final_state is None else final_state)
+    need = int(lib.kda_chunk_workspace_bytes_varlen(ctypes.byref(dims), nseq, 0))
+    ws = workspace if (workspace is not None and workspace.numel() >= need) else \
+        torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.kda_chunk_fwd_varlen(ctypes.byref(dims), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k),
+                                  _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(o),
+                                  int(output_final_state), _ptr(ht), _ptr(ws), need,
+                                  _stream(stream))
+    _raise(st, "kda_chunk_fwd_varlen")
+    return o, ht
+
+
+def chunk_kda_bwd_varlen(q, k, v, g, beta, do, cu_seqlens, dht=None, scale=None,
+                         initial_state=None, chunk_size=64, impl="auto", workspace=None,
+                         grads=None, stream=None, use_qk_l2norm_in_kernel=False):
+    """Backward of chunk_kda_fwd_varlen.  Returns dict dq, dk, dv, dg, dbeta,
+    dh0 (dh0 [N,HV,K,V] when ``initial_state`` is given)."""
+    lib = load_library()
+    _check_dev(q, k, v, g, beta, do, dht, initial_state)
+    nseq = _check_cu(cu_seqlens)
+    dims = make_dims(q, v, chunk_size, scale, impl, use_qk_l2norm_in_kernel)
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
+                     dh0=(torch.empty(nseq, dims.HV, dims.K, dims.V, dtype=torch.float32,
+                                      device=q.device) if initial_state is not None else None))
+    need = int(lib.kda_chunk_workspace_bytes_varlen(ctypes.byref(dims), nseq, 1))
+    ws = workspace if (workspace is not None and workspace.numel() >= need) else \
+        torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.kda_chunk_bwd_varlen(ctypes.byref(dims), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k),
+                                  _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(do),
+                                  _ptr(dht), _ptr(grads["dq"]), _ptr(grads["dk"]),
+                                  _ptr(grads["dv"]), _ptr(grads["dg"]), _ptr(grads["dbeta"]),
+                                  _ptr(grads.get("dh0")), _ptr(ws), need, _stream(stream))
+    _raise(st, "kda_chunk_bwd_varlen")
     return grads
 
 

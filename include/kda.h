@@ -150,6 +150,40 @@ kda_status kda_chunk_bwd_saved(const kda_dims* dims, const void* q, const void* 
                                void* dg, void* dbeta, float* dh0, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* Packed variable-length sequences.  The pages run one length per batch
+ * (the DM-KDAGQA-1.7B-SD card notes that its KDA layers have no padding
+ * mask); these entry points let a batch of unequal sequences be packed
+ * along T instead, each sequence scanned on its own.
+ *   dims        B must be 1; T = the total token count (any T >= 0, no
+ *               multiple of chunk_size needed); impl AUTO or SIMT (the fp32
+ *               CUDA-core kernels run; TCGEN05 returns KDA_ERR_UNSUPPORTED).
+ *   cu_seqlens  DEVICE int32 [num_seqs + 1]: sequence s is tokens
+ *               [cu_seqlens[s], cu_seqlens[s+1]); it must start at 0, end at
+ *               T and not decrease (empty sequences allowed).  It is read on
+ *               the device only; a violation is reported by kda_check as
+ *               KDA_ERR_SHAPE, and then no sequence is scanned (the final
+ *               states are the initial ones, o is not written) and nothing is
+ *               accessed out of bounds.
+ *   h0, ht, dht, dh0  per sequence: [num_seqs][HV][K][V] f32.
+ *   Other arguments, layouts and results are those of kda_chunk_fwd /
+ *   kda_chunk_bwd with B = 1, and the workspace must hold
+ *   kda_chunk_workspace_bytes_varlen bytes (0 on invalid dims).  Each
+ *   sequence's last chunk may be partial: its rows past the sequence end enter
+ *   as q = k = v = 0, g = 0, beta = 0 (which leaves the state unchanged) and
+ *   are not written. */
+size_t kda_chunk_workspace_bytes_varlen(const kda_dims* dims, int num_seqs, int for_bwd);
+kda_status kda_chunk_fwd_varlen(const kda_dims* dims, const int* cu_seqlens, int num_seqs,
+                                const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, const float* h0, void* o,
+                                int output_final_state, float* ht, void* workspace,
+                                size_t workspace_bytes, void* stream);
+kda_status kda_chunk_bwd_varlen(const kda_dims* dims, const int* cu_seqlens, int num_seqs,
+                                const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, const float* h0, const void* dout,
+                                const float* dht, void* dq, void* dk, void* dv, void* dg,
+                                void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
 /* One decode token per head, state updated in place (K3 row L6).
  * dims->T is ignored; q, k [B,H,K]; v, o [B,HV,V]; g [B,HV,K]; beta [B,HV]
  * (dtype); state [B,HV,K,V] f32, read and overwritten. */
@@ -186,7 +220,8 @@ kda_status kda_chunk_fwd_noalloc(const kda_dims* dims, const void* q, const void
 
 /* Synchronise `stream`, then report (and clear) any error a kernel recorded on
  * the device since the last check: KDA_ERR_TIMEOUT for an expired bounded
- * wait, KDA_ERR_CUDA for a runtime error. */
+ * wait, KDA_ERR_SHAPE for cu_seqlens that break the rules of the varlen
+ * entry points, KDA_ERR_CUDA for a runtime error. */
 kda_status kda_check(void* stream);
 
 /* Diagnostics: per-kernel device timing.  kda_timing_enable(1) clears the
