@@ -185,15 +185,17 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* base, int v, int col0, c
 // K-major operand tile, then arrive on `bar_tile` (the products that read
 // the tile may start).
 __device__ __forceinline__ void chain_state_tile(uint32_t tS, uint8_t* tile, bool first,
-                                                 const float* init, int v, int half,
+                                                 const float* init, int D, int v, int half,
                                                  uint64_t* bar_tile, float (&r0)[32],
                                                  float (&r1)[32]) {
     const int k0 = 64 * half;
     if (first) {
+        // init is [D][D]: rows and columns at D and beyond are zero
+        const bool on = init && v < D && k0 < D;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            r0[i] = init ? init[(size_t)(k0 + i) * kD + v] : 0.f;
-            r1[i] = init ? init[(size_t)(k0 + 32 + i) * kD + v] : 0.f;
+            r0[i] = on ? init[(size_t)(k0 + i) * D + v] : 0.f;
+            r1[i] = on ? init[(size_t)(k0 + 32 + i) * D + v] : 0.f;
         }
     } else {
         tmem_ld32_nw(tS + k0, r0);
@@ -270,6 +272,7 @@ __device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile, con
 
 struct ChainArgs {
     int B, T, HV, NT;
+    int D;              // K = V of the tensors (64 or 128); the kernel works at 128
     const float* gam;   // [BH*NT][128]
     const float* h0;    // [BH][K][V] or null
     __nv_bfloat16* o;   // [B,T,HV,V]
@@ -349,7 +352,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     const int z = b * a.T + (j - 1) * kC;
                     const uint8_t* tile = smem + sj * STAGE_BYTES + OFF_U;
                     tma_store_3d(&tm_o, tile, 0, hv, z);
-                    tma_store_3d(&tm_o, tile + 8192, 64, hv, z);
+                    if (a.D > 64) tma_store_3d(&tm_o, tile + 8192, 64, hv, z);
                     bulk_commit_group();
                     bulk_wait_read_all();
                 }
@@ -491,7 +494,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             const int s = n & 1;
             float r0[32], r1[32];
             chain_state_tile(tmem + lane_off + TM_S, smem + OFF_S + s * S_TILE, n == 0,
-                             a.h0 ? a.h0 + (size_t)bh * kD * kD : nullptr, v, half, bar_S, r0, r1);
+                             a.h0 ? a.h0 + (size_t)bh * a.D * a.D : nullptr, a.D, v, half, bar_S,
+                             r0, r1);
             if (!wait_bar_warp(&full[s], (n >> 1) & 1, 7)) return false;
             chain_state_rescale(tmem + lane_off + TM_S,
                                 reinterpret_cast<const float*>(smem + OFF_GAM + s * 512), half,
@@ -528,11 +532,11 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             }
         };
         auto o_out = [&](int m) {
-            if (q >= 2) return;
+            if (q >= 2 || half * 64 >= a.D) return;
             float x1[32];
             o_rows(m, r, x1);
             __nv_bfloat16* op =
-                a.o + (((size_t)b * a.T + (size_t)m * kC + v) * a.HV + hv) * kD + half * 64;
+                a.o + (((size_t)b * a.T + (size_t)m * kC + v) * a.HV + hv) * a.D + half * 64;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 float e0[8], e1v[8];
@@ -580,9 +584,10 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 #pragma unroll 1
                 for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     tmem_ld32(tmem + lane_off + TM_S + cb * 32, r);
-                    float* hp = a.ht + ((size_t)bh * kD + cb * 32) * kD + v;
+                    if (v >= a.D || cb * 32 >= a.D) continue;   // [D][D]
+                    float* hp = a.ht + ((size_t)bh * a.D + cb * 32) * a.D + v;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) hp[(size_t)i * kD] = r[i];
+                    for (int i = 0; i < 32; ++i) hp[(size_t)i * a.D] = r[i];
                 }
             }
         }
@@ -620,6 +625,7 @@ constexpr uint32_t TM2_S = 0, TM2_DD = 128, TM2_COLS = 256;
 
 struct ChainBwdArgs {
     int B, T, HV, NT;
+    int D;              // K = V of the tensors (64 or 128); the kernel works at 128
     const float* gam;
     const float* dht;            // [BH][K][V] or null
     float* dh0;                  // [BH][K][V] or null
@@ -721,7 +727,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 if (n >= 2) {
                     const int row2 = row - 2 * kC, crow2 = crow - 2, trow2 = trow - 2 * kC;
                     tma_prefetch_3d(&tm_do, 0, hv, trow2);
-                    tma_prefetch_3d(&tm_do, 64, hv, trow2);
+                    if (a.D > 64) tma_prefetch_3d(&tm_do, 64, hv, trow2);
                     tma_prefetch_2d(&tm_q, 0, row2);
                     tma_prefetch_2d(&tm_q, 64, row2);
                     tma_prefetch_2d(&tm_w, 0, row2);
@@ -813,7 +819,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             const int s = i & 1;
             float r0[32], r1[32];
             chain_state_tile(tmem + lane_off + TM2_S, smem + OFF_S + s * S_TILE, i == 0,
-                             a.dht ? a.dht + (size_t)bh * kD * kD : nullptr, v, half, bar_S, r0,
+                             a.dht ? a.dht + (size_t)bh * a.D * a.D : nullptr, a.D, v, half, bar_S, r0,
                              r1);
             if (!wait_bar_warp(&full[s], (i >> 1) & 1, 17)) return false;
             chain_state_rescale(tmem + lane_off + TM2_S,
@@ -840,9 +846,10 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 #pragma unroll 1
                 for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     tmem_ld32(tmem + lane_off + TM2_S + cb * 32, r);
-                    float* hp = a.dh0 + ((size_t)bh * kD + cb * 32) * kD + v;
+                    if (v >= a.D || cb * 32 >= a.D) continue;   // [D][D]
+                    float* hp = a.dh0 + ((size_t)bh * a.D + cb * 32) * a.D + v;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) hp[(size_t)j * kD] = r[j];
+                    for (int j = 0; j < 32; ++j) hp[(size_t)j * a.D] = r[j];
                 }
             }
         }
@@ -879,6 +886,7 @@ constexpr int kGradThreads = 256;
 
 struct GradArgs {
     int T, HV, NT, BH;
+    int D;              // V of the tensors (64 or 128); the kernel works at 128
     const __nv_bfloat16* beta;  // [B,T,HV]
     __nv_bfloat16* dv;          // [B,T,HV,V]
     float *dQh, *dKb, *dgam, *dTv, *dbv;
@@ -1112,7 +1120,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             for (int j = 0; j < 32; ++j) {
                 const int m = cb * 32 + j;
                 const float bt = beta_s[m];
-                a.dv[(((size_t)trow + m) * a.HV + hv) * kD + l] = __float2bfloat16_rn(bt * r[j]);
+                if (l < a.D) a.dv[(((size_t)trow + m) * a.HV + hv) * a.D + l] = __float2bfloat16_rn(bt * r[j]);
                 const uint32_t voff = G_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
                 r[j] *= __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
             }
@@ -1209,6 +1217,7 @@ __host__ __device__ constexpr uint32_t right_col(int R) { return 8u * (uint32_t)
 
 struct IntraArgs {
     int T, H, HV, NT, BH;
+    int D;                     // K = V of the tensors (64 or 128); the kernel works at 128
     float scale;
     int qkn;                   // L2-normalise the q and k tiles first
     const __nv_bfloat16* beta;
@@ -1303,13 +1312,15 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         int trow, hv, h;
         coords(ch, trow, hv, h);
         tma_prefetch_3d(&tm_k, 0, h, trow);
-        tma_prefetch_3d(&tm_k, 64, h, trow);
         tma_prefetch_3d(&tm_q, 0, h, trow);
-        tma_prefetch_3d(&tm_q, 64, h, trow);
         tma_prefetch_3d(&tm_g, 0, hv, trow);
-        tma_prefetch_3d(&tm_g, 64, hv, trow);
         tma_prefetch_3d(&tm_v, 0, hv, trow);
-        tma_prefetch_3d(&tm_v, 64, hv, trow);
+        if (a.D > 64) {   // at D = 64 the upper boxes lie past the rows
+            tma_prefetch_3d(&tm_k, 64, h, trow);
+            tma_prefetch_3d(&tm_q, 64, h, trow);
+            tma_prefetch_3d(&tm_g, 64, hv, trow);
+            tma_prefetch_3d(&tm_v, 64, hv, trow);
+        }
     };
     auto load_beta = [&](int ch) {
         int trow, hv, h;
@@ -1859,6 +1870,7 @@ __host__ __device__ constexpr uint32_t lb_dkb_row(int r) {
 
 struct LocalTcArgs {
     int T, H, HV, NT, G, BH;
+    int D;              // K of the tensors (64 or 128); the kernel works at 128
     float scale;
     int qkn;   // L2-normalise the q and k tiles first; dq, dk then go out as fp32
     const float *dQh, *dKb, *dTv, *dgam, *dbv;
@@ -2366,8 +2378,10 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             dG[u] = fmaf(qr, dqs, kr * (bp - l - caq));
             lastp = fmaf(kr, l, lastp);
             dbps[u] = kr * pb;
-            const size_t io = (((size_t)trow + t) * a.HV + hv) * kD + c;
-            if (a.G == 1 && !a.qkn) {
+            const size_t io = (((size_t)trow + t) * a.HV + hv) * a.D + c;
+            if (c >= a.D) {
+                // a key channel past the tensors' width: zero-filled, not written
+            } else if (a.G == 1 && !a.qkn) {
                 a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
                 a.dk[io] = __float2bfloat16_rn(dkv);
             } else {
@@ -2415,8 +2429,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int u = 15; u >= 0; --u) {
             run += dG[u];
             const int t = 16 * R + u;
-            const size_t ig = (((size_t)trow + t) * a.HV + hv) * kD + c;
-            a.dg[ig] = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
+            const size_t ig = (((size_t)trow + t) * a.HV + hv) * a.D + c;
+            if (c < a.D) a.dg[ig] = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
         }
     }
     if (tid < kC)
@@ -2493,11 +2507,14 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
 
 // 3-D bf16 map over a token tensor [B*T][heads][128] (a per-head tile of 64
 // tokens is a box {64 columns, 1 head, 64 tokens}), 128B swizzle.
-bool make_map_tok(CUtensorMap* m, const void* ptr, uint64_t BT, uint64_t heads) {
+// The row width D (64 or 128) is the tensor's own: with D = 64 the box at
+// column 64 lies wholly past the row, so TMA loads fill it with zeros and
+// stores skip it, and the 128-wide kernels see zero channels there.
+bool make_map_tok(CUtensorMap* m, const void* ptr, uint64_t BT, uint64_t heads, uint64_t D) {
     EncodeFn enc = get_encoder();
     if (!enc) return false;
-    cuuint64_t dims[3] = {kD, heads, BT};
-    cuuint64_t strides[2] = {kD * 2, heads * kD * 2};
+    cuuint64_t dims[3] = {D, heads, BT};
+    cuuint64_t strides[2] = {D * 2, heads * D * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
@@ -2512,6 +2529,15 @@ struct TcWs {
     __nv_bfloat16 *h2, *d2, *dh2, *dd2;              // backward only
 };
 
+// The tensor-core kernels work at K = V = 128 whatever the tensors' width
+// (64 or 128): the fp32 arrays they share with the SIMT carve are laid out
+// at that width.
+kda_dims tc_wide(const kda_dims& d) {
+    kda_dims p = d;
+    p.K = p.V = kD;
+    return p;
+}
+
 size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     const size_t BH = (size_t)d.B * d.HV, T = d.T, NT = d.T / kC;
     size_t off = 0;
@@ -2522,7 +2548,7 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     };
     auto bf = [&](size_t elems) { return reinterpret_cast<__nv_bfloat16*>(take(elems * 2)); };
     TcWs x{};
-    x.simt = take(simt_workspace_bytes(d, for_bwd));
+    x.simt = take(simt_workspace_bytes(tc_wide(d), for_bwd));
     x.W2 = bf(BH * T * kD);
     x.Q2 = bf(BH * T * kD);
     x.U2 = bf(BH * T * kD);
@@ -2548,13 +2574,13 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
                         const void* v, const void* g, const void* beta, bool keep_T,
                         cudaStream_t s, float** gam_out) {
     SimtWsPtrs p;
-    simt_ws_ptrs(d, 0, w.simt, &p);
+    simt_ws_ptrs(tc_wide(d), 0, w.simt, &p);
     const int BH = d.B * d.HV, NT = d.T / kC;
     const uint64_t BT = (uint64_t)d.B * d.T;
     const uint64_t rows = (uint64_t)BH * d.T;
     CUtensorMap mk, mq, mg, mv, mw2, mq2, mu2, mkb2, ma2;
-    if (!make_map_tok(&mk, k, BT, d.H) || !make_map_tok(&mq, q, BT, d.H) ||
-        !make_map_tok(&mg, g, BT, d.HV) || !make_map_tok(&mv, v, BT, d.HV) ||
+    if (!make_map_tok(&mk, k, BT, d.H, d.K) || !make_map_tok(&mq, q, BT, d.H, d.K) ||
+        !make_map_tok(&mg, g, BT, d.HV, d.K) || !make_map_tok(&mv, v, BT, d.HV, d.V) ||
         !make_map(&mw2, w.W2, rows, kD, 64, 64, true) ||
         !make_map(&mq2, w.Q2, rows, kD, 64, 64, true) ||
         !make_map(&mu2, w.U2, rows, kD, 64, 64, true) ||
@@ -2567,6 +2593,7 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     a.HV = d.HV;
     a.NT = NT;
     a.BH = BH;
+    a.D = d.K;
     a.scale = d.scale;
     a.qkn = d.qk_l2norm != 0;
     a.beta = static_cast<const __nv_bfloat16*>(beta);
@@ -2593,8 +2620,8 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
     const uint64_t BT = (uint64_t)d.B * d.T;
     const uint64_t rows = (uint64_t)d.B * d.HV * d.T;  // [BH*T] and [BH*NT*64] alike
     CUtensorMap mk, mq, mg, mdw, mt, mtl, mda;
-    if (!make_map_tok(&mk, k, BT, d.H) || !make_map_tok(&mq, q, BT, d.H) ||
-        !make_map_tok(&mg, g, BT, d.HV) || !make_map(&mdw, p.dWm, rows, kD, 64, 64, true) ||
+    if (!make_map_tok(&mk, k, BT, d.H, d.K) || !make_map_tok(&mq, q, BT, d.H, d.K) ||
+        !make_map_tok(&mg, g, BT, d.HV, d.K) || !make_map(&mdw, p.dWm, rows, kD, 64, 64, true) ||
         !make_map(&mt, w.T2, rows, kC, 64, 64, true) ||
         !make_map(&mtl, w.Tlo2, rows, kC, 64, 64, true) ||
         !make_map(&mda, p.dAqk, rows, kC, 64, 16, true))
@@ -2606,6 +2633,7 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
     a.NT = d.T / kC;
     a.G = d.HV / d.H;
     a.BH = d.B * d.HV;
+    a.D = d.K;
     a.scale = d.scale;
     a.qkn = d.qk_l2norm != 0;
     a.dQh = p.dQh;
@@ -2659,13 +2687,14 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         return KDA_ERR_CUDA;
     // the output o [B*T][HV][V] in [64 t][64 v] boxes (a dummy map over W when
     // there is no output)
-    if (!(o ? make_map_tok(&mo, o, (uint64_t)d.B * d.T, d.HV) : make_map_tok(&mo, w.W2, rows, 1)))
+    if (!(o ? make_map_tok(&mo, o, (uint64_t)d.B * d.T, d.HV, d.V) : make_map_tok(&mo, w.W2, rows, 1, kD)))
         return KDA_ERR_CUDA;
     ChainArgs args;
     args.B = d.B;
     args.T = d.T;
     args.HV = d.HV;
     args.NT = NT;
+    args.D = d.K;
     args.gam = gam;
     args.h0 = h0;
     args.o = static_cast<__nv_bfloat16*>(o);
@@ -2687,8 +2716,11 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
 
 }  // namespace
 
+// K = V = 128, or K = V = 64 run at 128 with the upper channels zero (the
+// tensor maps fill them on load and skip them on store; the plain global
+// accesses of states and gradients use the tensors' own width).
 bool tc_supported(const kda_dims& d) {
-    return d.dtype == KDA_BF16 && d.K == kD && d.V == kD && d.chunk_size == kC &&
+    return d.dtype == KDA_BF16 && d.K == d.V && (d.K == kD || d.K == 64) && d.chunk_size == kC &&
            get_encoder() != nullptr;
 }
 
@@ -2717,7 +2749,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     kda_status st = KDA_OK;
     if (from_saved) {
         SimtWsPtrs p0;
-        simt_ws_ptrs(d, 0, w.simt, &p0);  // where the intra kernel left gam
+        simt_ws_ptrs(tc_wide(d), 0, w.simt, &p0);  // where the intra kernel left gam
         gam = p0.gam;
     } else {
         if ((st = run_intra_tc(d, w, q, k, v, g, beta, true, s, &gam)) != KDA_OK) return st;
@@ -2731,7 +2763,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     {
         CUtensorMap mdo, mq, mw, mk, ma, mdh, mddst;
         if (!make_map(&mdh, w.dh2, (uint64_t)BH * NT * kD, kD, 64, 128, true) ||
-            !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
+            !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV, d.V) ||
             !make_map(&mq, w.Q2, rows, kD, 64, 64, true) ||
             !make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
             !make_map(&mk, w.Kb2, rows, kD, 64, 64, true) ||
@@ -2743,6 +2775,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.T = d.T;
         a.HV = d.HV;
         a.NT = NT;
+        a.D = d.K;
         a.gam = gam;
         a.dht = dht;
         a.dh0 = dh0;
@@ -2758,21 +2791,22 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     // contractions over V
     {
         SimtWsPtrs p;
-        simt_ws_ptrs(d, 1, w.simt, &p);
+        simt_ws_ptrs(tc_wide(d), 1, w.simt, &p);
         CUtensorMap mh, mdh, mdo, mdd, md, mv, mt;
         const uint64_t srows = (uint64_t)BH * NT * kD;
         if (!make_map(&mh, w.h2, srows, kD, 64, 128, true) ||
             !make_map(&mdh, w.dh2, srows, kD, 64, 128, true) ||
-            !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV) ||
+            !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV, d.V) ||
             !make_map(&mdd, w.dd2, rows, kD, 64, 64, true) ||
             !make_map(&md, w.d2, srows, kC, 64, 128, true) ||
-            !make_map_tok(&mv, v, (uint64_t)d.B * d.T, d.HV) ||
+            !make_map_tok(&mv, v, (uint64_t)d.B * d.T, d.HV, d.V) ||
             !make_map(&mt, w.T2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
             return KDA_ERR_CUDA;
         GradArgs a;
         a.T = d.T;
         a.HV = d.HV;
         a.NT = NT;
+        a.D = d.V;
         a.BH = BH;
         a.beta = static_cast<const __nv_bfloat16*>(beta);
         a.dv = static_cast<__nv_bfloat16*>(dv);
@@ -2793,7 +2827,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     }
     if ((st = launch_status()) != KDA_OK) return st;
     SimtWsPtrs p;
-    simt_ws_ptrs(d, 1, w.simt, &p);
+    simt_ws_ptrs(tc_wide(d), 1, w.simt, &p);
     if ((st = run_local_bwd_tc(d, w, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
     if (d.HV == d.H && !d.qk_l2norm) return KDA_OK;
     return group_sum_launch(d, p.dqh, p.dkh, q, k, dq, dk, s);

@@ -72,7 +72,8 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
  *   KDA_IMPL_AUTO     tensor-core path when it supports the sizes, else SIMT.
  *   KDA_IMPL_SIMT     fp32 CUDA-core kernels; any K, V <= 128, chunk 16/32/64,
  *                     f32 or bf16 inputs.
- *   KDA_IMPL_TCGEN05  tcgen05/TMEM tensor-core kernels; bf16, K = V = 128,
+ *   KDA_IMPL_TCGEN05  tcgen05/TMEM tensor-core kernels; bf16, K = V = 128 or
+ *                     K = V = 64 (run at 128 with the upper channels zero),
  *                     chunk 64.  KDA_ERR_UNSUPPORTED otherwise.  The
  *                     tensor-core backward does not take dht (it keeps the
  *                     chunk states as bf16, which an O(1) final-state gradient

@@ -78,8 +78,13 @@ def test_fp32_gva_chunks_with_h0(impl, chunk):
 
 @pytest.mark.parametrize("impl", IMPLS)
 def test_small_bf16_full(impl):
+    """bf16 B4 T512 H8 K = V = 64 with an initial state; on the tensor cores
+    (K = V = 64 run at 128 with zero-filled upper channels) without the
+    upstream final-state gradient, which their backward does not take."""
     w = I.SMALL_BF16
     inp = I.make_chunk_inputs(w)
+    if impl == "tcgen05":
+        inp["dht"] = None
     res = run_gpu(inp, w, impl)
     compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
 
@@ -142,16 +147,17 @@ def test_saved_backward_rejects_other_dims():
                           t["beta"][:, :64], t["do"][:, :64], saved=saved)
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("saved", [False, True])
 @pytest.mark.parametrize("B,T,H,HV", [(1, 64, 1, 1), (1, 128, 1, 1), (2, 192, 1, 4),
                                       (1, 256, 1, 2), (1, 320, 2, 2)])
-def test_tcgen05_chunk_counts_and_groups(B, T, H, HV, saved):
+def test_tcgen05_chunk_counts_and_groups(B, T, H, HV, saved, D):
     """Tensor-core path on one chunk, odd and even chunk counts (the state
     passes alternate two state tiles and two stages) and GVA groups of 2 and
     4, with an initial state and the final state, stateless and saved
-    backward."""
-    w = I.Workload("tc_shapes", B, T, H, HV, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
-                   h0_std=0.1, seed=31 + T + HV)
+    backward; K = V = 128, and 64 (zero-filled upper channels)."""
+    w = I.Workload("tc_shapes", B, T, H, HV, D, D, 64, torch.bfloat16, g_sigma=2.0,
+                   h0_std=0.1, seed=31 + T + HV + D)
     inp = I.make_chunk_inputs(w)
     t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
     if saved:
@@ -184,7 +190,7 @@ def test_clamp_active_below_minus_five(impl):
     """Gates far below -5 reach the kernel: it must clamp them and pass no
     gradient through them (g == -5 exactly still passes)."""
     w = I.Workload("clamp", 2, 128, 2, 2, 64, 64, 64, torch.bfloat16, g_mu=3.0, g_sigma=3.0,
-                   h0_std=0.2, dht=True, seed=24)
+                   h0_std=0.2, dht=impl != "tcgen05", seed=24)
     inp = I.make_chunk_inputs(w, g_floor=None)
     g = inp["g"].float()
     g[:, :8] = -5.0  # exact boundary values
@@ -224,14 +230,15 @@ def test_tcgen05_clamp_below_minus_five(saved):
     assert torch.all(res["dg"].float().cpu()[below] == 0)
 
 
-@pytest.mark.parametrize("impl,saved", [("simt", False), ("tcgen05", False), ("tcgen05", True)])
+@pytest.mark.parametrize("impl,saved,D", [("simt", False, 128), ("tcgen05", False, 128),
+                                          ("tcgen05", True, 128), ("tcgen05", True, 64)])
 @pytest.mark.parametrize("H,HV", [(2, 2), (1, 2)])
-def test_qk_l2norm_in_kernel(impl, saved, H, HV):
+def test_qk_l2norm_in_kernel(impl, saved, D, H, HV):
     """The kernels L2-normalise raw q and k themselves (the K3 README's "q/k
     L2-norm" variant): outputs are the scan of the normalised q, k, and dq, dk
     are gradients with respect to the raw q, k (after the GVA group sum)."""
-    w = I.Workload("qkn", 2, 192, H, HV, 128, 128, 64, torch.bfloat16, g_sigma=2.0, h0_std=0.1,
-                   seed=51 + H + HV)
+    w = I.Workload("qkn", 2, 192, H, HV, D, D, 64, torch.bfloat16, g_sigma=2.0, h0_std=0.1,
+                   seed=51 + H + HV + D)
     inp = I.make_chunk_inputs(w, normalize_qk=False)
     t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
     out = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
@@ -344,6 +351,7 @@ def test_long_context_full_size_sampled_heads(impl):
 
 
 @pytest.mark.parametrize("impl,K,dtype", [("simt", 64, torch.bfloat16), ("simt", 64, torch.float32),
+                                           ("tcgen05", 64, torch.bfloat16),
                                            ("tcgen05", 128, torch.bfloat16)])
 def test_96_heads_sampled(impl, K, dtype):
     """H = HV = 96 heads, head dim 64 (CUDA-core path) and 128 (tensor cores),
