@@ -279,7 +279,79 @@ struct ChainArgs {
     float* ht;          // [BH][K][V] or null
     __nv_bfloat16* h_out;  // [BH][NT][V][K] or null (states at chunk starts, transposed, bf16)
     __nv_bfloat16* delta_out;  // [BH][NT][V][C] or null (transposed); set iff h_out is
+    // Segmented scan of long sequences (nseg >= 3; 0: one CTA per head over
+    // all chunks).  The chunks are cut into nseg segments of seglen (the last
+    // may be shorter).  pass 1: CTAs [0, BH) run segment 0 in full (its end
+    // state into sbuf[.][1]); CTAs [BH, BH (nseg-1)) run segments 1..nseg-2
+    // from zero, their end states into zbuf; CTAs [BH (nseg-1), BH (2 nseg-3))
+    // run the same segments from the identity with U = 0, their transition
+    // matrices into mbuf.  pass 3: CTAs [0, BH (nseg-1)) run segments
+    // 1..nseg-1 in full from sbuf (the last one's end state into ht).
+    // Buffers: [BH][nseg][K][V] fp32 at the tensors' width; ident [K][V].
+    int nseg, seglen, pass;
+    float *sbuf, *zbuf, *mbuf;
+    const float* ident;
 };
+
+// The work of one chain CTA: head bh walks chunks n0 .. n0 + cnt - 1 from
+// h0 ([D][D], null: zero) with U taken as zero if zero_u, writes o if
+// write_o, and its end state to ht ([D][D], null: none).
+struct ChainJob {
+    int bh, n0, cnt;
+    bool write_o, zero_u;
+    const float* h0;
+    float* ht;
+};
+
+__device__ __forceinline__ ChainJob chain_job(const ChainArgs& a, int c) {
+    const int BH = a.B * a.HV;
+    const size_t S = (size_t)a.D * a.D;
+    ChainJob j;
+    j.zero_u = false;
+    if (a.nseg == 0) {
+        j.bh = c;
+        j.n0 = 0;
+        j.cnt = a.NT;
+        j.write_o = a.o != nullptr;
+        j.h0 = a.h0 ? a.h0 + (size_t)c * S : nullptr;
+        j.ht = a.ht ? a.ht + (size_t)c * S : nullptr;
+        return j;
+    }
+    auto seg = [&](int p) {
+        j.n0 = p * a.seglen;
+        j.cnt = min(a.seglen, a.NT - j.n0);
+    };
+    auto buf = [&](float* base, int p) { return base + ((size_t)j.bh * a.nseg + p) * S; };
+    j.bh = c % BH;
+    if (a.pass == 1) {
+        const int role = c / BH;   // 0: segment 0; 1..nseg-2: Z; nseg-1..2 nseg-4: M
+        if (role == 0) {
+            seg(0);
+            j.write_o = true;
+            j.h0 = a.h0 ? a.h0 + (size_t)j.bh * S : nullptr;
+            j.ht = buf(a.sbuf, 1);
+        } else if (role <= a.nseg - 2) {
+            seg(role);
+            j.write_o = false;
+            j.h0 = nullptr;
+            j.ht = buf(a.zbuf, role);
+        } else {
+            const int p = role - (a.nseg - 2);
+            seg(p);
+            j.write_o = false;
+            j.zero_u = true;
+            j.h0 = a.ident;
+            j.ht = buf(a.mbuf, p);
+        }
+    } else {
+        const int p = c / BH + 1;
+        seg(p);
+        j.write_o = true;
+        j.h0 = buf(a.sbuf, p);
+        j.ht = p == a.nseg - 1 && a.ht ? a.ht + (size_t)j.bh * S : nullptr;
+    }
+    return j;
+}
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
@@ -305,9 +377,12 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 13);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
+    const ChainJob job = chain_job(a, blockIdx.x);
+    const int bh = job.bh;
     const int b = bh / a.HV, hv = bh % a.HV;
-    const int NT = a.NT;
+    const int NT = job.cnt;      // chunks of this CTA: n0 .. n0 + NT - 1
+    const int n0 = job.n0;
+    const bool write_o = job.write_o && a.o;
 
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1);
@@ -348,8 +423,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             auto drain_o = [&](int j) -> bool {
                 const int sj = j & 1;
                 if (!wait_bar(&bar_o[sj], (j >> 1) & 1, 21)) return false;
-                if (a.o && j >= 1) {
-                    const int z = b * a.T + (j - 1) * kC;
+                if (write_o && j >= 1) {
+                    const int z = b * a.T + (n0 + j - 1) * kC;
                     const uint8_t* tile = smem + sj * STAGE_BYTES + OFF_U;
                     tma_store_3d(&tm_o, tile, 0, hv, z);
                     if (a.D > 64) tma_store_3d(&tm_o, tile + 8192, 64, hv, z);
@@ -364,16 +439,19 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 if (!wait_bar(&empty[s], ((n >> 1) & 1) ^ 1, 1)) break;
                 if (n >= 2 && !drain_o(n - 2)) break;
                 uint8_t* st = smem + s * STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[s], STAGE_TX);
-                const int row = bh * a.T + n * kC;
-                const int crow = bh * NT + n;
+                // a CTA that writes no output reads neither Qh nor Aqk
+                mbar_arrive_expect_tx(&full[s], write_o ? STAGE_TX : STAGE_TX - 16384 - 8192);
+                const int row = bh * a.T + (n0 + n) * kC;
+                const int crow = bh * a.NT + n0 + n;
                 tma_load_2d(st + OFF_W, &tm_w, &full[s], 0, row);
                 tma_load_2d(st + OFF_W + 8192, &tm_w, &full[s], 64, row);
-                tma_load_2d(st + OFF_Q, &tm_q, &full[s], 0, row);
-                tma_load_2d(st + OFF_Q + 8192, &tm_q, &full[s], 64, row);
+                if (write_o) {
+                    tma_load_2d(st + OFF_Q, &tm_q, &full[s], 0, row);
+                    tma_load_2d(st + OFF_Q + 8192, &tm_q, &full[s], 64, row);
+                    tma_load_2d(st + OFF_AQK, &tm_aqk, &full[s], 0, crow * kC);
+                }
                 tma_load_2d(st + OFF_KBT, &tm_kbt, &full[s], 0, row);
                 tma_load_2d(st + OFF_KBT + 8192, &tm_kbt, &full[s], 64, row);
-                tma_load_2d(st + OFF_AQK, &tm_aqk, &full[s], 0, crow * kC);
                 tma_load_2d(st + OFF_U, &tm_u, &full[s], 0, row);
                 bulk_load(smem + OFF_GAM + s * 512, a.gam + (size_t)crow * kD, 512, &full[s]);
                 issued = n + 1;
@@ -383,11 +461,13 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     const int row2 = row + 2 * kC, crow2 = crow + 2;
                     tma_prefetch_2d(&tm_w, 0, row2);
                     tma_prefetch_2d(&tm_w, 64, row2);
-                    tma_prefetch_2d(&tm_q, 0, row2);
-                    tma_prefetch_2d(&tm_q, 64, row2);
+                    if (write_o) {
+                        tma_prefetch_2d(&tm_q, 0, row2);
+                        tma_prefetch_2d(&tm_q, 64, row2);
+                        tma_prefetch_2d(&tm_aqk, 0, crow2 * kC);
+                    }
                     tma_prefetch_2d(&tm_kbt, 0, row2);
                     tma_prefetch_2d(&tm_kbt, 64, row2);
-                    tma_prefetch_2d(&tm_aqk, 0, crow2 * kC);
                     tma_prefetch_2d(&tm_u, 0, row2);
                     bulk_prefetch_l2(a.gam + (size_t)crow2 * kD, 512);
                 }
@@ -433,7 +513,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 mma_commit(bar_D12);
                 // stores are issued after the products they would otherwise delay
                 if (a.h_out) {  // S_n^T tile (rows v) as it stands to h_out, by TMA
-                    const int y = (bh * NT + n) * kD;
+                    const int y = (bh * a.NT + n0 + n) * kD;
                     uint8_t* tile = smem + OFF_S + (n & 1) * S_TILE;
                     tma_store_2d(&tm_hout, tile, 0, y);
                     tma_store_2d(&tm_hout, tile + 16384, 64, y);
@@ -459,18 +539,21 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 // rewritten only after the next D3).  A = the Qh and Aqk tiles
                 // with M = 128: their rows 64..127 are the next 64 rows of the
                 // stage, don't-care; B = the S^T and delta^T tiles (N = v).
+                if (write_o) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_bf16(tO, dQ0 + so + kb, dSn + ka, idesc128, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        const uint32_t kb = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                        mma_bf16(tO, dQ0 + so + kb, dSn + ka, idesc128, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tO, dAq0 + so + ((kk * 32) >> 4), dD + ((kk * 32) >> 4), idesc128,
+                                 1);
                 }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tO, dAq0 + so + ((kk * 32) >> 4), dD + ((kk * 32) >> 4), idesc128, 1);
                 mma_commit(&empty[s]);
                 if (a.delta_out) {  // delta_n^T tile (rows v) to delta_out, by TMA
-                    tma_store_2d(&tm_dout, smem + OFF_DELTA, 0, (bh * NT + n) * kD);
+                    tma_store_2d(&tm_dout, smem + OFF_DELTA, 0, (bh * a.NT + n0 + n) * kD);
                     bulk_commit_group();
                 }
             }
@@ -493,9 +576,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         auto e1 = [&](int n) -> bool {
             const int s = n & 1;
             float r0[32], r1[32];
-            chain_state_tile(tmem + lane_off + TM_S, smem + OFF_S + s * S_TILE, n == 0,
-                             a.h0 ? a.h0 + (size_t)bh * a.D * a.D : nullptr, a.D, v, half, bar_S,
-                             r0, r1);
+            chain_state_tile(tmem + lane_off + TM_S, smem + OFF_S + s * S_TILE, n == 0, job.h0,
+                             a.D, v, half, bar_S, r0, r1);
             if (!wait_bar_warp(&full[s], (n >> 1) & 1, 7)) return false;
             chain_state_rescale(tmem + lane_off + TM_S,
                                 reinterpret_cast<const float*>(smem + OFF_GAM + s * 512), half,
@@ -536,7 +618,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             float x1[32];
             o_rows(m, r, x1);
             __nv_bfloat16* op =
-                a.o + (((size_t)b * a.T + (size_t)m * kC + v) * a.HV + hv) * a.D + half * 64;
+                a.o + (((size_t)b * a.T + (size_t)(n0 + m) * kC + v) * a.HV + hv) * a.D + half * 64;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 float e0[8], e1v[8];
@@ -560,7 +642,8 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 const __nv_bfloat16* U =
                     reinterpret_cast<const __nv_bfloat16*>(smem + s * STAGE_BYTES + OFF_U);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) u[i] = __bfloat162float(U[(32 * half + i) * kD + v]);
+                for (int i = 0; i < 32; ++i)
+                    u[i] = job.zero_u ? 0.f : __bfloat162float(U[(32 * half + i) * kD + v]);
             }
             if (!wait_bar_warp(bar_D12, n & 1, 8)) { ok = false; break; }
             tc_fence_after();
@@ -569,7 +652,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             // the previous chunk's output, while this chunk's state update
             // runs, into the U area of this chunk's stage once every thread
             // has read its U values; the TMA thread stores it
-            if (a.o) {
+            if (write_o) {
                 mbar_arrive(bar_u);
                 if (!wait_bar_warp(bar_u, n & 1, 22)) { ok = false; break; }
                 if (n > 0) o_tile(n - 1, smem + s * STAGE_BYTES + OFF_U);
@@ -580,19 +663,19 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             tc_fence_after();
             if (n + 1 < NT) {
                 if (!e1(n + 1)) { ok = false; break; }
-            } else if (a.ht) {
+            } else if (job.ht) {
 #pragma unroll 1
                 for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     tmem_ld32(tmem + lane_off + TM_S + cb * 32, r);
                     if (v >= a.D || cb * 32 >= a.D) continue;   // [D][D]
-                    float* hp = a.ht + ((size_t)bh * a.D + cb * 32) * a.D + v;
+                    float* hp = job.ht + (size_t)(cb * 32) * a.D + v;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) hp[(size_t)i * a.D] = r[i];
                 }
             }
         }
         // the last chunk's output products are covered by the final commit only
-        if (ok && a.o && wait_bar_warp(bar_fin, 0, 6)) {
+        if (ok && write_o && wait_bar_warp(bar_fin, 0, 6)) {
             tc_fence_after();
             o_out(NT - 1);
         }
@@ -603,6 +686,53 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, TM_COLS);
+}
+
+// Combine step of the segmented scan: per head, the true start state of
+// segment p + 1 is M_p S_p + Z_p for p = 1 .. nseg - 2 (S_1 comes from the
+// full run of segment 0).  One CTA of 256 threads per head; thread (i, h)
+// owns row i and columns 64 h .. 64 h + 63 of the [D][D] result (D <= 128),
+// with M transposed in shared memory so that a warp reads consecutive rows.
+__global__ void __launch_bounds__(256)
+chain_combine_kernel(int D, int nseg, float* __restrict__ sbuf, const float* __restrict__ zbuf,
+                     const float* __restrict__ mbuf) {
+    extern __shared__ float cs[];
+    float* MT = cs;            // MT[k][i] = M[i][k]
+    float* Sk = cs + D * D;    // S[k][j]
+    const int bh = blockIdx.x, tid = threadIdx.x;
+    const size_t SZ = (size_t)D * D;
+    const int i = tid >> 1, j0 = (tid & 1) * 64;
+    for (int p = 1; p <= nseg - 2; ++p) {
+        const float* M = mbuf + ((size_t)bh * nseg + p) * SZ;
+        const float* Sp = sbuf + ((size_t)bh * nseg + p) * SZ;
+        __syncthreads();   // the previous step's rows are written
+        for (int e = tid; e < D * D; e += 256) {
+            MT[(e % D) * D + e / D] = M[e];
+            Sk[e] = Sp[e];
+        }
+        __syncthreads();
+        if (i < D && j0 < D) {
+            float acc[64];
+            const float* Z = zbuf + ((size_t)bh * nseg + p) * SZ + (size_t)i * D + j0;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = Z[j];
+            for (int k = 0; k < D; ++k) {
+                const float m = MT[k * D + i];
+                const float* srow = Sk + k * D + j0;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) acc[j] = fmaf(m, srow[j], acc[j]);
+            }
+            float* out = sbuf + ((size_t)bh * nseg + p + 1) * SZ + (size_t)i * D + j0;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) out[j] = acc[j];
+        }
+    }
+}
+
+// The D x D identity (the start of the transition runs of the segmented scan).
+__global__ void fill_identity_kernel(float* __restrict__ I, int D) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < D * D; e += gridDim.x * blockDim.x)
+        I[e] = (e / D == e % D) ? 1.f : 0.f;
 }
 
 // ===========================================================================
@@ -893,6 +1023,9 @@ struct GradArgs {
     __nv_bfloat16 *dW, *dAqk;  // bf16: the local backward uses them only as MMA operands
 };
 
+// DW: V of the tensors (64 or 128), a compile-time constant so that the
+// 128-wide instantiation indexes exactly as a kernel written for 128 does.
+template <int DW>
 __global__ void __launch_bounds__(kGradThreads, 1)
 grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dh,
               const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dd,
@@ -1120,7 +1253,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             for (int j = 0; j < 32; ++j) {
                 const int m = cb * 32 + j;
                 const float bt = beta_s[m];
-                if (l < a.D) a.dv[(((size_t)trow + m) * a.HV + hv) * a.D + l] = __float2bfloat16_rn(bt * r[j]);
+                if (DW == kD || l < DW)
+                    a.dv[(((size_t)trow + m) * a.HV + hv) * DW + l] = __float2bfloat16_rn(bt * r[j]);
                 const uint32_t voff = G_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
                 r[j] *= __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
             }
@@ -1879,6 +2013,8 @@ struct LocalTcArgs {
     float *dqh, *dkh;
 };
 
+// DW: K of the tensors (64 or 128), a compile-time constant (see grad_v).
+template <int DW>
 __global__ void __launch_bounds__(kLocalTcThreads, 1)
 local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_q,
@@ -2378,8 +2514,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             dG[u] = fmaf(qr, dqs, kr * (bp - l - caq));
             lastp = fmaf(kr, l, lastp);
             dbps[u] = kr * pb;
-            const size_t io = (((size_t)trow + t) * a.HV + hv) * a.D + c;
-            if (c >= a.D) {
+            const size_t io = (((size_t)trow + t) * a.HV + hv) * DW + c;
+            if (DW < kD && c >= DW) {
                 // a key channel past the tensors' width: zero-filled, not written
             } else if (a.G == 1 && !a.qkn) {
                 a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
@@ -2429,8 +2565,8 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int u = 15; u >= 0; --u) {
             run += dG[u];
             const int t = 16 * R + u;
-            const size_t ig = (((size_t)trow + t) * a.HV + hv) * a.D + c;
-            if (c < a.D) a.dg[ig] = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
+            const size_t ig = (((size_t)trow + t) * a.HV + hv) * DW + c;
+            if (DW == kD || c < DW) a.dg[ig] = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
         }
     }
     if (tid < kC)
@@ -2527,7 +2663,21 @@ struct TcWs {
     char* simt;  // SIMT workspace (fp32 quantities)
     __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2, *Tlo2;  // chain operands, T (hi, lo)
     __nv_bfloat16 *h2, *d2, *dh2, *dd2;              // backward only
+    float *sbuf, *zbuf, *mbuf, *ident;               // segmented forward scan (plain forward)
 };
+
+// Segments of the plain forward's state pass (0: one run over all chunks).
+// Its first launch holds BH (2P - 3) CTAs of one SM each and should fit one
+// wave; P >= 3, at least 16 chunks per segment.  Cutting the sequence only
+// pays when few heads leave most SMs idle during a long state pass.
+int chain_segments(const kda_dims& d) {
+    const int BH = d.B * d.HV, NT = d.T / kC;
+    if (BH <= 0 || NT < 48) return 0;
+    int P = (sm_count() / BH + 3) / 2;
+    P = std::min(P, 8);
+    P = std::min(P, NT / 16);
+    return P >= 3 ? P : 0;
+}
 
 // The tensor-core kernels work at K = V = 128 whatever the tensors' width
 // (64 or 128): the fp32 arrays they share with the SIMT carve are laid out
@@ -2561,6 +2711,13 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
         x.d2 = bf(BH * T * kD);
         x.dh2 = bf(BH * NT * kD * kD);
         x.dd2 = bf(BH * T * kD);
+    } else if (const int P = chain_segments(d)) {
+        const size_t st = (size_t)d.K * d.V * sizeof(float);
+        auto f32 = [&](size_t bytes) { return reinterpret_cast<float*>(take(bytes)); };
+        x.sbuf = f32(BH * P * st);
+        x.zbuf = f32(BH * P * st);
+        x.mbuf = f32(BH * P * st);
+        x.ident = f32(st);
     }
     if (w) *w = x;
     return off;
@@ -2651,21 +2808,24 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
     a.dbeta = static_cast<__nv_bfloat16*>(dbeta);
     a.dqh = p.dqh;
     a.dkh = p.dkh;
-    if (cudaFuncSetAttribute(local_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = d.K == kD ? local_bwd_tc_kernel<kD> : local_bwd_tc_kernel<64>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)LOCAL_TC_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
     {
         TimedLaunch tl("tc_local_bwd", s);
         // persistent: one CTA per SM walks the chunks
-        local_bwd_tc_kernel<<<std::min(a.BH * a.NT, sm_count()), kLocalTcThreads, LOCAL_TC_SMEM,
-                              s>>>(mk, mq, mg, mdw, mt, mtl, mda, a);
+        kern<<<std::min(a.BH * a.NT, sm_count()), kLocalTcThreads, LOCAL_TC_SMEM, s>>>(
+            mk, mq, mg, mdw, mt, mtl, mda, a);
     }
     return launch_status();
 }
 
+// nseg >= 3: the plain forward as a segmented scan (three launches and a
+// combine step; see ChainArgs), with its buffers in w.
 kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, const float* h0,
                          void* o, float* ht, __nv_bfloat16* h_out, __nv_bfloat16* delta_out,
-                         cudaStream_t s) {
+                         cudaStream_t s, int nseg = 0) {
     const int BH = d.B * d.HV, NT = d.T / kC;
     CUtensorMap mw, mq, mk, ma, mu;
     const uint64_t rows = (uint64_t)BH * d.T;
@@ -2701,15 +2861,55 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     args.ht = ht;
     args.h_out = h_out;
     args.delta_out = delta_out;
+    args.nseg = 0;
+    args.seglen = 0;
+    args.pass = 0;
+    args.sbuf = args.zbuf = args.mbuf = nullptr;
+    args.ident = nullptr;
     if (cudaFuncSetAttribute(chain_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)CHAIN_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
-    {
+    if (nseg < 3) {
         // three roles, timed apart: forward (o), saving forward (o and the
         // chunk-start states), and the backward's recompute (states only)
         TimedLaunch tl(!h_out ? "tc_chain_fwd" : o ? "tc_chain_fwd_save" : "tc_chain_states", s);
         chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, mdl, mo,
                                                                args);
+        return launch_status();
+    }
+    // segmented: pass 1 (segment 0 in full; later segments from zero and as
+    // transitions), the combine step, pass 3 (later segments in full)
+    args.nseg = nseg;
+    args.seglen = (NT + nseg - 1) / nseg;
+    args.sbuf = w.sbuf;
+    args.zbuf = w.zbuf;
+    args.mbuf = w.mbuf;
+    args.ident = w.ident;
+    const int D = d.K;
+    const size_t cbytes = 2 * (size_t)D * D * sizeof(float);
+    if (cudaFuncSetAttribute(chain_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)cbytes) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    fill_identity_kernel<<<(D * D + 255) / 256, 256, 0, s>>>(w.ident, D);
+    kda_status st;
+    if ((st = launch_status()) != KDA_OK) return st;
+    {
+        TimedLaunch tl("tc_chain_seg_pass1", s);
+        args.pass = 1;
+        chain_fwd_kernel<<<BH * (2 * nseg - 3), kChainThreads, CHAIN_SMEM, s>>>(
+            mw, mq, mk, ma, mu, mh, mdl, mo, args);
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    {
+        TimedLaunch tl("tc_chain_seg_combine", s);
+        chain_combine_kernel<<<BH, 256, cbytes, s>>>(D, nseg, w.sbuf, w.zbuf, w.mbuf);
+    }
+    if ((st = launch_status()) != KDA_OK) return st;
+    {
+        TimedLaunch tl("tc_chain_seg_pass3", s);
+        args.pass = 3;
+        chain_fwd_kernel<<<BH * (nseg - 1), kChainThreads, CHAIN_SMEM, s>>>(
+            mw, mq, mk, ma, mu, mh, mdl, mo, args);
     }
     return launch_status();
 }
@@ -2736,7 +2936,10 @@ kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v
     float* gam = nullptr;
     kda_status st = run_intra_tc(d, w, q, k, v, g, beta, save, s, &gam);
     if (st != KDA_OK) return st;
-    return run_chain_fwd(d, w, gam, h0, o, ht, save ? w.h2 : nullptr, save ? w.d2 : nullptr, s);
+    if (save) return run_chain_fwd(d, w, gam, h0, o, ht, w.h2, w.d2, s);
+    // the plain forward cuts long sequences into segments when few heads
+    // would leave most SMs idle during the state pass
+    return run_chain_fwd(d, w, gam, h0, o, ht, nullptr, nullptr, s, chain_segments(d));
 }
 
 kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
@@ -2817,13 +3020,14 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.dAqk = reinterpret_cast<__nv_bfloat16*>(p.dAqk);
         a.dTv = p.dTv;
         a.dbv = p.dbv;
-        if (cudaFuncSetAttribute(grad_v_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        auto kern = d.V == kD ? grad_v_kernel<kD> : grad_v_kernel<64>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)GRAD_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
         TimedLaunch tl("tc_grad_v", s);
         // persistent: one CTA per SM walks the chunks
-        grad_v_kernel<<<std::min(BH * NT, sm_count()), kGradThreads, GRAD_SMEM, s>>>(
-            mh, mdh, mdo, mdd, md, mv, mt, a);
+        kern<<<std::min(BH * NT, sm_count()), kGradThreads, GRAD_SMEM, s>>>(mh, mdh, mdo, mdd, md,
+                                                                          mv, mt, a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     SimtWsPtrs p;

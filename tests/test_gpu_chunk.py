@@ -270,6 +270,22 @@ def test_qk_l2norm_in_kernel_fp32_gva_with_final_state_gradient():
     compare_all(res, oracle_chunk(inp, True, qk_l2norm=True), w, with_h0=True)
 
 
+@pytest.mark.parametrize("B,T,H,HV,D", [(1, 4096, 2, 4, 128), (2, 3072, 1, 1, 64),
+                                        (1, 8192, 4, 4, 128)])
+def test_tcgen05_segmented_forward(B, T, H, HV, D):
+    """Few heads and long sequences: the plain forward cuts the state pass into
+    segments (segment 0 in full; later ones from zero and as K x K transitions,
+    combined, then rerun in full), which must give the oracle's outputs and
+    final state exactly as the single pass does."""
+    w = I.Workload("segmented", B, T, H, HV, D, D, 64, torch.bfloat16, g_mu=-3.0, g_sigma=1.0,
+                   h0_std=0.1, seed=71 + T + D)
+    inp = I.make_chunk_inputs(w)
+    res = run_gpu(inp, w, "tcgen05", backward=False)
+    ref = oracle_chunk(inp, False)
+    assert_close("o", res["o"], ref["o"], w.dtype)
+    assert_close("ht", res["ht"], ref["ht"], w.dtype)
+
+
 def test_ragged_value_width_simt():
     """V not a multiple of the 32-column tile, small K."""
     w = I.Workload("ragged_v", 1, 64, 1, 2, 16, 40, 32, torch.float32, h0_std=0.5, dht=True,
