@@ -279,6 +279,11 @@ kda_status kda_check(void* stream) {
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_selftest_wait_timeout(long long limit_cycles, void* stream) {
+    if (limit_cycles < 0 || limit_cycles > 4000000000LL) return KDA_ERR_INVALID_ARG;
+    return tc_selftest_timeout(limit_cycles, static_cast<cudaStream_t>(stream));
+}
+
 const char* kda_status_str(kda_status s) {
     switch (s) {
         case KDA_OK: return "ok";

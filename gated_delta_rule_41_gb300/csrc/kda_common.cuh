@@ -91,5 +91,8 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                   float* dh0, void* ws, bool from_saved, cudaStream_t s);
 // Reads and clears the device error word of the tensor-core kernels.
 kda_status tc_take_error(cudaStream_t s);
+// Diagnostic: a bounded wait on an mbarrier nothing arrives at, with the given
+// limit (cycles); it records KDA_ERR_TIMEOUT for the next kda_check.
+kda_status tc_selftest_timeout(long long limit_cycles, cudaStream_t s);
 
 }  // namespace kda

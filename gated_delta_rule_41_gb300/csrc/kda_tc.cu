@@ -37,20 +37,26 @@ constexpr int kC = 64, kD = 128;  // chunk size, K = V
 constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 // ---- error-aware bounded mbarrier wait ----
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, int code) {
+// Gives up after `limit` cycles (recording `code` in g_tc_error) or as soon
+// as another wait has recorded an error.
+__device__ __forceinline__ bool wait_bar_limit(uint64_t* bar, uint32_t parity, int code,
+                                               long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     uint32_t it = 0;
     while (!mbar_try_wait(bar, parity)) {
         if ((++it & 255u) == 0) {
             if (*reinterpret_cast<volatile int*>(&g_tc_error) != 0) return false;
-            if (clock64() - t0 > kTimeoutCycles) {
+            if (clock64() - t0 > limit) {
                 atomicCAS(&g_tc_error, 0, code);
                 return false;
             }
         }
     }
     return true;
+}
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, int code) {
+    return wait_bar_limit(bar, parity, code, kTimeoutCycles);
 }
 // Wait for a phase with the time bound only (also after another wait has
 // failed), for copies that must land before the CTA exits.
@@ -691,14 +697,16 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 // Combine step of the segmented scan: per head, the true start state of
 // segment p + 1 is M_p S_p + Z_p for p = 1 .. nseg - 2 (S_1 comes from the
 // full run of segment 0).  One CTA of 256 threads per head; thread (i, h)
-// owns row i and columns 64 h .. 64 h + 63 of the [D][D] result (D <= 128),
-// with M transposed in shared memory so that a warp reads consecutive rows.
+// owns row i and columns 64 h .. 64 h + 63 of the [D][D] result (D <= 128).
+// M is kept row-major with a row stride of D + 1 floats, so that the 16 rows
+// a warp reads at one k fall in distinct banks; S rows are read as float4.
 __global__ void __launch_bounds__(256)
 chain_combine_kernel(int D, int nseg, float* __restrict__ sbuf, const float* __restrict__ zbuf,
                      const float* __restrict__ mbuf) {
     extern __shared__ float cs[];
-    float* MT = cs;            // MT[k][i] = M[i][k]
-    float* Sk = cs + D * D;    // S[k][j]
+    const int MP = D + 1;
+    float* Ms = cs;                  // Ms[i * MP + k] = M[i][k]
+    float* Sk = cs + D * MP;         // S[k][j]; D (D + 1) is a multiple of 4: 16-byte aligned
     const int bh = blockIdx.x, tid = threadIdx.x;
     const size_t SZ = (size_t)D * D;
     const int i = tid >> 1, j0 = (tid & 1) * 64;
@@ -707,7 +715,7 @@ chain_combine_kernel(int D, int nseg, float* __restrict__ sbuf, const float* __r
         const float* Sp = sbuf + ((size_t)bh * nseg + p) * SZ;
         __syncthreads();   // the previous step's rows are written
         for (int e = tid; e < D * D; e += 256) {
-            MT[(e % D) * D + e / D] = M[e];
+            Ms[(e / D) * MP + e % D] = M[e];
             Sk[e] = Sp[e];
         }
         __syncthreads();
@@ -717,10 +725,16 @@ chain_combine_kernel(int D, int nseg, float* __restrict__ sbuf, const float* __r
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = Z[j];
             for (int k = 0; k < D; ++k) {
-                const float m = MT[k * D + i];
-                const float* srow = Sk + k * D + j0;
+                const float m = Ms[i * MP + k];
+                const float4* srow = reinterpret_cast<const float4*>(Sk + k * D + j0);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) acc[j] = fmaf(m, srow[j], acc[j]);
+                for (int j = 0; j < 16; ++j) {
+                    const float4 sv = srow[j];
+                    acc[4 * j] = fmaf(m, sv.x, acc[4 * j]);
+                    acc[4 * j + 1] = fmaf(m, sv.y, acc[4 * j + 1]);
+                    acc[4 * j + 2] = fmaf(m, sv.z, acc[4 * j + 2]);
+                    acc[4 * j + 3] = fmaf(m, sv.w, acc[4 * j + 3]);
+                }
             }
             float* out = sbuf + ((size_t)bh * nseg + p + 1) * SZ + (size_t)i * D + j0;
 #pragma unroll
@@ -2886,7 +2900,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     args.mbuf = w.mbuf;
     args.ident = w.ident;
     const int D = d.K;
-    const size_t cbytes = 2 * (size_t)D * D * sizeof(float);
+    const size_t cbytes = ((size_t)D * (D + 1) + (size_t)D * D) * sizeof(float);
     if (cudaFuncSetAttribute(chain_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)cbytes) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -3035,6 +3049,27 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     if ((st = run_local_bwd_tc(d, w, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
     if (d.HV == d.H && !d.qk_l2norm) return KDA_OK;
     return group_sum_launch(d, p.dqh, p.dkh, q, k, dq, dk, s);
+}
+
+namespace {
+// Diagnostic of the bounded-wait error path: one warp waits, with a limit of
+// `limit` cycles, on an mbarrier that nothing arrives at.  The wait gives up,
+// records its code in the error word and the kernel returns; nothing is in
+// flight, so the context stays usable.
+__global__ void __launch_bounds__(32, 1) wait_timeout_kernel(long long limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    wait_bar_limit(&bar, 0, 99, limit);
+}
+}  // namespace
+
+kda_status tc_selftest_timeout(long long limit_cycles, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 32, 0, s>>>(limit_cycles);
+    return launch_status();
 }
 
 kda_status tc_take_error(cudaStream_t s) {

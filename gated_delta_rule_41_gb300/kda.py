@@ -83,6 +83,8 @@ def load_library():
         lib.kda_timing_entry.restype = I
         lib.kda_selftest_mma.argtypes = [P, P, P, I, I, P, P]
         lib.kda_selftest_mma.restype = I
+        lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_longlong, P]
+        lib.kda_selftest_wait_timeout.restype = I
         _lib = lib
         return lib
 

@@ -249,6 +249,14 @@ int kda_timing_entry(int i, char* name, int name_len, double* total_ms, long* la
 kda_status kda_selftest_mma(const void* A, const void* B, float* D, int N, int flags,
                             int* status, void* stream);
 
+/* Diagnostics: the bounded-wait error path of the tensor-core kernels.  One
+ * warp waits, with a limit of limit_cycles (0 .. 4e9) SM clock cycles, on an
+ * mbarrier that nothing arrives at, through the same wait routine the chunk
+ * kernels use; it gives up, records the error and returns with nothing in
+ * flight.  The next kda_check on the stream then returns KDA_ERR_TIMEOUT
+ * and clears it. */
+kda_status kda_selftest_wait_timeout(long long limit_cycles, void* stream);
+
 /* Static description of a status code. */
 const char* kda_status_str(kda_status status);
 

@@ -43,3 +43,23 @@ def test_mn_major_operands(N, a_mn, b_mn):
     """MN-major operands (M/N contiguous): 64-element M/N blocks 8 KB apart,
     8-row K groups 1 KB apart."""
     assert _mn_case(N, a_mn, b_mn) < 1e-3
+
+
+def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
+    """A wait on an mbarrier that nothing arrives at gives up after its limit
+    (here about 1 ms at 2 GHz), records the error word, and kda_check reports
+    KDA_ERR_TIMEOUT once; the next calls run normally."""
+    lib = kda.load_library()
+    kda.check()
+    st = lib.kda_selftest_wait_timeout(2_000_000, kda.kda._stream(None))
+    assert st == 0
+    with pytest.raises(kda.KdaError) as ei:
+        kda.check()
+    assert ei.value.status == 7
+    kda.check()   # cleared
+    # the tensor cores still run and agree with a plain product
+    g = torch.Generator(device="cpu").manual_seed(5)
+    A = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    B = torch.randn(64, 64, generator=g).to(torch.bfloat16)
+    D = kda.kda.selftest_mma(A.cuda(), B.cuda())
+    torch.testing.assert_close(D.double().cpu(), A.double() @ B.double().T, atol=1e-3, rtol=1e-4)
