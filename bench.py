@@ -49,20 +49,22 @@ def _src_hash(name):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:12] if os.path.exists(path) else ""
 
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
-# keyed by kernel name: (bytes per launch at the capture workload, the source
-# file, that file's hash when captured).  A kernel whose source has changed
-# since reports traffic null.  Captured at B=1, T=8192, HV=16 (2048 chunks,
-# inputs and workspace above L2); the traffic grows with the chunk count, so a
-# launch at another size reports the bytes scaled by its head-tokens.
-NCU_TRAFFIC_HEAD_TOKENS = 1 * 8192 * 16
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
+# of that kernel alone (-k, one launch), keyed by kernel name: (bytes per
+# launch, head-tokens B*T*HV of the captured launch, the source file, that
+# file's hash when captured).  A kernel whose source has changed since reports
+# traffic null.  The step's kernels were captured at B=1, T=8192, HV=16 (2048
+# chunks, inputs and workspace above L2), the plain forward's state pass at
+# B=4 (at B=1 the plain forward cuts its state pass into segments); traffic
+# grows with the chunk count, so a launch at another size reports the bytes
+# scaled by its head-tokens.
 NCU_TRAFFIC = {
-    "tc_local_bwd": (354968832 + 78607360, "kda_tc.cu", "72b41d331d5e"),
-    "tc_intra": (134708736 + 132661504, "kda_tc.cu", "72b41d331d5e"),
-    "tc_grad_v": (286032640 + 197711360, "kda_tc.cu", "72b41d331d5e"),
-    "tc_chain_fwd_save": (152248320 + 91040768, "kda_tc.cu", "72b41d331d5e"),
-    "tc_chain_bwd": (152090368 + 64567040, "kda_tc.cu", "72b41d331d5e"),
-    "tc_chain_fwd": (152121344 + 20483072, "kda_tc.cu", "72b41d331d5e"),
+    "tc_local_bwd": (436776960, 1 * 8192 * 16, "kda_tc.cu", "5b979e94156a"),
+    "tc_intra": (275303936, 1 * 8192 * 16, "kda_tc.cu", "5b979e94156a"),
+    "tc_grad_v": (486793984, 1 * 8192 * 16, "kda_tc.cu", "5b979e94156a"),
+    "tc_chain_fwd_save": (247591424, 1 * 8192 * 16, "kda_tc.cu", "5b979e94156a"),
+    "tc_chain_bwd": (220102656, 1 * 8192 * 16, "kda_tc.cu", "5b979e94156a"),
+    "tc_chain_fwd": (725889280, 4 * 8192 * 16, "kda_tc.cu", "5b979e94156a"),
 }
 # decode_kernel: dram read + write per launch at the decode workload (B=256,
 # HV=16, K=V=128), its source file and that file's hash when captured
@@ -74,10 +76,10 @@ def ncu_traffic(name, w):
     when there is no capture of its current source."""
     if name not in NCU_TRAFFIC:
         return None
-    tb, src, h = NCU_TRAFFIC[name]
+    tb, ht, src, h = NCU_TRAFFIC[name]
     if _src_hash(src) != h:
         return None
-    return int(round(tb * (w.B * w.T * w.HV) / NCU_TRAFFIC_HEAD_TOKENS))
+    return int(round(tb * (w.B * w.T * w.HV) / ht))
 
 
 def kernel_algo_bytes(name, w):

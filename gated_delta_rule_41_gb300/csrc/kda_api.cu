@@ -150,18 +150,8 @@ static kda_status chunk_bwd(const kda_dims* d, const void* q, const void* k, con
                             void* stream, bool from_saved) {
     kda_status st = check_common(d, true);
     if (st != KDA_OK) return st;
-    int impl = pick_impl(*d);
+    const int impl = pick_impl(*d);
     if (impl < 0) return KDA_ERR_UNSUPPORTED;
-    // The tensor-core backward keeps chunk states and delta as bf16 between
-    // its kernels; with an upstream final-state gradient the state gradient
-    // is O(1) and those roundings exceed the accuracy bar, so such calls run
-    // the fp32 SIMT kernels (AUTO) or are refused (explicit TCGEN05).  The
-    // tensor-core workspace size covers the SIMT backward as well.
-    if (impl == KDA_IMPL_TCGEN05 && dht) {
-        if (d->impl == KDA_IMPL_TCGEN05) return KDA_ERR_UNSUPPORTED;
-        if (!simt_supported(*d)) return KDA_ERR_UNSUPPORTED;
-        impl = KDA_IMPL_SIMT;
-    }
     const bool empty = d->B == 0 || d->T == 0;
     if ((st = check_ptrs(empty, chunk_align(*d, impl), {q, k, v, g, dout, dq, dk, dv, dg},
                          {h0, dht, dh0})) != KDA_OK)

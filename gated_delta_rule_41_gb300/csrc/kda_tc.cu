@@ -144,6 +144,25 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&x)[8]) {
         x[2 * i + 1] = f.y;
     }
 }
+// Low part of a two-term bf16 split, x - bf16(x) rounded to bf16, for 8
+// values (the high part is pack8(x), the value the operand tiles hold).
+__device__ __forceinline__ uint4 pack8_lo(const float (&x)[8]) {
+    float h[8], l[8];
+    unpack8(pack8(x), h);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) l[i] = x[i] - h[i];
+    return pack8(l);
+}
+// Low parts of 32 consecutive values to global memory (16-byte aligned).
+__device__ __forceinline__ void store_lo32(__nv_bfloat16* dst, const float (&r)[32]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = r[8 * j + i];
+        *reinterpret_cast<uint4*>(dst + 8 * j) = pack8_lo(x);
+    }
+}
 
 // L2-normalises each of the 64 rows of a [64][128] bf16 token tile (two
 // 64-column 128B-swizzled boxes, 8 KB apart) in place: x / max(|x|, 1e-12),
@@ -248,10 +267,13 @@ __device__ __forceinline__ void chain_state_rescale(uint32_t tS, const float* ga
 // u is given: the 32 values U[c][v], read before the products completed) to
 // the bf16 K-major operand tile (negated if `neg_tile`), arrive on bar1 and
 // bar2 (if given), then, if `gtile` is given, the true-sign bf16 values into
-// it as a 128B-swizzled pair of [64 c][64 v] tiles (for a TMA store).
+// it as a 128B-swizzled pair of [64 c][64 v] tiles (for a TMA store).  If
+// `glo` is given, the low parts of the true-sign values (x - bf16(x)) go to
+// the 32 consecutive bf16 there.
 __device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile, const float* u,
                                                  bool neg_tile, int v, int half, uint64_t* bar1,
-                                                 uint64_t* bar2, uint8_t* gtile) {
+                                                 uint64_t* bar2, uint8_t* gtile,
+                                                 __nv_bfloat16* glo = nullptr) {
     const int c0 = 32 * half;
     float d0[32];
     tmem_ld32_nw(tD + c0, d0);
@@ -262,6 +284,7 @@ __device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile, con
     }
     const float sg = neg_tile ? -1.f : 1.f;
     store_row_bf16(tile, v, c0, d0, sg);
+    if (glo) store_lo32(glo, d0);
     fence_async_smem();
     tc_fence_before();
     mbar_arrive(bar1);
@@ -285,6 +308,11 @@ struct ChainArgs {
     float* ht;          // [BH][K][V] or null
     __nv_bfloat16* h_out;  // [BH][NT][V][K] or null (states at chunk starts, transposed, bf16)
     __nv_bfloat16* delta_out;  // [BH][NT][V][C] or null (transposed); set iff h_out is
+    // Two-term split of U and delta (the backward with an upstream final-state
+    // gradient): U = U2 + u_lo read from [BH*T][128], and the low parts of
+    // delta^T to delta_lo ([BH][NT][V][C], like delta_out).  Both or neither.
+    const __nv_bfloat16* u_lo;
+    __nv_bfloat16* delta_lo;
     // Segmented scan of long sequences (nseg >= 3; 0: one CTA per head over
     // all chunks).  The chunks are cut into nseg segments of seglen (the last
     // may be shorter).  pass 1: CTAs [0, BH) run segment 0 in full (its end
@@ -359,6 +387,10 @@ __device__ __forceinline__ ChainJob chain_job(const ChainArgs& a, int c) {
     return j;
 }
 
+// LO: U comes as two parts (a.u_lo added) and delta's low parts go to
+// a.delta_lo; a separate instantiation, so that the plain one's serial
+// chunk loop carries none of it.
+template <bool LO>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_kbt,
@@ -476,6 +508,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                     tma_prefetch_2d(&tm_kbt, 64, row2);
                     tma_prefetch_2d(&tm_u, 0, row2);
                     bulk_prefetch_l2(a.gam + (size_t)crow2 * kD, 512);
+                    if (LO) bulk_prefetch_l2(a.u_lo + (size_t)row2 * kD, kC * kD * 2);
                 }
             }
             // the epilogue's last two iterations (after an error, skipped)
@@ -650,11 +683,19 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     u[i] = job.zero_u ? 0.f : __bfloat162float(U[(32 * half + i) * kD + v]);
+                if (LO && !job.zero_u) {
+                    const __nv_bfloat16* ul =
+                        a.u_lo + ((size_t)bh * a.T + (size_t)(n0 + n) * kC + 32 * half) * kD + v;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) u[i] += __bfloat162float(ul[(size_t)i * kD]);
+                }
             }
             if (!wait_bar_warp(bar_D12, n & 1, 8)) { ok = false; break; }
             tc_fence_after();
-            chain_delta_step(tmem + lane_off + TM_W, sDelta, u, false, v, half, bar_delta, nullptr,
-                             nullptr);
+            chain_delta_step(
+                tmem + lane_off + TM_W, sDelta, u, false, v, half, bar_delta, nullptr, nullptr,
+                LO ? a.delta_lo + (((size_t)bh * a.NT + n0 + n) * kD + v) * kC + 32 * half
+                   : nullptr);
             // the previous chunk's output, while this chunk's state update
             // runs, into the U area of this chunk's stage once every thread
             // has read its U values; the TMA thread stores it
@@ -774,8 +815,12 @@ struct ChainBwdArgs {
     const float* dht;            // [BH][K][V] or null
     float* dh0;                  // [BH][K][V] or null
     __nv_bfloat16* dh_out;       // [BH][NT][V][K] (transposed)
+    __nv_bfloat16* dh_lo;        // low parts of dh_out (x - bf16(x)), same layout, or null
 };
 
+// LO: also write the low parts of dS (a.dh_lo); a separate instantiation,
+// so that the plain one keeps its registers.
+template <bool LO>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kbt,
@@ -965,6 +1010,12 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             chain_state_tile(tmem + lane_off + TM2_S, smem + OFF_S + s * S_TILE, i == 0,
                              a.dht ? a.dht + (size_t)bh * a.D * a.D : nullptr, a.D, v, half, bar_S, r0,
                              r1);
+            if (LO) {
+                __nv_bfloat16* lo =
+                    a.dh_lo + (((size_t)bh * NT + (NT - 1 - i)) * kD + v) * kD + 64 * half;
+                store_lo32(lo, r0);
+                store_lo32(lo + 32, r1);
+            }
             if (!wait_bar_warp(&full[s], (i >> 1) & 1, 17)) return false;
             chain_state_rescale(tmem + lane_off + TM2_S,
                                 reinterpret_cast<const float*>(smem + OFF_GAM + s * 512), half,
@@ -1305,6 +1356,305 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
 }
 
 // ===========================================================================
+// The contractions over V in two-term precision, for the backward with an
+// upstream final-state gradient.  dS then carries that gradient (of the size
+// of the inputs) back through the chunks, and products of dS, delta and Kb
+// with single bf16 operands lose too much: the parts of dk and dbeta they
+// feed cancel to values far smaller than their terms.  Here dS, delta and Kb
+// come as bf16 high + low parts (x = hi + lo, about 16 mantissa bits) and
+// each of their products takes three terms (hi hi + lo hi + hi lo):
+//     ddelta^T = dS^T Kb^T + dO^T Aqk   (recomputed: the reverse pass's own
+//                                        ddelta has single bf16 operands)
+//     D3 = dS delta^T,  dgam = rowsum(dS o S0)
+// and ddelta, split the same way, enters D2, D4 (bottom) and D5 as two
+// terms.  S0, dO, v and T stay single bf16 operands.  One chunk at a time
+// per CTA: every tile of a chunk loads at its start, with no overlap with
+// the previous chunk, so that the shared-memory plan holds all of them.
+// ===========================================================================
+constexpr uint32_t P_S0 = 0;         // S0^T [128 v][128 k]: two 64-column boxes, 16 KB apart
+constexpr uint32_t P_DS = 32768;     // dS^T high part, same layout
+constexpr uint32_t P_DSL = 65536;    // dS^T low part; after the products, partial sums
+constexpr uint32_t P_ODD = 98304;    // [dO; ddelta high], as in grad_v
+constexpr uint32_t P_DV = 131072;    // Aqk [64 t][64 c] at +0, v at +8192 and +24576, T at +16384
+constexpr uint32_t P_DT = 163840;    // delta^T high [128 v][64 c]
+constexpr uint32_t P_DTL = 180224;   // delta^T low
+constexpr uint32_t P_LO = 196608;    // Kb high at +0 / +16384, Kb low at +8192 / +24576 (one
+                                     // 64-column box each); then ddelta low at +8192 / +24576
+constexpr uint32_t P_BAR = 229376;
+constexpr uint32_t PX_TX = 3 * 32768 + 16384 + 2 * 16384 + 32768 + 8192 + 16384 + 8192;
+constexpr uint32_t PX_SMEM = P_BAR + 64 + 1024;
+static_assert(PX_SMEM <= 232448, "the two-term contraction kernel exceeds the shared memory limit");
+static_assert(P_DSL % 1024 == 0 && P_ODD % 1024 == 0 && P_DV % 1024 == 0 && P_DT % 1024 == 0 &&
+                  P_DTL % 1024 == 0 && P_LO % 1024 == 0,
+              "128-byte swizzled tiles need 1024-byte aligned bases");
+
+template <int DW>
+__global__ void __launch_bounds__(kGradThreads, 1)
+grad_v_px_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dh,
+                 const __grid_constant__ CUtensorMap tm_dhl, const __grid_constant__ CUtensorMap tm_do,
+                 const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_dl,
+                 const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_kbl,
+                 const __grid_constant__ CUtensorMap tm_aqk, const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_t, GradArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(smem + P_BAR);   // every tile of the chunk
+    uint64_t* bar_a = bar_ld + 1;                                     // ddelta, D1, D3
+    uint64_t* bar_b = bar_ld + 2;                                     // D2, D4, D5
+    uint64_t* bar_fin = bar_ld + 3;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_ld + 4);
+    float* dbv_part = reinterpret_cast<float*>(smem + P_DSL);   // [4 lane quadrants][64]
+    float* dg_part = dbv_part + 4 * 64;                          // [2 halves][128]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NT = a.NT, total = a.BH * NT;   // CTA i takes chunks i, i + grid, ...
+    int issued = 0, waited = 0;               // thread 0's loads (each waited for before exit)
+    auto issue = [&](int ch) {
+        const int nn = ch % NT, bb = ch / NT, hvv = bb % a.HV;
+        const int rw = bb * a.T + nn * kC, tr = (bb / a.HV) * a.T + nn * kC;
+        mbar_arrive_expect_tx(bar_ld, PX_TX);
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            tma_load_2d(smem + P_S0 + hb * 16384, &tm_h, bar_ld, 64 * hb, ch * kD);
+            tma_load_2d(smem + P_DS + hb * 16384, &tm_dh, bar_ld, 64 * hb, ch * kD);
+            tma_load_2d(smem + P_DSL + hb * 16384, &tm_dhl, bar_ld, 64 * hb, ch * kD);
+            tma_load_3d(smem + P_ODD + hb * 16384, &tm_do, bar_ld, 64 * hb, hvv, tr);
+            tma_load_2d(smem + P_LO + hb * 16384, &tm_kb, bar_ld, 64 * hb, rw);
+            tma_load_2d(smem + P_LO + 8192 + hb * 16384, &tm_kbl, bar_ld, 64 * hb, rw);
+            tma_load_3d(smem + P_DV + 8192 + hb * 16384, &tm_v, bar_ld, 64 * hb, hvv, tr);
+        }
+        tma_load_2d(smem + P_DT, &tm_d, bar_ld, 0, ch * kD);
+        tma_load_2d(smem + P_DTL, &tm_dl, bar_ld, 0, ch * kD);
+        tma_load_2d(smem + P_DV, &tm_aqk, bar_ld, 0, ch * kC);
+        tma_load_2d(smem + P_DV + 16384, &tm_t, bar_ld, 0, ch * kC);
+        ++issued;
+    };
+
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_a, 1);
+        mbar_init(bar_b, 1);
+        mbar_init(bar_fin, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t id64 = idesc_bf16_f32(128, 64);
+    const uint32_t s0 = smem_u32(smem + P_S0), ds = smem_u32(smem + P_DS),
+                   dsl = smem_u32(smem + P_DSL), odd = smem_u32(smem + P_ODD),
+                   dvb = smem_u32(smem + P_DV), dt = smem_u32(smem + P_DT),
+                   dtl = smem_u32(smem + P_DTL), lo = smem_u32(smem + P_LO);
+    // all 8 warps, two per TMEM lane quadrant, splitting the columns
+    const int q = warp & 3, half = warp >> 2;
+    const int l = q * 32 + lane;   // TMEM lane: v for ddelta^T and D5, k for D1-D3, row for D4
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    bool ok = true;
+
+#pragma unroll 1
+    for (int it = 0, chunk = blockIdx.x; chunk < total; ++it, chunk += gridDim.x) {
+        const uint32_t ph = it & 1;
+        const int n = chunk % NT, bh = chunk / NT;
+        const int b = bh / a.HV, hv = bh % a.HV;
+        const int row = bh * a.T + n * kC;
+        const int trow = b * a.T + n * kC;
+        if (tid == 0) {
+            issue(chunk);
+            if (wait_bar(bar_ld, ph, 51)) {
+                ++waited;
+                tc_fence_after();
+                // ddelta^T [v][c] -> TMEM columns 384..447: dS^T read K-major
+                // (rows v), Kb K-major (rows c), three terms
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + 384, sdesc_sw128(ds + ko), sdesc_sw128(lo + ko), id64, kk > 0);
+                    mma_bf16(tmem + 384, sdesc_sw128(dsl + ko), sdesc_sw128(lo + ko), id64, 1);
+                    mma_bf16(tmem + 384, sdesc_sw128(ds + ko), sdesc_sw128(lo + 8192 + ko), id64, 1);
+                }
+                // + dO^T Aqk: dO read MN-major (v blocks 16 KB apart), Aqk MN-major
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + 384, sdesc_mn_sw128(odd + kk * 2048, 16384),
+                             sdesc_mn_sw128(dvb + kk * 2048, 8192), id64 | kAMajorMN | kBMajorMN, 1);
+                // D1 = S0 dO^T -> columns 0..63; D3 = dS delta^T -> 128..191 (three terms).
+                // S0 and dS are stored transposed (rows v): A operands read
+                // MN-major, K = v advancing 16 rows per step
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint64_t ads = sdesc_mn_sw128(ds + kk * 2048, 16384);
+                    const uint64_t bdt = sdesc_mn_sw128(dt + kk * 2048, 16384);
+                    mma_bf16(tmem + 0, sdesc_mn_sw128(s0 + kk * 2048, 16384), sdesc_sw128(odd + ko),
+                             id64 | kAMajorMN, kk > 0);
+                    mma_bf16(tmem + 128, ads, bdt, id64 | kAMajorMN | kBMajorMN, kk > 0);
+                    mma_bf16(tmem + 128, sdesc_mn_sw128(dsl + kk * 2048, 16384), bdt,
+                             id64 | kAMajorMN | kBMajorMN, 1);
+                    mma_bf16(tmem + 128, ads, sdesc_mn_sw128(dtl + kk * 2048, 16384),
+                             id64 | kAMajorMN | kBMajorMN, 1);
+                }
+                mma_commit(bar_a);
+            } else {
+                ok = false;
+            }
+        }
+        __syncwarp();
+        float r[32];
+        ok = ok && wait_bar_warp(bar_a, ph, 52);
+        tc_fence_after();
+        if (ok) {
+            // ddelta (row c, column v = l) as high and low bf16 parts: the high
+            // part into rows 64..127 of the [dO; ddelta] tile, the low part
+            // over Kb's (read by the products above) in the same layout
+            tmem_ld32(tmem + lane_off + 384 + 32 * half, r);
+            const uint32_t box = (uint32_t)(l >> 6) * 16384;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint32_t off = 8192 + box + sw128_offset(32 * half + j, l & 63);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(r[j]);
+                *reinterpret_cast<__nv_bfloat16*>(smem + P_ODD + off) = hi;
+                *reinterpret_cast<__nv_bfloat16*>(smem + P_LO + off) =
+                    __float2bfloat16_rn(r[j] - __bfloat162float(hi));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0 && ok) {
+            const uint32_t tt = dvb + 16384;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                const uint64_t as0 = sdesc_mn_sw128(s0 + kk * 2048, 16384);
+                const uint64_t bv = sdesc_sw128(dvb + 8192 + ko);
+                // D2 = S0 ddelta^T -> columns 64..127 (two terms)
+                mma_bf16(tmem + 64, as0, sdesc_sw128(odd + 8192 + ko), id64 | kAMajorMN, kk > 0);
+                mma_bf16(tmem + 64, as0, sdesc_sw128(lo + 8192 + ko), id64 | kAMajorMN, 1);
+                // D4 = [dO; ddelta] [delta; v]^T: delta^T -> 256..319 (lanes 0..63
+                // used), v -> 320..383 (lanes 64..127 used), the low part of
+                // ddelta as a second term whose rows 0..63 (Kb's high part)
+                // land in the unused lanes
+                mma_bf16(tmem + 256, sdesc_sw128(odd + ko), sdesc_mn_sw128(dt + kk * 2048, 16384),
+                         id64 | kBMajorMN, kk > 0);
+                mma_bf16(tmem + 320, sdesc_sw128(odd + ko), bv, id64, kk > 0);
+                mma_bf16(tmem + 320, sdesc_sw128(lo + ko), bv, id64, 1);
+            }
+            // D5 = ddelta^T T -> 192..255 (two terms): ddelta read MN-major, T MN-major
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bt = sdesc_mn_sw128(tt + kk * 2048, 8192);
+                mma_bf16(tmem + 192, sdesc_mn_sw128(odd + 8192 + kk * 2048, 16384), bt,
+                         id64 | kAMajorMN | kBMajorMN, kk > 0);
+                mma_bf16(tmem + 192, sdesc_mn_sw128(lo + 8192 + kk * 2048, 16384), bt,
+                         id64 | kAMajorMN | kBMajorMN, 1);
+            }
+            mma_commit(bar_b);
+        }
+        __syncwarp();
+        ok = ok && wait_bar_warp(bar_b, ph, 53);
+        tc_fence_after();
+        // dgam[k] = sum_v (dS_hi + dS_lo)[v][k] S0[v][k]; thread (k = l, half)
+        // sums rows v in [64 half, 64 half + 64)
+        float dgp = 0.f;
+        if (ok) {
+            const uint32_t kb = (uint32_t)(l >> 6) * 16384;
+#pragma unroll 8
+            for (int vv = 0; vv < 64; ++vv) {
+                const uint32_t off = kb + sw128_offset(64 * half + vv, l & 63);
+                const float dsv =
+                    __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + P_DS + off)) +
+                    __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + P_DSL + off));
+                dgp += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + P_S0 + off)) *
+                       dsv;
+            }
+        }
+        __syncthreads();   // the dS low tile is read: the partial sums go there
+        dg_part[half * kD + l] = dgp;
+        if (ok) {
+            const size_t rb = (size_t)row * kD;
+            const int cb = half;  // columns 32*cb .. 32*cb+31 of D1-D3 and D5
+            tmem_ld32(tmem + lane_off + 0 + cb * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a.dQh[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
+            tmem_ld32(tmem + lane_off + 64 + cb * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                a.dW[rb + (size_t)(cb * 32 + j) * kD + l] = __float2bfloat16_rn(-r[j]);
+            tmem_ld32(tmem + lane_off + 128 + cb * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a.dKb[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
+            {
+                const size_t cc = (size_t)chunk * kC * kC;
+                const int c4 = (q < 2 ? 0 : 2) + half;
+                tmem_ld32(tmem + lane_off + 256 + c4 * 32, r);
+                if (q < 2) {  // dAqk row i (bf16), masked to j <= i
+                    const int i = l;
+                    __nv_bfloat16* dst = a.dAqk + cc + (size_t)i * kC + c4 * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = (c4 * 32 + j) <= i ? r[j] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8)
+                        *reinterpret_cast<uint4*>(dst + j) =
+                            make_uint4(pack_bf16(r[j], r[j + 1]), pack_bf16(r[j + 2], r[j + 3]),
+                                       pack_bf16(r[j + 4], r[j + 5]), pack_bf16(r[j + 6], r[j + 7]));
+                } else {  // dTv row i (fp32), masked to j < i
+                    const int i = l - 64;
+                    float* dst = a.dTv + cc + (size_t)i * kC + (c4 - 2) * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = ((c4 - 2) * 32 + j) < i ? r[j] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) =
+                            make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+                }
+            }
+            // D5: lane = v, columns m = 32*cb .. 32*cb+31
+            tmem_ld32(tmem + lane_off + 192 + cb * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int m = cb * 32 + j;
+                const float bt = __bfloat162float(a.beta[((size_t)trow + m) * a.HV + hv]);
+                if (DW == kD || l < DW)
+                    a.dv[(((size_t)trow + m) * a.HV + hv) * DW + l] = __float2bfloat16_rn(bt * r[j]);
+                const uint32_t voff = P_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
+                r[j] *= __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
+            }
+            // dbv[m] = sum over v of r: lane j ends with row cb*32 + j of this quadrant
+            dbv_part[q * 64 + cb * 32 + lane] = warp_sum_scatter<32>(r);
+        }
+        __syncthreads();
+        if (ok && tid < kD) a.dgam[(size_t)chunk * kD + tid] = dg_part[tid] + dg_part[kD + tid];
+        if (ok && tid < 64)
+            a.dbv[(size_t)row + tid] =
+                (dbv_part[tid] + dbv_part[64 + tid]) + (dbv_part[128 + tid] + dbv_part[192 + tid]);
+        // the next chunk's loads overwrite every tile and the partial sums
+        fence_async_smem();
+        tc_fence_before();
+        if (!__syncthreads_and(ok)) break;
+        tc_fence_after();
+    }
+    // a load issued for a chunk the loop did not finish (after an error)
+    // lands before shared memory is released; every product completes before
+    // TMEM is
+    if (tid == 0) {
+        for (; waited < issued; ++waited) wait_bar_drain(bar_ld, waited & 1);
+        mma_commit(bar_fin);
+        wait_bar_drain(bar_fin, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ===========================================================================
 // Intra-chunk quantities on tensor cores (K3 row L2 steps (1)-(3) plus the
 // operands of the state passes), one chunk of one head at a time per CTA of
 // 256 threads.  Shared memory stays under half an SM's, so two CTAs share an
@@ -1370,6 +1720,9 @@ struct IntraArgs {
     int qkn;                   // L2-normalise the q and k tiles first
     const __nv_bfloat16* beta;
     __nv_bfloat16 *T2, *Tlo;   // null: T is not kept (plain forward)
+    // low parts (x - bf16(x)) of U and Kb, [BH*T][128] like their arrays, or
+    // null (only the backward with an upstream final-state gradient asks)
+    __nv_bfloat16 *Ulo, *Kblo;
     float* gam;
 };
 
@@ -1389,6 +1742,9 @@ __device__ __forceinline__ void intra_read_block(uint32_t taddr, float* out /* 6
     for (int j = N; j < 64; ++j) out[j] = 0.f;
 }
 
+// LO: also write the low parts of U and Kb (a.Ulo, a.Kblo); a separate
+// instantiation, so that the plain one keeps its registers.
+template <bool LO>
 __global__ void __launch_bounds__(kIntraThreads, 2)
 intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
@@ -1681,6 +2037,8 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = Ei[i] * elb[i];                 // Kb = k exp(G_last - G)
             *reinterpret_cast<uint4*>(smem + J_K + tile_off) = pack8(x);
+            if (LO)
+                *reinterpret_cast<uint4*>(a.Kblo + (size_t)(row0 + r) * kD + c0) = pack8_lo(x);
         }
         fence_async_smem();
         tc_fence_before();
@@ -1930,6 +2288,11 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             *reinterpret_cast<uint4*>(box + sw128_offset(r, 8 * j)) = pack8(e0);
             *reinterpret_cast<uint4*>(box + sw128_offset(r, 32 + 8 * j)) = pack8(e1);
+        }
+        if (LO && isU) {
+            __nv_bfloat16* ul = a.Ulo + (size_t)(row0 + r) * kD + cb * 64;
+            store_lo32(ul, x0);
+            store_lo32(ul + 32, x1);
         }
     }
     fence_async_smem();
@@ -2677,6 +3040,10 @@ struct TcWs {
     char* simt;  // SIMT workspace (fp32 quantities)
     __nv_bfloat16 *W2, *Q2, *U2, *Kb2, *Aqk2, *T2, *Tlo2;  // chain operands, T (hi, lo)
     __nv_bfloat16 *h2, *d2, *dh2, *dd2;              // backward only
+    // low parts of the two-term split (backward with an upstream final-state
+    // gradient): U, Kb, delta^T, dS^T; dhlo takes the space of U2 and Ulo,
+    // which the recompute has read before the reverse pass writes it
+    __nv_bfloat16 *Ulo, *Kblo, *d2lo, *dhlo;
     float *sbuf, *zbuf, *mbuf, *ident;               // segmented forward scan (plain forward)
 };
 
@@ -2716,6 +3083,10 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     x.W2 = bf(BH * T * kD);
     x.Q2 = bf(BH * T * kD);
     x.U2 = bf(BH * T * kD);
+    if (for_bwd) {
+        x.Ulo = bf(BH * T * kD);   // directly after U2: [BH][NT][V][K] fits both
+        x.dhlo = x.U2;
+    }
     x.Kb2 = bf(BH * T * kD);
     x.Aqk2 = bf(BH * NT * kC * kC);
     x.T2 = bf(BH * NT * kC * kC);
@@ -2725,6 +3096,8 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
         x.d2 = bf(BH * T * kD);
         x.dh2 = bf(BH * NT * kD * kD);
         x.dd2 = bf(BH * T * kD);
+        x.Kblo = bf(BH * T * kD);
+        x.d2lo = bf(BH * NT * kD * kC);
     } else if (const int P = chain_segments(d)) {
         const size_t st = (size_t)d.K * d.V * sizeof(float);
         auto f32 = [&](size_t bytes) { return reinterpret_cast<float*>(take(bytes)); };
@@ -2743,7 +3116,8 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
 // the plain forward does not).
 kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const void* k,
                         const void* v, const void* g, const void* beta, bool keep_T,
-                        cudaStream_t s, float** gam_out) {
+                        cudaStream_t s, float** gam_out, __nv_bfloat16* ulo = nullptr,
+                        __nv_bfloat16* kblo = nullptr) {
     SimtWsPtrs p;
     simt_ws_ptrs(tc_wide(d), 0, w.simt, &p);
     const int BH = d.B * d.HV, NT = d.T / kC;
@@ -2770,16 +3144,19 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     a.beta = static_cast<const __nv_bfloat16*>(beta);
     a.T2 = keep_T ? w.T2 : nullptr;
     a.Tlo = keep_T ? w.Tlo2 : nullptr;
+    a.Ulo = ulo;
+    a.Kblo = kblo;
     a.gam = p.gam;
-    if (cudaFuncSetAttribute(intra_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((ulo == nullptr) != (kblo == nullptr)) return KDA_ERR_INVALID_ARG;
+    auto kern = ulo ? intra_tc_kernel<true> : intra_tc_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)INTRA_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
     {
         TimedLaunch tl("tc_intra", s);
         // persistent: two CTAs per SM walk the chunks
         const int grid = std::min(BH * NT, 2 * sm_count());
-        intra_tc_kernel<<<grid, kIntraThreads, INTRA_SMEM, s>>>(mk, mq, mg, mv, mw2, mq2, mu2,
-                                                                 mkb2, ma2, a);
+        kern<<<grid, kIntraThreads, INTRA_SMEM, s>>>(mk, mq, mg, mv, mw2, mq2, mu2, mkb2, ma2, a);
     }
     *gam_out = p.gam;
     return launch_status();
@@ -2839,7 +3216,8 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
 // combine step; see ChainArgs), with its buffers in w.
 kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, const float* h0,
                          void* o, float* ht, __nv_bfloat16* h_out, __nv_bfloat16* delta_out,
-                         cudaStream_t s, int nseg = 0) {
+                         cudaStream_t s, int nseg = 0, const __nv_bfloat16* u_lo = nullptr,
+                         __nv_bfloat16* delta_lo = nullptr) {
     const int BH = d.B * d.HV, NT = d.T / kC;
     CUtensorMap mw, mq, mk, ma, mu;
     const uint64_t rows = (uint64_t)BH * d.T;
@@ -2853,6 +3231,8 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     // map over W when no states are kept)
     // and delta, [BH*NT*V][C]: one box of 128 rows
     if ((h_out == nullptr) != (delta_out == nullptr)) return KDA_ERR_INVALID_ARG;
+    if ((u_lo == nullptr) != (delta_lo == nullptr) || (delta_lo && (!delta_out || nseg >= 3)))
+        return KDA_ERR_INVALID_ARG;
     CUtensorMap mh, mdl, mo;
     if (!(h_out ? make_map(&mh, h_out, (uint64_t)BH * NT * kD, kD, 64, 128, true)
                 : make_map(&mh, w.W2, rows, kD, 64, 64, true)) ||
@@ -2875,20 +3255,22 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     args.ht = ht;
     args.h_out = h_out;
     args.delta_out = delta_out;
+    args.u_lo = u_lo;
+    args.delta_lo = delta_lo;
     args.nseg = 0;
     args.seglen = 0;
     args.pass = 0;
     args.sbuf = args.zbuf = args.mbuf = nullptr;
     args.ident = nullptr;
-    if (cudaFuncSetAttribute(chain_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto chain = delta_lo ? chain_fwd_kernel<true> : chain_fwd_kernel<false>;
+    if (cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)CHAIN_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (nseg < 3) {
         // three roles, timed apart: forward (o), saving forward (o and the
         // chunk-start states), and the backward's recompute (states only)
         TimedLaunch tl(!h_out ? "tc_chain_fwd" : o ? "tc_chain_fwd_save" : "tc_chain_states", s);
-        chain_fwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, mdl, mo,
-                                                               args);
+        chain<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, mdl, mo, args);
         return launch_status();
     }
     // segmented: pass 1 (segment 0 in full; later segments from zero and as
@@ -2910,7 +3292,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     {
         TimedLaunch tl("tc_chain_seg_pass1", s);
         args.pass = 1;
-        chain_fwd_kernel<<<BH * (2 * nseg - 3), kChainThreads, CHAIN_SMEM, s>>>(
+        chain<<<BH * (2 * nseg - 3), kChainThreads, CHAIN_SMEM, s>>>(
             mw, mq, mk, ma, mu, mh, mdl, mo, args);
     }
     if ((st = launch_status()) != KDA_OK) return st;
@@ -2922,7 +3304,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     {
         TimedLaunch tl("tc_chain_seg_pass3", s);
         args.pass = 3;
-        chain_fwd_kernel<<<BH * (nseg - 1), kChainThreads, CHAIN_SMEM, s>>>(
+        chain<<<BH * (nseg - 1), kChainThreads, CHAIN_SMEM, s>>>(
             mw, mq, mk, ma, mu, mh, mdl, mo, args);
     }
     return launch_status();
@@ -2964,14 +3346,22 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     tc_carve(d, 1, static_cast<char*>(ws), &w);
     float* gam = nullptr;
     kda_status st = KDA_OK;
-    if (from_saved) {
+    // An upstream final-state gradient runs the two-term path: U, Kb, delta
+    // and dS also leave their kernels as bf16 low parts, and the contractions
+    // over V take grad_v_px_kernel.  The saving forward keeps no low parts,
+    // so this path always recomputes.
+    const bool px = dht != nullptr;
+    if (from_saved && !px) {
         SimtWsPtrs p0;
         simt_ws_ptrs(tc_wide(d), 0, w.simt, &p0);  // where the intra kernel left gam
         gam = p0.gam;
     } else {
-        if ((st = run_intra_tc(d, w, q, k, v, g, beta, true, s, &gam)) != KDA_OK) return st;
+        if ((st = run_intra_tc(d, w, q, k, v, g, beta, true, s, &gam, px ? w.Ulo : nullptr,
+                               px ? w.Kblo : nullptr)) != KDA_OK)
+            return st;
         // forward recompute: chunk-start states and delta
-        if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s)) != KDA_OK)
+        if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s, 0,
+                                px ? w.Ulo : nullptr, px ? w.d2lo : nullptr)) != KDA_OK)
             return st;
     }
     const int BH = d.B * d.HV, NT = d.T / kC;
@@ -2997,12 +3387,13 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.dht = dht;
         a.dh0 = dh0;
         a.dh_out = w.dh2;
-        if (cudaFuncSetAttribute(chain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        a.dh_lo = px ? w.dhlo : nullptr;
+        auto kern = px ? chain_bwd_kernel<true> : chain_bwd_kernel<false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)CHAIN_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
         TimedLaunch tl("tc_chain_bwd", s);
-        chain_bwd_kernel<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, mdh, mddst,
-                                                               a);
+        kern<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, mdh, mddst, a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     // contractions over V
@@ -3034,14 +3425,31 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.dAqk = reinterpret_cast<__nv_bfloat16*>(p.dAqk);
         a.dTv = p.dTv;
         a.dbv = p.dbv;
-        auto kern = d.V == kD ? grad_v_kernel<kD> : grad_v_kernel<64>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)GRAD_SMEM) != cudaSuccess)
-            return KDA_ERR_CUDA;
-        TimedLaunch tl("tc_grad_v", s);
-        // persistent: one CTA per SM walks the chunks
-        kern<<<std::min(BH * NT, sm_count()), kGradThreads, GRAD_SMEM, s>>>(mh, mdh, mdo, mdd, md,
-                                                                          mv, mt, a);
+        if (px) {
+            CUtensorMap mdhl, mdl, mkb, mkbl, ma;
+            if (!make_map(&mdhl, w.dhlo, srows, kD, 64, 128, true) ||
+                !make_map(&mdl, w.d2lo, srows, kC, 64, 128, true) ||
+                !make_map(&mkb, w.Kb2, rows, kD, 64, 64, true) ||
+                !make_map(&mkbl, w.Kblo, rows, kD, 64, 64, true) ||
+                !make_map(&ma, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
+                return KDA_ERR_CUDA;
+            auto kern = d.V == kD ? grad_v_px_kernel<kD> : grad_v_px_kernel<64>;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)PX_SMEM) != cudaSuccess)
+                return KDA_ERR_CUDA;
+            TimedLaunch tl("tc_grad_v_px", s);
+            kern<<<std::min(BH * NT, sm_count()), kGradThreads, PX_SMEM, s>>>(
+                mh, mdh, mdhl, mdo, md, mdl, mkb, mkbl, ma, mv, mt, a);
+        } else {
+            auto kern = d.V == kD ? grad_v_kernel<kD> : grad_v_kernel<64>;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)GRAD_SMEM) != cudaSuccess)
+                return KDA_ERR_CUDA;
+            TimedLaunch tl("tc_grad_v", s);
+            // persistent: one CTA per SM walks the chunks
+            kern<<<std::min(BH * NT, sm_count()), kGradThreads, GRAD_SMEM, s>>>(
+                mh, mdh, mdo, mdd, md, mv, mt, a);
+        }
     }
     if ((st = launch_status()) != KDA_OK) return st;
     SimtWsPtrs p;

@@ -74,12 +74,14 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
  *                     f32 or bf16 inputs.
  *   KDA_IMPL_TCGEN05  tcgen05/TMEM tensor-core kernels; bf16, K = V = 128 or
  *                     K = V = 64 (run at 128 with the upper channels zero),
- *                     chunk 64.  KDA_ERR_UNSUPPORTED otherwise.  The
- *                     tensor-core backward does not take dht (it keeps the
- *                     chunk states as bf16, which an O(1) final-state gradient
- *                     does not fit to the accuracy bar): with dht != NULL,
- *                     AUTO runs the SIMT backward and TCGEN05 returns
- *                     KDA_ERR_UNSUPPORTED. */
+ *                     chunk 64.  KDA_ERR_UNSUPPORTED otherwise.  With
+ *                     dht != NULL the tensor-core backward runs a two-term
+ *                     variant: an O(1) final-state gradient makes the
+ *                     products of the state gradient with delta and Kb cancel
+ *                     to values far below their terms, so U, Kb, delta and
+ *                     the state gradient also leave their kernels as bf16 low
+ *                     parts (x - bf16(x)) and those products take three terms
+ *                     (hi hi + lo hi + hi lo). */
 typedef enum { KDA_IMPL_AUTO = 0, KDA_IMPL_SIMT = 1, KDA_IMPL_TCGEN05 = 2 } kda_impl;
 
 typedef struct {
@@ -141,9 +143,10 @@ kda_status kda_chunk_fwd_save(const kda_dims* dims, const void* q, const void* k
 /* Backward from a workspace filled by kda_chunk_fwd_save with the same dims
  * (impl included), inputs and h0, and not written since.  Arguments, results
  * and errors are those of kda_chunk_bwd.  The tensor-core kernels skip the
- * intra-chunk recompute and the forward state pass; a call that runs the
- * SIMT kernels (dims->impl SIMT, or AUTO with dht given) recomputes from the
- * inputs, so its results do not depend on what the workspace holds.  A
+ * intra-chunk recompute and the forward state pass unless dht is given (their
+ * two-term variant recomputes: the saving forward keeps no low parts); a call
+ * that recomputes (that one, or any call on the SIMT kernels) reads nothing
+ * saved from the workspace, so its results do not depend on what it holds.  A
  * workspace not filled as stated gives undefined results, not an error. */
 kda_status kda_chunk_bwd_saved(const kda_dims* dims, const void* q, const void* k,
                                const void* v, const void* g, const void* beta, const float* h0,

@@ -48,12 +48,15 @@ def test_tc_algorithmic_bytes_scale_with_the_workload(bench):
 
 def test_measured_traffic_scales_with_head_tokens(bench):
     w = I.TRAIN_BF16
-    for name, (tb, src, h) in bench.NCU_TRAFFIC.items():
+    for name, (tb, ht, src, h) in bench.NCU_TRAFFIC.items():
         got = bench.ncu_traffic(name, w)
         if bench._src_hash(src) != h:
             assert got is None   # source changed since the capture
             continue
-        assert got == round(tb * w.B * w.T * w.HV / bench.NCU_TRAFFIC_HEAD_TOKENS)
+        assert got == round(tb * w.B * w.T * w.HV / ht)
+        # the captured launch itself reports its own bytes
+        cap = dataclasses.replace(w, B=ht // (w.T * w.HV))
+        assert bench.ncu_traffic(name, cap) == tb
     assert bench.ncu_traffic("no_such_kernel", w) is None
 
 

@@ -78,13 +78,11 @@ def test_fp32_gva_chunks_with_h0(impl, chunk):
 
 @pytest.mark.parametrize("impl", IMPLS)
 def test_small_bf16_full(impl):
-    """bf16 B4 T512 H8 K = V = 64 with an initial state; on the tensor cores
-    (K = V = 64 run at 128 with zero-filled upper channels) without the
-    upstream final-state gradient, which their backward does not take."""
+    """bf16 B4 T512 H8 K = V = 64 with an initial state and an upstream
+    final-state gradient; on the tensor cores K = V = 64 runs at 128 with
+    zero-filled upper channels, and dht takes the two-term backward."""
     w = I.SMALL_BF16
     inp = I.make_chunk_inputs(w)
-    if impl == "tcgen05":
-        inp["dht"] = None
     res = run_gpu(inp, w, impl)
     compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
 
@@ -99,10 +97,10 @@ def test_fp32_k128_full_tile(impl):
 
 
 @pytest.mark.parametrize("impl,with_dht", [("simt", True), ("auto", True), ("simt", False),
-                                           ("tcgen05", False)])
+                                           ("tcgen05", False), ("tcgen05", True)])
 def test_bf16_gva_k128(impl, with_dht):
-    """K = V = 128 with GVA; with an O(1) upstream final-state gradient the
-    backward runs the fp32 kernels (AUTO), without it the tensor cores."""
+    """K = V = 128 with GVA, with and without an O(1) upstream final-state
+    gradient (on the tensor cores, dht takes the two-term backward)."""
     w = I.Workload("bf16_gva_k128", 2, 256, 2, 4, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
                    dht=with_dht, seed=23)
     inp = I.make_chunk_inputs(w)
@@ -115,13 +113,15 @@ def test_bf16_gva_k128(impl, with_dht):
                            g_sigma=2.0, h0_std=0.1, seed=27)),
     ("auto", I.Workload("saved_k128_dht", 1, 192, 2, 2, 128, 128, 64, torch.bfloat16,
                         g_sigma=2.0, h0_std=0.1, dht=True, seed=28)),
+    ("tcgen05", I.Workload("saved_k64_dht", 2, 192, 2, 4, 64, 64, 64, torch.bfloat16,
+                           g_sigma=2.0, h0_std=0.1, dht=True, seed=30)),
     ("simt", I.Workload("saved_simt", 2, 128, 2, 4, 32, 32, 32, torch.float32, g_sigma=2.0,
                         h0_std=0.3, dht=True, seed=29)),
 ])
 def test_saved_forward_backward(impl, wl):
     """A saving forward followed by the backward from its workspace gives the
-    oracle's outputs and gradients (the tensor cores skip the recompute; the
-    SIMT kernels and AUTO with dht recompute)."""
+    oracle's outputs and gradients (the tensor cores skip the recompute unless
+    dht is given; the SIMT kernels always recompute)."""
     t = {n: (x.cuda() if x is not None else None) for n, x in I.make_chunk_inputs(wl).items()}
     o, ht, saved = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"],
                                      initial_state=t["h0"], output_final_state=True,
@@ -176,13 +176,29 @@ def test_tcgen05_chunk_counts_and_groups(B, T, H, HV, saved, D):
     compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
 
 
-def test_tcgen05_backward_refuses_final_state_gradient():
-    w = I.Workload("bf16_dht", 1, 128, 1, 1, 128, 128, 64, torch.bfloat16, dht=True, seed=26)
-    t = {n: (x.cuda() if x is not None else None) for n, x in I.make_chunk_inputs(w).items()}
-    with pytest.raises(kda.KdaError) as ei:
-        kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], dht=t["dht"],
-                          impl="tcgen05")
-    assert ei.value.status == 3
+@pytest.mark.parametrize("B,T,H,HV,D,saved,h0", [
+    (2, 256, 2, 4, 128, False, True), (2, 256, 2, 4, 128, True, True),
+    (1, 512, 2, 2, 128, False, True), (2, 1024, 1, 1, 128, False, True),
+    (1, 64, 1, 1, 128, False, False), (1, 320, 3, 3, 64, True, True),
+    (3, 192, 1, 2, 64, False, False)])
+def test_tcgen05_final_state_gradient(B, T, H, HV, D, saved, h0):
+    """An O(1) upstream final-state gradient on the tensor cores (the two-term
+    backward: U, Kb, delta and dS split into bf16 high and low parts), with
+    GVA, K = V = 64 and 128, one to sixteen chunks, with and without h0 and a
+    saving forward: every output and gradient within the bf16 bar."""
+    w = I.Workload("tc_dht", B, T, H, HV, D, D, 64, torch.bfloat16, g_sigma=2.0,
+                   h0_std=0.1 if h0 else None, dht=True, seed=26 + T + D)
+    inp = I.make_chunk_inputs(w)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    out = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
+                            output_final_state=True, impl="tcgen05", save_for_backward=saved)
+    res = dict(o=out[0], ht=out[1])
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                 dht=t["dht"], initial_state=t["h0"], impl="tcgen05",
+                                 saved=out[2] if saved else None))
+    torch.cuda.synchronize()
+    kda.check()
+    compare_all(res, oracle_chunk(inp, True), w, with_h0=h0)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
@@ -190,7 +206,7 @@ def test_clamp_active_below_minus_five(impl):
     """Gates far below -5 reach the kernel: it must clamp them and pass no
     gradient through them (g == -5 exactly still passes)."""
     w = I.Workload("clamp", 2, 128, 2, 2, 64, 64, 64, torch.bfloat16, g_mu=3.0, g_sigma=3.0,
-                   h0_std=0.2, dht=impl != "tcgen05", seed=24)
+                   h0_std=0.2, dht=True, seed=24)
     inp = I.make_chunk_inputs(w, g_floor=None)
     g = inp["g"].float()
     g[:, :8] = -5.0  # exact boundary values
@@ -247,6 +263,26 @@ def test_qk_l2norm_in_kernel(impl, saved, D, H, HV):
     res = dict(o=out[0], ht=out[1])
     res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
                                  initial_state=t["h0"], impl=impl,
+                                 saved=out[2] if saved else None, use_qk_l2norm_in_kernel=True))
+    torch.cuda.synchronize()
+    kda.check()
+    compare_all(res, oracle_chunk(inp, True, qk_l2norm=True), w, with_h0=True)
+
+
+@pytest.mark.parametrize("saved", [False, True])
+def test_qk_l2norm_in_kernel_tcgen05_with_final_state_gradient(saved):
+    """q/k L2 normalisation in the kernels together with an upstream
+    final-state gradient on the tensor cores (GVA, K = V = 128)."""
+    w = I.Workload("qkn_dht", 2, 192, 2, 4, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
+                   h0_std=0.1, dht=True, seed=57)
+    inp = I.make_chunk_inputs(w, normalize_qk=False)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    out = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
+                            output_final_state=True, impl="tcgen05", save_for_backward=saved,
+                            use_qk_l2norm_in_kernel=True)
+    res = dict(o=out[0], ht=out[1])
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                 dht=t["dht"], initial_state=t["h0"], impl="tcgen05",
                                  saved=out[2] if saved else None, use_qk_l2norm_in_kernel=True))
     torch.cuda.synchronize()
     kda.check()
