@@ -373,6 +373,43 @@ def measure_forward(kda, w, dev, hbm, steps, warmup, path):
                         for n, (t, c) in sorted(kernels.items(), key=lambda x: -x[1][0])}}
 
 
+def measure_chunk_sizes(kda, dev, steps=10, warmup=3):
+    """The fwd+bwd step (stateless forward with the final state, backward
+    with dht and dh0) at the K = V = 64 shape with an initial state
+    (B=4, T=512, H=HV=8, bf16) for chunk 64 (AUTO: the tensor cores) and
+    chunk 128 (AUTO: the CUDA-core kernels, the only ones with 128-row
+    tiles), timed with CUDA events.  A small, launch-bound shape: tokens/s
+    only, no roofline."""
+    from gated_delta_rule_41_gb300 import inputs as I
+    w = I.SMALL_BF16
+    t = I.make_chunk_inputs(w, device=dev)
+    out = {}
+    for chunk in (64, 128):
+        def step():
+            o, ht = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                      initial_state=t["h0"], output_final_state=True,
+                                      chunk_size=chunk)
+            kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], dht=t["dht"],
+                              initial_state=t["h0"], chunk_size=chunk)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        kda.check()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        kda.check()
+        ms = e0.elapsed_time(e1) / steps
+        out[f"chunk_{chunk}"] = {"ms_per_step": ms, "tokens_per_s": w.tokens / (ms / 1e3),
+                                 "path": "tcgen05" if chunk == 64 else "simt"}
+    out["workload"] = w.name
+    out["pass"] = "fwd+bwd, dht and h0, stateless backward"
+    return out
+
+
 def measure_decode(kda, dev, hbm):
     """Decode step at B=256, HV=16, K=V=128 (state 256 MiB fp32), 64 steps,
     timed with CUDA events; HBM roofline of the step."""
@@ -652,6 +689,7 @@ def main():
                                                        args.path)
     if world == 1 and args.part == "all":
         line["decode"] = measure_decode(kda, dev, hbm)
+        line["chunk_sizes"] = measure_chunk_sizes(kda, dev)
     if world == 1 and not args.no_cpu_baseline and args.part == "all":
         import oracle
         oracle.build()

@@ -25,7 +25,7 @@ kda_status check_common(const kda_dims* d, bool need_chunk) {
     if ((long long)d->B * d->HV > 65535) return KDA_ERR_UNSUPPORTED;
     if (need_chunk) {
         const int c = d->chunk_size;
-        if (c != 16 && c != 32 && c != 64) return KDA_ERR_UNSUPPORTED;
+        if (c != 16 && c != 32 && c != 64 && c != 128) return KDA_ERR_UNSUPPORTED;
         if (d->T % c != 0) return KDA_ERR_SHAPE;
     }
     return KDA_OK;

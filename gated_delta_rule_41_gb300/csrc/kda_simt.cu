@@ -1,5 +1,5 @@
-// Generic fp32 CUDA-core (SIMT) chunk scan: any K, V <= 128, chunk 16/32/64,
-// f32 or bf16 inputs, all arithmetic in fp32.
+// Generic fp32 CUDA-core (SIMT) chunk scan: any K, V <= 128, chunk 16/32/64
+// or 128, f32 or bf16 inputs, all arithmetic in fp32.
 //
 // Chunk form (K3 README, table 实现路线表, row L2: (1) cumsum of the clamped
 // gate inside each chunk, (2) the lower-triangular system, (3) the solve,
@@ -40,12 +40,20 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVT = 32;  // value columns per CTA in the state passes
+// Chunks of 128 rows (BIG instantiations): a chunk's C x C matrices and
+// some C x K arrays no longer fit in shared memory beside its k, q and G
+// rows, so they live in a per-(chunk, head) scratch area of the workspace
+// (5 C (C + 1) floats), the state passes read their operands from the
+// workspace arrays directly, and the per-thread result arrays hold
+// C * max(C, K) / 256 = 64 values.
+constexpr int kScratchMats = 5;
 
 struct Ws {
     float *W, *U, *Qh, *Kb, *Aqk, *Tm, *gam, *dlt;   // forward quantities
     float *hs, *dhs, *ddl;                           // bwd: states, state grads, ddelta
     float *dQh, *dWm, *dKb, *dgam, *dAqk, *dTv, *dbv;  // bwd: V contractions
     float *dqh, *dkh;                                // bwd: dq, dk per value head (fp32)
+    float* scr;   // C > 64: kScratchMats C x (C + 1) floats per (chunk, head)
 };
 
 struct Dims {
@@ -104,6 +112,7 @@ size_t carve(const Dims& d, int for_bwd, char* base, Ws* w) {
     x.Tm = take(BH * NT * C * C);
     x.gam = take(BH * NT * K);
     x.dlt = take(BH * T * V);
+    if (C > 64) x.scr = take(BH * NT * kScratchMats * C * (C + 1));
     if (for_bwd) {
         x.hs = take(BH * NT * K * V);
         x.dhs = take(BH * NT * K * V);
@@ -161,11 +170,13 @@ __device__ __forceinline__ void l2norm_rows(float* kS, float* qS, int C, int K, 
 // intra: per (chunk, head)
 // smem: k[C][K+1], qs[C][K+1], G[C][K+1], A[C][C+1], Tm[C][C+1], beta[C]
 // ---------------------------------------------------------------------------
+// (BIG: A and Tm in the chunk's scratch area instead)
 size_t intra_smem(const Dims& d) {
-    return sizeof(float) * (3 * (size_t)d.C * (d.K + 1) + 2 * (size_t)d.C * (d.C + 1) + d.C);
+    const size_t mats = d.C > 64 ? 0 : 2 * (size_t)d.C * (d.C + 1);
+    return sizeof(float) * (3 * (size_t)d.C * (d.K + 1) + mats + d.C);
 }
 
-template <typename Tin>
+template <typename Tin, bool BIG>
 __global__ void __launch_bounds__(kThreads)
 intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
              const Tin* __restrict__ v, const Tin* __restrict__ g, const Tin* __restrict__ beta) {
@@ -179,9 +190,9 @@ intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     float* kS = sm;
     float* qS = kS + C * KP;
     float* GS = qS + C * KP;
-    float* A = GS + C * KP;
+    float* A = BIG ? w.scr + ((size_t)bh * d.NT + n) * kScratchMats * C * CP : GS + C * KP;
     float* Tm = A + C * CP;
-    float* bS = Tm + C * CP;
+    float* bS = BIG ? GS + C * KP : Tm + C * CP;
     const int t0 = cr.t0, len = cr.len;
 
     // rows past a sequence's end enter as q = k = v = 0, g = 0, beta = 0:
@@ -276,12 +287,13 @@ intra_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
 // mode bits: 1 = write o, 2 = store h (state at chunk start) and delta.
 // smem: W[C][K], Qh[C][K], Kb[C][K], Aqk[C][C], gam[K], S[K][VT], U/delta[C][VT]
 // ---------------------------------------------------------------------------
+// (BIG: W, Qh, Kb and Aqk are read from the workspace arrays in place)
 size_t statef_smem(const Dims& d) {
-    return sizeof(float) * (3 * (size_t)d.C * d.K + (size_t)d.C * d.C + d.K +
-                            (size_t)d.K * kVT + 2 * (size_t)d.C * kVT);
+    const size_t ops = d.C > 64 ? 0 : 3 * (size_t)d.C * d.K + (size_t)d.C * d.C;
+    return sizeof(float) * (ops + d.K + (size_t)d.K * kVT + 2 * (size_t)d.C * kVT);
 }
 
-template <typename Tout>
+template <typename Tout, bool BIG>
 __global__ void __launch_bounds__(kThreads)
 state_fwd_kernel(Dims d, Ws w, const float* __restrict__ h0, Tout* __restrict__ o,
                  float* __restrict__ ht, int mode) {
@@ -296,11 +308,12 @@ state_fwd_kernel(Dims d, Ws w, const float* __restrict__ h0, Tout* __restrict__ 
     const int VT = min(kVT, V - j0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     extern __shared__ float sm[];
+    const int ops = BIG ? 0 : 3 * C * K + C * C;
     float* Ws_ = sm;
     float* Qs = Ws_ + C * K;
     float* Kbs = Qs + C * K;
     float* As = Kbs + C * K;
-    float* gs = As + C * C;
+    float* gs = sm + ops;
     float* S = gs + K;
     float* Us = S + K * kVT;
     float* Ds = Us + C * kVT;
@@ -313,12 +326,20 @@ state_fwd_kernel(Dims d, Ws w, const float* __restrict__ h0, Tout* __restrict__ 
         __syncthreads();
         const ChunkRef cr = chunk_ref(d, bw, n);
         const size_t row0 = (size_t)bw * d.T + (size_t)n * C;
-        for (int i = tid; i < C * K; i += kThreads) {
-            Ws_[i] = w.W[row0 * K + i];
-            Qs[i] = w.Qh[row0 * K + i];
-            Kbs[i] = w.Kb[row0 * K + i];
+        if (BIG) {
+            Ws_ = w.W + row0 * K;
+            Qs = w.Qh + row0 * K;
+            Kbs = w.Kb + row0 * K;
+            As = w.Aqk + ((size_t)bw * d.NT + n) * C * C;
+        } else {
+            for (int i = tid; i < C * K; i += kThreads) {
+                Ws_[i] = w.W[row0 * K + i];
+                Qs[i] = w.Qh[row0 * K + i];
+                Kbs[i] = w.Kb[row0 * K + i];
+            }
+            for (int i = tid; i < C * C; i += kThreads)
+                As[i] = w.Aqk[((size_t)bw * d.NT + n) * C * C + i];
         }
-        for (int i = tid; i < C * C; i += kThreads) As[i] = w.Aqk[((size_t)bw * d.NT + n) * C * C + i];
         for (int c = tid; c < K; c += kThreads) gs[c] = w.gam[((size_t)bw * d.NT + n) * K + c];
         for (int i = tid; i < C * kVT; i += kThreads) {
             const int r = i / kVT, j = i % kVT;
@@ -371,7 +392,7 @@ state_fwd_kernel(Dims d, Ws w, const float* __restrict__ h0, Tout* __restrict__ 
 // state_b: per (V tile, head); reverse over chunks.
 // smem: W[C][K], Qh[C][K], Kb[C][K], Aqk[C][C], gam[K], dS[K][VT], dO[C][VT], dd[C][VT]
 // ---------------------------------------------------------------------------
-template <typename Tin>
+template <typename Tin, bool BIG>
 __global__ void __launch_bounds__(kThreads)
 state_bwd_kernel(Dims d, Ws w, const Tin* __restrict__ dout, const float* __restrict__ dht,
                  float* __restrict__ dh0) {
@@ -384,11 +405,12 @@ state_bwd_kernel(Dims d, Ws w, const Tin* __restrict__ dout, const float* __rest
     const int VT = min(kVT, V - j0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     extern __shared__ float sm[];
+    const int ops = BIG ? 0 : 3 * C * K + C * C;
     float* Ws_ = sm;
     float* Qs = Ws_ + C * K;
     float* Kbs = Qs + C * K;
     float* As = Kbs + C * K;
-    float* gs = As + C * C;
+    float* gs = sm + ops;
     float* dS = gs + K;
     float* dOs = dS + K * kVT;
     float* dds = dOs + C * kVT;
@@ -401,12 +423,20 @@ state_bwd_kernel(Dims d, Ws w, const Tin* __restrict__ dout, const float* __rest
         __syncthreads();
         const ChunkRef cr = chunk_ref(d, bw, n);
         const size_t row0 = (size_t)bw * d.T + (size_t)n * C;
-        for (int i = tid; i < C * K; i += kThreads) {
-            Ws_[i] = w.W[row0 * K + i];
-            Qs[i] = w.Qh[row0 * K + i];
-            Kbs[i] = w.Kb[row0 * K + i];
+        if (BIG) {
+            Ws_ = w.W + row0 * K;
+            Qs = w.Qh + row0 * K;
+            Kbs = w.Kb + row0 * K;
+            As = w.Aqk + ((size_t)bw * d.NT + n) * C * C;
+        } else {
+            for (int i = tid; i < C * K; i += kThreads) {
+                Ws_[i] = w.W[row0 * K + i];
+                Qs[i] = w.Qh[row0 * K + i];
+                Kbs[i] = w.Kb[row0 * K + i];
+            }
+            for (int i = tid; i < C * C; i += kThreads)
+                As[i] = w.Aqk[((size_t)bw * d.NT + n) * C * C + i];
         }
-        for (int i = tid; i < C * C; i += kThreads) As[i] = w.Aqk[((size_t)bw * d.NT + n) * C * C + i];
         for (int c = tid; c < K; c += kThreads) gs[c] = w.gam[((size_t)bw * d.NT + n) * K + c];
         for (int i = tid; i < C * kVT; i += kThreads) {
             const int r = i / kVT, j = i % kVT;
@@ -455,13 +485,14 @@ state_bwd_kernel(Dims d, Ws w, const Tin* __restrict__ dout, const float* __rest
 // ---------------------------------------------------------------------------
 constexpr int kVS = 32, kVSP = 33;
 constexpr int kMaxPer = 32;  // C*K/256 and C*C/256 upper bounds (C<=64, K<=128)
+constexpr int kMaxPerBig = 64;  // the same for C = 128
 
 size_t vgrad_smem(const Dims& d) {
     return sizeof(float) * (2 * (size_t)d.K * kVSP + 4 * (size_t)d.C * kVSP +
                             (size_t)d.C * (d.C + 1) + 2 * (size_t)d.C);
 }
 
-template <typename Tin>
+template <typename Tin, bool BIG>
 __global__ void __launch_bounds__(kThreads)
 vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ beta,
              const Tin* __restrict__ dout, Tin* __restrict__ dv) {
@@ -471,6 +502,8 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
     const int b = cr.b, hv = bh % d.HV, t0 = cr.t0, len = cr.len;
     const int C = d.C, K = d.K, V = d.V, CP = C + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int KMP = BIG ? kMaxPerBig : kMaxPer;
+    constexpr int UNR = BIG ? 1 : KMP;   // (BIG: the arrays live in local memory)
     extern __shared__ float sm[];
     float* S0 = sm;
     float* dSs = S0 + K * kVSP;
@@ -497,9 +530,9 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
     // (r, m) outputs with m = tid % C, r = tid / C + i * (256 / C)
     const int mc = tid % C, rcstep = kThreads / C;
     const int nrc = (C * C + kThreads - 1) / kThreads;
-    float aQ[kMaxPer], aW[kMaxPer], aKb[kMaxPer], aAq[kMaxPer], aTv[kMaxPer];
-#pragma unroll
-    for (int i = 0; i < kMaxPer; ++i) aQ[i] = aW[i] = aKb[i] = aAq[i] = aTv[i] = 0.f;
+    float aQ[KMP], aW[KMP], aKb[KMP], aAq[KMP], aTv[KMP];
+#pragma unroll UNR
+    for (int i = 0; i < KMP; ++i) aQ[i] = aW[i] = aKb[i] = aAq[i] = aTv[i] = 0.f;
     float agam = 0.f;
 
     for (int j0 = 0; j0 < V; j0 += kVS) {
@@ -525,8 +558,8 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
         for (int j = 0; j < kVS; ++j) {
             const float s0 = S0[ck * kVSP + j], ds = dSs[ck * kVSP + j];
             if (tid < K) agam += ds * s0;
-#pragma unroll
-            for (int i = 0; i < kMaxPer; ++i) {
+#pragma unroll UNR
+            for (int i = 0; i < KMP; ++i) {
                 if (i < nrk) {
                     const int r = tid / K + i * rstep;
                     if (r < C) {
@@ -540,8 +573,8 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
         // C x C contractions
         for (int j = 0; j < kVS; ++j) {
             const float dlm = dls[mc * kVSP + j], vm = vs[mc * kVSP + j];
-#pragma unroll
-            for (int i = 0; i < kMaxPer; ++i) {
+#pragma unroll UNR
+            for (int i = 0; i < KMP; ++i) {
                 if (i < nrc) {
                     const int r = tid / C + i * rcstep;
                     if (r < C) {
@@ -564,8 +597,8 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
         }
     }
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kMaxPer; ++i) {
+#pragma unroll UNR
+    for (int i = 0; i < KMP; ++i) {
         if (i < nrk) {
             const int r = tid / K + i * rstep;
             if (r < C) {
@@ -592,12 +625,18 @@ vgrad_kernel(Dims d, Ws w, const Tin* __restrict__ v, const Tin* __restrict__ be
 // smem: k[C][K+1], qs[C][K+1], G[C][K+1], X[C][K+1], Y[C][K+1],
 //       Tm[C][C+1], dAqk[C][C+1], D[C][C+1], beta[C], dbeta[C]
 // ---------------------------------------------------------------------------
+// Factor tables for NB = C / 16 row blocks: Fb holds NB (NB + 1) / 2 block
+// pairs, eGbS and eLbS NB blocks, each K wide.  (BIG: X, Y, Tm, dAqk and D
+// in the chunk's scratch area instead of shared memory.)
 size_t kgrad_smem(const Dims& d) {
-    return sizeof(float) * (5 * (size_t)d.C * (d.K + 1) + 3 * (size_t)d.C * (d.C + 1) + 2 * d.C +
-                            18 * (size_t)d.K);
+    const size_t NB = d.C / 16;
+    const size_t mats =
+        d.C > 64 ? 0 : 2 * (size_t)d.C * (d.K + 1) + 3 * (size_t)d.C * (d.C + 1);
+    return sizeof(float) * (3 * (size_t)d.C * (d.K + 1) + mats + 2 * d.C +
+                            (NB * (NB + 1) / 2 + 2 * NB) * (size_t)d.K);
 }
 
-template <typename Tin>
+template <typename Tin, bool BIG>
 __global__ void __launch_bounds__(kThreads)
 kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
              const Tin* __restrict__ g, const Tin* __restrict__ beta, Tin* __restrict__ dg,
@@ -608,20 +647,27 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     const int b = cr.b, hv = bh % d.HV, h = hv / d.G, len = cr.len;
     const int C = d.C, K = d.K, KP = K + 1, CP = C + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int KMP = BIG ? kMaxPerBig : kMaxPer;
+    constexpr int UNR = BIG ? 1 : KMP;   // (BIG: the arrays live in local memory)
+    const int NB = C / 16;
     extern __shared__ float sm[];
     float* kS = sm;
     float* qS = kS + C * KP;
     float* GS = qS + C * KP;
-    float* X = GS + C * KP;   // dW, then d(beta khat)
-    float* Y = X + C * KP;    // beta khat, then dG
-    float* Tm = Y + C * KP;
+    // the five matrices: in shared memory, or (BIG) in the chunk's scratch
+    // area, each C x (C + 1) floats there
+    float* mats = BIG ? w.scr + ((size_t)bh * d.NT + n) * kScratchMats * C * CP : GS + C * KP;
+    const int XS = BIG ? C * CP : C * KP;   // space of X and of Y
+    float* X = mats;          // dW, then d(beta khat)
+    float* Y = X + XS;        // beta khat, then dG
+    float* Tm = Y + XS;
     float* dAq = Tm + C * CP;
     float* D = dAq + C * CP;  // dT -> dT T^T -> dA
-    float* bS = D + C * CP;
+    float* bS = BIG ? GS + C * KP : D + C * CP;
     float* dbS = bS + C;
-    float* Fb = dbS + C;              // Fb[fidx(R,J)*K + c] = exp(G_bR - G_bJ), J <= R
-    float* eGbS = Fb + 10 * K;        // eGbS[R*K + c] = exp(G_bR)
-    float* eLbS = eGbS + 4 * K;       // eLbS[R*K + c] = exp(G_last - G_bR)
+    float* Fb = dbS + C;                    // Fb[fidx(R,J)*K + c] = exp(G_bR - G_bJ), J <= R
+    float* eGbS = Fb + NB * (NB + 1) / 2 * K;   // eGbS[R*K + c] = exp(G_bR)
+    float* eLbS = eGbS + NB * K;                // eLbS[R*K + c] = exp(G_last - G_bR)
     const int t0 = cr.t0;
     const size_t row0 = (size_t)bh * d.T + (size_t)n * C;
     const size_t cc0 = ((size_t)bh * d.NT + n) * C * C;
@@ -676,10 +722,10 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     // dbeta += sum_c d(beta khat)[m][c] khat[m][c], with d(beta khat) = T^T dW
     // and in the same pass: X <- T^T dW
     {
-        float reg[kMaxPer];
+        float reg[KMP];
         const int nr = (C * K + kThreads - 1) / kThreads;
-#pragma unroll
-        for (int u = 0; u < kMaxPer; ++u) {
+#pragma unroll UNR
+        for (int u = 0; u < KMP; ++u) {
             reg[u] = 0.f;
             if (u < nr) {
                 const int i = tid + u * kThreads;
@@ -692,8 +738,8 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int u = 0; u < kMaxPer; ++u) {
+#pragma unroll UNR
+        for (int u = 0; u < KMP; ++u) {
             if (u < nr) {
                 const int i = tid + u * kThreads;
                 if (i < C * K) X[(i / K) * KP + i % K] = reg[u];
@@ -701,9 +747,9 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
         }
         // Y2 = dT T^T  (into registers, then back into D)
         const int nrc = (C * C + kThreads - 1) / kThreads;
-        float rc[kMaxPer];
-#pragma unroll
-        for (int u = 0; u < kMaxPer; ++u) {
+        float rc[KMP];
+#pragma unroll UNR
+        for (int u = 0; u < KMP; ++u) {
             rc[u] = 0.f;
             if (u < nrc) {
                 const int p = tid + u * kThreads;
@@ -716,8 +762,8 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int u = 0; u < kMaxPer; ++u) {
+#pragma unroll UNR
+        for (int u = 0; u < KMP; ++u) {
             if (u < nrc) {
                 const int p = tid + u * kThreads;
                 if (p < C * C) D[(p / C) * CP + p % C] = rc[u];
@@ -725,8 +771,8 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
         }
         __syncthreads();
         // dA = -mask_strict(T^T Y2)
-#pragma unroll
-        for (int u = 0; u < kMaxPer; ++u) {
+#pragma unroll UNR
+        for (int u = 0; u < KMP; ++u) {
             rc[u] = 0.f;
             if (u < nrc) {
                 const int p = tid + u * kThreads;
@@ -740,8 +786,8 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int u = 0; u < kMaxPer; ++u) {
+#pragma unroll UNR
+        for (int u = 0; u < KMP; ++u) {
             if (u < nrc) {
                 const int p = tid + u * kThreads;
                 if (p < C * C) D[(p / C) * CP + p % C] = rc[u];
@@ -757,10 +803,9 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     // (reference b = first row of the block): e(t,j) = E_t F[R(t)][R(j)] / E_j
     // with E_r = exp(G_r - G_b(r)) in [e^-75, 1] and F[R][J] = exp(G_bR - G_bJ),
     // so the inner loops are plain FMAs over tables and no factor overflows.
-    const int NB = C / 16;
     auto fidx = [](int R, int J) { return R * (R + 1) / 2 + J; };
-    for (int i = tid; i < 16 * K; i += kThreads) {
-        const int R = i / (4 * K), J = (i / K) % 4, c = i % K;
+    for (int i = tid; i < NB * NB * K; i += kThreads) {
+        const int R = i / (NB * K), J = (i / K) % NB, c = i % K;
         if (R < NB && J <= R)
             Fb[fidx(R, J) * K + c] = expf(GS[16 * R * KP + c] - GS[16 * J * KP + c]);
     }
@@ -776,9 +821,9 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
     }
     __syncthreads();
     const int nper = (C * K + kThreads - 1) / kThreads;
-    float sAr[kMaxPer], sQr[kMaxPer], dKr[kMaxPer];
-#pragma unroll
-    for (int u = 0; u < kMaxPer; ++u) {
+    float sAr[KMP], sQr[KMP], dKr[KMP];
+#pragma unroll UNR
+    for (int u = 0; u < KMP; ++u) {
         sAr[u] = sQr[u] = dKr[u] = 0.f;
         const int i = tid + u * kThreads;
         if (u < nper && i < C * K) {
@@ -811,9 +856,9 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
         Y[r * KP + c] = qS[r * KP + c] * E;
     }
     __syncthreads();
-    float dGr[kMaxPer], dbr[kMaxPer];
-#pragma unroll
-    for (int u = 0; u < kMaxPer; ++u) {
+    float dGr[KMP], dbr[KMP];
+#pragma unroll UNR
+    for (int u = 0; u < KMP; ++u) {
         dGr[u] = dbr[u] = 0.f;
         const int i = tid + u * kThreads;
         if (u < nper && i < C * K) {
@@ -853,8 +898,8 @@ kgrad_kernel(Dims d, Ws w, const Tin* __restrict__ q, const Tin* __restrict__ k,
         }
     }
     __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kMaxPer; ++u) {
+#pragma unroll UNR
+    for (int u = 0; u < KMP; ++u) {
         const int i = tid + u * kThreads;
         if (u < nper && i < C * K) {
             const int r = i / K, c = i % K;
@@ -1020,10 +1065,11 @@ kda_status run_intra(const Dims& d, const Ws& w, const void* q, const void* k, c
                      const void* g, const void* beta, cudaStream_t s) {
     kda_status st;
     const size_t si = intra_smem(d);
-    if ((st = set_smem(intra_kernel<Tin>, si)) != KDA_OK) return st;
+    auto intra = d.C > 64 ? intra_kernel<Tin, true> : intra_kernel<Tin, false>;
+    if ((st = set_smem(intra, si)) != KDA_OK) return st;
     {
         TimedLaunch tl("simt_intra", s);
-        intra_kernel<Tin><<<dim3(d.NT, d.B * d.HV), kThreads, si, s>>>(
+        intra<<<dim3(d.NT, d.B * d.HV), kThreads, si, s>>>(
             d, w, static_cast<const Tin*>(q), static_cast<const Tin*>(k),
             static_cast<const Tin*>(v), static_cast<const Tin*>(g), static_cast<const Tin*>(beta));
     }
@@ -1037,10 +1083,11 @@ kda_status run_forward_parts(const Dims& d, const Ws& w, const void* q, const vo
     kda_status st = run_intra<Tin>(d, w, q, k, v, g, beta, s);
     if (st != KDA_OK) return st;
     const size_t sf = statef_smem(d);
-    if ((st = set_smem(state_fwd_kernel<Tin>, sf)) != KDA_OK) return st;
+    auto statef = d.C > 64 ? state_fwd_kernel<Tin, true> : state_fwd_kernel<Tin, false>;
+    if ((st = set_smem(statef, sf)) != KDA_OK) return st;
     {
         TimedLaunch tl("simt_state_fwd", s);
-        state_fwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, d.NS), kThreads, sf, s>>>(
+        statef<<<dim3((d.V + kVT - 1) / kVT, d.NS), kThreads, sf, s>>>(
             d, w, h0, static_cast<Tin*>(o), ht, mode);
     }
     return launch_status();
@@ -1070,11 +1117,12 @@ kda_status simt_tail_t(const Dims& d, const Ws& w, const void* q, const void* k,
                        cudaStream_t s) {
     kda_status st;
     const size_t sk = kgrad_smem(d);
-    if ((st = set_smem(kgrad_kernel<Tin>, sk)) != KDA_OK) return st;
+    auto kgrad = d.C > 64 ? kgrad_kernel<Tin, true> : kgrad_kernel<Tin, false>;
+    if ((st = set_smem(kgrad, sk)) != KDA_OK) return st;
     const int BH = d.B * d.HV;
     {
         TimedLaunch tl("simt_kgrad", s);
-        kgrad_kernel<Tin><<<dim3(d.NT, BH), kThreads, sk, s>>>(
+        kgrad<<<dim3(d.NT, BH), kThreads, sk, s>>>(
             d, w, static_cast<const Tin*>(q), static_cast<const Tin*>(k),
             static_cast<const Tin*>(g), static_cast<const Tin*>(beta), static_cast<Tin*>(dg),
             static_cast<Tin*>(dbeta));
@@ -1100,18 +1148,20 @@ kda_status simt_bwd_t(const Dims& d, const Ws& w, const void* q, const void* k, 
     kda_status st = run_forward_parts<Tin>(d, w, q, k, v, g, beta, h0, nullptr, nullptr, 2, s);
     if (st != KDA_OK) return st;
     const size_t sb = statef_smem(d), sv = vgrad_smem(d);
-    if ((st = set_smem(state_bwd_kernel<Tin>, sb)) != KDA_OK) return st;
-    if ((st = set_smem(vgrad_kernel<Tin>, sv)) != KDA_OK) return st;
+    auto stateb = d.C > 64 ? state_bwd_kernel<Tin, true> : state_bwd_kernel<Tin, false>;
+    auto vgrad = d.C > 64 ? vgrad_kernel<Tin, true> : vgrad_kernel<Tin, false>;
+    if ((st = set_smem(stateb, sb)) != KDA_OK) return st;
+    if ((st = set_smem(vgrad, sv)) != KDA_OK) return st;
     const int BH = d.B * d.HV;
     {
         TimedLaunch tl("simt_state_bwd", s);
-        state_bwd_kernel<Tin><<<dim3((d.V + kVT - 1) / kVT, d.NS), kThreads, sb, s>>>(
+        stateb<<<dim3((d.V + kVT - 1) / kVT, d.NS), kThreads, sb, s>>>(
             d, w, static_cast<const Tin*>(dout), dht, dh0);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     {
         TimedLaunch tl("simt_vgrad", s);
-        vgrad_kernel<Tin><<<dim3(d.NT, BH), kThreads, sv, s>>>(
+        vgrad<<<dim3(d.NT, BH), kThreads, sv, s>>>(
             d, w, static_cast<const Tin*>(v), static_cast<const Tin*>(beta),
             static_cast<const Tin*>(dout), static_cast<Tin*>(dv));
     }

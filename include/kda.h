@@ -58,7 +58,7 @@ typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1,  /* null pointer where one is required, bad flag */
     KDA_ERR_SHAPE = 2,        /* non-positive size, HV % H != 0, T % chunk != 0 */
-    KDA_ERR_UNSUPPORTED = 3,  /* K or V > 128, chunk not in {16,32,64}, impl not
+    KDA_ERR_UNSUPPORTED = 3,  /* K or V > 128, chunk not in {16,32,64,128}, impl not
                                  available for these sizes or this dtype */
     KDA_ERR_ALIGNMENT = 4,    /* a pointer is misaligned (see Alignment above) */
     KDA_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
@@ -70,8 +70,10 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
 /* Which kernel family runs the chunk scan.
  *   KDA_IMPL_AUTO     tensor-core path when it supports the sizes, else SIMT.
- *   KDA_IMPL_SIMT     fp32 CUDA-core kernels; any K, V <= 128, chunk 16/32/64,
- *                     f32 or bf16 inputs.
+ *   KDA_IMPL_SIMT     fp32 CUDA-core kernels; any K, V <= 128, chunk 16/32/64
+ *                     or 128, f32 or bf16 inputs.  At chunk 128 a chunk's
+ *                     C x C matrices live in the workspace, not in shared
+ *                     memory (a slower tile configuration).
  *   KDA_IMPL_TCGEN05  tcgen05/TMEM tensor-core kernels; bf16, K = V = 128 or
  *                     K = V = 64 (run at 128 with the upper channels zero),
  *                     chunk 64.  KDA_ERR_UNSUPPORTED otherwise.  With
@@ -86,7 +88,8 @@ typedef enum { KDA_IMPL_AUTO = 0, KDA_IMPL_SIMT = 1, KDA_IMPL_TCGEN05 = 2 } kda_
 
 typedef struct {
     int B, T, H, HV, K, V;
-    int chunk_size;   /* 16, 32 or 64; T % chunk_size == 0 (ignored by the decode step) */
+    int chunk_size;   /* 16, 32, 64 or 128 (128: the SIMT kernels only; AUTO picks them);
+                       * T % chunk_size == 0 (ignored by the decode step) */
     float scale;      /* multiplies q; pass 1/sqrt(K) for the standard scale */
     kda_dtype dtype;
     kda_impl impl;

@@ -52,6 +52,11 @@ def test_workspace_sizes(lib):
     bwd = lib.kda_chunk_workspace_bytes(ctypes.byref(d), 1)
     assert 0 < fwd < bwd
     assert fwd % 256 == 0 and bwd % 256 == 0
+    # chunk 128: the SIMT kernels (AUTO or SIMT), not the tensor cores
+    c128 = dims(T=256, chunk_size=128)
+    assert lib.kda_chunk_workspace_bytes(ctypes.byref(c128), 1) > 0
+    assert lib.kda_chunk_workspace_bytes(ctypes.byref(dims(T=256, chunk_size=128, impl=1)), 0) > 0
+    assert lib.kda_chunk_workspace_bytes(ctypes.byref(dims(T=256, chunk_size=128, impl=2)), 0) == 0
     for bad in (dims(T=100), dims(HV=3), dims(K=256), dims(chunk_size=48), dims(dtype=7),
                 dims(impl=9)):
         assert lib.kda_chunk_workspace_bytes(ctypes.byref(bad), 0) == 0

@@ -67,13 +67,50 @@ def test_tiny_gva_fp32(impl):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128])
 def test_fp32_gva_chunks_with_h0(impl, chunk):
     w = I.Workload("fp32_gva", 2, 128, 2, 4, 32, 32, chunk, torch.float32, g_sigma=2.0,
                    h0_std=0.3, dht=True, seed=21)
     inp = I.make_chunk_inputs(w)
     res = run_gpu(inp, w, impl)
     compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
+
+
+@pytest.mark.parametrize("dtype,K,H,HV,qkn", [(torch.float32, 32, 2, 2, False),
+                                              (torch.float32, 16, 1, 2, False),
+                                              (torch.bfloat16, 64, 2, 4, False),
+                                              (torch.bfloat16, 128, 2, 2, False),
+                                              (torch.bfloat16, 128, 1, 2, True)])
+def test_chunk_128(dtype, K, H, HV, qkn):
+    """Chunks of 128 rows (the K3 README's 关键约束 / 风险点 table, row
+    chunk_size: 64 by default, 128 on a large-memory GPU) on the CUDA-core
+    kernels, whose C x C matrices then live in the workspace: three chunks
+    with an initial state and an upstream final-state gradient, with GVA and
+    the in-kernel q/k normalisation; every output and gradient against the
+    oracle, through AUTO (which picks those kernels) and the saving forward."""
+    w = I.Workload("chunk128", 2, 384, H, HV, K, K, 128, dtype, g_sigma=2.0, h0_std=0.1,
+                   dht=True, seed=81 + K + H)
+    inp = I.make_chunk_inputs(w, normalize_qk=not qkn)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    out = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
+                            output_final_state=True, chunk_size=128, save_for_backward=True,
+                            use_qk_l2norm_in_kernel=qkn)
+    res = dict(o=out[0], ht=out[1])
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                 dht=t["dht"], initial_state=t["h0"], chunk_size=128,
+                                 saved=out[2], use_qk_l2norm_in_kernel=qkn))
+    torch.cuda.synchronize()
+    kda.check()
+    compare_all(res, oracle_chunk(inp, True, qk_l2norm=qkn), w, with_h0=True)
+
+
+def test_chunk_128_refused_on_tensor_cores():
+    w = I.Workload("chunk128_tc", 1, 256, 1, 1, 128, 128, 128, torch.bfloat16, seed=85)
+    t = {n: (x.cuda() if x is not None else None) for n, x in I.make_chunk_inputs(w).items()}
+    with pytest.raises(kda.KdaError) as ei:
+        kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], chunk_size=128,
+                          impl="tcgen05")
+    assert ei.value.status == 3
 
 
 @pytest.mark.parametrize("impl", IMPLS)

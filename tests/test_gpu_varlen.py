@@ -89,7 +89,7 @@ def compare(res, ref, dtype, with_h0=True):
         assert_close("dh0", res["dh0"], ref["dh0"], dtype)
 
 
-@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128])
 def test_varlen_fp32_gva_ragged_and_empty_sequences(chunk):
     lengths = [1, 37, 64, 100, 0, 130]
     inp, cu = packed_inputs(lengths, 2, 4, 32, 32, torch.float32, seed=61 + chunk)
