@@ -23,6 +23,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -410,6 +412,47 @@ def measure_chunk_sizes(kda, dev, steps=10, warmup=3):
     return out
 
 
+def measure_varlen(kda, dev, steps=5, warmup=3):
+    """Packed variable-length sequences at the training head shape (H=HV=16,
+    K=V=128, bf16): 32768 tokens cut into seeded lengths of 512 to 4096,
+    fwd+bwd (stateless backward) through kda_chunk_fwd_varlen /
+    _bwd_varlen on the tensor cores (AUTO) and on the CUDA-core kernels,
+    timed with CUDA events."""
+    from gated_delta_rule_41_gb300 import inputs as I
+    gen = torch.Generator().manual_seed(91)
+    lengths, total = [], 32768
+    while total > 0:
+        n = min(total, int(torch.randint(512, 4097, (1,), generator=gen)))
+        lengths.append(n)
+        total -= n
+    w = I.Workload("varlen_32k", 1, 32768, 16, 16, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
+                   seed=92)
+    t = I.make_chunk_inputs(w, device=dev)
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32, device=dev)
+    out = {"sequences": len(lengths), "tokens": w.T, "min_len": min(lengths),
+           "max_len": max(lengths)}
+    for impl in ("tcgen05", "simt"):
+        def step():
+            kda.chunk_kda_fwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], cu, impl=impl)
+            kda.chunk_kda_bwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], cu,
+                                     impl=impl)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        kda.check()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        kda.check()
+        ms = e0.elapsed_time(e1) / steps
+        out[impl] = {"ms_per_step": ms, "tokens_per_s": w.T / (ms / 1e3)}
+    out["pass"] = "fwd+bwd, stateless backward, no h0"
+    return out
+
+
 def measure_decode(kda, dev, hbm):
     """Decode step at B=256, HV=16, K=V=128 (state 256 MiB fp32), 64 steps,
     timed with CUDA events; HBM roofline of the step."""
@@ -690,6 +733,7 @@ def main():
     if world == 1 and args.part == "all":
         line["decode"] = measure_decode(kda, dev, hbm)
         line["chunk_sizes"] = measure_chunk_sizes(kda, dev)
+        line["varlen"] = measure_varlen(kda, dev)
     if world == 1 and not args.no_cpu_baseline and args.part == "all":
         import oracle
         oracle.build()

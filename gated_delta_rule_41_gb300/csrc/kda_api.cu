@@ -85,7 +85,7 @@ kda_status copy_or_zero(const kda_dims& d, float* dst, const float* src, cudaStr
 }
 
 // Variable-length batches: dims as for kda_chunk_fwd except B == 1 and no
-// T % chunk_size rule; the sequences run on the SIMT kernels.
+// T % chunk_size rule.
 kda_status check_varlen_dims(const kda_dims* d, int nseq) {
     if (!d) return KDA_ERR_INVALID_ARG;
     kda_dims t = *d;
@@ -94,8 +94,20 @@ kda_status check_varlen_dims(const kda_dims* d, int nseq) {
     if (st != KDA_OK) return st;
     if (d->T < 0 || d->B != 1 || nseq < 1) return KDA_ERR_SHAPE;
     if ((long long)nseq * d->HV > 65535) return KDA_ERR_UNSUPPORTED;
-    if (d->impl == KDA_IMPL_TCGEN05 || !simt_supported(*d)) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;
+}
+
+// The kernels of a packed batch: as pick_impl; an empty batch (T == 0) runs
+// the SIMT kernels (the tensor maps need rows).
+int pick_varlen_impl(const kda_dims& d) {
+    const int impl = pick_impl(d);
+    if (impl == KDA_IMPL_TCGEN05 && d.T == 0)
+        return d.impl == KDA_IMPL_TCGEN05 || !simt_supported(d) ? -1 : KDA_IMPL_SIMT;
+    return impl;
+}
+size_t varlen_ws_bytes(const kda_dims& d, int impl, int nseq, int for_bwd) {
+    return impl == KDA_IMPL_TCGEN05 ? tc_varlen_workspace_bytes(d, nseq, for_bwd)
+                                    : simt_varlen_workspace_bytes(d, nseq, for_bwd);
 }
 
 kda_status check_varlen(const kda_dims* d, const int* cu, int nseq) {
@@ -205,7 +217,9 @@ kda_status kda_chunk_bwd_saved(const kda_dims* d, const void* q, const void* k, 
 
 size_t kda_chunk_workspace_bytes_varlen(const kda_dims* d, int num_seqs, int for_bwd) {
     if (check_varlen_dims(d, num_seqs) != KDA_OK) return 0;
-    return simt_varlen_workspace_bytes(*d, num_seqs, for_bwd ? 1 : 0);
+    const int impl = pick_varlen_impl(*d);
+    if (impl < 0) return 0;
+    return varlen_ws_bytes(*d, impl, num_seqs, for_bwd ? 1 : 0);
 }
 
 kda_status kda_chunk_fwd_varlen(const kda_dims* d, const int* cu_seqlens, int num_seqs,
@@ -215,17 +229,23 @@ kda_status kda_chunk_fwd_varlen(const kda_dims* d, const int* cu_seqlens, int nu
                                 size_t workspace_bytes, void* stream) {
     kda_status st = check_varlen(d, cu_seqlens, num_seqs);
     if (st != KDA_OK) return st;
+    const int impl = pick_varlen_impl(*d);
+    if (impl < 0) return KDA_ERR_UNSUPPORTED;
     if (output_final_state && !ht) return KDA_ERR_INVALID_ARG;
     const bool empty = d->T == 0;
-    if ((st = check_ptrs(empty, elem_bytes(*d), {q, k, v, g, beta, o},
+    if ((st = check_ptrs(empty, chunk_align(*d, impl), {q, k, v, g, o},
                          {h0, output_final_state ? ht : nullptr})) != KDA_OK)
         return st;
-    const size_t need = simt_varlen_workspace_bytes(*d, num_seqs, 0);
+    if ((st = check_ptrs(empty, elem_bytes(*d), {beta}, {})) != KDA_OK) return st;
+    const size_t need = varlen_ws_bytes(*d, impl, num_seqs, 0);
     if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_ALIGNMENT;
+    auto s = static_cast<cudaStream_t>(stream);
+    if (impl == KDA_IMPL_TCGEN05)
+        return tc_fwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, o,
+                             output_final_state ? ht : nullptr, workspace, s);
     return simt_fwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, o,
-                           output_final_state ? ht : nullptr, workspace,
-                           static_cast<cudaStream_t>(stream));
+                           output_final_state ? ht : nullptr, workspace, s);
 }
 
 kda_status kda_chunk_bwd_varlen(const kda_dims* d, const int* cu_seqlens, int num_seqs,
@@ -236,15 +256,22 @@ kda_status kda_chunk_bwd_varlen(const kda_dims* d, const int* cu_seqlens, int nu
                                 void* stream) {
     kda_status st = check_varlen(d, cu_seqlens, num_seqs);
     if (st != KDA_OK) return st;
+    const int impl = pick_varlen_impl(*d);
+    if (impl < 0) return KDA_ERR_UNSUPPORTED;
     const bool empty = d->T == 0;
-    if ((st = check_ptrs(empty, elem_bytes(*d), {q, k, v, g, beta, dout, dq, dk, dv, dg, dbeta},
+    if ((st = check_ptrs(empty, chunk_align(*d, impl), {q, k, v, g, dout, dq, dk, dv, dg},
                          {h0, dht, dh0})) != KDA_OK)
         return st;
-    const size_t need = simt_varlen_workspace_bytes(*d, num_seqs, 1);
+    if ((st = check_ptrs(empty, elem_bytes(*d), {beta, dbeta}, {})) != KDA_OK) return st;
+    const size_t need = varlen_ws_bytes(*d, impl, num_seqs, 1);
     if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_ALIGNMENT;
+    auto s = static_cast<cudaStream_t>(stream);
+    if (impl == KDA_IMPL_TCGEN05)
+        return tc_bwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, dout, dht, dq, dk,
+                             dv, dg, dbeta, dh0, workspace, s);
     return simt_bwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, dout, dht, dq, dk, dv,
-                           dg, dbeta, dh0, workspace, static_cast<cudaStream_t>(stream));
+                           dg, dbeta, dh0, workspace, s);
 }
 
 kda_status kda_recurrent_step(const kda_dims* d, const void* q, const void* k, const void* v,

@@ -75,6 +75,12 @@ kda_status simt_bwd_varlen(const kda_dims& d, const int* cu, int nseq, const voi
 // Reads and clears the device error word of the SIMT kernels (invalid
 // cu_seqlens: KDA_ERR_SHAPE).
 kda_status simt_take_error(cudaStream_t s);
+// The chunk table of a packed batch (both kernel families): ctab [NT][2] =
+// (first token, valid rows) of every chunk slot, sfirst [nseq + 1] = each
+// sequence's first slot; an invalid cu_seqlens is recorded for kda_check and
+// leaves every sequence without chunks.
+kda_status varlen_table_launch(const int* cu, int nseq, int T, int C, int NT, int* ctab,
+                               int* sfirst, cudaStream_t s);
 
 bool tc_supported(const kda_dims& d);
 size_t tc_workspace_bytes(const kda_dims& d, int for_bwd);
@@ -89,6 +95,16 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                   const void* g, const void* beta, const float* h0, const void* dout,
                   const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
                   float* dh0, void* ws, bool from_saved, cudaStream_t s);
+// Packed variable-length sequences on the tensor-core kernels (same
+// arguments as the SIMT versions; the stateless backward).
+size_t tc_varlen_workspace_bytes(const kda_dims& d, int nseq, int for_bwd);
+kda_status tc_fwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q, const void* k,
+                         const void* v, const void* g, const void* beta, const float* h0, void* o,
+                         float* ht, void* ws, cudaStream_t s);
+kda_status tc_bwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q, const void* k,
+                         const void* v, const void* g, const void* beta, const float* h0,
+                         const void* dout, const float* dht, void* dq, void* dk, void* dv,
+                         void* dg, void* dbeta, float* dh0, void* ws, cudaStream_t s);
 // Reads and clears the device error word of the tensor-core kernels.
 kda_status tc_take_error(cudaStream_t s);
 // Diagnostic: a bounded wait on an mbarrier nothing arrives at, with the given

@@ -1204,6 +1204,12 @@ kda_status varlen_table(const Dims& d, const int* cu, int nseq, cudaStream_t s) 
 }
 }  // namespace
 
+kda_status varlen_table_launch(const int* cu, int nseq, int T, int C, int NT, int* ctab,
+                               int* sfirst, cudaStream_t s) {
+    varlen_table_kernel<<<1, 256, 0, s>>>(cu, nseq, T, C, NT, ctab, sfirst);
+    return launch_status();
+}
+
 size_t simt_varlen_workspace_bytes(const kda_dims& kd, int nseq, int for_bwd) {
     return varlen_carve(kd, nseq, for_bwd, nullptr, nullptr, nullptr);
 }

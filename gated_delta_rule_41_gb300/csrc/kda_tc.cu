@@ -299,6 +299,32 @@ __device__ __forceinline__ void chain_delta_step(uint32_t tD, uint8_t* tile, con
     }
 }
 
+// Token row (in the [B*T] token tensors) of chunk n of batch b, and its
+// valid rows.  Fixed-length batches: b T + n C and C.  Packed sequences (B =
+// 1): the chunk table ctab [NT][2] (first token, valid rows; 0 rows for an
+// unused slot).  Only a sequence's last chunk can be partial.
+__device__ __forceinline__ int tok_row(const int* ctab, int b, int T, int n) {
+    return ctab ? ctab[2 * n] : b * T + n * kC;
+}
+__device__ __forceinline__ int tok_len(const int* ctab, int n) {
+    return ctab ? ctab[2 * n + 1] : kC;
+}
+// Zeroes rows [len, 64) of a [64][128] bf16 token tile (two 128B-swizzled
+// 64-column boxes, 8 KB apart; a row of a box is 128 contiguous bytes).
+__device__ __forceinline__ void zero_tile_rows(uint8_t* tile, int len, int tid, int nthreads) {
+    const int n16 = (kC - len) * 16;   // 16-byte units: 8 per row and box
+    for (int i = tid; i < n16; i += nthreads) {
+        const int r = len + (i >> 4), box = (i >> 3) & 1, u = i & 7;
+        *reinterpret_cast<uint4*>(tile + box * 8192 + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+    }
+}
+// Copies a [D][D] fp32 state (zeros if src is null): an empty sequence's
+// final state is its initial state, and its dh0 is its dht.
+__device__ __forceinline__ void copy_state(float* dst, const float* src, int D, int tid,
+                                           int nthreads) {
+    for (int e = tid; e < D * D; e += nthreads) dst[e] = src ? src[e] : 0.f;
+}
+
 struct ChainArgs {
     int B, T, HV, NT;
     int D;              // K = V of the tensors (64 or 128); the kernel works at 128
@@ -325,6 +351,10 @@ struct ChainArgs {
     int nseg, seglen, pass;
     float *sbuf, *zbuf, *mbuf;
     const float* ident;
+    // Packed sequences (B = 1; null for fixed-length batches): the chunk
+    // table and each sequence's first chunk slot; CTA c runs sequence c / HV
+    // of value head c % HV over its chunk slots, with h0 / ht at row c.
+    const int *ctab, *sfirst;
 };
 
 // The work of one chain CTA: head bh walks chunks n0 .. n0 + cnt - 1 from
@@ -337,11 +367,22 @@ struct ChainJob {
     float* ht;
 };
 
+template <bool VL>
 __device__ __forceinline__ ChainJob chain_job(const ChainArgs& a, int c) {
     const int BH = a.B * a.HV;
     const size_t S = (size_t)a.D * a.D;
     ChainJob j;
     j.zero_u = false;
+    if (VL && a.sfirst) {
+        const int sq = c / a.HV;
+        j.bh = c % a.HV;
+        j.n0 = a.sfirst[sq];
+        j.cnt = a.sfirst[sq + 1] - j.n0;
+        j.write_o = a.o != nullptr;
+        j.h0 = a.h0 ? a.h0 + (size_t)c * S : nullptr;
+        j.ht = a.ht ? a.ht + (size_t)c * S : nullptr;
+        return j;
+    }
     if (a.nseg == 0) {
         j.bh = c;
         j.n0 = 0;
@@ -390,7 +431,7 @@ __device__ __forceinline__ ChainJob chain_job(const ChainArgs& a, int c) {
 // LO: U comes as two parts (a.u_lo added) and delta's low parts go to
 // a.delta_lo; a separate instantiation, so that the plain one's serial
 // chunk loop carries none of it.
-template <bool LO>
+template <bool LO, bool VL>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_kbt,
@@ -415,7 +456,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 13);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const ChainJob job = chain_job(a, blockIdx.x);
+    const ChainJob job = chain_job<VL>(a, blockIdx.x);
     const int bh = job.bh;
     const int b = bh / a.HV, hv = bh % a.HV;
     const int NT = job.cnt;      // chunks of this CTA: n0 .. n0 + NT - 1
@@ -462,7 +503,7 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                 const int sj = j & 1;
                 if (!wait_bar(&bar_o[sj], (j >> 1) & 1, 21)) return false;
                 if (write_o && j >= 1) {
-                    const int z = b * a.T + (n0 + j - 1) * kC;
+                    const int z = tok_row((VL ? a.ctab : nullptr), b, a.T, n0 + j - 1);
                     const uint8_t* tile = smem + sj * STAGE_BYTES + OFF_U;
                     tma_store_3d(&tm_o, tile, 0, hv, z);
                     if (a.D > 64) tma_store_3d(&tm_o, tile + 8192, 64, hv, z);
@@ -653,11 +694,13 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             }
         };
         auto o_out = [&](int m) {
-            if (q >= 2 || half * 64 >= a.D) return;
+            if (q >= 2 || half * 64 >= a.D) return;   // warp-uniform: the TMEM load is .aligned
             float x1[32];
             o_rows(m, r, x1);
+            // rows past a partial chunk's end belong to the next sequence
+            if (v >= tok_len((VL ? a.ctab : nullptr), n0 + m)) return;
             __nv_bfloat16* op =
-                a.o + (((size_t)b * a.T + (size_t)(n0 + m) * kC + v) * a.HV + hv) * a.D + half * 64;
+                a.o + (((size_t)tok_row((VL ? a.ctab : nullptr), b, a.T, n0 + m) + v) * a.HV + hv) * a.D + half * 64;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 float e0[8], e1v[8];
@@ -671,7 +714,12 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             }
         };
 
-        ok = e1(0);
+        if (NT == 0) {   // an empty sequence: ht = h0
+            if (job.ht) copy_state(job.ht, job.h0, a.D, threadIdx.x - 64, kChainEpi);
+            ok = false;
+        } else {
+            ok = e1(0);
+        }
         for (int n = 0; ok && n < NT; ++n) {
             const int s = n & 1;
             // E2: delta^T = U^T - S^T W^T  -> bf16 operand tile.  U (in the
@@ -810,6 +858,7 @@ constexpr uint32_t TM2_S = 0, TM2_DD = 128, TM2_COLS = 256;
 
 struct ChainBwdArgs {
     int B, T, HV, NT;
+    const int *ctab, *sfirst;    // packed sequences (as in ChainArgs), or null
     int D;              // K = V of the tensors (64 or 128); the kernel works at 128
     const float* gam;
     const float* dht;            // [BH][K][V] or null
@@ -820,7 +869,7 @@ struct ChainBwdArgs {
 
 // LO: also write the low parts of dS (a.dh_lo); a separate instantiation,
 // so that the plain one keeps its registers.
-template <bool LO>
+template <bool LO, bool VL>
 __global__ void __launch_bounds__(kChainThreads, 1)
 chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kbt,
@@ -842,9 +891,25 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 12);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int b = bh / a.HV, hv = bh % a.HV;
-    const int NT = a.NT;
+    // this CTA's chunk slots n0 .. n0 + NT - 1 of workspace head row bh,
+    // walked in reverse; dht and dh0 at state row srow
+    int bh, b, hv, n0, NT, srow;
+    if ((VL ? a.sfirst : nullptr)) {
+        const int sq = blockIdx.x / a.HV;
+        hv = blockIdx.x % a.HV;
+        bh = hv;
+        b = 0;
+        n0 = (VL ? a.sfirst : nullptr)[sq];
+        NT = (VL ? a.sfirst : nullptr)[sq + 1] - n0;
+        srow = blockIdx.x;
+    } else {
+        bh = blockIdx.x;
+        b = bh / a.HV;
+        hv = bh % a.HV;
+        n0 = 0;
+        NT = a.NT;
+        srow = bh;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(&full[0], 1);
@@ -883,7 +948,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             auto drain_dd = [&](int j) -> bool {
                 const int sj = j & 1;
                 if (!wait_bar(&bar_o[sj], (j >> 1) & 1, 23)) return false;
-                const int y = bh * a.T + (NT - 1 - j) * kC;
+                const int y = bh * a.T + (n0 + NT - 1 - j) * kC;
                 const uint8_t* tile = smem + sj * STAGE_BYTES + RB_KBT;
                 tma_store_2d(&tm_dd, tile, 0, y);
                 tma_store_2d(&tm_dd, tile + 8192, 64, y);
@@ -898,9 +963,9 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 if (i >= 2 && !drain_dd(i - 2)) break;
                 uint8_t* st = smem + s * STAGE_BYTES;
                 mbar_arrive_expect_tx(&full[s], STAGE_TX);
-                const int row = bh * a.T + n * kC;
-                const int crow = bh * NT + n;
-                const int trow = b * a.T + n * kC;
+                const int row = bh * a.T + (n0 + n) * kC;
+                const int crow = bh * a.NT + n0 + n;
+                const int trow = tok_row((VL ? a.ctab : nullptr), b, a.T, n0 + n);
                 tma_load_3d(st + RB_DO, &tm_do, &full[s], 0, hv, trow);
                 tma_load_3d(st + RB_DO + 8192, &tm_do, &full[s], 64, hv, trow);
                 tma_load_2d(st + RB_Q, &tm_q, &full[s], 0, row);
@@ -914,7 +979,8 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 issued = i + 1;
                 // the chunk two ahead (n - 2) into L2
                 if (n >= 2) {
-                    const int row2 = row - 2 * kC, crow2 = crow - 2, trow2 = trow - 2 * kC;
+                    const int row2 = row - 2 * kC, crow2 = crow - 2;
+                    const int trow2 = tok_row((VL ? a.ctab : nullptr), b, a.T, n0 + n - 2);
                     tma_prefetch_3d(&tm_do, 0, hv, trow2);
                     if (a.D > 64) tma_prefetch_3d(&tm_do, 64, hv, trow2);
                     tma_prefetch_2d(&tm_q, 0, row2);
@@ -953,7 +1019,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 tc_fence_after();
                 const uint64_t dSi = dS + (uint64_t)((i & 1) * (S_TILE >> 4));
                 {  // dS^T tile (rows v, parity i) of chunk n = NT-1-i to dh_out, by TMA
-                    const int y = (bh * NT + (NT - 1 - i)) * kD;
+                    const int y = (bh * a.NT + n0 + (NT - 1 - i)) * kD;
                     uint8_t* tile = smem + OFF_S + (i & 1) * S_TILE;
                     tma_store_2d(&tm_dhout, tile, 0, y);
                     tma_store_2d(&tm_dhout, tile + 16384, 64, y);
@@ -1008,11 +1074,11 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             const int s = i & 1;
             float r0[32], r1[32];
             chain_state_tile(tmem + lane_off + TM2_S, smem + OFF_S + s * S_TILE, i == 0,
-                             a.dht ? a.dht + (size_t)bh * a.D * a.D : nullptr, a.D, v, half, bar_S, r0,
-                             r1);
+                             a.dht ? a.dht + (size_t)srow * a.D * a.D : nullptr, a.D, v, half, bar_S,
+                             r0, r1);
             if (LO) {
                 __nv_bfloat16* lo =
-                    a.dh_lo + (((size_t)bh * NT + (NT - 1 - i)) * kD + v) * kD + 64 * half;
+                    a.dh_lo + (((size_t)bh * a.NT + n0 + (NT - 1 - i)) * kD + v) * kD + 64 * half;
                 store_lo32(lo, r0);
                 store_lo32(lo + 32, r1);
             }
@@ -1023,7 +1089,15 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
             return true;
         };
 
-        ok = e1(0);
+        if (NT == 0) {   // an empty sequence: dh0 = dht
+            if (a.dh0)
+                copy_state(a.dh0 + (size_t)srow * a.D * a.D,
+                           a.dht ? a.dht + (size_t)srow * a.D * a.D : nullptr, a.D,
+                           threadIdx.x - 64, kChainEpi);
+            ok = false;
+        } else {
+            ok = e1(0);
+        }
         for (int i = 0; ok && i < NT; ++i) {
             const int s = i & 1;
             if (!wait_bar_warp(bar_dd, i & 1, 18)) { ok = false; break; }
@@ -1042,7 +1116,7 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
                 for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
                     tmem_ld32(tmem + lane_off + TM2_S + cb * 32, r);
                     if (v >= a.D || cb * 32 >= a.D) continue;   // [D][D]
-                    float* hp = a.dh0 + ((size_t)bh * a.D + cb * 32) * a.D + v;
+                    float* hp = a.dh0 + ((size_t)srow * a.D + cb * 32) * a.D + v;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) hp[(size_t)j * a.D] = r[j];
                 }
@@ -1086,11 +1160,12 @@ struct GradArgs {
     __nv_bfloat16* dv;          // [B,T,HV,V]
     float *dQh, *dKb, *dgam, *dTv, *dbv;
     __nv_bfloat16 *dW, *dAqk;  // bf16: the local backward uses them only as MMA operands
+    const int* ctab;           // packed sequences: the chunk table, or null
 };
 
 // DW: V of the tensors (64 or 128), a compile-time constant so that the
 // 128-wide instantiation indexes exactly as a kernel written for 128 does.
-template <int DW>
+template <int DW, bool VL>
 __global__ void __launch_bounds__(kGradThreads, 1)
 grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dh,
               const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dd,
@@ -1127,7 +1202,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     };
     auto issue_main = [&](int ch) {   // [dO; ddelta], delta^T, T
         const int nn = ch % NT, bb = ch / NT, hvv = bb % a.HV;
-        const int rw = bb * a.T + nn * kC, tr = (bb / a.HV) * a.T + nn * kC;
+        const int rw = bb * a.T + nn * kC, tr = tok_row((VL ? a.ctab : nullptr), bb / a.HV, a.T, nn);
         mbar_arrive_expect_tx(bar_tma, GRAD_TX - 16384 - 65536);
         tma_load_3d(smem + G_ODD, &tm_do, bar_tma, 0, hvv, tr);
         tma_load_3d(smem + G_ODD + 16384, &tm_do, bar_tma, 64, hvv, tr);
@@ -1139,7 +1214,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     };
     auto issue_v = [&](int ch) {
         const int nn = ch % NT, bb = ch / NT, hvv = bb % a.HV;
-        const int tr = (bb / a.HV) * a.T + nn * kC;
+        const int tr = tok_row((VL ? a.ctab : nullptr), bb / a.HV, a.T, nn);
         mbar_arrive_expect_tx(bar_v, 16384);
         tma_load_3d(smem + G_DV + 8192, &tm_v, bar_v, 0, hvv, tr);
         tma_load_3d(smem + G_DV + 24576, &tm_v, bar_v, 64, hvv, tr);
@@ -1147,8 +1222,10 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     };
     auto load_beta = [&](int ch) {
         const int nn = ch % NT, bb = ch / NT;
-        return __bfloat162float(
-            a.beta[((size_t)(bb / a.HV) * a.T + (size_t)nn * kC + tid) * a.HV + bb % a.HV]);
+        return tid < tok_len((VL ? a.ctab : nullptr), nn)   // 0 past a packed sequence's end
+                   ? __bfloat162float(a.beta[((size_t)tok_row((VL ? a.ctab : nullptr), bb / a.HV, a.T, nn) + tid) *
+                                                 a.HV + bb % a.HV])
+                   : 0.f;
     };
 
     if (tid == 0) {
@@ -1184,7 +1261,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         const int b = bh / a.HV, hv = bh % a.HV;
         const int row = bh * a.T + n * kC;
         const int crow = chunk;
-        const int trow = b * a.T + n * kC;
+        const int trow = tok_row((VL ? a.ctab : nullptr), b, a.T, n);
+        const int len = tok_len((VL ? a.ctab : nullptr), n);   // rows past it belong to the next sequence
         if (tid < kC) {
             beta_s[tid] = beta_next;                          // read after later barriers
             if (next < total) beta_next = load_beta(next);    // in flight meanwhile
@@ -1318,7 +1396,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             for (int j = 0; j < 32; ++j) {
                 const int m = cb * 32 + j;
                 const float bt = beta_s[m];
-                if (DW == kD || l < DW)
+                if ((DW == kD || l < DW) && m < len)
                     a.dv[(((size_t)trow + m) * a.HV + hv) * DW + l] = __float2bfloat16_rn(bt * r[j]);
                 const uint32_t voff = G_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
                 r[j] *= __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
@@ -1388,7 +1466,7 @@ static_assert(P_DSL % 1024 == 0 && P_ODD % 1024 == 0 && P_DV % 1024 == 0 && P_DT
                   P_DTL % 1024 == 0 && P_LO % 1024 == 0,
               "128-byte swizzled tiles need 1024-byte aligned bases");
 
-template <int DW>
+template <int DW, bool VL>
 __global__ void __launch_bounds__(kGradThreads, 1)
 grad_v_px_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dh,
                  const __grid_constant__ CUtensorMap tm_dhl, const __grid_constant__ CUtensorMap tm_do,
@@ -1412,7 +1490,7 @@ grad_v_px_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     int issued = 0, waited = 0;               // thread 0's loads (each waited for before exit)
     auto issue = [&](int ch) {
         const int nn = ch % NT, bb = ch / NT, hvv = bb % a.HV;
-        const int rw = bb * a.T + nn * kC, tr = (bb / a.HV) * a.T + nn * kC;
+        const int rw = bb * a.T + nn * kC, tr = tok_row((VL ? a.ctab : nullptr), bb / a.HV, a.T, nn);
         mbar_arrive_expect_tx(bar_ld, PX_TX);
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
@@ -1463,7 +1541,8 @@ grad_v_px_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
         const int n = chunk % NT, bh = chunk / NT;
         const int b = bh / a.HV, hv = bh % a.HV;
         const int row = bh * a.T + n * kC;
-        const int trow = b * a.T + n * kC;
+        const int trow = tok_row((VL ? a.ctab : nullptr), b, a.T, n);
+        const int len = tok_len((VL ? a.ctab : nullptr), n);   // rows past it belong to the next sequence
         if (tid == 0) {
             issue(chunk);
             if (wait_bar(bar_ld, ph, 51)) {
@@ -1620,8 +1699,9 @@ grad_v_px_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int m = cb * 32 + j;
-                const float bt = __bfloat162float(a.beta[((size_t)trow + m) * a.HV + hv]);
-                if (DW == kD || l < DW)
+                const float bt =
+                    m < len ? __bfloat162float(a.beta[((size_t)trow + m) * a.HV + hv]) : 0.f;
+                if ((DW == kD || l < DW) && m < len)
                     a.dv[(((size_t)trow + m) * a.HV + hv) * DW + l] = __float2bfloat16_rn(bt * r[j]);
                 const uint32_t voff = P_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
                 r[j] *= __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
@@ -1724,6 +1804,7 @@ struct IntraArgs {
     // null (only the backward with an upstream final-state gradient asks)
     __nv_bfloat16 *Ulo, *Kblo;
     float* gam;
+    const int* ctab;           // packed sequences: the chunk table, or null
 };
 
 template <int R>
@@ -1744,7 +1825,7 @@ __device__ __forceinline__ void intra_read_block(uint32_t taddr, float* out /* 6
 
 // LO: also write the low parts of U and Kb (a.Ulo, a.Kblo); a separate
 // instantiation, so that the plain one keeps its registers.
-template <bool LO>
+template <bool LO, bool VL>
 __global__ void __launch_bounds__(kIntraThreads, 2)
 intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
@@ -1786,7 +1867,7 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         const int nn = ch % a.NT, bb = ch / a.NT;
         hv = bb % a.HV;
         h = hv / (a.HV / a.H);
-        trow = (bb / a.HV) * a.T + nn * kC;
+        trow = tok_row((VL ? a.ctab : nullptr), bb / a.HV, a.T, nn);
     };
     // thread 0's counts of issued and consumed loads (every load is waited for
     // before the CTA exits)
@@ -1826,10 +1907,12 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             tma_prefetch_3d(&tm_v, 64, hv, trow);
         }
     };
-    auto load_beta = [&](int ch) {
+    auto load_beta = [&](int ch) {   // 0 past a packed sequence's end
         int trow, hv, h;
         coords(ch, trow, hv, h);
-        return __bfloat162float(a.beta[((size_t)trow + tid) * a.HV + hv]);
+        return tid < tok_len((VL ? a.ctab : nullptr), ch % a.NT)
+                   ? __bfloat162float(a.beta[((size_t)trow + tid) * a.HV + hv])
+                   : 0.f;
     };
 
     if (tid == 0) {
@@ -1876,15 +1959,24 @@ intra_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int n = chunk % a.NT, bh = chunk / a.NT;
     const int row0 = bh * a.T + n * kC;       // row in the [BH*T] workspace arrays
     const int crow = chunk;                   // chunk index
+    const int len = tok_len((VL ? a.ctab : nullptr), n);       // valid rows (a partial chunk of a packed batch)
     if (tid == 0 && next < total) prefetch(next);
     if (tid < kC) {
-        sBeta[tid] = beta_next;                                   // read after later barriers
+        sBeta[tid] = tid < len ? beta_next : 0.f;                 // read after later barriers
         if (next < total) beta_next = load_beta(next);            // in flight meanwhile
     }
     {
         const bool got = wait_bar_warp(bar_kqg, ph, 31);
         if (got && tid == 0) ++kqg_waited;
         ok = ok && got;
+    }
+    if (len < kC) {
+        // rows past the end of a packed sequence: q = k = 0, g = 0 (with
+        // beta = 0 they leave every output of the valid rows unchanged)
+        zero_tile_rows(smem + J_K, len, tid, kIntraThreads);
+        zero_tile_rows(smem + J_Q, len, tid, kIntraThreads);
+        zero_tile_rows(smem + J_G, len, tid, kIntraThreads);
+        __syncthreads();
     }
 
     // ---- (1) clamp the g tile in place (1024 units of 8 bf16); with qkn,
@@ -2388,10 +2480,13 @@ struct LocalTcArgs {
     const __nv_bfloat16 *q, *k, *g, *beta;
     __nv_bfloat16 *dq, *dk, *dg, *dbeta;
     float *dqh, *dkh;
+    const int* ctab;    // packed sequences: the chunk table, or null
 };
 
 // DW: K of the tensors (64 or 128), a compile-time constant (see grad_v).
-template <int DW>
+// VL: packed sequences (a.ctab); a separate instantiation, so that the
+// fixed-length one carries no row masks.
+template <int DW, bool VL>
 __global__ void __launch_bounds__(kLocalTcThreads, 1)
 local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_q,
@@ -2435,7 +2530,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     // into the rows 32R + 16 + u of [dA; dAqk]
     auto issue_main = [&](int ch) {
         const int nn = ch % a.NT, bb = ch / a.NT, hvv = bb % a.HV, hh = hvv / a.G;
-        const int tr = (bb / a.HV) * a.T + nn * kC, rw = bb * a.T + nn * kC, c64 = ch * kC;
+        const int tr = tok_row(VL ? a.ctab : nullptr, bb / a.HV, a.T, nn), rw = bb * a.T + nn * kC, c64 = ch * kC;
         mbar_arrive_expect_tx(bar_tma, 2 * 16384 + 16384 + 2 * 8192 + 8192);
         tma_load_3d(smem + LB_K, &tm_k, bar_tma, 0, hh, tr);
         tma_load_3d(smem + LB_K + 8192, &tm_k, bar_tma, 64, hh, tr);
@@ -2452,7 +2547,7 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     };
     auto issue_g = [&](int ch) {
         const int nn = ch % a.NT, bb = ch / a.NT, hvv = bb % a.HV;
-        const int tr = (bb / a.HV) * a.T + nn * kC;
+        const int tr = tok_row(VL ? a.ctab : nullptr, bb / a.HV, a.T, nn);
         mbar_arrive_expect_tx(bar_g, 16384);
         tma_load_3d(smem + LB_G, &tm_g, bar_g, 0, hvv, tr);
         tma_load_3d(smem + LB_G + 8192, &tm_g, bar_g, 64, hvv, tr);
@@ -2471,10 +2566,13 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         cp_async_commit();
     };
-    auto load_beta = [&](int ch) {
+    auto load_beta = [&](int ch) {   // 0 past a packed sequence's end
         const int nn = ch % a.NT, bb = ch / a.NT;
-        return __bfloat162float(
-            a.beta[((size_t)(bb / a.HV) * a.T + (size_t)nn * kC + tid) * a.HV + bb % a.HV]);
+        const int* ct = VL ? a.ctab : nullptr;
+        return tid < tok_len(ct, nn)
+                   ? __bfloat162float(a.beta[((size_t)tok_row(ct, bb / a.HV, a.T, nn) + tid) * a.HV +
+                                             bb % a.HV])
+                   : 0.f;
     };
 
     if (tid == 0) {
@@ -2511,16 +2609,21 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int next = chunk + gridDim.x;
     const int n = chunk % a.NT, bh = chunk / a.NT;
     const int b = bh / a.HV, hv = bh % a.HV;
-    const int trow = b * a.T + n * kC;
+    const int trow = tok_row(VL ? a.ctab : nullptr, b, a.T, n);
+    const int len = tok_len(VL ? a.ctab : nullptr, n);   // valid rows (a partial chunk of a packed batch)
     const size_t row0 = (size_t)bh * a.T + (size_t)n * kC;
     if (tid < kC) {
-        sBeta[tid] = beta_next;                          // read after later barriers
+        sBeta[tid] = tid < len ? beta_next : 0.f;        // read after later barriers
         if (next < total) beta_next = load_beta(next);   // in flight meanwhile
     }
     {
         const bool got = wait_bar_warp(bar_g, ph, 46);
         if (got && tid == 0) ++g_waited;
         ok = ok && got;
+    }
+    if (len < kC) {   // rows past the end of a packed sequence: g = 0
+        zero_tile_rows(smem + LB_G, len, tid, kLocalTcThreads);
+        __syncthreads();
     }
 
     const uint32_t kbo = (c >> 6) * 8192, cc = c & 63;
@@ -2572,6 +2675,11 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         const bool got = wait_bar_warp(bar_tma, ph, 41);
         if (got && tid == 0) ++main_waited;
         ok = ok && got;
+    }
+    if (len < kC) {   // and q = k = 0 there
+        zero_tile_rows(smem + LB_K, len, tid, kLocalTcThreads);
+        zero_tile_rows(smem + LB_Q, len, tid, kLocalTcThreads);
+        __syncthreads();
     }
     if (a.qkn) {
         l2norm_tile_rows(smem + LB_K, tid, kLocalTcThreads);
@@ -2892,8 +3000,9 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             lastp = fmaf(kr, l, lastp);
             dbps[u] = kr * pb;
             const size_t io = (((size_t)trow + t) * a.HV + hv) * DW + c;
-            if (DW < kD && c >= DW) {
-                // a key channel past the tensors' width: zero-filled, not written
+            if ((DW < kD && c >= DW) || t >= len) {
+                // a key channel past the tensors' width (zero-filled), or a
+                // row past a packed sequence's end: not written
             } else if (a.G == 1 && !a.qkn) {
                 a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
                 a.dk[io] = __float2bfloat16_rn(dkv);
@@ -2943,10 +3052,11 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             run += dG[u];
             const int t = 16 * R + u;
             const size_t ig = (((size_t)trow + t) * a.HV + hv) * DW + c;
-            if (DW == kD || c < DW) a.dg[ig] = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
+            if ((DW == kD || c < DW) && t < len)
+                a.dg[ig] = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
         }
     }
-    if (tid < kC)
+    if (tid < len)
         a.dbeta[((size_t)trow + tid) * a.HV + hv] =
             __float2bfloat16_rn((sDbp[tid] + sDbp[64 + tid]) + (sDbp[128 + tid] + sDbp[192 + tid]) +
                                 dbv_t);
@@ -3069,6 +3179,18 @@ kda_dims tc_wide(const kda_dims& d) {
     return p;
 }
 
+// A packed variable-length batch: the chunk table and each sequence's first
+// chunk slot (in the workspace), the sequence count and the real token count.
+// The kernels then see B = 1 and T = the padded slot count times 64 (the
+// workspace arrays' row count); the token tensors have Ttok rows.
+struct TcVl {
+    const int *ctab, *sfirst;
+    int nseq, Ttok;
+};
+inline uint64_t tok_rows(const kda_dims& d, const TcVl* vl) {
+    return vl ? (uint64_t)vl->Ttok : (uint64_t)d.B * d.T;
+}
+
 size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
     const size_t BH = (size_t)d.B * d.HV, T = d.T, NT = d.T / kC;
     size_t off = 0;
@@ -3117,11 +3239,11 @@ size_t tc_carve(const kda_dims& d, int for_bwd, char* base, TcWs* w) {
 kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const void* k,
                         const void* v, const void* g, const void* beta, bool keep_T,
                         cudaStream_t s, float** gam_out, __nv_bfloat16* ulo = nullptr,
-                        __nv_bfloat16* kblo = nullptr) {
+                        __nv_bfloat16* kblo = nullptr, const TcVl* vl = nullptr) {
     SimtWsPtrs p;
     simt_ws_ptrs(tc_wide(d), 0, w.simt, &p);
     const int BH = d.B * d.HV, NT = d.T / kC;
-    const uint64_t BT = (uint64_t)d.B * d.T;
+    const uint64_t BT = tok_rows(d, vl);
     const uint64_t rows = (uint64_t)BH * d.T;
     CUtensorMap mk, mq, mg, mv, mw2, mq2, mu2, mkb2, ma2;
     if (!make_map_tok(&mk, k, BT, d.H, d.K) || !make_map_tok(&mq, q, BT, d.H, d.K) ||
@@ -3147,8 +3269,10 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
     a.Ulo = ulo;
     a.Kblo = kblo;
     a.gam = p.gam;
+    a.ctab = vl ? vl->ctab : nullptr;
     if ((ulo == nullptr) != (kblo == nullptr)) return KDA_ERR_INVALID_ARG;
-    auto kern = ulo ? intra_tc_kernel<true> : intra_tc_kernel<false>;
+    auto kern = vl ? (ulo ? intra_tc_kernel<true, true> : intra_tc_kernel<false, true>)
+                   : (ulo ? intra_tc_kernel<true, false> : intra_tc_kernel<false, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)INTRA_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -3164,8 +3288,9 @@ kda_status run_intra_tc(const kda_dims& d, const TcWs& w, const void* q, const v
 
 kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& p,
                             const void* q, const void* k, const void* g, const void* beta,
-                            void* dq, void* dk, void* dg, void* dbeta, cudaStream_t s) {
-    const uint64_t BT = (uint64_t)d.B * d.T;
+                            void* dq, void* dk, void* dg, void* dbeta, cudaStream_t s,
+                            const TcVl* vl = nullptr) {
+    const uint64_t BT = tok_rows(d, vl);
     const uint64_t rows = (uint64_t)d.B * d.HV * d.T;  // [BH*T] and [BH*NT*64] alike
     CUtensorMap mk, mq, mg, mdw, mt, mtl, mda;
     if (!make_map_tok(&mk, k, BT, d.H, d.K) || !make_map_tok(&mq, q, BT, d.H, d.K) ||
@@ -3199,7 +3324,9 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
     a.dbeta = static_cast<__nv_bfloat16*>(dbeta);
     a.dqh = p.dqh;
     a.dkh = p.dkh;
-    auto kern = d.K == kD ? local_bwd_tc_kernel<kD> : local_bwd_tc_kernel<64>;
+    a.ctab = vl ? vl->ctab : nullptr;
+    auto kern = d.K == kD ? (vl ? local_bwd_tc_kernel<kD, true> : local_bwd_tc_kernel<kD, false>)
+                          : (vl ? local_bwd_tc_kernel<64, true> : local_bwd_tc_kernel<64, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)LOCAL_TC_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -3217,8 +3344,10 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
 kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, const float* h0,
                          void* o, float* ht, __nv_bfloat16* h_out, __nv_bfloat16* delta_out,
                          cudaStream_t s, int nseg = 0, const __nv_bfloat16* u_lo = nullptr,
-                         __nv_bfloat16* delta_lo = nullptr) {
+                         __nv_bfloat16* delta_lo = nullptr, const TcVl* vl = nullptr) {
     const int BH = d.B * d.HV, NT = d.T / kC;
+    // one CTA per (b, hv), or per (sequence, hv) of a packed batch
+    const int ctas = vl ? vl->nseq * d.HV : BH;
     CUtensorMap mw, mq, mk, ma, mu;
     const uint64_t rows = (uint64_t)BH * d.T;
     if (!make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
@@ -3231,7 +3360,8 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     // map over W when no states are kept)
     // and delta, [BH*NT*V][C]: one box of 128 rows
     if ((h_out == nullptr) != (delta_out == nullptr)) return KDA_ERR_INVALID_ARG;
-    if ((u_lo == nullptr) != (delta_lo == nullptr) || (delta_lo && (!delta_out || nseg >= 3)))
+    if ((u_lo == nullptr) != (delta_lo == nullptr) || (delta_lo && (!delta_out || nseg >= 3)) ||
+        (vl && nseg >= 3))
         return KDA_ERR_INVALID_ARG;
     CUtensorMap mh, mdl, mo;
     if (!(h_out ? make_map(&mh, h_out, (uint64_t)BH * NT * kD, kD, 64, 128, true)
@@ -3241,7 +3371,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         return KDA_ERR_CUDA;
     // the output o [B*T][HV][V] in [64 t][64 v] boxes (a dummy map over W when
     // there is no output)
-    if (!(o ? make_map_tok(&mo, o, (uint64_t)d.B * d.T, d.HV, d.V) : make_map_tok(&mo, w.W2, rows, 1, kD)))
+    if (!(o ? make_map_tok(&mo, o, tok_rows(d, vl), d.HV, d.V) : make_map_tok(&mo, w.W2, rows, 1, kD)))
         return KDA_ERR_CUDA;
     ChainArgs args;
     args.B = d.B;
@@ -3262,7 +3392,10 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     args.pass = 0;
     args.sbuf = args.zbuf = args.mbuf = nullptr;
     args.ident = nullptr;
-    auto chain = delta_lo ? chain_fwd_kernel<true> : chain_fwd_kernel<false>;
+    args.ctab = vl ? vl->ctab : nullptr;
+    args.sfirst = vl ? vl->sfirst : nullptr;
+    auto chain = vl ? (delta_lo ? chain_fwd_kernel<true, true> : chain_fwd_kernel<false, true>)
+                    : (delta_lo ? chain_fwd_kernel<true, false> : chain_fwd_kernel<false, false>);
     if (cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)CHAIN_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -3270,7 +3403,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
         // three roles, timed apart: forward (o), saving forward (o and the
         // chunk-start states), and the backward's recompute (states only)
         TimedLaunch tl(!h_out ? "tc_chain_fwd" : o ? "tc_chain_fwd_save" : "tc_chain_states", s);
-        chain<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, mdl, mo, args);
+        chain<<<ctas, kChainThreads, CHAIN_SMEM, s>>>(mw, mq, mk, ma, mu, mh, mdl, mo, args);
         return launch_status();
     }
     // segmented: pass 1 (segment 0 in full; later segments from zero and as
@@ -3338,12 +3471,14 @@ kda_status tc_fwd(const kda_dims& d, const void* q, const void* k, const void* v
     return run_chain_fwd(d, w, gam, h0, o, ht, nullptr, nullptr, s, chain_segments(d));
 }
 
-kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
-                  const void* beta, const float* h0, const void* dout, const float* dht,
-                  void* dq, void* dk, void* dv, void* dg, void* dbeta, float* dh0, void* ws,
-                  bool from_saved, cudaStream_t s) {
-    TcWs w;
-    tc_carve(d, 1, static_cast<char*>(ws), &w);
+namespace {
+// The backward on a carved workspace; vl: a packed batch (d then has B = 1
+// and the padded T), or null.
+kda_status tc_bwd_run(const kda_dims& d, const TcWs& w, const TcVl* vl, const void* q,
+                      const void* k, const void* v, const void* g, const void* beta,
+                      const float* h0, const void* dout, const float* dht, void* dq, void* dk,
+                      void* dv, void* dg, void* dbeta, float* dh0, bool from_saved,
+                      cudaStream_t s) {
     float* gam = nullptr;
     kda_status st = KDA_OK;
     // An upstream final-state gradient runs the two-term path: U, Kb, delta
@@ -3357,11 +3492,11 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         gam = p0.gam;
     } else {
         if ((st = run_intra_tc(d, w, q, k, v, g, beta, true, s, &gam, px ? w.Ulo : nullptr,
-                               px ? w.Kblo : nullptr)) != KDA_OK)
+                               px ? w.Kblo : nullptr, vl)) != KDA_OK)
             return st;
         // forward recompute: chunk-start states and delta
         if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s, 0,
-                                px ? w.Ulo : nullptr, px ? w.d2lo : nullptr)) != KDA_OK)
+                                px ? w.Ulo : nullptr, px ? w.d2lo : nullptr, vl)) != KDA_OK)
             return st;
     }
     const int BH = d.B * d.HV, NT = d.T / kC;
@@ -3370,7 +3505,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     {
         CUtensorMap mdo, mq, mw, mk, ma, mdh, mddst;
         if (!make_map(&mdh, w.dh2, (uint64_t)BH * NT * kD, kD, 64, 128, true) ||
-            !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV, d.V) ||
+            !make_map_tok(&mdo, dout, tok_rows(d, vl), d.HV, d.V) ||
             !make_map(&mq, w.Q2, rows, kD, 64, 64, true) ||
             !make_map(&mw, w.W2, rows, kD, 64, 64, true) ||
             !make_map(&mk, w.Kb2, rows, kD, 64, 64, true) ||
@@ -3388,12 +3523,16 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.dh0 = dh0;
         a.dh_out = w.dh2;
         a.dh_lo = px ? w.dhlo : nullptr;
-        auto kern = px ? chain_bwd_kernel<true> : chain_bwd_kernel<false>;
+        a.ctab = vl ? vl->ctab : nullptr;
+        a.sfirst = vl ? vl->sfirst : nullptr;
+        auto kern = vl ? (px ? chain_bwd_kernel<true, true> : chain_bwd_kernel<false, true>)
+                       : (px ? chain_bwd_kernel<true, false> : chain_bwd_kernel<false, false>);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)CHAIN_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
         TimedLaunch tl("tc_chain_bwd", s);
-        kern<<<BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, mdh, mddst, a);
+        kern<<<vl ? vl->nseq * d.HV : BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, mdh,
+                                                                         mddst, a);
     }
     if ((st = launch_status()) != KDA_OK) return st;
     // contractions over V
@@ -3404,10 +3543,10 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         const uint64_t srows = (uint64_t)BH * NT * kD;
         if (!make_map(&mh, w.h2, srows, kD, 64, 128, true) ||
             !make_map(&mdh, w.dh2, srows, kD, 64, 128, true) ||
-            !make_map_tok(&mdo, dout, (uint64_t)d.B * d.T, d.HV, d.V) ||
+            !make_map_tok(&mdo, dout, tok_rows(d, vl), d.HV, d.V) ||
             !make_map(&mdd, w.dd2, rows, kD, 64, 64, true) ||
             !make_map(&md, w.d2, srows, kC, 64, 128, true) ||
-            !make_map_tok(&mv, v, (uint64_t)d.B * d.T, d.HV, d.V) ||
+            !make_map_tok(&mv, v, tok_rows(d, vl), d.HV, d.V) ||
             !make_map(&mt, w.T2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
             return KDA_ERR_CUDA;
         GradArgs a;
@@ -3425,6 +3564,7 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
         a.dAqk = reinterpret_cast<__nv_bfloat16*>(p.dAqk);
         a.dTv = p.dTv;
         a.dbv = p.dbv;
+        a.ctab = vl ? vl->ctab : nullptr;
         if (px) {
             CUtensorMap mdhl, mdl, mkb, mkbl, ma;
             if (!make_map(&mdhl, w.dhlo, srows, kD, 64, 128, true) ||
@@ -3433,7 +3573,8 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                 !make_map(&mkbl, w.Kblo, rows, kD, 64, 64, true) ||
                 !make_map(&ma, w.Aqk2, (uint64_t)BH * NT * kC, kC, 64, 64, true))
                 return KDA_ERR_CUDA;
-            auto kern = d.V == kD ? grad_v_px_kernel<kD> : grad_v_px_kernel<64>;
+            auto kern = d.V == kD ? (vl ? grad_v_px_kernel<kD, true> : grad_v_px_kernel<kD, false>)
+                                  : (vl ? grad_v_px_kernel<64, true> : grad_v_px_kernel<64, false>);
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)PX_SMEM) != cudaSuccess)
                 return KDA_ERR_CUDA;
@@ -3441,7 +3582,8 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
             kern<<<std::min(BH * NT, sm_count()), kGradThreads, PX_SMEM, s>>>(
                 mh, mdh, mdhl, mdo, md, mdl, mkb, mkbl, ma, mv, mt, a);
         } else {
-            auto kern = d.V == kD ? grad_v_kernel<kD> : grad_v_kernel<64>;
+            auto kern = d.V == kD ? (vl ? grad_v_kernel<kD, true> : grad_v_kernel<kD, false>)
+                                  : (vl ? grad_v_kernel<64, true> : grad_v_kernel<64, false>);
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)GRAD_SMEM) != cudaSuccess)
                 return KDA_ERR_CUDA;
@@ -3454,9 +3596,80 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
     if ((st = launch_status()) != KDA_OK) return st;
     SimtWsPtrs p;
     simt_ws_ptrs(tc_wide(d), 1, w.simt, &p);
-    if ((st = run_local_bwd_tc(d, w, p, q, k, g, beta, dq, dk, dg, dbeta, s)) != KDA_OK) return st;
+    if ((st = run_local_bwd_tc(d, w, p, q, k, g, beta, dq, dk, dg, dbeta, s, vl)) != KDA_OK)
+        return st;
     if (d.HV == d.H && !d.qk_l2norm) return KDA_OK;
-    return group_sum_launch(d, p.dqh, p.dkh, q, k, dq, dk, s);
+    kda_dims dt = d;   // the token rows of the dq, dk arrays
+    if (vl) dt.T = vl->Ttok;
+    return group_sum_launch(dt, p.dqh, p.dkh, q, k, dq, dk, s);
+}
+
+// Padded dims of a packed batch (the SIMT kernels use the same bound): B = 1
+// and ceil(T / 64) + nseq chunk slots.
+kda_dims tc_varlen_dims(const kda_dims& d, int nseq) {
+    kda_dims p = d;
+    p.B = 1;
+    p.T = ((d.T + kC - 1) / kC + nseq) * kC;
+    return p;
+}
+// The workspace of a packed batch: the tensor-core carve of the padded dims,
+// then the chunk table [NT][2] and the first chunk slot of every sequence.
+size_t tc_varlen_carve(const kda_dims& d, int nseq, int for_bwd, char* base, TcWs* w,
+                       TcVl* vl) {
+    const kda_dims p = tc_varlen_dims(d, nseq);
+    size_t off = tc_carve(p, for_bwd, base, w);
+    int* ctab = base ? reinterpret_cast<int*>(base + off) : nullptr;
+    off += align256((size_t)(p.T / kC) * 2 * sizeof(int));
+    int* sfirst = base ? reinterpret_cast<int*>(base + off) : nullptr;
+    off += align256((size_t)(nseq + 1) * sizeof(int));
+    if (vl) *vl = TcVl{ctab, sfirst, nseq, d.T};
+    return off;
+}
+}  // namespace
+
+kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v, const void* g,
+                  const void* beta, const float* h0, const void* dout, const float* dht,
+                  void* dq, void* dk, void* dv, void* dg, void* dbeta, float* dh0, void* ws,
+                  bool from_saved, cudaStream_t s) {
+    TcWs w;
+    tc_carve(d, 1, static_cast<char*>(ws), &w);
+    return tc_bwd_run(d, w, nullptr, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0,
+                      from_saved, s);
+}
+
+size_t tc_varlen_workspace_bytes(const kda_dims& d, int nseq, int for_bwd) {
+    return tc_varlen_carve(d, nseq, for_bwd ? 1 : 0, nullptr, nullptr, nullptr);
+}
+
+kda_status tc_fwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q, const void* k,
+                         const void* v, const void* g, const void* beta, const float* h0, void* o,
+                         float* ht, void* ws, cudaStream_t s) {
+    TcWs w;
+    TcVl vl;
+    tc_varlen_carve(d, nseq, 0, static_cast<char*>(ws), &w, &vl);
+    const kda_dims p = tc_varlen_dims(d, nseq);
+    kda_status st = varlen_table_launch(cu, nseq, d.T, kC, p.T / kC, const_cast<int*>(vl.ctab),
+                                        const_cast<int*>(vl.sfirst), s);
+    if (st != KDA_OK) return st;
+    float* gam = nullptr;
+    if ((st = run_intra_tc(p, w, q, k, v, g, beta, false, s, &gam, nullptr, nullptr, &vl)) != KDA_OK)
+        return st;
+    return run_chain_fwd(p, w, gam, h0, o, ht, nullptr, nullptr, s, 0, nullptr, nullptr, &vl);
+}
+
+kda_status tc_bwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q, const void* k,
+                         const void* v, const void* g, const void* beta, const float* h0,
+                         const void* dout, const float* dht, void* dq, void* dk, void* dv,
+                         void* dg, void* dbeta, float* dh0, void* ws, cudaStream_t s) {
+    TcWs w;
+    TcVl vl;
+    tc_varlen_carve(d, nseq, 1, static_cast<char*>(ws), &w, &vl);
+    const kda_dims p = tc_varlen_dims(d, nseq);
+    kda_status st = varlen_table_launch(cu, nseq, d.T, kC, p.T / kC, const_cast<int*>(vl.ctab),
+                                        const_cast<int*>(vl.sfirst), s);
+    if (st != KDA_OK) return st;
+    return tc_bwd_run(p, w, &vl, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0,
+                      false, s);
 }
 
 namespace {

@@ -162,8 +162,12 @@ kda_status kda_chunk_bwd_saved(const kda_dims* dims, const void* q, const void* 
  * mask); these entry points let a batch of unequal sequences be packed
  * along T instead, each sequence scanned on its own.
  *   dims        B must be 1; T = the total token count (any T >= 0, no
- *               multiple of chunk_size needed); impl AUTO or SIMT (the fp32
- *               CUDA-core kernels run; TCGEN05 returns KDA_ERR_UNSUPPORTED).
+ *               multiple of chunk_size needed); impl as for kda_chunk_fwd
+ *               (AUTO: the tensor cores for bf16, K = V = 64 or 128, chunk
+ *               64, and T > 0; else the SIMT kernels).  On the tensor cores
+ *               each sequence's chunks are tiles of 64 tokens from its
+ *               first token; the state passes run one CTA per (sequence,
+ *               value head).  The backward always recomputes the forward.
  *   cu_seqlens  DEVICE int32 [num_seqs + 1]: sequence s is tokens
  *               [cu_seqlens[s], cu_seqlens[s+1]); it must start at 0, end at
  *               T and not decrease (empty sequences allowed).  It is read on

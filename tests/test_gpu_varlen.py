@@ -163,3 +163,64 @@ def test_invalid_cu_seqlens_reported_by_check():
     with pytest.raises(kda.KdaError):
         kda.check()
     assert torch.equal(ht, h0 + 1.0)
+
+
+@pytest.mark.parametrize("H,HV,K,lengths,with_h0,with_dht,qkn", [
+    (2, 4, 128, [200, 64, 7, 0, 129, 1, 300], True, True, False),
+    (2, 2, 64, [65, 127, 64, 3], True, False, False),
+    (1, 2, 128, [100, 28, 250], True, False, True),
+])
+def test_varlen_tcgen05(H, HV, K, lengths, with_h0, with_dht, qkn):
+    """Packed sequences on the tensor cores: each sequence's chunks are
+    64-token tiles from its first token (the last one partial, its rows past
+    the end masked on load and not written), the state passes run one CTA per
+    (sequence, value head).  GVA, K = V = 64 and 128, empty and one-token
+    sequences, an upstream final-state gradient (the two-term backward) and
+    the in-kernel q/k normalisation.  (The normalisation with an O(1) dht is
+    left to the fixed-length test: the kernels' bf16 rounding of the
+    normalised q, k alone can move a small dbeta element to the bar.)"""
+    inp, cu = packed_inputs(lengths, H, HV, K, K, torch.bfloat16, seed=71 + K + len(lengths),
+                            with_h0=with_h0, with_dht=with_dht, normalize_qk=not qkn)
+    res = run_packed(inp, cu, 64, impl="tcgen05", qk_l2norm=qkn)
+    compare(res, oracle_packed(inp, cu, True, qk_l2norm=qkn), torch.bfloat16, with_h0=with_h0)
+
+
+def test_varlen_tcgen05_one_sequence_equals_the_fixed_length_scan():
+    w = I.Workload("one_seq_tc", 1, 256, 2, 2, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
+                   h0_std=0.2, dht=True, seed=74)
+    inp = I.make_chunk_inputs(w)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    res = run_packed(inp, np.array([0, 256], dtype=np.int32), 64, impl="tcgen05")
+    o, ht = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
+                              output_final_state=True, impl="tcgen05")
+    gr = kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], dht=t["dht"],
+                           initial_state=t["h0"], impl="tcgen05")
+    torch.cuda.synchronize()
+    assert torch.equal(res["o"], o) and torch.equal(res["ht"], ht)
+    for n in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        assert torch.equal(res[n], gr[n]), n
+
+
+def test_varlen_tcgen05_invalid_cu_seqlens_and_empty_batch():
+    """On the tensor-core dims: an invalid cu_seqlens leaves every final
+    state at its initial value and is reported by kda_check; an empty packed
+    batch (T = 0) returns the initial states."""
+    inp, _ = packed_inputs([70, 58], 2, 2, 128, 128, torch.bfloat16, seed=75)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    bad = torch.tensor([0, 90, 40, 128], dtype=torch.int32, device="cuda")
+    h0 = torch.randn(3, 2, 128, 128, device="cuda")
+    kda.check()
+    _, ht = kda.chunk_kda_fwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], bad,
+                                     initial_state=h0, output_final_state=True, impl="tcgen05")
+    with pytest.raises(kda.KdaError) as ei:
+        kda.check()
+    assert ei.value.status == 2
+    assert torch.equal(ht, h0)
+    e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")
+    cu = torch.zeros(3, dtype=torch.int32, device="cuda")
+    _, ht = kda.chunk_kda_fwd_varlen(e(1, 0, 2, 128), e(1, 0, 2, 128), e(1, 0, 2, 128),
+                                     e(1, 0, 2, 128), e(1, 0, 2), cu, initial_state=h0[:2],
+                                     output_final_state=True)
+    torch.cuda.synchronize()
+    kda.check()
+    assert torch.equal(ht, h0[:2])
