@@ -1,6 +1,8 @@
 """Parity of the CUDA chunk scan (forward and backward) with the float64
 oracle, on the seeded workloads and on edge cases.  All calls go through the
 C ABI via the ctypes binding."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -432,6 +434,33 @@ def test_train_shape_full_size_saved_sampled_heads():
         assert_close(f"ht[{b},{hv}]", res["ht"][b:b + 1, hv:hv + 1], ref["ht"], w.dtype)
         for n in GRADS:
             assert_close(f"{n}[{b},{hv}]", sl(res[n]), ref[n], w.dtype)
+
+
+def test_train_shape_full_size_final_state_gradient_sampled_heads():
+    """The training size with an initial state and an O(1) upstream
+    final-state gradient on the tensor cores (the two-term backward, which
+    recomputes even after a saving forward), on sampled heads against the
+    oracle."""
+    w = dataclasses.replace(I.TRAIN_BF16, h0_std=0.1, dht=True, seed=33)
+    heads = [(1, 5), (3, 14)]
+    inp = I.make_chunk_inputs(w, device="cuda")
+    o, ht, sv = kda.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                  initial_state=inp["h0"], output_final_state=True,
+                                  impl="tcgen05", save_for_backward=True)
+    res = dict(o=o, ht=ht)
+    res.update(kda.chunk_kda_bwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["do"],
+                                 dht=inp["dht"], initial_state=inp["h0"], impl="tcgen05",
+                                 saved=sv))
+    torch.cuda.synchronize()
+    kda.check()
+    refs = oracle_chunk(inp, True, heads=heads)
+    for (b, hv), ref in zip(heads, refs):
+        sl = lambda x: x[b:b + 1, :, hv:hv + 1]
+        assert_close(f"o[{b},{hv}]", sl(res["o"]), ref["o"], w.dtype)
+        assert_close(f"ht[{b},{hv}]", res["ht"][b:b + 1, hv:hv + 1], ref["ht"], w.dtype)
+        for n in GRADS:
+            assert_close(f"{n}[{b},{hv}]", sl(res[n]), ref[n], w.dtype)
+        assert_close(f"dh0[{b},{hv}]", res["dh0"][b:b + 1, hv:hv + 1], ref["dh0"], w.dtype)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
