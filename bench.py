@@ -415,9 +415,9 @@ def measure_chunk_sizes(kda, dev, steps=10, warmup=3):
 def measure_varlen(kda, dev, steps=5, warmup=3):
     """Packed variable-length sequences at the training head shape (H=HV=16,
     K=V=128, bf16): 32768 tokens cut into seeded lengths of 512 to 4096,
-    fwd+bwd (stateless backward) through kda_chunk_fwd_varlen /
-    _bwd_varlen on the tensor cores (AUTO) and on the CUDA-core kernels,
-    timed with CUDA events."""
+    fwd+bwd through kda_chunk_fwd_varlen / _bwd_varlen on the tensor cores
+    (saving forward + saved backward, and stateless) and on the CUDA-core
+    kernels, timed with CUDA events."""
     from gated_delta_rule_41_gb300 import inputs as I
     gen = torch.Generator().manual_seed(91)
     lengths, total = [], 32768
@@ -431,11 +431,18 @@ def measure_varlen(kda, dev, steps=5, warmup=3):
     cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32, device=dev)
     out = {"sequences": len(lengths), "tokens": w.T, "min_len": min(lengths),
            "max_len": max(lengths)}
-    for impl in ("tcgen05", "simt"):
+    for name in ("tcgen05_saved", "tcgen05", "simt"):
+        impl = name.split("_")[0]
+
         def step():
-            kda.chunk_kda_fwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], cu, impl=impl)
+            if name.endswith("_saved"):   # saving forward, backward from its workspace
+                _, _, sv = kda.chunk_kda_fwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                                    cu, impl=impl, save_for_backward=True)
+            else:
+                sv = None
+                kda.chunk_kda_fwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], cu, impl=impl)
             kda.chunk_kda_bwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], cu,
-                                     impl=impl)
+                                     impl=impl, saved=sv)
         for _ in range(warmup):
             step()
         torch.cuda.synchronize()
@@ -448,8 +455,9 @@ def measure_varlen(kda, dev, steps=5, warmup=3):
         torch.cuda.synchronize()
         kda.check()
         ms = e0.elapsed_time(e1) / steps
-        out[impl] = {"ms_per_step": ms, "tokens_per_s": w.T / (ms / 1e3)}
-    out["pass"] = "fwd+bwd, stateless backward, no h0"
+        out[name] = {"ms_per_step": ms, "tokens_per_s": w.T / (ms / 1e3)}
+    out["pass"] = ("fwd+bwd, no h0; tcgen05_saved: saving forward and the backward from its "
+                   "workspace; tcgen05, simt: stateless backward")
     return out
 
 

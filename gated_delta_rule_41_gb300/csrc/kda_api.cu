@@ -222,11 +222,11 @@ size_t kda_chunk_workspace_bytes_varlen(const kda_dims* d, int num_seqs, int for
     return varlen_ws_bytes(*d, impl, num_seqs, for_bwd ? 1 : 0);
 }
 
-kda_status kda_chunk_fwd_varlen(const kda_dims* d, const int* cu_seqlens, int num_seqs,
-                                const void* q, const void* k, const void* v, const void* g,
-                                const void* beta, const float* h0, void* o,
-                                int output_final_state, float* ht, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+static kda_status varlen_fwd(const kda_dims* d, const int* cu_seqlens, int num_seqs,
+                             const void* q, const void* k, const void* v, const void* g,
+                             const void* beta, const float* h0, void* o, int output_final_state,
+                             float* ht, void* workspace, size_t workspace_bytes, void* stream,
+                             bool save) {
     kda_status st = check_varlen(d, cu_seqlens, num_seqs);
     if (st != KDA_OK) return st;
     const int impl = pick_varlen_impl(*d);
@@ -237,23 +237,24 @@ kda_status kda_chunk_fwd_varlen(const kda_dims* d, const int* cu_seqlens, int nu
                          {h0, output_final_state ? ht : nullptr})) != KDA_OK)
         return st;
     if ((st = check_ptrs(empty, elem_bytes(*d), {beta}, {})) != KDA_OK) return st;
-    const size_t need = varlen_ws_bytes(*d, impl, num_seqs, 0);
+    const size_t need = varlen_ws_bytes(*d, impl, num_seqs, save ? 1 : 0);
     if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_ALIGNMENT;
     auto s = static_cast<cudaStream_t>(stream);
     if (impl == KDA_IMPL_TCGEN05)
         return tc_fwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, o,
-                             output_final_state ? ht : nullptr, workspace, s);
+                             output_final_state ? ht : nullptr, workspace, save, s);
+    // the SIMT backward recomputes everything: nothing extra to save
     return simt_fwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, o,
                            output_final_state ? ht : nullptr, workspace, s);
 }
 
-kda_status kda_chunk_bwd_varlen(const kda_dims* d, const int* cu_seqlens, int num_seqs,
-                                const void* q, const void* k, const void* v, const void* g,
-                                const void* beta, const float* h0, const void* dout,
-                                const float* dht, void* dq, void* dk, void* dv, void* dg,
-                                void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
-                                void* stream) {
+static kda_status varlen_bwd(const kda_dims* d, const int* cu_seqlens, int num_seqs,
+                             const void* q, const void* k, const void* v, const void* g,
+                             const void* beta, const float* h0, const void* dout,
+                             const float* dht, void* dq, void* dk, void* dv, void* dg,
+                             void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                             void* stream, bool from_saved) {
     kda_status st = check_varlen(d, cu_seqlens, num_seqs);
     if (st != KDA_OK) return st;
     const int impl = pick_varlen_impl(*d);
@@ -269,9 +270,47 @@ kda_status kda_chunk_bwd_varlen(const kda_dims* d, const int* cu_seqlens, int nu
     auto s = static_cast<cudaStream_t>(stream);
     if (impl == KDA_IMPL_TCGEN05)
         return tc_bwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, dout, dht, dq, dk,
-                             dv, dg, dbeta, dh0, workspace, s);
+                             dv, dg, dbeta, dh0, workspace, from_saved, s);
     return simt_bwd_varlen(*d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, dout, dht, dq, dk, dv,
                            dg, dbeta, dh0, workspace, s);
+}
+
+kda_status kda_chunk_fwd_varlen(const kda_dims* d, const int* cu_seqlens, int num_seqs,
+                                const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, const float* h0, void* o,
+                                int output_final_state, float* ht, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    return varlen_fwd(d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, o, output_final_state, ht,
+                      workspace, workspace_bytes, stream, false);
+}
+
+kda_status kda_chunk_fwd_varlen_save(const kda_dims* d, const int* cu_seqlens, int num_seqs,
+                                     const void* q, const void* k, const void* v, const void* g,
+                                     const void* beta, const float* h0, void* o,
+                                     int output_final_state, float* ht, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+    return varlen_fwd(d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, o, output_final_state, ht,
+                      workspace, workspace_bytes, stream, true);
+}
+
+kda_status kda_chunk_bwd_varlen(const kda_dims* d, const int* cu_seqlens, int num_seqs,
+                                const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, const float* h0, const void* dout,
+                                const float* dht, void* dq, void* dk, void* dv, void* dg,
+                                void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    return varlen_bwd(d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg,
+                      dbeta, dh0, workspace, workspace_bytes, stream, false);
+}
+
+kda_status kda_chunk_bwd_varlen_saved(const kda_dims* d, const int* cu_seqlens, int num_seqs,
+                                      const void* q, const void* k, const void* v, const void* g,
+                                      const void* beta, const float* h0, const void* dout,
+                                      const float* dht, void* dq, void* dk, void* dv, void* dg,
+                                      void* dbeta, float* dh0, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    return varlen_bwd(d, cu_seqlens, num_seqs, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg,
+                      dbeta, dh0, workspace, workspace_bytes, stream, true);
 }
 
 kda_status kda_recurrent_step(const kda_dims* d, const void* q, const void* k, const void* v,

@@ -96,15 +96,16 @@ kda_status tc_bwd(const kda_dims& d, const void* q, const void* k, const void* v
                   const float* dht, void* dq, void* dk, void* dv, void* dg, void* dbeta,
                   float* dh0, void* ws, bool from_saved, cudaStream_t s);
 // Packed variable-length sequences on the tensor-core kernels (same
-// arguments as the SIMT versions; the stateless backward).
+// arguments as the SIMT versions; save / from_saved as for tc_fwd / tc_bwd).
 size_t tc_varlen_workspace_bytes(const kda_dims& d, int nseq, int for_bwd);
 kda_status tc_fwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q, const void* k,
                          const void* v, const void* g, const void* beta, const float* h0, void* o,
-                         float* ht, void* ws, cudaStream_t s);
+                         float* ht, void* ws, bool save, cudaStream_t s);
 kda_status tc_bwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q, const void* k,
                          const void* v, const void* g, const void* beta, const float* h0,
                          const void* dout, const float* dht, void* dq, void* dk, void* dv,
-                         void* dg, void* dbeta, float* dh0, void* ws, cudaStream_t s);
+                         void* dg, void* dbeta, float* dh0, void* ws, bool from_saved,
+                         cudaStream_t s);
 // Reads and clears the device error word of the tensor-core kernels.
 kda_status tc_take_error(cudaStream_t s);
 // Diagnostic: a bounded wait on an mbarrier nothing arrives at, with the given

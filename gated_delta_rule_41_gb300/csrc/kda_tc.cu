@@ -3643,24 +3643,26 @@ size_t tc_varlen_workspace_bytes(const kda_dims& d, int nseq, int for_bwd) {
 
 kda_status tc_fwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q, const void* k,
                          const void* v, const void* g, const void* beta, const float* h0, void* o,
-                         float* ht, void* ws, cudaStream_t s) {
+                         float* ht, void* ws, bool save, cudaStream_t s) {
     TcWs w;
     TcVl vl;
-    tc_varlen_carve(d, nseq, 0, static_cast<char*>(ws), &w, &vl);
+    tc_varlen_carve(d, nseq, save ? 1 : 0, static_cast<char*>(ws), &w, &vl);
     const kda_dims p = tc_varlen_dims(d, nseq);
     kda_status st = varlen_table_launch(cu, nseq, d.T, kC, p.T / kC, const_cast<int*>(vl.ctab),
                                         const_cast<int*>(vl.sfirst), s);
     if (st != KDA_OK) return st;
     float* gam = nullptr;
-    if ((st = run_intra_tc(p, w, q, k, v, g, beta, false, s, &gam, nullptr, nullptr, &vl)) != KDA_OK)
+    if ((st = run_intra_tc(p, w, q, k, v, g, beta, save, s, &gam, nullptr, nullptr, &vl)) != KDA_OK)
         return st;
-    return run_chain_fwd(p, w, gam, h0, o, ht, nullptr, nullptr, s, 0, nullptr, nullptr, &vl);
+    return run_chain_fwd(p, w, gam, h0, o, ht, save ? w.h2 : nullptr, save ? w.d2 : nullptr, s, 0,
+                         nullptr, nullptr, &vl);
 }
 
 kda_status tc_bwd_varlen(const kda_dims& d, const int* cu, int nseq, const void* q, const void* k,
                          const void* v, const void* g, const void* beta, const float* h0,
                          const void* dout, const float* dht, void* dq, void* dk, void* dv,
-                         void* dg, void* dbeta, float* dh0, void* ws, cudaStream_t s) {
+                         void* dg, void* dbeta, float* dh0, void* ws, bool from_saved,
+                         cudaStream_t s) {
     TcWs w;
     TcVl vl;
     tc_varlen_carve(d, nseq, 1, static_cast<char*>(ws), &w, &vl);
@@ -3668,8 +3670,9 @@ kda_status tc_bwd_varlen(const kda_dims& d, const int* cu, int nseq, const void*
     kda_status st = varlen_table_launch(cu, nseq, d.T, kC, p.T / kC, const_cast<int*>(vl.ctab),
                                         const_cast<int*>(vl.sfirst), s);
     if (st != KDA_OK) return st;
+    // (the table is rebuilt from cu_seqlens even after a saving forward)
     return tc_bwd_run(p, w, &vl, q, k, v, g, beta, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0,
-                      false, s);
+                      from_saved, s);
 }
 
 namespace {

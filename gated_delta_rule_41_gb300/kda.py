@@ -64,10 +64,12 @@ def load_library():
             getattr(lib, name).restype = I
         lib.kda_chunk_workspace_bytes_varlen.argtypes = [D, I, I]
         lib.kda_chunk_workspace_bytes_varlen.restype = S
-        lib.kda_chunk_fwd_varlen.argtypes = [D, P, I, P, P, P, P, P, P, P, I, P, P, S, P]
-        lib.kda_chunk_fwd_varlen.restype = I
-        lib.kda_chunk_bwd_varlen.argtypes = [D, P, I] + [P] * 15 + [S, P]
-        lib.kda_chunk_bwd_varlen.restype = I
+        for name in ("kda_chunk_fwd_varlen", "kda_chunk_fwd_varlen_save"):
+            getattr(lib, name).argtypes = [D, P, I, P, P, P, P, P, P, P, I, P, P, S, P]
+            getattr(lib, name).restype = I
+        for name in ("kda_chunk_bwd_varlen", "kda_chunk_bwd_varlen_saved"):
+            getattr(lib, name).argtypes = [D, P, I] + [P] * 15 + [S, P]
+            getattr(lib, name).restype = I
         lib.kda_recurrent_step.argtypes = [D] + [P] * 8
         lib.kda_recurrent_step.restype = I
         lib.kda_check.argtypes = [P]
@@ -219,10 +221,13 @@ def _check_cu(cu_seqlens):
 
 def chunk_kda_fwd_varlen(q, k, v, g, beta, cu_seqlens, scale=None, initial_state=None,
                          output_final_state=False, chunk_size=64, impl="auto", workspace=None,
-                         out=None, final_state=None, stream=None, use_qk_l2norm_in_kernel=False):
+                         out=None, final_state=None, stream=None, use_qk_l2norm_in_kernel=False,
+                         save_for_backward=False):
     """Forward over sequences packed along T: q, k [1,T,H,K]; v [1,T,HV,V];
     g [1,T,HV,K]; beta [1,T,HV]; ``cu_seqlens`` int32 [N+1] on the device.
-    ``initial_state`` / the final state are [N,HV,K,V].  Returns (o, ht)."""
+    ``initial_state`` / the final state are [N,HV,K,V].  Returns (o, ht), or
+    (o, ht, saved) with ``save_for_backward`` (pass ``saved`` to
+    ``chunk_kda_bwd_varlen`` with the same inputs and cu_seqlens)."""
     lib = load_library()
     _check_dev(q, k, v, g, beta, initial_state)
     nseq = _check_cu(cu_seqlens)
@@ -232,22 +237,27 @@ def chunk_kda_fwd_varlen(q, k, v, g, beta, cu_seqlens, scale=None, initial_state
     if output_final_state:
         ht = (torch.empty(nseq, dims.HV, dims.K, dims.V, dtype=torch.float32, device=q.device)
               if final_state is None else final_state)
-    need = int(lib.kda_chunk_workspace_bytes_varlen(ctypes.byref(dims), nseq, 0))
+    need = int(lib.kda_chunk_workspace_bytes_varlen(ctypes.byref(dims), nseq,
+                                                   int(save_for_backward)))
     ws = workspace if (workspace is not None and workspace.numel() >= need) else \
         torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    st = lib.kda_chunk_fwd_varlen(ctypes.byref(dims), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k),
-                                  _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(o),
-                                  int(output_final_state), _ptr(ht), _ptr(ws), need,
-                                  _stream(stream))
+    fn = lib.kda_chunk_fwd_varlen_save if save_for_backward else lib.kda_chunk_fwd_varlen
+    st = fn(ctypes.byref(dims), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+            _ptr(beta), _ptr(initial_state), _ptr(o), int(output_final_state), _ptr(ht), _ptr(ws),
+            need, _stream(stream))
     _raise(st, "kda_chunk_fwd_varlen")
+    if save_for_backward:
+        return o, ht, SavedForward(ws, need, dims)
     return o, ht
 
 
 def chunk_kda_bwd_varlen(q, k, v, g, beta, do, cu_seqlens, dht=None, scale=None,
                          initial_state=None, chunk_size=64, impl="auto", workspace=None,
-                         grads=None, stream=None, use_qk_l2norm_in_kernel=False):
+                         grads=None, stream=None, use_qk_l2norm_in_kernel=False, saved=None):
     """Backward of chunk_kda_fwd_varlen.  Returns dict dq, dk, dv, dg, dbeta,
-    dh0 (dh0 [N,HV,K,V] when ``initial_state`` is given)."""
+    dh0 (dh0 [N,HV,K,V] when ``initial_state`` is given).  With ``saved``
+    (from a saving forward on the same inputs and cu_seqlens) the tensor-core
+    kernels start from the saved intermediates."""
     lib = load_library()
     _check_dev(q, k, v, g, beta, do, dht, initial_state)
     nseq = _check_cu(cu_seqlens)
@@ -257,14 +267,22 @@ def chunk_kda_bwd_varlen(q, k, v, g, beta, do, cu_seqlens, dht=None, scale=None,
                      dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
                      dh0=(torch.empty(nseq, dims.HV, dims.K, dims.V, dtype=torch.float32,
                                       device=q.device) if initial_state is not None else None))
-    need = int(lib.kda_chunk_workspace_bytes_varlen(ctypes.byref(dims), nseq, 1))
-    ws = workspace if (workspace is not None and workspace.numel() >= need) else \
-        torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    st = lib.kda_chunk_bwd_varlen(ctypes.byref(dims), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k),
-                                  _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(do),
-                                  _ptr(dht), _ptr(grads["dq"]), _ptr(grads["dk"]),
-                                  _ptr(grads["dv"]), _ptr(grads["dg"]), _ptr(grads["dbeta"]),
-                                  _ptr(grads.get("dh0")), _ptr(ws), need, _stream(stream))
+    if saved is not None:
+        if (saved.dims.T, saved.dims.H, saved.dims.HV, saved.dims.K, saved.dims.V,
+                saved.dims.chunk_size, saved.dims.impl, saved.dims.qk_l2norm) != (
+                    dims.T, dims.H, dims.HV, dims.K, dims.V, dims.chunk_size, dims.impl,
+                    dims.qk_l2norm):
+            raise KdaError(1, "chunk_kda_bwd_varlen: saved forward has other dims")
+        ws, need, fn = saved.workspace, saved.nbytes, lib.kda_chunk_bwd_varlen_saved
+    else:
+        need = int(lib.kda_chunk_workspace_bytes_varlen(ctypes.byref(dims), nseq, 1))
+        ws = workspace if (workspace is not None and workspace.numel() >= need) else \
+            torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        fn = lib.kda_chunk_bwd_varlen
+    st = fn(ctypes.byref(dims), _ptr(cu_seqlens), nseq, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+            _ptr(beta), _ptr(initial_state), _ptr(do), _ptr(dht), _ptr(grads["dq"]),
+            _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dg"]), _ptr(grads["dbeta"]),
+            _ptr(grads.get("dh0")), _ptr(ws), need, _stream(stream))
     _raise(st, "kda_chunk_bwd_varlen")
     return grads
 

@@ -195,6 +195,26 @@ kda_status kda_chunk_bwd_varlen(const kda_dims* dims, const int* cu_seqlens, int
                                 void* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/* The saving pair of the packed entry points, as kda_chunk_fwd_save /
+ * kda_chunk_bwd_saved are of the fixed-length ones: the forward keeps what
+ * the backward needs in a workspace of kda_chunk_workspace_bytes_varlen(dims,
+ * num_seqs, 1) bytes, and the backward, given that workspace untouched and
+ * the same dims, cu_seqlens and inputs, skips the intra-chunk recompute and
+ * the forward state pass on the tensor cores (unless dht is given; the SIMT
+ * kernels always recompute).  Arguments, results and errors otherwise as
+ * kda_chunk_fwd_varlen / kda_chunk_bwd_varlen. */
+kda_status kda_chunk_fwd_varlen_save(const kda_dims* dims, const int* cu_seqlens, int num_seqs,
+                                     const void* q, const void* k, const void* v, const void* g,
+                                     const void* beta, const float* h0, void* o,
+                                     int output_final_state, float* ht, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+kda_status kda_chunk_bwd_varlen_saved(const kda_dims* dims, const int* cu_seqlens, int num_seqs,
+                                      const void* q, const void* k, const void* v, const void* g,
+                                      const void* beta, const float* h0, const void* dout,
+                                      const float* dht, void* dq, void* dk, void* dv, void* dg,
+                                      void* dbeta, float* dh0, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
 /* One decode token per head, state updated in place (K3 row L6).
  * dims->T is ignored; q, k [B,H,K]; v, o [B,HV,V]; g [B,HV,K]; beta [B,HV]
  * (dtype); state [B,HV,K,V] f32, read and overwritten. */

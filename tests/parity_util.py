@@ -72,14 +72,26 @@ def oracle_chunk(inp, want_bwd, heads=None, qk_l2norm=False):
             res.update(oracle.bwd_recurrent(q, k, v, g, beta, do, h0=h0, dht=dht))
         return res
     assert q.shape[2] == v.shape[2], "per-head oracle runs need H == HV"
+    # the sampled heads side by side as the heads of one batch row, so that
+    # one oracle call runs them in parallel (the heads are independent)
+    cat = lambda x: None if x is None else np.concatenate(
+        [x[b:b + 1, :, hv:hv + 1] for b, hv in heads], axis=2)
+    cst = lambda x: None if x is None else np.concatenate(
+        [x[b:b + 1, hv:hv + 1] for b, hv in heads], axis=1)
+    qs, ks, vs, gs, bs = cat(q), cat(k), cat(v), cat(g), cat(beta)
+    o, ht = oracle.fwd_recurrent(qs, ks, vs, gs, bs, h0=cst(h0))
+    allr = dict(o=o, ht=ht)
+    if want_bwd:
+        allr.update(oracle.bwd_recurrent(qs, ks, vs, gs, bs, cat(do), h0=cst(h0), dht=cst(dht)))
     out = []
-    for b, hv in heads:
-        sl = lambda x: None if x is None else x[b:b + 1, :, hv:hv + 1]
-        st = lambda x: None if x is None else x[b:b + 1, hv:hv + 1]
-        qs, ks, vs, gs, bs = sl(q), sl(k), sl(v), sl(g), beta[b:b + 1, :, hv:hv + 1]
-        o, ht = oracle.fwd_recurrent(qs, ks, vs, gs, bs, h0=st(h0))
-        r = dict(o=o, ht=ht)
-        if want_bwd:
-            r.update(oracle.bwd_recurrent(qs, ks, vs, gs, bs, sl(do), h0=st(h0), dht=st(dht)))
+    for i in range(len(heads)):
+        r = {}
+        for n_, x in allr.items():
+            if x is None:
+                r[n_] = None
+            elif n_ in ("ht", "dh0"):
+                r[n_] = x[:, i:i + 1]
+            else:
+                r[n_] = x[:, :, i:i + 1]
         out.append(r)
     return out

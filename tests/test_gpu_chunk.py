@@ -406,7 +406,8 @@ def _sampled(w, heads, impl, backward):
 @pytest.mark.parametrize("impl", IMPLS)
 def test_train_shape_full_size_sampled_heads(impl):
     w = I.TRAIN_BF16
-    res = _sampled(w, [(0, 0), (1, 7), (3, 15)], impl, backward=True)
+    heads = [(0, 0), (0, 9), (1, 3), (1, 14), (2, 6), (2, 11), (3, 1), (3, 15)]
+    res = _sampled(w, heads, impl, backward=True)
     for n in ["o"] + GRADS:
         assert torch.isfinite(res[n].float()).all(), n
 
@@ -416,7 +417,7 @@ def test_train_shape_full_size_saved_sampled_heads():
     backward from its workspace, at the full training size (AUTO takes the
     tensor cores), on sampled heads against the oracle."""
     w = I.TRAIN_BF16
-    heads = [(0, 3), (2, 12)]
+    heads = [(0, 3), (0, 12), (1, 8), (2, 0), (2, 12), (3, 7)]
     inp = I.make_chunk_inputs(w, device="cuda")
     o, ht, sv = kda.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                   initial_state=inp["h0"], output_final_state=True,
@@ -442,7 +443,7 @@ def test_train_shape_full_size_final_state_gradient_sampled_heads():
     recomputes even after a saving forward), on sampled heads against the
     oracle."""
     w = dataclasses.replace(I.TRAIN_BF16, h0_std=0.1, dht=True, seed=33)
-    heads = [(1, 5), (3, 14)]
+    heads = [(0, 10), (1, 5), (2, 2), (3, 14)]
     inp = I.make_chunk_inputs(w, device="cuda")
     o, ht, sv = kda.chunk_kda_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                                   initial_state=inp["h0"], output_final_state=True,
@@ -465,7 +466,7 @@ def test_train_shape_full_size_final_state_gradient_sampled_heads():
 
 @pytest.mark.parametrize("impl", IMPLS)
 def test_long_context_full_size_sampled_heads(impl):
-    _sampled(I.LONG_BF16, [(0, 0), (0, 31)], impl, backward=False)
+    _sampled(I.LONG_BF16, [(0, h) for h in (0, 4, 9, 13, 18, 22, 27, 31)], impl, backward=False)
 
 
 @pytest.mark.parametrize("impl,K,dtype", [("simt", 64, torch.bfloat16), ("simt", 64, torch.float32),

@@ -224,3 +224,25 @@ def test_varlen_tcgen05_invalid_cu_seqlens_and_empty_batch():
     torch.cuda.synchronize()
     kda.check()
     assert torch.equal(ht, h0[:2])
+
+
+@pytest.mark.parametrize("impl,K,dtype,with_dht", [("tcgen05", 128, torch.bfloat16, False),
+                                                   ("tcgen05", 64, torch.bfloat16, True),
+                                                   ("simt", 32, torch.float32, True)])
+def test_varlen_saved_forward_backward(impl, K, dtype, with_dht):
+    """A saving packed forward, then the backward from its workspace (the
+    tensor cores skip the recompute unless dht is given; the SIMT kernels
+    always recompute): the oracle's outputs and gradients per sequence."""
+    lengths = [130, 0, 64, 9, 190]
+    inp, cu = packed_inputs(lengths, 2, 2, K, K, dtype, seed=77 + K, with_dht=with_dht)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    cu_d = torch.from_numpy(cu).cuda()
+    o, ht, sv = kda.chunk_kda_fwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], cu_d,
+                                         initial_state=t["h0"], output_final_state=True,
+                                         impl=impl, save_for_backward=True)
+    res = dict(o=o, ht=ht)
+    res.update(kda.chunk_kda_bwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], cu_d,
+                                        dht=t["dht"], initial_state=t["h0"], impl=impl, saved=sv))
+    torch.cuda.synchronize()
+    kda.check()
+    compare(res, oracle_packed(inp, cu, True), dtype)
