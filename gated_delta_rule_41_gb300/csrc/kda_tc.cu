@@ -2447,6 +2447,10 @@ constexpr uint32_t LB_DAQ = 90112;    // [dA_R; dAqk_R] rows 32R + 16s + u, 64 c
 constexpr uint32_t LB_T = 106496, LB_TLO = LB_T + 8192;
 constexpr uint32_t LB_RIGHT = 122880; // Right_R tiles, 16(R+1) rows each
 constexpr uint32_t LB_LCOL = 163840;  // [beta k E; qs E] rows 32R + 16s + u, 128 c
+// dq, dk, dg staging tiles for their TMA stores ([64 t][128 c] bf16 as two
+// 128B-swizzled 64-column boxes each), over Right and Lcol: free from the
+// end of P5/P6 until the next chunk's operand build
+constexpr uint32_t LB_STQ = LB_RIGHT, LB_STK = LB_RIGHT + 16384, LB_STG = LB_LCOL;
 constexpr uint32_t LB_SMALL = 196608; // fp32 small arrays
 constexpr uint32_t LB_F = LB_SMALL + 8192;   // F [6 block pairs][128] fp32
 // LB_F + 3072 .. LB_SMALL + 16384: unused
@@ -2495,6 +2499,9 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_t,     // T high part [BH*NT*64][64]
                     const __grid_constant__ CUtensorMap tm_tlo,   // T low part
                     const __grid_constant__ CUtensorMap tm_daq,   // dAqk bf16, 16-row boxes
+                    const __grid_constant__ CUtensorMap tm_dqo,   // dq, dk, dg token tensors:
+                    const __grid_constant__ CUtensorMap tm_dko,   // the outputs' TMA stores
+                    const __grid_constant__ CUtensorMap tm_dgo,
                     LocalTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -2646,6 +2653,9 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         sGtot[R * kD + c] = acc;
     }
+    // the previous chunk's output stores have read the staging tiles before
+    // the operand build below rewrites them
+    if (!VL && tid == 0) bulk_wait_read_all();
     __syncthreads();
     if (tid == 0 && next < total) issue_g(next);   // the next chunk's g tile
     float off = 0.f, Glast = 0.f;
@@ -3004,8 +3014,15 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 // a key channel past the tensors' width (zero-filled), or a
                 // row past a packed sequence's end: not written
             } else if (a.G == 1 && !a.qkn) {
-                a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
-                a.dk[io] = __float2bfloat16_rn(dkv);
+                if (!VL) {   // into the staging tiles, for one TMA store each
+                    const uint32_t so = (uint32_t)(c >> 6) * 8192 + sw128_offset(t, c & 63);
+                    *reinterpret_cast<__nv_bfloat16*>(smem + LB_STQ + so) =
+                        __float2bfloat16_rn(a.scale * dqs);
+                    *reinterpret_cast<__nv_bfloat16*>(smem + LB_STK + so) = __float2bfloat16_rn(dkv);
+                } else {
+                    a.dq[io] = __float2bfloat16_rn(a.scale * dqs);
+                    a.dk[io] = __float2bfloat16_rn(dkv);
+                }
             } else {
                 a.dqh[io] = a.scale * dqs;
                 a.dkh[io] = dkv;
@@ -3040,6 +3057,15 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (tid == 0) issue_main(next);
         issue_dtv(next);
     }
+    if (!VL && tid == 0 && ok && a.G == 1 && !a.qkn) {   // dq, dk (key head = value head)
+        tma_store_3d(&tm_dqo, smem + LB_STQ, 0, hv, trow);
+        tma_store_3d(&tm_dko, smem + LB_STK, 0, hv, trow);
+        if (DW > 64) {
+            tma_store_3d(&tm_dqo, smem + LB_STQ + 8192, 64, hv, trow);
+            tma_store_3d(&tm_dko, smem + LB_STK + 8192, 64, hv, trow);
+        }
+        bulk_commit_group();
+    }
     {
         // dG_last += sum_r dKb_r Kb_r + dgam gam; it enters every row's suffix sum
         float extra = dgam_c * __expf(Glast);
@@ -3052,8 +3078,14 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             run += dG[u];
             const int t = 16 * R + u;
             const size_t ig = (((size_t)trow + t) * a.HV + hv) * DW + c;
-            if ((DW == kD || c < DW) && t < len)
-                a.dg[ig] = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
+            if ((DW == kD || c < DW) && t < len) {
+                const __nv_bfloat16 x = __float2bfloat16_rn((gmask >> u) & 1u ? run : 0.f);
+                if (!VL)
+                    *reinterpret_cast<__nv_bfloat16*>(smem + LB_STG + (uint32_t)(c >> 6) * 8192 +
+                                                      sw128_offset(t, c & 63)) = x;
+                else
+                    a.dg[ig] = x;
+            }
         }
     }
     if (tid < len)
@@ -3061,12 +3093,19 @@ local_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             __float2bfloat16_rn((sDbp[tid] + sDbp[64 + tid]) + (sDbp[128 + tid] + sDbp[192 + tid]) +
                                 dbv_t);
     // partial sums, beta and TMEM are reused by the next chunk
+    fence_async_smem();
     tc_fence_before();
     if (!__syncthreads_and(ok)) break;
     tc_fence_after();
+    if (!VL && tid == 0) {   // dg from its staging tile
+        tma_store_3d(&tm_dgo, smem + LB_STG, 0, hv, trow);
+        if (DW > 64) tma_store_3d(&tm_dgo, smem + LB_STG + 8192, 64, hv, trow);
+        bulk_commit_group();
+    }
     }  // chunk loop
     // loads issued for chunks the loop did not reach (after an error) land
-    // before shared memory is released
+    // before shared memory is released, and the output stores complete
+    if (tid == 0) bulk_wait_all();
     cp_async_wait_all16();
     if (tid == 0) {
         for (; main_waited < main_issued; ++main_waited) wait_bar_drain(bar_tma, main_waited & 1);
@@ -3299,6 +3338,10 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
         !make_map(&mtl, w.Tlo2, rows, kC, 64, 64, true) ||
         !make_map(&mda, p.dAqk, rows, kC, 64, 16, true))
         return KDA_ERR_CUDA;
+    CUtensorMap mdqo, mdko, mdgo;   // the outputs (used by the fixed-length kernel)
+    if (!make_map_tok(&mdqo, dq, BT, d.H, d.K) || !make_map_tok(&mdko, dk, BT, d.H, d.K) ||
+        !make_map_tok(&mdgo, dg, BT, d.HV, d.K))
+        return KDA_ERR_CUDA;
     LocalTcArgs a;
     a.T = d.T;
     a.H = d.H;
@@ -3334,7 +3377,7 @@ kda_status run_local_bwd_tc(const kda_dims& d, const TcWs& w, const SimtWsPtrs& 
         TimedLaunch tl("tc_local_bwd", s);
         // persistent: one CTA per SM walks the chunks
         kern<<<std::min(a.BH * a.NT, sm_count()), kLocalTcThreads, LOCAL_TC_SMEM, s>>>(
-            mk, mq, mg, mdw, mt, mtl, mda, a);
+            mk, mq, mg, mdw, mt, mtl, mda, mdqo, mdko, mdgo, a);
     }
     return launch_status();
 }
