@@ -685,6 +685,29 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_value = world * w.tokens / (e2e_ms / 1e3)
+    # the host link alone: the same copies, both directions at once, no compute
+    # (the floor the end-to-end step cannot go below)
+    reps = max(3, min(args.steps, 10))
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(stream)
+    s_in.wait_event(c0)
+    s_out.wait_event(c0)
+    for i in range(reps):
+        with torch.cuda.stream(s_in):
+            for n in names_in:
+                d_in[i & 1][n].copy_(h_in[n], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for n in h_out:
+                h_out[n].copy_(d_out[i & 1][n], non_blocking=True)
+    e_in, e_out = torch.cuda.Event(), torch.cuda.Event()
+    e_in.record(s_in)
+    e_out.record(s_out)
+    stream.wait_event(e_in)
+    stream.wait_event(e_out)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    copy_ms = c0.elapsed_time(c1) / reps
 
     if rank != 0:
         if world > 1:
@@ -724,6 +747,7 @@ def main():
                           "note": "whole fwd+bwd step: 5638 B per head-token at the copy peak"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "copy_floor_ms": copy_ms, "frac_of_copy_floor": copy_ms / e2e_ms,
                 "via": "the Python binding (kda.chunk_kda_fwd / chunk_kda_bwd); torch copies "
                        "pinned host buffers to and from the device, the C ABI takes device "
                        "pointers"},

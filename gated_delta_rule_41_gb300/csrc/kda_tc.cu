@@ -3150,6 +3150,19 @@ int sm_count() {
     return cache[dev];
 }
 
+// A second stream per device, created on first use: the recomputing backward
+// runs its reverse state pass there, beside the forward state pass.
+cudaStream_t aux_stream() {
+    static std::mutex mu;
+    static cudaStream_t per_dev[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!per_dev[dev] && cudaStreamCreateWithFlags(&per_dev[dev], cudaStreamNonBlocking) != cudaSuccess)
+        per_dev[dev] = nullptr;
+    return per_dev[dev];
+}
+
 // 2-D bf16 map over a row-major [rows][cols] array with a box of
 // box_cols x box_rows.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
@@ -3529,23 +3542,11 @@ kda_status tc_bwd_run(const kda_dims& d, const TcWs& w, const TcVl* vl, const vo
     // over V take grad_v_px_kernel.  The saving forward keeps no low parts,
     // so this path always recomputes.
     const bool px = dht != nullptr;
-    if (from_saved && !px) {
-        SimtWsPtrs p0;
-        simt_ws_ptrs(tc_wide(d), 0, w.simt, &p0);  // where the intra kernel left gam
-        gam = p0.gam;
-    } else {
-        if ((st = run_intra_tc(d, w, q, k, v, g, beta, true, s, &gam, px ? w.Ulo : nullptr,
-                               px ? w.Kblo : nullptr, vl)) != KDA_OK)
-            return st;
-        // forward recompute: chunk-start states and delta
-        if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s, 0,
-                                px ? w.Ulo : nullptr, px ? w.d2lo : nullptr, vl)) != KDA_OK)
-            return st;
-    }
     const int BH = d.B * d.HV, NT = d.T / kC;
     const uint64_t rows = (uint64_t)BH * d.T;
-    // reverse chain
-    {
+    // reverse chain, on stream rs: dS and ddelta from dO and the intra-chunk
+    // quantities alone (the forward states do not enter)
+    auto run_chain_rev = [&](cudaStream_t rs) -> kda_status {
         CUtensorMap mdo, mq, mw, mk, ma, mdh, mddst;
         if (!make_map(&mdh, w.dh2, (uint64_t)BH * NT * kD, kD, 64, 128, true) ||
             !make_map_tok(&mdo, dout, tok_rows(d, vl), d.HV, d.V) ||
@@ -3573,11 +3574,57 @@ kda_status tc_bwd_run(const kda_dims& d, const TcWs& w, const TcVl* vl, const vo
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)CHAIN_SMEM) != cudaSuccess)
             return KDA_ERR_CUDA;
-        TimedLaunch tl("tc_chain_bwd", s);
-        kern<<<vl ? vl->nseq * d.HV : BH, kChainThreads, CHAIN_SMEM, s>>>(mdo, mq, mw, mk, ma, mdh,
-                                                                         mddst, a);
+        TimedLaunch tl("tc_chain_bwd", rs);
+        kern<<<vl ? vl->nseq * d.HV : BH, kChainThreads, CHAIN_SMEM, rs>>>(mdo, mq, mw, mk, ma,
+                                                                          mdh, mddst, a);
+        return launch_status();
+    };
+    if (from_saved && !px) {
+        SimtWsPtrs p0;
+        simt_ws_ptrs(tc_wide(d), 0, w.simt, &p0);  // where the intra kernel left gam
+        gam = p0.gam;
+        if ((st = run_chain_rev(s)) != KDA_OK) return st;
+    } else {
+        if ((st = run_intra_tc(d, w, q, k, v, g, beta, true, s, &gam, px ? w.Ulo : nullptr,
+                               px ? w.Kblo : nullptr, vl)) != KDA_OK)
+            return st;
+        // forward recompute (chunk-start states and delta) and the reverse
+        // pass.  Without an upstream final-state gradient the two read only
+        // the intra-chunk quantities and write disjoint arrays, and each
+        // fills one SM per (sequence, head): they run side by side, the
+        // reverse pass on a second stream.  With one, the reverse pass writes
+        // dS's low parts over U's, which the forward pass reads first.
+        cudaStream_t as = px ? nullptr : aux_stream();
+        if (!as) {
+            if ((st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s, 0,
+                                    px ? w.Ulo : nullptr, px ? w.d2lo : nullptr, vl)) != KDA_OK)
+                return st;
+            if ((st = run_chain_rev(s)) != KDA_OK) return st;
+        } else {
+            cudaEvent_t fork = nullptr, join = nullptr;
+            if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+                if (fork) cudaEventDestroy(fork);
+                return KDA_ERR_CUDA;
+            }
+            kda_status st_rev = KDA_ERR_CUDA;
+            if (cudaEventRecord(fork, s) == cudaSuccess &&
+                cudaStreamWaitEvent(as, fork, 0) == cudaSuccess) {
+                st_rev = run_chain_rev(as);
+                st = run_chain_fwd(d, w, gam, h0, nullptr, nullptr, w.h2, w.d2, s, 0, nullptr,
+                                   nullptr, vl);
+                // the join is recorded whatever the launches returned, so
+                // that the caller's stream always waits for the second one
+                if (cudaEventRecord(join, as) != cudaSuccess ||
+                    cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
+                    st_rev = KDA_ERR_CUDA;
+            }
+            cudaEventDestroy(fork);
+            cudaEventDestroy(join);
+            if (st_rev != KDA_OK) return st_rev;
+            if (st != KDA_OK) return st;
+        }
     }
-    if ((st = launch_status()) != KDA_OK) return st;
     // contractions over V
     {
         SimtWsPtrs p;
