@@ -1145,6 +1145,9 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 // read by the chunk-local backward kernel; dv is written directly.
 // ===========================================================================
 constexpr uint32_t G_S0 = 0, G_DS = 32768, G_ODD = 65536, G_DV = 98304, G_T = 131072;
+// v tiles, double-buffered: buffer b's two 64-column boxes at G_DV + vbuf(b)
+// and 16 KB later (the stride of the [dO; ddelta] k-blocks its product reads)
+__host__ __device__ constexpr uint32_t vbuf(int b) { return b ? 0u : 8192u; }
 constexpr uint32_t G_DT = 139264;  // delta^T [128 v][64 c], 16 KB
 constexpr uint32_t G_BAR = G_DT + 16384, G_DBV = G_BAR + 64;
 constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
@@ -1176,11 +1179,12 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + G_BAR);   // all tiles but v
     uint64_t* bar_mma = bar_tma + 1;
-    uint64_t* bar_v = bar_tma + 2;                                     // v tile
+    uint64_t* bar_v = bar_tma + 2;                                     // v tile, buffer 0
     uint64_t* bar_sd = bar_tma + 3;    // S0 and dS tiles
     uint64_t* bar_s = bar_tma + 4;     // the products that read S0 and dS are done
     uint64_t* bar_dg = bar_tma + 5;    // every thread is done reading S0 and dS
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_tma + 6);
+    uint64_t* bar_v1 = bar_tma + 7;                                    // v tile, buffer 1
     float* dbv_part = reinterpret_cast<float*>(smem + G_DBV);  // [4 lane quadrants][64]
     float* beta_s = dbv_part + 4 * 64;                          // [64]
     float* dg_part = beta_s + 64;                               // [2 halves][128]
@@ -1212,12 +1216,16 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         tma_load_2d(smem + G_T, &tm_t, bar_tma, 0, ch * kC);
         ++main_issued;
     };
+    // the i-th v load of the CTA (chunk blockIdx.x + i grid) goes to buffer
+    // i & 1 and completes phase (i >> 1) & 1 of that buffer's barrier
     auto issue_v = [&](int ch) {
         const int nn = ch % NT, bb = ch / NT, hvv = bb % a.HV;
         const int tr = tok_row((VL ? a.ctab : nullptr), bb / a.HV, a.T, nn);
-        mbar_arrive_expect_tx(bar_v, 16384);
-        tma_load_3d(smem + G_DV + 8192, &tm_v, bar_v, 0, hvv, tr);
-        tma_load_3d(smem + G_DV + 24576, &tm_v, bar_v, 64, hvv, tr);
+        const int b = v_issued & 1;
+        uint64_t* bar = b ? bar_v1 : bar_v;
+        mbar_arrive_expect_tx(bar, 16384);
+        tma_load_3d(smem + G_DV + vbuf(b), &tm_v, bar, 0, hvv, tr);
+        tma_load_3d(smem + G_DV + vbuf(b) + 16384, &tm_v, bar, 64, hvv, tr);
         ++v_issued;
     };
     auto load_beta = [&](int ch) {
@@ -1232,6 +1240,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_v, 1);
+        mbar_init(bar_v1, 1);
         mbar_init(bar_sd, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_dg, kGradThreads);
@@ -1249,6 +1258,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         issue_sd(blockIdx.x);
         issue_main(blockIdx.x);
         issue_v(blockIdx.x);
+        if ((int)(blockIdx.x + gridDim.x) < total) issue_v(blockIdx.x + gridDim.x);
     }
     float beta_next = (tid < kC && (int)blockIdx.x < total) ? load_beta(blockIdx.x) : 0.f;
     bool ok = true;
@@ -1268,14 +1278,16 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             if (next < total) beta_next = load_beta(next);    // in flight meanwhile
         }
         if (tid == 0) {   // the thread that issues the loads also issues the products
-            if (wait_bar(bar_sd, ph, 26) && wait_bar(bar_tma, ph, 21) && wait_bar(bar_v, ph, 25)) {
+            if (wait_bar(bar_sd, ph, 26) && wait_bar(bar_tma, ph, 21) &&
+                wait_bar((it & 1) ? bar_v1 : bar_v, (it >> 1) & 1, 25)) {
                 ++sd_waited;
                 ++main_waited;
                 ++v_waited;
                 tc_fence_after();
                 const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
                 const uint32_t s0 = smem_u32(smem + G_S0), ds = smem_u32(smem + G_DS);
-                const uint32_t odd = smem_u32(smem + G_ODD), dvt = smem_u32(smem + G_DV);
+                const uint32_t odd = smem_u32(smem + G_ODD),
+                               dvt = smem_u32(smem + G_DV + vbuf(it & 1));
                 const uint32_t tt = smem_u32(smem + G_T), dt = smem_u32(smem + G_DT);
                 // the products that read S0 and dS first, so that their tiles
                 // can be refilled while the others run
@@ -1299,8 +1311,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                     const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
                     const uint64_t bdt = sdesc_mn_sw128(dt + kk * 2048, 16384);
                     mma_bf16(tmem + 256, sdesc_sw128(odd + ko), bdt, id64 | kBMajorMN, kk > 0);
-                    mma_bf16(tmem + 320, sdesc_sw128(odd + ko), sdesc_sw128(dvt + 8192 + ko),
-                             id64, kk > 0);
+                    mma_bf16(tmem + 320, sdesc_sw128(odd + ko), sdesc_sw128(dvt + ko), id64,
+                             kk > 0);
                 }
                 // D5 = ddelta^T T: ddelta tile read MN-major (v blocks 16 KB apart), T MN-major
 #pragma unroll
@@ -1398,7 +1410,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
                 const float bt = beta_s[m];
                 if ((DW == kD || l < DW) && m < len)
                     a.dv[(((size_t)trow + m) * a.HV + hv) * DW + l] = __float2bfloat16_rn(bt * r[j]);
-                const uint32_t voff = G_DV + 8192 + (l >> 6) * 16384 + sw128_offset(m, l & 63);
+                const uint32_t voff =
+                    G_DV + vbuf(it & 1) + (l >> 6) * 16384 + sw128_offset(m, l & 63);
                 r[j] *= __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
             }
             // dbv[m] = sum over v of r: lane j ends with row cb*32 + j of this quadrant
@@ -1408,8 +1421,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // the v tile has been read: the next chunk's v loads now
-        if (tid == 0 && ok && next < total) issue_v(next);
+        // this v buffer has been read: the v tile two chunks ahead loads into it
+        if (tid == 0 && ok && next + (int)gridDim.x < total) issue_v(next + gridDim.x);
         if (tid < kD)
             a.dgam[(size_t)crow * kD + tid] = dg_part[tid] + dg_part[kD + tid];
         if (tid < 64) {
@@ -1425,7 +1438,8 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     if (tid == 0) {
         for (; sd_waited < sd_issued; ++sd_waited) wait_bar_drain(bar_sd, sd_waited & 1);
         for (; main_waited < main_issued; ++main_waited) wait_bar_drain(bar_tma, main_waited & 1);
-        for (; v_waited < v_issued; ++v_waited) wait_bar_drain(bar_v, v_waited & 1);
+        for (; v_waited < v_issued; ++v_waited)
+            wait_bar_drain((v_waited & 1) ? bar_v1 : bar_v, (v_waited >> 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
