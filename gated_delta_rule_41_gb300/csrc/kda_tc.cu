@@ -1150,8 +1150,11 @@ constexpr uint32_t G_S0 = 0, G_DS = 32768, G_ODD = 65536, G_DV = 98304, G_T = 13
 __host__ __device__ constexpr uint32_t vbuf(int b) { return b ? 0u : 8192u; }
 constexpr uint32_t G_DT = 139264;  // delta^T [128 v][64 c], 16 KB
 constexpr uint32_t G_BAR = G_DT + 16384, G_DBV = G_BAR + 64;
+// dQh and dKb staged, fp32 [64 rows][128 k] row-major, for one TMA store each
+constexpr uint32_t G_STQ = (G_DBV + 2304 + 1023) & ~1023u, G_STK = G_STQ + 32768;
 constexpr uint32_t GRAD_TX = 4 * 32768 + 8192;
-constexpr uint32_t GRAD_SMEM = G_DBV + 2304 + 1024;
+constexpr uint32_t GRAD_SMEM = G_STK + 32768 + 1024;
+static_assert(GRAD_SMEM <= 232448, "grad_v exceeds the per-CTA shared memory limit");
 // 8 warps (two per SM sub-partition, so up to 255 registers a thread): thread
 // 0 issues the TMA copies and the MMAs, then all eight run the epilogue
 constexpr int kGradThreads = 256;
@@ -1173,7 +1176,8 @@ __global__ void __launch_bounds__(kGradThreads, 1)
 grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_dh,
               const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dd,
               const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_v,
-              const __grid_constant__ CUtensorMap tm_t, GradArgs a) {
+              const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_dqh,
+              const __grid_constant__ CUtensorMap tm_dkb, GradArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1360,22 +1364,26 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         // done: the next chunk's copies of them start while this chunk's
         // results leave
         if (tid == 0 && ok && next < total) issue_main(next);
+        // the previous chunk's dQh / dKb stores have read their staging tiles
+        if (tid == 0) bulk_wait_read_all();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
         if (ok) {
             const size_t rb = (size_t)row * kD;
             const int cb = half;  // columns 32*cb .. 32*cb+31 of D1-D3 and D5
+            float* stq = reinterpret_cast<float*>(smem + G_STQ);
+            float* stk = reinterpret_cast<float*>(smem + G_STK);
             tmem_ld32(tmem + lane_off + 0 + cb * 32, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a.dQh[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
+            for (int j = 0; j < 32; ++j) stq[(cb * 32 + j) * kD + l] = r[j];
             tmem_ld32(tmem + lane_off + 64 + cb * 32, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 a.dW[rb + (size_t)(cb * 32 + j) * kD + l] = __float2bfloat16_rn(-r[j]);
             tmem_ld32(tmem + lane_off + 128 + cb * 32, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a.dKb[rb + (size_t)(cb * 32 + j) * kD + l] = r[j];
+            for (int j = 0; j < 32; ++j) stk[(cb * 32 + j) * kD + l] = r[j];
             // D4: lanes 0-63 need columns 0-63 (dAqk), lanes 64-127 columns 64-127 (dTv)
             {
                 const size_t cc = (size_t)crow * kC * kC;
@@ -1421,6 +1429,11 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (tid == 0 && ok) {   // dQh and dKb from their staging tiles
+            tma_store_2d(&tm_dqh, smem + G_STQ, 0, row);
+            tma_store_2d(&tm_dkb, smem + G_STK, 0, row);
+            bulk_commit_group();
+        }
         // this v buffer has been read: the v tile two chunks ahead loads into it
         if (tid == 0 && ok && next + (int)gridDim.x < total) issue_v(next + gridDim.x);
         if (tid < kD)
@@ -1436,6 +1449,7 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
     // loads issued for chunks the loop did not reach (after an error) land
     // before shared memory is released
     if (tid == 0) {
+        bulk_wait_all();   // the output stores complete
         for (; sd_waited < sd_issued; ++sd_waited) wait_bar_drain(bar_sd, sd_waited & 1);
         for (; main_waited < main_issued; ++main_waited) wait_bar_drain(bar_tma, main_waited & 1);
         for (; v_waited < v_issued; ++v_waited)
@@ -3194,6 +3208,22 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
            CUDA_SUCCESS;
 }
 
+// 2-D fp32 map over a row-major [rows][cols] array, no swizzle (a plain
+// row-major shared-memory box of box_cols x box_rows).
+bool make_map_f32(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                  uint32_t box_cols, uint32_t box_rows) {
+    EncodeFn enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // 3-D bf16 map over a token tensor [B*T][heads][128] (a per-head tile of 64
 // tokens is a box {64 columns, 1 head, 64 tokens}), 128B swizzle.
 // The row width D (64 or 128) is the tensor's own: with D = 64 the box at
@@ -3686,6 +3716,10 @@ kda_status tc_bwd_run(const kda_dims& d, const TcWs& w, const TcVl* vl, const vo
             kern<<<std::min(BH * NT, sm_count()), kGradThreads, PX_SMEM, s>>>(
                 mh, mdh, mdhl, mdo, md, mdl, mkb, mkbl, ma, mv, mt, a);
         } else {
+            CUtensorMap mdqh, mdkb;   // the fp32 outputs [BH*T][128], one box per chunk
+            if (!make_map_f32(&mdqh, p.dQh, rows, kD, kD, kC) ||
+                !make_map_f32(&mdkb, p.dKb, rows, kD, kD, kC))
+                return KDA_ERR_CUDA;
             auto kern = d.V == kD ? (vl ? grad_v_kernel<kD, true> : grad_v_kernel<kD, false>)
                                   : (vl ? grad_v_kernel<64, true> : grad_v_kernel<64, false>);
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -3694,7 +3728,7 @@ kda_status tc_bwd_run(const kda_dims& d, const TcWs& w, const TcVl* vl, const vo
             TimedLaunch tl("tc_grad_v", s);
             // persistent: one CTA per SM walks the chunks
             kern<<<std::min(BH * NT, sm_count()), kGradThreads, GRAD_SMEM, s>>>(
-                mh, mdh, mdo, mdd, md, mv, mt, a);
+                mh, mdh, mdo, mdd, md, mv, mt, mdqh, mdkb, a);
         }
     }
     if ((st = launch_status()) != KDA_OK) return st;
