@@ -61,12 +61,12 @@ def _src_hash(name):
 # grows with the chunk count, so a launch at another size reports the bytes
 # scaled by its head-tokens.
 NCU_TRAFFIC = {
-    "tc_local_bwd": (436659456, 1 * 8192 * 16, "kda_tc.cu", "b800628420d1"),
-    "tc_intra": (275913728, 1 * 8192 * 16, "kda_tc.cu", "b800628420d1"),
-    "tc_grad_v": (486593024, 1 * 8192 * 16, "kda_tc.cu", "b800628420d1"),
-    "tc_chain_fwd_save": (247587840, 1 * 8192 * 16, "kda_tc.cu", "b800628420d1"),
-    "tc_chain_bwd": (220003328, 1 * 8192 * 16, "kda_tc.cu", "b800628420d1"),
-    "tc_chain_fwd": (726201344, 4 * 8192 * 16, "kda_tc.cu", "b800628420d1"),
+    "tc_local_bwd": (435024640, 1 * 8192 * 16, "kda_tc.cu", "a7e87dc824f8"),
+    "tc_intra": (276392448, 1 * 8192 * 16, "kda_tc.cu", "a7e87dc824f8"),
+    "tc_grad_v": (485464064, 1 * 8192 * 16, "kda_tc.cu", "a7e87dc824f8"),
+    "tc_chain_fwd_save": (248650496, 1 * 8192 * 16, "kda_tc.cu", "a7e87dc824f8"),
+    "tc_chain_bwd": (221356288, 1 * 8192 * 16, "kda_tc.cu", "a7e87dc824f8"),
+    "tc_chain_fwd": (726172928, 4 * 8192 * 16, "kda_tc.cu", "a7e87dc824f8"),
 }
 # decode_kernel: dram read + write per launch at the decode workload (B=256,
 # HV=16, K=V=128), its source file and that file's hash when captured
