@@ -215,6 +215,54 @@ def test_tcgen05_chunk_counts_and_groups(B, T, H, HV, saved, D):
     compare_all(res, oracle_chunk(inp, True), w, with_h0=True)
 
 
+@pytest.mark.parametrize("vl", [False, True])
+def test_recompute_backward_on_a_side_stream(vl):
+    """The recomputing tensor-core backward runs its reverse state pass on a
+    second stream beside the forward state pass and joins the caller's stream
+    before the contractions over V.  Called on a non-default stream, with the
+    results copied on that stream right after the call (no host
+    synchronisation in between), every output equals the default-stream run
+    bit for bit (the kernels use no atomics) and is within the bar of the
+    oracle.  Also for packed sequences."""
+    w = I.Workload("side_stream", 2, 1024, 2, 2, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
+                   h0_std=0.1, seed=77)
+    inp = I.make_chunk_inputs(w)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    if vl:
+        lens = [700, 1348]   # one packed batch of the same 2048 tokens
+        cu = torch.tensor([0, lens[0], sum(lens)], dtype=torch.int32, device="cuda")
+        pk = {n: t[n].reshape(1, -1, *t[n].shape[2:]) for n in ("q", "k", "v", "g", "beta", "do")}
+
+    def step():
+        if vl:
+            o, ht = kda.chunk_kda_fwd_varlen(pk["q"], pk["k"], pk["v"], pk["g"], pk["beta"], cu,
+                                             output_final_state=True, impl="tcgen05")
+            grads = kda.chunk_kda_bwd_varlen(pk["q"], pk["k"], pk["v"], pk["g"], pk["beta"],
+                                             pk["do"], cu, impl="tcgen05")
+        else:
+            o, ht = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"],
+                                      initial_state=t["h0"], output_final_state=True,
+                                      impl="tcgen05")
+            grads = kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                      initial_state=t["h0"], impl="tcgen05")
+        out = dict(o=o, ht=ht, **grads)
+        return {n: x.clone() for n, x in out.items() if x is not None}
+
+    ref = step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        got = step()
+    torch.cuda.synchronize()
+    kda.check()
+    assert set(got) == set(ref)
+    for n in ref:
+        assert torch.equal(got[n], ref[n]), n
+    if not vl:
+        compare_all(got, oracle_chunk(inp, True), w, with_h0=True)
+
+
 @pytest.mark.parametrize("B,T,H,HV,D,saved,h0", [
     (2, 256, 2, 4, 128, False, True), (2, 256, 2, 4, 128, True, True),
     (1, 512, 2, 2, 128, False, True), (2, 1024, 1, 1, 128, False, True),
