@@ -28,9 +28,15 @@
  * Dtypes   q, k, v, g, beta, o and all gradients of those are `dtype`
  *          (KDA_F32 or KDA_BF16).  States are always float32.
  * Memory   Every pointer is a DEVICE pointer.  The caller owns every buffer,
- *          including the workspace.  The library never allocates, frees or
- *          synchronises inside these calls; all work is enqueued on `stream`
- *          (a cudaStream_t; NULL = legacy default stream).
+ *          including the workspace.  The library never allocates device
+ *          memory, frees or synchronises inside these calls; all work is
+ *          ordered on `stream` (a cudaStream_t; NULL = legacy default
+ *          stream).  One exception to "enqueued on `stream`": a stateless
+ *          tensor-core backward without dht runs its reverse state pass on a
+ *          second stream that the library creates once per device.  That
+ *          stream waits for `stream` first, and `stream` waits for it (CUDA
+ *          events made for the call) before the call's later kernels, so
+ *          callers see only `stream`'s order.
  * Alignment  Every pointer must be aligned to its element size.  In addition:
  *          the decode state must be 16-byte aligned; with the tensor-core
  *          implementation q, k, v, g, o, dout, dq, dk, dv, dg, h0, ht, dht
@@ -118,7 +124,10 @@ kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const void* k, con
                          size_t workspace_bytes, void* stream);
 
 /* Backward of kda_chunk_fwd (K3 row L4 role: dq, dk, dv, dg, dbeta).
- * Stateless: it recomputes the forward from the inputs.
+ * Stateless: it recomputes the forward from the inputs.  On the tensor cores
+ * without dht the recomputed forward state pass and the reverse state pass
+ * run side by side (the reverse pass needs only dout and the intra-chunk
+ * quantities), the latter on the library's second stream (see Memory).
  *   dout   upstream gradient of o [B,T,HV,V] (dtype).
  *   dht    upstream gradient of the final state [B,HV,K,V] f32, or NULL.
  *   dq, dk [B,T,H,K]; dv [B,T,HV,V]; dg [B,T,HV,K]; dbeta [B,T,HV] (dtype).
