@@ -1132,8 +1132,9 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 }
 
 // ===========================================================================
-// Backward contractions over V, one CTA per (chunk, head), with S0 (state at
-// the chunk start) and dS (gradient at its end) from the two chains:
+// Backward contractions over V, per (chunk, head): persistent CTAs, one per
+// SM, walk the chunks.  S0 (state at the chunk start) and dS (gradient at its
+// end) come from the two chains:
 //     D1 = S0 dO^T       = dQh^T      (M=128 k, N=64)
 //     D2 = S0 ddelta^T   = -dW^T
 //     D3 = dS delta^T    = dKb^T
@@ -1141,8 +1142,9 @@ chain_bwd_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constan
 //                                      bottom-right = ddelta v^T (-> dTv)
 //     D5 = ddelta^T T    = d(beta v)^T (M=128 v, N=64): dv = beta * D5^T,
 //                                       dbeta += sum_v D5^T o v
-// plus dgam = rowsum(dS o S0).  Results go to the fp32 workspace arrays
-// read by the chunk-local backward kernel; dv is written directly.
+// plus dgam = rowsum(dS o S0).  Results go to the workspace arrays read by
+// the chunk-local backward kernel (dQh and dKb through staging tiles and one
+// TMA store each); dv is written directly.
 // ===========================================================================
 constexpr uint32_t G_S0 = 0, G_DS = 32768, G_ODD = 65536, G_DV = 98304, G_T = 131072;
 // v tiles, double-buffered: buffer b's two 64-column boxes at G_DV + vbuf(b)

@@ -60,6 +60,22 @@ def test_measured_traffic_scales_with_head_tokens(bench):
     assert bench.ncu_traffic("no_such_kernel", w) is None
 
 
+def test_source_hash_ignores_comments_only(bench, tmp_path, monkeypatch):
+    """A capture stays valid across edits of comments and whitespace, and is
+    dropped when the code itself changes."""
+    d = tmp_path / "gated_delta_rule_41_gb300" / "csrc"
+    d.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f = d / "k.cu"
+    f.write_text("__global__ void k(int* p) { p[0] = 1; }  // one\n/* block\n comment */\n")
+    h = bench._src_hash("k.cu")
+    f.write_text("// another comment\n__global__ void k(int* p)\n{\n    p[0] = 1;\n}\n")
+    assert bench._src_hash("k.cu") == h
+    f.write_text("__global__ void k(int* p) { p[0] = 2; }\n")
+    assert bench._src_hash("k.cu") != h
+    assert bench._src_hash("missing.cu") == ""
+
+
 def test_measured_traffic_is_dropped_for_a_changed_source(bench, monkeypatch):
     monkeypatch.setattr(bench, "_src_hash", lambda src: "0" * 12)
     assert all(bench.ncu_traffic(n, I.TRAIN_BF16) is None for n in bench.NCU_TRAFFIC)
