@@ -60,9 +60,9 @@ def _src_hash(name):
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
 # of that kernel alone (-k, one launch), keyed by kernel name: (bytes per
-# launch, head-tokens B*T*HV of the captured launch, the source file, that
-# file's hash when captured).  A kernel whose source has changed since reports
-# traffic null.  The step's kernels were captured at B=1, T=8192, HV=16 (2048
+# launch, head-tokens B*T*HV of the captured launch, the source file, the
+# hash of that file's code when captured).  A kernel whose source code has
+# changed since (comments aside) reports traffic null.  The step's kernels were captured at B=1, T=8192, HV=16 (2048
 # chunks, inputs and workspace above L2), the plain forward's state pass at
 # B=4 (at B=1 the plain forward cuts its state pass into segments); traffic
 # grows with the chunk count, so a launch at another size reports the bytes
@@ -76,7 +76,7 @@ NCU_TRAFFIC = {
     "tc_chain_fwd": (726172928, 4 * 8192 * 16, "kda_tc.cu", "46a54cc88e01"),
 }
 # decode_kernel: dram read + write per launch at the decode workload (B=256,
-# HV=16, K=V=128), its source file and that file's hash when captured
+# HV=16, K=V=128), its source file and the hash of its code when captured
 NCU_DECODE_TRAFFIC = (272657152 + 205334272, "kda_decode.cu", "a2c70e05645a")
 
 
