@@ -1379,10 +1379,20 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             tmem_ld32(tmem + lane_off + 0 + cb * 32, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j) stq[(cb * 32 + j) * kD + l] = r[j];
+            // dW and dv: lanes l and l ^ 1 trade one value per column pair, so
+            // that each lane writes two adjacent entries of one column (the
+            // even lane column j, the odd lane column j + 1): 4-byte stores,
+            // two rows per warp instruction
+            const bool odd = (lane & 1) != 0;
+            const int l2 = l & ~1;
             tmem_ld32(tmem + lane_off + 64 + cb * 32, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                a.dW[rb + (size_t)(cb * 32 + j) * kD + l] = __float2bfloat16_rn(-r[j]);
+            for (int j = 0; j < 32; j += 2) {
+                const float recv = __shfl_xor_sync(0xffffffffu, odd ? r[j] : r[j + 1], 1);
+                const float lo = odd ? recv : r[j], hi = odd ? r[j + 1] : recv;
+                *reinterpret_cast<uint32_t*>(a.dW + rb + (size_t)(cb * 32 + j + (odd ? 1 : 0)) * kD +
+                                             l2) = pack_bf16(-lo, -hi);
+            }
             tmem_ld32(tmem + lane_off + 128 + cb * 32, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j) stk[(cb * 32 + j) * kD + l] = r[j];
@@ -1415,11 +1425,18 @@ grad_v_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ 
             // D5: lane = v, columns m = 32*cb .. 32*cb+31
             tmem_ld32(tmem + lane_off + 192 + cb * 32, r);
 #pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float recv = __shfl_xor_sync(0xffffffffu, odd ? r[j] : r[j + 1], 1);
+                const float lo = odd ? recv : r[j], hi = odd ? r[j + 1] : recv;
+                const int m = cb * 32 + j + (odd ? 1 : 0);
+                const float bt = beta_s[m];
+                if ((DW == kD || l2 < DW) && m < len)
+                    *reinterpret_cast<uint32_t*>(a.dv + (((size_t)trow + m) * a.HV + hv) * DW + l2) =
+                        pack_bf16(bt * lo, bt * hi);
+            }
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int m = cb * 32 + j;
-                const float bt = beta_s[m];
-                if ((DW == kD || l < DW) && m < len)
-                    a.dv[(((size_t)trow + m) * a.HV + hv) * DW + l] = __float2bfloat16_rn(bt * r[j]);
                 const uint32_t voff =
                     G_DV + vbuf(it & 1) + (l >> 6) * 16384 + sw128_offset(m, l & 63);
                 r[j] *= __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + voff));
