@@ -502,6 +502,24 @@ def measure_decode(kda, dev, hbm):
 # GPU arm
 # --------------------------------------------------------------------------
 
+
+def slowest_rank_ms(ms, world, device=None):
+    """The job's step time: every rank timed the same steps between barriers,
+    and the job runs as fast as its slowest rank (max over ranks)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms):
+    """Whole-job throughput: the tokens all ranks processed (each runs its own
+    replica of the workload) over the job's step time."""
+    return world * tokens_per_rank / (ms / 1e3)
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,12 +636,8 @@ def main():
     kda.timing_enable(False)
     clocks = stop_clock_sampler(sampler, spath, local) if rank == 0 else None
     kda.check()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * w.tokens / (ms / 1e3)
+    ms = slowest_rank_ms(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    value = job_tokens_per_s(w.tokens, world, ms)
 
     # ---- end to end: pinned host buffers, copies inside the timed region ----
     # Each step copies its inputs host -> device and its outputs device -> host.
@@ -713,12 +727,8 @@ def main():
     stream.wait_event(ev_out[(args.steps - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * w.tokens / (e2e_ms / 1e3)
+    e2e_ms = slowest_rank_ms(e0.elapsed_time(e1) / args.steps, world, dev)
+    e2e_value = job_tokens_per_s(w.tokens, world, e2e_ms)
     copy_ms = min(copy_ms, copy_floor())
 
     if rank != 0:

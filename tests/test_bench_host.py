@@ -101,3 +101,48 @@ def test_forward_method_bytes(bench):
     # GVA: q and k are read once per key head
     g = dataclasses.replace(w, H=w.HV // 2)
     assert bench.fwd_method_bytes(g, False) == (1282 - 256) * w.B * w.T * w.HV
+
+
+def test_two_ranks_take_the_slowest_rank_and_count_every_rank():
+    """bench.py under torchrun (here: two gloo ranks on the CPU): the job's
+    step time is the slowest rank's, and the value counts the tokens of
+    every rank's replica."""
+    import multiprocessing as mp
+    import socket
+
+    import dist_worker
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    ms_by_rank, tokens = [2.0, 3.0], 131072
+    procs = [ctx.Process(target=dist_worker.timing_rank,
+                         args=(r, 2, port, ms_by_rank, tokens, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    try:
+        got = sorted(out.get(timeout=120) for _ in procs)
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+    assert [p.exitcode for p in procs] == [0, 0]
+    assert [r for r, _, _ in got] == [0, 1]
+    for _, ms, value in got:
+        assert ms == 3.0
+        assert value == pytest.approx(2 * tokens / 3e-3)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the oracle arm runs and prints on rank 0 alone; any
+    other rank exits 0 without work or output."""
+    import subprocess
+    import sys
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
