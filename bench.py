@@ -68,12 +68,12 @@ def _src_hash(name):
 # grows with the chunk count, so a launch at another size reports the bytes
 # scaled by its head-tokens.
 NCU_TRAFFIC = {
-    "tc_local_bwd": (435024640, 1 * 8192 * 16, "kda_tc.cu", "46a54cc88e01"),
-    "tc_intra": (276392448, 1 * 8192 * 16, "kda_tc.cu", "46a54cc88e01"),
-    "tc_grad_v": (485464064, 1 * 8192 * 16, "kda_tc.cu", "46a54cc88e01"),
-    "tc_chain_fwd_save": (248650496, 1 * 8192 * 16, "kda_tc.cu", "46a54cc88e01"),
-    "tc_chain_bwd": (221356288, 1 * 8192 * 16, "kda_tc.cu", "46a54cc88e01"),
-    "tc_chain_fwd": (726172928, 4 * 8192 * 16, "kda_tc.cu", "46a54cc88e01"),
+    "tc_local_bwd": (434774784, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
+    "tc_intra": (276096000, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
+    "tc_grad_v": (485031936, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
+    "tc_chain_fwd_save": (247920384, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
+    "tc_chain_bwd": (219795456, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
+    "tc_chain_fwd": (726114304, 4 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
 }
 # decode_kernel: dram read + write per launch at the decode workload (B=256,
 # HV=16, K=V=128), its source file and the hash of its code when captured
