@@ -13,6 +13,11 @@ bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p)
 
 unsigned elem_bytes(const kda_dims& d) { return d.dtype == KDA_BF16 ? 2u : 4u; }
 
+// Largest B * HV * T the chunk kernels index (per-head token rows times two
+// fit a signed 32-bit tile coordinate); a token tensor of that many rows at
+// K = 128 in bf16 would already take 256 GB.
+constexpr long long kMaxHeadTokens = 1LL << 30;
+
 kda_status check_common(const kda_dims* d, bool need_chunk) {
     if (!d) return KDA_ERR_INVALID_ARG;
     if (d->dtype != KDA_F32 && d->dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
@@ -27,6 +32,9 @@ kda_status check_common(const kda_dims* d, bool need_chunk) {
         const int c = d->chunk_size;
         if (c != 16 && c != 32 && c != 64 && c != 128) return KDA_ERR_UNSUPPORTED;
         if (d->T % c != 0) return KDA_ERR_SHAPE;
+        // tile coordinates and row indices are 32-bit: the chunk-start state
+        // rows of all heads (2 B HV T at chunk 64) stay below 2^31
+        if ((long long)d->B * d->HV * d->T >= kMaxHeadTokens) return KDA_ERR_UNSUPPORTED;
     }
     return KDA_OK;
 }
@@ -94,6 +102,9 @@ kda_status check_varlen_dims(const kda_dims* d, int nseq) {
     if (st != KDA_OK) return st;
     if (d->T < 0 || d->B != 1 || nseq < 1) return KDA_ERR_SHAPE;
     if ((long long)nseq * d->HV > 65535) return KDA_ERR_UNSUPPORTED;
+    // the kernels see the padded chunk slots: ceil(T / C) + nseq of them
+    const long long slots = ((long long)d->T + d->chunk_size - 1) / d->chunk_size + nseq;
+    if (slots * d->chunk_size * d->HV >= kMaxHeadTokens) return KDA_ERR_UNSUPPORTED;
     return KDA_OK;
 }
 

@@ -44,6 +44,11 @@
  * Gates    g is a log-decay: values <= 0 are the supported domain (values
  *          below -5 are clamped to -5; positive values may overflow the
  *          in-chunk decay factors and are not supported).
+ * Sizes    B * HV * T must stay below 2^30 (for packed sequences: the padded
+ *          slot count (ceil(T / chunk_size) + num_seqs) * chunk_size * HV),
+ *          and B * HV at most 65535; larger problems are refused with
+ *          KDA_ERR_UNSUPPORTED.  Tile coordinates and row indices are 32-bit.
+ *          A token tensor at the first limit would hold 256 GB at K = 128.
  * Errors   Arguments are validated before any launch; on a validation error
  *          nothing is enqueued and no output is written.  KDA_ERR_CUDA means
  *          a launch failed (cudaGetLastError); KDA_ERR_TIMEOUT means a device

@@ -91,5 +91,20 @@ def test_validation_errors(lib):
     assert st == 2
 
 
+def test_size_limits(lib):
+    """B * HV * T at 2^30 (32-bit tile coordinates) is refused before any
+    pointer is looked at; just below it only the workspace is missing."""
+    big = dims(B=8192, HV=4, T=32768)                   # 2^13 * 4 * 2^15 = 2^30
+    assert fwd(lib, big, ptrs=[None] * 6) == 3
+    assert lib.kda_chunk_workspace_bytes(ctypes.byref(big), 0) == 0
+    assert fwd(lib, dims(B=8192, HV=4, T=16384)) == 5
+    assert lib.kda_chunk_workspace_bytes(ctypes.byref(dims(B=8192, HV=4, T=16384)), 0) > 0
+    # packed sequences count their padded chunk slots
+    vl = dims(B=1, HV=4, T=(1 << 28) - 64 * 1000)
+    assert lib.kda_chunk_workspace_bytes_varlen(ctypes.byref(vl), 1000, 0) == 0
+    assert lib.kda_chunk_workspace_bytes_varlen(ctypes.byref(vl), 999, 0) > 0
+    assert lib.kda_chunk_workspace_bytes(ctypes.byref(dims(B=65536, HV=1, H=1, T=64)), 0) == 0
+
+
 def test_build_flags_target_sm103a():
     assert "arch=compute_103a,code=sm_103a" in kbuild.ARCH
