@@ -185,6 +185,30 @@ def test_varlen_tcgen05(H, HV, K, lengths, with_h0, with_dht, qkn):
     compare(res, oracle_packed(inp, cu, True, qk_l2norm=qkn), torch.bfloat16, with_h0=with_h0)
 
 
+@pytest.mark.parametrize("saved", [False, True])
+def test_varlen_tcgen05_many_sequences(saved):
+    """64 packed sequences (seeded lengths 0 to 200, a few empty and
+    one-token ones) at HV = 4: the state passes run 256 CTAs, more than one
+    wave, and the persistent kernels walk about 300 chunk slots.  Stateless
+    (the recomputed forward state pass beside the reverse pass) and saved."""
+    rng = np.random.default_rng(4242)
+    lengths = [int(x) for x in rng.integers(0, 201, size=64)]
+    lengths[3], lengths[10], lengths[20], lengths[41] = 0, 1, 0, 1
+    inp, cu = packed_inputs(lengths, 2, 4, 128, 128, torch.bfloat16, seed=83, with_dht=False)
+    t = {n: (x.cuda() if x is not None else None) for n, x in inp.items()}
+    cu_d = torch.from_numpy(cu).cuda()
+    out = kda.chunk_kda_fwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], cu_d,
+                                   initial_state=t["h0"], output_final_state=True,
+                                   impl="tcgen05", save_for_backward=saved)
+    res = dict(o=out[0], ht=out[1])
+    res.update(kda.chunk_kda_bwd_varlen(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"], cu_d,
+                                        initial_state=t["h0"], impl="tcgen05",
+                                        saved=out[2] if saved else None))
+    torch.cuda.synchronize()
+    kda.check()
+    compare(res, oracle_packed(inp, cu, True), torch.bfloat16)
+
+
 def test_varlen_tcgen05_one_sequence_equals_the_fixed_length_scan():
     w = I.Workload("one_seq_tc", 1, 256, 2, 2, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
                    h0_std=0.2, dht=True, seed=74)
