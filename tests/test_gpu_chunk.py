@@ -537,6 +537,34 @@ def test_96_heads_sampled(impl, K, dtype):
             assert_close(f"{n}[{hv}]", sl(res[n]), ref[n], w.dtype)
 
 
+@pytest.mark.parametrize("saved", [False, True])
+def test_tcgen05_more_heads_than_sms(saved):
+    """B = 2 x 96 heads: 192 (batch, head) pairs, so the one-CTA-per-SM state
+    passes run in two waves; heads from both waves (bh 0, 95, 150, 191) on
+    the oracle, with an initial state, stateless and saved."""
+    w = I.Workload("heads192", 2, 192, 96, 96, 128, 128, 64, torch.bfloat16, g_sigma=2.0,
+                   h0_std=0.1, seed=57)
+    inp = I.make_chunk_inputs(w, device="cuda")
+    t = inp
+    out = kda.chunk_kda_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["h0"],
+                            output_final_state=True, impl="tcgen05", save_for_backward=saved)
+    res = dict(o=out[0], ht=out[1])
+    res.update(kda.chunk_kda_bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["do"],
+                                 initial_state=t["h0"], impl="tcgen05",
+                                 saved=out[2] if saved else None))
+    torch.cuda.synchronize()
+    kda.check()
+    heads = [(0, 0), (0, 95), (1, 54), (1, 95)]
+    refs = oracle_chunk(inp, True, heads=heads)
+    for (b, hv), ref in zip(heads, refs):
+        sl = lambda x: x[b:b + 1, :, hv:hv + 1]
+        assert_close(f"o[{b},{hv}]", sl(res["o"]), ref["o"], w.dtype)
+        assert_close(f"ht[{b},{hv}]", res["ht"][b:b + 1, hv:hv + 1], ref["ht"], w.dtype)
+        assert_close(f"dh0[{b},{hv}]", res["dh0"][b:b + 1, hv:hv + 1], ref["dh0"], w.dtype)
+        for n in GRADS:
+            assert_close(f"{n}[{b},{hv}]", sl(res[n]), ref[n], w.dtype)
+
+
 def test_impls_agree_train_shape_subset():
     """The SIMT and tensor-core paths agree with each other on a slice of the
     training workload (T = 1024)."""
