@@ -23,9 +23,11 @@ constexpr float kNormEps = 1e-12f;
 
 // Fast path: K, V multiples of 4 with (V/4) threads per row.  Each thread
 // owns 4 consecutive columns of ROWS rows.  QKN: q and k are L2-normalised
-// over K first (x / max(|x|, 1e-12)).
+// over K first (x / max(|x|, 1e-12)).  Three CTAs per SM (at most 85
+// registers a thread): each CTA alternates a load, a reduction and a store
+// phase, and a third CTA keeps more of the state in flight.
 template <typename Tin, int K, int V, bool QKN>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 3)
 decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* __restrict__ k,
               const Tin* __restrict__ v, const Tin* __restrict__ g,
               const Tin* __restrict__ beta, float* __restrict__ state, Tin* __restrict__ o) {
