@@ -21,37 +21,43 @@ constexpr int kDecodeThreads = 256;
 
 constexpr float kNormEps = 1e-12f;
 
-// Fast path: K, V multiples of 4 with (V/4) threads per row.  Each thread
-// owns 4 consecutive columns of ROWS rows.  QKN: q and k are L2-normalised
-// over K first (x / max(|x|, 1e-12)).  Three CTAs per SM (at most 85
-// registers a thread): each CTA alternates a load, a reduction and a store
-// phase, and a third CTA keeps more of the state in flight.
-template <typename Tin, int K, int V, bool QKN>
-__global__ void __launch_bounds__(kDecodeThreads, 3)
+// Fast path: K, V multiples of 4.  A CTA takes VT of a head's V value
+// columns (the columns are independent: each one's reductions over K and
+// its update touch only that column), with (VT/4) threads per state row;
+// each thread owns 4 consecutive columns of ROWS rows.  QKN: q and k are
+// L2-normalised over K first (x / max(|x|, 1e-12)).  Each CTA alternates a
+// load, a reduction and a store phase; with VT = 64 a thread holds 32
+// floats of state and five CTAs share an SM (at most 51 registers a
+// thread), so more of the state stays in flight.
+template <typename Tin, int K, int V, bool QKN, int VT = V>
+__global__ void __launch_bounds__(kDecodeThreads, VT < V ? 5 : 3)
 decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* __restrict__ k,
               const Tin* __restrict__ v, const Tin* __restrict__ g,
               const Tin* __restrict__ beta, float* __restrict__ state, Tin* __restrict__ o) {
-    constexpr int TPR = V / 4;                  // threads per state row
+    constexpr int NVT = V / VT;                 // CTAs per head
+    constexpr int TPR = VT / 4;                 // threads per state row
+    constexpr int RS = V / 4;                   // float4 per state row
     constexpr int RP = kDecodeThreads / TPR;    // rows per pass
     constexpr int ROWS = K / RP;                // rows per thread
+    static_assert(V % VT == 0 && VT % 4 == 0, "bad value tile");
     static_assert(kDecodeThreads % TPR == 0 && K % RP == 0, "bad decode tiling");
 
     __shared__ float s_qa[K], s_ka[K], s_a[K], s_k[K];
-    __shared__ float s_red[2][RP][V];
-    __shared__ float s_e[V];
+    __shared__ float s_red[2][RP][VT];
+    __shared__ float s_e[VT];
     __shared__ float s_kq[K / 32];
     __shared__ float s_nk[K / 32], s_nq[K / 32];
 
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x / NVT, v0 = (blockIdx.x % NVT) * VT;
     const int b = bh / HV, hv = bh % HV, h = hv / (HV / H);
     const int tid = threadIdx.x;
     const int col4 = tid % TPR;
     const int row0 = tid / TPR;
 
-    float4* S4 = reinterpret_cast<float4*>(state + (size_t)bh * K * V);
+    float4* S4 = reinterpret_cast<float4*>(state + (size_t)bh * K * V + v0);
     float4 s[ROWS];
 #pragma unroll
-    for (int i = 0; i < ROWS; ++i) s[i] = __ldcs(S4 + (size_t)(row0 + i * RP) * TPR + col4);
+    for (int i = 0; i < ROWS; ++i) s[i] = __ldcs(S4 + (size_t)(row0 + i * RP) * RS + col4);
 
     const size_t qk_off = ((size_t)b * H + h) * K;
     float kk = 0.f, qq = 0.f;
@@ -112,7 +118,7 @@ decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* 
     __syncthreads();
 
     const float bt = to_f(beta[bh]);
-    if (tid < V) {
+    if (tid < VT) {
         float sk = 0.f, sq = 0.f;
 #pragma unroll 8
         for (int p = 0; p < RP; ++p) {
@@ -122,9 +128,9 @@ decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* 
         float kq = 0.f;
 #pragma unroll
         for (int w = 0; w < K / 32; ++w) kq += s_kq[w];
-        const float e = to_f(v[(size_t)bh * V + tid]) - sk;
+        const float e = to_f(v[(size_t)bh * V + v0 + tid]) - sk;
         s_e[tid] = e;
-        o[(size_t)bh * V + tid] = from_f<Tin>(sq + bt * kq * e);
+        o[(size_t)bh * V + v0 + tid] = from_f<Tin>(sq + bt * kq * e);
     }
     __syncthreads();
 
@@ -138,7 +144,7 @@ decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* 
         r.y = a * s[i].y + bk * e4.y;
         r.z = a * s[i].z + bk * e4.z;
         r.w = a * s[i].w + bk * e4.w;
-        __stcs(S4 + (size_t)c * TPR + col4, r);
+        __stcs(S4 + (size_t)c * RS + col4, r);
     }
 }
 
@@ -205,11 +211,12 @@ kda_status decode_dispatch(const kda_dims& d, const void* q, const void* k, cons
     TimedLaunch tl("decode_step", s);
     const bool qkn = d.qk_l2norm != 0;
     if (d.K == 128 && d.V == 128) {
+        // two CTAs per head, 64 value columns each
         if (qkn)
-            decode_kernel<Tin, 128, 128, true><<<nb, kDecodeThreads, 0, s>>>(
+            decode_kernel<Tin, 128, 128, true, 64><<<2 * nb, kDecodeThreads, 0, s>>>(
                 d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
         else
-            decode_kernel<Tin, 128, 128, false><<<nb, kDecodeThreads, 0, s>>>(
+            decode_kernel<Tin, 128, 128, false, 64><<<2 * nb, kDecodeThreads, 0, s>>>(
                 d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
     } else if (d.K == 64 && d.V == 64) {
         if (qkn)
