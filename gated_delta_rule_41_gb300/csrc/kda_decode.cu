@@ -26,11 +26,11 @@ constexpr float kNormEps = 1e-12f;
 // its update touch only that column), with (VT/4) threads per state row;
 // each thread owns 4 consecutive columns of ROWS rows.  QKN: q and k are
 // L2-normalised over K first (x / max(|x|, 1e-12)).  Each CTA alternates a
-// load, a reduction and a store phase; with VT = 64 a thread holds 32
-// floats of state and five CTAs share an SM (at most 51 registers a
-// thread), so more of the state stays in flight.
+// load, a reduction and a store phase; with VT = 32 a thread holds 16 (K =
+// 128) or 8 (K = 64) floats of state and six CTAs share an SM, so more of
+// the state stays in flight than with a whole head per CTA.
 template <typename Tin, int K, int V, bool QKN, int VT = V>
-__global__ void __launch_bounds__(kDecodeThreads, VT < V ? 5 : 3)
+__global__ void __launch_bounds__(kDecodeThreads, VT == V ? 3 : (VT >= 64 ? 5 : 6))
 decode_kernel(int H, int HV, float scale, const Tin* __restrict__ q, const Tin* __restrict__ k,
               const Tin* __restrict__ v, const Tin* __restrict__ g,
               const Tin* __restrict__ beta, float* __restrict__ state, Tin* __restrict__ o) {
@@ -211,19 +211,20 @@ kda_status decode_dispatch(const kda_dims& d, const void* q, const void* k, cons
     TimedLaunch tl("decode_step", s);
     const bool qkn = d.qk_l2norm != 0;
     if (d.K == 128 && d.V == 128) {
-        // two CTAs per head, 64 value columns each
+        // four CTAs per head, 32 value columns each
         if (qkn)
-            decode_kernel<Tin, 128, 128, true, 64><<<2 * nb, kDecodeThreads, 0, s>>>(
+            decode_kernel<Tin, 128, 128, true, 32><<<4 * nb, kDecodeThreads, 0, s>>>(
                 d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
         else
-            decode_kernel<Tin, 128, 128, false, 64><<<2 * nb, kDecodeThreads, 0, s>>>(
+            decode_kernel<Tin, 128, 128, false, 32><<<4 * nb, kDecodeThreads, 0, s>>>(
                 d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
     } else if (d.K == 64 && d.V == 64) {
+        // two CTAs per head, 32 value columns each
         if (qkn)
-            decode_kernel<Tin, 64, 64, true><<<nb, kDecodeThreads, 0, s>>>(
+            decode_kernel<Tin, 64, 64, true, 32><<<2 * nb, kDecodeThreads, 0, s>>>(
                 d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
         else
-            decode_kernel<Tin, 64, 64, false><<<nb, kDecodeThreads, 0, s>>>(
+            decode_kernel<Tin, 64, 64, false, 32><<<2 * nb, kDecodeThreads, 0, s>>>(
                 d.H, d.HV, d.scale, qq, kk, vv, gg, bb, state, oo);
     } else {
         decode_kernel_generic<Tin><<<nb, 128, 0, s>>>(d.H, d.HV, d.K, d.V, d.scale, qkn ? 1 : 0,
