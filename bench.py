@@ -77,7 +77,7 @@ NCU_TRAFFIC = {
 }
 # decode_kernel: dram read + write per launch at the decode workload (B=256,
 # HV=16, K=V=128), its source file and the hash of its code when captured
-NCU_DECODE_TRAFFIC = (272657152 + 205334272, "kda_decode.cu", "a2c70e05645a")
+NCU_DECODE_TRAFFIC = (272652544 + 205543936, "kda_decode.cu", "fc013c481cc7")
 
 
 def ncu_traffic(name, w):
