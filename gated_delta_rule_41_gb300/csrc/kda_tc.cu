@@ -785,49 +785,57 @@ chain_fwd_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 
 // Combine step of the segmented scan: per head, the true start state of
 // segment p + 1 is M_p S_p + Z_p for p = 1 .. nseg - 2 (S_1 comes from the
-// full run of segment 0).  One CTA of 256 threads per head; thread (i, h)
-// owns row i and columns 64 h .. 64 h + 63 of the [D][D] result (D <= 128).
-// M is kept row-major with a row stride of D + 1 floats, so that the 16 rows
-// a warp reads at one k fall in distinct banks; S rows are read as float4.
+// full run of segment 0).  One CTA of 256 threads per head; thread (j, h)
+// owns column j and rows 64 h .. 64 h + 63 of the [D][D] result (D <= 128),
+// so that a warp's global loads of Z and stores of the result cover 128
+// contiguous bytes of a row.  M is held transposed in shared memory with a
+// row stride of D + 4 floats: a thread's 64 rows at one k are 16 broadcast
+// float4 loads, and S_p[k][j] one conflict-free load.
 __global__ void __launch_bounds__(256)
 chain_combine_kernel(int D, int nseg, float* __restrict__ sbuf, const float* __restrict__ zbuf,
                      const float* __restrict__ mbuf) {
     extern __shared__ float cs[];
-    const int MP = D + 1;
-    float* Ms = cs;                  // Ms[i * MP + k] = M[i][k]
-    float* Sk = cs + D * MP;         // S[k][j]; D (D + 1) is a multiple of 4: 16-byte aligned
+    const int MT = D + 4;
+    float* Mt = cs;                  // Mt[k * MT + i] = M[i][k]; MT * 4 bytes is 16-byte aligned
+    float* Sk = cs + D * MT;         // S[k][j]
     const int bh = blockIdx.x, tid = threadIdx.x;
     const size_t SZ = (size_t)D * D;
-    const int i = tid >> 1, j0 = (tid & 1) * 64;
+    const int j = tid & 127, i0 = (tid >> 7) * 64;
     for (int p = 1; p <= nseg - 2; ++p) {
         const float* M = mbuf + ((size_t)bh * nseg + p) * SZ;
         const float* Sp = sbuf + ((size_t)bh * nseg + p) * SZ;
         __syncthreads();   // the previous step's rows are written
-        for (int e = tid; e < D * D; e += 256) {
-            Ms[(e / D) * MP + e % D] = M[e];
-            Sk[e] = Sp[e];
+        // 16-byte loads (D is a multiple of 4; the buffers are 16-byte aligned)
+        for (int e4 = tid; e4 < D * D / 4; e4 += 256) {
+            const float4 m = reinterpret_cast<const float4*>(M)[e4];
+            const int i = (4 * e4) / D, k = (4 * e4) % D;
+            Mt[k * MT + i] = m.x;
+            Mt[(k + 1) * MT + i] = m.y;
+            Mt[(k + 2) * MT + i] = m.z;
+            Mt[(k + 3) * MT + i] = m.w;
+            reinterpret_cast<float4*>(Sk)[e4] = reinterpret_cast<const float4*>(Sp)[e4];
         }
         __syncthreads();
-        if (i < D && j0 < D) {
+        if (j < D && i0 < D) {
             float acc[64];
-            const float* Z = zbuf + ((size_t)bh * nseg + p) * SZ + (size_t)i * D + j0;
+            const float* Z = zbuf + ((size_t)bh * nseg + p) * SZ + (size_t)i0 * D + j;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = Z[j];
+            for (int ii = 0; ii < 64; ++ii) acc[ii] = Z[(size_t)ii * D];
             for (int k = 0; k < D; ++k) {
-                const float m = Ms[i * MP + k];
-                const float4* srow = reinterpret_cast<const float4*>(Sk + k * D + j0);
+                const float sv = Sk[k * D + j];
+                const float4* mrow = reinterpret_cast<const float4*>(Mt + k * MT + i0);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float4 sv = srow[j];
-                    acc[4 * j] = fmaf(m, sv.x, acc[4 * j]);
-                    acc[4 * j + 1] = fmaf(m, sv.y, acc[4 * j + 1]);
-                    acc[4 * j + 2] = fmaf(m, sv.z, acc[4 * j + 2]);
-                    acc[4 * j + 3] = fmaf(m, sv.w, acc[4 * j + 3]);
+                for (int q = 0; q < 16; ++q) {
+                    const float4 m = mrow[q];
+                    acc[4 * q] = fmaf(m.x, sv, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(m.y, sv, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(m.z, sv, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(m.w, sv, acc[4 * q + 3]);
                 }
             }
-            float* out = sbuf + ((size_t)bh * nseg + p + 1) * SZ + (size_t)i * D + j0;
+            float* out = sbuf + ((size_t)bh * nseg + p + 1) * SZ + (size_t)i0 * D + j;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) out[j] = acc[j];
+            for (int ii = 0; ii < 64; ++ii) out[(size_t)ii * D] = acc[ii];
         }
     }
 }
@@ -3534,7 +3542,7 @@ kda_status run_chain_fwd(const kda_dims& d, const TcWs& w, const float* gam, con
     args.mbuf = w.mbuf;
     args.ident = w.ident;
     const int D = d.K;
-    const size_t cbytes = ((size_t)D * (D + 1) + (size_t)D * D) * sizeof(float);
+    const size_t cbytes = ((size_t)D * (D + 4) + (size_t)D * D) * sizeof(float);
     if (cudaFuncSetAttribute(chain_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)cbytes) != cudaSuccess)
         return KDA_ERR_CUDA;
