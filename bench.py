@@ -68,12 +68,12 @@ def _src_hash(name):
 # grows with the chunk count, so a launch at another size reports the bytes
 # scaled by its head-tokens.
 NCU_TRAFFIC = {
-    "tc_local_bwd": (434774784, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
-    "tc_intra": (276096000, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
-    "tc_grad_v": (485031936, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
-    "tc_chain_fwd_save": (247920384, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
-    "tc_chain_bwd": (219795456, 1 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
-    "tc_chain_fwd": (726114304, 4 * 8192 * 16, "kda_tc.cu", "a09417bb5b2c"),
+    "tc_local_bwd": (434779904, 1 * 8192 * 16, "kda_tc.cu", "7d87e21548ab"),
+    "tc_intra": (276193536, 1 * 8192 * 16, "kda_tc.cu", "7d87e21548ab"),
+    "tc_grad_v": (485224192, 1 * 8192 * 16, "kda_tc.cu", "7d87e21548ab"),
+    "tc_chain_fwd_save": (247514112, 1 * 8192 * 16, "kda_tc.cu", "7d87e21548ab"),
+    "tc_chain_bwd": (220022528, 1 * 8192 * 16, "kda_tc.cu", "7d87e21548ab"),
+    "tc_chain_fwd": (726314752, 4 * 8192 * 16, "kda_tc.cu", "7d87e21548ab"),
 }
 # decode_kernel: dram read + write per launch at the decode workload (B=256,
 # HV=16, K=V=128), its source file and the hash of its code when captured
